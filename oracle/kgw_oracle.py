@@ -1,0 +1,229 @@
+"""CPU oracle for the K-grouped MoE weight-gradient GEMM.
+
+TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this module. The product path (the CUDA library
+and its Python binding) never imports, links or calls it, and this module
+shares no code with it: it reads stored operand bits and does its own decoding
+and arithmetic in float64 with numpy.
+
+What it computes is the plain definition of the operation ("Grouped GEMM +
+WGrad (Unified)", section "Operation"): for expert e, begin = 0 when e == 0,
+else offsets[e-1]; end = offsets[e]; and
+
+    Wgrad[e] = A[:, begin:end] @ B[begin:end, :]
+
+with A [hidden, tokens_sum] and B [tokens_sum, intermediate]. In MoE terms this
+is dW_e = dY_e^T X_e, a GEMM whose contraction axis is the per-expert token
+count ("05 · Grouped GEMM 与 Expert 计算", section 5.2). With accumulate the
+result is added to the existing output; without it the output is overwritten
+and an empty expert yields zeros (section "Operation").
+
+The FP8 variant multiplies every decoded e4m3 element by its per-128-token
+FP32 scale before the product: a row m of A and a column n of B each carry one
+scale per block of 128 consecutive tokens ("05 · Grouped GEMM 与 Expert 计算",
+section 3: per-block 1x128 scaling, scales stored MN-major).
+
+Every product here is exact in float64 only up to rounding of the float64
+sums; the tests pin it against exact rational brute force, so "the oracle"
+means "the definition, evaluated in float64".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TOKEN_ALIGN = 256
+SCALE_BLOCK = 128
+
+
+# ---------------------------------------------------------------------------------------------
+# Exact decoding of stored element bits
+# ---------------------------------------------------------------------------------------------
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """Decode raw bfloat16 bit patterns (uint16/int16) exactly to float64.
+
+    A bfloat16 value is the upper half of an IEEE binary32 word, so shifting the
+    16 bits up by 16 gives the binary32 word that holds the same value exactly.
+    (BF16 contract: operands are torch.bfloat16.)
+    """
+    u = np.asarray(bits).view(np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def f32_to_f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(bits) -> np.ndarray:
+    """Decode raw float8 e4m3 (the 'fn' variant: no infinities) bit patterns to float64.
+
+    Layout: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits. Exponent field 0 is
+    subnormal: m/8 * 2**-6. The pattern S.1111.111 is NaN; every other pattern with
+    exponent field 15 is a normal number (max 448).
+    """
+    b = np.asarray(bits).view(np.uint8).astype(np.int64)
+    sign = np.where((b >> 7) & 1, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.ldexp(1.0, (e - 7).astype(np.int64))
+    sub = (m / 8.0) * 2.0 ** -6
+    mag = np.where(e == 0, sub, normal)
+    mag = np.where((e == 15) & ((b & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+# ---------------------------------------------------------------------------------------------
+# Offsets (section "BF16 contract": non-decreasing cumulative sum, counts % 256 == 0,
+# final offset == tokens_sum)
+# ---------------------------------------------------------------------------------------------
+
+def expert_ranges(offsets):
+    """[(begin_e, end_e)] with begin_0 = 0 and begin_e = offsets[e-1] (section "Operation")."""
+    off = [int(v) for v in np.asarray(offsets).tolist()]
+    return [((0 if e == 0 else off[e - 1]), off[e]) for e in range(len(off))]
+
+
+def offsets_valid(offsets, tokens_sum: int) -> bool:
+    off = [int(v) for v in np.asarray(offsets).tolist()]
+    if len(off) == 0:
+        return False
+    prev = 0
+    for v in off:
+        n = v - prev
+        if n < 0 or n % TOKEN_ALIGN != 0:
+            return False
+        prev = v
+    return prev == tokens_sum
+
+
+# ---------------------------------------------------------------------------------------------
+# Logical operands from stored operands (section "BF16 contract", input_order)
+# ---------------------------------------------------------------------------------------------
+
+def logical_a(a_values: np.ndarray, hidden: int, offsets, input_order: str) -> np.ndarray:
+    """Logical A [hidden, tokens_sum] from its stored values.
+
+    tensor2d: the stored tensor is A itself ([hidden, tokens_sum], stride (tokens_sum, 1)).
+    ragged:   per-expert K-contiguous blocks concatenated in memory; only the unit-stride
+              (token) axis keeps its meaning, so expert e's block is [hidden, n_e] row-major
+              starting at element begin_e*hidden.
+    """
+    ranges = expert_ranges(offsets)
+    tokens_sum = ranges[-1][1] if ranges else 0
+    if input_order == "tensor2d":
+        return np.asarray(a_values).reshape(hidden, tokens_sum)
+    assert input_order == "ragged"
+    flat = np.asarray(a_values).reshape(-1)
+    out = np.zeros((hidden, tokens_sum), dtype=flat.dtype)
+    for (b, e) in ranges:
+        n = e - b
+        if n:
+            out[:, b:e] = flat[b * hidden:(b + n) * hidden].reshape(hidden, n)
+    return out
+
+
+def logical_b(b_values: np.ndarray, intermediate: int, offsets, input_order: str) -> np.ndarray:
+    """Logical B [tokens_sum, intermediate].
+
+    B's unit-stride axis is the intermediate axis, so expert e's K-contiguous block is
+    [n_e, intermediate] row-major starting at element begin_e*intermediate: identical to
+    the tensor2d storage in both input orders.
+    """
+    ranges = expert_ranges(offsets)
+    tokens_sum = ranges[-1][1] if ranges else 0
+    flat = np.asarray(b_values).reshape(-1)
+    out = np.zeros((tokens_sum, intermediate), dtype=flat.dtype)
+    for (b, e) in ranges:
+        if e > b:
+            out[b:e, :] = flat[b * intermediate:e * intermediate].reshape(e - b, intermediate)
+    return out
+
+
+def apply_block_scales_rows(x: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """A-side FP8 scaling: x [rows, tokens], scales [tokens/128, rows] -> x[m,k]*s[k//128, m]."""
+    rows, tokens = x.shape
+    s = np.asarray(scales, dtype=np.float64).reshape(tokens // SCALE_BLOCK, rows)
+    return x * np.repeat(s.T, SCALE_BLOCK, axis=1)
+
+
+def apply_block_scales_cols(x: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """B-side FP8 scaling: x [tokens, cols], scales [tokens/128, cols] -> x[k,n]*s[k//128, n]."""
+    tokens, cols = x.shape
+    s = np.asarray(scales, dtype=np.float64).reshape(tokens // SCALE_BLOCK, cols)
+    return x * np.repeat(s, SCALE_BLOCK, axis=0)
+
+
+# ---------------------------------------------------------------------------------------------
+# The operation
+# ---------------------------------------------------------------------------------------------
+
+def wgrad(A: np.ndarray, B: np.ndarray, offsets, c_init=None, accumulate: bool = False,
+          with_bound: bool = True):
+    """Per-expert Wgrad in float64 ("Grouped GEMM + WGrad (Unified)", section "Operation").
+
+    A: float64 [hidden, tokens_sum]; B: float64 [tokens_sum, intermediate].
+    Returns (out, S): out [E, hidden, intermediate] is R_e (overwrite; zeros for an empty
+    expert) or C_e + R_e (accumulate; C_e unchanged for an empty expert); S = |A_e| @ |B_e|
+    is the magnitude sum used by the error bound (None when with_bound is False).
+    """
+    ranges = expert_ranges(offsets)
+    E = len(ranges)
+    H, T = A.shape
+    T2, I = B.shape
+    assert T == T2 == (ranges[-1][1] if ranges else 0)
+    out = np.zeros((E, H, I), dtype=np.float64)
+    S = np.zeros((E, H, I), dtype=np.float64) if with_bound else None
+    for e, (b, end) in enumerate(ranges):
+        if accumulate:
+            out[e] = np.asarray(c_init[e], dtype=np.float64)
+        if end > b:
+            Ae, Be = A[:, b:end], B[b:end, :]
+            out[e] += Ae @ Be
+            if with_bound:
+                S[e] = np.abs(Ae) @ np.abs(Be)
+    return out, S
+
+
+def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, *,
+                       input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
+                       c_init=None, accumulate: bool = False, with_bound: bool = True):
+    """Decode stored operands (raw bits) and evaluate the operation in float64.
+
+    a_bits/b_bits: uint16 (bf16) or uint8 (e4m3) numpy arrays as stored.
+    sfa [tokens/128, hidden], sfb [tokens/128, intermediate]: float32 scales (FP8 only).
+    c_init: the pre-filled output values (any float dtype, decoded by the caller) or None.
+    """
+    dec = e4m3_to_f64 if fp8 else bf16_to_f64
+    A = logical_a(dec(a_bits), hidden, offsets, input_order)
+    B = logical_b(dec(b_bits), intermediate, offsets, input_order)
+    if fp8:
+        A = apply_block_scales_rows(A, sfa)
+        B = apply_block_scales_cols(B, sfb)
+    return wgrad(A, B, offsets, c_init=c_init, accumulate=accumulate, with_bound=with_bound)
+
+
+def wgrad_element(A: np.ndarray, B: np.ndarray, offsets, e: int, m: int, n: int):
+    """One output element R_e[m, n] and its bound S_e[m, n] (for sampled checks at full size)."""
+    b, end = expert_ranges(offsets)[e]
+    a = A[m, b:end]
+    bb = B[b:end, n]
+    return float(np.dot(a, bb)), float(np.dot(np.abs(a), np.abs(bb)))
+
+
+# ---------------------------------------------------------------------------------------------
+# Tolerance
+# ---------------------------------------------------------------------------------------------
+
+def tolerance(S: np.ndarray, ref: np.ndarray, out_dtype: str, c_init=None) -> np.ndarray:
+    """Per-element error bound for a GPU result against the float64 oracle.
+
+    FP32 output: 2e-5*S + 1e-6 (FP32 accumulation over the ragged token axis).
+    Accumulate into FP32 adds one FP32 rounding of the sum: 2**-23*(|C| + |ref|).
+    BF16 output adds one final BF16 rounding: 2**-8*|ref|.
+    """
+    tol = 2e-5 * S + 1e-6
+    if c_init is not None:
+        tol = tol + 2.0 ** -23 * (np.abs(np.asarray(c_init, dtype=np.float64)) + np.abs(ref))
+    if out_dtype == "bf16":
+        tol = tol + 2.0 ** -8 * np.abs(ref)
+    return tol

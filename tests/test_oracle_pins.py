@@ -1,0 +1,488 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test ties the oracle to something the pages or mathematics fix: exact rational
+brute force, the block-masked dense GEMM identity, closed forms, special cases that
+reduce to a plain library GEMM, the empty-expert and accumulate semantics of
+"Grouped GEMM + WGrad (Unified)" (section "Operation"), the offsets contract (section
+"BF16 contract"), and the exact decoding of the stored number formats.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.kgw_oracle as O
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def e4m3_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.uint8).numpy()
+
+
+def random_bf16(rng, shape, choices=None):
+    if choices is None:
+        x = rng.standard_normal(shape).astype(np.float32)
+    else:
+        x = rng.choice(np.asarray(choices, dtype=np.float32), size=shape)
+    return torch.from_numpy(x).to(torch.bfloat16)
+
+
+# ------------------------------------------------------------------------------------------
+# Number formats
+# ------------------------------------------------------------------------------------------
+
+def test_bf16_decode_known_values():
+    known = {0x3F80: 1.0, 0xC000: -2.0, 0x4049: 3.140625, 0x0000: 0.0, 0x3F00: 0.5,
+             0x0001: 2.0 ** -133, 0x0080: 2.0 ** -126, 0x7F7F: (2 - 2 ** -7) * 2.0 ** 127}
+    bits = np.array(list(known.keys()), dtype=np.uint16)
+    got = O.bf16_to_f64(bits)
+    assert got.tolist() == list(known.values())
+
+
+def test_bf16_decode_all_patterns_vs_torch():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = O.bf16_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_decode_known_values():
+    known = {0x38: 1.0, 0x7E: 448.0, 0xFE: -448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6,
+             0x07: 7 * 2.0 ** -9, 0x40: 2.0, 0x3C: 1.5, 0x00: 0.0}
+    got = O.e4m3_to_f64(np.array(list(known.keys()), dtype=np.uint8))
+    assert got.tolist() == list(known.values())
+    assert np.isnan(O.e4m3_to_f64(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def test_e4m3_decode_all_codes_vs_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = O.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# ------------------------------------------------------------------------------------------
+# Offsets contract
+# ------------------------------------------------------------------------------------------
+
+def _read_golden_offsets():
+    rows = []
+    with open(os.path.join(GOLDEN, "contract_offsets.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            ts, offs, valid, why = [p.strip() for p in line.split("|")]
+            rows.append((int(ts), [int(v) for v in offs.split()], bool(int(valid)), why))
+    return rows
+
+
+@pytest.mark.parametrize("case", _read_golden_offsets(), ids=lambda c: c[3])
+def test_offsets_contract_golden(case):
+    tokens_sum, offsets, valid, _ = case
+    assert O.offsets_valid(np.array(offsets, dtype=np.int32), tokens_sum) == valid
+
+
+def test_howto_example_counts_rejected():
+    kv = {}
+    with open(os.path.join(GOLDEN, "howto_example_counts.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            k, *v = line.split()
+            kv[k] = [int(x) for x in v]
+    counts = np.array(kv["tokens_per_expert"])
+    assert len(counts) == kv["num_experts"][0]
+    offsets = np.cumsum(counts)
+    assert O.offsets_valid(offsets, int(counts.sum())) == bool(kv["valid"][0])
+
+
+def test_expert_ranges_definition():
+    assert O.expert_ranges([256, 768, 768, 1536]) == [(0, 256), (256, 768), (768, 768), (768, 1536)]
+
+
+# ------------------------------------------------------------------------------------------
+# Exact brute force (Fraction) on tiny shapes
+# ------------------------------------------------------------------------------------------
+
+def _fraction_wgrad(A, B, offsets, C=None):
+    """Exact rational per-expert product, written as a plain triple loop."""
+    H, T = A.shape
+    I = B.shape[1]
+    fa = [[Fraction(float(A[m, k])) for k in range(T)] for m in range(H)]
+    fb = [[Fraction(float(B[k, n])) for n in range(I)] for k in range(T)]
+    out = []
+    prev = 0
+    for e, end in enumerate([int(v) for v in offsets]):
+        res = [[Fraction(0) if C is None else Fraction(float(C[e][m][n])) for n in range(I)]
+               for m in range(H)]
+        for m in range(H):
+            for n in range(I):
+                s = res[m][n]
+                for k in range(prev, end):
+                    s += fa[m][k] * fb[k][n]
+                res[m][n] = s
+        out.append(res)
+        prev = end
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_oracle_matches_exact_fraction_bruteforce(seed):
+    rng = np.random.default_rng(100 + seed)
+    E, H, I = 3, 5, 4
+    counts = np.array([256, 0, 512])[rng.permutation(3)]
+    offsets = np.cumsum(counts)
+    T = int(offsets[-1])
+    a = random_bf16(rng, (H, T))
+    b = random_bf16(rng, (T, I))
+    out, S = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    A = a.to(torch.float64).numpy()
+    B = b.to(torch.float64).numpy()
+    exact = _fraction_wgrad(A, B, offsets)
+    for e in range(E):
+        for m in range(H):
+            for n in range(I):
+                err = abs(Fraction(out[e, m, n]) - exact[e][m][n])
+                assert err <= Fraction(1e-12) * Fraction(S[e, m, n]) + Fraction(1e-300)
+
+
+def test_oracle_accumulate_matches_exact_fraction():
+    rng = np.random.default_rng(7)
+    E, H, I = 2, 3, 3
+    offsets = np.array([256, 256])
+    a = random_bf16(rng, (H, 256))
+    b = random_bf16(rng, (256, I))
+    C = rng.standard_normal((E, H, I))
+    out, S = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I, c_init=C, accumulate=True)
+    exact = _fraction_wgrad(a.to(torch.float64).numpy(), b.to(torch.float64).numpy(), offsets, C)
+    for e in range(E):
+        for m in range(H):
+            for n in range(I):
+                err = abs(Fraction(out[e, m, n]) - exact[e][m][n])
+                assert err <= Fraction(1e-12) * (Fraction(S[e, m, n]) + abs(Fraction(C[e, m, n]))) + Fraction(1e-300)
+    # empty expert (index 1) keeps C bit for bit
+    assert np.array_equal(out[1], C[1])
+
+
+# ------------------------------------------------------------------------------------------
+# Identities that tie the per-expert product to a plain dense GEMM (torch float64 matmul)
+# ------------------------------------------------------------------------------------------
+
+def _case(seed, counts, H=24, I=40):
+    rng = np.random.default_rng(seed)
+    offsets = np.cumsum(counts).astype(np.int32)
+    T = int(offsets[-1])
+    a = random_bf16(rng, (H, T))
+    b = random_bf16(rng, (T, I))
+    return a, b, offsets
+
+
+def test_block_masked_dense_identity():
+    counts = [512, 256, 0, 768, 256]
+    a, b, offsets = _case(11, counts)
+    H, I = a.shape[0], b.shape[1]
+    out, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    A = a.to(torch.float64)
+    B = b.to(torch.float64)
+    begin = 0
+    total = torch.zeros(H, I, dtype=torch.float64)
+    for e, n in enumerate(counts):
+        mask = torch.zeros(A.shape[1], dtype=torch.float64)
+        mask[begin:begin + n] = 1.0
+        masked = (A * mask) @ B                     # dense GEMM over the whole token axis
+        S = A.abs() @ B.abs()
+        assert torch.all((torch.from_numpy(out[e]) - masked).abs() <= 1e-12 * S + 1e-300)
+        total += torch.from_numpy(out[e])
+        begin += n
+    dense = A @ B
+    assert torch.allclose(total, dense, rtol=0, atol=1e-10 * float((A.abs() @ B.abs()).max()))
+
+
+def test_single_expert_is_plain_gemm():
+    a, b, offsets = _case(12, [1024])
+    out, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, a.shape[0], b.shape[1])
+    ref = (a.to(torch.float64) @ b.to(torch.float64)).numpy()
+    assert np.allclose(out[0], ref, rtol=0, atol=1e-12 * np.abs(ref).max() * 100)
+
+
+def test_empty_expert_overwrite_gives_zeros_and_accumulate_keeps_c():
+    a, b, offsets = _case(13, [256, 0, 512, 0])
+    H, I = a.shape[0], b.shape[1]
+    out, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    assert not out[1].any() and not out[3].any()
+    C = np.random.default_rng(1).standard_normal((4, H, I))
+    acc, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I, c_init=C, accumulate=True)
+    assert np.array_equal(acc[1], C[1]) and np.array_equal(acc[3], C[3])
+
+
+def test_accumulate_equals_c_plus_overwrite():
+    a, b, offsets = _case(14, [256, 768])
+    H, I = a.shape[0], b.shape[1]
+    # integer-valued C so that C + R is exact in float64 for this small K
+    C = np.random.default_rng(2).integers(-4, 5, size=(2, H, I)).astype(np.float64)
+    ow, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    acc, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I, c_init=C, accumulate=True)
+    assert np.allclose(acc, C + ow, rtol=0, atol=1e-9)
+
+
+def test_splitting_an_expert_sums_to_merged():
+    a, b, offsets_split = _case(15, [256, 512, 256])
+    H, I = a.shape[0], b.shape[1]
+    merged = np.array([256, 1024], dtype=np.int32)            # experts 1+2 merged
+    r_split, S = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets_split, H, I)
+    r_merged, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), merged, H, I)
+    assert np.array_equal(r_split[0], r_merged[0])
+    assert np.all(np.abs(r_split[1] + r_split[2] - r_merged[1]) <= 1e-12 * (S[1] + S[2]) + 1e-300)
+
+
+def test_token_permutation_within_expert_is_invariant():
+    counts = [512, 768]
+    a, b, offsets = _case(16, counts)
+    H, I = a.shape[0], b.shape[1]
+    perm = np.concatenate([np.random.default_rng(3).permutation(512),
+                           512 + np.random.default_rng(4).permutation(768)])
+    a2 = a[:, perm].contiguous()
+    b2 = b[perm, :].contiguous()
+    r1, S = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    r2, _ = O.wgrad_from_storage(bf16_bits(a2), bf16_bits(b2), offsets, H, I)
+    assert np.all(np.abs(r1 - r2) <= 1e-12 * S + 1e-300)
+
+
+def test_permuting_tokens_across_experts_changes_result():
+    """Sanity for the pins above: moving tokens between experts must change the result."""
+    a, b, offsets = _case(17, [256, 256])
+    H, I = a.shape[0], b.shape[1]
+    perm = np.concatenate([np.arange(256, 512), np.arange(0, 256)])
+    r1, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    r2, _ = O.wgrad_from_storage(bf16_bits(a[:, perm].contiguous()), bf16_bits(b[perm].contiguous()),
+                                 offsets, H, I)
+    assert not np.allclose(r1, r2)
+    assert np.allclose(r1[0], r2[1]) and np.allclose(r1[1], r2[0])
+
+
+def test_ragged_equals_tensor2d_on_same_logical_values():
+    counts = [256, 0, 768, 512]
+    a, b, offsets = _case(18, counts)
+    H, I = a.shape[0], b.shape[1]
+    ragged = W.pack_ragged_a(a, np.array(counts))
+    r2d, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I, input_order="tensor2d")
+    rrg, _ = O.wgrad_from_storage(bf16_bits(ragged), bf16_bits(b), offsets, H, I, input_order="ragged")
+    assert np.array_equal(r2d, rrg)
+    # and the ragged storage really is different memory order (leading dimension n_e)
+    assert not np.array_equal(bf16_bits(ragged), bf16_bits(a).reshape(-1))
+
+
+# ------------------------------------------------------------------------------------------
+# Closed forms
+# ------------------------------------------------------------------------------------------
+
+def test_ones_closed_form():
+    counts = [256, 0, 512, 1024]
+    offsets = np.cumsum(counts)
+    H, I = 8, 16
+    T = int(offsets[-1])
+    a = torch.ones(H, T, dtype=torch.bfloat16)
+    b = torch.ones(T, I, dtype=torch.bfloat16)
+    out, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    for e, n in enumerate(counts):
+        assert np.all(out[e] == float(n))
+
+
+def test_rank_one_closed_form_detects_transposition():
+    """A[m,k] = a_m and B[k,n] = b_n give R_e[m,n] = n_e * a_m * b_n exactly."""
+    counts = [256, 512, 0]
+    offsets = np.cumsum(counts)
+    H, I = 6, 10
+    T = int(offsets[-1])
+    am = np.array([1, -2, 0.5, 3, -0.25, 1.5], dtype=np.float32)
+    bn = np.linspace(-2, 2, I).astype(np.float32)
+    a = torch.from_numpy(np.repeat(am[:, None], T, axis=1)).to(torch.bfloat16)
+    b = torch.from_numpy(np.repeat(bn[None, :], T, axis=0)).to(torch.bfloat16)
+    out, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    av = a[:, 0].to(torch.float64).numpy()
+    bv = b[0, :].to(torch.float64).numpy()
+    for e, n in enumerate(counts):
+        assert np.array_equal(out[e], n * np.outer(av, bv))
+
+
+def test_one_hot_selects_rows_of_b():
+    """A[m,k] = [k == begin_e + m] picks row begin_e + m of B for expert e."""
+    counts = [256, 512]
+    offsets = np.cumsum(counts)
+    H, I = 4, 12
+    T = int(offsets[-1])
+    rng = np.random.default_rng(5)
+    b = random_bf16(rng, (T, I))
+    a = torch.zeros(H, T, dtype=torch.bfloat16)
+    begins = [0, 256]
+    for bgn in begins:
+        for m in range(H):
+            a[m, bgn + 3 * m + 1] = 1.0
+    out, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    B = b.to(torch.float64).numpy()
+    for e, bgn in enumerate(begins):
+        for m in range(H):
+            assert np.array_equal(out[e, m], B[bgn + 3 * m + 1])
+
+
+# ------------------------------------------------------------------------------------------
+# FP8 block-scaled variant
+# ------------------------------------------------------------------------------------------
+
+def _fp8_case(seed, counts, H=16, I=24):
+    offsets = np.cumsum(counts).astype(np.int32)
+    T = int(offsets[-1])
+    g = torch.Generator().manual_seed(seed)
+    a32 = torch.randn(H, T, generator=g)
+    b32 = torch.randn(T, I, generator=g)
+    qa, sfa = W.quantize_e4m3_blocks(a32, token_axis=1)
+    qb, sfb = W.quantize_e4m3_blocks(b32, token_axis=0)
+    return qa, sfa, qb, sfb, offsets
+
+
+def test_fp8_unit_scales_equal_decoded_product():
+    qa, sfa, qb, sfb, offsets = _fp8_case(21, [256, 0, 512])
+    H, I = qa.shape[0], qb.shape[1]
+    ones_a = torch.ones_like(sfa)
+    ones_b = torch.ones_like(sfb)
+    r, _ = O.wgrad_from_storage(e4m3_bits(qa), e4m3_bits(qb), offsets, H, I, fp8=True,
+                                sfa=ones_a.numpy(), sfb=ones_b.numpy())
+    A = qa.to(torch.float64)
+    B = qb.to(torch.float64)
+    begin = 0
+    for e, end in enumerate(offsets.tolist()):
+        ref = (A[:, begin:end] @ B[begin:end]).numpy()
+        assert np.allclose(r[e], ref, rtol=0, atol=1e-9)
+        begin = end
+
+
+def test_fp8_block_scale_power_of_two_is_exact():
+    """Scaling one 128-token block's A scales by 2**j scales that block's contribution by 2**j."""
+    qa, sfa, qb, sfb, offsets = _fp8_case(22, [256])
+    H, I = qa.shape[0], qb.shape[1]
+    # zero every token outside block 1 so that the result is that block's contribution alone
+    qa_only = qa.clone()
+    qa_only[:, :128] = 0
+    base, _ = O.wgrad_from_storage(e4m3_bits(qa_only), e4m3_bits(qb), offsets, H, I, fp8=True,
+                                   sfa=sfa.numpy(), sfb=sfb.numpy())
+    sfa2 = sfa.clone()
+    sfa2[1, :] *= 2.0 ** 5
+    scaled, _ = O.wgrad_from_storage(e4m3_bits(qa_only), e4m3_bits(qb), offsets, H, I, fp8=True,
+                                     sfa=sfa2.numpy(), sfb=sfb.numpy())
+    assert np.array_equal(scaled, base * 2.0 ** 5)
+
+
+def test_fp8_scale_indexing_row_vs_column():
+    """A's scale is per (block, row m); B's is per (block, column n): a closed form."""
+    H, I, T = 3, 5, 256
+    offsets = np.array([T], dtype=np.int32)
+    qa = torch.ones(H, T).to(torch.float8_e4m3fn)
+    qb = torch.ones(T, I).to(torch.float8_e4m3fn)
+    sfa = np.array([[1.0, 2.0, 4.0], [8.0, 16.0, 32.0]], dtype=np.float32)        # [2, H]
+    sfb = np.array([[1.0, 0.5, 0.25, 2.0, 4.0], [1.0, 1.0, 1.0, 1.0, 1.0]], dtype=np.float32)  # [2, I]
+    r, _ = O.wgrad_from_storage(e4m3_bits(qa), e4m3_bits(qb), offsets, H, I, fp8=True, sfa=sfa, sfb=sfb)
+    expect = 128 * (np.outer(sfa[0], sfb[0]) + np.outer(sfa[1], sfb[1]))
+    assert np.array_equal(r[0], expect)
+
+
+def test_fp8_quantiser_is_in_range_and_power_of_two():
+    g = torch.Generator().manual_seed(0)
+    x = torch.randn(8, 512, generator=g) * 3
+    q, s = W.quantize_e4m3_blocks(x, token_axis=1)
+    s = s.numpy()
+    mant, _ = np.frexp(s)
+    assert np.all(mant == 0.5)                                    # powers of two
+    dec = O.e4m3_to_f64(e4m3_bits(q))
+    assert np.all(np.abs(dec) <= 448)
+    recon = O.apply_block_scales_rows(dec, s)
+    # e4m3 keeps 3 mantissa bits: relative error <= 2**-4 (plus subnormal floor)
+    err = np.abs(recon - x.numpy().astype(np.float64))
+    assert np.all(err <= 2.0 ** -4 * np.abs(x.numpy()) + np.repeat(s.T, 128, axis=1) * 2.0 ** -10)
+
+
+# ------------------------------------------------------------------------------------------
+# Tolerance
+# ------------------------------------------------------------------------------------------
+
+def test_bf16_rounding_of_reference_is_within_tolerance():
+    a, b, offsets = _case(31, [256, 512])
+    H, I = a.shape[0], b.shape[1]
+    ref, S = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    rounded = torch.from_numpy(ref).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.all(np.abs(rounded - ref) <= O.tolerance(S, ref, "bf16"))
+    # and the bound is not vacuous: a 1% error is rejected somewhere
+    assert np.any(np.abs(ref * 1.01 - ref) > O.tolerance(S, ref, "f32"))
+
+
+# ------------------------------------------------------------------------------------------
+# Planted mistakes: each pin above must catch a plausible bug planted in the oracle
+# ------------------------------------------------------------------------------------------
+
+def _brute_force_agrees(fn_ranges=None, transpose_b=False):
+    rng = np.random.default_rng(99)
+    H, I = 4, 4
+    offsets = np.array([256, 512])
+    a = random_bf16(rng, (H, 512))
+    b = random_bf16(rng, (512, I))
+    bb = bf16_bits(b)
+    if transpose_b:
+        bb = bb.reshape(512, I)[:, ::-1].copy()
+    out, S = O.wgrad_from_storage(bf16_bits(a), bb, offsets, H, I)
+    exact = _fraction_wgrad(a.to(torch.float64).numpy(), b.to(torch.float64).numpy(), offsets)
+    for e in range(2):
+        for m in range(H):
+            for n in range(I):
+                if abs(Fraction(out[e, m, n]) - exact[e][m][n]) > Fraction(1e-12) * Fraction(S[e, m, n]) + Fraction(1e-300):
+                    return False
+    return True
+
+
+def test_planted_range_bug_is_caught(monkeypatch):
+    assert _brute_force_agrees()
+    good = O.expert_ranges
+
+    def off_by_one(offsets):
+        return [(b + (1 if e > 0 else 0), end) for e, (b, end) in enumerate(good(offsets))]
+
+    monkeypatch.setattr(O, "expert_ranges", off_by_one)
+    assert not _brute_force_agrees()
+
+
+def test_planted_operand_bug_is_caught():
+    assert not _brute_force_agrees(transpose_b=True)
+
+
+def test_planted_ragged_bug_is_caught(monkeypatch):
+    counts = [256, 512]
+    a, b, offsets = _case(41, counts, H=8, I=8)
+    ragged = W.pack_ragged_a(a, np.array(counts))
+    good = O.logical_a
+
+    def wrong_ld(a_values, hidden, offsets_, order):
+        if order != "ragged":
+            return good(a_values, hidden, offsets_, order)
+        # bug: treat the ragged buffer as if it had leading dimension tokens_sum
+        return np.asarray(a_values).reshape(hidden, -1)
+
+    r_ok, _ = O.wgrad_from_storage(bf16_bits(ragged), bf16_bits(b), offsets, 8, 8, input_order="ragged")
+    O.logical_a = wrong_ld
+    try:
+        r_bad, _ = O.wgrad_from_storage(bf16_bits(ragged), bf16_bits(b), offsets, 8, 8, input_order="ragged")
+    finally:
+        O.logical_a = good
+    r_2d, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, 8, 8)
+    assert np.array_equal(r_ok, r_2d)
+    assert not np.array_equal(r_bad, r_2d)

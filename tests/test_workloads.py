@@ -1,0 +1,65 @@
+"""The seeded input recipes: shapes, counts and determinism (no GPU)."""
+import numpy as np
+import torch
+
+import workloads as W
+
+
+def test_counts_are_multiples_of_256_and_offsets_cumulative():
+    for name, fn in W.NAMED.items():
+        w = fn()
+        c = np.asarray(w.counts)
+        assert c.shape == (w.num_experts,)
+        assert np.all(c % 256 == 0) and np.all(c >= 0), name
+        assert int(w.offsets[-1]) == w.tokens_sum
+        assert np.all(np.diff(np.concatenate([[0], w.offsets])) == c)
+
+
+def test_tiny_counts():
+    assert W.tiny().offsets.tolist() == [256, 768, 768, 1536]
+
+
+def test_zipf_split():
+    w = W.skewed()
+    c = np.asarray(w.counts)
+    assert w.tokens_sum == 262144
+    assert int((c == 0).sum()) == 20
+    assert int(c.max()) == 87296
+    assert int(((c > 0) & (c <= 512)).sum()) + int((c == 0).sum()) == 85
+
+
+def test_wide_has_two_zero_experts_and_accumulates():
+    w = W.wide()
+    assert int((np.asarray(w.counts) == 0).sum()) == 2
+    assert w.accumulate and w.out_dtype == "bf16"
+
+
+def test_round_to_256_is_nearest():
+    assert W.round_to_256(np.array([127.9, 128.0, 383.9, 384.0, 0.0])).tolist() == [0, 256, 256, 512, 0]
+
+
+def test_inputs_deterministic_and_shaped():
+    w = W.custom(3, 128, 256, [256, 0, 512], seed=9, accumulate=True, out_dtype="bf16")
+    x1 = W.make_inputs(w)
+    x2 = W.make_inputs(w)
+    assert torch.equal(x1.a.view(torch.int16), x2.a.view(torch.int16))
+    assert x1.a.shape == (128, 768) and x1.b.shape == (768, 256)
+    assert x1.c.shape == (3, 128, 256) and x1.c.dtype == torch.bfloat16
+    assert x1.offsets.dtype == torch.int32
+
+
+def test_ragged_packing_layout():
+    counts = [256, 0, 512]
+    a = torch.arange(4 * 768, dtype=torch.float32).reshape(4, 768).to(torch.bfloat16)
+    flat = W.pack_ragged_a(a, np.array(counts))
+    # expert 2 starts at element begin*hidden = 256*4 and has leading dimension 512
+    blk = flat[256 * 4: 256 * 4 + 4 * 512].reshape(4, 512)
+    assert torch.equal(blk, a[:, 256:768])
+
+
+def test_fp8_inputs_have_scales():
+    w = W.custom(2, 128, 256, [256, 256], seed=3, fp8=True, out_dtype="bf16")
+    x = W.make_inputs(w)
+    assert x.a.dtype == torch.float8_e4m3fn and x.b.dtype == torch.float8_e4m3fn
+    assert x.sfa.shape == (4, 128) and x.sfb.shape == (4, 256)
+    assert x.sfa.dtype == torch.float32

@@ -1,0 +1,273 @@
+"""Seeded synthetic inputs for the K-grouped MoE weight-gradient GEMM.
+
+This module only draws inputs. It holds none of the method's arithmetic
+(no products, no sums over tokens, no scaling of products) so that both the
+CUDA path and the CPU oracle can consume the same tensors without sharing
+any computation.
+
+Workloads follow the shapes of the pages' operation ("Grouped GEMM + WGrad
+(Unified)", sections "Operation" and "BF16 contract"): A is
+[hidden, tokens_sum] (K-major: stride (tokens_sum, 1)), B is
+[tokens_sum, intermediate] (N-major: stride (intermediate, 1)), offsets is
+the int32 cumulative token count per expert, and every per-expert count is a
+multiple of 256. The per-expert counts of the balanced workloads use the
+uniform(0.7, 1.3) spread of DeepGEMM's m-grouped generator described in
+"05 · Grouped GEMM 与 Expert 计算", section 2.1.
+
+Randomness: counts come from ``numpy.random.default_rng(seed)`` (draw order:
+counts, then the choice of zeroed experts, then the expert permutation);
+tensors come from a CPU ``torch.Generator`` seeded with ``seed`` (draw order:
+A, B, then the pre-filled output C).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+TOKEN_ALIGN = 256  # every per-expert count is a multiple of 256 (BF16 contract)
+FP8_BLOCK = 128    # one scale per 128 consecutive tokens, per row / column
+E4M3_MAX = 448.0
+
+
+def round_to_256(x: np.ndarray) -> np.ndarray:
+    """Nearest multiple of 256: 256 * floor(x / 256 + 0.5)."""
+    return (TOKEN_ALIGN * np.floor(np.asarray(x, dtype=np.float64) / TOKEN_ALIGN + 0.5)).astype(np.int64)
+
+
+def counts_uniform_spread(seed: int, num_experts: int, mean_tokens: int, lo: float, hi: float,
+                          zero_experts: int = 0) -> np.ndarray:
+    """Per-expert counts round_to_256(mean * U(lo, hi)); optionally zero some experts."""
+    rng = np.random.default_rng(seed)
+    counts = round_to_256(mean_tokens * rng.uniform(lo, hi, size=num_experts))
+    if zero_experts:
+        zeroed = rng.choice(num_experts, size=zero_experts, replace=False)
+        counts[zeroed] = 0
+    return counts
+
+
+def counts_zipf(seed: int, num_experts: int, total_tokens: int, s: float) -> np.ndarray:
+    """Zipf(s) split of ``total_tokens`` over a random expert permutation.
+
+    Rank r (1-based) gets weight r**-s; counts are 256*floor(total*p_r/256);
+    the rounding deficit goes to rank 1 so the counts sum to ``total_tokens``
+    exactly. A seeded permutation maps ranks to experts.
+    """
+    rng = np.random.default_rng(seed)
+    r = np.arange(1, num_experts + 1, dtype=np.float64)
+    p = r ** (-s)
+    p /= p.sum()
+    by_rank = TOKEN_ALIGN * np.floor(total_tokens * p / TOKEN_ALIGN).astype(np.int64)
+    by_rank[0] += total_tokens - int(by_rank.sum())
+    perm = rng.permutation(num_experts)
+    counts = np.zeros(num_experts, dtype=np.int64)
+    counts[perm] = by_rank
+    return counts
+
+
+def offsets_from_counts(counts) -> np.ndarray:
+    return np.cumsum(np.asarray(counts, dtype=np.int64)).astype(np.int32)
+
+
+@dataclasses.dataclass
+class Workload:
+    """Description of one synthetic problem (shapes, modes and the input recipe)."""
+    name: str
+    num_experts: int
+    hidden: int
+    intermediate: int
+    counts: np.ndarray
+    seed: int
+    a_std: float = 1.0
+    b_std: float = 1.0
+    out_dtype: str = "f32"          # "f32" | "bf16"
+    accumulate: bool = False
+    c_std: float = 1.0              # pre-filled output ~ N(0, c_std) when accumulating
+    input_order: str = "tensor2d"   # "tensor2d" | "ragged"
+    output_mode: str = "dense"      # "dense" | "discrete"
+    fp8: bool = False
+
+    @property
+    def tokens_sum(self) -> int:
+        return int(np.asarray(self.counts).sum())
+
+    @property
+    def offsets(self) -> np.ndarray:
+        return offsets_from_counts(self.counts)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.hidden * self.intermediate * self.tokens_sum
+
+
+def tiny() -> Workload:
+    return Workload("tiny BF16: E=4 hidden=128 intermediate=256 counts [256,512,0,768]",
+                    4, 128, 256, np.array([256, 512, 0, 768]), seed=0)
+
+
+def balanced() -> Workload:
+    return Workload("BF16 balanced: E=8 hidden=4096 intermediate=2048, FP32 dense overwrite",
+                    8, 4096, 2048, counts_uniform_spread(1, 8, 4096, 0.7, 1.3), seed=1,
+                    a_std=1.0, b_std=0.02)
+
+
+def wide() -> Workload:
+    return Workload("BF16 wide-hidden: E=32 hidden=7168 intermediate=2048, BF16 dense accumulate",
+                    32, 7168, 2048, counts_uniform_spread(2, 32, 2048, 0.5, 1.5, zero_experts=2), seed=2,
+                    out_dtype="bf16", accumulate=True)
+
+
+def fp8() -> Workload:
+    return Workload("FP8 block-scaled: E=16 hidden=4096 intermediate=1536, BF16 dense overwrite",
+                    16, 4096, 1536, counts_uniform_spread(3, 16, 4096, 0.7, 1.3), seed=3,
+                    out_dtype="bf16", fp8=True)
+
+
+def skewed() -> Workload:
+    return Workload("skewed ragged: E=128 hidden=2048 intermediate=768 Zipf(1.2) over 262144 tokens, "
+                    "discrete BF16 outputs",
+                    128, 2048, 768, counts_zipf(4, 128, 262144, 1.2), seed=4,
+                    out_dtype="bf16", input_order="ragged", output_mode="discrete")
+
+
+NAMED = {"tiny": tiny, "balanced": balanced, "wide": wide, "fp8": fp8, "skewed": skewed}
+
+
+def custom(num_experts: int, hidden: int, intermediate: int, counts, seed: int, **kw) -> Workload:
+    counts = np.asarray(counts, dtype=np.int64)
+    assert counts.shape == (num_experts,)
+    return Workload(f"custom E={num_experts} H={hidden} I={intermediate}", num_experts, hidden,
+                    intermediate, counts, seed, **kw)
+
+
+# --------------------------------------------------------------------------------------------
+# Tensors
+# --------------------------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class Inputs:
+    """Stored operands. All tensors live on ``device``.
+
+    a: tensor2d -> [hidden, tokens_sum] row-major; ragged -> flat buffer where expert e's
+       block [hidden, n_e] (row-major, leading dimension n_e) starts at element begin_e*hidden.
+    b: [tokens_sum, intermediate] row-major (identical in both input orders, because B's
+       unit-stride axis is the intermediate axis).
+    sfa/sfb (FP8 only): float32 [tokens_sum/128, hidden] / [tokens_sum/128, intermediate].
+    c: pre-filled output [E, hidden, intermediate] for accumulate mode, else None.
+    """
+    a: torch.Tensor
+    b: torch.Tensor
+    offsets: torch.Tensor
+    sfa: Optional[torch.Tensor] = None
+    sfb: Optional[torch.Tensor] = None
+    c: Optional[torch.Tensor] = None
+
+
+def _normal(gen: torch.Generator, shape, std: float) -> torch.Tensor:
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x
+
+
+def pow2_scale_exponent(amax: np.ndarray) -> np.ndarray:
+    """Exponent k with 2**k = 2**ceil(log2(amax/448)) (k = 0 where amax == 0), computed exactly."""
+    v = np.asarray(amax, dtype=np.float64) / E4M3_MAX
+    frac, ex = np.frexp(v)            # v = frac * 2**ex, frac in [0.5, 1)
+    k = np.where(frac == 0.5, ex - 1, ex)
+    return np.where(v == 0.0, 0, k).astype(np.int64)
+
+
+def quantize_e4m3_blocks(x: torch.Tensor, token_axis: int):
+    """Quantise ``x`` (float32 2-D) to e4m3 with one power-of-two FP32 scale per 128 tokens.
+
+    Returns (q [same shape, float8_e4m3fn], scales float32 [tokens/128, other]).
+    The scale is 2**ceil(log2(amax/448)), so |x/scale| <= 448 and nothing saturates.
+    """
+    assert x.dim() == 2 and x.dtype == torch.float32
+    xt = x if token_axis == 1 else x.t()          # [other, tokens]
+    other, tokens = xt.shape
+    assert tokens % FP8_BLOCK == 0
+    blocks = xt.reshape(other, tokens // FP8_BLOCK, FP8_BLOCK)
+    amax = blocks.abs().amax(dim=2)               # [other, nblk]
+    k = pow2_scale_exponent(amax.numpy())
+    scale = torch.from_numpy(np.ldexp(np.ones_like(k, dtype=np.float64), k).astype(np.float32))
+    q = (blocks / scale.unsqueeze(2)).to(torch.float8_e4m3fn).reshape(other, tokens)
+    if token_axis == 0:
+        q = q.t().contiguous()
+    return q.contiguous(), scale.t().contiguous()   # scales as [nblk, other]
+
+
+def pack_ragged_a(a2d: torch.Tensor, counts) -> torch.Tensor:
+    """Re-store a logical [hidden, tokens_sum] A as per-expert K-contiguous blocks.
+
+    Expert e's block is [hidden, n_e] row-major (leading dimension n_e) starting at
+    element begin_e*hidden of the flat buffer ("tensor_ragged" input order).
+    """
+    hidden = a2d.shape[0]
+    parts = []
+    begin = 0
+    for n in np.asarray(counts).tolist():
+        if n:
+            parts.append(a2d[:, begin:begin + n].contiguous().reshape(-1))
+        begin += n
+    if not parts:
+        return a2d.new_empty((0,))
+    flat = torch.cat(parts)
+    assert flat.numel() == hidden * begin
+    return flat
+
+
+def make_inputs(w: Workload, device="cpu") -> Inputs:
+    """Draw the inputs of workload ``w`` on the CPU (seeded) and move them to ``device``."""
+    gen = torch.Generator().manual_seed(int(w.seed))
+    H, I, T, E = w.hidden, w.intermediate, w.tokens_sum, w.num_experts
+    a32 = _normal(gen, (H, T), w.a_std)
+    b32 = _normal(gen, (T, I), w.b_std)
+    sfa = sfb = None
+    if w.fp8:
+        a_store, sfa = quantize_e4m3_blocks(a32, token_axis=1)
+        b_store, sfb = quantize_e4m3_blocks(b32, token_axis=0)
+    else:
+        a_store = a32.to(torch.bfloat16)
+        b_store = b32.to(torch.bfloat16)
+    del a32, b32
+    if w.input_order == "ragged":
+        a_store = pack_ragged_a(a_store, w.counts)
+    c = None
+    if w.accumulate:
+        c = _normal(gen, (E, H, I), w.c_std).to(torch.bfloat16 if w.out_dtype == "bf16" else torch.float32)
+    offsets = torch.from_numpy(w.offsets.astype(np.int32))
+    to = lambda t: None if t is None else t.to(device)
+    return Inputs(to(a_store), to(b_store), to(offsets), to(sfa), to(sfb), to(c))
+
+
+def make_inputs_device(w: Workload, device) -> Inputs:
+    """Same recipe as ``make_inputs`` but drawn with a device generator (fast, for timing only).
+
+    The values differ from ``make_inputs``; shapes, dtypes and distributions are identical.
+    """
+    gen = torch.Generator(device=device).manual_seed(int(w.seed))
+    H, I, T, E = w.hidden, w.intermediate, w.tokens_sum, w.num_experts
+
+    def normal(shape, std, dtype):
+        x = torch.randn(*shape, generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            x.mul_(std)
+        return x.to(dtype)
+
+    if w.fp8:
+        cpu = make_inputs(w, "cpu")   # quantisation recipe lives on the CPU side
+        return Inputs(cpu.a.to(device), cpu.b.to(device), cpu.offsets.to(device),
+                      cpu.sfa.to(device), cpu.sfb.to(device), None if cpu.c is None else cpu.c.to(device))
+    a = normal((H, T), w.a_std, torch.bfloat16)
+    b = normal((T, I), w.b_std, torch.bfloat16)
+    if w.input_order == "ragged":
+        a = pack_ragged_a(a, w.counts)
+    c = normal((E, H, I), w.c_std, torch.bfloat16 if w.out_dtype == "bf16" else torch.float32) \
+        if w.accumulate else None
+    offsets = torch.from_numpy(w.offsets.astype(np.int32)).to(device)
+    return Inputs(a, b, offsets, None, None, c)
