@@ -1,0 +1,386 @@
+"""Benchmark of the K-grouped MoE weight-gradient GEMM on GB300.
+
+One step = one call of the whole operation (plan kernel + persistent tcgen05 kernel) over one
+batch of synthetic input: Wgrad[e] = A[:, begin_e:end_e] @ B[begin_e:end_e, :] for every
+expert. Metric: TFLOP/s counting 2*hidden*intermediate*sum(n_e) FLOPs.
+
+Default workload: BF16 balanced, 8 experts, hidden 4096, intermediate 2048, per-expert tokens
+round_to_256(4096*U(0.7,1.3)) (seed 1), FP32 dense output, overwrite. Its working set
+(A + B + output, ~0.67 GB) is larger than L2, so no explicit flush is needed between steps.
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on the host cores
+instead (a bounded sample of the same workload per step).
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (experts are
+independent; there is no data-path exchange), timing is the max over ranks: weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+KERNEL_SOURCES = ["grouped_gemm_expert_gb300/csrc/kgw_kernels.cu", "grouped_gemm_expert_gb300/csrc/kgw_ptx.cuh",
+                  "grouped_gemm_expert_gb300/csrc/kgw_internal.h"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def traffic_record(workload: str):
+    """DRAM bytes per launch of the main kernel from a committed ncu summary, if still current."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def algorithmic_bytes(w) -> int:
+    esz = 1 if w.fp8 else 2
+    ts = w.tokens_sum
+    b = (w.hidden + w.intermediate) * ts * esz
+    if w.fp8:
+        b += (w.hidden + w.intermediate) * (ts // 128) * 4
+    osz = 2 if w.out_dtype == "bf16" else 4
+    counts = np.asarray(w.counts)
+    nonempty = int((counts > 0).sum())
+    if w.accumulate:
+        b += 2 * nonempty * w.hidden * w.intermediate * osz
+    else:
+        b += w.num_experts * w.hidden * w.intermediate * osz
+    return int(b)
+
+
+def run_ours(args, w, rank, local, world):
+    import grouped_gemm_expert_gb300 as kgw
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = W.make_inputs_device(w, dev)
+    E, H, I = w.num_experts, w.hidden, w.intermediate
+    odt = torch.bfloat16 if w.out_dtype == "bf16" else torch.float32
+    if w.output_mode == "dense":
+        out = torch.empty((E, H, I), dtype=odt, device=dev)
+        outs_list = None
+        ptrs = None
+    else:
+        outs_list = [torch.empty((H, I), dtype=odt, device=dev) for _ in range(E)]
+        out = None
+        ptrs = torch.tensor([t.data_ptr() for t in outs_list], dtype=torch.int64, device=dev)
+    if w.accumulate:
+        out.copy_(x.c)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kargs = kgw.make_args(E, H, I, w.tokens_sum, x.a, x.b, x.offsets, out=out, out_ptrs=ptrs,
+                          out_dtype=kgw.KGW_OUT_BF16 if w.out_dtype == "bf16" else kgw.KGW_OUT_F32,
+                          accumulate=w.accumulate,
+                          input_order=kgw.KGW_RAGGED if w.input_order == "ragged" else kgw.KGW_TENSOR2D,
+                          status_dev=status)
+    ws = kgw.workspace_for(kargs, w.fp8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if w.fp8:
+            kgw.kgw_wgrad_fp8_blockscaled(kargs, x.sfa, x.sfb, ws, stream=stream)
+        else:
+            kgw.kgw_wgrad_bf16(kargs, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {kgw.kgw_status_string(int(status.item()))}")
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    total_ms = t0.elapsed_time(t1)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # ---- end to end: pinned host inputs -> device, call, result -> host, every step ----
+    host_in = [t.cpu().pin_memory() for t in (x.a, x.b, x.offsets) + ((x.sfa, x.sfb) if w.fp8 else ())]
+    host_c = x.c.cpu().pin_memory() if w.accumulate else None
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    res_dev = out if out is not None else None
+    host_out = torch.empty(((E, H, I) if out is not None else (E, H, I)), dtype=odt).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in) + (
+        host_c.numel() * host_c.element_size() if host_c is not None else 0)
+    d2h = host_out.numel() * host_out.element_size()
+    kargs_e2e = kgw.make_args(E, H, I, w.tokens_sum, dev_in[0], dev_in[1], dev_in[2], out=out, out_ptrs=ptrs,
+                              out_dtype=kargs.out_dtype, accumulate=w.accumulate, input_order=kargs.input_order,
+                              status_dev=status)
+
+    def e2e_step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        if host_c is not None:
+            out.copy_(host_c, non_blocking=True)
+        if w.fp8:
+            kgw.kgw_wgrad_fp8_blockscaled(kargs_e2e, dev_in[3], dev_in[4], ws, stream=stream)
+        else:
+            kgw.kgw_wgrad_bf16(kargs_e2e, ws, stream=stream)
+        if res_dev is not None:
+            host_out.copy_(res_dev, non_blocking=True)
+        else:
+            for e in range(E):
+                host_out[e].copy_(outs_list[e], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {kgw.kgw_status_string(int(status.item()))}")
+    return ms_per_step, per_launch_ms, e2e_ms, h2d, d2h, clk
+
+
+def cpu_oracle_rate(w, budget_s: float):
+    """Time the float64 oracle on the host cores over whole experts until ``budget_s`` is spent."""
+    import oracle.kgw_oracle as O
+
+    x = W.make_inputs(w, "cpu")
+    bits = (lambda t: t.contiguous().view(torch.uint8).numpy()) if w.fp8 else \
+        (lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16))
+    a_bits, b_bits = bits(x.a), bits(x.b)
+    dec = O.e4m3_to_f64 if w.fp8 else O.bf16_to_f64
+    A = O.logical_a(dec(a_bits), w.hidden, w.offsets, w.input_order)
+    B = O.logical_b(dec(b_bits), w.intermediate, w.offsets, w.input_order)
+    if w.fp8:
+        A = O.apply_block_scales_rows(A, x.sfa.numpy())
+        B = O.apply_block_scales_cols(B, x.sfb.numpy())
+    ranges = O.expert_ranges(w.offsets)
+    flops = 0.0
+    done = []
+    t0 = time.perf_counter()
+    for e, (b, end) in enumerate(ranges):
+        if end == b:
+            continue
+        sub_off = np.array([end - b], dtype=np.int64)
+        O.wgrad(A[:, b:end], B[b:end, :], sub_off, with_bound=False)
+        flops += 2.0 * w.hidden * w.intermediate * (end - b)
+        done.append(e)
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, done
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max((i.get("num_threads", 0) for i in info), default=os.cpu_count())
+    except Exception:
+        return os.cpu_count()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="balanced", choices=sorted(W.NAMED))
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_env()
+    w = W.NAMED[args.workload]()
+    flops = w.flops
+    config = {"workload": w.name, "experts": w.num_experts, "hidden": w.hidden, "intermediate": w.intermediate,
+              "tokens_sum": w.tokens_sum, "input_order": w.input_order, "output": f"{w.output_mode} {w.out_dtype}",
+              "accumulate": w.accumulate, "l2": "inputs larger than L2 (no flush needed)",
+              "parallelism": f"replica x{args.gpus}"}
+    if w.tokens_sum * (w.hidden + w.intermediate) * 2 < 129e6:
+        config["l2"] = "working set fits L2 (warm)"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        budget = max(2.0, min(15.0, 120.0 / max(1, args.steps + args.warmup)))
+        rates = []
+        for i in range(args.warmup + args.steps):
+            r, dt, done = cpu_oracle_rate(w, budget)
+            if i >= args.warmup:
+                rates.append((r, dt))
+        val = statistics.median(r for r, _ in rates)
+        ms = statistics.median(dt for _, dt in rates) * 1e3
+        line = {"impl": "reference", "metric": "K-grouped wgrad TFLOP/s (2*H*I*sum n_e)", "value": val,
+                "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                                 "sample": f"float64 oracle over whole experts, about {budget:.0f} s per step"},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    ms_per_step, per_launch, e2e_ms, h2d, d2h, clk = run_ours(args, w, rank, local, world)
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    peaks = measured_peaks()
+    launch_ms = statistics.mean(per_launch)
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"] * (2.0 if w.fp8 else 1.0)
+    traffic = traffic_record(args.workload)
+    line = {"metric": "K-grouped wgrad TFLOP/s (2*H*I*sum n_e)", "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8" if w.fp8 else "bf16", "data": "synthetic", "config": config,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes": algorithmic_bytes(w),
+                         "peak_source": f"{peaks['source']} bf16 burst" + (" x2 (fp8 nominal ratio)" if w.fp8 else ""),
+                         "kernel": "wgrad_kernel (+ plan_kernel, a few us, inside the same events)"},
+            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, dt, done = cpu_oracle_rate(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": r, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"float64 oracle on experts {done} of the same workload ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

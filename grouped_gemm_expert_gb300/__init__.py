@@ -1,0 +1,202 @@
+"""Python binding of the K-grouped MoE weight-gradient library (``libkgw.so``).
+
+Argument marshalling only: every step of the operation runs in the CUDA kernels of the
+shared library. PyTorch supplies device memory and streams. There is no fallback: if the
+library has not been built (``python -m grouped_gemm_expert_gb300.build``) or the device is
+not sm_103, calls raise.
+
+The functions keep the C names of ``include/kgw.h``:
+
+  kgw_workspace_size(args, is_fp8) -> int
+  kgw_wgrad_bf16(args, workspace, stream=None)
+  kgw_wgrad_fp8_blockscaled(args, sfa, sfb, workspace, stream=None)
+  kgw_status_string(code) -> str
+  kgw_version() -> int
+  kgw_debug_set(key, value) -> int
+
+``make_args`` builds the argument struct from torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkgw.so")
+
+KGW_OK = 0
+KGW_ERR_INVALID_ARG = 1
+KGW_ERR_UNSUPPORTED = 2
+KGW_ERR_ALIGNMENT = 3
+KGW_ERR_DEVICE = 4
+KGW_ERR_CUDA = 5
+KGW_ERR_OFFSETS = 6
+KGW_ERR_TIMEOUT = 7
+KGW_ERR_WORKSPACE = 8
+KGW_ERR_OUT_PTRS = 9
+
+KGW_K_MAJOR = 0
+KGW_MN_MAJOR = 1
+KGW_TENSOR2D = 0
+KGW_RAGGED = 1
+KGW_OUT_F32 = 0
+KGW_OUT_BF16 = 1
+
+EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
+            "kgw_status_string", "kgw_version", "kgw_debug_set")
+
+
+class KgwArgs(ctypes.Structure):
+    """Mirror of ``kgw_wgrad_args`` (include/kgw.h)."""
+    _fields_ = [
+        ("num_experts", ctypes.c_int32),
+        ("hidden", ctypes.c_int32),
+        ("intermediate", ctypes.c_int32),
+        ("tokens_sum", ctypes.c_int64),
+        ("a", ctypes.c_void_p),
+        ("a_major", ctypes.c_int32),
+        ("b", ctypes.c_void_p),
+        ("b_major", ctypes.c_int32),
+        ("offsets", ctypes.c_void_p),
+        ("input_order", ctypes.c_int32),
+        ("out", ctypes.c_void_p),
+        ("out_ptrs", ctypes.c_void_p),
+        ("out_dtype", ctypes.c_int32),
+        ("accumulate", ctypes.c_int32),
+        ("status_dev", ctypes.c_void_p),
+    ]
+
+
+class KgwError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {kgw_status_string(code)} ({code})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libkgw.so`` (raises if it is missing: there is no other implementation)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run `python -m grouped_gemm_expert_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.kgw_workspace_size.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
+        L.kgw_workspace_size.restype = ctypes.c_int
+        L.kgw_wgrad_bf16.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_wgrad_bf16.restype = ctypes.c_int
+        L.kgw_wgrad_fp8_blockscaled.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_wgrad_fp8_blockscaled.restype = ctypes.c_int
+        L.kgw_status_string.argtypes = [ctypes.c_int32]
+        L.kgw_status_string.restype = ctypes.c_char_p
+        L.kgw_version.argtypes = []
+        L.kgw_version.restype = ctypes.c_int32
+        L.kgw_debug_set.argtypes = [ctypes.c_int32, ctypes.c_int64]
+        L.kgw_debug_set.restype = ctypes.c_int64
+        _lib = L
+    return _lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def make_args(num_experts: int, hidden: int, intermediate: int, tokens_sum: int, a, b, offsets, *,
+              out=None, out_ptrs=None, out_dtype: int = KGW_OUT_F32, accumulate: bool = False,
+              input_order: int = KGW_TENSOR2D, a_major: int = KGW_K_MAJOR, b_major: int = KGW_MN_MAJOR,
+              status_dev=None) -> KgwArgs:
+    """Build ``kgw_wgrad_args``; tensors (or raw integer addresses) are passed by address."""
+    return KgwArgs(num_experts, hidden, intermediate, tokens_sum, _ptr(a), a_major, _ptr(b), b_major,
+                   _ptr(offsets), input_order, _ptr(out), _ptr(out_ptrs), out_dtype, int(bool(accumulate)),
+                   _ptr(status_dev))
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def kgw_status_string(code: int) -> str:
+    return lib().kgw_status_string(int(code)).decode()
+
+
+def kgw_version() -> int:
+    return int(lib().kgw_version())
+
+
+def kgw_debug_set(key: int, value: int) -> int:
+    return int(lib().kgw_debug_set(int(key), int(value)))
+
+
+def kgw_workspace_size(args: KgwArgs, is_fp8: bool = False) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().kgw_workspace_size(ctypes.byref(args), int(bool(is_fp8)), ctypes.byref(n))
+    if rc != KGW_OK:
+        raise KgwError(rc, "kgw_workspace_size")
+    return int(n.value)
+
+
+def kgw_wgrad_bf16(args: KgwArgs, workspace, workspace_bytes: Optional[int] = None, stream=None,
+                   check: bool = True) -> int:
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_wgrad_bf16(ctypes.byref(args), _ptr(workspace), nbytes, _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_bf16")
+    return rc
+
+
+def kgw_wgrad_fp8_blockscaled(args: KgwArgs, sfa, sfb, workspace, workspace_bytes: Optional[int] = None,
+                              stream=None, check: bool = True) -> int:
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_wgrad_fp8_blockscaled(ctypes.byref(args), _ptr(sfa), _ptr(sfb), _ptr(workspace), nbytes,
+                                         _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_fp8_blockscaled")
+    return rc
+
+
+# ---------------------------------------------------------------------------------------------
+# Convenience layer over torch tensors (still marshalling only)
+# ---------------------------------------------------------------------------------------------
+
+def workspace_for(args: KgwArgs, is_fp8: bool = False, device=None):
+    import torch
+    n = kgw_workspace_size(args, is_fp8)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def wgrad(a, b, offsets, *, hidden: int, intermediate: int, out=None, out_ptrs=None,
+          out_dtype: str = "f32", accumulate: bool = False, input_order: str = "tensor2d",
+          sfa=None, sfb=None, workspace=None, status_dev=None, stream=None):
+    """One call of the operation on torch CUDA tensors. ``a``/``b`` are bf16 or float8_e4m3fn.
+
+    Exactly one of ``out`` (dense [E, hidden, intermediate]) and ``out_ptrs`` (int64 [E]
+    device addresses) must be given. Returns ``out`` (or None for pointer outputs).
+    """
+    import torch
+    E = int(offsets.numel())
+    tokens_sum = int(b.shape[0]) if b.dim() == 2 else 0
+    fp8 = a.dtype == torch.float8_e4m3fn
+    args = make_args(E, hidden, intermediate, tokens_sum, a, b, offsets, out=out, out_ptrs=out_ptrs,
+                     out_dtype=KGW_OUT_BF16 if out_dtype == "bf16" else KGW_OUT_F32,
+                     accumulate=accumulate, input_order=KGW_RAGGED if input_order == "ragged" else KGW_TENSOR2D,
+                     status_dev=status_dev)
+    if workspace is None:
+        workspace = workspace_for(args, fp8, device=b.device)
+    if fp8:
+        kgw_wgrad_fp8_blockscaled(args, sfa, sfb, workspace, stream=stream)
+    else:
+        kgw_wgrad_bf16(args, workspace, stream=stream)
+    return out

@@ -1,0 +1,277 @@
+// Host side of the C ABI declared in include/kgw.h: argument validation, workspace sizing,
+// TMA tensor-map encoding and the two launches (plan + persistent kernel) of one call.
+//
+// The checks follow "Grouped GEMM + WGrad (Unified)", sections "BF16 contract", "Output modes"
+// and "Scheduling, cache, and errors" (unsupported dtypes or layouts, malformed or unaligned
+// pointers and devices below SM100 are rejected). Everything that needs the device-resident
+// offsets is checked on the device by the plan kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kgw.h"
+#include "kgw_internal.h"
+
+namespace {
+
+using kgw::WsLayout;
+
+std::atomic<int64_t> g_timeout_ns{2000000000LL};
+std::atomic<int64_t> g_drop_stage{-1};
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+struct DevInfo {
+  int sm_count = 0;
+  int major = 0, minor = 0;
+  bool valid = false;
+};
+constexpr int kMaxDevices = 64;
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+kgw_status device_info(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KGW_ERR_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return KGW_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev[dev].valid) {
+    DevInfo d;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return KGW_ERR_CUDA;
+    }
+    d.valid = true;
+    g_dev[dev] = d;
+  }
+  *out = g_dev[dev];
+  return KGW_OK;
+}
+
+kgw_status get_encoder() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q{};
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode ? KGW_OK : KGW_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int bk_of(bool fp8) { return fp8 ? kgw::BK_FP8 : kgw::BK_BF16; }
+
+// Upper bound of the FP32 partial tiles split-K can use for these shapes.
+int32_t slot_cap(const kgw_wgrad_args* a, bool fp8) {
+  const int64_t T = int64_t(a->hidden / kgw::BM) * (a->intermediate / kgw::BN);
+  const int64_t kit = a->tokens_sum / bk_of(fp8);
+  // an expert is split only when its k-iterations exceed the chunk (>= MIN_SPLIT_KITERS), and
+  // then into fewer than 2*kiters/chunk pieces
+  const int64_t bound = T * ((2 * kit) / kgw::MIN_SPLIT_KITERS);
+  return static_cast<int32_t>(bound < kgw::MAX_PARTIAL_SLOTS ? bound : kgw::MAX_PARTIAL_SLOTS);
+}
+
+kgw_status validate(const kgw_wgrad_args* a, bool fp8) {
+  if (!a) return KGW_ERR_INVALID_ARG;
+  if (a->num_experts < 1 || a->num_experts > kgw::MAX_EXPERTS) return KGW_ERR_INVALID_ARG;
+  if (a->hidden <= 0 || a->intermediate <= 0 || a->tokens_sum < 0) return KGW_ERR_INVALID_ARG;
+  if (a->tokens_sum % kgw::TOKEN_ALIGN != 0) return KGW_ERR_INVALID_ARG;
+  if (a->hidden % kgw::BM != 0 || a->intermediate % kgw::BN != 0) return KGW_ERR_UNSUPPORTED;
+  if (a->a_major != KGW_K_MAJOR && a->a_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
+  if (a->b_major != KGW_K_MAJOR && a->b_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
+  if (a->a_major != KGW_K_MAJOR || a->b_major != KGW_MN_MAJOR) return KGW_ERR_UNSUPPORTED;
+  if (a->input_order != KGW_TENSOR2D && a->input_order != KGW_RAGGED) return KGW_ERR_INVALID_ARG;
+  if (a->out_dtype != KGW_OUT_F32 && a->out_dtype != KGW_OUT_BF16) return KGW_ERR_INVALID_ARG;
+  if (a->accumulate != 0 && a->accumulate != 1) return KGW_ERR_INVALID_ARG;
+  if (!a->offsets) return KGW_ERR_INVALID_ARG;
+  if ((a->out == nullptr) == (a->out_ptrs == nullptr)) return KGW_ERR_INVALID_ARG;
+  if (!aligned(a->offsets, 4)) return KGW_ERR_ALIGNMENT;
+  if (a->out && !aligned(a->out, 16)) return KGW_ERR_ALIGNMENT;
+  if (a->out_ptrs && !aligned(a->out_ptrs, 8)) return KGW_ERR_ALIGNMENT;
+  if (a->status_dev && !aligned(a->status_dev, 4)) return KGW_ERR_ALIGNMENT;
+  if (a->tokens_sum > 0) {
+    if (!a->a || !a->b) return KGW_ERR_INVALID_ARG;
+    if (!aligned(a->a, 16) || !aligned(a->b, 16)) return KGW_ERR_ALIGNMENT;
+    const int64_t esz = fp8 ? 1 : 2;
+    // TMA coordinates are int32: the ragged view of A has tokens_sum*hidden*esz/128 rows.
+    if (a->input_order == KGW_RAGGED && (a->tokens_sum * a->hidden * esz) / 128 >= (int64_t(1) << 31))
+      return KGW_ERR_UNSUPPORTED;
+    if (a->tokens_sum >= (int64_t(1) << 31)) return KGW_ERR_UNSUPPORTED;
+  }
+  // work items must fit int32: T * (E + 2*kiters/MIN_SPLIT)
+  const int64_t T = int64_t(a->hidden / kgw::BM) * (a->intermediate / kgw::BN);
+  const int64_t items = T * (a->num_experts + 2 * (a->tokens_sum / bk_of(fp8)) / kgw::MIN_SPLIT_KITERS + 1);
+  if (items >= (int64_t(1) << 31)) return KGW_ERR_UNSUPPORTED;
+  return KGW_OK;
+}
+
+kgw_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KGW_OK : KGW_ERR_CUDA;
+}
+
+kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws, size_t ws_bytes,
+               void* stream) {
+  kgw_status st = validate(a, fp8);
+  if (st != KGW_OK) return st;
+  if (fp8 && !kgw::fp8_supported()) return KGW_ERR_UNSUPPORTED;
+  if (fp8 && a->tokens_sum > 0) {
+    if (!sfa || !sfb) return KGW_ERR_INVALID_ARG;
+    if (!aligned(sfa, 16) || !aligned(sfb, 16)) return KGW_ERR_ALIGNMENT;
+  }
+  if (!ws || !aligned(ws, 256)) return KGW_ERR_WORKSPACE;
+  const WsLayout L0 = kgw::ws_layout(a->num_experts, 0);
+  if (ws_bytes < L0.total) return KGW_ERR_WORKSPACE;
+  int32_t max_slots = slot_cap(a, fp8);
+  {
+    const size_t room = ws_bytes - L0.total;
+    const size_t fit = room / (kgw::PARTIAL_TILE_BYTES + 4 * kgw::NUM_EPI_WARPS);
+    if (size_t(max_slots) > fit) max_slots = static_cast<int32_t>(fit);
+    while (max_slots > 0 && kgw::ws_layout(a->num_experts, max_slots).total > ws_bytes) --max_slots;
+  }
+  const WsLayout L = kgw::ws_layout(a->num_experts, max_slots);
+
+  DevInfo dev;
+  st = device_info(&dev);
+  if (st != KGW_OK) return st;
+  if (dev.major != 10 || dev.minor != 3) return KGW_ERR_DEVICE;
+  if (get_encoder() != KGW_OK) return KGW_ERR_CUDA;
+
+  const int bk = bk_of(fp8);
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  if (a->tokens_sum > 0) {
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t esz = fp8 ? 1 : 2;
+    const uint64_t Ts = static_cast<uint64_t>(a->tokens_sum);
+    if (a->input_order == KGW_TENSOR2D) {
+      // A [hidden, tokens]: inner = tokens; box = bk tokens x 128 rows
+      st = encode_2d(&tmA, dt, a->a, Ts, static_cast<uint64_t>(a->hidden), Ts * esz, bk, kgw::BM);
+    } else {
+      // ragged A viewed as rows of 128 bytes; gathered four rows at a time (box one row high)
+      const uint64_t per_row = 128 / esz;
+      st = encode_2d(&tmA, dt, a->a, per_row, Ts * static_cast<uint64_t>(a->hidden) / per_row, 128, per_row, 1);
+    }
+    if (st != KGW_OK) return st;
+    // B [tokens, intermediate]: inner = intermediate; box = one 128-byte swizzle row x bk tokens
+    st = encode_2d(&tmB, dt, a->b, static_cast<uint64_t>(a->intermediate), Ts,
+                   static_cast<uint64_t>(a->intermediate) * esz, 128 / esz, bk);
+    if (st != KGW_OK) return st;
+  }
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  kgw::PlanParams pp{};
+  pp.E = a->num_experts;
+  pp.H = a->hidden;
+  pp.I = a->intermediate;
+  pp.tokens_sum = a->tokens_sum;
+  pp.offsets = a->offsets;
+  pp.out_ptrs = a->out_ptrs;
+  pp.accumulate = a->accumulate;
+  pp.bk = bk;
+  pp.grid = dev.sm_count;
+  pp.max_slots = max_slots;
+  pp.status_dev = a->status_dev;
+  pp.ws = static_cast<uint8_t*>(ws);
+  pp.L = L;
+  if (kgw::launch_plan(pp, s) != cudaSuccess) return KGW_ERR_CUDA;
+
+  kgw::MainParams mp{};
+  mp.E = a->num_experts;
+  mp.H = a->hidden;
+  mp.I = a->intermediate;
+  mp.tokens_sum = a->tokens_sum;
+  mp.offsets = a->offsets;
+  mp.out_ptrs = a->out_ptrs;
+  mp.out = a->out;
+  mp.out_bf16 = a->out_dtype == KGW_OUT_BF16;
+  mp.accumulate = a->accumulate;
+  mp.ragged = a->input_order == KGW_RAGGED;
+  mp.discrete = a->out_ptrs != nullptr;
+  mp.fp8 = fp8;
+  mp.num_m_tiles = a->hidden / kgw::BM;
+  mp.num_n_tiles = a->intermediate / kgw::BN;
+  mp.sfa = sfa;
+  mp.sfb = sfb;
+  mp.status_dev = a->status_dev;
+  mp.ws = static_cast<uint8_t*>(ws);
+  mp.L = L;
+  mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
+  mp.test_drop_stage = static_cast<int32_t>(g_drop_stage.load());
+  cudaError_t e = fp8 ? kgw::launch_main_fp8(mp, tmA, tmB, dev.sm_count, s)
+                      : kgw::launch_main_bf16(mp, tmA, tmB, dev.sm_count, s);
+  return e == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t* bytes) {
+  if (!bytes) return KGW_ERR_INVALID_ARG;
+  kgw_status st = validate(args, is_fp8 != 0);
+  if (st != KGW_OK) return st;
+  *bytes = kgw::ws_layout(args->num_experts, slot_cap(args, is_fp8 != 0)).total;
+  return KGW_OK;
+}
+
+kgw_status kgw_wgrad_bf16(const kgw_wgrad_args* args, void* workspace, size_t workspace_bytes, void* stream) {
+  return run(args, false, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+kgw_status kgw_wgrad_fp8_blockscaled(const kgw_wgrad_args* args, const float* sfa, const float* sfb,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  return run(args, true, sfa, sfb, workspace, workspace_bytes, stream);
+}
+
+const char* kgw_status_string(int32_t status) {
+  switch (status) {
+    case KGW_OK: return "KGW_OK";
+    case KGW_ERR_INVALID_ARG: return "KGW_ERR_INVALID_ARG";
+    case KGW_ERR_UNSUPPORTED: return "KGW_ERR_UNSUPPORTED";
+    case KGW_ERR_ALIGNMENT: return "KGW_ERR_ALIGNMENT";
+    case KGW_ERR_DEVICE: return "KGW_ERR_DEVICE";
+    case KGW_ERR_CUDA: return "KGW_ERR_CUDA";
+    case KGW_ERR_OFFSETS: return "KGW_ERR_OFFSETS";
+    case KGW_ERR_TIMEOUT: return "KGW_ERR_TIMEOUT";
+    case KGW_ERR_WORKSPACE: return "KGW_ERR_WORKSPACE";
+    case KGW_ERR_OUT_PTRS: return "KGW_ERR_OUT_PTRS";
+    default: return "KGW_ERR_UNKNOWN";
+  }
+}
+
+int32_t kgw_version(void) { return 100; }
+
+int64_t kgw_debug_set(int32_t key, int64_t value) {
+  switch (key) {
+    case 1: return g_timeout_ns.exchange(value > 0 ? value : 1);
+    case 2: return g_drop_stage.exchange(value);
+    default: return -1;
+  }
+}
+
+}  // extern "C"

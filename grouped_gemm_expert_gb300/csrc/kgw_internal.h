@@ -1,0 +1,118 @@
+// Internal definitions shared by the host library (kgw_api.cu) and the kernels (kgw_kernels.cu).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+
+#include "kgw.h"
+
+namespace kgw {
+
+// Tile shape of the persistent kernel: one CTA owns a BM x BN output tile in TMEM (FP32,
+// BN columns), two such accumulators (512 TMEM columns) so the epilogue of one tile overlaps
+// the main loop of the next. BK is one 128-byte swizzle row of the operand type along K.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK_BF16 = 64;    // 64 bf16 = 128 bytes
+constexpr int BK_FP8 = 128;    // 128 e4m3 = 128 bytes = one scale block
+constexpr int STAGES = 4;
+constexpr int TOKEN_ALIGN = 256;
+constexpr int SCALE_BLOCK = 128;
+
+constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int EPI_WARP0 = 2;
+constexpr int NUM_EPI_WARPS = 4;
+constexpr int WORK_RING = 8;       // depth of the shared-memory work-item queue
+
+constexpr int MAX_EXPERTS = 4096;
+constexpr int PLAN_THREADS = 1024;
+constexpr int MIN_SPLIT_KITERS = 32;   // never split an expert's K into chunks shorter than this
+constexpr int MAX_PARTIAL_SLOTS = 256; // FP32 partial tiles for split-K (128 KiB each)
+constexpr size_t PARTIAL_TILE_BYTES = size_t(BM) * BN * sizeof(float);
+
+constexpr uint32_t STAGE_A_BYTES = BM * 128;          // 16 KiB, both dtypes
+constexpr uint32_t STAGE_B_BYTES = BN * 128;          // 32 KiB, both dtypes
+constexpr uint32_t STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
+// FP8 scale factors per stage: 128 rows (A) and 256 columns (B) x one UE8M0 byte replicated
+// to 4 bytes, staged as 16-byte rows for the TMEM copy.
+constexpr uint32_t SF_A_BYTES = BM * 16;
+constexpr uint32_t SF_B_BYTES = BN * 16;
+
+struct PlanHeader {
+  int32_t error;          // kgw_status found by the plan kernel (0 = OK)
+  int32_t total_items;    // work items of this call
+  int32_t chunk_kiters;   // split-K chunk length in k-iterations
+  int32_t slots_used;     // FP32 partial tiles in use
+  int32_t counters_used;  // split tiles (one arrival counter each)
+  int32_t item_counter;   // dynamic scheduler: next item to hand out
+  int32_t pad[58];
+};
+static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte block");
+
+// Workspace layout (all offsets 256-byte aligned):
+//   [PlanHeader][order E][item_prefix E+1][splits E][slot_base E][counter_base E]
+//   [arrival counters 4*max_slots (one per split tile and TMEM lane quadrant)]
+//   [partials max_slots * PARTIAL_TILE_BYTES]
+struct WsLayout {
+  size_t order, item_prefix, splits, slot_base, counter_base, counters, partials, total;
+  int32_t max_slots;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int32_t E, int32_t max_slots) {
+  WsLayout L{};
+  size_t off = sizeof(PlanHeader);
+  L.order = off;        off = align256(off + sizeof(int32_t) * E);
+  L.item_prefix = off;  off = align256(off + sizeof(int32_t) * (E + 1));
+  L.splits = off;       off = align256(off + sizeof(int32_t) * E);
+  L.slot_base = off;    off = align256(off + sizeof(int32_t) * E);
+  L.counter_base = off; off = align256(off + sizeof(int32_t) * E);
+  L.counters = off;     off = align256(off + sizeof(int32_t) * NUM_EPI_WARPS * (max_slots > 0 ? max_slots : 1));
+  L.partials = off;     off = align256(off + PARTIAL_TILE_BYTES * size_t(max_slots));
+  L.total = off;
+  L.max_slots = max_slots;
+  return L;
+}
+
+struct PlanParams {
+  int32_t E, H, I;
+  int64_t tokens_sum;
+  const int32_t* offsets;
+  const int64_t* out_ptrs;      // discrete mode, else null
+  int32_t accumulate;
+  int32_t bk;                   // k-iteration length in tokens
+  int32_t grid;                 // CTAs of the main kernel
+  int32_t max_slots;
+  int32_t* status_dev;
+  uint8_t* ws;
+  WsLayout L;
+};
+
+struct MainParams {
+  int32_t E, H, I;
+  int64_t tokens_sum;
+  const int32_t* offsets;
+  const int64_t* out_ptrs;
+  void* out;
+  int32_t out_bf16, accumulate, ragged, discrete, fp8;
+  int32_t num_m_tiles, num_n_tiles;
+  const float* sfa;             // FP8: [tokens_sum/128, H]
+  const float* sfb;             // FP8: [tokens_sum/128, I]
+  int32_t* status_dev;
+  uint8_t* ws;
+  WsLayout L;
+  uint64_t timeout_ns;
+  int32_t test_drop_stage;      // test hook: >=0 makes the producer skip one arrival (timeout path)
+};
+
+// Launchers (kgw_kernels.cu).
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
+cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                             cudaStream_t s);
+cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                            cudaStream_t s);
+size_t main_smem_bytes(bool fp8);
+bool fp8_supported();
+
+}  // namespace kgw

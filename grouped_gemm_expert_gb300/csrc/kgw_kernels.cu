@@ -1,0 +1,669 @@
+// Kernels of the K-grouped weight-gradient GEMM for sm_103a.
+//
+//   plan_kernel  (1 CTA)      validates the device-resident offsets, decides split-K, orders
+//                             experts longest-first and writes the per-call schedule into the
+//                             workspace ("Grouped GEMM + WGrad (Unified)", sections "BF16 contract"
+//                             and "Scheduling, cache, and errors": dynamic persistent scheduling).
+//   wgrad_kernel (1 CTA / SM) persistent, warp-specialised: warp 0 claims work items from an
+//                             atomic counter and streams K-slices of A and B with TMA into a
+//                             4-stage shared-memory ring; warp 1 issues tcgen05.mma into one of two
+//                             FP32 TMEM accumulators; warps 2..5 drain TMEM and write the output
+//                             (overwrite / accumulate, FP32 / BF16, dense / per-expert pointers),
+//                             reducing split-K partial tiles in a fixed order.
+//
+// A work item is (expert, m-tile, n-tile, K chunk). For expert e the contraction runs over tokens
+// [begin_e, end_e) ("Grouped GEMM + WGrad (Unified)", section "Operation").
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kgw_internal.h"
+#include "kgw_ptx.cuh"
+
+namespace kgw {
+
+// =============================================================================================
+// Plan kernel
+// =============================================================================================
+
+__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* s_warp, int64_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;
+  }
+  __syncthreads();
+  const int64_t base = warp ? s_warp[warp - 1] : 0;
+  *total = s_warp[nwarps - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+// Per-thread contiguous chunk of [0, n): thread t owns [t*c, min(n, (t+1)*c)).
+struct Chunk {
+  int lo, hi;
+};
+__device__ __forceinline__ Chunk my_chunk(int n) {
+  const int c = (n + blockDim.x - 1) / blockDim.x;
+  int lo = threadIdx.x * c;
+  int hi = lo + c;
+  if (lo > n) lo = n;
+  if (hi > n) hi = n;
+  return {lo, hi};
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanParams p) {
+  __shared__ int32_t s_kit[MAX_EXPERTS];    // k-iterations per expert
+  __shared__ int32_t s_key[MAX_EXPERTS];    // k-iterations per item (ordering key)
+  __shared__ int64_t s_warp[32];
+  __shared__ int32_t s_err;
+
+  const int E = p.E;
+  const int tid = threadIdx.x;
+  const int T = (p.H / BM) * (p.I / BN);
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
+  int32_t* order = reinterpret_cast<int32_t*>(p.ws + p.L.order);
+  int32_t* item_prefix = reinterpret_cast<int32_t*>(p.ws + p.L.item_prefix);
+  int32_t* splits = reinterpret_cast<int32_t*>(p.ws + p.L.splits);
+  int32_t* slot_base = reinterpret_cast<int32_t*>(p.ws + p.L.slot_base);
+  int32_t* counter_base = reinterpret_cast<int32_t*>(p.ws + p.L.counter_base);
+  int32_t* counters = reinterpret_cast<int32_t*>(p.ws + p.L.counters);
+
+  if (tid == 0) s_err = 0;
+  __syncthreads();
+
+  // 1. counts and validation (section "BF16 contract": non-decreasing cumulative sum, every
+  //    count a multiple of 256, final offset == tokens_sum; "Output modes": one non-null,
+  //    16-byte-aligned address per expert).
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int64_t prev = e ? static_cast<int64_t>(p.offsets[e - 1]) : 0;
+    const int64_t cur = p.offsets[e];
+    const int64_t n = cur - prev;
+    int err = 0;
+    if (n < 0 || (n % TOKEN_ALIGN) != 0) err = KGW_ERR_OFFSETS;
+    if (e == E - 1 && cur != p.tokens_sum) err = KGW_ERR_OFFSETS;
+    if (!err && p.out_ptrs) {
+      const uint64_t ptr = static_cast<uint64_t>(p.out_ptrs[e]);
+      if (ptr == 0 || (ptr & 15u)) err = KGW_ERR_OUT_PTRS;
+    }
+    if (err) atomicMax(&s_err, err == KGW_ERR_OFFSETS ? 2 : 1);
+    s_kit[e] = n > 0 ? static_cast<int32_t>(n / p.bk) : 0;
+  }
+  __syncthreads();
+  if (s_err) {
+    if (tid == 0) {
+      const int code = s_err == 2 ? KGW_ERR_OFFSETS : KGW_ERR_OUT_PTRS;
+      hdr->error = code;
+      hdr->total_items = 0;
+      hdr->item_counter = 0;
+      hdr->slots_used = 0;
+      hdr->counters_used = 0;
+      if (p.status_dev) *p.status_dev = code;
+    }
+    return;
+  }
+
+  // 2. total k-iterations W = T * sum(kiters)
+  int64_t mysum = 0;
+  const Chunk ch = my_chunk(E);
+  for (int e = ch.lo; e < ch.hi; ++e) mysum += s_kit[e];
+  int64_t ksum;
+  block_exclusive_scan(mysum, s_warp, &ksum);
+  const int64_t W = ksum * T;
+
+  // 3. split-K chunk: items no longer than W/(2*grid) k-iterations (at least MIN_SPLIT_KITERS),
+  //    doubled until the partial tiles fit in the workspace.
+  int64_t C = (W + 2 * int64_t(p.grid) - 1) / (2 * int64_t(p.grid));
+  if (C < MIN_SPLIT_KITERS) C = MIN_SPLIT_KITERS;
+  int64_t slots = 0;
+  for (int iter = 0; iter < 40; ++iter) {
+    int64_t mine = 0;
+    for (int e = ch.lo; e < ch.hi; ++e)
+      if (s_kit[e] > C) mine += int64_t(T) * ((s_kit[e] + C - 1) / C);
+    block_exclusive_scan(mine, s_warp, &slots);
+    if (slots <= p.max_slots) break;
+    C *= 2;
+  }
+  if (slots > p.max_slots) {  // cannot happen once C exceeds every expert; keep it safe
+    C = int64_t(1) << 40;
+    slots = 0;
+  }
+
+  // 4. per-expert splits, item counts and ordering keys
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int kit = s_kit[e];
+    const int ns = kit > C ? static_cast<int>((kit + C - 1) / C) : 1;
+    splits[e] = ns;
+    s_key[e] = kit > 0 ? (kit + ns - 1) / ns : 0;
+  }
+  __syncthreads();
+
+  // 5. longest items first (ties by expert index): rank = #experts ordered before e
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int key = s_key[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const int kf = s_key[f];
+      rank += (kf > key) || (kf == key && f < e);
+    }
+    order[rank] = e;
+  }
+  __syncthreads();
+  __threadfence_block();
+
+  // 6. item prefix over the ordered experts
+  int64_t myitems = 0;
+  for (int q = ch.lo; q < ch.hi; ++q) {
+    const int e = order[q];
+    myitems += s_kit[e] > 0 ? int64_t(T) * splits[e] : (p.accumulate ? 0 : T);
+  }
+  int64_t total_items;
+  int64_t run = block_exclusive_scan(myitems, s_warp, &total_items);
+  for (int q = ch.lo; q < ch.hi; ++q) {
+    item_prefix[q] = static_cast<int32_t>(run);
+    const int e = order[q];
+    run += s_kit[e] > 0 ? int64_t(T) * splits[e] : (p.accumulate ? 0 : T);
+  }
+  if (tid == 0) item_prefix[E] = static_cast<int32_t>(total_items);
+
+  // 7. partial-slot and counter bases for split experts (expert index order)
+  int64_t myslots = 0, mycnt = 0;
+  for (int e = ch.lo; e < ch.hi; ++e)
+    if (splits[e] > 1) {
+      myslots += int64_t(T) * splits[e];
+      mycnt += T;
+    }
+  int64_t slots_total, cnt_total;
+  int64_t sb = block_exclusive_scan(myslots, s_warp, &slots_total);
+  int64_t cb = block_exclusive_scan(mycnt, s_warp, &cnt_total);
+  for (int e = ch.lo; e < ch.hi; ++e) {
+    if (splits[e] > 1) {
+      slot_base[e] = static_cast<int32_t>(sb);
+      counter_base[e] = static_cast<int32_t>(cb);
+      sb += int64_t(T) * splits[e];
+      cb += T;
+    } else {
+      slot_base[e] = -1;
+      counter_base[e] = -1;
+    }
+  }
+
+  // 8. split-tile arrival counters start at zero every call
+  for (int64_t i = tid; i < cnt_total * NUM_EPI_WARPS; i += blockDim.x) counters[i] = 0;
+
+  if (tid == 0) {
+    hdr->error = 0;
+    hdr->total_items = static_cast<int32_t>(total_items);
+    hdr->chunk_kiters = static_cast<int32_t>(C > 0x7fffffff ? 0x7fffffff : C);
+    hdr->slots_used = static_cast<int32_t>(slots_total);
+    hdr->counters_used = static_cast<int32_t>(cnt_total);
+    hdr->item_counter = 0;
+    if (p.status_dev) *p.status_dev = KGW_OK;
+  }
+}
+
+// =============================================================================================
+// Main kernel
+// =============================================================================================
+
+struct Item {
+  int e;
+  int m0, n0;
+  int kbeg, kend;        // k-iterations (relative to the expert's first token)
+  int split, nsplit, tile;
+  int64_t begin;         // expert's first token
+  int64_t n_e;           // expert's token count
+};
+
+__device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk) {
+  const int32_t* order = reinterpret_cast<const int32_t*>(p.ws + p.L.order);
+  const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + p.L.item_prefix);
+  const int32_t* splits = reinterpret_cast<const int32_t*>(p.ws + p.L.splits);
+  int lo = 0, hi = p.E;  // largest q with prefix[q] <= idx
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(prefix + mid) <= idx) lo = mid; else hi = mid;
+  }
+  Item it;
+  it.e = __ldg(order + lo);
+  const int local = idx - __ldg(prefix + lo);
+  it.nsplit = __ldg(splits + it.e);
+  const int T = p.num_m_tiles * p.num_n_tiles;
+  it.split = local / T;
+  it.tile = local - it.split * T;
+  const int mt = it.tile / p.num_n_tiles;
+  const int nt = it.tile - mt * p.num_n_tiles;
+  it.m0 = mt * BM;
+  it.n0 = nt * BN;
+  it.begin = it.e ? static_cast<int64_t>(__ldg(p.offsets + it.e - 1)) : 0;
+  it.n_e = static_cast<int64_t>(__ldg(p.offsets + it.e)) - it.begin;
+  const int64_t kit = it.n_e / bk;
+  it.kbeg = static_cast<int>(it.split * kit / it.nsplit);
+  it.kend = static_cast<int>((it.split + 1) * kit / it.nsplit);
+  return it;
+}
+
+struct SmemCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t wfull[WORK_RING];
+  uint64_t wempty[WORK_RING];
+  uint64_t mma_done;
+  int32_t work_item[WORK_RING];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+size_t main_smem_bytes(bool fp8) {
+  size_t b = size_t(STAGES) * STAGE_BYTES;
+  if (fp8) b += size_t(STAGES) * (SF_A_BYTES + SF_B_BYTES);
+  return b + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
+}
+
+// Wait without the abort short-cut (used only while draining at the end).
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  int dummy = 0;
+  return wait_bounded(bar, parity, &dummy, timeout_ns);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Epilogue helpers: thread owns one output row; c = 32-column chunk index within the tile.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void store_chunk(const MainParams& p, char* row_ptr, int c, const float* v) {
+  if (!p.out_bf16) {
+    float4* dst = reinterpret_cast<float4*>(row_ptr) + c * 8;
+    if (p.accumulate) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float4 o = dst[j];
+        o.x += v[4 * j + 0];
+        o.y += v[4 * j + 1];
+        o.z += v[4 * j + 2];
+        o.w += v[4 * j + 3];
+        dst[j] = o;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(row_ptr) + c * 4;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float w[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) w[t] = v[8 * j + t];
+      if (p.accumulate) {
+        const uint4 o = dst[j];
+        w[0] += bf16_lo(o.x); w[1] += bf16_hi(o.x);
+        w[2] += bf16_lo(o.y); w[3] += bf16_hi(o.y);
+        w[4] += bf16_lo(o.z); w[5] += bf16_hi(o.z);
+        w[6] += bf16_lo(o.w); w[7] += bf16_hi(o.w);
+      }
+      uint4 r;
+      r.x = pack_bf16x2(w[0], w[1]);
+      r.y = pack_bf16x2(w[2], w[3]);
+      r.z = pack_bf16x2(w[4], w[5]);
+      r.w = pack_bf16x2(w[6], w[7]);
+      dst[j] = r;
+    }
+  }
+}
+
+__device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it, int row) {
+  const size_t esz = p.out_bf16 ? 2 : 4;
+  const size_t r = static_cast<size_t>(it.m0 + row);
+  if (p.discrete) {
+    char* base = reinterpret_cast<char*>(static_cast<uintptr_t>(__ldg(p.out_ptrs + it.e)));
+    return base + (r * p.I + it.n0) * esz;
+  }
+  return reinterpret_cast<char*>(p.out) + ((static_cast<size_t>(it.e) * p.H + r) * p.I + it.n0) * esz;
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
+                 const __grid_constant__ CUtensorMap tmB) {
+  extern __shared__ uint8_t smem_raw[];
+  const int bk = kFp8 ? BK_FP8 : BK_BF16;
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
+  if (hdr->error != 0) return;  // offsets/pointers rejected by the plan: write nothing
+  const int total_items = hdr->total_items;
+  if (total_items == 0) return;
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_mem = base;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(base + size_t(STAGES) * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int32_t* item_counter = const_cast<int32_t*>(&hdr->item_counter);
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&ctl->tfull[a], 1);
+      mbar_init(&ctl->tempty[a], NUM_EPI_WARPS * 32);
+    }
+    for (int w = 0; w < WORK_RING; ++w) {
+      mbar_init(&ctl->wfull[w], 1);
+      mbar_init(&ctl->wempty[w], 1 + NUM_EPI_WARPS);
+    }
+    mbar_init(&ctl->mma_done, 1);
+    ctl->abort_flag = 0;
+    fence_mbarrier_init();
+    if (p.tokens_sum > 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ======================= TMA producer + scheduler =======================
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    int cur = 0;
+    if (lane == 0) cur = atomicAdd(item_counter, 1);
+    for (int n = 0;; ++n) {
+      const int slot = n % WORK_RING;
+      bool ok = true;
+      if (lane == 0) {
+        ok = wait_bounded(&ctl->wempty[slot], ((n / WORK_RING) & 1) ^ 1, abort_flag, p.timeout_ns);
+        if (ok) {
+          ctl->work_item[slot] = cur < total_items ? cur : -1;
+          mbar_arrive(&ctl->wfull[slot]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      cur = __shfl_sync(0xffffffffu, cur, 0);
+      if (!ok || cur >= total_items) break;
+      int nxt = 0;
+      if (lane == 0) nxt = atomicAdd(item_counter, 1);
+      const Item it = decode_item(p, cur, bk);
+      for (int kb = it.kbeg; kb < it.kend; ++kb) {
+        bool ok2 = true;
+        const bool drop = (p.test_drop_stage >= 0 && blockIdx.x == 0 && issued == p.test_drop_stage);
+        if (lane == 0) {
+          ok2 = wait_bounded(&ctl->empty[stage], phase ^ 1, abort_flag, p.timeout_ns);
+          if (ok2 && !drop) mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
+        }
+        ok2 = __shfl_sync(0xffffffffu, ok2, 0);
+        if (!ok2) break;
+        uint8_t* sA = stage_mem + size_t(stage) * STAGE_BYTES;
+        uint8_t* sB = sA + STAGE_A_BYTES;
+        const int64_t tok = it.begin + int64_t(kb) * bk;
+        if (!drop) {
+          if (!p.ragged) {
+            if (lane == 0) tma_load_2d(sA, &tmA, &ctl->full[stage], static_cast<int32_t>(tok), it.m0);
+          } else {
+            // Ragged A: expert e's block is [H, n_e] row-major at element begin*H. View the buffer
+            // as rows of 128 bytes; tile row r, K-slice kb lives in view row
+            // (begin*H + (m0+r)*n_e + kb*bk) * elem / 128. Lane q fetches tile rows 4q..4q+3.
+            const int64_t elems_per_row = kFp8 ? 128 : 64;
+            const int64_t base_el = it.begin * p.H + int64_t(kb) * bk;
+            int32_t y[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              y[j] = static_cast<int32_t>((base_el + int64_t(it.m0 + 4 * lane + j) * it.n_e) / elems_per_row);
+            tma_gather4(sA + 4 * lane * 128, &tmA, &ctl->full[stage], 0, y[0], y[1], y[2], y[3]);
+          }
+          if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) {
+              if constexpr (kFp8) {
+                // FP8 B tiles are 128 columns (128 bytes) wide
+                if (j < BN / 128)
+                  tma_load_2d(sB + j * (128 * 128), &tmB, &ctl->full[stage], it.n0 + 128 * j,
+                              static_cast<int32_t>(tok));
+              } else {
+                tma_load_2d(sB + j * (64 * 128), &tmB, &ctl->full[stage], it.n0 + 64 * j,
+                            static_cast<int32_t>(tok));
+              }
+            }
+          }
+        }
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+      cur = nxt;
+    }
+    // Drain: every stage issued in the last STAGES k-iterations must land before exit.
+    if (lane == 0) {
+      int s = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < STAGES && i < issued; ++i) {
+        if (--s < 0) {
+          s = STAGES - 1;
+          ph ^= 1;
+        }
+        wait_drain(&ctl->full[s], ph, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int tcount = 0;
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, 1);
+      for (int n = 0;; ++n) {
+        const int slot = n % WORK_RING;
+        if (!wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns)) break;
+        const int cur = ctl->work_item[slot];
+        mbar_arrive(&ctl->wempty[slot]);
+        if (cur < 0) break;
+        const Item it = decode_item(p, cur, bk);
+        if (it.kend == it.kbeg) continue;
+        const int acc = tcount & 1;
+        const uint32_t use = static_cast<uint32_t>(tcount >> 1);
+        if (!wait_bounded(&ctl->tempty[acc], (use & 1) ^ 1, abort_flag, p.timeout_ns)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = it.kbeg; kb < it.kend; ++kb) {
+          if (!wait_bounded(&ctl->full[stage], phase, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * STAGE_BYTES);
+          const uint32_t b_addr = a_addr + STAGE_A_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; K step of 16 = 32 bytes.
+            const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
+            // B: MN-major, 64-column (128 B) atoms 8 KiB apart along N, 8-row K groups 1024 B
+            // apart; K step of 16 rows = 2048 bytes.
+            const uint64_t bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
+            mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > it.kbeg || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&ctl->empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&ctl->tfull[acc]);
+        ++tcount;
+      }
+      // All MMAs issued by this thread complete before TMEM is released.
+      mma_commit(&ctl->mma_done);
+      wait_drain(&ctl->mma_done, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ======================= Epilogue (warps 2..5) =======================
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane;          // tile row owned by this thread
+    int32_t* counters = reinterpret_cast<int32_t*>(p.ws + p.L.counters);
+    const int32_t* slot_base = reinterpret_cast<const int32_t*>(p.ws + p.L.slot_base);
+    const int32_t* counter_base = reinterpret_cast<const int32_t*>(p.ws + p.L.counter_base);
+    float* partials = reinterpret_cast<float*>(p.ws + p.L.partials);
+    int tcount = 0;
+    for (int n = 0;; ++n) {
+      const int slot = n % WORK_RING;
+      const bool okw = wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, okw)) break;
+      const int cur = ctl->work_item[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->wempty[slot]);
+      if (cur < 0) break;
+      const Item it = decode_item(p, cur, bk);
+      char* orow = out_row_ptr(p, it, row);
+      if (it.kend == it.kbeg) {
+        // empty expert, overwrite mode: the output tile is zero
+        if (p.out_bf16) {
+          uint4* d = reinterpret_cast<uint4*>(orow);
+#pragma unroll 4
+          for (int j = 0; j < BN * 2 / 16; ++j) d[j] = make_uint4(0, 0, 0, 0);
+        } else {
+          float4* d = reinterpret_cast<float4*>(orow);
+#pragma unroll 4
+          for (int j = 0; j < BN * 4 / 16; ++j) d[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        continue;
+      }
+      const int acc = tcount & 1;
+      const uint32_t use = static_cast<uint32_t>(tcount >> 1);
+      const bool okt = wait_bounded(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, okt)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      if (it.nsplit == 1) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+          store_chunk(p, orow, c, reinterpret_cast<const float*>(r));
+        }
+        tc_fence_before();
+        mbar_arrive(&ctl->tempty[acc]);
+      } else {
+        // split-K: publish this chunk's FP32 partial rows. Each warp owns 32 rows and its own
+        // arrival counter per (tile, lane quadrant), so no cross-warp barrier is needed; the
+        // last arriving warp sums the partials of its rows in split order (deterministic).
+        const int sb = __ldg(slot_base + it.e) + it.tile * it.nsplit;
+        float4* mine = reinterpret_cast<float4*>(partials + (size_t(sb + it.split) * BM + row) * BN);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            __stcg(mine + c * 8 + j, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+        }
+        tc_fence_before();
+        mbar_arrive(&ctl->tempty[acc]);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const int cidx = (__ldg(counter_base + it.e) + it.tile) * NUM_EPI_WARPS + q;
+          last = atomicAdd(counters + cidx, 1) == it.nsplit - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            for (int s = 0; s < it.nsplit; ++s) {
+              const float4* src = reinterpret_cast<const float4*>(partials + (size_t(sb + s) * BM + row) * BN) + c * 8;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 x = __ldcg(src + j);
+                v[4 * j] += x.x;
+                v[4 * j + 1] += x.y;
+                v[4 * j + 2] += x.z;
+                v[4 * j + 3] += x.w;
+              }
+            }
+            store_chunk(p, orow, c, v);
+          }
+        }
+      }
+      ++tcount;
+    }
+  }
+
+  // ======================= teardown =======================
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+  if (threadIdx.x == 0 && ctl->abort_flag && p.status_dev) atomicExch(p.status_dev, KGW_ERR_TIMEOUT);
+}
+
+// =============================================================================================
+// Launchers
+// =============================================================================================
+
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
+  plan_kernel<<<1, PLAN_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <bool kFp8>
+static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                               cudaStream_t s) {
+  const size_t smem = main_smem_bytes(kFp8);
+  // set on every launch: the attribute is per device and the call is cheap
+  cudaError_t e = cudaFuncSetAttribute(wgrad_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  wgrad_kernel<kFp8><<<grid, NUM_THREADS, smem, s>>>(p, tmA, tmB);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                             cudaStream_t s) {
+  return launch_main<false>(p, tmA, tmB, grid, s);
+}
+
+cudaError_t launch_main_fp8(const MainParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+
+bool fp8_supported() { return false; }
+
+}  // namespace kgw

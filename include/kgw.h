@@ -1,0 +1,137 @@
+/*
+ * kgw.h — K-grouped GEMM for Mixture-of-Experts weight gradients on sm_103a (GB300).
+ *
+ * Operation ("Grouped GEMM + WGrad (Unified)", section "Operation"): for expert e let
+ * begin = 0 when e == 0 and begin = offsets[e-1] otherwise, and end = offsets[e]; then
+ *
+ *     Wgrad[e] = A[:, begin:end] @ B[begin:end, :]
+ *
+ * with A = dY^T of shape [hidden, tokens_sum] and B = X of shape [tokens_sum, intermediate]
+ * ("05 · Grouped GEMM 与 Expert 计算", section 5.2: dW_i = dY_i^T X_i, the token axis is the
+ * ragged contraction axis, M and N are fixed). With accumulate != 0 the result is added to the
+ * existing output (the caller initialises it); with accumulate == 0 the output is overwritten
+ * and an empty expert produces zeros.
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer in kgw_wgrad_args except status_dev and the host-side struct itself is a
+ *    DEVICE pointer on the current CUDA device. The caller owns every buffer (inputs, offsets,
+ *    outputs, the per-expert pointer array, the workspace) and keeps it alive until the work
+ *    enqueued on `stream` completes. The library allocates nothing per call and never
+ *    synchronises the stream: offsets stay on the device and are validated there.
+ *  - Host-detected errors return immediately and enqueue nothing.
+ *  - Device-detected errors (malformed offsets, bad per-expert output pointers, a device wait
+ *    that gave up) are written to *status_dev when status_dev is non-null; when the offsets or
+ *    output pointers are malformed no output element is written.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *  - Two calls that share a workspace must be ordered on the GPU (same stream or events).
+ *  - Results are bitwise deterministic run to run for the same inputs and device.
+ */
+#ifndef KGW_H_
+#define KGW_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kgw_status {
+  KGW_OK = 0,
+  KGW_ERR_INVALID_ARG = 1,   /* null/negative/inconsistent argument (host-detected) */
+  KGW_ERR_UNSUPPORTED = 2,   /* layout, dtype or shape this build does not implement */
+  KGW_ERR_ALIGNMENT = 3,     /* an operand or output base address is not 16-byte aligned */
+  KGW_ERR_DEVICE = 4,        /* current device is not sm_103 (or no device) */
+  KGW_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+  KGW_ERR_OFFSETS = 6,       /* device-detected: offsets decrease, a count % 256 != 0, or
+                                offsets[E-1] != tokens_sum */
+  KGW_ERR_TIMEOUT = 7,       /* device-detected: a bounded wait inside the kernel gave up */
+  KGW_ERR_WORKSPACE = 8,     /* workspace null, misaligned or smaller than the minimum */
+  KGW_ERR_OUT_PTRS = 9       /* device-detected: an out_ptrs[e] is null or not 16-byte aligned */
+} kgw_status;
+
+/* Storage order of an operand ("Grouped GEMM + WGrad (Unified)", section "BF16 contract"). */
+typedef enum kgw_major {
+  KGW_K_MAJOR = 0,   /* token axis has unit stride: A stride (tokens_sum, 1)             */
+  KGW_MN_MAJOR = 1   /* hidden / intermediate axis has unit stride: B stride (intermediate, 1) */
+} kgw_major;
+
+/* How the token dimension is stored (section "BF16 contract", input_order). */
+typedef enum kgw_input_order {
+  KGW_TENSOR2D = 0,  /* one global 2-D tensor per operand */
+  KGW_RAGGED = 1     /* per-expert K-contiguous blocks concatenated in memory: expert e's block of
+                        A is [hidden, n_e] row-major starting at element begin_e*hidden; B's block
+                        is [n_e, intermediate] row-major starting at element begin_e*intermediate */
+} kgw_input_order;
+
+typedef enum kgw_out_dtype { KGW_OUT_F32 = 0, KGW_OUT_BF16 = 1 } kgw_out_dtype;
+
+typedef struct kgw_wgrad_args {
+  int32_t num_experts;      /* E >= 1 (<= 4096)                                              */
+  int32_t hidden;           /* M: multiple of 128                                            */
+  int32_t intermediate;     /* N: multiple of 256                                            */
+  int64_t tokens_sum;       /* total tokens; must equal offsets[E-1]; multiple of 256        */
+  const void* a;            /* A: bf16 (or e4m3) [hidden, tokens_sum], see a_major/input_order */
+  int32_t a_major;          /* KGW_K_MAJOR (the only order implemented for A)                */
+  const void* b;            /* B: bf16 (or e4m3) [tokens_sum, intermediate]                 */
+  int32_t b_major;          /* KGW_MN_MAJOR (the only order implemented for B)               */
+  const int32_t* offsets;   /* int32 [E]: non-decreasing cumulative token counts             */
+  int32_t input_order;      /* kgw_input_order                                               */
+  void* out;                /* dense output [E, hidden, intermediate] row-major, or NULL     */
+  const int64_t* out_ptrs;  /* int64 [E] device addresses of per-expert [hidden, intermediate]
+                               row-major outputs (discrete mode), or NULL; exactly one of out
+                               and out_ptrs is non-NULL (section "Output modes")              */
+  int32_t out_dtype;        /* kgw_out_dtype                                                 */
+  int32_t accumulate;       /* 0: overwrite (empty expert -> zeros); 1: out += result         */
+  int32_t* status_dev;      /* optional device int32 receiving device-detected kgw_status    */
+} kgw_wgrad_args;
+
+/*
+ * Workspace bytes needed by kgw_wgrad_bf16 (is_fp8 = 0) or kgw_wgrad_fp8_blockscaled
+ * (is_fp8 = 1) for these shapes. Depends only on num_experts, hidden, intermediate and
+ * tokens_sum (not on the offsets' values). Host-only; never touches the GPU.
+ * The workspace holds the per-call schedule and the FP32 partial tiles of split-K; a caller
+ * may pass less than this (down to the schedule alone) and the kernel then splits less.
+ */
+kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t* bytes);
+
+/*
+ * BF16 x BF16 -> FP32 accumulation -> FP32 or BF16 output
+ * ("Grouped GEMM + WGrad (Unified)", sections "Operation", "BF16 contract", "Output modes").
+ * a, b: bf16. There are no scale arguments: the BF16 path takes none.
+ * workspace: device buffer of workspace_bytes (256-byte aligned), owned by the caller.
+ * stream: cudaStream_t.
+ */
+kgw_status kgw_wgrad_bf16(const kgw_wgrad_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * FP8 block-scaled variant ("05 · Grouped GEMM 与 Expert 计算", section 3: per-block 1x128
+ * scaling along K, scales MN-major; "Grouped GEMM + WGrad (Unified)", section "Block-scaled
+ * contract"). a, b: float8 e4m3 (the "fn" encoding) in the same logical layouts as the BF16
+ * entry. sfa: float32 [tokens_sum/128, hidden], sfb: float32 [tokens_sum/128, intermediate]:
+ * sfa[kb][m] scales A[m, 128*kb : 128*kb+128] and sfb[kb][n] scales B[128*kb : 128*kb+128, n]
+ * (token blocks are global, also in ragged order). Every scale must be a power of two in
+ * [2^-127, 2^127]; the product is accumulated in FP32 with the scales applied per block.
+ */
+kgw_status kgw_wgrad_fp8_blockscaled(const kgw_wgrad_args* args, const float* sfa, const float* sfb,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* kgw_status_string(int32_t status);
+
+/* Library ABI version (major*100 + minor). */
+int32_t kgw_version(void);
+
+/*
+ * Testing hooks (process-wide, host side). key 1: device wait limit in nanoseconds
+ * (default 2e9); key 2: when >= 0, the TMA producer of CTA 0 skips the arrival of that
+ * k-iteration so that the bounded wait path is exercised (default -1). Returns the previous
+ * value, or -1 for an unknown key.
+ */
+int64_t kgw_debug_set(int32_t key, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KGW_H_ */

@@ -227,3 +227,31 @@ def tolerance(S: np.ndarray, ref: np.ndarray, out_dtype: str, c_init=None) -> np
     if out_dtype == "bf16":
         tol = tol + 2.0 ** -8 * np.abs(ref)
     return tol
+
+
+def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, e: int, m: int, n: int, *,
+                         input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None):
+    """R_e[m, n] and S_e[m, n] read straight from the stored operands (for sampled checks).
+
+    Only row m of A_e and column n of B_e are decoded, so this works at full problem size.
+    Addressing follows ``logical_a``/``logical_b``; FP8 scales follow
+    ``apply_block_scales_rows``/``apply_block_scales_cols``.
+    """
+    b, end = expert_ranges(offsets)[e]
+    cnt = end - b
+    if cnt == 0:
+        return 0.0, 0.0
+    dec = e4m3_to_f64 if fp8 else bf16_to_f64
+    flat_a = np.asarray(a_bits).reshape(-1)
+    if input_order == "tensor2d":
+        tokens_sum = expert_ranges(offsets)[-1][1]
+        arow = dec(flat_a[m * tokens_sum + b: m * tokens_sum + end])
+    else:
+        arow = dec(flat_a[b * hidden + m * cnt: b * hidden + (m + 1) * cnt])
+    flat_b = np.asarray(b_bits).reshape(-1)
+    bcol = dec(flat_b[b * intermediate + n: end * intermediate: intermediate])
+    if fp8:
+        ks = np.arange(b, end) // SCALE_BLOCK
+        arow = arow * np.asarray(sfa, dtype=np.float64)[ks, m]
+        bcol = bcol * np.asarray(sfb, dtype=np.float64)[ks, n]
+    return float(np.dot(arow, bcol)), float(np.dot(np.abs(arow), np.abs(bcol)))

@@ -486,3 +486,27 @@ def test_planted_ragged_bug_is_caught(monkeypatch):
     r_2d, _ = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, 8, 8)
     assert np.array_equal(r_ok, r_2d)
     assert not np.array_equal(r_bad, r_2d)
+
+
+@pytest.mark.parametrize("order", ["tensor2d", "ragged"])
+def test_element_from_storage_matches_full_oracle(order):
+    counts = [256, 0, 512, 768]
+    a, b, offsets = _case(51, counts, H=8, I=12)
+    H, I = 8, 12
+    a_store = a if order == "tensor2d" else W.pack_ragged_a(a, np.array(counts))
+    full, S = O.wgrad_from_storage(bf16_bits(a_store), bf16_bits(b), offsets, H, I, input_order=order)
+    for (e, m, n) in [(0, 0, 0), (2, 7, 11), (3, 3, 5), (1, 2, 2), (3, 7, 0)]:
+        v, s = O.element_from_storage(bf16_bits(a_store), bf16_bits(b), offsets, H, I, e, m, n, input_order=order)
+        assert abs(v - full[e, m, n]) <= 1e-12 * S[e, m, n] + 1e-300
+        assert abs(s - S[e, m, n]) <= 1e-12 * S[e, m, n] + 1e-300
+
+
+def test_element_from_storage_fp8():
+    qa, sfa, qb, sfb, offsets = _fp8_case(52, [256, 0, 512])
+    H, I = qa.shape[0], qb.shape[1]
+    full, S = O.wgrad_from_storage(e4m3_bits(qa), e4m3_bits(qb), offsets, H, I, fp8=True,
+                                   sfa=sfa.numpy(), sfb=sfb.numpy())
+    for (e, m, n) in [(0, 1, 2), (2, 15, 23), (1, 0, 0)]:
+        v, s = O.element_from_storage(e4m3_bits(qa), e4m3_bits(qb), offsets, H, I, e, m, n, fp8=True,
+                                      sfa=sfa.numpy(), sfb=sfb.numpy())
+        assert abs(v - full[e, m, n]) <= 1e-12 * S[e, m, n] + 1e-300

@@ -1,0 +1,174 @@
+"""Parity of the CUDA path with the CPU oracle, element by element, through the C ABI.
+
+Small cases span several 128x256 tiles, empty experts, split-K and both input orders and
+output modes; the oracle evaluates them in full. Tolerance (per element, from the operation's
+FP32 accumulation): |gpu - oracle| <= 2e-5*S + 1e-6 with S = |A_e| @ |B_e|, plus 2**-8*|ref|
+for BF16 output (one final rounding) and 2**-23*(|C|+|ref|) when accumulating into FP32.
+Empty experts must be exact (zeros, or the pre-filled output bit for bit).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from kgw_testlib import Outputs, assert_close_to_oracle, ensure_built, oracle_full, run_gpu, to_f64
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _check(w, status_expected=0):
+    kgw = ensure_built()
+    x_cpu = W.make_inputs(w, "cpu")
+    x = W.make_inputs(w, DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    outs = run_gpu(w, x, DEV, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == status_expected, kgw.kgw_status_string(int(status.item()))
+    assert outs.guards_intact(), "write outside the output buffers"
+    got = to_f64(outs.stacked())
+    ref, S = oracle_full(w, x_cpu)
+    c = None if x_cpu.c is None else to_f64(x_cpu.c)
+    assert_close_to_oracle(w, got, ref, S, c)
+    counts = np.asarray(w.counts)
+    for e in np.nonzero(counts == 0)[0]:
+        if w.accumulate:
+            assert torch.equal(outs.views[e].cpu(), x_cpu.c[e]), f"empty expert {e} changed"
+        else:
+            assert not outs.views[e].any(), f"empty expert {e} not zero"
+    return outs, got
+
+
+CASES = {
+    "tiny": W.tiny(),
+    "multi_tile_f32": W.custom(5, 384, 768, [256, 0, 1280, 512, 2304], seed=21),
+    "multi_tile_bf16": W.custom(5, 384, 768, [256, 0, 1280, 512, 2304], seed=22, out_dtype="bf16"),
+    "accumulate_f32": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=23, accumulate=True),
+    "accumulate_bf16": W.custom(4, 256, 512, [0, 512, 0, 256], seed=24, accumulate=True, out_dtype="bf16"),
+    "ragged_f32": W.custom(5, 384, 512, [768, 256, 0, 1536, 512], seed=25, input_order="ragged"),
+    "discrete_bf16": W.custom(4, 256, 768, [512, 0, 256, 1024], seed=26, out_dtype="bf16",
+                              output_mode="discrete"),
+    "ragged_discrete_accumulate": W.custom(3, 256, 512, [1024, 0, 768], seed=27, input_order="ragged",
+                                           output_mode="discrete", accumulate=True, out_dtype="bf16"),
+    "split_k": W.custom(2, 256, 512, [8192, 256], seed=28),
+    "split_k_bf16_accumulate": W.custom(3, 128, 256, [6144, 0, 12288], seed=29, accumulate=True,
+                                        out_dtype="bf16"),
+    "split_k_ragged_discrete": W.custom(3, 256, 256, [256, 10240, 512], seed=30, input_order="ragged",
+                                        output_mode="discrete", out_dtype="bf16"),
+    "all_empty_overwrite": W.custom(3, 128, 256, [0, 0, 0], seed=31),
+    "all_empty_accumulate": W.custom(3, 128, 256, [0, 0, 0], seed=32, accumulate=True),
+    "single_expert": W.custom(1, 256, 512, [4096], seed=33, b_std=0.02),
+    "many_experts": W.custom(256, 128, 256, np.random.default_rng(34).choice([0, 256, 512], 256), seed=34,
+                             out_dtype="bf16"),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_parity_small(name):
+    _check(CASES[name])
+
+
+def test_deterministic_bitwise():
+    w = CASES["split_k_bf16_accumulate"]
+    x = W.make_inputs(w, DEV)
+    o1 = run_gpu(w, x, DEV).stacked().clone()
+    o2 = run_gpu(w, x, DEV).stacked().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_dense_and_discrete_outputs_are_identical():
+    w1 = W.custom(4, 256, 512, [512, 0, 256, 1024], seed=40, out_dtype="bf16")
+    w2 = W.custom(4, 256, 512, [512, 0, 256, 1024], seed=40, out_dtype="bf16", output_mode="discrete")
+    x = W.make_inputs(w1, DEV)
+    a = run_gpu(w1, x, DEV).stacked()
+    b = run_gpu(w2, x, DEV).stacked()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_ragged_and_tensor2d_are_identical():
+    counts = [768, 0, 1536, 256]
+    w1 = W.custom(4, 256, 512, counts, seed=41)
+    w2 = W.custom(4, 256, 512, counts, seed=41, input_order="ragged")
+    x1 = W.make_inputs(w1, DEV)
+    x2 = W.make_inputs(w2, DEV)
+    assert torch.equal(x1.b, x2.b)
+    a = run_gpu(w1, x1, DEV).stacked()
+    b = run_gpu(w2, x2, DEV).stacked()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------------------------
+# Device-detected errors: nothing is written
+# ---------------------------------------------------------------------------------------------
+
+def _bad_offsets_run(offsets_list, tokens_sum):
+    kgw = ensure_built()
+    w = W.custom(3, 128, 256, [256, 512, 768], seed=50)
+    x = W.make_inputs(w, DEV)
+    x.offsets = torch.tensor(offsets_list, dtype=torch.int32, device=DEV)
+    outs = Outputs(w, DEV)
+    before = outs.buf.clone()
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    args = kgw.make_args(3, 128, 256, tokens_sum, x.a, x.b, x.offsets, out=outs.dense, status_dev=status)
+    ws = kgw.workspace_for(args, device=DEV)
+    kgw.kgw_wgrad_bf16(args, ws)
+    torch.cuda.synchronize()
+    return int(status.item()), torch.equal(before, outs.buf)
+
+
+@pytest.mark.parametrize("offsets", [[256, 128, 1536], [256, 700, 1536], [256, 768, 1280]])
+def test_malformed_offsets_are_rejected_on_device(offsets):
+    kgw = ensure_built()
+    st, untouched = _bad_offsets_run(offsets, 1536)
+    assert st == kgw.KGW_ERR_OFFSETS
+    assert untouched
+
+
+def test_bad_output_pointer_is_rejected_on_device():
+    kgw = ensure_built()
+    w = W.custom(3, 128, 256, [256, 512, 768], seed=51, output_mode="discrete")
+    x = W.make_inputs(w, DEV)
+    outs = Outputs(w, DEV)
+    ptrs = outs.ptrs.clone()
+    ptrs[1] = ptrs[1] + 8  # not 16-byte aligned
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    args = kgw.make_args(3, 128, 256, 1536, x.a, x.b, x.offsets, out_ptrs=ptrs, status_dev=status)
+    kgw.kgw_wgrad_bf16(args, kgw.workspace_for(args, device=DEV))
+    torch.cuda.synchronize()
+    assert int(status.item()) == kgw.KGW_ERR_OUT_PTRS
+    assert all(torch.all(v == 7.25) for v in outs.views)
+
+
+def test_host_rejects_unaligned_operand_on_gpu():
+    kgw = ensure_built()
+    w = W.tiny()
+    x = W.make_inputs(w, DEV)
+    outs = Outputs(w, DEV)
+    ws = kgw.workspace_for(kgw.make_args(4, 128, 256, 1536, x.a, x.b, x.offsets, out=outs.dense), device=DEV)
+    a_view = x.a.reshape(-1)[1:]  # 2-byte offset
+    args = kgw.make_args(4, 128, 256, 1536, a_view, x.b, x.offsets, out=outs.dense)
+    rc = kgw.kgw_wgrad_bf16(args, ws, check=False)
+    assert rc == kgw.KGW_ERR_ALIGNMENT
+
+
+def test_small_workspace_still_correct():
+    """Down to the schedule alone (no room for split-K partials) the result is unchanged."""
+    kgw = ensure_built()
+    w = CASES["split_k"]
+    x = W.make_inputs(w, DEV)
+    full = run_gpu(w, x, DEV).stacked().clone()
+    outs = Outputs(w, DEV)
+    args = kgw.make_args(w.num_experts, w.hidden, w.intermediate, w.tokens_sum, x.a, x.b, x.offsets,
+                         out=outs.dense)
+    ws = torch.empty(64 * 1024, dtype=torch.uint8, device=DEV)
+    kgw.kgw_wgrad_bf16(args, ws)
+    torch.cuda.synchronize()
+    x_cpu = W.make_inputs(w, "cpu")
+    ref, S = oracle_full(w, x_cpu)
+    assert_close_to_oracle(w, to_f64(outs.stacked()), ref, S)
+    assert_close_to_oracle(w, to_f64(full), ref, S)
+    assert not torch.equal(full, outs.stacked())  # split-K really changed the summation order
