@@ -216,6 +216,8 @@ def run_ours(args, w, rank, local, world):
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
 
+    if args.no_e2e:
+        return ms_per_step, per_launch_ms, None, 0, 0, clk
     # ---- end to end: pinned host inputs -> device, call, result -> host, every step ----
     host_in = [t.cpu().pin_memory() for t in (x.a, x.b, x.offsets) + ((x.sfa, x.sfb) if w.fp8 else ())]
     host_c = x.c.cpu().pin_memory() if w.accumulate else None
@@ -316,6 +318,7 @@ def main():
     ap.add_argument("--workload", default="balanced", choices=sorted(W.NAMED))
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -368,8 +371,8 @@ def main():
                          "algorithmic_bytes": algorithmic_bytes(w),
                          "peak_source": f"{peaks['source']} bf16 burst" + (" x2 (fp8 nominal ratio)" if w.fp8 else ""),
                          "kernel": "wgrad_kernel (+ plan_kernel, a few us, inside the same events)"},
-            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": None if e2e_ms is None else {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps,
             "clocks": clk}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
