@@ -13,6 +13,7 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_status_string(code) -> str
   kgw_version() -> int
   kgw_debug_set(key, value) -> int
+  kgw_wgrad_bf16_noalloc(args, stream=None)
 
 ``make_args`` builds the argument struct from torch tensors.
 """
@@ -35,6 +36,7 @@ KGW_ERR_OFFSETS = 6
 KGW_ERR_TIMEOUT = 7
 KGW_ERR_WORKSPACE = 8
 KGW_ERR_OUT_PTRS = 9
+KGW_ERR_SCRATCH_LIMIT = 10
 
 KGW_K_MAJOR = 0
 KGW_MN_MAJOR = 1
@@ -44,7 +46,7 @@ KGW_OUT_F32 = 0
 KGW_OUT_BF16 = 1
 
 EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
-            "kgw_status_string", "kgw_version", "kgw_debug_set")
+            "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc")
 
 
 class KgwArgs(ctypes.Structure):
@@ -95,6 +97,8 @@ def lib() -> ctypes.CDLL:
         L.kgw_status_string.restype = ctypes.c_char_p
         L.kgw_version.argtypes = []
         L.kgw_version.restype = ctypes.c_int32
+        L.kgw_wgrad_bf16_noalloc.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p]
+        L.kgw_wgrad_bf16_noalloc.restype = ctypes.c_int
         L.kgw_debug_set.argtypes = [ctypes.c_int32, ctypes.c_int64]
         L.kgw_debug_set.restype = ctypes.c_int64
         _lib = L
@@ -164,6 +168,19 @@ def kgw_wgrad_fp8_blockscaled(args: KgwArgs, sfa, sfb, workspace, workspace_byte
                                          _stream_handle(stream))
     if check and rc != KGW_OK:
         raise KgwError(rc, "kgw_wgrad_fp8_blockscaled")
+    return rc
+
+
+def kgw_wgrad_bf16_noalloc(args: KgwArgs, stream=None, check: bool = True) -> int:
+    """kgw_wgrad_bf16 using the library's static 2 MiB scratch instead of a workspace.
+
+    For callers that cannot allocate device memory when they call (see include/kgw.h). The
+    first call on a device performs a one-time set-up and should precede any stream capture;
+    calls that overlap on the GPU share the scratch and must be ordered.
+    """
+    rc = lib().kgw_wgrad_bf16_noalloc(ctypes.byref(args), _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_bf16_noalloc")
     return rc
 
 

@@ -227,6 +227,42 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
   return e == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Entry point without allocation: the scratch (schedule + split-K partials) lives in a
+// file-scope device array instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // 2 MiB per device that loads the library
+constexpr int32_t kNoAllocMaxExperts = 1024;
+
+// Host code may not pass this name to a kernel: on the host it is only a stand-in for the
+// device array. Its device address comes from cudaGetSymbolAddress (noalloc_scratch below).
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the static scratch on the current device (looked up once per device).
+kgw_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KGW_ERR_DEVICE;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return KGW_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return KGW_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return KGW_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -248,6 +284,20 @@ kgw_status kgw_wgrad_fp8_blockscaled(const kgw_wgrad_args* args, const float* sf
   return run(args, true, sfa, sfb, workspace, workspace_bytes, stream);
 }
 
+kgw_status kgw_wgrad_bf16_noalloc(const kgw_wgrad_args* args, void* stream) {
+  kgw_status st = validate(args, false);
+  if (st != KGW_OK) return st;
+  if (args->num_experts > kNoAllocMaxExperts) return KGW_ERR_SCRATCH_LIMIT;
+  DevInfo dev;
+  st = device_info(&dev);
+  if (st != KGW_OK) return st;
+  if (dev.major != 10 || dev.minor != 3) return KGW_ERR_DEVICE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != KGW_OK) return st;
+  return run(args, false, nullptr, nullptr, scratch, kNoAllocScratchBytes, stream);
+}
+
 const char* kgw_status_string(int32_t status) {
   switch (status) {
     case KGW_OK: return "KGW_OK";
@@ -260,6 +310,7 @@ const char* kgw_status_string(int32_t status) {
     case KGW_ERR_TIMEOUT: return "KGW_ERR_TIMEOUT";
     case KGW_ERR_WORKSPACE: return "KGW_ERR_WORKSPACE";
     case KGW_ERR_OUT_PTRS: return "KGW_ERR_OUT_PTRS";
+    case KGW_ERR_SCRATCH_LIMIT: return "KGW_ERR_SCRATCH_LIMIT";
     default: return "KGW_ERR_UNKNOWN";
   }
 }

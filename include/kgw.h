@@ -47,7 +47,8 @@ typedef enum kgw_status {
                                 offsets[E-1] != tokens_sum */
   KGW_ERR_TIMEOUT = 7,       /* device-detected: a bounded wait inside the kernel gave up */
   KGW_ERR_WORKSPACE = 8,     /* workspace null, misaligned or smaller than the minimum */
-  KGW_ERR_OUT_PTRS = 9       /* device-detected: an out_ptrs[e] is null or not 16-byte aligned */
+  KGW_ERR_OUT_PTRS = 9,      /* device-detected: an out_ptrs[e] is null or not 16-byte aligned */
+  KGW_ERR_SCRATCH_LIMIT = 10 /* kgw_wgrad_bf16_noalloc: the call exceeds its static scratch limits */
 } kgw_status;
 
 /* Storage order of an operand ("Grouped GEMM + WGrad (Unified)", section "BF16 contract"). */
@@ -115,6 +116,33 @@ kgw_status kgw_wgrad_bf16(const kgw_wgrad_args* args, void* workspace, size_t wo
  */
 kgw_status kgw_wgrad_fp8_blockscaled(const kgw_wgrad_args* args, const float* sfa, const float* sfb,
                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kgw_wgrad_bf16 without a workspace argument and without any device allocation.
+ *
+ * The paper has no counterpart to this entry point. It exists for callers that cannot allocate
+ * device memory at the point of the call: for example code running under a framework
+ * whose caching allocator owns all device memory, inference runtimes that forbid allocation
+ * after start-up, or a plug-in that receives only stream and tensor pointers. Such a caller
+ * still passes the inputs and outputs in `args`, exactly as for kgw_wgrad_bf16.
+ *
+ * Scratch: the per-call schedule and the split-K partial tiles live in one static device array
+ * of 2 MiB inside the library, which every GPU that loads the library keeps until the process
+ * exits. It holds the schedule for up to 1024 experts plus a few FP32 partial tiles; calls with
+ * more than 1024 experts return KGW_ERR_SCRATCH_LIMIT and enqueue nothing. With fewer partial
+ * tiles than kgw_wgrad_bf16 may use, long experts are split less; results stay within the same
+ * error bound (the summation order can differ from kgw_wgrad_bf16's).
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture. No call allocates (no cudaMalloc/cudaFree, no allocating library routine).
+ *
+ * Sharing: every call on a device uses the same array and it keeps the previous call's
+ * contents; the kernels re-initialise every counter they read, so nothing needs clearing by
+ * the caller. Calls that overlap on the GPU (different streams without ordering, or several
+ * host threads) race on the array and give wrong results: order them.
+ */
+kgw_status kgw_wgrad_bf16_noalloc(const kgw_wgrad_args* args, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* kgw_status_string(int32_t status);
