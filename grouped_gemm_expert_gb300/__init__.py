@@ -14,6 +14,7 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_version() -> int
   kgw_debug_set(key, value) -> int
   kgw_wgrad_bf16_noalloc(args, stream=None)
+  kgw_debug_check_ragged_maps(args, is_fp8, host_offsets, workspace) -> int
 
 ``make_args`` builds the argument struct from torch tensors.
 """
@@ -46,7 +47,8 @@ KGW_OUT_F32 = 0
 KGW_OUT_BF16 = 1
 
 EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
-            "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc")
+            "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc",
+            "kgw_debug_check_ragged_maps")
 
 
 class KgwArgs(ctypes.Structure):
@@ -99,6 +101,9 @@ def lib() -> ctypes.CDLL:
         L.kgw_version.restype = ctypes.c_int32
         L.kgw_wgrad_bf16_noalloc.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p]
         L.kgw_wgrad_bf16_noalloc.restype = ctypes.c_int
+        L.kgw_debug_check_ragged_maps.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_int32, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_debug_check_ragged_maps.restype = ctypes.c_int32
         L.kgw_debug_set.argtypes = [ctypes.c_int32, ctypes.c_int64]
         L.kgw_debug_set.restype = ctypes.c_int64
         _lib = L
@@ -182,6 +187,17 @@ def kgw_wgrad_bf16_noalloc(args: KgwArgs, stream=None, check: bool = True) -> in
     if check and rc != KGW_OK:
         raise KgwError(rc, "kgw_wgrad_bf16_noalloc")
     return rc
+
+
+def kgw_debug_check_ragged_maps(args: KgwArgs, is_fp8: bool, host_offsets, workspace,
+                                workspace_bytes: Optional[int] = None, host_dump=None) -> int:
+    """Testing hook: number of experts whose device-built A descriptor differs from the host encoding."""
+    import numpy as np
+    offs = np.ascontiguousarray(np.asarray(host_offsets, dtype=np.int32))
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    dump = None if host_dump is None else host_dump.ctypes.data
+    return int(lib().kgw_debug_check_ragged_maps(ctypes.byref(args), int(bool(is_fp8)), offs.ctypes.data,
+                                                 _ptr(workspace), nbytes, dump))
 
 
 # ---------------------------------------------------------------------------------------------

@@ -11,6 +11,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -133,8 +134,18 @@ kgw_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
   return r == CUDA_SUCCESS ? KGW_OK : KGW_ERR_CUDA;
 }
 
-kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws, size_t ws_bytes,
-               void* stream) {
+// Everything one call needs: validated arguments turned into kernel parameters.
+struct Prepared {
+  kgw::PlanParams pp;
+  kgw::MainParams mp;
+  CUtensorMap tmA;  // tensor2d: A itself; ragged: template of the per-expert descriptors (small class)
+  CUtensorMap tmA_large;  // ragged: template for expert blocks of at least TMAP_SIZE_CLASS_BYTES
+  CUtensorMap tmB;
+  int grid;
+};
+
+kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws,
+                   size_t ws_bytes, Prepared* P) {
   kgw_status st = validate(a, fp8);
   if (st != KGW_OK) return st;
   if (fp8 && !kgw::fp8_supported()) return KGW_ERR_UNSUPPORTED;
@@ -161,30 +172,36 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
   if (get_encoder() != KGW_OK) return KGW_ERR_CUDA;
 
   const int bk = bk_of(fp8);
-  CUtensorMap tmA, tmB;
-  std::memset(&tmA, 0, sizeof(tmA));
-  std::memset(&tmB, 0, sizeof(tmB));
+  const uint64_t esz = fp8 ? 1 : 2;
+  std::memset(&P->tmA, 0, sizeof(P->tmA));
+  std::memset(&P->tmA_large, 0, sizeof(P->tmA_large));
+  std::memset(&P->tmB, 0, sizeof(P->tmB));
   if (a->tokens_sum > 0) {
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const uint64_t esz = fp8 ? 1 : 2;
     const uint64_t Ts = static_cast<uint64_t>(a->tokens_sum);
     if (a->input_order == KGW_TENSOR2D) {
       // A [hidden, tokens]: inner = tokens; box = bk tokens x 128 rows
-      st = encode_2d(&tmA, dt, a->a, Ts, static_cast<uint64_t>(a->hidden), Ts * esz, bk, kgw::BM);
+      st = encode_2d(&P->tmA, dt, a->a, Ts, static_cast<uint64_t>(a->hidden), Ts * esz, bk, kgw::BM);
     } else {
-      // ragged A viewed as rows of 128 bytes; gathered four rows at a time (box one row high)
-      const uint64_t per_row = 128 / esz;
-      st = encode_2d(&tmA, dt, a->a, per_row, Ts * static_cast<uint64_t>(a->hidden) / per_row, 128, per_row, 1);
+      // template of one expert's block [hidden, n] (row stride n elements); the plan kernel
+      // sets the address, n and the stride per expert
+      const uint64_t H = static_cast<uint64_t>(a->hidden);
+      const uint64_t n_small = kgw::TOKEN_ALIGN;
+      uint64_t n_large = (kgw::TMAP_SIZE_CLASS_BYTES + H * esz - 1) / (H * esz);
+      n_large = (n_large + kgw::TOKEN_ALIGN - 1) / kgw::TOKEN_ALIGN * kgw::TOKEN_ALIGN;
+      if (n_large < n_small) n_large = n_small;
+      st = encode_2d(&P->tmA, dt, a->a, n_small, H, n_small * esz, bk, kgw::BM);
+      if (st == KGW_OK) st = encode_2d(&P->tmA_large, dt, a->a, n_large, H, n_large * esz, bk, kgw::BM);
     }
     if (st != KGW_OK) return st;
     // B [tokens, intermediate]: inner = intermediate; box = one 128-byte swizzle row x bk tokens
-    st = encode_2d(&tmB, dt, a->b, static_cast<uint64_t>(a->intermediate), Ts,
+    st = encode_2d(&P->tmB, dt, a->b, static_cast<uint64_t>(a->intermediate), Ts,
                    static_cast<uint64_t>(a->intermediate) * esz, 128 / esz, bk);
     if (st != KGW_OK) return st;
   }
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  kgw::PlanParams pp{};
+  kgw::PlanParams& pp = P->pp;
+  pp = kgw::PlanParams{};
   pp.E = a->num_experts;
   pp.H = a->hidden;
   pp.I = a->intermediate;
@@ -198,9 +215,12 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
   pp.status_dev = a->status_dev;
   pp.ws = static_cast<uint8_t*>(ws);
   pp.L = L;
-  if (kgw::launch_plan(pp, s) != cudaSuccess) return KGW_ERR_CUDA;
+  pp.ragged = a->input_order == KGW_RAGGED && a->tokens_sum > 0;
+  pp.a = static_cast<const uint8_t*>(a->a);
+  pp.esz = static_cast<int32_t>(esz);
 
-  kgw::MainParams mp{};
+  kgw::MainParams& mp = P->mp;
+  mp = kgw::MainParams{};
   mp.E = a->num_experts;
   mp.H = a->hidden;
   mp.I = a->intermediate;
@@ -222,8 +242,19 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
   mp.L = L;
   mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
   mp.test_drop_stage = static_cast<int32_t>(g_drop_stage.load());
-  cudaError_t e = fp8 ? kgw::launch_main_fp8(mp, tmA, tmB, dev.sm_count, s)
-                      : kgw::launch_main_bf16(mp, tmA, tmB, dev.sm_count, s);
+  P->grid = dev.sm_count;
+  return KGW_OK;
+}
+
+kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws, size_t ws_bytes,
+               void* stream) {
+  Prepared P;
+  kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P);
+  if (st != KGW_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (kgw::launch_plan(P.pp, P.tmA, P.tmA_large, s) != cudaSuccess) return KGW_ERR_CUDA;
+  cudaError_t e = fp8 ? kgw::launch_main_fp8(P.mp, P.tmA, P.tmB, P.grid, s)
+                      : kgw::launch_main_bf16(P.mp, P.tmA, P.tmB, P.grid, s);
   return e == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
 }
 
@@ -296,6 +327,50 @@ kgw_status kgw_wgrad_bf16_noalloc(const kgw_wgrad_args* args, void* stream) {
   st = noalloc_scratch(&scratch);
   if (st != KGW_OK) return st;
   return run(args, false, nullptr, nullptr, scratch, kNoAllocScratchBytes, stream);
+}
+
+int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, const int32_t* host_offsets,
+                                    void* workspace, size_t workspace_bytes, void* host_dump) {
+  if (!args || !host_offsets || args->input_order != KGW_RAGGED || args->tokens_sum <= 0) return -KGW_ERR_INVALID_ARG;
+  Prepared P;
+  kgw_status st = prepare(args, is_fp8 != 0, reinterpret_cast<const float*>(args->a),
+                          reinterpret_cast<const float*>(args->a), workspace, workspace_bytes, &P);
+  if (st != KGW_OK) return -static_cast<int32_t>(st);
+  if (kgw::launch_plan(P.pp, P.tmA, P.tmA_large, nullptr) != cudaSuccess) return -KGW_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -KGW_ERR_CUDA;
+  const int32_t E = args->num_experts;
+  const size_t bytes = size_t(E) * 128;
+  uint8_t* dev_maps = static_cast<uint8_t*>(std::malloc(bytes));
+  if (!dev_maps) return -KGW_ERR_INVALID_ARG;
+  if (cudaMemcpy(dev_maps, static_cast<uint8_t*>(workspace) + P.pp.L.tmaps, bytes, cudaMemcpyDeviceToHost) !=
+      cudaSuccess) {
+    std::free(dev_maps);
+    return -KGW_ERR_CUDA;
+  }
+  const bool fp8 = is_fp8 != 0;
+  const uint64_t esz = fp8 ? 1 : 2;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  int32_t mismatches = 0;
+  for (int32_t e = 0; e < E; ++e) {
+    const int64_t begin = e ? host_offsets[e - 1] : 0;
+    const int64_t n = host_offsets[e] - begin;
+    if (n <= 0) continue;
+    CUtensorMap ref;
+    std::memset(&ref, 0, sizeof(ref));
+    const uint8_t* base = static_cast<const uint8_t*>(args->a) + begin * args->hidden * esz;
+    if (encode_2d(&ref, dt, base, static_cast<uint64_t>(n), static_cast<uint64_t>(args->hidden), n * esz,
+                  bk_of(fp8), kgw::BM) != KGW_OK) {
+      std::free(dev_maps);
+      return -KGW_ERR_CUDA;
+    }
+    if (std::memcmp(&ref, dev_maps + size_t(e) * 128, 128) != 0) ++mismatches;
+    if (host_dump) {
+      std::memcpy(static_cast<uint8_t*>(host_dump) + size_t(e) * 256, dev_maps + size_t(e) * 128, 128);
+      std::memcpy(static_cast<uint8_t*>(host_dump) + size_t(e) * 256 + 128, &ref, 128);
+    }
+  }
+  std::free(dev_maps);
+  return mismatches;
 }
 
 const char* kgw_status_string(int32_t status) {

@@ -66,7 +66,9 @@ __device__ __forceinline__ Chunk my_chunk(int n) {
   return {lo, hi};
 }
 
-__global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanParams p) {
+__global__ void __launch_bounds__(PLAN_THREADS)
+    plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ CUtensorMap a_small,
+                const __grid_constant__ CUtensorMap a_large) {
   __shared__ int32_t s_kit[MAX_EXPERTS];    // k-iterations per expert
   __shared__ int32_t s_key[MAX_EXPERTS];    // k-iterations per item (ordering key)
   __shared__ int64_t s_warp[32];
@@ -115,6 +117,26 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_kernel(PlanParams p) {
       if (p.status_dev) *p.status_dev = code;
     }
     return;
+  }
+
+  // 1b. ragged A: one TMA descriptor per non-empty expert, copied from a host-encoded
+  //     template of the same size class and pointed at the expert's [H, n_e] block (row
+  //     stride n_e elements).
+  if (p.ragged) {
+    for (int e = tid; e < E; e += blockDim.x) {
+      const int64_t prev = e ? static_cast<int64_t>(p.offsets[e - 1]) : 0;
+      const int64_t n = static_cast<int64_t>(p.offsets[e]) - prev;
+      if (n <= 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(p.ws + p.L.tmaps + size_t(e) * 128);
+      const bool large = uint64_t(n) * uint64_t(p.H) * uint64_t(p.esz) >= TMAP_SIZE_CLASS_BYTES;
+      const uint4* src = reinterpret_cast<const uint4*>(large ? &a_large : &a_small);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[j] = src[j];
+      tmap_set_address(dst, reinterpret_cast<uint64_t>(p.a + prev * p.H * p.esz));
+      tmap_set_dim0(dst, static_cast<uint32_t>(n));
+      tmap_set_stride1(dst, static_cast<uint64_t>(n * p.esz));
+      fence_tmap_release();
+    }
   }
 
   // 2. total k-iterations W = T * sum(kiters)
@@ -408,6 +430,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int nxt = 0;
       if (lane == 0) nxt = atomicAdd(item_counter, 1);
       const Item it = decode_item(p, cur, bk);
+      const CUtensorMap* amap = &tmA;
+      if (p.ragged) {
+        amap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps + size_t(it.e) * 128);
+        if (lane == 0 && it.kend > it.kbeg) fence_tmap_acquire(amap);
+      }
       for (int kb = it.kbeg; kb < it.kend; ++kb) {
         bool ok2 = true;
         const bool drop = (p.test_drop_stage >= 0 && blockIdx.x == 0 && issued == p.test_drop_stage);
@@ -421,19 +448,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t* sB = sA + STAGE_A_BYTES;
         const int64_t tok = it.begin + int64_t(kb) * bk;
         if (!drop) {
-          if (!p.ragged) {
-            if (lane == 0) tma_load_2d(sA, &tmA, &ctl->full[stage], static_cast<int32_t>(tok), it.m0);
-          } else {
-            // Ragged A: expert e's block is [H, n_e] row-major at element begin*H. View the buffer
-            // as rows of 128 bytes; tile row r, K-slice kb lives in view row
-            // (begin*H + (m0+r)*n_e + kb*bk) * elem / 128. Lane q fetches tile rows 4q..4q+3.
-            const int64_t elems_per_row = kFp8 ? 128 : 64;
-            const int64_t base_el = it.begin * p.H + int64_t(kb) * bk;
-            int32_t y[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              y[j] = static_cast<int32_t>((base_el + int64_t(it.m0 + 4 * lane + j) * it.n_e) / elems_per_row);
-            tma_gather4(sA + 4 * lane * 128, &tmA, &ctl->full[stage], 0, y[0], y[1], y[2], y[3]);
+          if (lane == 0) {
+            if (!p.ragged) {
+              tma_load_2d(sA, &tmA, &ctl->full[stage], static_cast<int32_t>(tok), it.m0);
+            } else {
+              // ragged A: expert e's own descriptor, coordinates relative to its block
+              tma_load_2d(sA, amap, &ctl->full[stage], kb * bk, it.m0);
+            }
           }
           if (lane == 0) {
 #pragma unroll
@@ -638,8 +659,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // Launchers
 // =============================================================================================
 
-cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  plan_kernel<<<1, PLAN_THREADS, 0, s>>>(p);
+cudaError_t launch_plan(const PlanParams& p, const CUtensorMap& a_small, const CUtensorMap& a_large,
+                        cudaStream_t s) {
+  plan_kernel<<<1, PLAN_THREADS, 0, s>>>(p, a_small, a_large);
   return cudaGetLastError();
 }
 

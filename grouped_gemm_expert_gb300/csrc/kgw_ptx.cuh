@@ -92,6 +92,29 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// In-place edits of a tensor map held in global memory (generic-proxy writes), and the proxy
+// fences that make the edited map visible to the TMA unit: the writer releases, the thread
+// that issues TMA with the map acquires it first.
+__device__ __forceinline__ void tmap_set_address(void* gmap, uint64_t addr) {
+  asm volatile("tensormap.replace.tile.global_address.global.b1024.b64 [%0], %1;" ::"l"(gmap), "l"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void tmap_set_dim0(void* gmap, uint32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 0, %1;" ::"l"(gmap), "r"(extent)
+               : "memory");
+}
+// Byte stride of dimension 1 (the first strided dimension).
+__device__ __forceinline__ void tmap_set_stride1(void* gmap, uint64_t bytes) {
+  asm volatile("tensormap.replace.tile.global_stride.global.b1024.b64 [%0], 0, %1;" ::"l"(gmap), "l"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void fence_tmap_release() {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void fence_tmap_acquire(const void* gmap) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(gmap) : "memory");
+}
+
 // ------------------------------------------------------------------------------------------
 // tcgen05
 // ------------------------------------------------------------------------------------------

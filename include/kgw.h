@@ -158,6 +158,18 @@ int32_t kgw_version(void);
  */
 int64_t kgw_debug_set(int32_t key, int64_t value);
 
+/*
+ * Testing hook for the ragged input order: runs only the schedule kernel of a call (which builds
+ * one TMA descriptor per non-empty expert of A on the device, from the expert's offset and token
+ * count), then compares each descriptor byte for byte with one encoded on the host for the same
+ * block (host_offsets: a host copy of args->offsets). Synchronises the device. Returns the number
+ * of experts whose descriptors differ (0 = all identical) or -kgw_status on error. host_dump,
+ * if non-NULL, receives E x 256 bytes: per expert the device-built then the host-encoded
+ * descriptor. Allocates host memory only.
+ */
+int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, const int32_t* host_offsets,
+                                    void* workspace, size_t workspace_bytes, void* host_dump);
+
 #ifdef __cplusplus
 }
 #endif
