@@ -386,6 +386,7 @@ const char* kgw_status_string(int32_t status) {
     case KGW_ERR_WORKSPACE: return "KGW_ERR_WORKSPACE";
     case KGW_ERR_OUT_PTRS: return "KGW_ERR_OUT_PTRS";
     case KGW_ERR_SCRATCH_LIMIT: return "KGW_ERR_SCRATCH_LIMIT";
+    case KGW_ERR_SCALES: return "KGW_ERR_SCALES";
     default: return "KGW_ERR_UNKNOWN";
   }
 }

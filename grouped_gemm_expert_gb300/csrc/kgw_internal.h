@@ -38,10 +38,11 @@ constexpr uint64_t TMAP_SIZE_CLASS_BYTES = uint64_t(128) << 10;
 constexpr uint32_t STAGE_A_BYTES = BM * 128;          // 16 KiB, both dtypes
 constexpr uint32_t STAGE_B_BYTES = BN * 128;          // 32 KiB, both dtypes
 constexpr uint32_t STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
-// FP8 scale factors per stage: 128 rows (A) and 256 columns (B) x one UE8M0 byte replicated
-// to 4 bytes, staged as 16-byte rows for the TMEM copy.
-constexpr uint32_t SF_A_BYTES = BM * 16;
-constexpr uint32_t SF_B_BYTES = BN * 16;
+// FP8: one FP32 accumulator (TMEM columns 0..255) and, per pipeline stage, the UE8M0 scale
+// factors of A (4 columns) and B (8 columns) in TMEM columns from SF_COL0 on.
+constexpr uint32_t SF_COL0 = BN;
+constexpr uint32_t SF_A_COLS = 4;
+constexpr uint32_t SF_STAGE_COLS = 12;
 
 struct PlanHeader {
   int32_t error;          // kgw_status found by the plan kernel (0 = OK)

@@ -287,15 +287,29 @@ struct SmemCtl {
   uint64_t wfull[WORK_RING];
   uint64_t wempty[WORK_RING];
   uint64_t mma_done;
+  uint64_t sf_full[STAGES];     // FP8: scale factors of a stage are in TMEM
   int32_t work_item[WORK_RING];
   uint32_t tmem_base;
   int32_t abort_flag;
 };
 
-size_t main_smem_bytes(bool fp8) {
-  size_t b = size_t(STAGES) * STAGE_BYTES;
-  if (fp8) b += size_t(STAGES) * (SF_A_BYTES + SF_B_BYTES);
-  return b + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
+size_t main_smem_bytes(bool) {
+  return size_t(STAGES) * STAGE_BYTES + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
+}
+
+// UE8M0 scale-factor byte of a power-of-two FP32 scale, replicated to the 4 bytes of a TMEM
+// column (one byte per 32-token block of the 128-token scale block). Flags non-powers of two.
+__device__ __forceinline__ uint32_t ue8m0_x4(float s, bool& bad) {
+  const uint32_t b = __float_as_uint(s);
+  uint32_t e = (b >> 23) & 0xFFu;
+  const uint32_t m = b & 0x7FFFFFu;
+  if ((b >> 31) != 0u || e == 255u) bad = true;
+  if (e == 0u) {
+    if (m != 0x400000u) bad = true;  // only 2^-127 is representable below the normal range
+  } else if (m != 0u) {
+    bad = true;
+  }
+  return e * 0x01010101u;
 }
 
 // Wait without the abort short-cut (used only while draining at the end).
@@ -391,6 +405,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&ctl->wempty[w], 1 + NUM_EPI_WARPS);
     }
     mbar_init(&ctl->mma_done, 1);
+    for (int st = 0; st < STAGES; ++st) mbar_init(&ctl->sf_full[st], NUM_EPI_WARPS * 32);
     ctl->abort_flag = 0;
     fence_mbarrier_init();
     if (p.tokens_sum > 0) {
@@ -498,7 +513,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       int tcount = 0;
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, 1);
+      const uint32_t idesc = kFp8 ? idesc_mxf8(BM, BN, 1, 0) : idesc_bf16_f32(BM, BN, 1);
       for (int n = 0;; ++n) {
         const int slot = n % WORK_RING;
         if (!wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns)) break;
@@ -507,8 +522,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (cur < 0) break;
         const Item it = decode_item(p, cur, bk);
         if (it.kend == it.kbeg) continue;
-        const int acc = tcount & 1;
-        const uint32_t use = static_cast<uint32_t>(tcount >> 1);
+        // BF16: two accumulators alternate; FP8: one accumulator (TMEM also holds scale factors)
+        const int acc = kFp8 ? 0 : (tcount & 1);
+        const uint32_t use = kFp8 ? static_cast<uint32_t>(tcount) : static_cast<uint32_t>(tcount >> 1);
         if (!wait_bounded(&ctl->tempty[acc], (use & 1) ^ 1, abort_flag, p.timeout_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -518,17 +534,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
+          if constexpr (kFp8) {
+            if (!wait_bounded(&ctl->sf_full[stage], phase, abort_flag, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * STAGE_BYTES);
           const uint32_t b_addr = a_addr + STAGE_A_BYTES;
+          if constexpr (kFp8) {
+            const uint32_t sfa = tmem_base + SF_COL0 + stage * SF_STAGE_COLS;
+            const uint32_t sfb = sfa + SF_A_COLS;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // A: K-major, 128-byte rows, 8-row groups 1024 B apart; K step of 16 = 32 bytes.
-            const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
-            // B: MN-major, 64-column (128 B) atoms 8 KiB apart along N, 8-row K groups 1024 B
-            // apart; K step of 16 rows = 2048 bytes.
-            const uint64_t bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
-            mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > it.kbeg || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              // A: K-major 128-byte rows; K step of 32 e4m3 = 32 bytes.
+              const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
+              // B: MN-major, 128-column (128 B) atoms 16 KiB apart along N, 8-row K groups
+              // 1024 B apart; K step of 32 rows = 4096 bytes.
+              const uint64_t bdesc = sdesc_sw128(b_addr + k * 4096, 128 * 128, 1024);
+              mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa, sfb, (kb > it.kbeg || k > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              // A: K-major, 128-byte rows, 8-row groups 1024 B apart; K step of 16 = 32 bytes.
+              const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
+              // B: MN-major, 64-column (128 B) atoms 8 KiB apart along N, 8-row K groups 1024 B
+              // apart; K step of 16 rows = 2048 bytes.
+              const uint64_t bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
+              mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > it.kbeg || k > 0) ? 1u : 0u);
+            }
           }
           mma_commit(&ctl->empty[stage]);
           if (++stage == STAGES) {
@@ -554,6 +590,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int32_t* counter_base = reinterpret_cast<const int32_t*>(p.ws + p.L.counter_base);
     float* partials = reinterpret_cast<float*>(p.ws + p.L.partials);
     int tcount = 0;
+    int sf_stage = 0;          // FP8 scale-factor ring position (same sequence as the TMA ring)
+    uint32_t sf_phase = 0;
     for (int n = 0;; ++n) {
       const int slot = n % WORK_RING;
       const bool okw = wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
@@ -577,8 +615,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;
       }
-      const int acc = tcount & 1;
-      const uint32_t use = static_cast<uint32_t>(tcount >> 1);
+      if constexpr (kFp8) {
+        // Scale factors of this item's k-iterations go into the TMEM stage ring (UE8M0 per
+        // row of A / column of B, one 128-token block per k-iteration).
+        bool okf = true;
+        for (int kb = it.kbeg; kb < it.kend; ++kb) {
+          const bool oke = wait_bounded(&ctl->empty[sf_stage], sf_phase ^ 1, abort_flag, p.timeout_ns);
+          if (!__all_sync(0xffffffffu, oke)) {
+            okf = false;
+            break;
+          }
+          tc_fence_after();
+          const int64_t kblk = (it.begin + int64_t(kb) * bk) / SCALE_BLOCK;
+          const float* sa = p.sfa + kblk * p.H + it.m0;
+          const float* sb = p.sfb + kblk * p.I + it.n0;
+          bool bad = false;
+          uint32_t va[4], vb[8];
+          // TMEM scale-factor layout read by the block-scaled MMA: 32 lanes (repeated in every
+          // lane quadrant) x columns, column c holding rows (A) / columns (B) 32c + lane.
+#pragma unroll
+          for (int c = 0; c < 4; ++c) va[c] = ue8m0_x4(__ldg(sa + 32 * c + lane), bad);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) vb[c] = ue8m0_x4(__ldg(sb + 32 * c + lane), bad);
+          if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
+          const uint32_t tsf = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + SF_COL0 + sf_stage * SF_STAGE_COLS;
+          tmem_st_32x32b_x4(tsf, va);
+          tmem_st_32x32b_x8(tsf + SF_A_COLS, vb);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&ctl->sf_full[sf_stage]);
+          if (++sf_stage == STAGES) {
+            sf_stage = 0;
+            sf_phase ^= 1;
+          }
+        }
+        if (!okf) break;
+      }
+      const int acc = kFp8 ? 0 : (tcount & 1);
+      const uint32_t use = kFp8 ? static_cast<uint32_t>(tcount) : static_cast<uint32_t>(tcount >> 1);
       const bool okt = wait_bounded(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
       if (!__all_sync(0xffffffffu, okt)) break;
       tc_fence_after();
@@ -682,10 +756,11 @@ cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const 
   return launch_main<false>(p, tmA, tmB, grid, s);
 }
 
-cudaError_t launch_main_fp8(const MainParams&, const CUtensorMap&, const CUtensorMap&, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                            cudaStream_t s) {
+  return launch_main<true>(p, tmA, tmB, grid, s);
 }
 
-bool fp8_supported() { return false; }
+bool fp8_supported() { return true; }
 
 }  // namespace kgw

@@ -48,7 +48,9 @@ typedef enum kgw_status {
   KGW_ERR_TIMEOUT = 7,       /* device-detected: a bounded wait inside the kernel gave up */
   KGW_ERR_WORKSPACE = 8,     /* workspace null, misaligned or smaller than the minimum */
   KGW_ERR_OUT_PTRS = 9,      /* device-detected: an out_ptrs[e] is null or not 16-byte aligned */
-  KGW_ERR_SCRATCH_LIMIT = 10 /* kgw_wgrad_bf16_noalloc: the call exceeds its static scratch limits */
+  KGW_ERR_SCRATCH_LIMIT = 10, /* kgw_wgrad_bf16_noalloc: the call exceeds its static scratch limits */
+  KGW_ERR_SCALES = 11        /* device-detected: an FP8 scale is not a positive power of two in
+                                [2^-127, 2^127] (the output of that call is meaningless) */
 } kgw_status;
 
 /* Storage order of an operand ("Grouped GEMM + WGrad (Unified)", section "BF16 contract"). */

@@ -61,6 +61,11 @@ CASES = {
     "single_expert": W.custom(1, 256, 512, [4096], seed=33, b_std=0.02),
     "many_experts": W.custom(256, 128, 256, np.random.default_rng(34).choice([0, 256, 512], 256), seed=34,
                              out_dtype="bf16"),
+    "fp8_bf16_out": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=60, fp8=True, out_dtype="bf16"),
+    "fp8_f32_ragged": W.custom(3, 384, 768, [256, 1280, 0], seed=61, fp8=True, input_order="ragged"),
+    "fp8_split_k_accumulate": W.custom(3, 128, 256, [16384, 0, 256], seed=62, fp8=True, accumulate=True),
+    "fp8_discrete": W.custom(3, 256, 256, [1024, 512, 256], seed=63, fp8=True, out_dtype="bf16",
+                             output_mode="discrete"),
 }
 
 
