@@ -24,6 +24,7 @@ using kgw::WsLayout;
 
 std::atomic<int64_t> g_timeout_ns{2000000000LL};
 std::atomic<int64_t> g_drop_stage{-1};
+std::atomic<int64_t> g_single_cta{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -78,9 +79,15 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int bk_of(bool fp8) { return fp8 ? kgw::BK_FP8 : kgw::BK_BF16; }
 
+// Rows of a work tile: BF16 problems whose hidden size is a multiple of 256 run on CTA pairs.
+int32_t tile_rows(const kgw_wgrad_args* a, bool fp8) {
+  if (!fp8 && a->hidden % (2 * kgw::BM) == 0 && g_single_cta.load() == 0) return 2 * kgw::BM;
+  return kgw::BM;
+}
+
 // Upper bound of the FP32 partial tiles split-K can use for these shapes.
 int32_t slot_cap(const kgw_wgrad_args* a, bool fp8) {
-  const int64_t T = int64_t(a->hidden / kgw::BM) * (a->intermediate / kgw::BN);
+  const int64_t T = int64_t(a->hidden / tile_rows(a, fp8)) * (a->intermediate / kgw::BN);
   const int64_t kit = a->tokens_sum / bk_of(fp8);
   // an expert is split only when its k-iterations exceed the chunk (>= MIN_SPLIT_KITERS), and
   // then into fewer than 2*kiters/chunk pieces
@@ -154,16 +161,18 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return KGW_ERR_ALIGNMENT;
   }
   if (!ws || !aligned(ws, 256)) return KGW_ERR_WORKSPACE;
-  const WsLayout L0 = kgw::ws_layout(a->num_experts, 0);
+  const int32_t tile_m = tile_rows(a, fp8);
+  const int32_t halves = tile_m / kgw::BM;
+  const WsLayout L0 = kgw::ws_layout(a->num_experts, 0, halves);
   if (ws_bytes < L0.total) return KGW_ERR_WORKSPACE;
   int32_t max_slots = slot_cap(a, fp8);
   {
     const size_t room = ws_bytes - L0.total;
-    const size_t fit = room / (kgw::PARTIAL_TILE_BYTES + 4 * kgw::NUM_EPI_WARPS);
+    const size_t fit = room / (halves * (kgw::PARTIAL_TILE_BYTES + 4 * kgw::NUM_EPI_WARPS));
     if (size_t(max_slots) > fit) max_slots = static_cast<int32_t>(fit);
-    while (max_slots > 0 && kgw::ws_layout(a->num_experts, max_slots).total > ws_bytes) --max_slots;
+    while (max_slots > 0 && kgw::ws_layout(a->num_experts, max_slots, halves).total > ws_bytes) --max_slots;
   }
-  const WsLayout L = kgw::ws_layout(a->num_experts, max_slots);
+  const WsLayout L = kgw::ws_layout(a->num_experts, max_slots, halves);
 
   DevInfo dev;
   st = device_info(&dev);
@@ -210,8 +219,10 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   pp.out_ptrs = a->out_ptrs;
   pp.accumulate = a->accumulate;
   pp.bk = bk;
-  pp.grid = dev.sm_count;
+  const int grid = halves == 2 ? (dev.sm_count & ~1) : dev.sm_count;
+  pp.grid = grid / halves;  // tiles in flight at once
   pp.max_slots = max_slots;
+  pp.tile_m = tile_m;
   pp.status_dev = a->status_dev;
   pp.ws = static_cast<uint8_t*>(ws);
   pp.L = L;
@@ -233,7 +244,8 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   mp.ragged = a->input_order == KGW_RAGGED;
   mp.discrete = a->out_ptrs != nullptr;
   mp.fp8 = fp8;
-  mp.num_m_tiles = a->hidden / kgw::BM;
+  mp.num_m_tiles = a->hidden / tile_m;
+  mp.tile_m = tile_m;
   mp.num_n_tiles = a->intermediate / kgw::BN;
   mp.sfa = sfa;
   mp.sfb = sfb;
@@ -242,7 +254,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   mp.L = L;
   mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
   mp.test_drop_stage = static_cast<int32_t>(g_drop_stage.load());
-  P->grid = dev.sm_count;
+  P->grid = grid;
   return KGW_OK;
 }
 
@@ -302,7 +314,8 @@ kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t
   if (!bytes) return KGW_ERR_INVALID_ARG;
   kgw_status st = validate(args, is_fp8 != 0);
   if (st != KGW_OK) return st;
-  *bytes = kgw::ws_layout(args->num_experts, slot_cap(args, is_fp8 != 0)).total;
+  const int32_t halves = tile_rows(args, is_fp8 != 0) / kgw::BM;
+  *bytes = kgw::ws_layout(args->num_experts, slot_cap(args, is_fp8 != 0), halves).total;
   return KGW_OK;
 }
 
@@ -397,6 +410,7 @@ int64_t kgw_debug_set(int32_t key, int64_t value) {
   switch (key) {
     case 1: return g_timeout_ns.exchange(value > 0 ? value : 1);
     case 2: return g_drop_stage.exchange(value);
+    case 3: return g_single_cta.exchange(value);
     default: return -1;
   }
 }

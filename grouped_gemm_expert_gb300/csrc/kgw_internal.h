@@ -15,7 +15,9 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK_BF16 = 64;    // 64 bf16 = 128 bytes
 constexpr int BK_FP8 = 128;    // 128 e4m3 = 128 bytes = one scale block
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;          // single-CTA ring: 4 x 48 KiB
+constexpr int STAGES_PAIR = 6;     // CTA-pair ring: 6 x 32 KiB per CTA
+constexpr int MAX_STAGES = 6;
 constexpr int TOKEN_ALIGN = 256;
 constexpr int SCALE_BLOCK = 128;
 
@@ -67,7 +69,8 @@ struct WsLayout {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline WsLayout ws_layout(int32_t E, int32_t max_slots) {
+// halves = 2 when a work tile spans a CTA pair (256 rows): partial tiles and counters double.
+inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1) {
   WsLayout L{};
   size_t off = sizeof(PlanHeader);
   L.order = off;        off = align256(off + sizeof(int32_t) * E);
@@ -76,8 +79,8 @@ inline WsLayout ws_layout(int32_t E, int32_t max_slots) {
   L.slot_base = off;    off = align256(off + sizeof(int32_t) * E);
   L.counter_base = off; off = align256(off + sizeof(int32_t) * E);
   L.tmaps = off;        off = align256(off + size_t(128) * E);
-  L.counters = off;     off = align256(off + sizeof(int32_t) * NUM_EPI_WARPS * (max_slots > 0 ? max_slots : 1));
-  L.partials = off;     off = align256(off + PARTIAL_TILE_BYTES * size_t(max_slots));
+  L.counters = off;     off = align256(off + sizeof(int32_t) * NUM_EPI_WARPS * halves * (max_slots > 0 ? max_slots : 1));
+  L.partials = off;     off = align256(off + PARTIAL_TILE_BYTES * halves * size_t(max_slots));
   L.total = off;
   L.max_slots = max_slots;
   return L;
@@ -95,6 +98,7 @@ struct PlanParams {
   int32_t* status_dev;
   uint8_t* ws;
   WsLayout L;
+  int32_t tile_m;               // rows of a work tile: 128 (one CTA) or 256 (CTA pair)
   int32_t ragged;               // build per-expert descriptors of A from the template
   const uint8_t* a;             // A base (ragged: flat buffer of per-expert blocks)
   int32_t esz;                  // bytes per A element
@@ -108,6 +112,7 @@ struct MainParams {
   void* out;
   int32_t out_bf16, accumulate, ragged, discrete, fp8;
   int32_t num_m_tiles, num_n_tiles;
+  int32_t tile_m;               // 128 (one CTA per tile) or 256 (a CTA pair per tile)
   const float* sfa;             // FP8: [tokens_sum/128, H]
   const float* sfb;             // FP8: [tokens_sum/128, I]
   int32_t* status_dev;
@@ -123,7 +128,7 @@ cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const 
                              cudaStream_t s);
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s);
-size_t main_smem_bytes(bool fp8);
+size_t main_smem_bytes(bool pair);
 bool fp8_supported();
 
 }  // namespace kgw

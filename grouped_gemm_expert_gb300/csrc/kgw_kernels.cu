@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(PLAN_THREADS)
 
   const int E = p.E;
   const int tid = threadIdx.x;
-  const int T = (p.H / BM) * (p.I / BN);
+  const int T = (p.H / p.tile_m) * (p.I / BN);
+  const int halves = p.tile_m / BM;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
   int32_t* order = reinterpret_cast<int32_t*>(p.ws + p.L.order);
   int32_t* item_prefix = reinterpret_cast<int32_t*>(p.ws + p.L.item_prefix);
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
   }
 
   // 8. split-tile arrival counters start at zero every call
-  for (int64_t i = tid; i < cnt_total * NUM_EPI_WARPS; i += blockDim.x) counters[i] = 0;
+  for (int64_t i = tid; i < cnt_total * NUM_EPI_WARPS * halves; i += blockDim.x) counters[i] = 0;
 
   if (tid == 0) {
     hdr->error = 0;
@@ -269,7 +270,7 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
   it.tile = local - it.split * T;
   const int mt = it.tile / p.num_n_tiles;
   const int nt = it.tile - mt * p.num_n_tiles;
-  it.m0 = mt * BM;
+  it.m0 = mt * p.tile_m;
   it.n0 = nt * BN;
   it.begin = it.e ? static_cast<int64_t>(__ldg(p.offsets + it.e - 1)) : 0;
   it.n_e = static_cast<int64_t>(__ldg(p.offsets + it.e)) - it.begin;
@@ -280,21 +281,22 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
 }
 
 struct SmemCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t wfull[WORK_RING];
   uint64_t wempty[WORK_RING];
   uint64_t mma_done;
-  uint64_t sf_full[STAGES];     // FP8: scale factors of a stage are in TMEM
+  uint64_t sf_full[MAX_STAGES]; // FP8: scale factors of a stage are in TMEM
   int32_t work_item[WORK_RING];
   uint32_t tmem_base;
   int32_t abort_flag;
 };
 
-size_t main_smem_bytes(bool) {
-  return size_t(STAGES) * STAGE_BYTES + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
+size_t main_smem_bytes(bool pair) {
+  const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2) : size_t(STAGES) * STAGE_BYTES;
+  return ring + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
 }
 
 // UE8M0 scale-factor byte of a power-of-two FP32 scale, replicated to the 4 bytes of a TMEM
@@ -372,10 +374,22 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
   return reinterpret_cast<char*>(p.out) + ((static_cast<size_t>(it.e) * p.H + r) * p.I + it.n0) * esz;
 }
 
-template <bool kFp8>
+// One persistent kernel, two shapes:
+//  - kPair = false: one CTA owns a 128 x 256 output tile (BF16 or FP8).
+//  - kPair = true : a cluster of two CTAs owns a 256 x 256 tile (BF16). Each CTA loads its own
+//    128 rows of A and 128 columns of B; the even CTA issues tcgen05.mma.cta_group::2, which reads
+//    both CTAs' shared memory and writes each CTA's 128 rows into its own TMEM. Per SM this moves
+//    32 KiB per k-iteration into shared memory instead of 48 KiB.
+template <bool kFp8, bool kPair>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
+  static_assert(!(kFp8 && kPair), "the FP8 path runs on single CTAs");
+  constexpr int kStages = kPair ? STAGES_PAIR : STAGES;
+  constexpr uint32_t kStageB = kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
+  constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB;
+  constexpr uint32_t kExpectTx = kPair ? 2 * kStageBytes : kStageBytes;
+  constexpr int kHalves = kPair ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   const int bk = kFp8 ? BK_FP8 : BK_BF16;
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
@@ -385,27 +399,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_mem = base;
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(base + size_t(STAGES) * STAGE_BYTES);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(base + size_t(kStages) * kStageBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: leader (issues MMAs, claims work)
+  const bool leader = rank == 0;
   int32_t* item_counter = const_cast<int32_t*>(&hdr->item_counter);
   volatile int* abort_flag = &ctl->abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tfull[a], 1);
-      mbar_init(&ctl->tempty[a], NUM_EPI_WARPS * 32);
+      mbar_init(&ctl->tempty[a], NUM_EPI_WARPS * kHalves);
     }
     for (int w = 0; w < WORK_RING; ++w) {
       mbar_init(&ctl->wfull[w], 1);
-      mbar_init(&ctl->wempty[w], 1 + NUM_EPI_WARPS);
+      mbar_init(&ctl->wempty[w], kPair ? 2 * (1 + NUM_EPI_WARPS) : 1 + NUM_EPI_WARPS);
     }
     mbar_init(&ctl->mma_done, 1);
-    for (int st = 0; st < STAGES; ++st) mbar_init(&ctl->sf_full[st], NUM_EPI_WARPS * 32);
+    for (int st = 0; st < kStages; ++st) mbar_init(&ctl->sf_full[st], NUM_EPI_WARPS * 32);
     ctl->abort_flag = 0;
     fence_mbarrier_init();
     if (p.tokens_sum > 0) {
@@ -414,80 +430,117 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(&ctl->tmem_base, 512);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(&ctl->tmem_base, 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&ctl->tmem_base, 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) {
+    cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrival
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  // cluster addresses of the leader's barriers that the peer signals
+  const uint32_t leader_full0 = kPair ? mapa_shared(smem_u32(&ctl->full[0]), 0) : 0u;
+  const uint32_t leader_wempty0 = kPair ? mapa_shared(smem_u32(&ctl->wempty[0]), 0) : 0u;
+  const uint32_t leader_tempty0 = kPair ? mapa_shared(smem_u32(&ctl->tempty[0]), 0) : 0u;
+
+  // A consumer is done with work-ring slot `slot`.
+  auto release_slot = [&](int slot) {
+    if (kPair && !leader)
+      mbar_arrive_remote(leader_wempty0 + slot * 8);
+    else
+      mbar_arrive(&ctl->wempty[slot]);
+  };
 
   if (warp == 0) {
-    // ======================= TMA producer + scheduler =======================
+    // ======================= TMA producer (+ scheduler on the leader) =======================
     int stage = 0;
     uint32_t phase = 0;
     int issued = 0;
     int cur = 0;
-    if (lane == 0) cur = atomicAdd(item_counter, 1);
+    if (lane == 0 && leader) cur = atomicAdd(item_counter, 1);
     for (int n = 0;; ++n) {
       const int slot = n % WORK_RING;
       bool ok = true;
       if (lane == 0) {
-        ok = wait_bounded(&ctl->wempty[slot], ((n / WORK_RING) & 1) ^ 1, abort_flag, p.timeout_ns);
-        if (ok) {
-          ctl->work_item[slot] = cur < total_items ? cur : -1;
-          mbar_arrive(&ctl->wfull[slot]);
+        if (leader) {
+          ok = wait_bounded_t<kPair>(&ctl->wempty[slot], ((n / WORK_RING) & 1) ^ 1, abort_flag, p.timeout_ns);
+          if (ok) {
+            const int v = cur < total_items ? cur : -1;
+            ctl->work_item[slot] = v;
+            if constexpr (kPair) {
+              st_cluster_s32(mapa_shared(smem_u32(&ctl->work_item[slot]), 1), v);
+              mbar_arrive_remote(mapa_shared(smem_u32(&ctl->wfull[slot]), 1));
+            }
+            mbar_arrive(&ctl->wfull[slot]);
+          }
+        } else {
+          ok = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
+          if (ok) {
+            cur = ctl->work_item[slot];
+            if (cur < 0) cur = total_items;
+            release_slot(slot);
+          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       cur = __shfl_sync(0xffffffffu, cur, 0);
       if (!ok || cur >= total_items) break;
       int nxt = 0;
-      if (lane == 0) nxt = atomicAdd(item_counter, 1);
+      if (lane == 0 && leader) nxt = atomicAdd(item_counter, 1);
       const Item it = decode_item(p, cur, bk);
       const CUtensorMap* amap = &tmA;
       if (p.ragged) {
         amap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps + size_t(it.e) * 128);
         if (lane == 0 && it.kend > it.kbeg) fence_tmap_acquire(amap);
       }
+      const int a_row = it.m0 + static_cast<int>(rank) * BM;            // this CTA's A rows
+      const int b_col = it.n0 + static_cast<int>(rank) * (BN / kHalves);  // this CTA's B columns
       for (int kb = it.kbeg; kb < it.kend; ++kb) {
         bool ok2 = true;
         const bool drop = (p.test_drop_stage >= 0 && blockIdx.x == 0 && issued == p.test_drop_stage);
         if (lane == 0) {
-          ok2 = wait_bounded(&ctl->empty[stage], phase ^ 1, abort_flag, p.timeout_ns);
-          if (ok2 && !drop) mbar_arrive_expect_tx(&ctl->full[stage], STAGE_BYTES);
+          ok2 = wait_bounded_t<kPair>(&ctl->empty[stage], phase ^ 1, abort_flag, p.timeout_ns);
+          if (ok2 && !drop && leader) mbar_arrive_expect_tx(&ctl->full[stage], kExpectTx);
         }
         ok2 = __shfl_sync(0xffffffffu, ok2, 0);
         if (!ok2) break;
-        uint8_t* sA = stage_mem + size_t(stage) * STAGE_BYTES;
+        uint8_t* sA = stage_mem + size_t(stage) * kStageBytes;
         uint8_t* sB = sA + STAGE_A_BYTES;
         const int64_t tok = it.begin + int64_t(kb) * bk;
-        if (!drop) {
-          if (lane == 0) {
-            if (!p.ragged) {
-              tma_load_2d(sA, &tmA, &ctl->full[stage], static_cast<int32_t>(tok), it.m0);
-            } else {
-              // ragged A: expert e's own descriptor, coordinates relative to its block
-              tma_load_2d(sA, amap, &ctl->full[stage], kb * bk, it.m0);
-            }
-          }
-          if (lane == 0) {
+        if (!drop && lane == 0) {
+          const int32_t ax = p.ragged ? kb * bk : static_cast<int32_t>(tok);
+          if constexpr (kPair) {
+            const uint32_t fb = leader_full0 + stage * 8;
+            tma_load_2d_pair(sA, amap, fb, ax, a_row);
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) {
-              if constexpr (kFp8) {
-                // FP8 B tiles are 128 columns (128 bytes) wide
-                if (j < BN / 128)
-                  tma_load_2d(sB + j * (128 * 128), &tmB, &ctl->full[stage], it.n0 + 128 * j,
-                              static_cast<int32_t>(tok));
-              } else {
-                tma_load_2d(sB + j * (64 * 128), &tmB, &ctl->full[stage], it.n0 + 64 * j,
+            for (int j = 0; j < BN / kHalves / 64; ++j)
+              tma_load_2d_pair(sB + j * (64 * 128), &tmB, fb, b_col + 64 * j, static_cast<int32_t>(tok));
+          } else {
+            tma_load_2d(sA, amap, &ctl->full[stage], ax, a_row);
+            if constexpr (kFp8) {
+              // FP8 B boxes are 128 columns (128 bytes) wide
+#pragma unroll
+              for (int j = 0; j < BN / 128; ++j)
+                tma_load_2d(sB + j * (128 * 128), &tmB, &ctl->full[stage], b_col + 128 * j,
                             static_cast<int32_t>(tok));
-              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sB + j * (64 * 128), &tmB, &ctl->full[stage], b_col + 64 * j,
+                            static_cast<int32_t>(tok));
             }
           }
         }
         ++issued;
-        if (++stage == STAGES) {
+        if (++stage == kStages) {
           stage = 0;
           phase ^= 1;
         }
@@ -495,42 +548,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
       cur = nxt;
     }
-    // Drain: every stage issued in the last STAGES k-iterations must land before exit.
-    if (lane == 0) {
+    // Drain: the leader's last kStages stages must land before exit (the peer's copies complete
+    // on the leader's barriers, which the cluster barrier at the end waits for).
+    if (lane == 0 && leader) {
       int s = stage;
       uint32_t ph = phase;
-      for (int i = 0; i < STAGES && i < issued; ++i) {
+      for (int i = 0; i < kStages && i < issued; ++i) {
         if (--s < 0) {
-          s = STAGES - 1;
+          s = kStages - 1;
           ph ^= 1;
         }
-        wait_drain(&ctl->full[s], ph, p.timeout_ns);
+        int dummy = 0;
+        wait_bounded_t<kPair>(&ctl->full[s], ph, &dummy, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
+    // ======================= MMA issuer (leader only) =======================
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int tcount = 0;
-      const uint32_t idesc = kFp8 ? idesc_mxf8(BM, BN, 1, 0) : idesc_bf16_f32(BM, BN, 1);
+      const uint32_t idesc = kFp8 ? idesc_mxf8(BM, BN, 1, 0) : idesc_bf16_f32(BM * kHalves, BN, 1);
       for (int n = 0;; ++n) {
         const int slot = n % WORK_RING;
-        if (!wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns)) break;
+        if (!wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns)) break;
         const int cur = ctl->work_item[slot];
-        mbar_arrive(&ctl->wempty[slot]);
+        release_slot(slot);
         if (cur < 0) break;
         const Item it = decode_item(p, cur, bk);
         if (it.kend == it.kbeg) continue;
         // BF16: two accumulators alternate; FP8: one accumulator (TMEM also holds scale factors)
         const int acc = kFp8 ? 0 : (tcount & 1);
         const uint32_t use = kFp8 ? static_cast<uint32_t>(tcount) : static_cast<uint32_t>(tcount >> 1);
-        if (!wait_bounded(&ctl->tempty[acc], (use & 1) ^ 1, abort_flag, p.timeout_ns)) break;
+        if (!wait_bounded_t<kPair>(&ctl->tempty[acc], (use & 1) ^ 1, abort_flag, p.timeout_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = it.kbeg; kb < it.kend; ++kb) {
-          if (!wait_bounded(&ctl->full[stage], phase, abort_flag, p.timeout_ns)) {
+          if (!wait_bounded_t<kPair>(&ctl->full[stage], phase, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -541,7 +596,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * STAGE_BYTES);
+          const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * kStageBytes);
           const uint32_t b_addr = a_addr + STAGE_A_BYTES;
           if constexpr (kFp8) {
             const uint32_t sfa = tmem_base + SF_COL0 + stage * SF_STAGE_COLS;
@@ -561,30 +616,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               // A: K-major, 128-byte rows, 8-row groups 1024 B apart; K step of 16 = 32 bytes.
               const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
               // B: MN-major, 64-column (128 B) atoms 8 KiB apart along N, 8-row K groups 1024 B
-              // apart; K step of 16 rows = 2048 bytes.
+              // apart; K step of 16 rows = 2048 bytes. In a pair each CTA holds 128 columns.
               const uint64_t bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
-              mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > it.kbeg || k > 0) ? 1u : 0u);
+              if constexpr (kPair)
+                mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kbeg || k > 0) ? 1u : 0u);
+              else
+                mma_bf16(d_tmem, adesc, bdesc, idesc, (kb > it.kbeg || k > 0) ? 1u : 0u);
             }
           }
-          mma_commit(&ctl->empty[stage]);
-          if (++stage == STAGES) {
+          if constexpr (kPair)
+            mma_commit_pair(&ctl->empty[stage], 0x3);
+          else
+            mma_commit(&ctl->empty[stage]);
+          if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(&ctl->tfull[acc]);
+        if constexpr (kPair)
+          mma_commit_pair(&ctl->tfull[acc], 0x3);
+        else
+          mma_commit(&ctl->tfull[acc]);
         ++tcount;
       }
       // All MMAs issued by this thread complete before TMEM is released.
-      mma_commit(&ctl->mma_done);
-      wait_drain(&ctl->mma_done, 0, p.timeout_ns);
+      if constexpr (kPair)
+        mma_commit_pair(&ctl->mma_done, 0x1);
+      else
+        mma_commit(&ctl->mma_done);
+      int dummy = 0;
+      wait_bounded_t<kPair>(&ctl->mma_done, 0, &dummy, p.timeout_ns);
     }
     __syncwarp();
   } else {
     // ======================= Epilogue (warps 2..5) =======================
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int row = q * 32 + lane;          // tile row owned by this thread
+    const int row = q * 32 + lane;          // tile row owned by this thread (within this CTA's 128)
     int32_t* counters = reinterpret_cast<int32_t*>(p.ws + p.L.counters);
     const int32_t* slot_base = reinterpret_cast<const int32_t*>(p.ws + p.L.slot_base);
     const int32_t* counter_base = reinterpret_cast<const int32_t*>(p.ws + p.L.counter_base);
@@ -594,14 +662,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t sf_phase = 0;
     for (int n = 0;; ++n) {
       const int slot = n % WORK_RING;
-      const bool okw = wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
+      const bool okw = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
       if (!__all_sync(0xffffffffu, okw)) break;
       const int cur = ctl->work_item[slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->wempty[slot]);
+      if (lane == 0) release_slot(slot);
       if (cur < 0) break;
       const Item it = decode_item(p, cur, bk);
-      char* orow = out_row_ptr(p, it, row);
+      char* orow = out_row_ptr(p, it, static_cast<int>(rank) * BM + row);
       if (it.kend == it.kbeg) {
         // empty expert, overwrite mode: the output tile is zero
         if (p.out_bf16) {
@@ -644,7 +712,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&ctl->sf_full[sf_stage]);
-          if (++sf_stage == STAGES) {
+          if (++sf_stage == kStages) {
             sf_stage = 0;
             sf_phase ^= 1;
           }
@@ -653,10 +721,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const int acc = kFp8 ? 0 : (tcount & 1);
       const uint32_t use = kFp8 ? static_cast<uint32_t>(tcount) : static_cast<uint32_t>(tcount >> 1);
-      const bool okt = wait_bounded(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
+      const bool okt = wait_bounded_t<kPair>(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
       if (!__all_sync(0xffffffffu, okt)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      // This warp has read its 32 TMEM lanes: hand the accumulator back to the MMA issuer.
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (kPair && !leader)
+            mbar_arrive_remote(leader_tempty0 + acc * 8);
+          else
+            mbar_arrive(&ctl->tempty[acc]);
+        }
+      };
       if (it.nsplit == 1) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -665,14 +744,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
           store_chunk(p, orow, c, reinterpret_cast<const float*>(r));
         }
-        tc_fence_before();
-        mbar_arrive(&ctl->tempty[acc]);
+        release_acc();
       } else {
         // split-K: publish this chunk's FP32 partial rows. Each warp owns 32 rows and its own
-        // arrival counter per (tile, lane quadrant), so no cross-warp barrier is needed; the
-        // last arriving warp sums the partials of its rows in split order (deterministic).
+        // arrival counter per (tile, CTA half, lane quadrant), so no cross-warp barrier is
+        // needed; the last arriving warp sums the partials of its rows in split order.
         const int sb = __ldg(slot_base + it.e) + it.tile * it.nsplit;
-        float4* mine = reinterpret_cast<float4*>(partials + (size_t(sb + it.split) * BM + row) * BN);
+        auto prow = [&](int s) {
+          return partials + ((size_t(sb + s) * kHalves + rank) * BM + row) * BN;
+        };
+        float4* mine = reinterpret_cast<float4*>(prow(it.split));
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
@@ -683,13 +764,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __stcg(mine + c * 8 + j, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                                  __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
         }
-        tc_fence_before();
-        mbar_arrive(&ctl->tempty[acc]);
+        release_acc();
         __threadfence();
         __syncwarp();
         int last = 0;
         if (lane == 0) {
-          const int cidx = (__ldg(counter_base + it.e) + it.tile) * NUM_EPI_WARPS + q;
+          const int cidx = ((__ldg(counter_base + it.e) + it.tile) * kHalves + static_cast<int>(rank)) * NUM_EPI_WARPS + q;
           last = atomicAdd(counters + cidx, 1) == it.nsplit - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
@@ -701,7 +781,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0.f;
             for (int s = 0; s < it.nsplit; ++s) {
-              const float4* src = reinterpret_cast<const float4*>(partials + (size_t(sb + s) * BM + row) * BN) + c * 8;
+              const float4* src = reinterpret_cast<const float4*>(prow(s)) + c * 8;
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 const float4 x = __ldcg(src + j);
@@ -721,10 +801,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   // ======================= teardown =======================
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) {
+    cluster_sync_all();  // no CTA leaves while its peer's MMAs may still touch its memory
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, 512);
+    else
+      tmem_dealloc(tmem_base, 512);
   }
   if (threadIdx.x == 0 && ctl->abort_flag && p.status_dev) atomicExch(p.status_dev, KGW_ERR_TIMEOUT);
 }
@@ -739,26 +826,38 @@ cudaError_t launch_plan(const PlanParams& p, const CUtensorMap& a_small, const C
   return cudaGetLastError();
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kPair>
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
-  const size_t smem = main_smem_bytes(kFp8);
+  const size_t smem = main_smem_bytes(kPair);
   // set on every launch: the attribute is per device and the call is cheap
-  cudaError_t e = cudaFuncSetAttribute(wgrad_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(wgrad_kernel<kFp8, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  wgrad_kernel<kFp8><<<grid, NUM_THREADS, smem, s>>>(p, tmA, tmB);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, wgrad_kernel<kFp8, kPair>, p, tmA, tmB);
 }
 
 cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                              cudaStream_t s) {
-  return launch_main<false>(p, tmA, tmB, grid, s);
+  if (p.tile_m == 2 * BM) return launch_main<false, true>(p, tmA, tmB, grid, s);
+  return launch_main<false, false>(p, tmA, tmB, grid, s);
 }
 
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s) {
-  return launch_main<true>(p, tmA, tmB, grid, s);
+  return launch_main<true, false>(p, tmA, tmB, grid, s);
 }
 
 bool fp8_supported() { return true; }

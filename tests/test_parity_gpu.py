@@ -61,6 +61,12 @@ CASES = {
     "single_expert": W.custom(1, 256, 512, [4096], seed=33, b_std=0.02),
     "many_experts": W.custom(256, 128, 256, np.random.default_rng(34).choice([0, 256, 512], 256), seed=34,
                              out_dtype="bf16"),
+    # hidden a multiple of 256: BF16 tiles run on CTA pairs (256 x 256 per pair)
+    "pair_multi_tile": W.custom(4, 768, 512, [1280, 0, 256, 2048], seed=64),
+    "pair_bf16_accumulate_ragged": W.custom(3, 512, 768, [768, 256, 0], seed=65, accumulate=True,
+                                            out_dtype="bf16", input_order="ragged"),
+    "pair_split_k_discrete": W.custom(2, 512, 256, [16384, 256], seed=66, output_mode="discrete",
+                                      out_dtype="bf16"),
     "fp8_bf16_out": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=60, fp8=True, out_dtype="bf16"),
     "fp8_f32_ragged": W.custom(3, 384, 768, [256, 1280, 0], seed=61, fp8=True, input_order="ragged"),
     "fp8_split_k_accumulate": W.custom(3, 128, 256, [16384, 0, 256], seed=62, fp8=True, accumulate=True),
@@ -72,6 +78,21 @@ CASES = {
 @pytest.mark.parametrize("name", list(CASES))
 def test_parity_small(name):
     _check(CASES[name])
+
+
+def test_single_cta_and_pair_tiles_agree():
+    """The same BF16 problem on 128-row single-CTA tiles and 256-row CTA-pair tiles."""
+    kgw = ensure_built()
+    w = W.custom(3, 512, 512, [1024, 256, 768], seed=67, out_dtype="bf16")
+    x = W.make_inputs(w, DEV)
+    pair = run_gpu(w, x, DEV).stacked().clone()
+    prev = kgw.kgw_debug_set(3, 1)
+    try:
+        single = run_gpu(w, x, DEV).stacked().clone()
+    finally:
+        kgw.kgw_debug_set(3, prev)
+    torch.cuda.synchronize()
+    assert torch.equal(pair.view(torch.int16), single.view(torch.int16))
 
 
 def test_deterministic_bitwise():
