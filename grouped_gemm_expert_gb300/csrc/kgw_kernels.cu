@@ -294,9 +294,11 @@ struct SmemCtl {
   int32_t abort_flag;
 };
 
+constexpr uint32_t EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 32 FP32
+
 size_t main_smem_bytes(bool pair) {
   const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2) : size_t(STAGES) * STAGE_BYTES;
-  return ring + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
+  return ring + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
 }
 
 // UE8M0 scale-factor byte of a power-of-two FP32 scale, replicated to the 4 bytes of a TMEM
@@ -321,47 +323,55 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint6
 }
 
 // ---------------------------------------------------------------------------------------------
-// Epilogue helpers: thread owns one output row; c = 32-column chunk index within the tile.
+// Epilogue helpers. A warp owns 32 rows of the tile. Values come out of TMEM one row per thread;
+// they are staged through a per-warp 32 x 128-byte shared buffer (16-byte chunks XOR-swizzled by
+// row, so both the row-per-thread writes and the read-back are free of bank conflicts) and
+// written back four rows per instruction: 8 lanes cover 32 consecutive FP32 columns of one row.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void store_chunk(const MainParams& p, char* row_ptr, int c, const float* v) {
+
+// Previous contents of 4 consecutive outputs (accumulate mode) as raw bits (FP32: 4 words;
+// BF16: 2 words), loaded ahead of the arithmetic so several loads are in flight together.
+__device__ __forceinline__ uint4 load_old4(const MainParams& p, const char* src) {
+  if (!p.out_bf16) return *reinterpret_cast<const uint4*>(src);
+  const uint2 h = *reinterpret_cast<const uint2*>(src);
+  return make_uint4(h.x, h.y, 0u, 0u);
+}
+
+// Write 4 consecutive output values (FP32 accumulator values v) at dst: overwrite, or add the
+// previous contents (one FP32 add, then one rounding to the output type).
+__device__ __forceinline__ void emit4(const MainParams& p, char* dst, float4 v, const uint4& o) {
   if (!p.out_bf16) {
-    float4* dst = reinterpret_cast<float4*>(row_ptr) + c * 8;
     if (p.accumulate) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float4 o = dst[j];
-        o.x += v[4 * j + 0];
-        o.y += v[4 * j + 1];
-        o.z += v[4 * j + 2];
-        o.w += v[4 * j + 3];
-        dst[j] = o;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      v.x += __uint_as_float(o.x);
+      v.y += __uint_as_float(o.y);
+      v.z += __uint_as_float(o.z);
+      v.w += __uint_as_float(o.w);
     }
+    *reinterpret_cast<float4*>(dst) = v;
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(row_ptr) + c * 4;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float w[8];
-#pragma unroll
-      for (int t = 0; t < 8; ++t) w[t] = v[8 * j + t];
-      if (p.accumulate) {
-        const uint4 o = dst[j];
-        w[0] += bf16_lo(o.x); w[1] += bf16_hi(o.x);
-        w[2] += bf16_lo(o.y); w[3] += bf16_hi(o.y);
-        w[4] += bf16_lo(o.z); w[5] += bf16_hi(o.z);
-        w[6] += bf16_lo(o.w); w[7] += bf16_hi(o.w);
-      }
-      uint4 r;
-      r.x = pack_bf16x2(w[0], w[1]);
-      r.y = pack_bf16x2(w[2], w[3]);
-      r.z = pack_bf16x2(w[4], w[5]);
-      r.w = pack_bf16x2(w[6], w[7]);
-      dst[j] = r;
+    if (p.accumulate) {
+      v.x += bf16_lo(o.x);
+      v.y += bf16_hi(o.x);
+      v.z += bf16_lo(o.y);
+      v.w += bf16_hi(o.y);
     }
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
   }
+}
+
+// Stage this thread's 32 values (row `lane` of the warp's 32 rows) into the swizzled buffer.
+__device__ __forceinline__ void stage_row(uint4* stg, int lane, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    stg[lane * 8 + (c ^ (lane & 7))] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+}
+
+// Read back 4 columns of row (4j + lane/8), chunk lane%8, from the swizzled buffer.
+__device__ __forceinline__ float4 unstage(const uint4* stg, int j, int lane) {
+  const int r = 4 * j + (lane >> 3);
+  const int c = lane & 7;
+  const uint4 u = stg[r * 8 + (c ^ (r & 7))];
+  return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
 }
 
 __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it, int row) {
@@ -399,7 +409,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_mem = base;
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(base + size_t(kStages) * kStageBytes);
+  uint8_t* epi_stage_mem = base + size_t(kStages) * kStageBytes;
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_stage_mem + NUM_EPI_WARPS * EPI_STAGE_BYTES);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: leader (issues MMAs, claims work)
@@ -652,7 +663,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ======================= Epilogue (warps 2..5) =======================
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int row = q * 32 + lane;          // tile row owned by this thread (within this CTA's 128)
     int32_t* counters = reinterpret_cast<int32_t*>(p.ws + p.L.counters);
     const int32_t* slot_base = reinterpret_cast<const int32_t*>(p.ws + p.L.slot_base);
     const int32_t* counter_base = reinterpret_cast<const int32_t*>(p.ws + p.L.counter_base);
@@ -669,18 +679,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) release_slot(slot);
       if (cur < 0) break;
       const Item it = decode_item(p, cur, bk);
-      char* orow = out_row_ptr(p, it, static_cast<int>(rank) * BM + row);
+      // this warp's 32 output rows start at tile row rank*128 + q*32; row r is `ostride` bytes further
+      char* obase = out_row_ptr(p, it, static_cast<int>(rank) * BM + q * 32);
+      const size_t ostride = size_t(p.I) * (p.out_bf16 ? 2 : 4);
+      const int esz = p.out_bf16 ? 2 : 4;
       if (it.kend == it.kbeg) {
-        // empty expert, overwrite mode: the output tile is zero
-        if (p.out_bf16) {
-          uint4* d = reinterpret_cast<uint4*>(orow);
-#pragma unroll 4
-          for (int j = 0; j < BN * 2 / 16; ++j) d[j] = make_uint4(0, 0, 0, 0);
-        } else {
-          float4* d = reinterpret_cast<float4*>(orow);
-#pragma unroll 4
-          for (int j = 0; j < BN * 4 / 16; ++j) d[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        // empty expert, overwrite mode: the output tile is zero (4 rows x 512 bytes per instruction)
+        const int rb = BN * esz;  // bytes per row segment
+#pragma unroll 1
+        for (int r = 0; r < 32; ++r)
+          for (int off = lane * 16; off < rb; off += 32 * 16)
+            *reinterpret_cast<uint4*>(obase + r * ostride + off) = make_uint4(0, 0, 0, 0);
         continue;
       }
       if constexpr (kFp8) {
@@ -719,6 +728,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!okf) break;
       }
+      if (p.accumulate && it.split == it.nsplit - 1) {
+        // the previous output is read at the end of this item: start pulling this thread's row
+        // of it into L2 while the main loop runs (one bulk prefetch per row)
+        prefetch_l2_bulk(obase + lane * ostride, static_cast<uint32_t>(BN * esz));
+      }
       const int acc = kFp8 ? 0 : (tcount & 1);
       const uint32_t use = kFp8 ? static_cast<uint32_t>(tcount) : static_cast<uint32_t>(tcount >> 1);
       const bool okt = wait_bounded_t<kPair>(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
@@ -736,35 +750,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive(&ctl->tempty[acc]);
         }
       };
+      uint4* stg = reinterpret_cast<uint4*>(epi_stage_mem + (warp - EPI_WARP0) * EPI_STAGE_BYTES);
       if (it.nsplit == 1) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c * 32, r);
-          tmem_ld_wait();
-          store_chunk(p, orow, c, reinterpret_cast<const float*>(r));
+          char* cbase = obase + size_t(c * 32 + (lane & 7) * 4) * esz;
+          {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, r);
+            tmem_ld_wait();
+            if (c == BN / 32 - 1) release_acc();  // all TMEM reads of this warp are done
+            stage_row(stg, lane, r);
+          }
+          __syncwarp();
+          uint4 old[8];
+          if (p.accumulate) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) old[j] = load_old4(p, cbase + (4 * j + (lane >> 3)) * ostride);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) emit4(p, cbase + (4 * j + (lane >> 3)) * ostride, unstage(stg, j, lane), old[j]);
+          __syncwarp();
         }
-        release_acc();
       } else {
-        // split-K: publish this chunk's FP32 partial rows. Each warp owns 32 rows and its own
-        // arrival counter per (tile, CTA half, lane quadrant), so no cross-warp barrier is
-        // needed; the last arriving warp sums the partials of its rows in split order.
+        // split-K: publish this chunk's FP32 partial rows (row-major 128 x 256 per CTA half), then
+        // the last arriving warp for these 32 rows sums all partials in split order. Each warp has
+        // its own arrival counter per (tile, CTA half, lane quadrant): no cross-warp barrier.
         const int sb = __ldg(slot_base + it.e) + it.tile * it.nsplit;
-        auto prow = [&](int s) {
-          return partials + ((size_t(sb + s) * kHalves + rank) * BM + row) * BN;
+        auto prow = [&](int s, int rr) {
+          return partials + ((size_t(sb + s) * kHalves + rank) * BM + q * 32 + rr) * BN;
         };
-        float4* mine = reinterpret_cast<float4*>(prow(it.split));
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c * 32, r);
           tmem_ld_wait();
+          if (c == BN / 32 - 1) release_acc();
+          stage_row(stg, lane, r);
+          __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            __stcg(mine + c * 8 + j, make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+          for (int j = 0; j < 8; ++j) {
+            const int rr = 4 * j + (lane >> 3);
+            __stcg(reinterpret_cast<float4*>(prow(it.split, rr) + c * 32 + (lane & 7) * 4), unstage(stg, j, lane));
+          }
+          __syncwarp();
         }
-        release_acc();
         __threadfence();
         __syncwarp();
         int last = 0;
@@ -777,21 +807,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           __threadfence();
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
+            const int col = c * 32 + (lane & 7) * 4;
+            char* cbase = obase + size_t(col) * esz;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+              uint4 old[4];
+              if (p.accumulate) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            for (int s = 0; s < it.nsplit; ++s) {
-              const float4* src = reinterpret_cast<const float4*>(prow(s)) + c * 8;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 x = __ldcg(src + j);
-                v[4 * j] += x.x;
-                v[4 * j + 1] += x.y;
-                v[4 * j + 2] += x.z;
-                v[4 * j + 3] += x.w;
+                for (int j = 0; j < 4; ++j) old[j] = load_old4(p, cbase + (4 * (4 * h + j) + (lane >> 3)) * ostride);
               }
+              float4 v[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int s2 = 0; s2 < it.nsplit; ++s2) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float4 x = __ldcg(reinterpret_cast<const float4*>(prow(s2, 4 * (4 * h + j) + (lane >> 3)) + col));
+                  v[j].x += x.x;
+                  v[j].y += x.y;
+                  v[j].z += x.z;
+                  v[j].w += x.w;
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j) emit4(p, cbase + (4 * (4 * h + j) + (lane >> 3)) * ostride, v[j], old[j]);
             }
-            store_chunk(p, orow, c, v);
           }
         }
       }

@@ -151,6 +151,12 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Ask L2 to fetch [src, src+bytes) ahead of use (bytes a multiple of 16, src 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 // Four rows (y0..y3) of a 2-D tensor whose box is one row high, written to consecutive rows of dst.
 __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x,
                                             int32_t y0, int32_t y1, int32_t y2, int32_t y3) {
