@@ -283,21 +283,20 @@ def cpu_oracle_rate(w, budget_s: float):
     if w.fp8:
         A = O.apply_block_scales_rows(A, x.sfa.numpy())
         B = O.apply_block_scales_cols(B, x.sfb.numpy())
-    ranges = O.expert_ranges(w.offsets)
+    ranges = [(e, b, end) for e, (b, end) in enumerate(O.expert_ranges(w.offsets)) if end > b]
     flops = 0.0
-    done = []
+    n_experts = 0
     t0 = time.perf_counter()
-    for e, (b, end) in enumerate(ranges):
-        if end == b:
-            continue
-        sub_off = np.array([end - b], dtype=np.int64)
-        O.wgrad(A[:, b:end], B[b:end, :], sub_off, with_bound=False)
-        flops += 2.0 * w.hidden * w.intermediate * (end - b)
-        done.append(e)
-        if time.perf_counter() - t0 > budget_s:
-            break
+    # whole experts, in order, repeating the workload until the time budget is spent
+    while time.perf_counter() - t0 < budget_s:
+        for e, b, end in ranges:
+            O.wgrad(A[:, b:end], B[b:end, :], np.array([end - b], dtype=np.int64), with_bound=False)
+            flops += 2.0 * w.hidden * w.intermediate * (end - b)
+            n_experts += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
     dt = time.perf_counter() - t0
-    return flops / dt / 1e12, dt, done
+    return flops / dt / 1e12, dt, n_experts
 
 
 def blas_threads():
@@ -340,15 +339,16 @@ def main():
         for i in range(args.warmup + args.steps):
             r, dt, done = cpu_oracle_rate(w, budget)
             if i >= args.warmup:
-                rates.append((r, dt))
-        val = statistics.median(r for r, _ in rates)
-        ms = statistics.median(dt for _, dt in rates) * 1e3
+                rates.append((r, dt, done))
+        val = statistics.median(r for r, _, _ in rates)
+        ms = statistics.median(dt for _, dt, _ in rates) * 1e3
         line = {"impl": "reference", "metric": "K-grouped wgrad TFLOP/s (2*H*I*sum n_e)", "value": val,
                 "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                                 "sample": f"float64 oracle over whole experts, about {budget:.0f} s per step"},
+                                 "sample": f"float64 oracle over whole experts of the workload (repeating it), "
+                                           f"{ms / 1e3:.1f} s per step"},
                 "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -378,7 +378,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, dt, done = cpu_oracle_rate(w, args.cpu_budget)
         line["cpu_baseline"] = {"value": r, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"float64 oracle on experts {done} of the same workload ({dt:.1f} s)"}
+                                "sample": f"float64 oracle, {done} whole-expert products of the same workload "
+                                          f"(repeating it), {dt:.1f} s"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
