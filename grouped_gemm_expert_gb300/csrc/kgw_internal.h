@@ -43,6 +43,10 @@ constexpr uint32_t STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
 // FP8: one FP32 accumulator (TMEM columns 0..255) and, per pipeline stage, the UE8M0 scale
 // factors of A (4 columns) and B (8 columns) in TMEM columns from SF_COL0 on.
 constexpr uint32_t SF_COL0 = BN;
+// FP8 stages also carry the raw FP32 scales of their 128-token block: 128 of A and 256 of B,
+// brought in by bulk copies (padded so that every stage stays 1024-byte aligned).
+constexpr uint32_t SF_SMEM_BYTES = (BM + BN) * 4;
+constexpr uint32_t SF_SMEM_PAD = 2048;
 constexpr uint32_t SF_A_COLS = 4;
 constexpr uint32_t SF_STAGE_COLS = 12;
 
@@ -128,7 +132,7 @@ cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const 
                              cudaStream_t s);
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s);
-size_t main_smem_bytes(bool pair);
+size_t main_smem_bytes(bool pair, bool fp8);
 bool fp8_supported();
 
 }  // namespace kgw

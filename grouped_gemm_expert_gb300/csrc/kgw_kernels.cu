@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
   int32_t* counter_base = reinterpret_cast<int32_t*>(p.ws + p.L.counter_base);
   int32_t* counters = reinterpret_cast<int32_t*>(p.ws + p.L.counters);
 
+  pdl_launch_dependents();  // the main kernel may launch now; it waits for this grid to finish
   if (tid == 0) s_err = 0;
   __syncthreads();
 
@@ -296,8 +297,9 @@ struct SmemCtl {
 
 constexpr uint32_t EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 32 FP32
 
-size_t main_smem_bytes(bool pair) {
-  const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2) : size_t(STAGES) * STAGE_BYTES;
+size_t main_smem_bytes(bool pair, bool fp8) {
+  const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2)
+                           : size_t(STAGES) * (STAGE_BYTES + (fp8 ? SF_SMEM_PAD : 0u));
   return ring + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
 }
 
@@ -397,11 +399,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   static_assert(!(kFp8 && kPair), "the FP8 path runs on single CTAs");
   constexpr int kStages = kPair ? STAGES_PAIR : STAGES;
   constexpr uint32_t kStageB = kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
-  constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB;
-  constexpr uint32_t kExpectTx = kPair ? 2 * kStageBytes : kStageBytes;
+  constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB + (kFp8 ? SF_SMEM_PAD : 0u);
+  constexpr uint32_t kStageTx = STAGE_A_BYTES + kStageB + (kFp8 ? SF_SMEM_BYTES : 0u);
+  constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
   constexpr int kHalves = kPair ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
   const int bk = kFp8 ? BK_FP8 : BK_BF16;
+  pdl_wait();  // the plan of this call is complete and visible
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
   if (hdr->error != 0) return;  // offsets/pointers rejected by the plan: write nothing
   const int total_items = hdr->total_items;
@@ -542,6 +546,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int j = 0; j < BN / 128; ++j)
                 tma_load_2d(sB + j * (128 * 128), &tmB, &ctl->full[stage], b_col + 128 * j,
                             static_cast<int32_t>(tok));
+              // this 128-token block's FP32 scales: 128 rows of A, 256 columns of B
+              const int64_t kblk = tok / SCALE_BLOCK;
+              uint8_t* sS = sB + kStageB;
+              bulk_load(sS, p.sfa + kblk * p.H + it.m0, BM * 4, &ctl->full[stage]);
+              bulk_load(sS + BM * 4, p.sfb + kblk * p.I + it.n0, BN * 4, &ctl->full[stage]);
             } else {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
@@ -697,23 +706,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // row of A / column of B, one 128-token block per k-iteration).
         bool okf = true;
         for (int kb = it.kbeg; kb < it.kend; ++kb) {
-          const bool oke = wait_bounded(&ctl->empty[sf_stage], sf_phase ^ 1, abort_flag, p.timeout_ns);
+          // The stage's data (and its scales) have landed; this also means the MMAs that read
+          // this stage's TMEM scale factors in the previous round have completed.
+          const bool oke = wait_bounded(&ctl->full[sf_stage], sf_phase, abort_flag, p.timeout_ns);
           if (!__all_sync(0xffffffffu, oke)) {
             okf = false;
             break;
           }
           tc_fence_after();
-          const int64_t kblk = (it.begin + int64_t(kb) * bk) / SCALE_BLOCK;
-          const float* sa = p.sfa + kblk * p.H + it.m0;
-          const float* sb = p.sfb + kblk * p.I + it.n0;
+          const float* sa = reinterpret_cast<const float*>(stage_mem + size_t(sf_stage) * kStageBytes +
+                                                           STAGE_A_BYTES + kStageB);
+          const float* sb = sa + BM;
           bool bad = false;
           uint32_t va[4], vb[8];
           // TMEM scale-factor layout read by the block-scaled MMA: 32 lanes (repeated in every
           // lane quadrant) x columns, column c holding rows (A) / columns (B) 32c + lane.
 #pragma unroll
-          for (int c = 0; c < 4; ++c) va[c] = ue8m0_x4(__ldg(sa + 32 * c + lane), bad);
+          for (int c = 0; c < 4; ++c) va[c] = ue8m0_x4(sa[32 * c + lane], bad);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) vb[c] = ue8m0_x4(__ldg(sb + 32 * c + lane), bad);
+          for (int c = 0; c < 8; ++c) vb[c] = ue8m0_x4(sb[32 * c + lane], bad);
           if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
           const uint32_t tsf = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + SF_COL0 + sf_stage * SF_STAGE_COLS;
           tmem_st_32x32b_x4(tsf, va);
@@ -862,14 +873,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 cudaError_t launch_plan(const PlanParams& p, const CUtensorMap& a_small, const CUtensorMap& a_large,
                         cudaStream_t s) {
-  plan_kernel<<<1, PLAN_THREADS, 0, s>>>(p, a_small, a_large);
+  int threads = ((p.E + 31) / 32) * 32;
+  threads = threads < 128 ? 128 : (threads > PLAN_THREADS ? PLAN_THREADS : threads);
+  plan_kernel<<<1, threads, 0, s>>>(p, a_small, a_large);
   return cudaGetLastError();
 }
 
 template <bool kFp8, bool kPair>
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
-  const size_t smem = main_smem_bytes(kPair);
+  const size_t smem = main_smem_bytes(kPair, kFp8);
   // set on every launch: the attribute is per device and the call is cheap
   cudaError_t e = cudaFuncSetAttribute(wgrad_kernel<kFp8, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -879,13 +892,16 @@ static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, cons
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start launching while the plan kernel runs; griddepcontrol.wait orders the reads
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, wgrad_kernel<kFp8, kPair>, p, tmA, tmB);
 }
 
