@@ -72,6 +72,9 @@ CASES = {
     "fp8_split_k_accumulate": W.custom(3, 128, 256, [16384, 0, 256], seed=62, fp8=True, accumulate=True),
     "fp8_discrete": W.custom(3, 256, 256, [1024, 512, 256], seed=63, fp8=True, out_dtype="bf16",
                              output_mode="discrete"),
+    "fp8_pair_ragged_split_k": W.custom(3, 512, 512, [16384, 0, 768], seed=68, fp8=True, input_order="ragged",
+                                        out_dtype="bf16"),
+    "fp8_single_cta_accumulate": W.custom(2, 384, 512, [1280, 512], seed=69, fp8=True, accumulate=True),
 }
 
 
