@@ -22,6 +22,8 @@ constexpr int TOKEN_ALIGN = 256;
 constexpr int SCALE_BLOCK = 128;
 
 constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int NUM_THREADS_FP8 = 224;  // + warp 6: FP8 scale-factor converter
+constexpr int SF_WARP = 6;
 constexpr int EPI_WARP0 = 2;
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int WORK_RING = 8;       // depth of the shared-memory work-item queue
@@ -46,7 +48,11 @@ constexpr uint32_t SF_COL0 = BN;
 // FP8 stages also carry the raw FP32 scales of their 128-token block: 128 of A and 256 of B,
 // brought in by bulk copies (padded so that every stage stays 1024-byte aligned).
 constexpr uint32_t SF_SMEM_BYTES = (BM + BN) * 4;
-constexpr uint32_t SF_SMEM_PAD = 2048;
+// ... followed by the UE8M0 scale factors in the TMEM layout: 3 blocks of 32 rows x 16 bytes
+// (A; B columns 0..127; B columns 128..255), copied to TMEM by the MMA thread.
+constexpr uint32_t SF_UE8_OFFSET = SF_SMEM_BYTES;
+constexpr uint32_t SF_UE8_BLOCK = 32 * 16;
+constexpr uint32_t SF_SMEM_PAD = 4096;
 constexpr uint32_t SF_A_COLS = 4;
 constexpr uint32_t SF_STAGE_COLS = 12;
 

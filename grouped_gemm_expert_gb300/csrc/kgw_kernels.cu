@@ -394,7 +394,7 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
 //    both CTAs' shared memory and writes each CTA's 128 rows into its own TMEM. Per SM this moves
 //    32 KiB per k-iteration into shared memory instead of 48 KiB.
 template <bool kFp8, bool kPair>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
   // FP8 runs on single CTAs: a CTA-pair version (block-scaled cta_group::2 MMA, scale factors of
@@ -436,11 +436,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int w = 0; w < WORK_RING; ++w) {
       mbar_init(&ctl->wfull[w], 1);
-      mbar_init(&ctl->wempty[w], kPair ? 2 * (1 + NUM_EPI_WARPS) : 1 + NUM_EPI_WARPS);
+      mbar_init(&ctl->wempty[w], kPair ? 2 * (1 + NUM_EPI_WARPS) : 1 + NUM_EPI_WARPS + (kFp8 ? 1 : 0));
     }
     mbar_init(&ctl->mma_done, 1);
     for (int st = 0; st < kStages; ++st) {
-      mbar_init(&ctl->sf_full[st], NUM_EPI_WARPS * kHalves);
+      mbar_init(&ctl->sf_full[st], 1);
       mbar_init(&ctl->sfdata[st], 1);
     }
     ctl->abort_flag = 0;
@@ -471,7 +471,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t leader_full0 = kPair ? mapa_shared(smem_u32(&ctl->full[0]), 0) : 0u;
   const uint32_t leader_wempty0 = kPair ? mapa_shared(smem_u32(&ctl->wempty[0]), 0) : 0u;
   const uint32_t leader_tempty0 = kPair ? mapa_shared(smem_u32(&ctl->tempty[0]), 0) : 0u;
-  const uint32_t leader_sffull0 = kPair ? mapa_shared(smem_u32(&ctl->sf_full[0]), 0) : 0u;
 
   // A consumer is done with work-ring slot `slot`.
   auto release_slot = [&](int slot) {
@@ -632,6 +631,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if constexpr (kFp8) {
             const uint32_t sfa = tmem_base + SF_COL0 + stage * SF_STAGE_COLS;
             const uint32_t sfb = sfa + SF_A_COLS;
+            // scale factors of this stage: shared memory (TMEM layout) -> TMEM, in order before the MMAs
+            const uint32_t ue8 = b_addr + kStageB + SF_UE8_OFFSET;
+#pragma unroll
+            for (int blk = 0; blk < 3; ++blk)
+              tmem_cp_32x128b_warpx4(sfa + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               // A: K-major 128-byte rows; K step of 32 e4m3 = 32 bytes.
@@ -680,7 +684,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       wait_bounded_t<kPair>(&ctl->mma_done, 0, &dummy, p.timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp < EPI_WARP0 + NUM_EPI_WARPS) {
     // ======================= Epilogue (warps 2..5) =======================
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
     int32_t* counters = reinterpret_cast<int32_t*>(p.ws + p.L.counters);
@@ -688,8 +692,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int32_t* counter_base = reinterpret_cast<const int32_t*>(p.ws + p.L.counter_base);
     float* partials = reinterpret_cast<float*>(p.ws + p.L.partials);
     int tcount = 0;
-    int sf_stage = 0;          // FP8 scale-factor ring position (same sequence as the TMA ring)
-    uint32_t sf_phase = 0;
     for (int n = 0;; ++n) {
       const int slot = n % WORK_RING;
       const bool okw = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
@@ -711,55 +713,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int off = lane * 16; off < rb; off += 32 * 16)
             *reinterpret_cast<uint4*>(obase + r * ostride + off) = make_uint4(0, 0, 0, 0);
         continue;
-      }
-      if constexpr (kFp8) {
-        // Scale factors of this item's k-iterations go into the TMEM stage ring (UE8M0 per
-        // row of A / column of B, one 128-token block per k-iteration).
-        bool okf = true;
-        for (int kb = it.kbeg; kb < it.kend; ++kb) {
-          // This CTA's scales of the stage have landed; that also means the MMAs that read this
-          // stage's TMEM scale factors in the previous round have completed.
-          const bool oke = wait_bounded(&ctl->sfdata[sf_stage], sf_phase, abort_flag, p.timeout_ns);
-          if (!__all_sync(0xffffffffu, oke)) {
-            okf = false;
-            break;
-          }
-          tc_fence_after();
-          const float* sa = reinterpret_cast<const float*>(stage_mem + size_t(sf_stage) * kStageBytes +
-                                                           STAGE_A_BYTES + kStageB);
-          const float* sb = sa + BM;
-          bool bad = false;
-          uint32_t va[4], vb[8];
-          // TMEM scale-factor layout read by the block-scaled MMA: 32 lanes (repeated in every
-          // lane quadrant) x columns, column c holding rows (A) / columns (B) 32c + lane.
-#pragma unroll
-          for (int c = 0; c < 4; ++c) va[c] = ue8m0_x4(sa[32 * c + lane], bad);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) vb[c] = ue8m0_x4(sb[32 * c + lane], bad);
-          if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
-          const uint32_t tsf = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + SF_COL0 + sf_stage * SF_STAGE_COLS;
-          tmem_st_32x32b_x4(tsf, va);
-          tmem_st_32x32b_x8(tsf + SF_A_COLS, vb);
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) {
-            if (kPair && !leader)
-              mbar_arrive_remote(leader_sffull0 + sf_stage * 8);
-            else
-              mbar_arrive(&ctl->sf_full[sf_stage]);
-          }
-          if (++sf_stage == kStages) {
-            sf_stage = 0;
-            sf_phase ^= 1;
-          }
-        }
-        if (!okf) break;
-      }
-      if (p.accumulate && it.split == it.nsplit - 1) {
-        // the previous output is read at the end of this item: start pulling this thread's row
-        // of it into L2 while the main loop runs (one bulk prefetch per row)
-        prefetch_l2_bulk(obase + lane * ostride, static_cast<uint32_t>(BN * esz));
       }
       const int acc = kFp8 ? 0 : (tcount & 1);
       const uint32_t use = kFp8 ? static_cast<uint32_t>(tcount) : static_cast<uint32_t>(tcount >> 1);
@@ -867,6 +820,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
 
+  if constexpr (kFp8) {
+    if (warp == SF_WARP) {
+      // ======================= FP8 scale-factor converter (warp 6) =======================
+      // Per k-iteration: the stage's FP32 scales (128 of A, 256 of B) -> UE8M0 bytes (replicated
+      // over the four 32-token blocks) in the TMEM layout read by the block-scaled MMA: 32 rows x
+      // 4 words per block, word c of row l holding row/column 32c + l.
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int n = 0;; ++n) {
+        const int slot = n % WORK_RING;
+        const bool okw = wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, okw)) break;
+        const int cur = ctl->work_item[slot];
+        __syncwarp();
+        if (lane == 0) release_slot(slot);
+        if (cur < 0) break;
+        const Item it = decode_item(p, cur, bk);
+        bool ok = true;
+        for (int kb = it.kbeg; kb < it.kend; ++kb) {
+          // the scales have landed; this also means the copies of the previous round are done
+          const bool okd = wait_bounded(&ctl->sfdata[stage], phase, abort_flag, p.timeout_ns);
+          if (!__all_sync(0xffffffffu, okd)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sS = stage_mem + size_t(stage) * kStageBytes + STAGE_A_BYTES + kStageB;
+          const float* sa = reinterpret_cast<const float*>(sS);
+          const float* sb = sa + BM;
+          uint4* ue = reinterpret_cast<uint4*>(sS + SF_UE8_OFFSET);
+          bool bad = false;
+          ue[lane] = make_uint4(ue8m0_x4(sa[lane], bad), ue8m0_x4(sa[32 + lane], bad), ue8m0_x4(sa[64 + lane], bad),
+                                ue8m0_x4(sa[96 + lane], bad));
+          ue[32 + lane] = make_uint4(ue8m0_x4(sb[lane], bad), ue8m0_x4(sb[32 + lane], bad),
+                                     ue8m0_x4(sb[64 + lane], bad), ue8m0_x4(sb[96 + lane], bad));
+          ue[64 + lane] = make_uint4(ue8m0_x4(sb[128 + lane], bad), ue8m0_x4(sb[160 + lane], bad),
+                                     ue8m0_x4(sb[192 + lane], bad), ue8m0_x4(sb[224 + lane], bad));
+          if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->sf_full[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  }
+
   // ======================= teardown =======================
   tc_fence_before();
   if constexpr (kPair) {
@@ -906,7 +909,7 @@ static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, cons
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.blockDim = dim3(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
