@@ -103,7 +103,6 @@ kgw_status validate(const kgw_wgrad_args* a, bool fp8) {
   if (a->hidden % kgw::BM != 0 || a->intermediate % kgw::BN != 0) return KGW_ERR_UNSUPPORTED;
   if (a->a_major != KGW_K_MAJOR && a->a_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
   if (a->b_major != KGW_K_MAJOR && a->b_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
-  if (a->a_major != KGW_K_MAJOR || a->b_major != KGW_MN_MAJOR) return KGW_ERR_UNSUPPORTED;
   if (a->input_order != KGW_TENSOR2D && a->input_order != KGW_RAGGED) return KGW_ERR_INVALID_ARG;
   if (a->out_dtype != KGW_OUT_F32 && a->out_dtype != KGW_OUT_BF16) return KGW_ERR_INVALID_ARG;
   if (a->accumulate != 0 && a->accumulate != 1) return KGW_ERR_INVALID_ARG;
@@ -117,9 +116,8 @@ kgw_status validate(const kgw_wgrad_args* a, bool fp8) {
     if (!a->a || !a->b) return KGW_ERR_INVALID_ARG;
     if (!aligned(a->a, 16) || !aligned(a->b, 16)) return KGW_ERR_ALIGNMENT;
     const int64_t esz = fp8 ? 1 : 2;
-    // TMA coordinates are int32: the ragged view of A has tokens_sum*hidden*esz/128 rows.
-    if (a->input_order == KGW_RAGGED && (a->tokens_sum * a->hidden * esz) / 128 >= (int64_t(1) << 31))
-      return KGW_ERR_UNSUPPORTED;
+    (void)esz;
+    // TMA coordinates and per-expert extents are int32
     if (a->tokens_sum >= (int64_t(1) << 31)) return KGW_ERR_UNSUPPORTED;
   }
   // work items must fit int32: T * (E + 2*kiters/MIN_SPLIT)
@@ -145,9 +143,9 @@ kgw_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base,
 struct Prepared {
   kgw::PlanParams pp;
   kgw::MainParams mp;
-  CUtensorMap tmA;  // tensor2d: A itself; ragged: template of the per-expert descriptors (small class)
-  CUtensorMap tmA_large;  // ragged: template for expert blocks of at least TMAP_SIZE_CLASS_BYTES
-  CUtensorMap tmB;
+  CUtensorMap tmA;  // A's descriptor (for ragged K-major A: the small-class template, unused)
+  CUtensorMap tmB;  // B's descriptor (likewise)
+  kgw::MapTemplates tpl;  // templates of per-expert descriptors (ragged, K-major operands)
   int grid;
 };
 
@@ -183,29 +181,48 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   const int bk = bk_of(fp8);
   const uint64_t esz = fp8 ? 1 : 2;
   std::memset(&P->tmA, 0, sizeof(P->tmA));
-  std::memset(&P->tmA_large, 0, sizeof(P->tmA_large));
   std::memset(&P->tmB, 0, sizeof(P->tmB));
+  std::memset(&P->tpl, 0, sizeof(P->tpl));
+  const bool ragged = a->input_order == KGW_RAGGED;
+  const bool a_k = a->a_major == KGW_K_MAJOR;
+  const bool b_k = a->b_major == KGW_K_MAJOR;
+  const uint32_t b_rows_cta = static_cast<uint32_t>(kgw::BN / halves);  // B columns one CTA loads
   if (a->tokens_sum > 0) {
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t Ts = static_cast<uint64_t>(a->tokens_sum);
-    if (a->input_order == KGW_TENSOR2D) {
-      // A [hidden, tokens]: inner = tokens; box = bk tokens x 128 rows
-      st = encode_2d(&P->tmA, dt, a->a, Ts, static_cast<uint64_t>(a->hidden), Ts * esz, bk, kgw::BM);
-    } else {
-      // template of one expert's block [hidden, n] (row stride n elements); the plan kernel
-      // sets the address, n and the stride per expert
-      const uint64_t H = static_cast<uint64_t>(a->hidden);
+    const uint64_t H = static_cast<uint64_t>(a->hidden), I = static_cast<uint64_t>(a->intermediate);
+    const uint32_t atom = static_cast<uint32_t>(128 / esz);  // elements in one 128-byte swizzle row
+    // Template of a per-expert [rows, n] block (row stride n elements), in the size class below or
+    // at/above 128 KiB; the plan kernel sets the address, n and the stride per expert.
+    auto templates = [&](const void* base, uint64_t rows, uint32_t box_rows, CUtensorMap* small,
+                         CUtensorMap* large) {
       const uint64_t n_small = kgw::TOKEN_ALIGN;
-      uint64_t n_large = (kgw::TMAP_SIZE_CLASS_BYTES + H * esz - 1) / (H * esz);
+      uint64_t n_large = (kgw::TMAP_SIZE_CLASS_BYTES + rows * esz - 1) / (rows * esz);
       n_large = (n_large + kgw::TOKEN_ALIGN - 1) / kgw::TOKEN_ALIGN * kgw::TOKEN_ALIGN;
       if (n_large < n_small) n_large = n_small;
-      st = encode_2d(&P->tmA, dt, a->a, n_small, H, n_small * esz, bk, kgw::BM);
-      if (st == KGW_OK) st = encode_2d(&P->tmA_large, dt, a->a, n_large, H, n_large * esz, bk, kgw::BM);
+      kgw_status r = encode_2d(small, dt, base, n_small, rows, n_small * esz, bk, box_rows);
+      if (r == KGW_OK) r = encode_2d(large, dt, base, n_large, rows, n_large * esz, bk, box_rows);
+      return r;
+    };
+    // A
+    if (a_k && !ragged) {
+      st = encode_2d(&P->tmA, dt, a->a, Ts, H, Ts * esz, bk, kgw::BM);             // [H, tokens]
+    } else if (a_k) {
+      st = templates(a->a, H, kgw::BM, &P->tpl.a_small, &P->tpl.a_large);
+      P->tmA = P->tpl.a_small;
+    } else {
+      st = encode_2d(&P->tmA, dt, a->a, H, Ts, H * esz, atom, bk);                 // [tokens, H]
     }
     if (st != KGW_OK) return st;
-    // B [tokens, intermediate]: inner = intermediate; box = one 128-byte swizzle row x bk tokens
-    st = encode_2d(&P->tmB, dt, a->b, static_cast<uint64_t>(a->intermediate), Ts,
-                   static_cast<uint64_t>(a->intermediate) * esz, 128 / esz, bk);
+    // B
+    if (b_k && !ragged) {
+      st = encode_2d(&P->tmB, dt, a->b, Ts, I, Ts * esz, bk, b_rows_cta);         // [I, tokens]
+    } else if (b_k) {
+      st = templates(a->b, I, b_rows_cta, &P->tpl.b_small, &P->tpl.b_large);
+      P->tmB = P->tpl.b_small;
+    } else {
+      st = encode_2d(&P->tmB, dt, a->b, I, Ts, I * esz, atom, bk);                 // [tokens, I]
+    }
     if (st != KGW_OK) return st;
   }
 
@@ -226,8 +243,10 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   pp.status_dev = a->status_dev;
   pp.ws = static_cast<uint8_t*>(ws);
   pp.L = L;
-  pp.ragged = a->input_order == KGW_RAGGED && a->tokens_sum > 0;
+  pp.build_a = ragged && a_k && a->tokens_sum > 0;
+  pp.build_b = ragged && b_k && a->tokens_sum > 0;
   pp.a = static_cast<const uint8_t*>(a->a);
+  pp.b = static_cast<const uint8_t*>(a->b);
   pp.esz = static_cast<int32_t>(esz);
 
   kgw::MainParams& mp = P->mp;
@@ -241,7 +260,9 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   mp.out = a->out;
   mp.out_bf16 = a->out_dtype == KGW_OUT_BF16;
   mp.accumulate = a->accumulate;
-  mp.ragged = a->input_order == KGW_RAGGED;
+  mp.ragged = ragged;
+  mp.a_kmajor = a_k;
+  mp.b_kmajor = b_k;
   mp.discrete = a->out_ptrs != nullptr;
   mp.fp8 = fp8;
   mp.num_m_tiles = a->hidden / tile_m;
@@ -264,7 +285,7 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
   kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P);
   if (st != KGW_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (kgw::launch_plan(P.pp, P.tmA, P.tmA_large, s) != cudaSuccess) return KGW_ERR_CUDA;
+  if (kgw::launch_plan(P.pp, P.tpl, s) != cudaSuccess) return KGW_ERR_CUDA;
   cudaError_t e = fp8 ? kgw::launch_main_fp8(P.mp, P.tmA, P.tmB, P.grid, s)
                       : kgw::launch_main_bf16(P.mp, P.tmA, P.tmB, P.grid, s);
   return e == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
@@ -349,37 +370,46 @@ int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, 
   kgw_status st = prepare(args, is_fp8 != 0, reinterpret_cast<const float*>(args->a),
                           reinterpret_cast<const float*>(args->a), workspace, workspace_bytes, &P);
   if (st != KGW_OK) return -static_cast<int32_t>(st);
-  if (kgw::launch_plan(P.pp, P.tmA, P.tmA_large, nullptr) != cudaSuccess) return -KGW_ERR_CUDA;
+  if (kgw::launch_plan(P.pp, P.tpl, nullptr) != cudaSuccess) return -KGW_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return -KGW_ERR_CUDA;
   const int32_t E = args->num_experts;
   const size_t bytes = size_t(E) * 128;
-  uint8_t* dev_maps = static_cast<uint8_t*>(std::malloc(bytes));
+  uint8_t* dev_maps = static_cast<uint8_t*>(std::malloc(2 * bytes));
   if (!dev_maps) return -KGW_ERR_INVALID_ARG;
   if (cudaMemcpy(dev_maps, static_cast<uint8_t*>(workspace) + P.pp.L.tmaps, bytes, cudaMemcpyDeviceToHost) !=
-      cudaSuccess) {
+          cudaSuccess ||
+      cudaMemcpy(dev_maps + bytes, static_cast<uint8_t*>(workspace) + P.pp.L.tmaps_b, bytes,
+                 cudaMemcpyDeviceToHost) != cudaSuccess) {
     std::free(dev_maps);
     return -KGW_ERR_CUDA;
   }
   const bool fp8 = is_fp8 != 0;
   const uint64_t esz = fp8 ? 1 : 2;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t b_rows_cta = static_cast<uint32_t>(kgw::BN / (P.pp.tile_m / kgw::BM));
   int32_t mismatches = 0;
-  for (int32_t e = 0; e < E; ++e) {
-    const int64_t begin = e ? host_offsets[e - 1] : 0;
-    const int64_t n = host_offsets[e] - begin;
-    if (n <= 0) continue;
-    CUtensorMap ref;
-    std::memset(&ref, 0, sizeof(ref));
-    const uint8_t* base = static_cast<const uint8_t*>(args->a) + begin * args->hidden * esz;
-    if (encode_2d(&ref, dt, base, static_cast<uint64_t>(n), static_cast<uint64_t>(args->hidden), n * esz,
-                  bk_of(fp8), kgw::BM) != KGW_OK) {
-      std::free(dev_maps);
-      return -KGW_ERR_CUDA;
-    }
-    if (std::memcmp(&ref, dev_maps + size_t(e) * 128, 128) != 0) ++mismatches;
-    if (host_dump) {
-      std::memcpy(static_cast<uint8_t*>(host_dump) + size_t(e) * 256, dev_maps + size_t(e) * 128, 128);
-      std::memcpy(static_cast<uint8_t*>(host_dump) + size_t(e) * 256 + 128, &ref, 128);
+  for (int32_t op = 0; op < 2; ++op) {
+    if (op == 0 ? !P.pp.build_a : !P.pp.build_b) continue;
+    const uint64_t rows = op == 0 ? static_cast<uint64_t>(args->hidden) : static_cast<uint64_t>(args->intermediate);
+    const uint8_t* base0 = static_cast<const uint8_t*>(op == 0 ? args->a : args->b);
+    for (int32_t e = 0; e < E; ++e) {
+      const int64_t begin = e ? host_offsets[e - 1] : 0;
+      const int64_t n = host_offsets[e] - begin;
+      if (n <= 0) continue;
+      CUtensorMap ref;
+      std::memset(&ref, 0, sizeof(ref));
+      if (encode_2d(&ref, dt, base0 + begin * rows * esz, static_cast<uint64_t>(n), rows, n * esz, bk_of(fp8),
+                    op == 0 ? kgw::BM : b_rows_cta) != KGW_OK) {
+        std::free(dev_maps);
+        return -KGW_ERR_CUDA;
+      }
+      const uint8_t* got = dev_maps + size_t(op) * bytes + size_t(e) * 128;
+      if (std::memcmp(&ref, got, 128) != 0) ++mismatches;
+      if (host_dump) {
+        uint8_t* d = static_cast<uint8_t*>(host_dump) + (size_t(e) * 2 + op) * 256;
+        std::memcpy(d, got, 128);
+        std::memcpy(d + 128, &ref, 128);
+      }
     }
   }
   std::free(dev_maps);

@@ -69,11 +69,11 @@ static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte block");
 
 // Workspace layout (all offsets 256-byte aligned):
 //   [PlanHeader][order E][item_prefix E+1][splits E][slot_base E][counter_base E]
-//   [per-expert TMA descriptors of ragged A, 128 B each, E]
+//   [per-expert TMA descriptors of ragged K-major A, then of ragged K-major B: 128 B each, 2E]
 //   [arrival counters 4*max_slots (one per split tile and TMEM lane quadrant)]
 //   [partials max_slots * PARTIAL_TILE_BYTES]
 struct WsLayout {
-  size_t order, item_prefix, splits, slot_base, counter_base, tmaps, counters, partials, total;
+  size_t order, item_prefix, splits, slot_base, counter_base, tmaps, tmaps_b, counters, partials, total;
   int32_t max_slots;
 };
 
@@ -89,6 +89,7 @@ inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1) {
   L.slot_base = off;    off = align256(off + sizeof(int32_t) * E);
   L.counter_base = off; off = align256(off + sizeof(int32_t) * E);
   L.tmaps = off;        off = align256(off + size_t(128) * E);
+  L.tmaps_b = off;      off = align256(off + size_t(128) * E);
   L.counters = off;     off = align256(off + sizeof(int32_t) * NUM_EPI_WARPS * halves * (max_slots > 0 ? max_slots : 1));
   L.partials = off;     off = align256(off + PARTIAL_TILE_BYTES * halves * size_t(max_slots));
   L.total = off;
@@ -109,9 +110,16 @@ struct PlanParams {
   uint8_t* ws;
   WsLayout L;
   int32_t tile_m;               // rows of a work tile: 128 (one CTA) or 256 (CTA pair)
-  int32_t ragged;               // build per-expert descriptors of A from the template
+  int32_t build_a, build_b;     // ragged and K-major: build per-expert descriptors of A / B
   const uint8_t* a;             // A base (ragged: flat buffer of per-expert blocks)
-  int32_t esz;                  // bytes per A element
+  const uint8_t* b;             // B base
+  int32_t esz;                  // bytes per operand element
+};
+
+// Host-encoded templates of the per-expert descriptors (ragged, K-major operands): one per
+// size class for A ([hidden, n] blocks) and for B ([intermediate, n] blocks).
+struct MapTemplates {
+  CUtensorMap a_small, a_large, b_small, b_large;
 };
 
 struct MainParams {
@@ -121,6 +129,7 @@ struct MainParams {
   const int64_t* out_ptrs;
   void* out;
   int32_t out_bf16, accumulate, ragged, discrete, fp8;
+  int32_t a_kmajor, b_kmajor;   // operand storage orders (1: token axis has unit stride)
   int32_t num_m_tiles, num_n_tiles;
   int32_t tile_m;               // 128 (one CTA per tile) or 256 (a CTA pair per tile)
   const float* sfa;             // FP8: [tokens_sum/128, H]
@@ -133,7 +142,7 @@ struct MainParams {
 };
 
 // Launchers (kgw_kernels.cu).
-cudaError_t launch_plan(const PlanParams& p, const CUtensorMap& a_small, const CUtensorMap& a_large, cudaStream_t s);
+cudaError_t launch_plan(const PlanParams& p, const MapTemplates& t, cudaStream_t s);
 cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                              cudaStream_t s);
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,

@@ -67,8 +67,7 @@ __device__ __forceinline__ Chunk my_chunk(int n) {
 }
 
 __global__ void __launch_bounds__(PLAN_THREADS)
-    plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ CUtensorMap a_small,
-                const __grid_constant__ CUtensorMap a_large) {
+    plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ MapTemplates tm) {
   __shared__ int32_t s_kit[MAX_EXPERTS];    // k-iterations per expert
   __shared__ int32_t s_key[MAX_EXPERTS];    // k-iterations per item (ordering key)
   __shared__ int64_t s_warp[32];
@@ -121,23 +120,30 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     return;
   }
 
-  // 1b. ragged A: one TMA descriptor per non-empty expert, copied from a host-encoded
-  //     template of the same size class and pointed at the expert's [H, n_e] block (row
-  //     stride n_e elements).
-  if (p.ragged) {
+  // 1b. ragged input order: one TMA descriptor per non-empty expert for each K-major operand,
+  //     copied from a host-encoded template of the same size class and pointed at the expert's
+  //     block ([rows, n_e] row-major at element begin_e*rows; row stride n_e elements).
+  if (p.build_a || p.build_b) {
     for (int e = tid; e < E; e += blockDim.x) {
       const int64_t prev = e ? static_cast<int64_t>(p.offsets[e - 1]) : 0;
       const int64_t n = static_cast<int64_t>(p.offsets[e]) - prev;
       if (n <= 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(p.ws + p.L.tmaps + size_t(e) * 128);
-      const bool large = uint64_t(n) * uint64_t(p.H) * uint64_t(p.esz) >= TMAP_SIZE_CLASS_BYTES;
-      const uint4* src = reinterpret_cast<const uint4*>(large ? &a_large : &a_small);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) dst[j] = src[j];
-      tmap_set_address(dst, reinterpret_cast<uint64_t>(p.a + prev * p.H * p.esz));
-      tmap_set_dim0(dst, static_cast<uint32_t>(n));
-      tmap_set_stride1(dst, static_cast<uint64_t>(n * p.esz));
-      fence_tmap_release();
+      for (int op = 0; op < 2; ++op) {
+        if (op == 0 ? !p.build_a : !p.build_b) continue;
+        const int64_t rows = op == 0 ? p.H : p.I;
+        uint4* dst = reinterpret_cast<uint4*>(p.ws + (op == 0 ? p.L.tmaps : p.L.tmaps_b) + size_t(e) * 128);
+        const bool large = uint64_t(n) * uint64_t(rows) * uint64_t(p.esz) >= TMAP_SIZE_CLASS_BYTES;
+        const CUtensorMap* t = op == 0 ? (large ? &tm.a_large : &tm.a_small) : (large ? &tm.b_large : &tm.b_small);
+        const uint4* src = reinterpret_cast<const uint4*>(t);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j] = src[j];
+        const uint8_t* base = op == 0 ? p.a : p.b;
+        tmap_set_address(dst, reinterpret_cast<uint64_t>(base + prev * rows * p.esz));
+        tmap_set_dim0(dst, static_cast<uint32_t>(n));
+        tmap_set_stride1(dst, static_cast<uint64_t>(n * p.esz));
+        fence_tmap_release();
+      }
     }
   }
 
@@ -393,7 +399,7 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
 //    128 rows of A and 128 columns of B; the even CTA issues tcgen05.mma.cta_group::2, which reads
 //    both CTAs' shared memory and writes each CTA's 128 rows into its own TMEM. Per SM this moves
 //    32 KiB per k-iteration into shared memory instead of 48 KiB.
-template <bool kFp8, bool kPair>
+template <bool kFp8, bool kPair, bool kAK, bool kBK>
 __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
@@ -517,10 +523,16 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       int nxt = 0;
       if (lane == 0 && leader) nxt = atomicAdd(item_counter, 1);
       const Item it = decode_item(p, cur, bk);
+      // ragged + K-major operand: the expert's own descriptor, coordinates relative to its block
       const CUtensorMap* amap = &tmA;
-      if (p.ragged) {
+      const CUtensorMap* bmap = &tmB;
+      if (kAK && p.ragged) {
         amap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps + size_t(it.e) * 128);
         if (lane == 0 && it.kend > it.kbeg) fence_tmap_acquire(amap);
+      }
+      if (kBK && p.ragged) {
+        bmap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps_b + size_t(it.e) * 128);
+        if (lane == 0 && it.kend > it.kbeg) fence_tmap_acquire(bmap);
       }
       const int a_row = it.m0 + static_cast<int>(rank) * BM;            // this CTA's A rows
       const int b_col = it.n0 + static_cast<int>(rank) * (BN / kHalves);  // this CTA's B columns
@@ -537,27 +549,31 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         uint8_t* sB = sA + STAGE_A_BYTES;
         const int64_t tok = it.begin + int64_t(kb) * bk;
         if (!drop && lane == 0) {
-          const int32_t ax = p.ragged ? kb * bk : static_cast<int32_t>(tok);
-          if constexpr (kPair) {
-            const uint32_t fb = leader_full0 + stage * 8;
-            tma_load_2d_pair(sA, amap, fb, ax, a_row);
-#pragma unroll
-            for (int j = 0; j < BN / kHalves / 64; ++j)
-              tma_load_2d_pair(sB + j * (64 * 128), &tmB, fb, b_col + 64 * j, static_cast<int32_t>(tok));
+          const uint32_t fb = kPair ? leader_full0 + stage * 8 : 0u;
+          auto load = [&](void* dst, const CUtensorMap* map, int32_t x, int32_t y) {
+            if constexpr (kPair)
+              tma_load_2d_pair(dst, map, fb, x, y);
+            else
+              tma_load_2d(dst, map, &ctl->full[stage], x, y);
+          };
+          // token coordinate: relative to the expert's block for per-expert descriptors
+          const int32_t kx = p.ragged ? kb * bk : static_cast<int32_t>(tok);
+          constexpr int kAtom = kFp8 ? 128 : 64;  // elements per 128-byte swizzle row
+          // A: K-major -> one box [128 rows x bk tokens]; MN-major -> boxes [bk tokens x 128 B of rows]
+          if constexpr (kAK) {
+            load(sA, amap, kx, a_row);
           } else {
-            tma_load_2d(sA, amap, &ctl->full[stage], ax, a_row);
-            if constexpr (kFp8) {
-              // FP8 B boxes are 128 columns (128 bytes) wide
 #pragma unroll
-              for (int j = 0; j < BN / 128; ++j)
-                tma_load_2d(sB + j * (128 * 128), &tmB, &ctl->full[stage], b_col + 128 * j,
-                            static_cast<int32_t>(tok));
-            } else {
+            for (int j = 0; j < BM / kAtom; ++j)
+              load(sA + j * bk * 128, &tmA, a_row + kAtom * j, static_cast<int32_t>(tok));
+          }
+          // B: K-major -> one box [this CTA's columns x bk tokens]; MN-major -> boxes of 128 B of columns
+          if constexpr (kBK) {
+            load(sB, bmap, kx, b_col);
+          } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
-                tma_load_2d(sB + j * (64 * 128), &tmB, &ctl->full[stage], b_col + 64 * j,
-                            static_cast<int32_t>(tok));
-            }
+            for (int j = 0; j < BN / kHalves / kAtom; ++j)
+              load(sB + j * bk * 128, &tmB, b_col + kAtom * j, static_cast<int32_t>(tok));
           }
           if constexpr (kFp8) {
             // this 128-token block's FP32 scales: the tile's 128 rows of A and 256 columns of B;
@@ -565,7 +581,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             const int64_t kblk = tok / SCALE_BLOCK;
             uint8_t* sS = sB + kStageB;
             mbar_arrive_expect_tx(&ctl->sfdata[stage], SF_SMEM_BYTES);
-            bulk_load(sS, p.sfa + kblk * p.H + a_row, BM * 4, &ctl->sfdata[stage]);
+            bulk_load(sS, p.sfa + kblk * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
             bulk_load(sS + BM * 4, p.sfb + kblk * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
           }
         }
@@ -598,7 +614,24 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       int tcount = 0;
-      const uint32_t idesc = kFp8 ? idesc_mxf8(BM * kHalves, BN, 1, 0) : idesc_bf16_f32(BM * kHalves, BN, 1);
+      constexpr uint32_t a_mn = kAK ? 0u : 1u, b_mn = kBK ? 0u : 1u;
+      const uint32_t idesc = kFp8 ? idesc_mxf8(BM * kHalves, BN, a_mn, b_mn, 0)
+                                  : idesc_bf16_f32(BM * kHalves, BN, a_mn, b_mn);
+      // Shared-memory operand descriptors (128-byte swizzle). K-major: 128-byte rows, 8-row groups
+      // 1024 B apart, K step of 32 bytes. MN-major: 128-byte atoms of rows/columns stacked along K
+      // (one atom = bk x 128 B, LBO between atoms), 8-row K groups 1024 B apart, K step of
+      // 16 (BF16) / 32 (FP8) rows = 2048 / 4096 bytes.
+      constexpr uint32_t kMnStep = kFp8 ? 4096u : 2048u;
+      const uint32_t mn_lbo = static_cast<uint32_t>(bk) * 128u;
+      // descriptor = template (offsets, swizzle, version) + start address / 16 in the low 14 bits;
+      // the start address advances by the K step for each of the 4 MMAs of a stage
+      const uint64_t a_tmpl = kAK ? sdesc_sw128(0, 16, 1024) : sdesc_sw128(0, mn_lbo, 1024);
+      const uint64_t b_tmpl = kBK ? sdesc_sw128(0, 16, 1024) : sdesc_sw128(0, mn_lbo, 1024);
+      constexpr uint32_t a_step = (kAK ? 32u : kMnStep) >> 4;
+      constexpr uint32_t b_step = (kBK ? 32u : kMnStep) >> 4;
+      auto desc = [](uint64_t tmpl, uint32_t base, uint32_t step, int k) {
+        return tmpl + static_cast<uint64_t>(((base & 0x3FFFFu) >> 4) + k * step);
+      };
       for (int n = 0;; ++n) {
         const int slot = n % WORK_RING;
         if (!wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns)) break;
@@ -637,22 +670,15 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             for (int blk = 0; blk < 3; ++blk)
               tmem_cp_32x128b_warpx4(sfa + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              // A: K-major 128-byte rows; K step of 32 e4m3 = 32 bytes.
-              const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
-              // B: MN-major, 128-column (128 B) atoms 16 KiB apart along N, 8-row K groups
-              // 1024 B apart; K step of 32 rows = 4096 bytes.
-              const uint64_t bdesc = sdesc_sw128(b_addr + k * 4096, 128 * 128, 1024);
-              mma_mxf8(d_tmem, adesc, bdesc, idesc, sfa, sfb, (kb > it.kbeg || k > 0) ? 1u : 0u);
-            }
+            for (int k = 0; k < 4; ++k)
+              mma_mxf8(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc, sfa, sfb,
+                       (kb > it.kbeg || k > 0) ? 1u : 0u);
           } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              // A: K-major, 128-byte rows, 8-row groups 1024 B apart; K step of 16 = 32 bytes.
-              const uint64_t adesc = sdesc_sw128(a_addr + k * 32, 16, 1024);
-              // B: MN-major, 64-column (128 B) atoms 8 KiB apart along N, 8-row K groups 1024 B
-              // apart; K step of 16 rows = 2048 bytes. In a pair each CTA holds 128 columns.
-              const uint64_t bdesc = sdesc_sw128(b_addr + k * 2048, 64 * 128, 1024);
+              // in a pair each CTA holds 128 rows of A and 128 columns of B
+              const uint64_t adesc = desc(a_tmpl, a_addr, a_step, k);
+              const uint64_t bdesc = desc(b_tmpl, b_addr, b_step, k);
               if constexpr (kPair)
                 mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kbeg || k > 0) ? 1u : 0u);
               else
@@ -891,21 +917,20 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
 // Launchers
 // =============================================================================================
 
-cudaError_t launch_plan(const PlanParams& p, const CUtensorMap& a_small, const CUtensorMap& a_large,
-                        cudaStream_t s) {
+cudaError_t launch_plan(const PlanParams& p, const MapTemplates& t, cudaStream_t s) {
   int threads = ((p.E + 31) / 32) * 32;
   threads = threads < 128 ? 128 : (threads > PLAN_THREADS ? PLAN_THREADS : threads);
-  plan_kernel<<<1, threads, 0, s>>>(p, a_small, a_large);
+  plan_kernel<<<1, threads, 0, s>>>(p, t);
   return cudaGetLastError();
 }
 
-template <bool kFp8, bool kPair>
+template <bool kFp8, bool kPair, bool kAK, bool kBK>
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
+  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK>;
   const size_t smem = main_smem_bytes(kPair, kFp8);
   // set on every launch: the attribute is per device and the call is cheap
-  cudaError_t e = cudaFuncSetAttribute(wgrad_kernel<kFp8, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid, 1, 1);
@@ -922,18 +947,28 @@ static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, cons
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, wgrad_kernel<kFp8, kPair>, p, tmA, tmB);
+  return cudaLaunchKernelEx(&cfg, kernel, p, tmA, tmB);
+}
+
+// One instantiation per operand storage order (K-major A / K-major B), chosen at run time.
+template <bool kFp8, bool kPair>
+static cudaError_t launch_orders(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                                 cudaStream_t s) {
+  if (p.a_kmajor && !p.b_kmajor) return launch_main<kFp8, kPair, true, false>(p, tmA, tmB, grid, s);
+  if (!p.a_kmajor && !p.b_kmajor) return launch_main<kFp8, kPair, false, false>(p, tmA, tmB, grid, s);
+  if (p.a_kmajor && p.b_kmajor) return launch_main<kFp8, kPair, true, true>(p, tmA, tmB, grid, s);
+  return launch_main<kFp8, kPair, false, true>(p, tmA, tmB, grid, s);
 }
 
 cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                              cudaStream_t s) {
-  if (p.tile_m == 2 * BM) return launch_main<false, true>(p, tmA, tmB, grid, s);
-  return launch_main<false, false>(p, tmA, tmB, grid, s);
+  if (p.tile_m == 2 * BM) return launch_orders<false, true>(p, tmA, tmB, grid, s);
+  return launch_orders<false, false>(p, tmA, tmB, grid, s);
 }
 
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s) {
-  return launch_main<true, false>(p, tmA, tmB, grid, s);
+  return launch_orders<true, false>(p, tmA, tmB, grid, s);
 }
 
 bool fp8_supported() { return true; }

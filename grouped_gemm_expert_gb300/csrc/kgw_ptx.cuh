@@ -359,16 +359,20 @@ __device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor, kind::f16: D=F32 (bits 4-5 = 1), A=B=BF16 (bits 7-9, 10-12 = 1),
-// A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N>>3 at bits 17-22, M>>4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+// A MN-major (bit 15) / B MN-major (bit 16) when set, N>>3 at bits 17-22, M>>4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t a_mn_major,
+                                                      uint32_t b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) | (b_mn_major << 16) | ((N >> 3) << 17) |
+         ((M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf8f6f4 with UE8M0 scales: A=B=E4M3 (format 0), scale
-// format bit 23 = 1 (E8M0), B MN-major (bit 16), N>>3 at 17-22, M>>4 at 24-28; the scale
+// format bit 23 = 1 (E8M0), A/B MN-major bits 15/16, N>>3 at 17-22, M>>4 at 24-28; the scale
 // factor ids (bits 4-5 for B, 29-30 for A) select the byte of the 32-bit TMEM scale column.
-__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t b_mn_major, uint32_t sf_id) {
-  return (sf_id << 4) | (b_mn_major << 16) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sf_id << 29);
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t a_mn_major, uint32_t b_mn_major,
+                                                  uint32_t sf_id) {
+  return (sf_id << 4) | (a_mn_major << 15) | (b_mn_major << 16) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
+         (sf_id << 29);
 }
 
 // ------------------------------------------------------------------------------------------

@@ -62,9 +62,10 @@ typedef enum kgw_major {
 /* How the token dimension is stored (section "BF16 contract", input_order). */
 typedef enum kgw_input_order {
   KGW_TENSOR2D = 0,  /* one global 2-D tensor per operand */
-  KGW_RAGGED = 1     /* per-expert K-contiguous blocks concatenated in memory: expert e's block of
-                        A is [hidden, n_e] row-major starting at element begin_e*hidden; B's block
-                        is [n_e, intermediate] row-major starting at element begin_e*intermediate */
+  KGW_RAGGED = 1     /* per-expert blocks concatenated in memory, expert e's block starting at element
+                        begin_e*hidden (A) or begin_e*intermediate (B) and keeping the operand's
+                        unit-stride axis: K-major A [hidden, n_e], M-major A [n_e, hidden], N-major
+                        B [n_e, intermediate], K-major B [intermediate, n_e] (row-major each) */
 } kgw_input_order;
 
 typedef enum kgw_out_dtype { KGW_OUT_F32 = 0, KGW_OUT_BF16 = 1 } kgw_out_dtype;
@@ -75,9 +76,13 @@ typedef struct kgw_wgrad_args {
   int32_t intermediate;     /* N: multiple of 256                                            */
   int64_t tokens_sum;       /* total tokens; must equal offsets[E-1]; multiple of 256        */
   const void* a;            /* A: bf16 (or e4m3) [hidden, tokens_sum], see a_major/input_order */
-  int32_t a_major;          /* KGW_K_MAJOR (the only order implemented for A)                */
+  int32_t a_major;          /* KGW_K_MAJOR: stored [hidden, tokens_sum] (token stride 1);
+                               KGW_MN_MAJOR: stored [tokens_sum, hidden] (hidden stride 1), e.g.
+                               dY kept token-major; ragged: per-expert [n_e, hidden] blocks      */
   const void* b;            /* B: bf16 (or e4m3) [tokens_sum, intermediate]                 */
-  int32_t b_major;          /* KGW_MN_MAJOR (the only order implemented for B)               */
+  int32_t b_major;          /* KGW_MN_MAJOR: stored [tokens_sum, intermediate];
+                               KGW_K_MAJOR: stored [intermediate, tokens_sum] (token stride 1);
+                               ragged K-major: per-expert [intermediate, n_e] blocks            */
   const int32_t* offsets;   /* int32 [E]: non-decreasing cumulative token counts             */
   int32_t input_order;      /* kgw_input_order                                               */
   void* out;                /* dense output [E, hidden, intermediate] row-major, or NULL     */
@@ -162,12 +167,12 @@ int64_t kgw_debug_set(int32_t key, int64_t value);
 
 /*
  * Testing hook for the ragged input order: runs only the schedule kernel of a call (which builds
- * one TMA descriptor per non-empty expert of A on the device, from the expert's offset and token
- * count), then compares each descriptor byte for byte with one encoded on the host for the same
- * block (host_offsets: a host copy of args->offsets). Synchronises the device. Returns the number
- * of experts whose descriptors differ (0 = all identical) or -kgw_status on error. host_dump,
- * if non-NULL, receives E x 256 bytes: per expert the device-built then the host-encoded
- * descriptor. Allocates host memory only.
+ * one TMA descriptor per non-empty expert on the device, from the expert's offset and token
+ * count) for every K-major operand, then compares each descriptor byte for byte with one encoded
+ * on the host for the same block (host_offsets: a host copy of args->offsets). Synchronises the
+ * device. Returns the number of differing descriptors (0 = all identical) or -kgw_status on
+ * error. host_dump, if non-NULL, receives E x 2 x 256 bytes: per expert and operand (A, B) the
+ * device-built then the host-encoded descriptor. Allocates host memory only.
  */
 int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, const int32_t* host_offsets,
                                     void* workspace, size_t workspace_bytes, void* host_dump);

@@ -100,20 +100,24 @@ def offsets_valid(offsets, tokens_sum: int) -> bool:
 # Logical operands from stored operands (section "BF16 contract", input_order)
 # ---------------------------------------------------------------------------------------------
 
-def logical_a(a_values: np.ndarray, hidden: int, offsets, input_order: str) -> np.ndarray:
-    """Logical A [hidden, tokens_sum] from its stored values.
+def logical_a(a_values: np.ndarray, hidden: int, offsets, input_order: str, a_major: str = "k") -> np.ndarray:
+    """Logical A [hidden, tokens_sum] from its stored values ("Grouped GEMM + WGrad (Unified)",
+    section "BF16 contract": A is (hidden, tokens_sum) with stride (tokens_sum, 1) K-major or
+    (1, hidden) M-major; input_order "tensor_ragged" keeps only the unit-stride axis).
 
-    tensor2d: the stored tensor is A itself ([hidden, tokens_sum], stride (tokens_sum, 1)).
-    ragged:   per-expert K-contiguous blocks concatenated in memory; only the unit-stride
-              (token) axis keeps its meaning, so expert e's block is [hidden, n_e] row-major
-              starting at element begin_e*hidden.
+    K-major tensor2d: stored [hidden, tokens_sum]. K-major ragged: expert e's block is
+    [hidden, n_e] row-major starting at element begin_e*hidden. M-major (either order): stored
+    [tokens_sum, hidden]; expert e's rows are its [n_e, hidden] block, which already starts at
+    element begin_e*hidden.
     """
     ranges = expert_ranges(offsets)
     tokens_sum = ranges[-1][1] if ranges else 0
-    if input_order == "tensor2d":
-        return np.asarray(a_values).reshape(hidden, tokens_sum)
-    assert input_order == "ragged"
     flat = np.asarray(a_values).reshape(-1)
+    if a_major == "mn":
+        return flat.reshape(tokens_sum, hidden).T
+    if input_order == "tensor2d":
+        return flat.reshape(hidden, tokens_sum)
+    assert input_order == "ragged"
     out = np.zeros((hidden, tokens_sum), dtype=flat.dtype)
     for (b, e) in ranges:
         n = e - b
@@ -122,20 +126,26 @@ def logical_a(a_values: np.ndarray, hidden: int, offsets, input_order: str) -> n
     return out
 
 
-def logical_b(b_values: np.ndarray, intermediate: int, offsets, input_order: str) -> np.ndarray:
-    """Logical B [tokens_sum, intermediate].
+def logical_b(b_values: np.ndarray, intermediate: int, offsets, input_order: str, b_major: str = "mn") -> np.ndarray:
+    """Logical B [tokens_sum, intermediate] (section "BF16 contract": stride (intermediate, 1)
+    N-major or (1, tokens_sum) K-major).
 
-    B's unit-stride axis is the intermediate axis, so expert e's K-contiguous block is
-    [n_e, intermediate] row-major starting at element begin_e*intermediate: identical to
-    the tensor2d storage in both input orders.
+    N-major (either order): stored [tokens_sum, intermediate]; expert e's block [n_e, I] starts at
+    element begin_e*I. K-major tensor2d: stored [intermediate, tokens_sum]. K-major ragged:
+    expert e's block is [intermediate, n_e] row-major starting at element begin_e*intermediate.
     """
     ranges = expert_ranges(offsets)
     tokens_sum = ranges[-1][1] if ranges else 0
     flat = np.asarray(b_values).reshape(-1)
+    if b_major == "mn":
+        return flat.reshape(tokens_sum, intermediate)
+    if input_order == "tensor2d":
+        return flat.reshape(intermediate, tokens_sum).T
     out = np.zeros((tokens_sum, intermediate), dtype=flat.dtype)
     for (b, e) in ranges:
-        if e > b:
-            out[b:e, :] = flat[b * intermediate:e * intermediate].reshape(e - b, intermediate)
+        n = e - b
+        if n:
+            out[b:e, :] = flat[b * intermediate:(b + n) * intermediate].reshape(intermediate, n).T
     return out
 
 
@@ -186,7 +196,8 @@ def wgrad(A: np.ndarray, B: np.ndarray, offsets, c_init=None, accumulate: bool =
 
 def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, *,
                        input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
-                       c_init=None, accumulate: bool = False, with_bound: bool = True):
+                       c_init=None, accumulate: bool = False, with_bound: bool = True,
+                       a_major: str = "k", b_major: str = "mn"):
     """Decode stored operands (raw bits) and evaluate the operation in float64.
 
     a_bits/b_bits: uint16 (bf16) or uint8 (e4m3) numpy arrays as stored.
@@ -194,8 +205,8 @@ def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, 
     c_init: the pre-filled output values (any float dtype, decoded by the caller) or None.
     """
     dec = e4m3_to_f64 if fp8 else bf16_to_f64
-    A = logical_a(dec(a_bits), hidden, offsets, input_order)
-    B = logical_b(dec(b_bits), intermediate, offsets, input_order)
+    A = logical_a(dec(a_bits), hidden, offsets, input_order, a_major)
+    B = logical_b(dec(b_bits), intermediate, offsets, input_order, b_major)
     if fp8:
         A = apply_block_scales_rows(A, sfa)
         B = apply_block_scales_cols(B, sfb)
@@ -230,7 +241,8 @@ def tolerance(S: np.ndarray, ref: np.ndarray, out_dtype: str, c_init=None) -> np
 
 
 def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, e: int, m: int, n: int, *,
-                         input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None):
+                         input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
+                         a_major: str = "k", b_major: str = "mn"):
     """R_e[m, n] and S_e[m, n] read straight from the stored operands (for sampled checks).
 
     Only row m of A_e and column n of B_e are decoded, so this works at full problem size.
@@ -241,15 +253,22 @@ def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int
     cnt = end - b
     if cnt == 0:
         return 0.0, 0.0
+    tokens_sum = expert_ranges(offsets)[-1][1]
     dec = e4m3_to_f64 if fp8 else bf16_to_f64
     flat_a = np.asarray(a_bits).reshape(-1)
-    if input_order == "tensor2d":
-        tokens_sum = expert_ranges(offsets)[-1][1]
+    if a_major == "mn":
+        arow = dec(flat_a[b * hidden + m: end * hidden: hidden])
+    elif input_order == "tensor2d":
         arow = dec(flat_a[m * tokens_sum + b: m * tokens_sum + end])
     else:
         arow = dec(flat_a[b * hidden + m * cnt: b * hidden + (m + 1) * cnt])
     flat_b = np.asarray(b_bits).reshape(-1)
-    bcol = dec(flat_b[b * intermediate + n: end * intermediate: intermediate])
+    if b_major == "mn":
+        bcol = dec(flat_b[b * intermediate + n: end * intermediate: intermediate])
+    elif input_order == "tensor2d":
+        bcol = dec(flat_b[n * tokens_sum + b: n * tokens_sum + end])
+    else:
+        bcol = dec(flat_b[b * intermediate + n * cnt: b * intermediate + (n + 1) * cnt])
     if fp8:
         ks = np.arange(b, end) // SCALE_BLOCK
         arow = arow * np.asarray(sfa, dtype=np.float64)[ks, m]

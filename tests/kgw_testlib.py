@@ -83,6 +83,8 @@ def run_gpu(w, x, device="cuda", status=None, workspace=None, outputs=None):
                          out_dtype=kgw.KGW_OUT_BF16 if w.out_dtype == "bf16" else kgw.KGW_OUT_F32,
                          accumulate=w.accumulate,
                          input_order=kgw.KGW_RAGGED if w.input_order == "ragged" else kgw.KGW_TENSOR2D,
+                         a_major=kgw.KGW_MN_MAJOR if w.a_major == "mn" else kgw.KGW_K_MAJOR,
+                         b_major=kgw.KGW_K_MAJOR if w.b_major == "k" else kgw.KGW_MN_MAJOR,
                          status_dev=status)
     if workspace is None:
         workspace = kgw.workspace_for(args, w.fp8, device=device)
@@ -101,7 +103,7 @@ def oracle_full(w, x_cpu):
                                 w.intermediate, input_order=w.input_order, fp8=w.fp8,
                                 sfa=None if x_cpu.sfa is None else x_cpu.sfa.numpy(),
                                 sfb=None if x_cpu.sfb is None else x_cpu.sfb.numpy(),
-                                c_init=c, accumulate=w.accumulate)
+                                c_init=c, accumulate=w.accumulate, a_major=w.a_major, b_major=w.b_major)
 
 
 def assert_close_to_oracle(w, got: np.ndarray, ref: np.ndarray, S: np.ndarray, c_init=None):

@@ -471,9 +471,9 @@ def test_planted_ragged_bug_is_caught(monkeypatch):
     ragged = W.pack_ragged_a(a, np.array(counts))
     good = O.logical_a
 
-    def wrong_ld(a_values, hidden, offsets_, order):
+    def wrong_ld(a_values, hidden, offsets_, order, a_major="k"):
         if order != "ragged":
-            return good(a_values, hidden, offsets_, order)
+            return good(a_values, hidden, offsets_, order, a_major)
         # bug: treat the ragged buffer as if it had leading dimension tokens_sum
         return np.asarray(a_values).reshape(hidden, -1)
 
@@ -510,3 +510,44 @@ def test_element_from_storage_fp8():
         v, s = O.element_from_storage(e4m3_bits(qa), e4m3_bits(qb), offsets, H, I, e, m, n, fp8=True,
                                       sfa=sfa.numpy(), sfb=sfb.numpy())
         assert abs(v - full[e, m, n]) <= 1e-12 * S[e, m, n] + 1e-300
+
+
+# ------------------------------------------------------------------------------------------
+# Operand storage orders ("Grouped GEMM + WGrad (Unified)", section "BF16 contract": A K-major or
+# M-major, B K-major or N-major; ragged keeps each operand's unit-stride axis)
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("order", ["tensor2d", "ragged"])
+@pytest.mark.parametrize("a_major,b_major", [("k", "mn"), ("mn", "mn"), ("k", "k"), ("mn", "k")])
+def test_storage_orders_give_the_same_result(order, a_major, b_major):
+    counts = [256, 0, 768, 512]
+    w = W.custom(4, 16, 24, counts, seed=61, input_order=order, a_major=a_major, b_major=b_major)
+    ref_w = W.custom(4, 16, 24, counts, seed=61)
+    x = W.make_inputs(w)
+    x0 = W.make_inputs(ref_w)
+    r, S = O.wgrad_from_storage(bf16_bits(x.a), bf16_bits(x.b), x.offsets.numpy(), 16, 24, input_order=order,
+                                a_major=a_major, b_major=b_major)
+    r0, _ = O.wgrad_from_storage(bf16_bits(x0.a), bf16_bits(x0.b), x0.offsets.numpy(), 16, 24)
+    assert np.array_equal(r, r0)
+    # the stored bytes really differ from the K-major/N-major tensor2d layout unless nothing moved
+    if (a_major, b_major, order) != ("k", "mn", "tensor2d"):
+        same_a = bf16_bits(x.a).size == bf16_bits(x0.a).size and np.array_equal(bf16_bits(x.a).ravel(), bf16_bits(x0.a).ravel())
+        same_b = np.array_equal(bf16_bits(x.b).ravel(), bf16_bits(x0.b).ravel())
+        assert not (same_a and same_b)
+    for (e, m, n) in [(0, 3, 5), (2, 15, 23), (3, 0, 0)]:
+        v, s = O.element_from_storage(bf16_bits(x.a), bf16_bits(x.b), x.offsets.numpy(), 16, 24, e, m, n,
+                                      input_order=order, a_major=a_major, b_major=b_major)
+        assert abs(v - r[e, m, n]) <= 1e-12 * S[e, m, n] + 1e-300
+
+
+def test_mn_major_a_is_the_transpose_in_memory():
+    """M-major A stores A^T contiguously: element (m, k) at k*hidden + m."""
+    H, T = 8, 256
+    a = torch.arange(H * T, dtype=torch.float32).reshape(H, T).to(torch.bfloat16)
+    w = W.custom(1, H, 16, [T], seed=0, a_major="mn")
+    a_store, _ = W.store_operands(w, a, torch.zeros(T, 16, dtype=torch.bfloat16))
+    flat = a_store.reshape(-1)
+    for (m, k) in [(0, 0), (3, 17), (7, 255)]:
+        assert flat[k * H + m] == a[m, k]
+    L = O.logical_a(bf16_bits(a_store), H, np.array([T]), "tensor2d", "mn")
+    assert np.array_equal(L, bf16_bits(a).reshape(H, T))

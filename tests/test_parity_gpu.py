@@ -67,6 +67,15 @@ CASES = {
                                             out_dtype="bf16", input_order="ragged"),
     "pair_split_k_discrete": W.custom(2, 512, 256, [16384, 256], seed=66, output_mode="discrete",
                                       out_dtype="bf16"),
+    # operand storage orders: M-major A ([tokens, hidden]) and K-major B ([intermediate, tokens])
+    "a_mn_pair": W.custom(4, 512, 512, [768, 0, 1280, 256], seed=90, a_major="mn"),
+    "b_k_pair_bf16": W.custom(3, 512, 768, [1024, 256, 512], seed=91, b_major="k", out_dtype="bf16"),
+    "a_mn_b_k_single_ragged": W.custom(4, 384, 512, [768, 256, 0, 2048], seed=92, a_major="mn", b_major="k",
+                                       input_order="ragged"),
+    "b_k_ragged_pair_split_accumulate": W.custom(2, 512, 256, [12288, 512], seed=93, b_major="k",
+                                                 input_order="ragged", accumulate=True, out_dtype="bf16"),
+    "fp8_a_mn": W.custom(3, 256, 512, [512, 768, 256], seed=94, fp8=True, a_major="mn", out_dtype="bf16"),
+    "fp8_b_k_ragged": W.custom(3, 384, 512, [1280, 0, 512], seed=95, fp8=True, b_major="k", input_order="ragged"),
     "fp8_bf16_out": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=60, fp8=True, out_dtype="bf16"),
     "fp8_f32_ragged": W.custom(3, 384, 768, [256, 1280, 0], seed=61, fp8=True, input_order="ragged"),
     "fp8_split_k_accumulate": W.custom(3, 128, 256, [16384, 0, 256], seed=62, fp8=True, accumulate=True),
@@ -96,6 +105,18 @@ def test_single_cta_and_pair_tiles_agree():
         kgw.kgw_debug_set(3, prev)
     torch.cuda.synchronize()
     assert torch.equal(pair.view(torch.int16), single.view(torch.int16))
+
+
+@pytest.mark.parametrize("fp8,hidden", [(False, 512), (False, 384), (True, 256)])
+def test_storage_orders_are_bitwise_identical(fp8, hidden):
+    """The same logical operands stored in all four orders give the same bits."""
+    outs = []
+    for am, bm in (("k", "mn"), ("mn", "mn"), ("k", "k"), ("mn", "k")):
+        w = W.custom(3, hidden, 512, [768, 0, 1024], seed=96, fp8=fp8, a_major=am, b_major=bm, out_dtype="bf16")
+        outs.append(run_gpu(w, W.make_inputs(w, DEV), DEV).stacked().clone())
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int16), o.view(torch.int16))
 
 
 def test_deterministic_bitwise():

@@ -89,6 +89,8 @@ class Workload:
     input_order: str = "tensor2d"   # "tensor2d" | "ragged"
     output_mode: str = "dense"      # "dense" | "discrete"
     fp8: bool = False
+    a_major: str = "k"              # "k": A stored [hidden, tokens]; "mn": stored [tokens, hidden]
+    b_major: str = "mn"             # "mn": B stored [tokens, intermediate]; "k": stored [intermediate, tokens]
 
     @property
     def tokens_sum(self) -> int:
@@ -155,6 +157,9 @@ class Inputs:
        block [hidden, n_e] (row-major, leading dimension n_e) starts at element begin_e*hidden.
     b: [tokens_sum, intermediate] row-major (identical in both input orders, because B's
        unit-stride axis is the intermediate axis).
+    With a_major "mn" A is stored [tokens_sum, hidden] (expert blocks [n_e, hidden] back to back
+    in both orders); with b_major "k" B is stored [intermediate, tokens_sum] (tensor2d) or as
+    per-expert [intermediate, n_e] blocks (ragged).
     sfa/sfb (FP8 only): float32 [tokens_sum/128, hidden] / [tokens_sum/128, intermediate].
     c: pre-filled output [E, hidden, intermediate] for accumulate mode, else None.
     """
@@ -221,6 +226,22 @@ def pack_ragged_a(a2d: torch.Tensor, counts) -> torch.Tensor:
     return flat
 
 
+def store_operands(w: Workload, a_logical: torch.Tensor, b_logical: torch.Tensor):
+    """Lay out logical A [hidden, tokens] and B [tokens, intermediate] as the workload stores them."""
+    if w.a_major == "mn":
+        a_store = a_logical.t().contiguous()
+    elif w.input_order == "ragged":
+        a_store = pack_ragged_a(a_logical, w.counts)
+    else:
+        a_store = a_logical
+    if w.b_major == "k":
+        bt = b_logical.t().contiguous()
+        b_store = pack_ragged_a(bt, w.counts) if w.input_order == "ragged" else bt
+    else:
+        b_store = b_logical
+    return a_store, b_store
+
+
 def make_inputs(w: Workload, device="cpu") -> Inputs:
     """Draw the inputs of workload ``w`` on the CPU (seeded) and move them to ``device``."""
     gen = torch.Generator().manual_seed(int(w.seed))
@@ -235,8 +256,7 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
         a_store = a32.to(torch.bfloat16)
         b_store = b32.to(torch.bfloat16)
     del a32, b32
-    if w.input_order == "ragged":
-        a_store = pack_ragged_a(a_store, w.counts)
+    a_store, b_store = store_operands(w, a_store, b_store)
     c = None
     if w.accumulate:
         c = _normal(gen, (E, H, I), w.c_std).to(torch.bfloat16 if w.out_dtype == "bf16" else torch.float32)
@@ -265,8 +285,7 @@ def make_inputs_device(w: Workload, device) -> Inputs:
                       cpu.sfa.to(device), cpu.sfb.to(device), None if cpu.c is None else cpu.c.to(device))
     a = normal((H, T), w.a_std, torch.bfloat16)
     b = normal((T, I), w.b_std, torch.bfloat16)
-    if w.input_order == "ragged":
-        a = pack_ragged_a(a, w.counts)
+    a, b = store_operands(w, a, b)
     c = normal((E, H, I), w.c_std, torch.bfloat16 if w.out_dtype == "bf16" else torch.float32) \
         if w.accumulate else None
     offsets = torch.from_numpy(w.offsets.astype(np.int32)).to(device)
