@@ -45,6 +45,7 @@ KGW_TENSOR2D = 0
 KGW_RAGGED = 1
 KGW_OUT_F32 = 0
 KGW_OUT_BF16 = 1
+KGW_OUT_F16 = 2
 
 EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
             "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc",
@@ -223,7 +224,7 @@ def wgrad(a, b, offsets, *, hidden: int, intermediate: int, out=None, out_ptrs=N
     tokens_sum = int(b.shape[0]) if b.dim() == 2 else 0
     fp8 = a.dtype == torch.float8_e4m3fn
     args = make_args(E, hidden, intermediate, tokens_sum, a, b, offsets, out=out, out_ptrs=out_ptrs,
-                     out_dtype=KGW_OUT_BF16 if out_dtype == "bf16" else KGW_OUT_F32,
+                     out_dtype={"bf16": KGW_OUT_BF16, "f16": KGW_OUT_F16}.get(out_dtype, KGW_OUT_F32),
                      accumulate=accumulate, input_order=KGW_RAGGED if input_order == "ragged" else KGW_TENSOR2D,
                      status_dev=status_dev)
     if workspace is None:

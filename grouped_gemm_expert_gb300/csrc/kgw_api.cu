@@ -104,7 +104,8 @@ kgw_status validate(const kgw_wgrad_args* a, bool fp8) {
   if (a->a_major != KGW_K_MAJOR && a->a_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
   if (a->b_major != KGW_K_MAJOR && a->b_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
   if (a->input_order != KGW_TENSOR2D && a->input_order != KGW_RAGGED) return KGW_ERR_INVALID_ARG;
-  if (a->out_dtype != KGW_OUT_F32 && a->out_dtype != KGW_OUT_BF16) return KGW_ERR_INVALID_ARG;
+  if (a->out_dtype != KGW_OUT_F32 && a->out_dtype != KGW_OUT_BF16 && a->out_dtype != KGW_OUT_F16)
+    return KGW_ERR_INVALID_ARG;
   if (a->accumulate != 0 && a->accumulate != 1) return KGW_ERR_INVALID_ARG;
   if (!a->offsets) return KGW_ERR_INVALID_ARG;
   if ((a->out == nullptr) == (a->out_ptrs == nullptr)) return KGW_ERR_INVALID_ARG;
@@ -258,7 +259,8 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   mp.offsets = a->offsets;
   mp.out_ptrs = a->out_ptrs;
   mp.out = a->out;
-  mp.out_bf16 = a->out_dtype == KGW_OUT_BF16;
+  mp.out_bf16 = a->out_dtype == KGW_OUT_BF16 || a->out_dtype == KGW_OUT_F16;
+  mp.out_f16 = a->out_dtype == KGW_OUT_F16;
   mp.accumulate = a->accumulate;
   mp.ragged = ragged;
   mp.a_kmajor = a_k;

@@ -128,7 +128,8 @@ struct MainParams {
   const int32_t* offsets;
   const int64_t* out_ptrs;
   void* out;
-  int32_t out_bf16, accumulate, ragged, discrete, fp8;
+  int32_t out_bf16, accumulate, ragged, discrete, fp8;  // out_bf16: 16-bit output (BF16 or FP16)
+  int32_t out_f16;              // the 16-bit output is FP16
   int32_t a_kmajor, b_kmajor;   // operand storage orders (1: token axis has unit stride)
   int32_t num_m_tiles, num_n_tiles;
   int32_t tile_m;               // 128 (one CTA per tile) or 256 (a CTA pair per tile)

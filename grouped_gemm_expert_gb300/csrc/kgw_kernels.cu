@@ -347,7 +347,7 @@ __device__ __forceinline__ uint4 load_old4(const MainParams& p, const char* src)
 }
 
 // Write 4 consecutive output values (FP32 accumulator values v) at dst: overwrite, or add the
-// previous contents (one FP32 add, then one rounding to the output type).
+// previous contents (one FP32 add, then one rounding to the output type: FP32, BF16 or FP16).
 __device__ __forceinline__ void emit4(const MainParams& p, char* dst, float4 v, const uint4& o) {
   if (!p.out_bf16) {
     if (p.accumulate) {
@@ -357,7 +357,7 @@ __device__ __forceinline__ void emit4(const MainParams& p, char* dst, float4 v, 
       v.w += __uint_as_float(o.w);
     }
     *reinterpret_cast<float4*>(dst) = v;
-  } else {
+  } else if (!p.out_f16) {
     if (p.accumulate) {
       v.x += bf16_lo(o.x);
       v.y += bf16_hi(o.x);
@@ -365,6 +365,14 @@ __device__ __forceinline__ void emit4(const MainParams& p, char* dst, float4 v, 
       v.w += bf16_hi(o.y);
     }
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  } else {
+    if (p.accumulate) {
+      v.x += f16_lo(o.x);
+      v.y += f16_hi(o.x);
+      v.z += f16_lo(o.y);
+      v.w += f16_hi(o.y);
+    }
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_f16x2(v.x, v.y), pack_f16x2(v.z, v.w));
   }
 }
 

@@ -68,7 +68,9 @@ typedef enum kgw_input_order {
                         B [n_e, intermediate], K-major B [intermediate, n_e] (row-major each) */
 } kgw_input_order;
 
-typedef enum kgw_out_dtype { KGW_OUT_F32 = 0, KGW_OUT_BF16 = 1 } kgw_out_dtype;
+/* Output element type (section "BF16 contract": BF16, FP16 or FP32 outputs); FP32 accumulation,
+   one rounding to the output type (FP16 overflows to infinity beyond 65504). */
+typedef enum kgw_out_dtype { KGW_OUT_F32 = 0, KGW_OUT_BF16 = 1, KGW_OUT_F16 = 2 } kgw_out_dtype;
 
 typedef struct kgw_wgrad_args {
   int32_t num_experts;      /* E >= 1 (<= 4096)                                              */

@@ -230,13 +230,16 @@ def tolerance(S: np.ndarray, ref: np.ndarray, out_dtype: str, c_init=None) -> np
 
     FP32 output: 2e-5*S + 1e-6 (FP32 accumulation over the ragged token axis).
     Accumulate into FP32 adds one FP32 rounding of the sum: 2**-23*(|C| + |ref|).
-    BF16 output adds one final BF16 rounding: 2**-8*|ref|.
+    BF16 output adds one final BF16 rounding: 2**-8*|ref|; FP16 output one FP16 rounding:
+    2**-10*|ref| plus 2**-24 for the subnormal range.
     """
     tol = 2e-5 * S + 1e-6
     if c_init is not None:
         tol = tol + 2.0 ** -23 * (np.abs(np.asarray(c_init, dtype=np.float64)) + np.abs(ref))
     if out_dtype == "bf16":
         tol = tol + 2.0 ** -8 * np.abs(ref)
+    elif out_dtype == "f16":
+        tol = tol + 2.0 ** -10 * np.abs(ref) + 2.0 ** -24
     return tol
 
 

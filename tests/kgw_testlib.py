@@ -44,7 +44,7 @@ class Outputs:
 
     def __init__(self, w, device, c_init=None):
         self.w = w
-        dt = torch.bfloat16 if w.out_dtype == "bf16" else torch.float32
+        dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.out_dtype]
         E, H, I = w.num_experts, w.hidden, w.intermediate
         self.dtype = dt
         g = self.GUARD
@@ -80,7 +80,7 @@ def run_gpu(w, x, device="cuda", status=None, workspace=None, outputs=None):
     outs = outputs or Outputs(w, device, x.c)
     args = kgw.make_args(w.num_experts, w.hidden, w.intermediate, w.tokens_sum, x.a, x.b, x.offsets,
                          out=outs.dense, out_ptrs=outs.ptrs,
-                         out_dtype=kgw.KGW_OUT_BF16 if w.out_dtype == "bf16" else kgw.KGW_OUT_F32,
+                         out_dtype={"bf16": kgw.KGW_OUT_BF16, "f16": kgw.KGW_OUT_F16}.get(w.out_dtype, kgw.KGW_OUT_F32),
                          accumulate=w.accumulate,
                          input_order=kgw.KGW_RAGGED if w.input_order == "ragged" else kgw.KGW_TENSOR2D,
                          a_major=kgw.KGW_MN_MAJOR if w.a_major == "mn" else kgw.KGW_K_MAJOR,

@@ -551,3 +551,13 @@ def test_mn_major_a_is_the_transpose_in_memory():
         assert flat[k * H + m] == a[m, k]
     L = O.logical_a(bf16_bits(a_store), H, np.array([T]), "tensor2d", "mn")
     assert np.array_equal(L, bf16_bits(a).reshape(H, T))
+
+
+def test_f16_rounding_of_reference_is_within_tolerance():
+    a, b, offsets = _case(32, [256, 512])
+    H, I = a.shape[0], b.shape[1]
+    ref, S = O.wgrad_from_storage(bf16_bits(a), bf16_bits(b), offsets, H, I)
+    rounded = torch.from_numpy(ref).to(torch.float32).to(torch.float16).to(torch.float64).numpy()
+    assert np.all(np.abs(rounded - ref) <= O.tolerance(S, ref, "f16"))
+    # FP16 keeps 3 more mantissa bits than BF16: its bound is tighter
+    assert np.all(O.tolerance(S, ref, "f16") <= O.tolerance(S, ref, "bf16") + 2.0 ** -24)

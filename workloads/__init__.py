@@ -83,7 +83,7 @@ class Workload:
     seed: int
     a_std: float = 1.0
     b_std: float = 1.0
-    out_dtype: str = "f32"          # "f32" | "bf16"
+    out_dtype: str = "f32"          # "f32" | "bf16" | "f16"
     accumulate: bool = False
     c_std: float = 1.0              # pre-filled output ~ N(0, c_std) when accumulating
     input_order: str = "tensor2d"   # "tensor2d" | "ragged"
@@ -169,6 +169,10 @@ class Inputs:
     sfa: Optional[torch.Tensor] = None
     sfb: Optional[torch.Tensor] = None
     c: Optional[torch.Tensor] = None
+
+
+def out_torch_dtype(name: str) -> torch.dtype:
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[name]
 
 
 def _normal(gen: torch.Generator, shape, std: float) -> torch.Tensor:
@@ -259,7 +263,7 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
     a_store, b_store = store_operands(w, a_store, b_store)
     c = None
     if w.accumulate:
-        c = _normal(gen, (E, H, I), w.c_std).to(torch.bfloat16 if w.out_dtype == "bf16" else torch.float32)
+        c = _normal(gen, (E, H, I), w.c_std).to(out_torch_dtype(w.out_dtype))
     offsets = torch.from_numpy(w.offsets.astype(np.int32))
     to = lambda t: None if t is None else t.to(device)
     return Inputs(to(a_store), to(b_store), to(offsets), to(sfa), to(sfb), to(c))
@@ -286,7 +290,6 @@ def make_inputs_device(w: Workload, device) -> Inputs:
     a = normal((H, T), w.a_std, torch.bfloat16)
     b = normal((T, I), w.b_std, torch.bfloat16)
     a, b = store_operands(w, a, b)
-    c = normal((E, H, I), w.c_std, torch.bfloat16 if w.out_dtype == "bf16" else torch.float32) \
-        if w.accumulate else None
+    c = normal((E, H, I), w.c_std, out_torch_dtype(w.out_dtype)) if w.accumulate else None
     offsets = torch.from_numpy(w.offsets.astype(np.int32)).to(device)
     return Inputs(a, b, offsets, None, None, c)
