@@ -15,6 +15,7 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_debug_set(key, value) -> int
   kgw_wgrad_bf16_noalloc(args, stream=None)
   kgw_debug_check_ragged_maps(args, is_fp8, host_offsets, workspace) -> int
+  kgw_wgrad_fp8_ue8m0(args, sfa_packed, sfb_packed, workspace, stream=None)
 
 ``make_args`` builds the argument struct from torch tensors.
 """
@@ -49,7 +50,7 @@ KGW_OUT_F16 = 2
 
 EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
             "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc",
-            "kgw_debug_check_ragged_maps")
+            "kgw_debug_check_ragged_maps", "kgw_wgrad_fp8_ue8m0")
 
 
 class KgwArgs(ctypes.Structure):
@@ -96,6 +97,9 @@ def lib() -> ctypes.CDLL:
         L.kgw_wgrad_fp8_blockscaled.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.kgw_wgrad_fp8_blockscaled.restype = ctypes.c_int
+        L.kgw_wgrad_fp8_ue8m0.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_wgrad_fp8_ue8m0.restype = ctypes.c_int
         L.kgw_status_string.argtypes = [ctypes.c_int32]
         L.kgw_status_string.restype = ctypes.c_char_p
         L.kgw_version.argtypes = []
@@ -174,6 +178,16 @@ def kgw_wgrad_fp8_blockscaled(args: KgwArgs, sfa, sfb, workspace, workspace_byte
                                          _stream_handle(stream))
     if check and rc != KGW_OK:
         raise KgwError(rc, "kgw_wgrad_fp8_blockscaled")
+    return rc
+
+
+def kgw_wgrad_fp8_ue8m0(args: KgwArgs, sfa_packed, sfb_packed, workspace, workspace_bytes: Optional[int] = None,
+                        stream=None, check: bool = True) -> int:
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_wgrad_fp8_ue8m0(ctypes.byref(args), _ptr(sfa_packed), _ptr(sfb_packed), _ptr(workspace), nbytes,
+                                   _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_fp8_ue8m0")
     return rc
 
 

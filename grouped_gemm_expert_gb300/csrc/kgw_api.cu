@@ -282,10 +282,11 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
 }
 
 kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws, size_t ws_bytes,
-               void* stream) {
+               void* stream, bool sf_packed = false) {
   Prepared P;
   kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P);
   if (st != KGW_OK) return st;
+  P.mp.sf_packed = sf_packed;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kgw::launch_plan(P.pp, P.tpl, s) != cudaSuccess) return KGW_ERR_CUDA;
   cudaError_t e = fp8 ? kgw::launch_main_fp8(P.mp, P.tmA, P.tmB, P.grid, s)
@@ -349,6 +350,12 @@ kgw_status kgw_wgrad_bf16(const kgw_wgrad_args* args, void* workspace, size_t wo
 kgw_status kgw_wgrad_fp8_blockscaled(const kgw_wgrad_args* args, const float* sfa, const float* sfb,
                                      void* workspace, size_t workspace_bytes, void* stream) {
   return run(args, true, sfa, sfb, workspace, workspace_bytes, stream);
+}
+
+kgw_status kgw_wgrad_fp8_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return run(args, true, reinterpret_cast<const float*>(sfa_packed), reinterpret_cast<const float*>(sfb_packed),
+             workspace, workspace_bytes, stream, true);
 }
 
 kgw_status kgw_wgrad_bf16_noalloc(const kgw_wgrad_args* args, void* stream) {

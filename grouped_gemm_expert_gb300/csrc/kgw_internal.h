@@ -133,8 +133,9 @@ struct MainParams {
   int32_t a_kmajor, b_kmajor;   // operand storage orders (1: token axis has unit stride)
   int32_t num_m_tiles, num_n_tiles;
   int32_t tile_m;               // 128 (one CTA per tile) or 256 (a CTA pair per tile)
-  const float* sfa;             // FP8: [tokens_sum/128, H]
+  const float* sfa;             // FP8: [tokens_sum/128, H] FP32 (or packed UE8M0 words)
   const float* sfb;             // FP8: [tokens_sum/128, I]
+  int32_t sf_packed;            // FP8 scales given as packed UE8M0 words (4 x 32-token blocks)
   int32_t* status_dev;
   uint8_t* ws;
   WsLayout L;

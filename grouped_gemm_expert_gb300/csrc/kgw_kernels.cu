@@ -310,6 +310,14 @@ size_t main_smem_bytes(bool pair, bool fp8) {
   return ring + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
 }
 
+// Does any byte of these four words equal 0xFF (the UE8M0 NaN encoding)?
+__device__ __forceinline__ bool has_ue8m0_nan(uint4 v) {
+  auto ff = [](uint32_t w) {
+    return (w & 0xFFu) == 0xFFu || (w & 0xFF00u) == 0xFF00u || (w & 0xFF0000u) == 0xFF0000u || (w >> 24) == 0xFFu;
+  };
+  return ff(v.x) || ff(v.y) || ff(v.z) || ff(v.w);
+}
+
 // UE8M0 scale-factor byte of a power-of-two FP32 scale, replicated to the 4 bytes of a TMEM
 // column (one byte per 32-token block of the 128-token scale block). Flags non-powers of two.
 __device__ __forceinline__ uint32_t ue8m0_x4(float s, bool& bad) {
@@ -630,6 +638,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       // (one atom = bk x 128 B, LBO between atoms), 8-row K groups 1024 B apart, K step of
       // 16 (BF16) / 32 (FP8) rows = 2048 / 4096 bytes.
       constexpr uint32_t kMnStep = kFp8 ? 4096u : 2048u;
+      // FP32 per-128 scales repeat one byte in all 4 positions: keep byte 0 for every MMA
+      const uint32_t sf_sel = p.sf_packed ? 0xFFFFFFFFu : 0u;
       const uint32_t mn_lbo = static_cast<uint32_t>(bk) * 128u;
       // descriptor = template (offsets, swizzle, version) + start address / 16 in the low 14 bits;
       // the start address advances by the K step for each of the 4 MMAs of a stage
@@ -678,8 +688,9 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             for (int blk = 0; blk < 3; ++blk)
               tmem_cp_32x128b_warpx4(sfa + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_mxf8(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc, sfa, sfb,
+            for (int k = 0; k < 4; ++k)  // packed scales: MMA k uses byte k (its 32-token block)
+              mma_mxf8(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k),
+                       idesc | (idesc_sf_id(static_cast<uint32_t>(k)) & sf_sel), sfa, sfb,
                        (kb > it.kbeg || k > 0) ? 1u : 0u);
           } else {
 #pragma unroll
@@ -884,12 +895,30 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           const float* sb = sa + BM;
           uint4* ue = reinterpret_cast<uint4*>(sS + SF_UE8_OFFSET);
           bool bad = false;
-          ue[lane] = make_uint4(ue8m0_x4(sa[lane], bad), ue8m0_x4(sa[32 + lane], bad), ue8m0_x4(sa[64 + lane], bad),
-                                ue8m0_x4(sa[96 + lane], bad));
-          ue[32 + lane] = make_uint4(ue8m0_x4(sb[lane], bad), ue8m0_x4(sb[32 + lane], bad),
-                                     ue8m0_x4(sb[64 + lane], bad), ue8m0_x4(sb[96 + lane], bad));
-          ue[64 + lane] = make_uint4(ue8m0_x4(sb[128 + lane], bad), ue8m0_x4(sb[160 + lane], bad),
-                                     ue8m0_x4(sb[192 + lane], bad), ue8m0_x4(sb[224 + lane], bad));
+          if (!p.sf_packed) {
+            // FP32 powers of two -> one UE8M0 byte repeated in the 4 bytes of the word
+            ue[lane] = make_uint4(ue8m0_x4(sa[lane], bad), ue8m0_x4(sa[32 + lane], bad),
+                                  ue8m0_x4(sa[64 + lane], bad), ue8m0_x4(sa[96 + lane], bad));
+            ue[32 + lane] = make_uint4(ue8m0_x4(sb[lane], bad), ue8m0_x4(sb[32 + lane], bad),
+                                       ue8m0_x4(sb[64 + lane], bad), ue8m0_x4(sb[96 + lane], bad));
+            ue[64 + lane] = make_uint4(ue8m0_x4(sb[128 + lane], bad), ue8m0_x4(sb[160 + lane], bad),
+                                       ue8m0_x4(sb[192 + lane], bad), ue8m0_x4(sb[224 + lane], bad));
+          } else {
+            // packed UE8M0 words (one byte per 32-token block) are already in the TMEM word form
+            const uint32_t* wa = reinterpret_cast<const uint32_t*>(sa);
+            const uint32_t* wb = reinterpret_cast<const uint32_t*>(sb);
+            const uint4 x = make_uint4(wa[lane], wa[32 + lane], wa[64 + lane], wa[96 + lane]);
+            const uint4 y = make_uint4(wb[lane], wb[32 + lane], wb[64 + lane], wb[96 + lane]);
+            const uint4 z = make_uint4(wb[128 + lane], wb[160 + lane], wb[192 + lane], wb[224 + lane]);
+            ue[lane] = x;
+            ue[32 + lane] = y;
+            ue[64 + lane] = z;
+            // the byte 0xFF encodes NaN: report it
+            const uint32_t all = x.x & x.y & x.z & x.w & y.x & y.y & y.z & y.w & z.x & z.y & z.z & z.w;
+            if ((all & 0xFFu) == 0xFFu || (all & 0xFF00u) == 0xFF00u || (all & 0xFF0000u) == 0xFF0000u ||
+                (all >> 24) == 0xFFu)
+              bad = bad || has_ue8m0_nan(x) || has_ue8m0_nan(y) || has_ue8m0_nan(z);
+          }
           if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
           fence_proxy_async_smem();
           __syncwarp();

@@ -375,6 +375,9 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32
          (sf_id << 29);
 }
 
+// Scale-factor byte selector of the block-scaled instruction descriptor (A: bits 29-30, B: 4-5).
+__host__ __device__ constexpr uint32_t idesc_sf_id(uint32_t id) { return (id << 4) | (id << 29); }
+
 // ------------------------------------------------------------------------------------------
 // Misc
 // ------------------------------------------------------------------------------------------

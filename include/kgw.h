@@ -50,7 +50,8 @@ typedef enum kgw_status {
   KGW_ERR_OUT_PTRS = 9,      /* device-detected: an out_ptrs[e] is null or not 16-byte aligned */
   KGW_ERR_SCRATCH_LIMIT = 10, /* kgw_wgrad_bf16_noalloc: the call exceeds its static scratch limits */
   KGW_ERR_SCALES = 11        /* device-detected: an FP8 scale is not a positive power of two in
-                                [2^-127, 2^127] (the output of that call is meaningless) */
+                                [2^-127, 2^127], or a packed UE8M0 byte is 0xFF (the output of that
+                                call is meaningless) */
 } kgw_status;
 
 /* Storage order of an operand ("Grouped GEMM + WGrad (Unified)", section "BF16 contract"). */
@@ -125,6 +126,19 @@ kgw_status kgw_wgrad_bf16(const kgw_wgrad_args* args, void* workspace, size_t wo
  */
 kgw_status kgw_wgrad_fp8_blockscaled(const kgw_wgrad_args* args, const float* sfa, const float* sfb,
                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * FP8 variant with packed UE8M0 scales of 32-token granularity ("05 · Grouped GEMM 与 Expert 计算",
+ * section 3: UE8M0 scale format, MN-major TMA-aligned scale tensors; "How to Use K-Grouped GEMM for
+ * MoE Weight Backward Pass in DeepGEMM", step 2: gran_k = 32 with packed UE8M0). a, b: e4m3 as in
+ * kgw_wgrad_fp8_blockscaled. sfa_packed: int32 [tokens_sum/128, hidden], sfb_packed: int32
+ * [tokens_sum/128, intermediate]; byte j (least significant first) of sfa_packed[kb][m] is the
+ * biased exponent e of the scale 2^(e-127) of A[m, 128*kb + 32*j : 128*kb + 32*j + 32] (likewise
+ * for B and column n). The byte 0xFF (NaN) is reported as KGW_ERR_SCALES. Each 32-token block's
+ * scale is applied to its products before FP32 accumulation.
+ */
+kgw_status kgw_wgrad_fp8_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * kgw_wgrad_bf16 without a workspace argument and without any device allocation.

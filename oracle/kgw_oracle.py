@@ -163,6 +163,39 @@ def apply_block_scales_cols(x: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return x * np.repeat(s, SCALE_BLOCK, axis=0)
 
 
+def unpack_ue8m0_32(packed) -> np.ndarray:
+    """Packed UE8M0 words [tokens/128, other] -> float64 scales [tokens/32, other].
+
+    Byte j (least significant first) of word [kb][r] is the biased exponent e of the scale
+    2**(e - 127) of tokens 128*kb + 32*j .. +32 ("05 · Grouped GEMM 与 Expert 计算", section 3:
+    UE8M0 scale format; "How to Use K-Grouped GEMM ...", step 2: gran_k = 32, packed UE8M0).
+    """
+    w = np.asarray(packed).view(np.uint32)
+    nb, other = w.shape
+    out = np.empty((nb * 4, other), dtype=np.float64)
+    for j in range(4):
+        e = ((w >> (8 * j)) & 0xFF).astype(np.int64)
+        out[j::4, :] = np.ldexp(1.0, e - 127)
+    return out
+
+
+def apply_scales_rows(x: np.ndarray, scales: np.ndarray, block: int) -> np.ndarray:
+    """x [rows, tokens] * s[k // block, m] for scales [tokens/block, rows]."""
+    return x * np.repeat(np.asarray(scales, dtype=np.float64).T, block, axis=1)
+
+
+def apply_scales_cols(x: np.ndarray, scales: np.ndarray, block: int) -> np.ndarray:
+    """x [tokens, cols] * s[k // block, n] for scales [tokens/block, cols]."""
+    return x * np.repeat(np.asarray(scales, dtype=np.float64), block, axis=0)
+
+
+def decode_scales(sf, sf_format: str):
+    """(scales as float64 [tokens/block, other], block) for either scale format."""
+    if sf_format == "ue8m0_32":
+        return unpack_ue8m0_32(sf), 32
+    return np.asarray(sf, dtype=np.float64), SCALE_BLOCK
+
+
 # ---------------------------------------------------------------------------------------------
 # The operation
 # ---------------------------------------------------------------------------------------------
@@ -197,7 +230,7 @@ def wgrad(A: np.ndarray, B: np.ndarray, offsets, c_init=None, accumulate: bool =
 def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, *,
                        input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
                        c_init=None, accumulate: bool = False, with_bound: bool = True,
-                       a_major: str = "k", b_major: str = "mn"):
+                       a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128"):
     """Decode stored operands (raw bits) and evaluate the operation in float64.
 
     a_bits/b_bits: uint16 (bf16) or uint8 (e4m3) numpy arrays as stored.
@@ -208,8 +241,10 @@ def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, 
     A = logical_a(dec(a_bits), hidden, offsets, input_order, a_major)
     B = logical_b(dec(b_bits), intermediate, offsets, input_order, b_major)
     if fp8:
-        A = apply_block_scales_rows(A, sfa)
-        B = apply_block_scales_cols(B, sfb)
+        sa, blk = decode_scales(sfa, sf_format)
+        sb, _ = decode_scales(sfb, sf_format)
+        A = apply_scales_rows(A, sa, blk)
+        B = apply_scales_cols(B, sb, blk)
     return wgrad(A, B, offsets, c_init=c_init, accumulate=accumulate, with_bound=with_bound)
 
 
@@ -245,7 +280,7 @@ def tolerance(S: np.ndarray, ref: np.ndarray, out_dtype: str, c_init=None) -> np
 
 def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, e: int, m: int, n: int, *,
                          input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
-                         a_major: str = "k", b_major: str = "mn"):
+                         a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128"):
     """R_e[m, n] and S_e[m, n] read straight from the stored operands (for sampled checks).
 
     Only row m of A_e and column n of B_e are decoded, so this works at full problem size.
@@ -273,7 +308,9 @@ def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int
     else:
         bcol = dec(flat_b[b * intermediate + n * cnt: b * intermediate + (n + 1) * cnt])
     if fp8:
-        ks = np.arange(b, end) // SCALE_BLOCK
-        arow = arow * np.asarray(sfa, dtype=np.float64)[ks, m]
-        bcol = bcol * np.asarray(sfb, dtype=np.float64)[ks, n]
+        sa, blk = decode_scales(sfa, sf_format)
+        sb, _ = decode_scales(sfb, sf_format)
+        ks = np.arange(b, end) // blk
+        arow = arow * sa[ks, m]
+        bcol = bcol * sb[ks, n]
     return float(np.dot(arow, bcol)), float(np.dot(np.abs(arow), np.abs(bcol)))

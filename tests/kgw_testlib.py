@@ -88,7 +88,9 @@ def run_gpu(w, x, device="cuda", status=None, workspace=None, outputs=None):
                          status_dev=status)
     if workspace is None:
         workspace = kgw.workspace_for(args, w.fp8, device=device)
-    if w.fp8:
+    if w.fp8 and w.sf_format == "ue8m0_32":
+        kgw.kgw_wgrad_fp8_ue8m0(args, x.sfa, x.sfb, workspace)
+    elif w.fp8:
         kgw.kgw_wgrad_fp8_blockscaled(args, x.sfa, x.sfb, workspace)
     else:
         kgw.kgw_wgrad_bf16(args, workspace)
@@ -103,7 +105,8 @@ def oracle_full(w, x_cpu):
                                 w.intermediate, input_order=w.input_order, fp8=w.fp8,
                                 sfa=None if x_cpu.sfa is None else x_cpu.sfa.numpy(),
                                 sfb=None if x_cpu.sfb is None else x_cpu.sfb.numpy(),
-                                c_init=c, accumulate=w.accumulate, a_major=w.a_major, b_major=w.b_major)
+                                c_init=c, accumulate=w.accumulate, a_major=w.a_major, b_major=w.b_major,
+                                sf_format=w.sf_format)
 
 
 def assert_close_to_oracle(w, got: np.ndarray, ref: np.ndarray, S: np.ndarray, c_init=None):

@@ -561,3 +561,56 @@ def test_f16_rounding_of_reference_is_within_tolerance():
     assert np.all(np.abs(rounded - ref) <= O.tolerance(S, ref, "f16"))
     # FP16 keeps 3 more mantissa bits than BF16: its bound is tighter
     assert np.all(O.tolerance(S, ref, "f16") <= O.tolerance(S, ref, "bf16") + 2.0 ** -24)
+
+
+
+# ------------------------------------------------------------------------------------------
+# Packed UE8M0 scales, 32-token granularity
+# ------------------------------------------------------------------------------------------
+
+def test_ue8m0_unpack_known_words():
+    w = np.array([[127 | (128 << 8) | (126 << 16) | (0 << 24)]], dtype=np.uint32).view(np.int32)
+    s = O.unpack_ue8m0_32(w)
+    assert s[:, 0].tolist() == [1.0, 2.0, 0.5, 2.0 ** -127]
+
+
+def test_ue8m0_each_32_token_block_has_its_own_scale():
+    """Ones x ones with block scales 2^(j) on A's 32-token block j: R = 32 * sum_j 2^j * sb_j."""
+    H, I, T = 2, 3, 128
+    qa = torch.ones(H, T).to(torch.float8_e4m3fn)
+    qb = torch.ones(T, I).to(torch.float8_e4m3fn)
+    wa = np.array([[127 | (128 << 8) | (129 << 16) | (130 << 24)] * H], dtype=np.uint32).view(np.int32)
+    wb = np.array([[127 | (127 << 8) | (127 << 16) | (131 << 24)] * I], dtype=np.uint32).view(np.int32)
+    r, _ = O.wgrad_from_storage(e4m3_bits(qa), e4m3_bits(qb), np.array([T]), H, I, fp8=True, sfa=wa, sfb=wb,
+                                sf_format="ue8m0_32")
+    expect = 32 * (1 * 1 + 2 * 1 + 4 * 1 + 8 * 16)
+    assert np.all(r[0] == expect)
+
+
+def test_ue8m0_equal_subblocks_match_fp32_per_128_scales():
+    g = torch.Generator().manual_seed(5)
+    H, I, T = 8, 16, 256
+    qa = (torch.randn(H, T, generator=g) * 4).to(torch.float8_e4m3fn)
+    qb = (torch.randn(T, I, generator=g) * 4).to(torch.float8_e4m3fn)
+    ka = np.random.default_rng(1).integers(-5, 6, size=(2, H))
+    kb = np.random.default_rng(2).integers(-5, 6, size=(2, I))
+    def pack(k):
+        b = (k + 127).astype(np.uint32)
+        return (b | (b << 8) | (b << 16) | (b << 24)).view(np.int32)
+    r32, _ = O.wgrad_from_storage(e4m3_bits(qa), e4m3_bits(qb), np.array([T]), H, I, fp8=True,
+                                  sfa=pack(ka), sfb=pack(kb), sf_format="ue8m0_32")
+    r128, _ = O.wgrad_from_storage(e4m3_bits(qa), e4m3_bits(qb), np.array([T]), H, I, fp8=True,
+                                   sfa=np.ldexp(1.0, ka).astype(np.float32), sfb=np.ldexp(1.0, kb).astype(np.float32))
+    assert np.array_equal(r32, r128)
+
+
+def test_ue8m0_quantiser_recipe():
+    g = torch.Generator().manual_seed(0)
+    x = torch.randn(4, 256, generator=g) * 3
+    q, packed = W.quantize_e4m3_ue8m0_32(x, token_axis=1)
+    s = O.unpack_ue8m0_32(packed.numpy())           # [8, 4]
+    dec = O.e4m3_to_f64(e4m3_bits(q))
+    assert np.all(np.abs(dec) <= 448)
+    recon = O.apply_scales_rows(dec, s, 32)
+    err = np.abs(recon - x.numpy().astype(np.float64))
+    assert np.all(err <= 2.0 ** -4 * np.abs(x.numpy()) + np.repeat(s.T, 32, axis=1) * 2.0 ** -10)

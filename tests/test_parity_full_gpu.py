@@ -49,7 +49,8 @@ def _check_full(w):
     bad = []
     for (e, m, n) in _samples(w, rng):
         r, s = O.element_from_storage(a_bits, b_bits, offsets, w.hidden, w.intermediate, e, m, n,
-                                      input_order=w.input_order, fp8=w.fp8, sfa=sfa, sfb=sfb)
+                                      input_order=w.input_order, fp8=w.fp8, sfa=sfa, sfb=sfb,
+                                      a_major=w.a_major, b_major=w.b_major, sf_format=w.sf_format)
         c = float(x_cpu.c[e, m, n].to(torch.float64)) if w.accumulate else 0.0
         ref = c + r
         got = float(outs.views[e][m, n].to(torch.float64).item())
@@ -82,3 +83,14 @@ def test_full_fp8_blockscaled():
     if not kgw.lib():
         pytest.fail("library missing")
     _check_full(W.fp8())
+
+
+def test_full_fp8_ue8m0_gran32():
+    import dataclasses
+    _check_full(dataclasses.replace(W.fp8(), sf_format="ue8m0_32"))
+
+
+def test_full_balanced_token_major_a():
+    """The balanced workload with A = dY^T read from dY stored token-major (M-major A)."""
+    import dataclasses
+    _check_full(dataclasses.replace(W.balanced(), a_major="mn"))

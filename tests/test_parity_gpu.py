@@ -79,6 +79,9 @@ CASES = {
     "f16_out_pair": W.custom(4, 512, 512, [768, 0, 1024, 256], seed=97, out_dtype="f16"),
     "f16_accumulate_single_split": W.custom(3, 384, 256, [8192, 0, 512], seed=98, out_dtype="f16", accumulate=True),
     "fp8_f16_out": W.custom(2, 256, 512, [512, 1280], seed=99, fp8=True, out_dtype="f16"),
+    "fp8_ue8m0_32": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=100, fp8=True, sf_format="ue8m0_32"),
+    "fp8_ue8m0_32_ragged_mn_a": W.custom(3, 384, 512, [1280, 256, 0], seed=101, fp8=True, sf_format="ue8m0_32",
+                                         input_order="ragged", a_major="mn", out_dtype="bf16"),
     "fp8_bf16_out": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=60, fp8=True, out_dtype="bf16"),
     "fp8_f32_ragged": W.custom(3, 384, 768, [256, 1280, 0], seed=61, fp8=True, input_order="ragged"),
     "fp8_split_k_accumulate": W.custom(3, 128, 256, [16384, 0, 256], seed=62, fp8=True, accumulate=True),

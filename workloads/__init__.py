@@ -90,6 +90,7 @@ class Workload:
     output_mode: str = "dense"      # "dense" | "discrete"
     fp8: bool = False
     a_major: str = "k"              # "k": A stored [hidden, tokens]; "mn": stored [tokens, hidden]
+    sf_format: str = "f32_128"      # FP8 scales: "f32_128" (FP32 per 128 tokens) | "ue8m0_32" (packed)
     b_major: str = "mn"             # "mn": B stored [tokens, intermediate]; "k": stored [intermediate, tokens]
 
     @property
@@ -160,7 +161,8 @@ class Inputs:
     With a_major "mn" A is stored [tokens_sum, hidden] (expert blocks [n_e, hidden] back to back
     in both orders); with b_major "k" B is stored [intermediate, tokens_sum] (tensor2d) or as
     per-expert [intermediate, n_e] blocks (ragged).
-    sfa/sfb (FP8 only): float32 [tokens_sum/128, hidden] / [tokens_sum/128, intermediate].
+    sfa/sfb (FP8 only): float32 [tokens_sum/128, hidden] / [tokens_sum/128, intermediate], or with
+       sf_format "ue8m0_32" int32 packed UE8M0 words of the same shapes.
     c: pre-filled output [E, hidden, intermediate] for accumulate mode, else None.
     """
     a: torch.Tensor
@@ -210,6 +212,28 @@ def quantize_e4m3_blocks(x: torch.Tensor, token_axis: int):
     return q.contiguous(), scale.t().contiguous()   # scales as [nblk, other]
 
 
+def quantize_e4m3_ue8m0_32(x: torch.Tensor, token_axis: int):
+    """Quantise ``x`` (float32 2-D) to e4m3 with one power-of-two scale per 32 tokens, returned as
+    packed UE8M0 words: int32 [tokens/128, other], byte j of word [kb][r] = 127 + log2(scale) of
+    tokens 128*kb + 32*j .. +32 of row/column r (scale = 2**ceil(log2(amax/448)), 1 for amax 0).
+    """
+    assert x.dim() == 2 and x.dtype == torch.float32
+    xt = x if token_axis == 1 else x.t()
+    other, tokens = xt.shape
+    assert tokens % FP8_BLOCK == 0
+    blocks = xt.reshape(other, tokens // 32, 32)
+    amax = blocks.abs().amax(dim=2)                       # [other, tokens/32]
+    k = pow2_scale_exponent(amax.numpy())
+    scale = torch.from_numpy(np.ldexp(np.ones_like(k, dtype=np.float64), k).astype(np.float32))
+    q = (blocks / scale.unsqueeze(2)).to(torch.float8_e4m3fn).reshape(other, tokens)
+    if token_axis == 0:
+        q = q.t().contiguous()
+    byte = (k + 127).astype(np.uint32).reshape(other, tokens // 128, 4)
+    words = (byte[..., 0] | (byte[..., 1] << 8) | (byte[..., 2] << 16) | (byte[..., 3] << 24)).astype(np.uint32)
+    packed = torch.from_numpy(words.view(np.int32).T.copy())   # [tokens/128, other]
+    return q.contiguous(), packed
+
+
 def pack_ragged_a(a2d: torch.Tensor, counts) -> torch.Tensor:
     """Re-store a logical [hidden, tokens_sum] A as per-expert K-contiguous blocks.
 
@@ -253,7 +277,10 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
     a32 = _normal(gen, (H, T), w.a_std)
     b32 = _normal(gen, (T, I), w.b_std)
     sfa = sfb = None
-    if w.fp8:
+    if w.fp8 and w.sf_format == "ue8m0_32":
+        a_store, sfa = quantize_e4m3_ue8m0_32(a32, token_axis=1)
+        b_store, sfb = quantize_e4m3_ue8m0_32(b32, token_axis=0)
+    elif w.fp8:
         a_store, sfa = quantize_e4m3_blocks(a32, token_axis=1)
         b_store, sfb = quantize_e4m3_blocks(b32, token_axis=0)
     else:
