@@ -11,6 +11,9 @@ round_to_256(4096*U(0.7,1.3)) (seed 1), FP32 dense output, overwrite. Its workin
 Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on the host cores
 instead (a bounded sample of the same workload per step).
 
+``--workload mg_forward|mg_dgrad|mg_masked`` times the M-grouped GEMM instead (forward / dgrad
+of the same MoE layer, and the masked decode layout): TFLOP/s counting 2*N*K*(valid rows).
+
 Multi-GPU (torchrun): every rank runs its own replica of the workload (experts are
 independent; there is no data-path exchange), timing is the max over ranks: weak scaling.
 """
@@ -33,6 +36,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import workloads as W  # noqa: E402
+import workloads.mgrouped as MW  # noqa: E402
 
 KERNEL_SOURCES = ["grouped_gemm_expert_gb300/csrc/kgw_kernels.cu", "grouped_gemm_expert_gb300/csrc/kgw_ptx.cuh",
                   "grouped_gemm_expert_gb300/csrc/kgw_internal.h"]
@@ -304,6 +308,188 @@ def run_ours(args, w, rank, local, world):
     return ms_per_step, per_launch_ms, e2e_ms, h2d, d2h, clk
 
 
+def mg_algorithmic_bytes(w) -> int:
+    """A's valid rows, every non-empty group's weight, and D's valid rows (read too if accumulating)."""
+    counts = np.asarray(w.counts)
+    osz = {"f32": 4, "bf16": 2, "f16": 2}[w.out_dtype]
+    rows = int(counts.sum())
+    return int(rows * w.k * 2 + int((counts > 0).sum()) * w.n * w.k * 2 + rows * w.n * osz * (2 if w.accumulate else 1))
+
+
+def run_ours_mg(args, w, rank, local, world):
+    """Device-timed steps and the end-to-end leg for an M-grouped workload."""
+    import dataclasses
+
+    import grouped_gemm_expert_gb300 as kgw
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = MW.make_mg_inputs(dataclasses.replace(w, seed=w.seed + 1000 * rank), dev, on_device_rng=True)
+    odt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w.out_dtype]
+    d_shape = (w.num_groups, w.max_m, w.n) if w.layout == "masked" else (w.rows, w.n)
+    d = torch.zeros(d_shape, dtype=odt, device=dev) if x.d0 is None else x.d0.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    lay = {"offsets": kgw.KGW_MG_OFFSETS, "indices": kgw.KGW_MG_INDICES, "masked": kgw.KGW_MG_MASKED}[w.layout]
+    mk = lambda a, b, g, dd: kgw.make_mgrouped_args(
+        w.num_groups, w.m, w.n, w.k, a, b, g, dd, layout=lay,
+        b_major=kgw.KGW_K_MAJOR if w.b_major == "k" else kgw.KGW_MN_MAJOR,
+        out_dtype={"f32": kgw.KGW_OUT_F32, "bf16": kgw.KGW_OUT_BF16, "f16": kgw.KGW_OUT_F16}[w.out_dtype],
+        accumulate=w.accumulate, status_dev=status)
+    kargs = mk(x.a, x.b, x.groups, d)
+    ws = torch.empty(kgw.kgw_mgrouped_workspace_size(kargs), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    # the masked decode workload (~0.3 GB) fits in L2: flush it between steps with a 256 MB write
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if w.layout == "masked" else None
+
+    def step():
+        if flush is not None:
+            flush.fill_(1)
+        kgw.kgw_mgrouped_bf16(kargs, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {kgw.kgw_status_string(int(status.item()))}")
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(1)
+        starts[i].record(stream)
+        kgw.kgw_mgrouped_bf16(kargs, ws, stream=stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # a step is the call; the L2 flush between calls is not part of it
+    ms_per_step = max_over_ranks(statistics.mean(per_launch_ms), world, dev)
+    if args.no_e2e:
+        return ms_per_step, per_launch_ms, None, 0, 0, clk
+    # end to end: inputs from pinned host memory, the call, D back to pinned host memory (serial)
+    host_in = [t.cpu().pin_memory() for t in (x.a, x.b, x.groups)]
+    host_d0 = None if x.d0 is None else x.d0.cpu().pin_memory()
+    d_in = [torch.empty_like(t, device=dev) for t in host_in]
+    d_out = torch.empty_like(d)
+    h_out = torch.empty(d.shape, dtype=odt).pin_memory()
+    ea = mk(d_in[0], d_in[1], d_in[2], d_out)
+    h2d = sum(t.numel() * t.element_size() for t in host_in) + (0 if host_d0 is None else host_d0.numel() * host_d0.element_size())
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for dd, h in zip(d_in, host_in):
+            dd.copy_(h, non_blocking=True)
+        if host_d0 is not None:
+            d_out.copy_(host_d0, non_blocking=True)
+        kgw.kgw_mgrouped_bf16(ea, ws, stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n = max(3, min(args.steps, 8))
+    e0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n, world, dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {kgw.kgw_status_string(int(status.item()))}")
+    return ms_per_step, per_launch_ms, e2e_ms, h2d, d2h, clk
+
+
+def cpu_oracle_rate_mg(w, budget_s: float):
+    """Time the float64 M-grouped oracle over whole groups until ``budget_s`` is spent."""
+    import oracle.kgw_oracle as O
+    import oracle.mgrouped_oracle as MO
+
+    x = MW.make_mg_inputs(w, "cpu")
+    A = O.bf16_to_f64(x.a.contiguous().view(torch.int16).numpy().view(np.uint16)).reshape(-1, w.k)
+    B = O.bf16_to_f64(x.b.contiguous().view(torch.int16).numpy().view(np.uint16))
+    groups = x.groups.numpy()
+    per_group = [(g, r) for g, r in enumerate(MO.group_rows(w.layout, groups, w.m, w.num_groups)) if len(r)]
+    flops, done = 0.0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        for g, r in per_group:
+            # one group at a time through the oracle's own entry point (a single-group problem)
+            MO.mgrouped(A[r], B[g:g + 1], "offsets", [len(r)], len(r), b_major=w.b_major, with_bound=False)
+            flops += 2.0 * len(r) * w.n * w.k
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, done
+
+
+def main_mg(args, world, rank, local):
+    w = MW.MG_NAMED[args.workload]()
+    flops = w.flops
+    metric = "M-grouped GEMM TFLOP/s (2*N*K*valid rows)"
+    config = {"workload": w.name, "groups": w.num_groups, "layout": w.layout, "m": w.m, "n": w.n, "k": w.k,
+              "valid_rows": w.valid_rows, "b_major": w.b_major, "output": w.out_dtype, "accumulate": w.accumulate,
+              "l2": "L2 flushed (256 MB write) between steps" if w.layout == "masked"
+              else "inputs larger than L2 (no flush needed)", "parallelism": f"replica x{args.gpus}"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        budget = max(2.0, min(15.0, 120.0 / max(1, args.steps + args.warmup)))
+        rates = []
+        for i in range(args.warmup + args.steps):
+            r, dt, done = cpu_oracle_rate_mg(w, budget)
+            if i >= args.warmup:
+                rates.append((r, dt, done))
+        val = statistics.median(r for r, _, _ in rates)
+        ms = statistics.median(dt for _, dt, _ in rates) * 1e3
+        print(json.dumps({"impl": "reference", "metric": metric, "value": val, "unit": "TFLOP/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": config,
+                          "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                                           "sample": f"float64 oracle over whole groups, {ms / 1e3:.1f} s per step"},
+                          "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    ms_per_step, per_launch, e2e_ms, h2d, d2h, clk = run_ours_mg(args, w, rank, local, world)
+    value = job_throughput(flops, ms_per_step, world)
+    peaks = measured_peaks()
+    launch_ms = statistics.mean(per_launch)
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    abytes = mg_algorithmic_bytes(w)
+    line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": traffic_record(args.workload),
+                         "algorithmic_bytes": abytes,
+                         "hbm_gbs_at_algorithmic_bytes": abytes / (launch_ms * 1e-3) / 1e9,
+                         "peak_source": f"{peaks['source']} bf16 burst",
+                         "kernel": "wgrad_kernel M-grouped instantiation (+ plan_mgrouped_kernel)"},
+            "e2e": None if e2e_ms is None else {"value": job_throughput(flops, e2e_ms, world), "unit": "TFLOP/s",
+                                                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps, "clocks": clk}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, dt, done = cpu_oracle_rate_mg(w, args.cpu_budget)
+        line["cpu_baseline"] = {"value": r, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"float64 oracle, {done} whole-group products of the same workload, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def cpu_oracle_rate(w, budget_s: float):
     """Time the float64 oracle on the host cores over whole experts until ``budget_s`` is spent."""
     import oracle.kgw_oracle as O
@@ -349,7 +535,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="balanced", choices=sorted(W.NAMED))
+    ap.add_argument("--workload", default="balanced", choices=sorted(W.NAMED) + sorted(MW.MG_NAMED))
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
@@ -357,6 +543,9 @@ def main():
     args.warmup = max(args.warmup, 3)
 
     world, rank, local = dist_env()
+    if args.workload in MW.MG_NAMED:
+        main_mg(args, world, rank, local)
+        return
     w = W.NAMED[args.workload]()
     flops = w.flops
     config = {"workload": w.name, "experts": w.num_experts, "hidden": w.hidden, "intermediate": w.intermediate,

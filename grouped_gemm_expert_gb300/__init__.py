@@ -16,8 +16,10 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_wgrad_bf16_noalloc(args, stream=None)
   kgw_debug_check_ragged_maps(args, is_fp8, host_offsets, workspace) -> int
   kgw_wgrad_fp8_ue8m0(args, sfa_packed, sfb_packed, workspace, stream=None)
+  kgw_mgrouped_workspace_size(args) -> int
+  kgw_mgrouped_bf16(args, workspace, stream=None)
 
-``make_args`` builds the argument struct from torch tensors.
+``make_args`` / ``make_mgrouped_args`` build the argument structs from torch tensors.
 """
 from __future__ import annotations
 
@@ -47,10 +49,14 @@ KGW_RAGGED = 1
 KGW_OUT_F32 = 0
 KGW_OUT_BF16 = 1
 KGW_OUT_F16 = 2
+KGW_MG_OFFSETS = 0
+KGW_MG_INDICES = 1
+KGW_MG_MASKED = 2
 
 EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
             "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc",
-            "kgw_debug_check_ragged_maps", "kgw_wgrad_fp8_ue8m0")
+            "kgw_debug_check_ragged_maps", "kgw_wgrad_fp8_ue8m0", "kgw_mgrouped_workspace_size",
+            "kgw_mgrouped_bf16")
 
 
 class KgwArgs(ctypes.Structure):
@@ -68,6 +74,25 @@ class KgwArgs(ctypes.Structure):
         ("input_order", ctypes.c_int32),
         ("out", ctypes.c_void_p),
         ("out_ptrs", ctypes.c_void_p),
+        ("out_dtype", ctypes.c_int32),
+        ("accumulate", ctypes.c_int32),
+        ("status_dev", ctypes.c_void_p),
+    ]
+
+
+class KgwMgroupedArgs(ctypes.Structure):
+    """Mirror of ``kgw_mgrouped_args`` (include/kgw.h)."""
+    _fields_ = [
+        ("num_groups", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
+        ("m", ctypes.c_int64),
+        ("n", ctypes.c_int32),
+        ("k", ctypes.c_int32),
+        ("a", ctypes.c_void_p),
+        ("b", ctypes.c_void_p),
+        ("b_major", ctypes.c_int32),
+        ("groups", ctypes.c_void_p),
+        ("d", ctypes.c_void_p),
         ("out_dtype", ctypes.c_int32),
         ("accumulate", ctypes.c_int32),
         ("status_dev", ctypes.c_void_p),
@@ -100,6 +125,11 @@ def lib() -> ctypes.CDLL:
         L.kgw_wgrad_fp8_ue8m0.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.kgw_wgrad_fp8_ue8m0.restype = ctypes.c_int
+        L.kgw_mgrouped_workspace_size.argtypes = [ctypes.POINTER(KgwMgroupedArgs), ctypes.POINTER(ctypes.c_size_t)]
+        L.kgw_mgrouped_workspace_size.restype = ctypes.c_int
+        L.kgw_mgrouped_bf16.argtypes = [ctypes.POINTER(KgwMgroupedArgs), ctypes.c_void_p, ctypes.c_size_t,
+                                        ctypes.c_void_p]
+        L.kgw_mgrouped_bf16.restype = ctypes.c_int
         L.kgw_status_string.argtypes = [ctypes.c_int32]
         L.kgw_status_string.restype = ctypes.c_char_p
         L.kgw_version.argtypes = []
@@ -131,6 +161,14 @@ def make_args(num_experts: int, hidden: int, intermediate: int, tokens_sum: int,
     return KgwArgs(num_experts, hidden, intermediate, tokens_sum, _ptr(a), a_major, _ptr(b), b_major,
                    _ptr(offsets), input_order, _ptr(out), _ptr(out_ptrs), out_dtype, int(bool(accumulate)),
                    _ptr(status_dev))
+
+
+def make_mgrouped_args(num_groups: int, m: int, n: int, k: int, a, b, groups, d, *,
+                       layout: int = KGW_MG_OFFSETS, b_major: int = KGW_K_MAJOR, out_dtype: int = KGW_OUT_BF16,
+                       accumulate: bool = False, status_dev=None) -> KgwMgroupedArgs:
+    """Build ``kgw_mgrouped_args``; tensors (or raw integer addresses) are passed by address."""
+    return KgwMgroupedArgs(num_groups, layout, m, n, k, _ptr(a), _ptr(b), b_major, _ptr(groups), _ptr(d),
+                           out_dtype, int(bool(accumulate)), _ptr(status_dev))
 
 
 def _stream_handle(stream) -> Optional[int]:
@@ -191,6 +229,23 @@ def kgw_wgrad_fp8_ue8m0(args: KgwArgs, sfa_packed, sfb_packed, workspace, worksp
     return rc
 
 
+def kgw_mgrouped_workspace_size(args: KgwMgroupedArgs) -> int:
+    n = ctypes.c_size_t(0)
+    rc = lib().kgw_mgrouped_workspace_size(ctypes.byref(args), ctypes.byref(n))
+    if rc != KGW_OK:
+        raise KgwError(rc, "kgw_mgrouped_workspace_size")
+    return int(n.value)
+
+
+def kgw_mgrouped_bf16(args: KgwMgroupedArgs, workspace, workspace_bytes: Optional[int] = None, stream=None,
+                      check: bool = True) -> int:
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_mgrouped_bf16(ctypes.byref(args), _ptr(workspace), nbytes, _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_mgrouped_bf16")
+    return rc
+
+
 def kgw_wgrad_bf16_noalloc(args: KgwArgs, stream=None, check: bool = True) -> int:
     """kgw_wgrad_bf16 using the library's static 2 MiB scratch instead of a workspace.
 
@@ -248,3 +303,32 @@ def wgrad(a, b, offsets, *, hidden: int, intermediate: int, out=None, out_ptrs=N
     else:
         kgw_wgrad_bf16(args, workspace, stream=stream)
     return out
+
+
+def mgrouped(a, b, groups, *, layout: str = "offsets", d=None, b_major: str = "k", out_dtype: str = "bf16",
+             accumulate: bool = False, workspace=None, status_dev=None, stream=None):
+    """M-grouped GEMM on torch CUDA tensors: D[rows of g] (+)= A[rows of g] @ op(B[g]).
+
+    ``a`` bf16 [m, k] (contiguous layouts) or [G, max_m, k] (``layout="masked"``); ``b`` bf16
+    [G, n, k] (``b_major="k"``, op = transpose) or [G, k, n] (``b_major="mn"``); ``groups`` int32:
+    cumulative row counts [G] (``"offsets"``), per-row group ids [m] (``"indices"``) or valid rows
+    per group [G] (``"masked"``). Returns ``d``.
+    """
+    import torch
+    G = int(b.shape[0])
+    k = int(a.shape[-1])
+    m = int(a.shape[1] if layout == "masked" else a.shape[0])
+    n = int(b.shape[1] if b_major == "k" else b.shape[2])
+    lay = {"offsets": KGW_MG_OFFSETS, "indices": KGW_MG_INDICES, "masked": KGW_MG_MASKED}[layout]
+    odt = {"bf16": KGW_OUT_BF16, "f16": KGW_OUT_F16, "f32": KGW_OUT_F32}[out_dtype]
+    if d is None:
+        shape = (G, m, n) if layout == "masked" else (m, n)
+        d = torch.zeros(shape, dtype={"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[out_dtype],
+                        device=a.device)
+    args = make_mgrouped_args(G, m, n, k, a, b, groups, d, layout=lay,
+                              b_major=KGW_K_MAJOR if b_major == "k" else KGW_MN_MAJOR, out_dtype=odt,
+                              accumulate=accumulate, status_dev=status_dev)
+    if workspace is None:
+        workspace = torch.empty(kgw_mgrouped_workspace_size(args), dtype=torch.uint8, device=a.device)
+    kgw_mgrouped_bf16(args, workspace, stream=stream)
+    return d

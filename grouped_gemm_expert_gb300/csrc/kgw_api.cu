@@ -330,6 +330,100 @@ kgw_status noalloc_scratch(void** out) {
   return KGW_OK;
 }
 
+// Rows of A (and D) and the largest tile-table size of an M-grouped call.
+int64_t mg_rows(const kgw_mgrouped_args* a) {
+  return a->layout == KGW_MG_MASKED ? int64_t(a->num_groups) * a->m : a->m;
+}
+int64_t mg_max_tiles(const kgw_mgrouped_args* a) {
+  return a->layout == KGW_MG_MASKED ? int64_t(a->num_groups) * ((a->m + kgw::BM - 1) / kgw::BM) : a->m / kgw::BM;
+}
+
+kgw_status validate_mg(const kgw_mgrouped_args* a) {
+  if (!a) return KGW_ERR_INVALID_ARG;
+  if (a->num_groups < 1 || a->num_groups > kgw::MAX_EXPERTS) return KGW_ERR_INVALID_ARG;
+  if (a->layout != KGW_MG_OFFSETS && a->layout != KGW_MG_INDICES && a->layout != KGW_MG_MASKED)
+    return KGW_ERR_INVALID_ARG;
+  if (a->m < 0 || a->n <= 0 || a->k <= 0) return KGW_ERR_INVALID_ARG;
+  if (a->layout != KGW_MG_MASKED && a->m % kgw::MG_ROW_ALIGN != 0) return KGW_ERR_INVALID_ARG;
+  if (a->m >= (int64_t(1) << 31) || mg_rows(a) >= (int64_t(1) << 31)) return KGW_ERR_UNSUPPORTED;
+  if (a->n % kgw::BN != 0 || a->k % kgw::BK_BF16 != 0) return KGW_ERR_UNSUPPORTED;
+  if (int64_t(a->num_groups) * a->n >= (int64_t(1) << 31) || int64_t(a->num_groups) * a->k >= (int64_t(1) << 31))
+    return KGW_ERR_UNSUPPORTED;
+  if (mg_max_tiles(a) * (a->n / kgw::BN) >= (int64_t(1) << 31)) return KGW_ERR_UNSUPPORTED;
+  if (a->b_major != KGW_K_MAJOR && a->b_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
+  if (a->out_dtype != KGW_OUT_F32 && a->out_dtype != KGW_OUT_BF16 && a->out_dtype != KGW_OUT_F16)
+    return KGW_ERR_INVALID_ARG;
+  if (a->accumulate != 0 && a->accumulate != 1) return KGW_ERR_INVALID_ARG;
+  const bool has_rows = mg_rows(a) > 0;
+  if (!a->b || (!a->groups && (a->layout != KGW_MG_INDICES || has_rows)) || (has_rows && (!a->a || !a->d)))
+    return KGW_ERR_INVALID_ARG;
+  if (!aligned(a->b, 16) || (a->groups && !aligned(a->groups, 4)) || (a->a && !aligned(a->a, 16)) ||
+      (a->d && !aligned(a->d, 16)))
+    return KGW_ERR_ALIGNMENT;
+  if (a->status_dev && !aligned(a->status_dev, 4)) return KGW_ERR_ALIGNMENT;
+  return KGW_OK;
+}
+
+kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* stream) {
+  kgw_status st = validate_mg(a);
+  if (st != KGW_OK) return st;
+  if (!ws || !aligned(ws, 256)) return KGW_ERR_WORKSPACE;
+  const WsLayout L = kgw::ws_layout_mg(mg_max_tiles(a));
+  if (ws_bytes < L.total) return KGW_ERR_WORKSPACE;
+  DevInfo dev;
+  st = device_info(&dev);
+  if (st != KGW_OK) return st;
+  if (dev.major != 10 || dev.minor != 3) return KGW_ERR_DEVICE;
+  if (get_encoder() != KGW_OK) return KGW_ERR_CUDA;
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  const uint64_t M = static_cast<uint64_t>(mg_rows(a)), N = static_cast<uint64_t>(a->n),
+                 K = static_cast<uint64_t>(a->k), G = static_cast<uint64_t>(a->num_groups);
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (M > 0) {
+    st = encode_2d(&tmA, dt, a->a, K, M, K * 2, kgw::BK_BF16, kgw::BM);                // A [rows, K]
+    if (st != KGW_OK) return st;
+    if (a->b_major == KGW_K_MAJOR)
+      st = encode_2d(&tmB, dt, a->b, K, G * N, K * 2, kgw::BK_BF16, kgw::BN);         // B [G*N, K]
+    else
+      st = encode_2d(&tmB, dt, a->b, N, G * K, N * 2, 64, kgw::BK_BF16);             // B [G*K, N]
+    if (st != KGW_OK) return st;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  kgw::PlanParams pp{};
+  pp.E = a->num_groups;
+  pp.I = a->n;
+  pp.offsets = a->groups;
+  pp.grid = dev.sm_count;
+  pp.status_dev = a->status_dev;
+  pp.ws = static_cast<uint8_t*>(ws);
+  pp.L = L;
+  pp.tile_m = kgw::BM;
+  pp.mg_layout = a->layout;
+  pp.mg_m = a->m;
+  if (kgw::launch_plan_mgrouped(pp, s) != cudaSuccess) return KGW_ERR_CUDA;
+  kgw::MainParams mp{};
+  mp.E = a->num_groups;
+  mp.I = a->n;
+  mp.K = a->k;
+  mp.tokens_sum = static_cast<int64_t>(M);
+  mp.out = a->d;
+  mp.out_bf16 = a->out_dtype == KGW_OUT_BF16 || a->out_dtype == KGW_OUT_F16;
+  mp.out_f16 = a->out_dtype == KGW_OUT_F16;
+  mp.accumulate = a->accumulate;
+  mp.a_kmajor = 1;
+  mp.b_kmajor = a->b_major == KGW_K_MAJOR;
+  mp.num_n_tiles = a->n / kgw::BN;
+  mp.tile_m = kgw::BM;
+  mp.status_dev = a->status_dev;
+  mp.ws = static_cast<uint8_t*>(ws);
+  mp.L = L;
+  mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
+  mp.test_drop_stage = -1;
+  return kgw::launch_main_mgrouped(mp, tmA, tmB, dev.sm_count, s) == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -423,6 +517,18 @@ int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, 
   }
   std::free(dev_maps);
   return mismatches;
+}
+
+kgw_status kgw_mgrouped_workspace_size(const kgw_mgrouped_args* args, size_t* bytes) {
+  if (!bytes) return KGW_ERR_INVALID_ARG;
+  kgw_status st = validate_mg(args);
+  if (st != KGW_OK) return st;
+  *bytes = kgw::ws_layout_mg(mg_max_tiles(args)).total;
+  return KGW_OK;
+}
+
+kgw_status kgw_mgrouped_bf16(const kgw_mgrouped_args* args, void* workspace, size_t workspace_bytes, void* stream) {
+  return run_mg(args, workspace, workspace_bytes, stream);
 }
 
 const char* kgw_status_string(int32_t status) {

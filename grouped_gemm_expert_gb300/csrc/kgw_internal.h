@@ -97,6 +97,17 @@ inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1) {
   return L;
 }
 
+// M-grouped GEMM workspace: [PlanHeader][tile table: int2 {first row, group | rows << 16} per
+// 128-row tile, max_tiles entries]. The table lives where the K-grouped layout keeps `order`.
+inline WsLayout ws_layout_mg(int64_t max_tiles) {
+  WsLayout L{};
+  L.order = sizeof(PlanHeader);
+  L.total = align256(L.order + sizeof(int32_t) * 2 * size_t(max_tiles > 0 ? max_tiles : 1));
+  L.item_prefix = L.splits = L.slot_base = L.counter_base = L.tmaps = L.tmaps_b = L.counters = L.partials = L.total;
+  L.max_slots = 0;
+  return L;
+}
+
 struct PlanParams {
   int32_t E, H, I;
   int64_t tokens_sum;
@@ -114,6 +125,8 @@ struct PlanParams {
   const uint8_t* a;             // A base (ragged: flat buffer of per-expert blocks)
   const uint8_t* b;             // B base
   int32_t esz;                  // bytes per operand element
+  int32_t mg_layout;            // M-grouped: kgw_mg_layout
+  int64_t mg_m;                 // M-grouped: rows (contiguous) or rows per group (masked)
 };
 
 // Host-encoded templates of the per-expert descriptors (ragged, K-major operands): one per
@@ -131,6 +144,7 @@ struct MainParams {
   int32_t out_bf16, accumulate, ragged, discrete, fp8;  // out_bf16: 16-bit output (BF16 or FP16)
   int32_t out_f16;              // the 16-bit output is FP16
   int32_t a_kmajor, b_kmajor;   // operand storage orders (1: token axis has unit stride)
+  int32_t K;                    // M-grouped GEMM: contraction length (fixed for every group)
   int32_t num_m_tiles, num_n_tiles;
   int32_t tile_m;               // 128 (one CTA per tile) or 256 (a CTA pair per tile)
   const float* sfa;             // FP8: [tokens_sum/128, H] FP32 (or packed UE8M0 words)
@@ -149,6 +163,11 @@ cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const 
                              cudaStream_t s);
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s);
+// M-grouped GEMM (rows of A grouped by expert, each group with its own B): schedule + main kernel.
+cudaError_t launch_plan_mgrouped(const PlanParams& p, cudaStream_t s);
+cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                                 cudaStream_t s);
+constexpr int MG_ROW_ALIGN = 128;   // every group's row count is a multiple of the 128-row tile
 size_t main_smem_bytes(bool pair, bool fp8);
 bool fp8_supported();
 

@@ -246,6 +246,91 @@ __global__ void __launch_bounds__(PLAN_THREADS)
   }
 }
 
+// Schedule of the M-grouped GEMM ("05 · Grouped GEMM 与 Expert 计算", section 2.1: rows of A are
+// grouped by expert, each group aligned to the 128-row tile and multiplied by its own B): validate
+// the cumulative row offsets and lay out the work items group by group.
+// M-grouped plan: turns the device-side group description into the tile table (one entry per
+// 128-row tile: its first row in A/D, its group and its valid rows) and the item count
+// (tiles x n-tiles). Contiguous layouts check that no tile spans two groups; masked checks
+// 0 <= masked_m[g] <= max_m. Any violation: KGW_ERR_OFFSETS and no items.
+__global__ void __launch_bounds__(PLAN_THREADS) plan_mgrouped_kernel(const __grid_constant__ PlanParams p) {
+  __shared__ int64_t s_warp[32];
+  __shared__ int32_t s_err;
+  pdl_launch_dependents();
+  const int G = p.E;
+  const int tid = threadIdx.x;
+  const int NT = p.I / BN;
+  const int32_t* grp = p.offsets;
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
+  int2* tiles = reinterpret_cast<int2*>(p.ws + p.L.order);
+  if (tid == 0) s_err = 0;
+  __syncthreads();
+  int64_t ntiles = 0;
+  if (p.mg_layout == KGW_MG_OFFSETS) {
+    for (int g = tid; g < G; g += blockDim.x) {
+      const int64_t prev = g ? static_cast<int64_t>(grp[g - 1]) : 0;
+      const int64_t cur = grp[g];
+      if (cur < prev || ((cur - prev) % BM) != 0 || (g == G - 1 && cur != p.mg_m)) atomicExch(&s_err, 1);
+    }
+    __syncthreads();
+    ntiles = p.mg_m / BM;
+    if (!s_err) {
+      for (int64_t t = tid; t < ntiles; t += blockDim.x) {
+        const int64_t r0 = t * BM;
+        int lo = 0, hi = G - 1;  // first g with offsets[g] > r0 (exists: offsets[G-1] = m > r0)
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (static_cast<int64_t>(grp[mid]) > r0) hi = mid; else lo = mid + 1;
+        }
+        tiles[t] = make_int2(static_cast<int32_t>(r0), lo | (BM << 16));
+      }
+    }
+  } else if (p.mg_layout == KGW_MG_INDICES) {
+    ntiles = p.mg_m / BM;
+#pragma unroll 4
+    for (int64_t i = tid; i < p.mg_m; i += blockDim.x) {
+      const int32_t g = grp[i];
+      const int32_t head = grp[i & ~int64_t(BM - 1)];
+      if (g != head || g < 0 || g >= G) atomicExch(&s_err, 1);
+      if ((i & (BM - 1)) == 0) tiles[i / BM] = make_int2(static_cast<int32_t>(i), g | (BM << 16));
+    }
+    __syncthreads();
+  } else {
+    // masked: group g's valid rows masked_m[g] start at row g * max_m; ceil(masked_m / 128) tiles
+    const Chunk ch = my_chunk(G);
+    int64_t mine = 0;
+    for (int g = ch.lo; g < ch.hi; ++g) {
+      const int32_t c = grp[g];
+      if (c < 0 || c > p.mg_m) {
+        atomicExch(&s_err, 1);
+      } else {
+        mine += (c + BM - 1) / BM;
+      }
+    }
+    int64_t run = block_exclusive_scan(mine, s_warp, &ntiles);
+    if (!s_err) {
+      for (int g = ch.lo; g < ch.hi; ++g) {
+        const int32_t c = grp[g];
+        for (int t = 0; t * BM < c; ++t, ++run) {
+          const int rows = c - t * BM < BM ? c - t * BM : BM;
+          tiles[run] = make_int2(static_cast<int32_t>(g * p.mg_m + int64_t(t) * BM), g | (rows << 16));
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int32_t err = s_err ? KGW_ERR_OFFSETS : KGW_OK;
+    hdr->error = err;
+    hdr->total_items = err ? 0 : static_cast<int32_t>(ntiles * NT);
+    hdr->chunk_kiters = 0;
+    hdr->slots_used = 0;
+    hdr->counters_used = 0;
+    hdr->item_counter = 0;
+    if (p.status_dev) *p.status_dev = err;
+  }
+}
+
 // =============================================================================================
 // Main kernel
 // =============================================================================================
@@ -255,11 +340,32 @@ struct Item {
   int m0, n0;
   int kbeg, kend;        // k-iterations (relative to the expert's first token)
   int split, nsplit, tile;
+  int rows;              // valid rows of the tile (M-grouped masked layout: may be < 128)
   int64_t begin;         // expert's first token
   int64_t n_e;           // expert's token count
 };
 
+template <bool kMG = false>
 __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk) {
+  Item it;
+  if constexpr (kMG) {
+    // M-grouped: item = (128-row tile, n-tile); the tile table gives the rows and the group
+    const int mt = idx / p.num_n_tiles;
+    const int nt = idx - mt * p.num_n_tiles;
+    const int2 ti = __ldg(reinterpret_cast<const int2*>(p.ws + p.L.order) + mt);
+    it.e = ti.y & 0xFFFF;
+    it.rows = ti.y >> 16;
+    it.m0 = ti.x;
+    it.n0 = nt * BN;
+    it.split = 0;
+    it.nsplit = 1;
+    it.tile = idx;
+    it.kbeg = 0;
+    it.kend = p.K / bk;
+    it.begin = 0;
+    it.n_e = 0;
+    return it;
+  }
   const int32_t* order = reinterpret_cast<const int32_t*>(p.ws + p.L.order);
   const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + p.L.item_prefix);
   const int32_t* splits = reinterpret_cast<const int32_t*>(p.ws + p.L.splits);
@@ -268,9 +374,9 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
     const int mid = (lo + hi) >> 1;
     if (__ldg(prefix + mid) <= idx) lo = mid; else hi = mid;
   }
-  Item it;
   it.e = __ldg(order + lo);
   const int local = idx - __ldg(prefix + lo);
+  it.rows = p.tile_m;
   it.nsplit = __ldg(splits + it.e);
   const int T = p.num_m_tiles * p.num_n_tiles;
   it.split = local / T;
@@ -399,9 +505,11 @@ __device__ __forceinline__ float4 unstage(const uint4* stg, int j, int lane) {
   return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
 }
 
+template <bool kMG = false>
 __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it, int row) {
   const size_t esz = p.out_bf16 ? 2 : 4;
   const size_t r = static_cast<size_t>(it.m0 + row);
+  if constexpr (kMG) return reinterpret_cast<char*>(p.out) + (r * p.I + it.n0) * esz;  // D [M_total, N]
   if (p.discrete) {
     char* base = reinterpret_cast<char*>(static_cast<uintptr_t>(__ldg(p.out_ptrs + it.e)));
     return base + (r * p.I + it.n0) * esz;
@@ -415,7 +523,7 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
 //    128 rows of A and 128 columns of B; the even CTA issues tcgen05.mma.cta_group::2, which reads
 //    both CTAs' shared memory and writes each CTA's 128 rows into its own TMEM. Per SM this moves
 //    32 KiB per k-iteration into shared memory instead of 48 KiB.
-template <bool kFp8, bool kPair, bool kAK, bool kBK>
+template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false>
 __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
@@ -538,7 +646,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       if (!ok || cur >= total_items) break;
       int nxt = 0;
       if (lane == 0 && leader) nxt = atomicAdd(item_counter, 1);
-      const Item it = decode_item(p, cur, bk);
+      const Item it = decode_item<kMG>(p, cur, bk);
       // ragged + K-major operand: the expert's own descriptor, coordinates relative to its block
       const CUtensorMap* amap = &tmA;
       const CUtensorMap* bmap = &tmB;
@@ -572,8 +680,12 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             else
               tma_load_2d(dst, map, &ctl->full[stage], x, y);
           };
-          // token coordinate: relative to the expert's block for per-expert descriptors
-          const int32_t kx = p.ragged ? kb * bk : static_cast<int32_t>(tok);
+          // token coordinate: relative to the expert's block for per-expert descriptors (and for
+          // the M-grouped GEMM, whose K axis is the fixed contraction axis)
+          const int32_t kx = (kMG || p.ragged) ? kb * bk : static_cast<int32_t>(tok);
+          // M-grouped: group e's B occupies rows [e*N, e*N+N) (K-major) or [e*K, e*K+K) (N-major)
+          const int32_t b_row = kMG ? it.e * p.I + b_col : b_col;
+          const int32_t b_tok = kMG ? it.e * p.K + kb * bk : static_cast<int32_t>(tok);
           constexpr int kAtom = kFp8 ? 128 : 64;  // elements per 128-byte swizzle row
           // A: K-major -> one box [128 rows x bk tokens]; MN-major -> boxes [bk tokens x 128 B of rows]
           if constexpr (kAK) {
@@ -585,11 +697,11 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           }
           // B: K-major -> one box [this CTA's columns x bk tokens]; MN-major -> boxes of 128 B of columns
           if constexpr (kBK) {
-            load(sB, bmap, kx, b_col);
+            load(sB, bmap, kx, b_row);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / kHalves / kAtom; ++j)
-              load(sB + j * bk * 128, &tmB, b_col + kAtom * j, static_cast<int32_t>(tok));
+              load(sB + j * bk * 128, &tmB, b_col + kAtom * j, b_tok);
           }
           if constexpr (kFp8) {
             // this 128-token block's FP32 scales: the tile's 128 rows of A and 256 columns of B;
@@ -656,7 +768,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         const int cur = ctl->work_item[slot];
         release_slot(slot);
         if (cur < 0) break;
-        const Item it = decode_item(p, cur, bk);
+        const Item it = decode_item<kMG>(p, cur, bk);
         if (it.kend == it.kbeg) continue;
         // BF16: two accumulators alternate; FP8: one accumulator (TMEM also holds scale factors)
         const int acc = kFp8 ? 0 : (tcount & 1);
@@ -745,9 +857,9 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) release_slot(slot);
       if (cur < 0) break;
-      const Item it = decode_item(p, cur, bk);
+      const Item it = decode_item<kMG>(p, cur, bk);
       // this warp's 32 output rows start at tile row rank*128 + q*32; row r is `ostride` bytes further
-      char* obase = out_row_ptr(p, it, static_cast<int>(rank) * BM + q * 32);
+      char* obase = out_row_ptr<kMG>(p, it, static_cast<int>(rank) * BM + q * 32);
       const size_t ostride = size_t(p.I) * (p.out_bf16 ? 2 : 4);
       const int esz = p.out_bf16 ? 2 : 4;
       if (it.kend == it.kbeg) {
@@ -790,12 +902,16 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           }
           __syncwarp();
           uint4 old[8];
+          // M-grouped masked layout: rows at or past the group's valid count are not touched
+          auto live = [&](int j) { return !kMG || q * 32 + 4 * j + (lane >> 3) < it.rows; };
           if (p.accumulate) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) old[j] = load_old4(p, cbase + (4 * j + (lane >> 3)) * ostride);
+            for (int j = 0; j < 8; ++j)
+              if (live(j)) old[j] = load_old4(p, cbase + (4 * j + (lane >> 3)) * ostride);
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) emit4(p, cbase + (4 * j + (lane >> 3)) * ostride, unstage(stg, j, lane), old[j]);
+          for (int j = 0; j < 8; ++j)
+            if (live(j)) emit4(p, cbase + (4 * j + (lane >> 3)) * ostride, unstage(stg, j, lane), old[j]);
           __syncwarp();
         }
       } else {
@@ -881,7 +997,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) release_slot(slot);
         if (cur < 0) break;
-        const Item it = decode_item(p, cur, bk);
+        const Item it = decode_item<kMG>(p, cur, bk);
         bool ok = true;
         for (int kb = it.kbeg; kb < it.kend; ++kb) {
           // the scales have landed; this also means the copies of the previous round are done
@@ -954,6 +1070,11 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
 // Launchers
 // =============================================================================================
 
+cudaError_t launch_plan_mgrouped(const PlanParams& p, cudaStream_t s) {
+  plan_mgrouped_kernel<<<1, PLAN_THREADS, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_plan(const PlanParams& p, const MapTemplates& t, cudaStream_t s) {
   int threads = ((p.E + 31) / 32) * 32;
   threads = threads < 128 ? 128 : (threads > PLAN_THREADS ? PLAN_THREADS : threads);
@@ -961,10 +1082,10 @@ cudaError_t launch_plan(const PlanParams& p, const MapTemplates& t, cudaStream_t
   return cudaGetLastError();
 }
 
-template <bool kFp8, bool kPair, bool kAK, bool kBK>
+template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false>
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
-  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK>;
+  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG>;
   const size_t smem = main_smem_bytes(kPair, kFp8);
   // set on every launch: the attribute is per device and the call is cheap
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -1001,6 +1122,12 @@ cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const 
                              cudaStream_t s) {
   if (p.tile_m == 2 * BM) return launch_orders<false, true>(p, tmA, tmB, grid, s);
   return launch_orders<false, false>(p, tmA, tmB, grid, s);
+}
+
+cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                                 cudaStream_t s) {
+  if (p.b_kmajor) return launch_main<false, false, true, true, true>(p, tmA, tmB, grid, s);
+  return launch_main<false, false, true, false, true>(p, tmA, tmB, grid, s);
 }
 
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,

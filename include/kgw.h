@@ -167,6 +167,63 @@ kgw_status kgw_wgrad_fp8_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
  */
 kgw_status kgw_wgrad_bf16_noalloc(const kgw_wgrad_args* args, void* stream);
 
+/*
+ * M-grouped GEMM: the forward / dgrad GEMM of the same MoE layer ("05 · Grouped GEMM 与 Expert 计算",
+ * sections 1, 2 and 5.1: only M varies between groups, N and K are fixed). Each group g multiplies
+ * its own rows of A by its own weight B_g:
+ *
+ *     D[rows of g, :] (+)= A[rows of g, :] @ op(B_g)
+ *
+ * B is K-major [G, n, k] (forward, op(B_g) = B_g^T, the "nt" layout) or N-major [G, k, n]
+ * (dgrad, op(B_g) = B_g). A and D are row-major with K resp. N contiguous. FP32 accumulation, one
+ * rounding to the output type (kgw_out_dtype), overwrite or accumulate (D = D + result, one FP32
+ * add before that rounding). Which rows belong to which group is given on the device, in one of
+ * three layouts (section 2):
+ *
+ *   KGW_MG_OFFSETS    A [m, k], D [m, n]. groups = int32 [G] cumulative row counts (group g owns
+ *                     rows [offsets[g-1], offsets[g]), offsets[-1] = 0): contiguous layout, every
+ *                     count a multiple of 128 (a 128-row tile never spans two groups) and
+ *                     offsets[G-1] == m. Counts of 0 are allowed.
+ *   KGW_MG_INDICES    A [m, k], D [m, n]. groups = int32 [m] group id of every row (the pages'
+ *                     m_indices): contiguous layout, every aligned 128-row block carries one id in
+ *                     [0, G). Blocks need not be sorted by group.
+ *   KGW_MG_MASKED     A [G, m, k], D [G, m, n] with m = max_m rows reserved per group. groups =
+ *                     int32 [G] valid rows per group (masked_m, 0 <= masked_m[g] <= m): masked
+ *                     layout (section 2.2). Only the first masked_m[g] rows of each group are
+ *                     computed and written; the other rows of D are left untouched, and the
+ *                     values in the unused rows of A do not matter.
+ *
+ * Device-detected violations of these rules set KGW_ERR_OFFSETS (in *status_dev when given) and
+ * nothing is written. Conventions as for kgw_wgrad_bf16: device pointers, caller-owned buffers,
+ * asynchronous on stream, no host synchronisation (CUDA-graph capturable), host-detected errors
+ * returned before anything is enqueued. Constraints: n % 256 == 0, k % 64 == 0, 1 <= G <= 4096,
+ * m % 128 == 0 for the contiguous layouts, A/B/D 16-byte aligned, fewer than 2^31 rows of A and
+ * of B.
+ */
+typedef enum { KGW_MG_OFFSETS = 0, KGW_MG_INDICES = 1, KGW_MG_MASKED = 2 } kgw_mg_layout;
+
+typedef struct kgw_mgrouped_args {
+  int32_t num_groups;       /* G                                                              */
+  int32_t layout;           /* kgw_mg_layout                                                  */
+  int64_t m;                /* contiguous: rows of A and D; masked: rows reserved per group   */
+  int32_t n;                /* columns of D                                                   */
+  int32_t k;                /* contraction length                                             */
+  const void* a;            /* bf16 A (see layout)                                            */
+  const void* b;            /* bf16 [G, n, k] (KGW_K_MAJOR) or [G, k, n] (KGW_MN_MAJOR)       */
+  int32_t b_major;          /* kgw_major                                                      */
+  const int32_t* groups;    /* device int32: offsets [G], m_indices [m] or masked_m [G]       */
+  void* d;                  /* output (see layout), dtype out_dtype                           */
+  int32_t out_dtype;        /* kgw_out_dtype                                                  */
+  int32_t accumulate;       /* 0: overwrite; 1: D += result                                   */
+  int32_t* status_dev;      /* optional device int32 receiving device-detected kgw_status     */
+} kgw_mgrouped_args;
+
+/* Workspace bytes of kgw_mgrouped_bf16 (host-only; depends on G, m and the layout). */
+kgw_status kgw_mgrouped_workspace_size(const kgw_mgrouped_args* args, size_t* bytes);
+
+/* M-grouped BF16 GEMM (see kgw_mgrouped_args). workspace: 256-byte aligned device buffer. */
+kgw_status kgw_mgrouped_bf16(const kgw_mgrouped_args* args, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* kgw_status_string(int32_t status);
 
