@@ -21,7 +21,10 @@ and an empty expert yields zeros (section "Operation").
 The FP8 variant multiplies every decoded e4m3 element by its per-128-token
 FP32 scale before the product: a row m of A and a column n of B each carry one
 scale per block of 128 consecutive tokens ("05 · Grouped GEMM 与 Expert 计算",
-section 3: per-block 1x128 scaling, scales stored MN-major).
+section 3: per-block 1x128 scaling, scales stored MN-major). The FP4 variant
+does the same with e2m1 elements (two per byte along the token axis, first
+token in the low nibble) and one UE8M0 scale per 32 tokens ("How to Use K-Grouped
+GEMM ...", steps 1-2: FP4 casts with gran_k = 32 for both operands).
 
 Every product here is exact in float64 only up to rounding of the float64
 sums; the tests pin it against exact rational brute force, so "the oracle"
@@ -70,6 +73,26 @@ def e4m3_to_f64(bits) -> np.ndarray:
     mag = np.where(e == 0, sub, normal)
     mag = np.where((e == 15) & ((b & 0x7) == 7), np.nan, mag)
     return sign * mag
+
+
+E2M1_VALUES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def e2m1_to_f64(packed) -> np.ndarray:
+    """Decode packed FP4 e2m1 bytes to float64, two elements per byte, low nibble first.
+
+    A 4-bit code is 1 sign bit, 2 exponent bits (bias 1) and 1 mantissa bit: exponent field 0
+    is subnormal m * 0.5, otherwise (1 + m/2) * 2**(e-1); there is no NaN or infinity, the
+    largest magnitude is 6. The result has twice the elements of ``packed`` (flattened).
+    """
+    b = np.asarray(packed).view(np.uint8).reshape(-1).astype(np.int64)
+    codes = np.empty(2 * b.size, dtype=np.int64)
+    codes[0::2] = b & 0xF
+    codes[1::2] = b >> 4
+    e = (codes >> 1) & 0x3
+    m = (codes & 0x1).astype(np.float64)
+    mag = np.where(e == 0, 0.5 * m, (1.0 + m / 2.0) * np.ldexp(1.0, (e - 1).astype(np.int64)))
+    return np.where(codes & 0x8, -mag, mag)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -230,14 +253,19 @@ def wgrad(A: np.ndarray, B: np.ndarray, offsets, c_init=None, accumulate: bool =
 def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, *,
                        input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
                        c_init=None, accumulate: bool = False, with_bound: bool = True,
-                       a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128"):
+                       a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128",
+                       fp4: bool = False):
     """Decode stored operands (raw bits) and evaluate the operation in float64.
 
-    a_bits/b_bits: uint16 (bf16) or uint8 (e4m3) numpy arrays as stored.
-    sfa [tokens/128, hidden], sfb [tokens/128, intermediate]: float32 scales (FP8 only).
-    c_init: the pre-filled output values (any float dtype, decoded by the caller) or None.
+    a_bits/b_bits: uint16 (bf16), uint8 (e4m3) or uint8 packed e2m1 (fp4, K-major only) numpy
+    arrays as stored. sfa [tokens/128, hidden], sfb [tokens/128, intermediate]: float32 scales
+    or packed UE8M0 words (FP8/FP4). c_init: the pre-filled output values (any float dtype,
+    decoded by the caller) or None.
     """
-    dec = e4m3_to_f64 if fp8 else bf16_to_f64
+    if fp4:
+        assert a_major == "k" and b_major == "k" and sf_format == "ue8m0_32"
+        fp8 = True   # from here on the same steps: decoded elements times their scales
+    dec = e2m1_to_f64 if fp4 else (e4m3_to_f64 if fp8 else bf16_to_f64)
     A = logical_a(dec(a_bits), hidden, offsets, input_order, a_major)
     B = logical_b(dec(b_bits), intermediate, offsets, input_order, b_major)
     if fp8:
@@ -280,7 +308,8 @@ def tolerance(S: np.ndarray, ref: np.ndarray, out_dtype: str, c_init=None) -> np
 
 def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, e: int, m: int, n: int, *,
                          input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
-                         a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128"):
+                         a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128",
+                         fp4: bool = False):
     """R_e[m, n] and S_e[m, n] read straight from the stored operands (for sampled checks).
 
     Only row m of A_e and column n of B_e are decoded, so this works at full problem size.
@@ -292,6 +321,23 @@ def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int
     if cnt == 0:
         return 0.0, 0.0
     tokens_sum = expert_ranges(offsets)[-1][1]
+    if fp4:
+        # K-major only: a row of A / column of B is a contiguous element range [s, e) with s and e
+        # even, i.e. the packed bytes [s/2, e/2)
+        assert a_major == "k" and b_major == "k"
+        fa, fb = np.asarray(a_bits).reshape(-1), np.asarray(b_bits).reshape(-1)
+        if input_order == "tensor2d":
+            sa0, sb0 = m * tokens_sum + b, n * tokens_sum + b
+        else:
+            sa0, sb0 = b * hidden + m * cnt, b * intermediate + n * cnt
+        arow = e2m1_to_f64(fa[sa0 // 2:(sa0 + cnt) // 2])
+        bcol = e2m1_to_f64(fb[sb0 // 2:(sb0 + cnt) // 2])
+        sa, blk = decode_scales(sfa, sf_format)
+        sb, _ = decode_scales(sfb, sf_format)
+        ks = np.arange(b, end) // blk
+        arow = arow * sa[ks, m]
+        bcol = bcol * sb[ks, n]
+        return float(np.dot(arow, bcol)), float(np.dot(np.abs(arow), np.abs(bcol)))
     dec = e4m3_to_f64 if fp8 else bf16_to_f64
     flat_a = np.asarray(a_bits).reshape(-1)
     if a_major == "mn":

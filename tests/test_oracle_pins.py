@@ -614,3 +614,104 @@ def test_ue8m0_quantiser_recipe():
     recon = O.apply_scales_rows(dec, s, 32)
     err = np.abs(recon - x.numpy().astype(np.float64))
     assert np.all(err <= 2.0 ** -4 * np.abs(x.numpy()) + np.repeat(s.T, 32, axis=1) * 2.0 ** -10)
+
+
+# ------------------------------------------------------------------------------------------
+# FP4 (e2m1 elements, UE8M0 scales per 32 tokens)
+# ------------------------------------------------------------------------------------------
+
+def _fp4_golden():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "e2m1_codes.txt")) if l.strip() and not l.startswith("#")]
+    return {int(c, 16): float(v) for c, v in rows}
+
+
+def test_e2m1_decode_matches_format_table():
+    table = _fp4_golden()
+    codes = np.arange(16, dtype=np.uint8)
+    packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)   # low nibble = first element
+    got = O.e2m1_to_f64(packed)
+    for c in range(16):
+        assert got[c] == table[c] and np.signbit(got[c]) == np.signbit(table[c]), c
+
+
+def test_e2m1_nibble_order():
+    assert O.e2m1_to_f64(np.array([0x21], dtype=np.uint8)).tolist() == [0.5, 1.0]
+    assert O.e2m1_to_f64(np.array([0x7F], dtype=np.uint8)).tolist() == [-6.0, 6.0]
+
+
+def test_fp4_quantiser_round_trip_on_grid():
+    """Values that are grid points times a power of two come back exactly, with their scale."""
+    rng = np.random.default_rng(31)
+    grid = np.array(sorted(set(_fp4_golden().values())))
+    k = rng.integers(-6, 6, size=(3, 8))                       # one exponent per 32-token block
+    vals = rng.choice(grid, size=(3, 256))
+    vals[:, ::32] = 6.0                                        # amax of every block is 6 * 2**k
+    x = vals * np.ldexp(1.0, np.repeat(k, 32, axis=1))
+    q, sf = W.quantize_e2m1_ue8m0_32(torch.from_numpy(x.astype(np.float32)), token_axis=1)
+    dec = O.e2m1_to_f64(q.numpy()).reshape(3, 256)
+    scales = O.unpack_ue8m0_32(sf.numpy())                     # [256/32, 3]
+    assert np.array_equal(dec * np.repeat(scales.T, 32, axis=1), x)
+
+
+def test_fp4_unit_scales_equal_bf16_oracle():
+    """FP4 with all scales 1 is the BF16 operation on the decoded values (all e2m1 values are
+    exact in bf16): ties the FP4 decoding and layout to the independently pinned BF16 path."""
+    rng = np.random.default_rng(32)
+    counts = [256, 0, 512]
+    offs = np.cumsum(counts).astype(np.int32)
+    T, H, I = 768, 8, 16
+    codes_a = rng.integers(0, 16, size=(H, T)).astype(np.uint8)
+    codes_b = rng.integers(0, 16, size=(I, T)).astype(np.uint8)         # K-major B [I, T]
+    pa = codes_a[:, 0::2] | (codes_a[:, 1::2] << 4)
+    pb = codes_b[:, 0::2] | (codes_b[:, 1::2] << 4)
+    ones_a = np.full((T // 128, H), 0x7F7F7F7F, dtype=np.uint32).view(np.int32)
+    ones_b = np.full((T // 128, I), 0x7F7F7F7F, dtype=np.uint32).view(np.int32)
+    got, S = O.wgrad_from_storage(pa, pb, offs, H, I, fp4=True, sfa=ones_a, sfb=ones_b, b_major="k",
+                                  sf_format="ue8m0_32")
+    table = _fp4_golden()
+    va = np.vectorize(table.get)(codes_a).astype(np.float32)
+    vb = np.vectorize(table.get)(codes_b).astype(np.float32)
+    a16 = torch.from_numpy(va).to(torch.bfloat16)
+    b16 = torch.from_numpy(vb.T.copy()).to(torch.bfloat16)                # N-major [T, I]
+    ref, S2 = O.wgrad_from_storage(bf16_bits(a16), bf16_bits(b16), offs, H, I)
+    assert np.array_equal(got, ref) and np.array_equal(S, S2)
+
+
+def test_fp4_brute_force_with_scales():
+    rng = np.random.default_rng(33)
+    counts = [256, 256]
+    offs = np.cumsum(counts).astype(np.int32)
+    T, H, I = 512, 2, 3
+    codes_a = rng.integers(0, 16, size=(H, T)).astype(np.uint8)
+    codes_b = rng.integers(0, 16, size=(I, T)).astype(np.uint8)
+    pa = codes_a[:, 0::2] | (codes_a[:, 1::2] << 4)
+    pb = codes_b[:, 0::2] | (codes_b[:, 1::2] << 4)
+    ea = rng.integers(120, 135, size=(T // 32, H))
+    eb = rng.integers(120, 135, size=(T // 32, I))
+
+    def pack(e):
+        e = e.astype(np.uint32).reshape(T // 128, 4, -1)
+        return (e[:, 0] | (e[:, 1] << 8) | (e[:, 2] << 16) | (e[:, 3] << 24)).view(np.int32)
+
+    got, _ = O.wgrad_from_storage(pa, pb, offs, H, I, fp4=True, sfa=pack(ea), sfb=pack(eb), b_major="k",
+                                  sf_format="ue8m0_32")
+    table = {c: Fraction(v) for c, v in _fp4_golden().items()}
+    for e, (b, end) in enumerate([(0, 256), (256, 512)]):
+        for m in range(H):
+            for n in range(I):
+                exact = sum(table[int(codes_a[m, k])] * Fraction(2) ** int(ea[k // 32, m] - 127) *
+                            table[int(codes_b[n, k])] * Fraction(2) ** int(eb[k // 32, n] - 127)
+                            for k in range(b, end))
+                assert Fraction(got[e, m, n]) == exact
+
+
+def test_fp4_element_from_storage_matches_full():
+    w = W.custom(3, 128, 256, [256, 0, 512], seed=34, fp4=True, b_major="k", sf_format="ue8m0_32",
+                 out_dtype="bf16")
+    x = W.make_inputs(w, "cpu")
+    full, S = O.wgrad_from_storage(x.a.numpy(), x.b.numpy(), w.offsets, 128, 256, fp4=True, sfa=x.sfa.numpy(),
+                                   sfb=x.sfb.numpy(), b_major="k", sf_format="ue8m0_32")
+    for (e, m, n) in [(0, 0, 0), (0, 127, 255), (2, 64, 17), (2, 3, 200)]:
+        v, s = O.element_from_storage(x.a.numpy(), x.b.numpy(), w.offsets, 128, 256, e, m, n, fp4=True,
+                                      sfa=x.sfa.numpy(), sfb=x.sfb.numpy(), b_major="k", sf_format="ue8m0_32")
+        assert abs(v - full[e, m, n]) <= 1e-12 * (1 + S[e, m, n]) and abs(s - S[e, m, n]) <= 1e-12 * (1 + S[e, m, n])

@@ -92,6 +92,7 @@ class Workload:
     a_major: str = "k"              # "k": A stored [hidden, tokens]; "mn": stored [tokens, hidden]
     sf_format: str = "f32_128"      # FP8 scales: "f32_128" (FP32 per 128 tokens) | "ue8m0_32" (packed)
     b_major: str = "mn"             # "mn": B stored [tokens, intermediate]; "k": stored [intermediate, tokens]
+    fp4: bool = False               # e2m1 operands (K-major A and B), UE8M0 scales per 32 tokens
 
     @property
     def tokens_sum(self) -> int:
@@ -136,7 +137,14 @@ def skewed() -> Workload:
                     out_dtype="bf16", input_order="ragged", output_mode="discrete")
 
 
-NAMED = {"tiny": tiny, "balanced": balanced, "wide": wide, "fp8": fp8, "skewed": skewed}
+def fp4() -> Workload:
+    return Workload("FP4 block-scaled: E=16 hidden=4096 intermediate=1536, e2m1 with UE8M0 per 32 tokens, "
+                    "K-major A and B, BF16 dense overwrite",
+                    16, 4096, 1536, counts_uniform_spread(3, 16, 4096, 0.7, 1.3), seed=8,
+                    out_dtype="bf16", fp4=True, b_major="k", sf_format="ue8m0_32")
+
+
+NAMED = {"tiny": tiny, "balanced": balanced, "wide": wide, "fp8": fp8, "skewed": skewed, "fp4": fp4}
 
 
 def custom(num_experts: int, hidden: int, intermediate: int, counts, seed: int, **kw) -> Workload:
@@ -234,6 +242,46 @@ def quantize_e4m3_ue8m0_32(x: torch.Tensor, token_axis: int):
     return q.contiguous(), packed
 
 
+E2M1_MAX = 6.0
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def e2m1_codes(v: np.ndarray) -> np.ndarray:
+    """Round float64 values with |v| <= 6 to the nearest e2m1 code (ties to the even code)."""
+    a = np.abs(v)
+    idx = np.searchsorted(_E2M1_GRID, a)                 # first grid point >= |v|
+    idx = np.clip(idx, 1, 7)
+    lo, hi = _E2M1_GRID[idx - 1], _E2M1_GRID[idx]
+    pick_hi = (a - lo > hi - a) | ((a - lo == hi - a) & ((idx & 1) == 0))
+    code = np.where(pick_hi, idx, idx - 1)
+    code = np.where(a == 0.0, 0, code)
+    return (code | np.where(np.signbit(v) & (code != 0), 8, 0)).astype(np.uint8)
+
+
+def quantize_e2m1_ue8m0_32(x: torch.Tensor, token_axis: int):
+    """Quantise ``x`` (float32 2-D) to FP4 e2m1 with one power-of-two scale per 32 tokens.
+
+    Returns (packed uint8 [other, tokens/2]: the token axis contiguous, two elements per byte, the
+    first in the low nibble; packed UE8M0 words int32 [tokens/128, other] as in
+    ``quantize_e4m3_ue8m0_32``). The scale is 2**ceil(log2(amax/6)) (1 for amax 0), so
+    |x/scale| <= 6 and nothing saturates.
+    """
+    assert x.dim() == 2 and x.dtype == torch.float32
+    xt = (x if token_axis == 1 else x.t()).double().numpy()
+    other, tokens = xt.shape
+    assert tokens % FP8_BLOCK == 0
+    blocks = xt.reshape(other, tokens // 32, 32)
+    amax = np.abs(blocks).max(axis=2)
+    v = amax / E2M1_MAX
+    frac, ex = np.frexp(v)
+    k = np.where(v == 0.0, 0, np.where(frac == 0.5, ex - 1, ex)).astype(np.int64)
+    codes = e2m1_codes(blocks / np.ldexp(1.0, k)[..., None]).reshape(other, tokens)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    byte = (k + 127).astype(np.uint32).reshape(other, tokens // 128, 4)
+    words = (byte[..., 0] | (byte[..., 1] << 8) | (byte[..., 2] << 16) | (byte[..., 3] << 24)).astype(np.uint32)
+    return torch.from_numpy(np.ascontiguousarray(packed)), torch.from_numpy(words.view(np.int32).T.copy())
+
+
 def pack_ragged_a(a2d: torch.Tensor, counts) -> torch.Tensor:
     """Re-store a logical [hidden, tokens_sum] A as per-expert K-contiguous blocks.
 
@@ -277,6 +325,15 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
     a32 = _normal(gen, (H, T), w.a_std)
     b32 = _normal(gen, (T, I), w.b_std)
     sfa = sfb = None
+    if w.fp4:
+        assert w.a_major == "k" and w.b_major == "k" and w.input_order == "tensor2d"
+        a_store, sfa = quantize_e2m1_ue8m0_32(a32, token_axis=1)     # [H, T/2]
+        b_store, sfb = quantize_e2m1_ue8m0_32(b32, token_axis=0)     # [I, T/2] (K-major)
+        del a32, b32
+        c = _normal(gen, (E, H, I), w.c_std).to(out_torch_dtype(w.out_dtype)) if w.accumulate else None
+        offsets = torch.from_numpy(w.offsets.astype(np.int32))
+        to = lambda t: None if t is None else t.to(device)
+        return Inputs(to(a_store), to(b_store), to(offsets), to(sfa), to(sfb), to(c))
     if w.fp8 and w.sf_format == "ue8m0_32":
         a_store, sfa = quantize_e4m3_ue8m0_32(a32, token_axis=1)
         b_store, sfb = quantize_e4m3_ue8m0_32(b32, token_axis=0)
@@ -310,7 +367,7 @@ def make_inputs_device(w: Workload, device) -> Inputs:
             x.mul_(std)
         return x.to(dtype)
 
-    if w.fp8:
+    if w.fp8 or w.fp4:
         cpu = make_inputs(w, "cpu")   # quantisation recipe lives on the CPU side
         return Inputs(cpu.a.to(device), cpu.b.to(device), cpu.offsets.to(device),
                       cpu.sfa.to(device), cpu.sfb.to(device), None if cpu.c is None else cpu.c.to(device))
