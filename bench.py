@@ -151,9 +151,11 @@ def traffic_record(workload: str):
 
 
 def algorithmic_bytes(w) -> int:
-    esz = 1 if w.fp8 else 2
     ts = w.tokens_sum
-    b = (w.hidden + w.intermediate) * ts * esz
+    if w.fp4:   # e2m1 two per byte, one UE8M0 byte per 32 tokens
+        b = (w.hidden + w.intermediate) * ts // 2 + (w.hidden + w.intermediate) * (ts // 32)
+    else:
+        b = (w.hidden + w.intermediate) * ts * (1 if w.fp8 else 2)
     if w.fp8:
         b += (w.hidden + w.intermediate) * (ts // 128) * 4
     osz = 2 if w.out_dtype == "bf16" else 4
@@ -191,15 +193,25 @@ def run_ours(args, w, rank, local, world):
                           out_dtype=kgw.KGW_OUT_BF16 if w.out_dtype == "bf16" else kgw.KGW_OUT_F32,
                           accumulate=w.accumulate,
                           input_order=kgw.KGW_RAGGED if w.input_order == "ragged" else kgw.KGW_TENSOR2D,
+                          a_major=kgw.KGW_MN_MAJOR if w.a_major == "mn" else kgw.KGW_K_MAJOR,
+                          b_major=kgw.KGW_K_MAJOR if w.b_major == "k" else kgw.KGW_MN_MAJOR,
                           status_dev=status)
-    ws = kgw.workspace_for(kargs, w.fp8, device=dev)
+    ws = kgw.workspace_for(kargs, w.fp8 or w.fp4, device=dev)
     stream = torch.cuda.current_stream()
+    scaled = w.fp8 or w.fp4
+
+    def call(args, sfa, sfb, s):
+        if w.fp4:
+            kgw.kgw_wgrad_fp4_ue8m0(args, sfa, sfb, ws, stream=s)
+        elif w.fp8 and w.sf_format == "ue8m0_32":
+            kgw.kgw_wgrad_fp8_ue8m0(args, sfa, sfb, ws, stream=s)
+        elif w.fp8:
+            kgw.kgw_wgrad_fp8_blockscaled(args, sfa, sfb, ws, stream=s)
+        else:
+            kgw.kgw_wgrad_bf16(args, ws, stream=s)
 
     def step():
-        if w.fp8:
-            kgw.kgw_wgrad_fp8_blockscaled(kargs, x.sfa, x.sfb, ws, stream=stream)
-        else:
-            kgw.kgw_wgrad_bf16(kargs, ws, stream=stream)
+        call(kargs, x.sfa, x.sfb, stream)
 
     for _ in range(args.warmup):
         step()
@@ -239,7 +251,7 @@ def run_ours(args, w, rank, local, world):
     # pinned host memory to the device, the call runs, and its result is copied back to pinned
     # host memory. Steps are pipelined over two buffer sets and three streams (copy-in, compute,
     # copy-out), so step i+1's upload and step i-1's download overlap step i's call.
-    host_in = [t.cpu().pin_memory() for t in (x.a, x.b, x.offsets) + ((x.sfa, x.sfb) if w.fp8 else ())]
+    host_in = [t.cpu().pin_memory() for t in (x.a, x.b, x.offsets) + ((x.sfa, x.sfb) if scaled else ())]
     host_c = x.c.cpu().pin_memory() if w.accumulate else None
     h2d = sum(t.numel() * t.element_size() for t in host_in) + (
         host_c.numel() * host_c.element_size() if host_c is not None else 0)
@@ -253,7 +265,7 @@ def run_ours(args, w, rank, local, world):
             d_out, d_ptrs = None, torch.tensor([t.data_ptr() for t in d_list], dtype=torch.int64, device=dev)
         ka = kgw.make_args(E, H, I, w.tokens_sum, d_in[0], d_in[1], d_in[2], out=d_out, out_ptrs=d_ptrs,
                            out_dtype=kargs.out_dtype, accumulate=w.accumulate, input_order=kargs.input_order,
-                           status_dev=status)
+                           a_major=kargs.a_major, b_major=kargs.b_major, status_dev=status)
         h_out = torch.empty((E, H, I), dtype=odt).pin_memory()
         sets.append(dict(d_in=d_in, d_out=d_out, d_list=d_list, args=ka, h_out=h_out,
                          ev_in=torch.cuda.Event(), ev_comp=torch.cuda.Event(), ev_out=torch.cuda.Event()))
@@ -274,10 +286,7 @@ def run_ours(args, w, rank, local, world):
                 S["d_out"].copy_(host_c, non_blocking=True)
             S["ev_in"].record(s_in)
         s_comp.wait_event(S["ev_in"])
-        if w.fp8:
-            kgw.kgw_wgrad_fp8_blockscaled(S["args"], S["d_in"][3], S["d_in"][4], ws, stream=s_comp)
-        else:
-            kgw.kgw_wgrad_bf16(S["args"], ws, stream=s_comp)
+        call(S["args"], S["d_in"][3] if scaled else None, S["d_in"][4] if scaled else None, s_comp)
         S["ev_comp"].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(S["ev_comp"])
@@ -501,15 +510,17 @@ def cpu_oracle_rate(w, budget_s: float):
     import oracle.kgw_oracle as O
 
     x = W.make_inputs(w, "cpu")
-    bits = (lambda t: t.contiguous().view(torch.uint8).numpy()) if w.fp8 else \
+    bits = (lambda t: t.contiguous().view(torch.uint8).numpy()) if (w.fp8 or w.fp4) else \
         (lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16))
     a_bits, b_bits = bits(x.a), bits(x.b)
-    dec = O.e4m3_to_f64 if w.fp8 else O.bf16_to_f64
-    A = O.logical_a(dec(a_bits), w.hidden, w.offsets, w.input_order)
-    B = O.logical_b(dec(b_bits), w.intermediate, w.offsets, w.input_order)
-    if w.fp8:
-        A = O.apply_block_scales_rows(A, x.sfa.numpy())
-        B = O.apply_block_scales_cols(B, x.sfb.numpy())
+    dec = O.e2m1_to_f64 if w.fp4 else (O.e4m3_to_f64 if w.fp8 else O.bf16_to_f64)
+    A = O.logical_a(dec(a_bits), w.hidden, w.offsets, w.input_order, w.a_major)
+    B = O.logical_b(dec(b_bits), w.intermediate, w.offsets, w.input_order, w.b_major)
+    if w.fp8 or w.fp4:
+        sa, blk = O.decode_scales(x.sfa.numpy(), w.sf_format)
+        sb, _ = O.decode_scales(x.sfb.numpy(), w.sf_format)
+        A = O.apply_scales_rows(A, sa, blk)
+        B = O.apply_scales_cols(B, sb, blk)
     ranges = [(e, b, end) for e, (b, end) in enumerate(O.expert_ranges(w.offsets)) if end > b]
     flops = 0.0
     n_experts = 0
@@ -590,16 +601,18 @@ def main():
     peaks = measured_peaks()
     launch_ms = statistics.mean(per_launch)
     achieved = flops / (launch_ms * 1e-3) / 1e12
-    peak = peaks["bf16_tflops"] * (2.0 if w.fp8 else 1.0)
+    # another dtype's peak: the measured bf16 burst times the nominal dense ratio (fp8 2x, fp4 6x)
+    ratio = 6.0 if w.fp4 else (2.0 if w.fp8 else 1.0)
+    peak = peaks["bf16_tflops"] * ratio
     traffic = traffic_record(args.workload)
     line = {"metric": "K-grouped wgrad TFLOP/s (2*H*I*sum n_e)", "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "fp8" if w.fp8 else "bf16", "data": "synthetic", "config": config,
+            "dtype": "fp4" if w.fp4 else ("fp8" if w.fp8 else "bf16"), "data": "synthetic", "config": config,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes": algorithmic_bytes(w),
-                         "peak_source": f"{peaks['source']} bf16 burst" + (" x2 (fp8 nominal ratio)" if w.fp8 else ""),
+                         "peak_source": f"{peaks['source']} bf16 burst" + (f" x{ratio:g} (nominal dense ratio)" if ratio != 1 else ""),
                          "kernel": "wgrad_kernel (+ plan_kernel, a few us, inside the same events)"},
             "e2e": None if e2e_ms is None else {"value": job_throughput(flops, e2e_ms, world), "unit": "TFLOP/s",
                                                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

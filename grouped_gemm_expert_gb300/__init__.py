@@ -16,6 +16,7 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_wgrad_bf16_noalloc(args, stream=None)
   kgw_debug_check_ragged_maps(args, is_fp8, host_offsets, workspace) -> int
   kgw_wgrad_fp8_ue8m0(args, sfa_packed, sfb_packed, workspace, stream=None)
+  kgw_wgrad_fp4_ue8m0(args, sfa_packed, sfb_packed, workspace, stream=None)
   kgw_mgrouped_workspace_size(args) -> int
   kgw_mgrouped_bf16(args, workspace, stream=None)
 
@@ -56,7 +57,7 @@ KGW_MG_MASKED = 2
 EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
             "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc",
             "kgw_debug_check_ragged_maps", "kgw_wgrad_fp8_ue8m0", "kgw_mgrouped_workspace_size",
-            "kgw_mgrouped_bf16")
+            "kgw_mgrouped_bf16", "kgw_wgrad_fp4_ue8m0")
 
 
 class KgwArgs(ctypes.Structure):
@@ -125,6 +126,9 @@ def lib() -> ctypes.CDLL:
         L.kgw_wgrad_fp8_ue8m0.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.kgw_wgrad_fp8_ue8m0.restype = ctypes.c_int
+        L.kgw_wgrad_fp4_ue8m0.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_wgrad_fp4_ue8m0.restype = ctypes.c_int
         L.kgw_mgrouped_workspace_size.argtypes = [ctypes.POINTER(KgwMgroupedArgs), ctypes.POINTER(ctypes.c_size_t)]
         L.kgw_mgrouped_workspace_size.restype = ctypes.c_int
         L.kgw_mgrouped_bf16.argtypes = [ctypes.POINTER(KgwMgroupedArgs), ctypes.c_void_p, ctypes.c_size_t,
@@ -243,6 +247,17 @@ def kgw_mgrouped_bf16(args: KgwMgroupedArgs, workspace, workspace_bytes: Optiona
     rc = lib().kgw_mgrouped_bf16(ctypes.byref(args), _ptr(workspace), nbytes, _stream_handle(stream))
     if check and rc != KGW_OK:
         raise KgwError(rc, "kgw_mgrouped_bf16")
+    return rc
+
+
+def kgw_wgrad_fp4_ue8m0(args: KgwArgs, sfa_packed, sfb_packed, workspace, workspace_bytes: Optional[int] = None,
+                        stream=None, check: bool = True) -> int:
+    """FP4 e2m1 operands (packed uint8, K-major A and B) with packed UE8M0 scales per 32 tokens."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_wgrad_fp4_ue8m0(ctypes.byref(args), _ptr(sfa_packed), _ptr(sfb_packed), _ptr(workspace), nbytes,
+                                   _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_fp4_ue8m0")
     return rc
 
 

@@ -95,7 +95,7 @@ int32_t slot_cap(const kgw_wgrad_args* a, bool fp8) {
   return static_cast<int32_t>(bound < kgw::MAX_PARTIAL_SLOTS ? bound : kgw::MAX_PARTIAL_SLOTS);
 }
 
-kgw_status validate(const kgw_wgrad_args* a, bool fp8) {
+kgw_status validate(const kgw_wgrad_args* a, bool fp8, bool fp4 = false) {
   if (!a) return KGW_ERR_INVALID_ARG;
   if (a->num_experts < 1 || a->num_experts > kgw::MAX_EXPERTS) return KGW_ERR_INVALID_ARG;
   if (a->hidden <= 0 || a->intermediate <= 0 || a->tokens_sum < 0) return KGW_ERR_INVALID_ARG;
@@ -107,6 +107,9 @@ kgw_status validate(const kgw_wgrad_args* a, bool fp8) {
   if (a->out_dtype != KGW_OUT_F32 && a->out_dtype != KGW_OUT_BF16 && a->out_dtype != KGW_OUT_F16)
     return KGW_ERR_INVALID_ARG;
   if (a->accumulate != 0 && a->accumulate != 1) return KGW_ERR_INVALID_ARG;
+  // FP4: both operands K-major (the token axis packed two elements per byte), tensor2d order
+  if (fp4 && (a->a_major != KGW_K_MAJOR || a->b_major != KGW_K_MAJOR || a->input_order != KGW_TENSOR2D))
+    return KGW_ERR_UNSUPPORTED;
   if (!a->offsets) return KGW_ERR_INVALID_ARG;
   if ((a->out == nullptr) == (a->out_ptrs == nullptr)) return KGW_ERR_INVALID_ARG;
   if (!aligned(a->offsets, 4)) return KGW_ERR_ALIGNMENT;
@@ -151,8 +154,8 @@ struct Prepared {
 };
 
 kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws,
-                   size_t ws_bytes, Prepared* P) {
-  kgw_status st = validate(a, fp8);
+                   size_t ws_bytes, Prepared* P, bool fp4 = false) {
+  kgw_status st = validate(a, fp8, fp4);
   if (st != KGW_OK) return st;
   if (fp8 && !kgw::fp8_supported()) return KGW_ERR_UNSUPPORTED;
   if (fp8 && a->tokens_sum > 0) {
@@ -179,7 +182,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   if (dev.major != 10 || dev.minor != 3) return KGW_ERR_DEVICE;
   if (get_encoder() != KGW_OK) return KGW_ERR_CUDA;
 
-  const int bk = bk_of(fp8);
+  const int bk = fp4 ? kgw::BK_FP4 : bk_of(fp8);
   const uint64_t esz = fp8 ? 1 : 2;
   std::memset(&P->tmA, 0, sizeof(P->tmA));
   std::memset(&P->tmB, 0, sizeof(P->tmB));
@@ -205,8 +208,15 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
       if (r == KGW_OK) r = encode_2d(large, dt, base, n_large, rows, n_large * esz, bk, box_rows);
       return r;
     };
+    if (fp4) {
+      // packed e2m1: the tensors count bytes along the token axis (two tokens per byte)
+      st = encode_2d(&P->tmA, dt, a->a, Ts / 2, H, Ts / 2, 128, kgw::BM);             // [H, tokens/2]
+      if (st == KGW_OK) st = encode_2d(&P->tmB, dt, a->b, Ts / 2, I, Ts / 2, 128, kgw::BN);  // [I, tokens/2]
+      if (st != KGW_OK) return st;
+    }
     // A
-    if (a_k && !ragged) {
+    if (fp4) {
+    } else if (a_k && !ragged) {
       st = encode_2d(&P->tmA, dt, a->a, Ts, H, Ts * esz, bk, kgw::BM);             // [H, tokens]
     } else if (a_k) {
       st = templates(a->a, H, kgw::BM, &P->tpl.a_small, &P->tpl.a_large);
@@ -216,7 +226,8 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     }
     if (st != KGW_OK) return st;
     // B
-    if (b_k && !ragged) {
+    if (fp4) {
+    } else if (b_k && !ragged) {
       st = encode_2d(&P->tmB, dt, a->b, Ts, I, Ts * esz, bk, b_rows_cta);         // [I, tokens]
     } else if (b_k) {
       st = templates(a->b, I, b_rows_cta, &P->tpl.b_small, &P->tpl.b_large);
@@ -282,15 +293,16 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
 }
 
 kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws, size_t ws_bytes,
-               void* stream, bool sf_packed = false) {
+               void* stream, bool sf_packed = false, bool fp4 = false) {
   Prepared P;
-  kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P);
+  kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P, fp4);
   if (st != KGW_OK) return st;
   P.mp.sf_packed = sf_packed;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kgw::launch_plan(P.pp, P.tpl, s) != cudaSuccess) return KGW_ERR_CUDA;
-  cudaError_t e = fp8 ? kgw::launch_main_fp8(P.mp, P.tmA, P.tmB, P.grid, s)
-                      : kgw::launch_main_bf16(P.mp, P.tmA, P.tmB, P.grid, s);
+  cudaError_t e = fp4 ? kgw::launch_main_fp4(P.mp, P.tmA, P.tmB, P.grid, s)
+                 : fp8 ? kgw::launch_main_fp8(P.mp, P.tmA, P.tmB, P.grid, s)
+                       : kgw::launch_main_bf16(P.mp, P.tmA, P.tmB, P.grid, s);
   return e == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
 }
 
@@ -450,6 +462,12 @@ kgw_status kgw_wgrad_fp8_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
                                void* workspace, size_t workspace_bytes, void* stream) {
   return run(args, true, reinterpret_cast<const float*>(sfa_packed), reinterpret_cast<const float*>(sfb_packed),
              workspace, workspace_bytes, stream, true);
+}
+
+kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return run(args, true, reinterpret_cast<const float*>(sfa_packed), reinterpret_cast<const float*>(sfb_packed),
+             workspace, workspace_bytes, stream, true, true);
 }
 
 kgw_status kgw_wgrad_bf16_noalloc(const kgw_wgrad_args* args, void* stream) {

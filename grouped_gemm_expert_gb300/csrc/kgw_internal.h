@@ -15,6 +15,7 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK_BF16 = 64;    // 64 bf16 = 128 bytes
 constexpr int BK_FP8 = 128;    // 128 e4m3 = 128 bytes = one scale block
+constexpr int BK_FP4 = 256;    // 256 e2m1 = 128 bytes = two 128-token scale words
 constexpr int STAGES = 4;          // single-CTA ring: 4 x 48 KiB
 constexpr int STAGES_PAIR = 6;     // CTA-pair ring: 6 x 32 KiB per CTA
 constexpr int MAX_STAGES = 6;
@@ -55,6 +56,11 @@ constexpr uint32_t SF_UE8_BLOCK = 32 * 16;
 constexpr uint32_t SF_SMEM_PAD = 4096;
 constexpr uint32_t SF_A_COLS = 4;
 constexpr uint32_t SF_STAGE_COLS = 12;
+// FP4 stages: two 128-token scale words per row/column (A 2 x 128, B 2 x 256 words, 3 KiB),
+// converted in place into 6 blocks (A word 0, A word 1, B word 0 columns 0..127 / 128..255,
+// B word 1 likewise) that land in 24 TMEM columns per stage.
+constexpr uint32_t SF_SMEM_BYTES_FP4 = 2 * (BM + BN) * 4;
+constexpr uint32_t SF_STAGE_COLS_FP4 = 24;
 
 struct PlanHeader {
   int32_t error;          // kgw_status found by the plan kernel (0 = OK)
@@ -162,6 +168,8 @@ cudaError_t launch_plan(const PlanParams& p, const MapTemplates& t, cudaStream_t
 cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                              cudaStream_t s);
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                            cudaStream_t s);
+cudaError_t launch_main_fp4(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s);
 // M-grouped GEMM (rows of A grouped by expert, each group with its own B): schedule + main kernel.
 cudaError_t launch_plan_mgrouped(const PlanParams& p, cudaStream_t s);

@@ -523,13 +523,16 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
 //    128 rows of A and 128 columns of B; the even CTA issues tcgen05.mma.cta_group::2, which reads
 //    both CTAs' shared memory and writes each CTA's 128 rows into its own TMEM. Per SM this moves
 //    32 KiB per k-iteration into shared memory instead of 48 KiB.
-template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false>
+// kFp8 selects the block-scaled path (scale-factor converter, one accumulator); kFp4 narrows it
+// to e2m1 operands (kind::mxf4, 256 tokens per stage, K-major A and B, UE8M0 words only).
+template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false>
 __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
   // FP8 runs on single CTAs: a CTA-pair version (block-scaled cta_group::2 MMA, scale factors of
   // all 256 B columns in each CTA's TMEM) was correct but 1.85x slower on the FP8 workload.
   static_assert(!(kFp8 && kPair), "the FP8 path runs on single CTAs");
+  static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
   constexpr int kStages = kPair ? STAGES_PAIR : STAGES;
   constexpr uint32_t kStageB = kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
   constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB + (kFp8 ? SF_SMEM_PAD : 0u);
@@ -537,7 +540,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
   constexpr int kHalves = kPair ? 2 : 1;
   extern __shared__ uint8_t smem_raw[];
-  const int bk = kFp8 ? BK_FP8 : BK_BF16;
+  const int bk = kFp4 ? BK_FP4 : (kFp8 ? BK_FP8 : BK_BF16);
   pdl_wait();  // the plan of this call is complete and visible
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
   if (hdr->error != 0) return;  // offsets/pointers rejected by the plan: write nothing
@@ -682,7 +685,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           };
           // token coordinate: relative to the expert's block for per-expert descriptors (and for
           // the M-grouped GEMM, whose K axis is the fixed contraction axis)
-          const int32_t kx = (kMG || p.ragged) ? kb * bk : static_cast<int32_t>(tok);
+          // (FP4: the TMA tensor counts bytes, two tokens each)
+          const int32_t kx = ((kMG || p.ragged) ? kb * bk : static_cast<int32_t>(tok)) / (kFp4 ? 2 : 1);
           // M-grouped: group e's B occupies rows [e*N, e*N+N) (K-major) or [e*K, e*K+K) (N-major)
           const int32_t b_row = kMG ? it.e * p.I + b_col : b_col;
           const int32_t b_tok = kMG ? it.e * p.K + kb * bk : static_cast<int32_t>(tok);
@@ -703,7 +707,17 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             for (int j = 0; j < BN / kHalves / kAtom; ++j)
               load(sB + j * bk * 128, &tmB, b_col + kAtom * j, b_tok);
           }
-          if constexpr (kFp8) {
+          if constexpr (kFp4) {
+            // the two 128-token scale words of this 256-token stage: [A word 0][A word 1]
+            // [B word 0][B word 1], on the stage's scale barrier
+            const int64_t kblk = tok / SCALE_BLOCK;
+            uint8_t* sS = sB + kStageB;
+            mbar_arrive_expect_tx(&ctl->sfdata[stage], SF_SMEM_BYTES_FP4);
+            bulk_load(sS, p.sfa + kblk * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
+            bulk_load(sS + BM * 4, p.sfa + (kblk + 1) * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
+            bulk_load(sS + 2 * BM * 4, p.sfb + kblk * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
+            bulk_load(sS + 2 * BM * 4 + BN * 4, p.sfb + (kblk + 1) * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
+          } else if constexpr (kFp8) {
             // this 128-token block's FP32 scales: the tile's 128 rows of A and 256 columns of B;
             // they complete on the stage's scale barrier
             const int64_t kblk = tok / SCALE_BLOCK;
@@ -743,8 +757,9 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       uint32_t phase = 0;
       int tcount = 0;
       constexpr uint32_t a_mn = kAK ? 0u : 1u, b_mn = kBK ? 0u : 1u;
-      const uint32_t idesc = kFp8 ? idesc_mxf8(BM * kHalves, BN, a_mn, b_mn, 0)
-                                  : idesc_bf16_f32(BM * kHalves, BN, a_mn, b_mn);
+      const uint32_t idesc = kFp4 ? idesc_mxf4(BM, BN)
+                             : kFp8 ? idesc_mxf8(BM * kHalves, BN, a_mn, b_mn, 0)
+                                    : idesc_bf16_f32(BM * kHalves, BN, a_mn, b_mn);
       // Shared-memory operand descriptors (128-byte swizzle). K-major: 128-byte rows, 8-row groups
       // 1024 B apart, K step of 32 bytes. MN-major: 128-byte atoms of rows/columns stacked along K
       // (one atom = bk x 128 B, LBO between atoms), 8-row K groups 1024 B apart, K step of
@@ -791,7 +806,20 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * kStageBytes);
           const uint32_t b_addr = a_addr + STAGE_A_BYTES;
-          if constexpr (kFp8) {
+          if constexpr (kFp4) {
+            // 6 scale blocks of this stage -> TMEM columns 4i of the stage's 24; MMA k (64 tokens)
+            // reads word k/2 of A (columns 0/4) and B (8/16), byte pair (k%2)*2 of it
+            const uint32_t sf = tmem_base + SF_COL0 + stage * SF_STAGE_COLS_FP4;
+            const uint32_t ue8 = b_addr + kStageB;
+#pragma unroll
+            for (int blk = 0; blk < 6; ++blk)
+              tmem_cp_32x128b_warpx4(sf + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_mxf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k),
+                       idesc | idesc_sf_id(static_cast<uint32_t>(k & 1) * 2u), sf + 4 * (k >> 1), sf + 8 + 8 * (k >> 1),
+                       (kb > it.kbeg || k > 0) ? 1u : 0u);
+          } else if constexpr (kFp8) {
             const uint32_t sfa = tmem_base + SF_COL0 + stage * SF_STAGE_COLS;
             const uint32_t sfb = sfa + SF_A_COLS;
             // scale factors of this stage: shared memory (TMEM layout) -> TMEM, in order before the MMAs
@@ -1007,6 +1035,44 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             break;
           }
           uint8_t* sS = stage_mem + size_t(stage) * kStageBytes + STAGE_A_BYTES + kStageB;
+          if constexpr (kFp4) {
+            // packed UE8M0 words, two per row/column; rearranged in place into the 6 TMEM blocks
+            uint32_t* sw = reinterpret_cast<uint32_t*>(sS);
+            uint32_t a0[4], a1[4], b0[8], b1[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              a0[j] = sw[32 * j + lane];
+              a1[j] = sw[BM + 32 * j + lane];
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              b0[j] = sw[2 * BM + 32 * j + lane];
+              b1[j] = sw[2 * BM + BN + 32 * j + lane];
+            }
+            __syncwarp();  // every lane has read its words before any is overwritten
+            const bool bad = has_ue8m0_nan(make_uint4(a0[0], a0[1], a0[2], a0[3])) ||
+                             has_ue8m0_nan(make_uint4(a1[0], a1[1], a1[2], a1[3])) ||
+                             has_ue8m0_nan(make_uint4(b0[0], b0[1], b0[2], b0[3])) ||
+                             has_ue8m0_nan(make_uint4(b0[4], b0[5], b0[6], b0[7])) ||
+                             has_ue8m0_nan(make_uint4(b1[0], b1[1], b1[2], b1[3])) ||
+                             has_ue8m0_nan(make_uint4(b1[4], b1[5], b1[6], b1[7]));
+            if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
+            uint4* ue = reinterpret_cast<uint4*>(sS);
+            ue[lane] = make_uint4(a0[0], a0[1], a0[2], a0[3]);
+            ue[32 + lane] = make_uint4(a1[0], a1[1], a1[2], a1[3]);
+            ue[64 + lane] = make_uint4(b0[0], b0[1], b0[2], b0[3]);
+            ue[96 + lane] = make_uint4(b0[4], b0[5], b0[6], b0[7]);
+            ue[128 + lane] = make_uint4(b1[0], b1[1], b1[2], b1[3]);
+            ue[160 + lane] = make_uint4(b1[4], b1[5], b1[6], b1[7]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->sf_full[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           const float* sa = reinterpret_cast<const float*>(sS);
           const float* sb = sa + BM;
           uint4* ue = reinterpret_cast<uint4*>(sS + SF_UE8_OFFSET);
@@ -1082,10 +1148,10 @@ cudaError_t launch_plan(const PlanParams& p, const MapTemplates& t, cudaStream_t
   return cudaGetLastError();
 }
 
-template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false>
+template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false>
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
-  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG>;
+  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG, kFp4>;
   const size_t smem = main_smem_bytes(kPair, kFp8);
   // set on every launch: the attribute is per device and the call is cheap
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -1133,6 +1199,11 @@ cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, co
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s) {
   return launch_orders<true, false>(p, tmA, tmB, grid, s);
+}
+
+cudaError_t launch_main_fp4(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                            cudaStream_t s) {
+  return launch_main<true, false, true, true, false, true>(p, tmA, tmB, grid, s);
 }
 
 bool fp8_supported() { return true; }

@@ -141,6 +141,20 @@ kgw_status kgw_wgrad_fp8_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * FP4 block-scaled variant ("How to Use K-Grouped GEMM for MoE Weight Backward Pass in DeepGEMM",
+ * steps 1-2: both operands cast to FP4 with the same gran_k = 32; "Grouped GEMM + WGrad (Unified)",
+ * the legacy block-scaled backend selected by a matching FP4 operand pair). a, b: e2m1 (1 sign,
+ * 2 exponent bits with bias 1, 1 mantissa bit; values 0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte
+ * along the token axis with the earlier token in the low nibble. Both operands K-major: A stored
+ * [hidden, tokens_sum/2] bytes, B stored [intermediate, tokens_sum/2] bytes (a_major = b_major =
+ * KGW_K_MAJOR), tensor2d input order; anything else is KGW_ERR_UNSUPPORTED. Scales as in
+ * kgw_wgrad_fp8_ue8m0 (packed UE8M0 words, one byte per 32 tokens). Workspace as for FP8
+ * (kgw_workspace_size with is_fp8 = 1).
+ */
+kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * kgw_wgrad_bf16 without a workspace argument and without any device allocation.
  *
  * The paper has no counterpart to this entry point. It exists for callers that cannot allocate

@@ -87,8 +87,10 @@ def run_gpu(w, x, device="cuda", status=None, workspace=None, outputs=None):
                          b_major=kgw.KGW_K_MAJOR if w.b_major == "k" else kgw.KGW_MN_MAJOR,
                          status_dev=status)
     if workspace is None:
-        workspace = kgw.workspace_for(args, w.fp8, device=device)
-    if w.fp8 and w.sf_format == "ue8m0_32":
+        workspace = kgw.workspace_for(args, w.fp8 or w.fp4, device=device)
+    if w.fp4:
+        kgw.kgw_wgrad_fp4_ue8m0(args, x.sfa, x.sfb, workspace)
+    elif w.fp8 and w.sf_format == "ue8m0_32":
         kgw.kgw_wgrad_fp8_ue8m0(args, x.sfa, x.sfb, workspace)
     elif w.fp8:
         kgw.kgw_wgrad_fp8_blockscaled(args, x.sfa, x.sfb, workspace)
@@ -99,14 +101,14 @@ def run_gpu(w, x, device="cuda", status=None, workspace=None, outputs=None):
 
 def oracle_full(w, x_cpu):
     import oracle.kgw_oracle as O
-    dec_bits = bits8 if w.fp8 else bits16
+    dec_bits = bits8 if (w.fp8 or w.fp4) else bits16
     c = None if x_cpu.c is None else to_f64(x_cpu.c)
     return O.wgrad_from_storage(dec_bits(x_cpu.a), dec_bits(x_cpu.b), x_cpu.offsets.numpy(), w.hidden,
                                 w.intermediate, input_order=w.input_order, fp8=w.fp8,
                                 sfa=None if x_cpu.sfa is None else x_cpu.sfa.numpy(),
                                 sfb=None if x_cpu.sfb is None else x_cpu.sfb.numpy(),
                                 c_init=c, accumulate=w.accumulate, a_major=w.a_major, b_major=w.b_major,
-                                sf_format=w.sf_format)
+                                sf_format=w.sf_format, fp4=w.fp4)
 
 
 def assert_close_to_oracle(w, got: np.ndarray, ref: np.ndarray, S: np.ndarray, c_init=None):

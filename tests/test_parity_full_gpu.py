@@ -40,7 +40,7 @@ def _check_full(w):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, kgw.kgw_status_string(int(status.item()))
     assert outs.guards_intact()
-    bits = bits8 if w.fp8 else bits16
+    bits = bits8 if (w.fp8 or w.fp4) else bits16
     a_bits, b_bits = bits(x_cpu.a), bits(x_cpu.b)
     offsets = x_cpu.offsets.numpy()
     sfa = None if x_cpu.sfa is None else x_cpu.sfa.numpy()
@@ -50,7 +50,7 @@ def _check_full(w):
     for (e, m, n) in _samples(w, rng):
         r, s = O.element_from_storage(a_bits, b_bits, offsets, w.hidden, w.intermediate, e, m, n,
                                       input_order=w.input_order, fp8=w.fp8, sfa=sfa, sfb=sfb,
-                                      a_major=w.a_major, b_major=w.b_major, sf_format=w.sf_format)
+                                      a_major=w.a_major, b_major=w.b_major, sf_format=w.sf_format, fp4=w.fp4)
         c = float(x_cpu.c[e, m, n].to(torch.float64)) if w.accumulate else 0.0
         ref = c + r
         got = float(outs.views[e][m, n].to(torch.float64).item())
@@ -94,3 +94,8 @@ def test_full_balanced_token_major_a():
     """The balanced workload with A = dY^T read from dY stored token-major (M-major A)."""
     import dataclasses
     _check_full(dataclasses.replace(W.balanced(), a_major="mn"))
+
+
+def test_full_fp4_blockscaled():
+    """FP4 e2m1 operands with UE8M0 scales per 32 tokens, at the FP8 workload's shape."""
+    _check_full(W.fp4())

@@ -90,6 +90,15 @@ CASES = {
     "fp8_pair_ragged_split_k": W.custom(3, 512, 512, [16384, 0, 768], seed=68, fp8=True, input_order="ragged",
                                         out_dtype="bf16"),
     "fp8_single_cta_accumulate": W.custom(2, 384, 512, [1280, 512], seed=69, fp8=True, accumulate=True),
+    # FP4 e2m1, K-major A and B, UE8M0 scales per 32 tokens (256 tokens per pipeline stage)
+    "fp4_bf16_out": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=110, fp4=True, b_major="k",
+                             sf_format="ue8m0_32", out_dtype="bf16"),
+    "fp4_f32_multi_tile": W.custom(3, 384, 768, [256, 2048, 0], seed=111, fp4=True, b_major="k",
+                                   sf_format="ue8m0_32"),
+    "fp4_split_k_accumulate": W.custom(3, 128, 256, [32768, 0, 256], seed=112, fp4=True, b_major="k",
+                                       sf_format="ue8m0_32", accumulate=True),
+    "fp4_discrete_f16": W.custom(3, 256, 256, [1024, 512, 256], seed=113, fp4=True, b_major="k",
+                                 sf_format="ue8m0_32", out_dtype="f16", output_mode="discrete"),
 }
 
 
@@ -228,3 +237,16 @@ def test_small_workspace_still_correct():
     assert_close_to_oracle(w, to_f64(outs.stacked()), ref, S)
     assert_close_to_oracle(w, to_f64(full), ref, S)
     assert not torch.equal(full, outs.stacked())  # split-K really changed the summation order
+
+
+def test_fp4_rejects_unsupported_layouts():
+    """FP4 needs K-major A and B in tensor2d order: anything else is KGW_ERR_UNSUPPORTED, host-side."""
+    kgw = ensure_built()
+    w = W.custom(2, 128, 256, [256, 256], seed=114, fp4=True, b_major="k", sf_format="ue8m0_32")
+    x = W.make_inputs(w, DEV)
+    out = torch.empty((2, 128, 256), dtype=torch.float32, device=DEV)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=DEV)
+    for kw in ({"b_major": kgw.KGW_MN_MAJOR}, {"a_major": kgw.KGW_MN_MAJOR}, {"input_order": kgw.KGW_RAGGED}):
+        args = kgw.make_args(2, 128, 256, 512, x.a, x.b, x.offsets, out=out,
+                             **{"b_major": kgw.KGW_K_MAJOR, **kw})
+        assert kgw.kgw_wgrad_fp4_ue8m0(args, x.sfa, x.sfb, ws, check=False) == kgw.KGW_ERR_UNSUPPORTED

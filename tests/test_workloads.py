@@ -63,3 +63,25 @@ def test_fp8_inputs_have_scales():
     assert x.a.dtype == torch.float8_e4m3fn and x.b.dtype == torch.float8_e4m3fn
     assert x.sfa.shape == (4, 128) and x.sfb.shape == (4, 256)
     assert x.sfa.dtype == torch.float32
+
+
+def test_fp4_quantiser_follows_the_rounding_rule():
+    """The chunked torch quantiser rounds exactly like the plain per-element rule (nearest e2m1
+    value, ties to the even code), including every midpoint."""
+    import numpy as np
+    import torch
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(48, 512, generator=g) * 3
+    mids = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0])
+    x[0:2, :32] = 0.0
+    x[0, :8], x[1, :8] = mids, -mids              # blocks with amax 6: scale 1, exact midpoints
+    q, _ = W.quantize_e2m1_ue8m0_32(x, 1)
+    xt = x.double().numpy().reshape(48, 16, 32)
+    v = np.abs(xt).max(2) / 6.0
+    fr, ex = np.frexp(v)
+    k = np.where(v == 0, 0, np.where(fr == 0.5, ex - 1, ex))
+    codes = W.e2m1_codes(xt / np.ldexp(1.0, k)[..., None]).reshape(48, 512)
+    ref = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    assert np.array_equal(q.numpy(), ref)
+    assert q.numpy()[0, :4].tolist() == [0x20, 0x42, 0x64, 0x76]
+    assert q.numpy()[1, :4].tolist() == [0xA0, 0xCA, 0xEC, 0xFE]

@@ -258,28 +258,43 @@ def e2m1_codes(v: np.ndarray) -> np.ndarray:
     return (code | np.where(np.signbit(v) & (code != 0), 8, 0)).astype(np.uint8)
 
 
+_E2M1_MIDS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+
+
 def quantize_e2m1_ue8m0_32(x: torch.Tensor, token_axis: int):
     """Quantise ``x`` (float32 2-D) to FP4 e2m1 with one power-of-two scale per 32 tokens.
 
     Returns (packed uint8 [other, tokens/2]: the token axis contiguous, two elements per byte, the
     first in the low nibble; packed UE8M0 words int32 [tokens/128, other] as in
     ``quantize_e4m3_ue8m0_32``). The scale is 2**ceil(log2(amax/6)) (1 for amax 0), so
-    |x/scale| <= 6 and nothing saturates.
+    |x/scale| <= 6 and nothing saturates; elements round to the nearest e2m1 value, ties to the
+    even code (the same rule as ``e2m1_codes``).
     """
     assert x.dim() == 2 and x.dtype == torch.float32
-    xt = (x if token_axis == 1 else x.t()).double().numpy()
+    xt = (x if token_axis == 1 else x.t()).contiguous()
     other, tokens = xt.shape
     assert tokens % FP8_BLOCK == 0
-    blocks = xt.reshape(other, tokens // 32, 32)
-    amax = np.abs(blocks).max(axis=2)
+    blocks = xt.view(other, tokens // 32, 32)
+    amax = blocks.abs().amax(dim=2).double().numpy()
     v = amax / E2M1_MAX
     frac, ex = np.frexp(v)
     k = np.where(v == 0.0, 0, np.where(frac == 0.5, ex - 1, ex)).astype(np.int64)
-    codes = e2m1_codes(blocks / np.ldexp(1.0, k)[..., None]).reshape(other, tokens)
-    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    scale = torch.from_numpy(np.ldexp(1.0, k).astype(np.float32))
+    mids = torch.tensor(_E2M1_MIDS, dtype=torch.float32)
+    packed = torch.empty((other, tokens // 2), dtype=torch.uint8)
+    step = max(1, (1 << 22) // tokens)
+    for r0 in range(0, other, step):          # row chunks bound the temporaries
+        y = blocks[r0:r0 + step] / scale[r0:r0 + step, :, None]    # exact: power-of-two scale
+        a = y.abs().reshape(-1)
+        code = torch.bucketize(a, mids)                              # ties land on the lower code
+        tie_up = (code < 7) & (a == mids[code.clamp(max=6)]) & ((code & 1) == 1)
+        code = code + tie_up.to(code.dtype)
+        neg = torch.signbit(y.reshape(-1)) & (code != 0)
+        code = (code | (neg.to(code.dtype) << 3)).to(torch.uint8).view(-1, tokens)
+        packed[r0:r0 + step] = code[:, 0::2] | (code[:, 1::2] << 4)
     byte = (k + 127).astype(np.uint32).reshape(other, tokens // 128, 4)
     words = (byte[..., 0] | (byte[..., 1] << 8) | (byte[..., 2] << 16) | (byte[..., 3] << 24)).astype(np.uint32)
-    return torch.from_numpy(np.ascontiguousarray(packed)), torch.from_numpy(words.view(np.int32).T.copy())
+    return packed, torch.from_numpy(words.view(np.int32).T.copy())
 
 
 def pack_ragged_a(a2d: torch.Tensor, counts) -> torch.Tensor:
