@@ -207,6 +207,8 @@ def run_ours(args, w, rank, local, world):
             kgw.kgw_wgrad_fp8_ue8m0(args, sfa, sfb, ws, stream=s)
         elif w.fp8:
             kgw.kgw_wgrad_fp8_blockscaled(args, sfa, sfb, ws, stream=s)
+        elif w.unaligned:
+            kgw.kgw_wgrad_bf16_unaligned(args, ws, stream=s)
         else:
             kgw.kgw_wgrad_bf16(args, ws, stream=s)
 

@@ -17,6 +17,7 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_debug_check_ragged_maps(args, is_fp8, host_offsets, workspace) -> int
   kgw_wgrad_fp8_ue8m0(args, sfa_packed, sfb_packed, workspace, stream=None)
   kgw_wgrad_fp4_ue8m0(args, sfa_packed, sfb_packed, workspace, stream=None)
+  kgw_wgrad_bf16_unaligned(args, workspace, stream=None)
   kgw_mgrouped_workspace_size(args) -> int
   kgw_mgrouped_bf16(args, workspace, stream=None)
 
@@ -57,7 +58,8 @@ KGW_MG_MASKED = 2
 EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
             "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc",
             "kgw_debug_check_ragged_maps", "kgw_wgrad_fp8_ue8m0", "kgw_mgrouped_workspace_size",
-            "kgw_mgrouped_bf16", "kgw_wgrad_fp4_ue8m0")
+            "kgw_mgrouped_bf16", "kgw_wgrad_fp4_ue8m0", "kgw_wgrad_bf16_unaligned",
+            "kgw_debug_check_tail_maps")
 
 
 class KgwArgs(ctypes.Structure):
@@ -129,6 +131,9 @@ def lib() -> ctypes.CDLL:
         L.kgw_wgrad_fp4_ue8m0.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.kgw_wgrad_fp4_ue8m0.restype = ctypes.c_int
+        L.kgw_wgrad_bf16_unaligned.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_size_t,
+                                               ctypes.c_void_p]
+        L.kgw_wgrad_bf16_unaligned.restype = ctypes.c_int
         L.kgw_mgrouped_workspace_size.argtypes = [ctypes.POINTER(KgwMgroupedArgs), ctypes.POINTER(ctypes.c_size_t)]
         L.kgw_mgrouped_workspace_size.restype = ctypes.c_int
         L.kgw_mgrouped_bf16.argtypes = [ctypes.POINTER(KgwMgroupedArgs), ctypes.c_void_p, ctypes.c_size_t,
@@ -143,6 +148,9 @@ def lib() -> ctypes.CDLL:
         L.kgw_debug_check_ragged_maps.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_int32, ctypes.c_void_p,
                                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.kgw_debug_check_ragged_maps.restype = ctypes.c_int32
+        L.kgw_debug_check_tail_maps.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_debug_check_tail_maps.restype = ctypes.c_int32
         L.kgw_debug_set.argtypes = [ctypes.c_int32, ctypes.c_int64]
         L.kgw_debug_set.restype = ctypes.c_int64
         _lib = L
@@ -210,6 +218,16 @@ def kgw_wgrad_bf16(args: KgwArgs, workspace, workspace_bytes: Optional[int] = No
     rc = lib().kgw_wgrad_bf16(ctypes.byref(args), _ptr(workspace), nbytes, _stream_handle(stream))
     if check and rc != KGW_OK:
         raise KgwError(rc, "kgw_wgrad_bf16")
+    return rc
+
+
+def kgw_wgrad_bf16_unaligned(args: KgwArgs, workspace, workspace_bytes: Optional[int] = None, stream=None,
+                             check: bool = True) -> int:
+    """kgw_wgrad_bf16 with token counts that are multiples of 8 (any count if A and B are MN-major)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_wgrad_bf16_unaligned(ctypes.byref(args), _ptr(workspace), nbytes, _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_bf16_unaligned")
     return rc
 
 
@@ -283,6 +301,16 @@ def kgw_debug_check_ragged_maps(args: KgwArgs, is_fp8: bool, host_offsets, works
     dump = None if host_dump is None else host_dump.ctypes.data
     return int(lib().kgw_debug_check_ragged_maps(ctypes.byref(args), int(bool(is_fp8)), offs.ctypes.data,
                                                  _ptr(workspace), nbytes, dump))
+
+
+def kgw_debug_check_tail_maps(args: KgwArgs, host_offsets, workspace, workspace_bytes: Optional[int] = None,
+                              host_dump=None) -> int:
+    """Testing hook: number of per-expert token-tail descriptors that differ from host encodings."""
+    import numpy as np
+    offs = np.ascontiguousarray(np.asarray(host_offsets, dtype=np.int32))
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    dump = None if host_dump is None else host_dump.ctypes.data
+    return int(lib().kgw_debug_check_tail_maps(ctypes.byref(args), offs.ctypes.data, _ptr(workspace), nbytes, dump))
 
 
 # ---------------------------------------------------------------------------------------------

@@ -95,11 +95,13 @@ int32_t slot_cap(const kgw_wgrad_args* a, bool fp8) {
   return static_cast<int32_t>(bound < kgw::MAX_PARTIAL_SLOTS ? bound : kgw::MAX_PARTIAL_SLOTS);
 }
 
-kgw_status validate(const kgw_wgrad_args* a, bool fp8, bool fp4 = false) {
+// count_align: the multiple every token count (and tokens_sum) must be: the pages' 256, or the
+// unaligned entry point's 8 (a K-major operand: 16-byte TMA coordinates) / 1 (both MN-major).
+kgw_status validate(const kgw_wgrad_args* a, bool fp8, bool fp4 = false, int64_t count_align = kgw::TOKEN_ALIGN) {
   if (!a) return KGW_ERR_INVALID_ARG;
   if (a->num_experts < 1 || a->num_experts > kgw::MAX_EXPERTS) return KGW_ERR_INVALID_ARG;
   if (a->hidden <= 0 || a->intermediate <= 0 || a->tokens_sum < 0) return KGW_ERR_INVALID_ARG;
-  if (a->tokens_sum % kgw::TOKEN_ALIGN != 0) return KGW_ERR_INVALID_ARG;
+  if (a->tokens_sum % count_align != 0) return KGW_ERR_INVALID_ARG;
   if (a->hidden % kgw::BM != 0 || a->intermediate % kgw::BN != 0) return KGW_ERR_UNSUPPORTED;
   if (a->a_major != KGW_K_MAJOR && a->a_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
   if (a->b_major != KGW_K_MAJOR && a->b_major != KGW_MN_MAJOR) return KGW_ERR_INVALID_ARG;
@@ -153,9 +155,16 @@ struct Prepared {
   int grid;
 };
 
+// Token-count multiple of the unaligned BF16 entry: 8 when an operand stores tokens innermost
+// (TMA coordinates must start on 16 bytes), else 1.
+int64_t unaligned_count_multiple(const kgw_wgrad_args* a) {
+  return (a->a_major == KGW_K_MAJOR || a->b_major == KGW_K_MAJOR) ? 8 : 1;
+}
+
 kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws,
-                   size_t ws_bytes, Prepared* P, bool fp4 = false) {
-  kgw_status st = validate(a, fp8, fp4);
+                   size_t ws_bytes, Prepared* P, bool fp4 = false, bool tail = false) {
+  const int64_t count_align = tail ? unaligned_count_multiple(a) : kgw::TOKEN_ALIGN;
+  kgw_status st = validate(a, fp8, fp4, count_align);
   if (st != KGW_OK) return st;
   if (fp8 && !kgw::fp8_supported()) return KGW_ERR_UNSUPPORTED;
   if (fp8 && a->tokens_sum > 0) {
@@ -200,7 +209,8 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     // at/above 128 KiB; the plan kernel sets the address, n and the stride per expert.
     auto templates = [&](const void* base, uint64_t rows, uint32_t box_rows, CUtensorMap* small,
                          CUtensorMap* large) {
-      const uint64_t n_small = kgw::TOKEN_ALIGN;
+      // small class: the narrowest block (16-byte rows), under 128 KiB unless rows alone reach it
+      const uint64_t n_small = 16 / esz;
       uint64_t n_large = (kgw::TMAP_SIZE_CLASS_BYTES + rows * esz - 1) / (rows * esz);
       n_large = (n_large + kgw::TOKEN_ALIGN - 1) / kgw::TOKEN_ALIGN * kgw::TOKEN_ALIGN;
       if (n_large < n_small) n_large = n_small;
@@ -236,6 +246,28 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
       st = encode_2d(&P->tmB, dt, a->b, I, Ts, I * esz, atom, bk);                 // [tokens, I]
     }
     if (st != KGW_OK) return st;
+    if (tail) {
+      // token tails: per-expert copies of the operand's own descriptor with the token extent cut
+      // at end_e; an MN-major operand's small-class template has a token extent under 128 KiB
+      auto tail_templates = [&](const CUtensorMap& whole, const void* base, uint64_t cols, uint64_t row_bytes,
+                                bool k_major, uint32_t box_inner, uint32_t box_outer, CUtensorMap* small,
+                                CUtensorMap* large) {
+        *large = whole;
+        if (k_major) {
+          *small = whole;
+          return KGW_OK;
+        }
+        return encode_2d(small, dt, base, cols, 1, row_bytes, box_inner, box_outer);
+      };
+      if (!(ragged && a_k)) {
+        st = tail_templates(P->tmA, a->a, H, H * esz, a_k, atom, bk, &P->tpl.a_small, &P->tpl.a_large);
+        if (st != KGW_OK) return st;
+      }
+      if (!(ragged && b_k)) {
+        st = tail_templates(P->tmB, a->b, I, I * esz, b_k, atom, bk, &P->tpl.b_small, &P->tpl.b_large);
+        if (st != KGW_OK) return st;
+      }
+    }
   }
 
   kgw::PlanParams& pp = P->pp;
@@ -260,6 +292,13 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   pp.a = static_cast<const uint8_t*>(a->a);
   pp.b = static_cast<const uint8_t*>(a->b);
   pp.esz = static_cast<int32_t>(esz);
+  pp.count_align = static_cast<int32_t>(count_align);
+  if (tail && a->tokens_sum > 0) {
+    pp.tail_a = (ragged && a_k) ? 0 : (a_k ? 1 : 2);   // ragged K-major blocks already end at n_e
+    pp.tail_b = (ragged && b_k) ? 0 : (b_k ? 1 : 2);
+    pp.row_bytes_a = static_cast<uint64_t>(a->hidden) * esz;
+    pp.row_bytes_b = static_cast<uint64_t>(a->intermediate) * esz;
+  }
 
   kgw::MainParams& mp = P->mp;
   mp = kgw::MainParams{};
@@ -288,14 +327,16 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   mp.L = L;
   mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
   mp.test_drop_stage = static_cast<int32_t>(g_drop_stage.load());
+  mp.tail_a = pp.tail_a;
+  mp.tail_b = pp.tail_b;
   P->grid = grid;
   return KGW_OK;
 }
 
 kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws, size_t ws_bytes,
-               void* stream, bool sf_packed = false, bool fp4 = false) {
+               void* stream, bool sf_packed = false, bool fp4 = false, bool tail = false) {
   Prepared P;
-  kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P, fp4);
+  kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P, fp4, tail);
   if (st != KGW_OK) return st;
   P.mp.sf_packed = sf_packed;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -442,7 +483,7 @@ extern "C" {
 
 kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t* bytes) {
   if (!bytes) return KGW_ERR_INVALID_ARG;
-  kgw_status st = validate(args, is_fp8 != 0);
+  kgw_status st = validate(args, is_fp8 != 0, false, 1);  // sizing only: the call checks its own count rule
   if (st != KGW_OK) return st;
   const int32_t halves = tile_rows(args, is_fp8 != 0) / kgw::BM;
   *bytes = kgw::ws_layout(args->num_experts, slot_cap(args, is_fp8 != 0), halves).total;
@@ -462,6 +503,11 @@ kgw_status kgw_wgrad_fp8_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
                                void* workspace, size_t workspace_bytes, void* stream) {
   return run(args, true, reinterpret_cast<const float*>(sfa_packed), reinterpret_cast<const float*>(sfb_packed),
              workspace, workspace_bytes, stream, true);
+}
+
+kgw_status kgw_wgrad_bf16_unaligned(const kgw_wgrad_args* args, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  return run(args, false, nullptr, nullptr, workspace, workspace_bytes, stream, false, false, true);
 }
 
 kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
@@ -521,6 +567,66 @@ int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, 
       std::memset(&ref, 0, sizeof(ref));
       if (encode_2d(&ref, dt, base0 + begin * rows * esz, static_cast<uint64_t>(n), rows, n * esz, bk_of(fp8),
                     op == 0 ? kgw::BM : b_rows_cta) != KGW_OK) {
+        std::free(dev_maps);
+        return -KGW_ERR_CUDA;
+      }
+      const uint8_t* got = dev_maps + size_t(op) * bytes + size_t(e) * 128;
+      if (std::memcmp(&ref, got, 128) != 0) ++mismatches;
+      if (host_dump) {
+        uint8_t* d = static_cast<uint8_t*>(host_dump) + (size_t(e) * 2 + op) * 256;
+        std::memcpy(d, got, 128);
+        std::memcpy(d + 128, &ref, 128);
+      }
+    }
+  }
+  std::free(dev_maps);
+  return mismatches;
+}
+
+int32_t kgw_debug_check_tail_maps(const kgw_wgrad_args* args, const int32_t* host_offsets, void* workspace,
+                                  size_t workspace_bytes, void* host_dump) {
+  if (!args || !host_offsets || args->tokens_sum <= 0) return -KGW_ERR_INVALID_ARG;
+  Prepared P;
+  kgw_status st = prepare(args, false, nullptr, nullptr, workspace, workspace_bytes, &P, false, true);
+  if (st != KGW_OK) return -static_cast<int32_t>(st);
+  if (kgw::launch_plan(P.pp, P.tpl, nullptr) != cudaSuccess) return -KGW_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -KGW_ERR_CUDA;
+  const int32_t E = args->num_experts;
+  const size_t bytes = size_t(E) * 128;
+  uint8_t* dev_maps = static_cast<uint8_t*>(std::malloc(2 * bytes));
+  if (!dev_maps) return -KGW_ERR_INVALID_ARG;
+  if (cudaMemcpy(dev_maps, static_cast<uint8_t*>(workspace) + P.pp.L.tmaps, bytes, cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemcpy(dev_maps + bytes, static_cast<uint8_t*>(workspace) + P.pp.L.tmaps_b, bytes,
+                 cudaMemcpyDeviceToHost) != cudaSuccess) {
+    std::free(dev_maps);
+    return -KGW_ERR_CUDA;
+  }
+  const uint64_t esz = 2, Ts = static_cast<uint64_t>(args->tokens_sum);
+  const uint64_t H = static_cast<uint64_t>(args->hidden), I = static_cast<uint64_t>(args->intermediate);
+  const uint32_t b_rows_cta = static_cast<uint32_t>(kgw::BN / (P.pp.tile_m / kgw::BM));
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  int32_t mismatches = 0;
+  for (int32_t op = 0; op < 2; ++op) {
+    const int mode = op == 0 ? P.pp.tail_a : P.pp.tail_b;
+    const bool block = op == 0 ? P.pp.build_a : P.pp.build_b;   // ragged K-major: per-expert blocks
+    if (!mode && !block) continue;
+    const uint64_t rows = op == 0 ? H : I;
+    const uint8_t* base = static_cast<const uint8_t*>(op == 0 ? args->a : args->b);
+    const uint32_t box_rows = op == 0 ? kgw::BM : b_rows_cta;
+    for (int32_t e = 0; e < E; ++e) {
+      const int64_t begin = e ? host_offsets[e - 1] : 0;
+      const int64_t end = host_offsets[e];
+      if (end <= begin) continue;
+      const uint64_t n = static_cast<uint64_t>(end - begin);
+      CUtensorMap ref;
+      std::memset(&ref, 0, sizeof(ref));
+      kgw_status r = block       ? encode_2d(&ref, dt, base + begin * rows * esz, n, rows, n * esz, kgw::BK_BF16, box_rows)
+                     : mode == 1 ? encode_2d(&ref, dt, base, static_cast<uint64_t>(end), rows, Ts * esz, kgw::BK_BF16,
+                                             box_rows)
+                                 : encode_2d(&ref, dt, base, rows, static_cast<uint64_t>(end), rows * esz, 64,
+                                             kgw::BK_BF16);
+      if (r != KGW_OK) {
         std::free(dev_maps);
         return -KGW_ERR_CUDA;
       }

@@ -133,10 +133,18 @@ struct PlanParams {
   int32_t esz;                  // bytes per operand element
   int32_t mg_layout;            // M-grouped: kgw_mg_layout
   int64_t mg_m;                 // M-grouped: rows (contiguous) or rows per group (masked)
+  int32_t count_align;          // every token count must be a multiple of this (256, or 8 / 1 unaligned)
+  // token counts not multiples of the stage: per-expert descriptors whose token extent ends at
+  // the expert's last token (TMA fills the rest of its last stage with zeros). 1: the token axis
+  // is dimension 0 (K-major tensor2d operand), 2: dimension 1 (MN-major operand); the templates
+  // are the operand's own descriptor (small: for dimension-1 extents x row stride < 128 KiB)
+  int32_t tail_a, tail_b;
+  uint64_t row_bytes_a, row_bytes_b;   // row strides of MN-major operands (size class of tails)
 };
 
-// Host-encoded templates of the per-expert descriptors (ragged, K-major operands): one per
-// size class for A ([hidden, n] blocks) and for B ([intermediate, n] blocks).
+// Host-encoded templates of the per-expert descriptors (ragged, K-major operands: one per size
+// class for A ([hidden, n] blocks) and for B ([intermediate, n] blocks); token tails: the
+// operand's descriptor, and for MN-major operands the same with a small token extent).
 struct MapTemplates {
   CUtensorMap a_small, a_large, b_small, b_large;
 };
@@ -151,6 +159,7 @@ struct MainParams {
   int32_t out_f16;              // the 16-bit output is FP16
   int32_t a_kmajor, b_kmajor;   // operand storage orders (1: token axis has unit stride)
   int32_t K;                    // M-grouped GEMM: contraction length (fixed for every group)
+  int32_t tail_a, tail_b;       // per-expert descriptors with the token extent ending at end_e
   int32_t num_m_tiles, num_n_tiles;
   int32_t tile_m;               // 128 (one CTA per tile) or 256 (a CTA pair per tile)
   const float* sfa;             // FP8: [tokens_sum/128, H] FP32 (or packed UE8M0 words)

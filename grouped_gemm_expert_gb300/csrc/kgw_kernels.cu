@@ -97,14 +97,14 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     const int64_t cur = p.offsets[e];
     const int64_t n = cur - prev;
     int err = 0;
-    if (n < 0 || (n % TOKEN_ALIGN) != 0) err = KGW_ERR_OFFSETS;
+    if (n < 0 || (n % p.count_align) != 0) err = KGW_ERR_OFFSETS;
     if (e == E - 1 && cur != p.tokens_sum) err = KGW_ERR_OFFSETS;
     if (!err && p.out_ptrs) {
       const uint64_t ptr = static_cast<uint64_t>(p.out_ptrs[e]);
       if (ptr == 0 || (ptr & 15u)) err = KGW_ERR_OUT_PTRS;
     }
     if (err) atomicMax(&s_err, err == KGW_ERR_OFFSETS ? 2 : 1);
-    s_kit[e] = n > 0 ? static_cast<int32_t>(n / p.bk) : 0;
+    s_kit[e] = n > 0 ? static_cast<int32_t>((n + p.bk - 1) / p.bk) : 0;  // a partial last stage counts
   }
   __syncthreads();
   if (s_err) {
@@ -142,6 +142,35 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         tmap_set_address(dst, reinterpret_cast<uint64_t>(base + prev * rows * p.esz));
         tmap_set_dim0(dst, static_cast<uint32_t>(n));
         tmap_set_stride1(dst, static_cast<uint64_t>(n * p.esz));
+        fence_tmap_release();
+      }
+    }
+  }
+
+  // 1c. token counts that are not multiples of the stage: per-expert descriptors of the whole
+  //     operand whose token extent ends at end_e, so that TMA zero-fills the tail of the
+  //     expert's last stage instead of reading the next expert's tokens.
+  if (p.tail_a || p.tail_b) {
+    for (int e = tid; e < E; e += blockDim.x) {
+      const int64_t prev = e ? static_cast<int64_t>(p.offsets[e - 1]) : 0;
+      const int64_t end = static_cast<int64_t>(p.offsets[e]);
+      if (end <= prev) continue;
+#pragma unroll
+      for (int op = 0; op < 2; ++op) {
+        const int mode = op == 0 ? p.tail_a : p.tail_b;
+        if (!mode) continue;
+        uint4* dst = reinterpret_cast<uint4*>(p.ws + (op == 0 ? p.L.tmaps : p.L.tmaps_b) + size_t(e) * 128);
+        // dimension 0: the size class does not change; dimension 1: end_e x row stride decides it
+        const uint64_t rb = op == 0 ? p.row_bytes_a : p.row_bytes_b;
+        const bool large = mode == 1 || uint64_t(end) * rb >= TMAP_SIZE_CLASS_BYTES;
+        const CUtensorMap* t = op == 0 ? (large ? &tm.a_large : &tm.a_small) : (large ? &tm.b_large : &tm.b_small);
+        const uint4* src = reinterpret_cast<const uint4*>(t);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j] = src[j];
+        if (mode == 1)
+          tmap_set_dim0(dst, static_cast<uint32_t>(end));
+        else
+          tmap_set_dim1(dst, static_cast<uint32_t>(end));
         fence_tmap_release();
       }
     }
@@ -387,7 +416,7 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
   it.n0 = nt * BN;
   it.begin = it.e ? static_cast<int64_t>(__ldg(p.offsets + it.e - 1)) : 0;
   it.n_e = static_cast<int64_t>(__ldg(p.offsets + it.e)) - it.begin;
-  const int64_t kit = it.n_e / bk;
+  const int64_t kit = (it.n_e + bk - 1) / bk;  // a partial last stage counts (zero-filled tail)
   it.kbeg = static_cast<int>(it.split * kit / it.nsplit);
   it.kend = static_cast<int>((it.split + 1) * kit / it.nsplit);
   return it;
@@ -653,11 +682,11 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       // ragged + K-major operand: the expert's own descriptor, coordinates relative to its block
       const CUtensorMap* amap = &tmA;
       const CUtensorMap* bmap = &tmB;
-      if (kAK && p.ragged) {
+      if ((kAK && p.ragged) || p.tail_a) {
         amap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps + size_t(it.e) * 128);
         if (lane == 0 && it.kend > it.kbeg) fence_tmap_acquire(amap);
       }
-      if (kBK && p.ragged) {
+      if ((kBK && p.ragged) || p.tail_b) {
         bmap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps_b + size_t(it.e) * 128);
         if (lane == 0 && it.kend > it.kbeg) fence_tmap_acquire(bmap);
       }
@@ -697,7 +726,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < BM / kAtom; ++j)
-              load(sA + j * bk * 128, &tmA, a_row + kAtom * j, static_cast<int32_t>(tok));
+              load(sA + j * bk * 128, amap, a_row + kAtom * j, static_cast<int32_t>(tok));
           }
           // B: K-major -> one box [this CTA's columns x bk tokens]; MN-major -> boxes of 128 B of columns
           if constexpr (kBK) {
@@ -705,7 +734,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < BN / kHalves / kAtom; ++j)
-              load(sB + j * bk * 128, &tmB, b_col + kAtom * j, b_tok);
+              load(sB + j * bk * 128, bmap, b_col + kAtom * j, b_tok);
           }
           if constexpr (kFp4) {
             // the two 128-token scale words of this 256-token stage: [A word 0][A word 1]

@@ -194,6 +194,10 @@ __device__ __forceinline__ void tmap_set_dim0(void* gmap, uint32_t extent) {
   asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 0, %1;" ::"l"(gmap), "r"(extent)
                : "memory");
 }
+__device__ __forceinline__ void tmap_set_dim1(void* gmap, uint32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(gmap), "r"(extent)
+               : "memory");
+}
 // Byte stride of dimension 1 (the first strided dimension).
 __device__ __forceinline__ void tmap_set_stride1(void* gmap, uint64_t bytes) {
   asm volatile("tensormap.replace.tile.global_stride.global.b1024.b64 [%0], 0, %1;" ::"l"(gmap), "l"(bytes)

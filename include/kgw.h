@@ -116,6 +116,19 @@ kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t
 kgw_status kgw_wgrad_bf16(const kgw_wgrad_args* args, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kgw_wgrad_bf16 without the 256-token contract on the counts (an extension beyond the pages'
+ * "BF16 contract"): every per-expert count (and tokens_sum) must be a multiple of 8 when A or B
+ * stores the token axis innermost (K-major; TMA coordinates start on 16 bytes) and may be any
+ * count when both operands are MN-major. An expert's last pipeline stage is partly beyond its
+ * last token: the kernel reads it through a per-expert TMA descriptor whose token extent ends at
+ * end_e, so the rest of the stage is zero and the next expert's tokens are not read. Same
+ * operation, layouts, outputs, workspace (kgw_workspace_size) and error reporting as
+ * kgw_wgrad_bf16; a count that breaks the rule is KGW_ERR_OFFSETS on the device.
+ */
+kgw_status kgw_wgrad_bf16_unaligned(const kgw_wgrad_args* args, void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/*
  * FP8 block-scaled variant ("05 · Grouped GEMM 与 Expert 计算", section 3: per-block 1x128
  * scaling along K, scales MN-major; "Grouped GEMM + WGrad (Unified)", section "Block-scaled
  * contract"). a, b: float8 e4m3 (the "fn" encoding) in the same logical layouts as the BF16
@@ -264,6 +277,14 @@ int64_t kgw_debug_set(int32_t key, int64_t value);
  */
 int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, const int32_t* host_offsets,
                                     void* workspace, size_t workspace_bytes, void* host_dump);
+
+/* Testing hook: like kgw_debug_check_ragged_maps for every per-expert descriptor that
+ * kgw_wgrad_bf16_unaligned builds (token extent cut at end_e for tensor2d K-major and for
+ * MN-major operands; per-expert blocks for ragged K-major operands): runs the plan only and
+ * returns how many differ from host encodings (negative kgw_status on error). host_dump as for
+ * kgw_debug_check_ragged_maps. */
+int32_t kgw_debug_check_tail_maps(const kgw_wgrad_args* args, const int32_t* host_offsets, void* workspace,
+                                  size_t workspace_bytes, void* host_dump);
 
 #ifdef __cplusplus
 }

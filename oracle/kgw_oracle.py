@@ -106,14 +106,16 @@ def expert_ranges(offsets):
     return [((0 if e == 0 else off[e - 1]), off[e]) for e in range(len(off))]
 
 
-def offsets_valid(offsets, tokens_sum: int) -> bool:
+def offsets_valid(offsets, tokens_sum: int, align: int = TOKEN_ALIGN) -> bool:
+    """The offsets contract: non-decreasing, every count a multiple of ``align`` (the pages' 256
+    by default; the unaligned entry point relaxes it), last offset == tokens_sum."""
     off = [int(v) for v in np.asarray(offsets).tolist()]
     if len(off) == 0:
         return False
     prev = 0
     for v in off:
         n = v - prev
-        if n < 0 or n % TOKEN_ALIGN != 0:
+        if n < 0 or n % align != 0:
             return False
         prev = v
     return prev == tokens_sum

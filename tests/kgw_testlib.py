@@ -94,6 +94,8 @@ def run_gpu(w, x, device="cuda", status=None, workspace=None, outputs=None):
         kgw.kgw_wgrad_fp8_ue8m0(args, x.sfa, x.sfb, workspace)
     elif w.fp8:
         kgw.kgw_wgrad_fp8_blockscaled(args, x.sfa, x.sfb, workspace)
+    elif w.unaligned:
+        kgw.kgw_wgrad_bf16_unaligned(args, workspace)
     else:
         kgw.kgw_wgrad_bf16(args, workspace)
     return outs

@@ -82,9 +82,29 @@ def test_workspace_size_is_host_only_and_monotone():
 def test_host_validation(kw, code):
     args = good_args(**kw)
     assert rc_bf16(args) == code
-    if code != kgw.KGW_ERR_UNSUPPORTED or "hidden" in kw or "intermediate" in kw:
+    # the sizing call takes any token total (it also sizes kgw_wgrad_bf16_unaligned calls)
+    if (code != kgw.KGW_ERR_UNSUPPORTED or "hidden" in kw or "intermediate" in kw) and kw.get("tokens_sum") != 1000:
         n = ctypes.c_size_t(0)
         assert kgw.lib().kgw_workspace_size(ctypes.byref(args), 0, ctypes.byref(n)) == code
+
+
+@pytest.mark.parametrize("a_major,b_major,tokens_sum,code", [
+    (0, 1, 1000, None),                       # K-major A: multiples of 8 pass host validation
+    (0, 1, 1001, kgw.KGW_ERR_INVALID_ARG),
+    (1, 0, 1004, kgw.KGW_ERR_INVALID_ARG),    # K-major B: likewise
+    (1, 1, 1001, None),                       # both MN-major: any count
+])
+def test_unaligned_entry_token_rule(a_major, b_major, tokens_sum, code):
+    """kgw_wgrad_bf16_unaligned: host-side token-total rule (no device work is enqueued on CPU;
+    a passing call gets as far as the device check, which fails here without a GPU)."""
+    args = good_args(a_major=a_major, b_major=b_major, tokens_sum=tokens_sum)
+    rc = kgw.lib().kgw_wgrad_bf16_unaligned(ctypes.byref(args), FAKE, 1 << 30, None)
+    if code is None:
+        assert rc in (kgw.KGW_ERR_DEVICE, kgw.KGW_ERR_CUDA)
+    else:
+        assert rc == code
+    n = ctypes.c_size_t(0)
+    assert kgw.lib().kgw_workspace_size(ctypes.byref(args), 0, ctypes.byref(n)) == kgw.KGW_OK
 
 
 @pytest.mark.parametrize("a_major,b_major", [(0, 1), (1, 1), (0, 0), (1, 0)])

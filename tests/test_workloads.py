@@ -10,7 +10,7 @@ def test_counts_are_multiples_of_256_and_offsets_cumulative():
         w = fn()
         c = np.asarray(w.counts)
         assert c.shape == (w.num_experts,)
-        assert np.all(c % 256 == 0) and np.all(c >= 0), name
+        assert np.all(c % (8 if w.unaligned else 256) == 0) and np.all(c >= 0), name
         assert int(w.offsets[-1]) == w.tokens_sum
         assert np.all(np.diff(np.concatenate([[0], w.offsets])) == c)
 
@@ -85,3 +85,8 @@ def test_fp4_quantiser_follows_the_rounding_rule():
     assert np.array_equal(q.numpy(), ref)
     assert q.numpy()[0, :4].tolist() == [0x20, 0x42, 0x64, 0x76]
     assert q.numpy()[1, :4].tolist() == [0xA0, 0xCA, 0xEC, 0xFE]
+
+
+def test_unaligned_counts_are_multiples_of_8_not_all_of_256():
+    c = np.asarray(W.unaligned().counts)
+    assert np.all(c % 8 == 0) and np.any(c % 256 != 0) and np.any(c % 64 != 0)

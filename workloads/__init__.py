@@ -93,6 +93,7 @@ class Workload:
     sf_format: str = "f32_128"      # FP8 scales: "f32_128" (FP32 per 128 tokens) | "ue8m0_32" (packed)
     b_major: str = "mn"             # "mn": B stored [tokens, intermediate]; "k": stored [intermediate, tokens]
     fp4: bool = False               # e2m1 operands (K-major A and B), UE8M0 scales per 32 tokens
+    unaligned: bool = False         # counts multiples of 8, not 256 (the unaligned BF16 entry point)
 
     @property
     def tokens_sum(self) -> int:
@@ -137,6 +138,20 @@ def skewed() -> Workload:
                     out_dtype="bf16", input_order="ragged", output_mode="discrete")
 
 
+def round_to_8(x: np.ndarray) -> np.ndarray:
+    """Nearest multiple of 8: 8 * floor(x / 8 + 0.5)."""
+    return (8 * np.floor(np.asarray(x, dtype=np.float64) / 8 + 0.5)).astype(np.int64)
+
+
+def unaligned() -> Workload:
+    """The balanced shape with counts rounded to 8 tokens instead of 256 (same seed and spread)."""
+    rng = np.random.default_rng(1)
+    counts = round_to_8(4096 * rng.uniform(0.7, 1.3, size=8))
+    return Workload("BF16 unaligned counts: E=8 hidden=4096 intermediate=2048, counts multiples of 8, "
+                    "FP32 dense overwrite", 8, 4096, 2048, counts, seed=9, a_std=1.0, b_std=0.02,
+                    unaligned=True)
+
+
 def fp4() -> Workload:
     return Workload("FP4 block-scaled: E=16 hidden=4096 intermediate=1536, e2m1 with UE8M0 per 32 tokens, "
                     "K-major A and B, BF16 dense overwrite",
@@ -144,7 +159,8 @@ def fp4() -> Workload:
                     out_dtype="bf16", fp4=True, b_major="k", sf_format="ue8m0_32")
 
 
-NAMED = {"tiny": tiny, "balanced": balanced, "wide": wide, "fp8": fp8, "skewed": skewed, "fp4": fp4}
+NAMED = {"tiny": tiny, "balanced": balanced, "wide": wide, "fp8": fp8, "skewed": skewed, "fp4": fp4,
+         "unaligned": unaligned}
 
 
 def custom(num_experts: int, hidden: int, intermediate: int, counts, seed: int, **kw) -> Workload:
