@@ -43,6 +43,7 @@ KGW_ERR_TIMEOUT = 7
 KGW_ERR_WORKSPACE = 8
 KGW_ERR_OUT_PTRS = 9
 KGW_ERR_SCRATCH_LIMIT = 10
+KGW_ERR_SCALES = 11
 
 KGW_K_MAJOR = 0
 KGW_MN_MAJOR = 1

@@ -445,12 +445,10 @@ size_t main_smem_bytes(bool pair, bool fp8) {
   return ring + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
 }
 
-// Does any byte of these four words equal 0xFF (the UE8M0 NaN encoding)?
-__device__ __forceinline__ bool has_ue8m0_nan(uint4 v) {
-  auto ff = [](uint32_t w) {
-    return (w & 0xFFu) == 0xFFu || (w & 0xFF00u) == 0xFF00u || (w & 0xFF0000u) == 0xFF0000u || (w >> 24) == 0xFFu;
-  };
-  return ff(v.x) || ff(v.y) || ff(v.z) || ff(v.w);
+// Bit 7 of every byte of w that equals 0xFF (the UE8M0 NaN encoding), branch-free: (b & 0x7F) + 1
+// reaches 0x80 exactly when the low seven bits are all ones, and no carry crosses a byte.
+__device__ __forceinline__ uint32_t ff_bytes(uint32_t w) {
+  return ((w & 0x7F7F7F7Fu) + 0x01010101u) & w & 0x80808080u;
 }
 
 // UE8M0 scale-factor byte of a power-of-two FP32 scale, replicated to the 4 bytes of a TMEM
@@ -719,23 +717,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           // M-grouped: group e's B occupies rows [e*N, e*N+N) (K-major) or [e*K, e*K+K) (N-major)
           const int32_t b_row = kMG ? it.e * p.I + b_col : b_col;
           const int32_t b_tok = kMG ? it.e * p.K + kb * bk : static_cast<int32_t>(tok);
-          constexpr int kAtom = kFp8 ? 128 : 64;  // elements per 128-byte swizzle row
-          // A: K-major -> one box [128 rows x bk tokens]; MN-major -> boxes [bk tokens x 128 B of rows]
-          if constexpr (kAK) {
-            load(sA, amap, kx, a_row);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BM / kAtom; ++j)
-              load(sA + j * bk * 128, amap, a_row + kAtom * j, static_cast<int32_t>(tok));
-          }
-          // B: K-major -> one box [this CTA's columns x bk tokens]; MN-major -> boxes of 128 B of columns
-          if constexpr (kBK) {
-            load(sB, bmap, kx, b_row);
-          } else {
-#pragma unroll
-            for (int j = 0; j < BN / kHalves / kAtom; ++j)
-              load(sB + j * bk * 128, bmap, b_col + kAtom * j, b_tok);
-          }
+          // scales first: they are small and land before the operand tiles, so the converter's
+          // work is done by the time the MMA has its operands
           if constexpr (kFp4) {
             // the two 128-token scale words of this 256-token stage: [A word 0][A word 1]
             // [B word 0][B word 1], on the stage's scale barrier
@@ -754,6 +737,23 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             mbar_arrive_expect_tx(&ctl->sfdata[stage], SF_SMEM_BYTES);
             bulk_load(sS, p.sfa + kblk * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
             bulk_load(sS + BM * 4, p.sfb + kblk * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
+          }
+          constexpr int kAtom = kFp8 ? 128 : 64;  // elements per 128-byte swizzle row
+          // A: K-major -> one box [128 rows x bk tokens]; MN-major -> boxes [bk tokens x 128 B of rows]
+          if constexpr (kAK) {
+            load(sA, amap, kx, a_row);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / kAtom; ++j)
+              load(sA + j * bk * 128, amap, a_row + kAtom * j, static_cast<int32_t>(tok));
+          }
+          // B: K-major -> one box [this CTA's columns x bk tokens]; MN-major -> boxes of 128 B of columns
+          if constexpr (kBK) {
+            load(sB, bmap, kx, b_row);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / kHalves / kAtom; ++j)
+              load(sB + j * bk * 128, bmap, b_col + kAtom * j, b_tok);
           }
         }
         ++issued;
@@ -1079,13 +1079,6 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
               b1[j] = sw[2 * BM + BN + 32 * j + lane];
             }
             __syncwarp();  // every lane has read its words before any is overwritten
-            const bool bad = has_ue8m0_nan(make_uint4(a0[0], a0[1], a0[2], a0[3])) ||
-                             has_ue8m0_nan(make_uint4(a1[0], a1[1], a1[2], a1[3])) ||
-                             has_ue8m0_nan(make_uint4(b0[0], b0[1], b0[2], b0[3])) ||
-                             has_ue8m0_nan(make_uint4(b0[4], b0[5], b0[6], b0[7])) ||
-                             has_ue8m0_nan(make_uint4(b1[0], b1[1], b1[2], b1[3])) ||
-                             has_ue8m0_nan(make_uint4(b1[4], b1[5], b1[6], b1[7]));
-            if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
             uint4* ue = reinterpret_cast<uint4*>(sS);
             ue[lane] = make_uint4(a0[0], a0[1], a0[2], a0[3]);
             ue[32 + lane] = make_uint4(a1[0], a1[1], a1[2], a1[3]);
@@ -1096,6 +1089,13 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->sf_full[stage]);
+            // the NaN byte check runs after the hand-off, off the MMA's critical path
+            uint32_t ff = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ff |= ff_bytes(a0[j]) | ff_bytes(a1[j]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ff |= ff_bytes(b0[j]) | ff_bytes(b1[j]);
+            if (ff && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
@@ -1106,6 +1106,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           const float* sb = sa + BM;
           uint4* ue = reinterpret_cast<uint4*>(sS + SF_UE8_OFFSET);
           bool bad = false;
+          uint32_t packed_ff = 0;
           if (!p.sf_packed) {
             // FP32 powers of two -> one UE8M0 byte repeated in the 4 bytes of the word
             ue[lane] = make_uint4(ue8m0_x4(sa[lane], bad), ue8m0_x4(sa[32 + lane], bad),
@@ -1124,16 +1125,14 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             ue[lane] = x;
             ue[32 + lane] = y;
             ue[64 + lane] = z;
-            // the byte 0xFF encodes NaN: report it
-            const uint32_t all = x.x & x.y & x.z & x.w & y.x & y.y & y.z & y.w & z.x & z.y & z.z & z.w;
-            if ((all & 0xFFu) == 0xFFu || (all & 0xFF00u) == 0xFF00u || (all & 0xFF0000u) == 0xFF0000u ||
-                (all >> 24) == 0xFFu)
-              bad = bad || has_ue8m0_nan(x) || has_ue8m0_nan(y) || has_ue8m0_nan(z);
+            // the byte 0xFF encodes NaN: checked after the hand-off below
+            packed_ff = ff_bytes(x.x) | ff_bytes(x.y) | ff_bytes(x.z) | ff_bytes(x.w) | ff_bytes(y.x) | ff_bytes(y.y) |
+                        ff_bytes(y.z) | ff_bytes(y.w) | ff_bytes(z.x) | ff_bytes(z.y) | ff_bytes(z.z) | ff_bytes(z.w);
           }
-          if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->sf_full[stage]);
+          if ((bad || packed_ff) && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;

@@ -5,7 +5,7 @@ import ctypes
 import pytest
 import torch
 
-from kgw_testlib import ensure_built, header_functions
+from kgw_testlib import HEADER, ensure_built, header_functions
 
 kgw = ensure_built()
 
@@ -139,3 +139,14 @@ def test_debug_hooks_roundtrip():
     prev = kgw.kgw_debug_set(1, 123456789)
     assert kgw.kgw_debug_set(1, prev) == 123456789
     assert kgw.kgw_debug_set(99, 0) == -1
+
+
+def test_binding_constants_match_the_header():
+    """Every enumerator of include/kgw.h has the same value in the Python binding."""
+    import re
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    found = re.findall(r"\b(KGW_[A-Z0-9_]+)\s*=\s*(\d+)", src)
+    assert len(found) >= 15
+    for name, value in found:
+        assert getattr(kgw, name) == int(value), name

@@ -250,3 +250,35 @@ def test_fp4_rejects_unsupported_layouts():
         args = kgw.make_args(2, 128, 256, 512, x.a, x.b, x.offsets, out=out,
                              **{"b_major": kgw.KGW_K_MAJOR, **kw})
         assert kgw.kgw_wgrad_fp4_ue8m0(args, x.sfa, x.sfb, ws, check=False) == kgw.KGW_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kind", ["fp8_f32_not_pow2", "fp8_ue8m0_nan", "fp4_ue8m0_nan"])
+def test_bad_scales_are_reported(kind):
+    """A scale that is not a power of two (FP32 scales) or a UE8M0 byte 0xFF (NaN) anywhere in
+    the scale tensors is reported as KGW_ERR_SCALES; clean scales report KGW_OK."""
+    kgw = ensure_built()
+    if kind == "fp8_f32_not_pow2":
+        w = W.custom(3, 256, 512, [512, 256, 768], seed=140, fp8=True, out_dtype="bf16")
+    elif kind == "fp8_ue8m0_nan":
+        w = W.custom(3, 256, 512, [512, 256, 768], seed=141, fp8=True, sf_format="ue8m0_32", out_dtype="bf16")
+    else:
+        w = W.custom(3, 256, 512, [512, 256, 768], seed=142, fp4=True, b_major="k", sf_format="ue8m0_32",
+                     out_dtype="bf16")
+    x = W.make_inputs(w, DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    run_gpu(w, x, DEV, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kgw.KGW_OK
+    # one bad entry, in B's scales of the last expert's last 128-token block, a column in the
+    # second 128-column half of its n-tile, one byte that is not byte 0
+    sfb = x.sfb.clone()
+    if kind == "fp8_f32_not_pow2":
+        sfb[-1, 300] = 3.0
+    else:
+        words = sfb.view(torch.int32)
+        words[-1, 300] = int(np.array([0x7FFF7F7F], dtype=np.uint32).view(np.int32)[0])
+    x2 = W.Inputs(x.a, x.b, x.offsets, x.sfa, sfb, x.c)
+    status.fill_(-1)
+    run_gpu(w, x2, DEV, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kgw.KGW_ERR_SCALES
