@@ -179,7 +179,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   int32_t max_slots = slot_cap(a, fp8);
   {
     const size_t room = ws_bytes - L0.total;
-    const size_t fit = room / (halves * (kgw::PARTIAL_TILE_BYTES + 4 * kgw::NUM_EPI_WARPS));
+    const size_t fit = room / (halves * (kgw::PARTIAL_TILE_BYTES + 4 * kgw::EPI_COUNTERS));
     if (size_t(max_slots) > fit) max_slots = static_cast<int32_t>(fit);
     while (max_slots > 0 && kgw::ws_layout(a->num_experts, max_slots, halves).total > ws_bytes) --max_slots;
   }

@@ -23,10 +23,14 @@ constexpr int TOKEN_ALIGN = 256;
 constexpr int SCALE_BLOCK = 128;
 
 constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
-constexpr int NUM_THREADS_FP8 = 224;  // + warp 6: FP8 scale-factor converter
-constexpr int SF_WARP = 6;
+// block-scaled kernels (one accumulator, so the MMA waits while the epilogue drains TMEM): eight
+// epilogue warps, two per TMEM lane quadrant, one per 128-column half; warp 10 converts scales
+constexpr int NUM_THREADS_FP8 = 352;
+constexpr int SF_WARP = 10;
 constexpr int EPI_WARP0 = 2;
 constexpr int NUM_EPI_WARPS = 4;
+constexpr int NUM_EPI_WARPS_FP8 = 8;
+constexpr int EPI_COUNTERS = 8;    // split-K arrival counters per (tile, CTA half): one per epilogue warp
 constexpr int WORK_RING = 8;       // depth of the shared-memory work-item queue
 
 constexpr int MAX_EXPERTS = 4096;
@@ -96,7 +100,7 @@ inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1) {
   L.counter_base = off; off = align256(off + sizeof(int32_t) * E);
   L.tmaps = off;        off = align256(off + size_t(128) * E);
   L.tmaps_b = off;      off = align256(off + size_t(128) * E);
-  L.counters = off;     off = align256(off + sizeof(int32_t) * NUM_EPI_WARPS * halves * (max_slots > 0 ? max_slots : 1));
+  L.counters = off;     off = align256(off + sizeof(int32_t) * EPI_COUNTERS * halves * (max_slots > 0 ? max_slots : 1));
   L.partials = off;     off = align256(off + PARTIAL_TILE_BYTES * halves * size_t(max_slots));
   L.total = off;
   L.max_slots = max_slots;

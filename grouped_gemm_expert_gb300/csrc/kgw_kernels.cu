@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
   }
 
   // 8. split-tile arrival counters start at zero every call
-  for (int64_t i = tid; i < cnt_total * NUM_EPI_WARPS * halves; i += blockDim.x) counters[i] = 0;
+  for (int64_t i = tid; i < cnt_total * EPI_COUNTERS * halves; i += blockDim.x) counters[i] = 0;
 
   if (tid == 0) {
     hdr->error = 0;
@@ -437,12 +437,15 @@ struct SmemCtl {
   int32_t abort_flag;
 };
 
-constexpr uint32_t EPI_STAGE_BYTES = 32 * 128;  // per epilogue warp: 32 rows x 32 FP32
+// Epilogue staging: 16 KiB per CTA, split over its epilogue warps (4 x 32 rows x 32 FP32, or in the
+// block-scaled kernels 8 x 32 rows x 16 FP32 / 32 16-bit values).
+constexpr uint32_t EPI_STAGE_TOTAL = 16384;
+constexpr uint32_t EPI_STAGE_BYTES = EPI_STAGE_TOTAL / NUM_EPI_WARPS;
 
 size_t main_smem_bytes(bool pair, bool fp8) {
   const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + (fp8 ? SF_SMEM_PAD : 0u))
                            : size_t(STAGES) * (STAGE_BYTES + (fp8 ? SF_SMEM_PAD : 0u));
-  return ring + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
+  return ring + EPI_STAGE_TOTAL + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
 }
 
 // Bit 7 of every byte of w that equals 0xFF (the UE8M0 NaN encoding), branch-free: (b & 0x7F) + 1
@@ -566,6 +569,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   constexpr uint32_t kStageTx = STAGE_A_BYTES + kStageB;
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
   constexpr int kHalves = kPair ? 2 : 1;
+  constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   const int bk = kFp4 ? BK_FP4 : (kFp8 ? BK_FP8 : BK_BF16);
   pdl_wait();  // the plan of this call is complete and visible
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_mem = base;
   uint8_t* epi_stage_mem = base + size_t(kStages) * kStageBytes;
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_stage_mem + NUM_EPI_WARPS * EPI_STAGE_BYTES);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_stage_mem + EPI_STAGE_TOTAL);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: leader (issues MMAs, claims work)
@@ -592,11 +596,11 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tfull[a], 1);
-      mbar_init(&ctl->tempty[a], NUM_EPI_WARPS * kHalves);
+      mbar_init(&ctl->tempty[a], kEpiWarps * kHalves);
     }
     for (int w = 0; w < WORK_RING; ++w) {
       mbar_init(&ctl->wfull[w], 1);
-      mbar_init(&ctl->wempty[w], kPair ? 2 * (1 + NUM_EPI_WARPS) : 1 + NUM_EPI_WARPS + (kFp8 ? 1 : 0));
+      mbar_init(&ctl->wempty[w], kHalves * (1 + kEpiWarps + (kFp8 ? 1 : 0)));
     }
     mbar_init(&ctl->mma_done, 1);
     for (int st = 0; st < kStages; ++st) {
@@ -898,7 +902,186 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       wait_bounded_t<kPair>(&ctl->mma_done, 0, &dummy, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp < EPI_WARP0 + NUM_EPI_WARPS) {
+  } else if (kFp8 && warp < EPI_WARP0 + kEpiWarps) {
+    // ======================= Epilogue of the block-scaled kernels (warps 2..9) =======================
+    // Eight warps: warp w reads TMEM lane quadrant w % 4 and accumulator columns 128 * ((w - 2) / 4)
+    // onward. With 16-bit output and no accumulation the warp moves its whole 32 x 128 block out of
+    // TMEM into registers (packed to 16 bits) first and hands the accumulator back at once, so the
+    // MMA of the next tile does not wait for the stores.
+    const int q = warp & 3;
+    const int ew = warp - EPI_WARP0;
+    const int col0 = (ew >> 2) * (BN / 2);
+    int32_t* counters = reinterpret_cast<int32_t*>(p.ws + p.L.counters);
+    const int32_t* slot_base = reinterpret_cast<const int32_t*>(p.ws + p.L.slot_base);
+    const int32_t* counter_base = reinterpret_cast<const int32_t*>(p.ws + p.L.counter_base);
+    float* partials = reinterpret_cast<float*>(p.ws + p.L.partials);
+    uint4* stg = reinterpret_cast<uint4*>(epi_stage_mem + ew * (EPI_STAGE_TOTAL / NUM_EPI_WARPS_FP8));
+    const int rsub = lane >> 2;       // row within an 8-row group of the read-back
+    const int csub = lane & 3;        // 16-byte chunk within a 64-byte row segment
+    int tcount = 0;
+    for (int n = 0;; ++n) {
+      const int slot = n % WORK_RING;
+      const bool okw = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, okw)) break;
+      const int cur = ctl->work_item[slot];
+      __syncwarp();
+      if (lane == 0) release_slot(slot);
+      if (cur < 0) break;
+      const Item it = decode_item<kMG>(p, cur, bk);
+      const int esz = p.out_bf16 ? 2 : 4;
+      char* obase = out_row_ptr<kMG>(p, it, static_cast<int>(rank) * BM + q * 32) + size_t(col0) * esz;
+      const size_t ostride = size_t(p.I) * esz;
+      if (it.kend == it.kbeg) {
+        const int rb = (BN / 2) * esz;
+#pragma unroll 1
+        for (int r = 0; r < 32; ++r)
+          for (int off = lane * 16; off < rb; off += 32 * 16)
+            *reinterpret_cast<uint4*>(obase + r * ostride + off) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const bool okt = wait_bounded_t<kPair>(&ctl->tfull[0], static_cast<uint32_t>(tcount) & 1, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, okt)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + col0;
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->tempty[0]);
+      };
+      // row `lane` of the staging buffer: four 16-byte chunks, chunk c at slot c ^ ((lane >> 1) & 3)
+      auto stage4 = [&](uint4 v0, uint4 v1, uint4 v2, uint4 v3) {
+        const int sw = (lane >> 1) & 3;
+        stg[lane * 4 + (0 ^ sw)] = v0;
+        stg[lane * 4 + (1 ^ sw)] = v1;
+        stg[lane * 4 + (2 ^ sw)] = v2;
+        stg[lane * 4 + (3 ^ sw)] = v3;
+      };
+      auto unstage4 = [&](int j) {
+        const int r = 8 * j + rsub;
+        return stg[r * 4 + (csub ^ ((r >> 1) & 3))];
+      };
+      if (it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[16 * c + i] = p.out_f16 ? pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]))
+                                       : pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        }
+        release_acc();
+        // 32 columns (64 bytes per row) per round: 4 lanes per row, 8 rows per store instruction
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          stage4(make_uint4(pk[16 * c + 0], pk[16 * c + 1], pk[16 * c + 2], pk[16 * c + 3]),
+                 make_uint4(pk[16 * c + 4], pk[16 * c + 5], pk[16 * c + 6], pk[16 * c + 7]),
+                 make_uint4(pk[16 * c + 8], pk[16 * c + 9], pk[16 * c + 10], pk[16 * c + 11]),
+                 make_uint4(pk[16 * c + 12], pk[16 * c + 13], pk[16 * c + 14], pk[16 * c + 15]));
+          __syncwarp();
+          char* cbase = obase + size_t(c * 32 + csub * 8) * 2;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(cbase + (8 * j + rsub) * ostride) = unstage4(j);
+          __syncwarp();
+        }
+      } else if (it.nsplit == 1) {
+        // FP32 output or accumulation: 16 columns per TMEM load, the accumulator is handed back
+        // after the last load
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + (c >> 1) * 32, r);  // (x32 load, use the half of this round)
+            tmem_ld_wait();
+            if (c == 7) release_acc();
+            const int h = (c & 1) * 16;
+            stage4(make_uint4(r[h + 0], r[h + 1], r[h + 2], r[h + 3]), make_uint4(r[h + 4], r[h + 5], r[h + 6], r[h + 7]),
+                   make_uint4(r[h + 8], r[h + 9], r[h + 10], r[h + 11]),
+                   make_uint4(r[h + 12], r[h + 13], r[h + 14], r[h + 15]));
+          }
+          __syncwarp();
+          char* cbase = obase + size_t(c * 16 + csub * 4) * esz;
+          uint4 old[4];
+          if (p.accumulate) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) old[j] = load_old4(p, cbase + (8 * j + rsub) * ostride);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 u = unstage4(j);
+            emit4(p, cbase + (8 * j + rsub) * ostride,
+                  make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)),
+                  old[j]);
+          }
+          __syncwarp();
+        }
+      } else {
+        // split-K: this warp's 32 x 128 partial block to the workspace, then the last arriving
+        // warp for this block sums the partials in split order
+        const int sb = __ldg(slot_base + it.e) + it.tile * it.nsplit;
+        auto prow = [&](int s, int rr) {
+          return partials + ((size_t(sb + s) * kHalves + rank) * BM + q * 32 + rr) * BN + col0;
+        };
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + (c >> 1) * 32, r);
+            tmem_ld_wait();
+            if (c == 7) release_acc();
+            const int h = (c & 1) * 16;
+            stage4(make_uint4(r[h + 0], r[h + 1], r[h + 2], r[h + 3]), make_uint4(r[h + 4], r[h + 5], r[h + 6], r[h + 7]),
+                   make_uint4(r[h + 8], r[h + 9], r[h + 10], r[h + 11]),
+                   make_uint4(r[h + 12], r[h + 13], r[h + 14], r[h + 15]));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            __stcg(reinterpret_cast<uint4*>(prow(it.split, 8 * j + rsub) + c * 16 + csub * 4), unstage4(j));
+          __syncwarp();
+        }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const int cidx = ((__ldg(counter_base + it.e) + it.tile) * kHalves + static_cast<int>(rank)) * EPI_COUNTERS + ew;
+          last = atomicAdd(counters + cidx, 1) == it.nsplit - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            const int col = c * 16 + csub * 4;
+            char* cbase = obase + size_t(col) * esz;
+            uint4 old[4];
+            if (p.accumulate) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) old[j] = load_old4(p, cbase + (8 * j + rsub) * ostride);
+            }
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s2 = 0; s2 < it.nsplit; ++s2) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float4 x = __ldcg(reinterpret_cast<const float4*>(prow(s2, 8 * j + rsub) + col));
+                v[j].x += x.x;
+                v[j].y += x.y;
+                v[j].z += x.z;
+                v[j].w += x.w;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) emit4(p, cbase + (8 * j + rsub) * ostride, v[j], old[j]);
+          }
+        }
+      }
+      ++tcount;
+    }
+  } else if (!kFp8 && warp < EPI_WARP0 + kEpiWarps) {
     // ======================= Epilogue (warps 2..5) =======================
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
     int32_t* counters = reinterpret_cast<int32_t*>(p.ws + p.L.counters);
@@ -998,7 +1181,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         __syncwarp();
         int last = 0;
         if (lane == 0) {
-          const int cidx = ((__ldg(counter_base + it.e) + it.tile) * kHalves + static_cast<int>(rank)) * NUM_EPI_WARPS + q;
+          const int cidx = ((__ldg(counter_base + it.e) + it.tile) * kHalves + static_cast<int>(rank)) * EPI_COUNTERS + q;
           last = atomicAdd(counters + cidx, 1) == it.nsplit - 1;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
