@@ -65,6 +65,10 @@ constexpr uint32_t SF_STAGE_COLS = 12;
 // B word 1 likewise) that land in 24 TMEM columns per stage.
 constexpr uint32_t SF_SMEM_BYTES_FP4 = 2 * (BM + BN) * 4;
 constexpr uint32_t SF_STAGE_COLS_FP4 = 24;
+// Block-scaled epilogue: TMEM columns 384..511 (past the accumulator and the scale-factor ring)
+// hold each epilogue warp's 32 x 128 results packed to 16 bits (64 columns per column half), so
+// the accumulator can be handed back before the stores.
+constexpr uint32_t EPI_HOLD_COL0 = 384;
 
 struct PlanHeader {
   int32_t error;          // kgw_status found by the plan kernel (0 = OK)

@@ -905,8 +905,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   } else if (kFp8 && warp < EPI_WARP0 + kEpiWarps) {
     // ======================= Epilogue of the block-scaled kernels (warps 2..9) =======================
     // Eight warps: warp w reads TMEM lane quadrant w % 4 and accumulator columns 128 * ((w - 2) / 4)
-    // onward. With 16-bit output and no accumulation the warp moves its whole 32 x 128 block out of
-    // TMEM into registers (packed to 16 bits) first and hands the accumulator back at once, so the
+    // onward. With 16-bit output and no accumulation the warp first moves its whole 32 x 128 block
+    // into its holding columns of TMEM (packed to 16 bits) and hands the accumulator back, so the
     // MMA of the next tile does not wait for the stores.
     const int q = warp & 3;
     const int ew = warp - EPI_WARP0;
@@ -961,25 +961,29 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         return stg[r * 4 + (csub ^ ((r >> 1) & 3))];
       };
       if (it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
-        uint32_t pk[64];
-#pragma unroll
+        // TMEM accumulator -> packed 16-bit values in this warp's holding columns -> hand back
+        const uint32_t hold = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + EPI_HOLD_COL0 + (ew >> 2) * 64;
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
+          uint32_t r[32], pk[16];
           tmem_ld_32x32b_x32(taddr + c * 32, r);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            pk[16 * c + i] = p.out_f16 ? pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]))
-                                       : pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            pk[i] = p.out_f16 ? pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]))
+                              : pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          tmem_st_32x32b_x16(hold + c * 16, pk);
         }
         release_acc();
+        tmem_st_wait();
         // 32 columns (64 bytes per row) per round: 4 lanes per row, 8 rows per store instruction
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          stage4(make_uint4(pk[16 * c + 0], pk[16 * c + 1], pk[16 * c + 2], pk[16 * c + 3]),
-                 make_uint4(pk[16 * c + 4], pk[16 * c + 5], pk[16 * c + 6], pk[16 * c + 7]),
-                 make_uint4(pk[16 * c + 8], pk[16 * c + 9], pk[16 * c + 10], pk[16 * c + 11]),
-                 make_uint4(pk[16 * c + 12], pk[16 * c + 13], pk[16 * c + 14], pk[16 * c + 15]));
+          uint32_t pk[16];
+          tmem_ld_32x32b_x16(hold + c * 16, pk);
+          tmem_ld_wait();
+          stage4(make_uint4(pk[0], pk[1], pk[2], pk[3]), make_uint4(pk[4], pk[5], pk[6], pk[7]),
+                 make_uint4(pk[8], pk[9], pk[10], pk[11]), make_uint4(pk[12], pk[13], pk[14], pk[15]));
           __syncwarp();
           char* cbase = obase + size_t(c * 32 + csub * 8) * 2;
 #pragma unroll
@@ -992,14 +996,12 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + (c >> 1) * 32, r);  // (x32 load, use the half of this round)
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(taddr + c * 16, r);
             tmem_ld_wait();
             if (c == 7) release_acc();
-            const int h = (c & 1) * 16;
-            stage4(make_uint4(r[h + 0], r[h + 1], r[h + 2], r[h + 3]), make_uint4(r[h + 4], r[h + 5], r[h + 6], r[h + 7]),
-                   make_uint4(r[h + 8], r[h + 9], r[h + 10], r[h + 11]),
-                   make_uint4(r[h + 12], r[h + 13], r[h + 14], r[h + 15]));
+            stage4(make_uint4(r[0], r[1], r[2], r[3]), make_uint4(r[4], r[5], r[6], r[7]),
+                   make_uint4(r[8], r[9], r[10], r[11]), make_uint4(r[12], r[13], r[14], r[15]));
           }
           __syncwarp();
           char* cbase = obase + size_t(c * 16 + csub * 4) * esz;
@@ -1027,14 +1029,12 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + (c >> 1) * 32, r);
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(taddr + c * 16, r);
             tmem_ld_wait();
             if (c == 7) release_acc();
-            const int h = (c & 1) * 16;
-            stage4(make_uint4(r[h + 0], r[h + 1], r[h + 2], r[h + 3]), make_uint4(r[h + 4], r[h + 5], r[h + 6], r[h + 7]),
-                   make_uint4(r[h + 8], r[h + 9], r[h + 10], r[h + 11]),
-                   make_uint4(r[h + 12], r[h + 13], r[h + 14], r[h + 15]));
+            stage4(make_uint4(r[0], r[1], r[2], r[3]), make_uint4(r[4], r[5], r[6], r[7]),
+                   make_uint4(r[8], r[9], r[10], r[11]), make_uint4(r[12], r[13], r[14], r[15]));
           }
           __syncwarp();
 #pragma unroll
