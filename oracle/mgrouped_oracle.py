@@ -25,12 +25,18 @@ With accumulate the result is added to D's previous contents; otherwise it
 replaces them. Alignment rules (every contiguous segment a multiple of 128
 rows, section 2.1) are the caller's contract and are checked by
 ``layout_valid``; the arithmetic itself does not depend on them.
+
+FP8 (section 3: per-block 1x128 scaling along K): every e4m3 element is
+multiplied by its scale before the product; row r of A carries one scale per
+128 consecutive K (sfa [K/128, rows], MN-major), and so does column n of each
+group's weight (sfb [G, K/128, N]). Scales may also be packed UE8M0 words with
+one byte per 32 K (the same format as the K-grouped FP8 path).
 """
 from __future__ import annotations
 
 import numpy as np
 
-from .kgw_oracle import bf16_to_f64
+from .kgw_oracle import bf16_to_f64, decode_scales, e4m3_to_f64
 
 MG_ALIGN = 128
 
@@ -120,6 +126,47 @@ def mgrouped_from_storage(a_bits, b_bits, layout: str, groups, m: int, *, b_majo
     B = bf16_to_f64(b_bits)
     return mgrouped(A, B, layout, groups, m, b_major=b_major, d_init=d_init, accumulate=accumulate,
                     with_bound=with_bound)
+
+
+def dequantize_fp8(a_bits, b_bits, sfa, sfb, b_major: str = "k", sf_format: str = "f32_128"):
+    """Decoded, scaled operands: A [rows, K] and B [G, N, K] (K-major) or [G, K, N] (N-major)."""
+    a = e4m3_to_f64(a_bits)
+    a = a.reshape(-1, np.asarray(a_bits).shape[-1])
+    rows, K = a.shape
+    sa, blk = decode_scales(sfa, sf_format)                     # [K/blk, rows]
+    A = a * np.repeat(sa.T, blk, axis=1)
+    b = e4m3_to_f64(b_bits).reshape(np.asarray(b_bits).shape)
+    sfb = np.asarray(sfb)
+    B = np.empty_like(b)
+    for g in range(b.shape[0]):
+        sb, _ = decode_scales(sfb[g], sf_format)                 # [K/blk, N]
+        per_kn = np.repeat(sb, blk, axis=0)                      # [K, N]
+        B[g] = b[g] * (per_kn.T if b_major == "k" else per_kn)
+    return A, B
+
+
+def mgrouped_fp8_from_storage(a_bits, b_bits, sfa, sfb, layout: str, groups, m: int, *, b_major: str = "k",
+                              sf_format: str = "f32_128", d_init=None, accumulate: bool = False,
+                              with_bound: bool = True):
+    """Decode stored e4m3 operands and their scales, then evaluate ``mgrouped``."""
+    A, B = dequantize_fp8(a_bits, b_bits, sfa, sfb, b_major, sf_format)
+    return mgrouped(A, B, layout, groups, m, b_major=b_major, d_init=d_init, accumulate=accumulate,
+                    with_bound=with_bound)
+
+
+def element_fp8_from_storage(a_bits, b_bits, sfa, sfb, layout: str, groups, m: int, row: int, col: int, *,
+                             b_major: str = "k", sf_format: str = "f32_128"):
+    """(D[row, col] without accumulate, S[row, col]) from the stored FP8 operands and scales."""
+    g = group_of_row(layout, groups, m, row)
+    assert g >= 0, "row owned by no group"
+    a = np.asarray(a_bits)
+    K = a.shape[-1]
+    sa, blk = decode_scales(sfa, sf_format)
+    arow = e4m3_to_f64(a.reshape(-1, K)[row]) * np.repeat(sa[:, row], blk)
+    b = np.asarray(b_bits)
+    sb, _ = decode_scales(np.asarray(sfb)[g], sf_format)
+    bcol = e4m3_to_f64(b[g, col, :] if b_major == "k" else b[g, :, col]) * np.repeat(sb[:, col], blk)
+    return float(np.dot(arow, bcol)), float(np.dot(np.abs(arow), np.abs(bcol)))
 
 
 def group_of_row(layout: str, groups, m: int, row: int) -> int:

@@ -324,3 +324,83 @@ def test_mg_inputs_are_seeded():
     x1, x2 = MW.make_mg_inputs(w), MW.make_mg_inputs(w)
     assert torch.equal(x1.a, x2.a) and torch.equal(x1.b, x2.b) and torch.equal(x1.d0, x2.d0)
     assert x1.a.shape == (2, 96, 64) and x1.b.shape == (2, 256, 64) and x1.d0.shape == (2, 96, 256)
+
+
+# ------------------------------------------------------------------------------------------
+# FP8 (per-block 1x128 scaling along K, section 3)
+# ------------------------------------------------------------------------------------------
+
+def _u8(t):
+    return t.contiguous().view(torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("b_major", ["k", "mn"])
+def test_fp8_unit_scales_equal_the_bf16_oracle(b_major):
+    """With every scale 1 the FP8 result is the BF16-path oracle on the decoded e4m3 values (all
+    of which are exact in bf16): ties FP8 decoding and layout to the pinned BF16 definition."""
+    rng = np.random.default_rng(40)
+    G, N, K = 3, 32, 256
+    a8 = torch.from_numpy(rng.standard_normal((384, K)).astype(np.float32)).to(torch.float8_e4m3fn)
+    b_shape = (G, N, K) if b_major == "k" else (G, K, N)
+    b8 = torch.from_numpy(rng.standard_normal(b_shape).astype(np.float32)).to(torch.float8_e4m3fn)
+    sfa = np.ones((K // 128, 384), dtype=np.float32)
+    sfb = np.ones((G, K // 128, N), dtype=np.float32)
+    groups = np.array([128, 128, 384])
+    D8, S8 = MO.mgrouped_fp8_from_storage(_u8(a8), _u8(b8), sfa, sfb, "offsets", groups, 384, b_major=b_major)
+    D16, S16 = MO.mgrouped_from_storage(bits(a8.to(torch.bfloat16)), bits(b8.to(torch.bfloat16)), "offsets",
+                                        groups, 384, b_major=b_major)
+    assert np.array_equal(D8, D16) and np.array_equal(S8, S16)
+
+
+def test_fp8_scale_blocks_scale_exactly():
+    """Doubling the scale of one 128-K block of one row doubles exactly that block's contribution."""
+    rng = np.random.default_rng(41)
+    G, N, K = 2, 16, 256
+    a8 = torch.from_numpy(rng.standard_normal((256, K)).astype(np.float32)).to(torch.float8_e4m3fn)
+    b8 = torch.from_numpy(rng.standard_normal((G, N, K)).astype(np.float32)).to(torch.float8_e4m3fn)
+    sfa = np.ones((2, 256), dtype=np.float32)
+    sfb = np.ones((G, 2, N), dtype=np.float32)
+    groups = np.array([128, 256])
+    D0, _ = MO.mgrouped_fp8_from_storage(_u8(a8), _u8(b8), sfa, sfb, "offsets", groups, 256)
+    sfa2 = sfa.copy()
+    sfa2[1, 200] = 4.0                                  # row 200 (group 1), K block 1
+    D1, _ = MO.mgrouped_fp8_from_storage(_u8(a8), _u8(b8), sfa2, sfb, "offsets", groups, 256)
+    a = KO.e4m3_to_f64(_u8(a8)).reshape(a8.shape)
+    b = KO.e4m3_to_f64(_u8(b8)).reshape(b8.shape)
+    blk = a[200, 128:] @ b[1][:, 128:].T
+    assert np.array_equal(np.delete(D1, 200, axis=0), np.delete(D0, 200, axis=0))
+    assert np.allclose(D1[200] - D0[200], 3.0 * blk, rtol=0, atol=1e-9)
+    sfb2 = sfb.copy()
+    sfb2[0, 0, 5] = 0.5                                 # group 0, K block 0, column 5
+    D2, _ = MO.mgrouped_fp8_from_storage(_u8(a8), _u8(b8), sfa, sfb2, "offsets", groups, 256)
+    changed = np.nonzero(np.any(D2 != D0, axis=1))[0]
+    assert changed.min() >= 0 and changed.max() < 128 and np.all(np.nonzero(np.any(D2 != D0, axis=0))[0] == 5)
+
+
+def test_fp8_ue8m0_scales_match_the_f32_form():
+    """Packed UE8M0 words whose four bytes are equal describe the same per-128 scale as FP32."""
+    rng = np.random.default_rng(42)
+    G, N, K = 2, 16, 256
+    a8 = torch.from_numpy(rng.standard_normal((256, K)).astype(np.float32)).to(torch.float8_e4m3fn)
+    b8 = torch.from_numpy(rng.standard_normal((G, K, N)).astype(np.float32)).to(torch.float8_e4m3fn)
+    ea = rng.integers(120, 134, size=(2, 256))
+    eb = rng.integers(120, 134, size=(G, 2, N))
+    pack = lambda e: (e.astype(np.uint32) * 0x01010101).view(np.int32)
+    f32 = lambda e: np.ldexp(1.0, e - 127).astype(np.float32)
+    groups = np.array([128, 256])
+    Dp, _ = MO.mgrouped_fp8_from_storage(_u8(a8), _u8(b8), pack(ea), pack(eb), "offsets", groups, 256,
+                                         b_major="mn", sf_format="ue8m0_32")
+    Df, _ = MO.mgrouped_fp8_from_storage(_u8(a8), _u8(b8), f32(ea), f32(eb), "offsets", groups, 256,
+                                         b_major="mn")
+    assert np.array_equal(Dp, Df)
+
+
+def test_fp8_element_matches_full():
+    w = MW.mg_custom(3, 256, 256, "masked", [100, 0, 128], seed=43, max_m=128, fp8=True)
+    x = MW.make_mg_inputs(w)
+    D, S = MO.mgrouped_fp8_from_storage(_u8(x.a), _u8(x.b), x.sfa.numpy(), x.sfb.numpy(), "masked",
+                                        x.groups.numpy(), 128, d_init=np.zeros((w.rows, w.n)))
+    for (r, c) in [(0, 0), (99, 255), (256, 17), (383, 200)]:
+        v, s = MO.element_fp8_from_storage(_u8(x.a), _u8(x.b), x.sfa.numpy(), x.sfb.numpy(), "masked",
+                                           x.groups.numpy(), 128, r, c)
+        assert abs(v - D[r, c]) <= 1e-12 * (1 + S[r, c])

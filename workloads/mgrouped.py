@@ -51,6 +51,8 @@ class MGWorkload:
     b_std: float = 0.02
     d_std: float = 1.0          # D's previous contents ~ N(0, d_std) (accumulate, masked)
     shuffle_blocks: bool = False  # index layout: 128-row blocks in random group order
+    fp8: bool = False           # e4m3 operands, scales per row / column per 128 K (or UE8M0 per 32)
+    sf_format: str = "f32_128"  # "f32_128" | "ue8m0_32"
 
     @property
     def m(self) -> int:
@@ -102,7 +104,20 @@ def mg_masked() -> MGWorkload:
                       16, 4096, 2048, "masked", c, seed=7, max_m=1024)
 
 
-MG_NAMED = {"mg_tiny": mg_tiny, "mg_forward": mg_forward, "mg_dgrad": mg_dgrad, "mg_masked": mg_masked}
+def mg_fp8_forward() -> MGWorkload:
+    c, _ = counts_spread(5, 8, 4096, aligned=True)
+    return MGWorkload("M-grouped FP8 forward: G=8 rows ~4096 each, N=4096 K=2048, e4m3 with per-128-K FP32 scales, "
+                      "BF16 out", 8, 4096, 2048, "offsets", c, seed=11, fp8=True, b_std=1.0)
+
+
+def mg_fp8_masked() -> MGWorkload:
+    c, _ = counts_spread(7, 16, 256, aligned=False, cap=1024)
+    return MGWorkload("M-grouped FP8 masked decode: G=16 max_m=1024 masked_m ~256, N=4096 K=2048, e4m3, BF16 out",
+                      16, 4096, 2048, "masked", c, seed=12, max_m=1024, fp8=True, b_std=1.0)
+
+
+MG_NAMED = {"mg_tiny": mg_tiny, "mg_forward": mg_forward, "mg_dgrad": mg_dgrad, "mg_masked": mg_masked,
+            "mg_fp8_forward": mg_fp8_forward, "mg_fp8_masked": mg_fp8_masked}
 
 
 def mg_custom(num_groups: int, n: int, k: int, layout: str, counts, seed: int, **kw) -> MGWorkload:
@@ -117,11 +132,14 @@ class MGInputs:
     """a: bf16 [rows, K] (masked: [G, max_m, K]); b: bf16 [G, N, K] or [G, K, N];
     groups: int32 offsets [G] / m_indices [rows] / masked_m [G]; d0: D's previous contents
     ([rows, N] or [G, max_m, N]) in the output dtype, or None (overwrite of a contiguous layout,
-    where every row is written)."""
+    where every row is written). FP8: a, b are float8_e4m3fn of the same shapes; sfa float32
+    [K/128, rows] (or packed UE8M0 int32 words of that shape), sfb [G, K/128, N]."""
     a: torch.Tensor
     b: torch.Tensor
     groups: torch.Tensor
     d0: Optional[torch.Tensor]
+    sfa: Optional[torch.Tensor] = None
+    sfb: Optional[torch.Tensor] = None
 
 
 def group_ids(w: MGWorkload) -> np.ndarray:
@@ -160,9 +178,24 @@ def make_mg_inputs(w: MGWorkload, device="cpu", on_device_rng: bool = False) -> 
     a_shape = (w.num_groups, w.max_m, w.k) if w.layout == "masked" else (w.rows, w.k)
     b_shape = (w.num_groups, w.n, w.k) if w.b_major == "k" else (w.num_groups, w.k, w.n)
     d_shape = (w.num_groups, w.max_m, w.n) if w.layout == "masked" else (w.rows, w.n)
-    a = normal(a_shape, w.a_std, torch.bfloat16)
-    b = normal(b_shape, w.b_std, torch.bfloat16)
+    sfa = sfb = None
+    if w.fp8:
+        from . import quantize_e4m3_blocks, quantize_e4m3_ue8m0_32
+        quant = quantize_e4m3_ue8m0_32 if w.sf_format == "ue8m0_32" else quantize_e4m3_blocks
+        a32 = normal(a_shape, w.a_std, torch.float32).cpu()
+        b32 = normal(b_shape, w.b_std, torch.float32).cpu()
+        a, sfa = quant(a32.reshape(-1, w.k), token_axis=1)            # per row, per block of K
+        a = a.reshape(a_shape)
+        qb, sb = [], []
+        for g in range(w.num_groups):                                 # per column, per block of K
+            q, sc = quant(b32[g], token_axis=1 if w.b_major == "k" else 0)
+            qb.append(q)
+            sb.append(sc)
+        b, sfb = torch.stack(qb), torch.stack(sb)
+    else:
+        a = normal(a_shape, w.a_std, torch.bfloat16)
+        b = normal(b_shape, w.b_std, torch.bfloat16)
     d0 = normal(d_shape, w.d_std, _torch_dtype(w.out_dtype)) if (w.accumulate or w.layout == "masked") else None
     groups = torch.from_numpy(groups_array(w))
     to = lambda t: None if t is None else t.to(device)
-    return MGInputs(to(a), to(b), to(groups), to(d0))
+    return MGInputs(to(a), to(b), to(groups), to(d0), to(sfa), to(sfb))
