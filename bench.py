@@ -320,11 +320,17 @@ def run_ours(args, w, rank, local, world):
 
 
 def mg_algorithmic_bytes(w) -> int:
-    """A's valid rows, every non-empty group's weight, and D's valid rows (read too if accumulating)."""
+    """A's valid rows, every non-empty group's weight, and D's valid rows (read too if accumulating);
+    FP8 adds the scales of those rows and columns (one word per 128 K)."""
     counts = np.asarray(w.counts)
     osz = {"f32": 4, "bf16": 2, "f16": 2}[w.out_dtype]
+    esz = 1 if w.fp8 else 2
     rows = int(counts.sum())
-    return int(rows * w.k * 2 + int((counts > 0).sum()) * w.n * w.k * 2 + rows * w.n * osz * (2 if w.accumulate else 1))
+    groups = int((counts > 0).sum())
+    b = rows * w.k * esz + groups * w.n * w.k * esz + rows * w.n * osz * (2 if w.accumulate else 1)
+    if w.fp8:
+        b += (rows + groups * w.n) * (w.k // 128) * 4
+    return int(b)
 
 
 def run_ours_mg(args, w, rank, local, world):
@@ -341,6 +347,7 @@ def run_ours_mg(args, w, rank, local, world):
     d = torch.zeros(d_shape, dtype=odt, device=dev) if x.d0 is None else x.d0.clone()
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     lay = {"offsets": kgw.KGW_MG_OFFSETS, "indices": kgw.KGW_MG_INDICES, "masked": kgw.KGW_MG_MASKED}[w.layout]
+    fmt = 1 if w.sf_format == "ue8m0_32" else 0
     mk = lambda a, b, g, dd: kgw.make_mgrouped_args(
         w.num_groups, w.m, w.n, w.k, a, b, g, dd, layout=lay,
         b_major=kgw.KGW_K_MAJOR if w.b_major == "k" else kgw.KGW_MN_MAJOR,
@@ -352,10 +359,16 @@ def run_ours_mg(args, w, rank, local, world):
     # the masked decode workload (~0.3 GB) fits in L2: flush it between steps with a 256 MB write
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if w.layout == "masked" else None
 
+    def call(args, sfa, sfb):
+        if w.fp8:
+            kgw.kgw_mgrouped_fp8(args, sfa, sfb, fmt, ws, stream=stream)
+        else:
+            kgw.kgw_mgrouped_bf16(args, ws, stream=stream)
+
     def step():
         if flush is not None:
             flush.fill_(1)
-        kgw.kgw_mgrouped_bf16(kargs, ws, stream=stream)
+        call(kargs, x.sfa, x.sfb)
 
     for _ in range(args.warmup):
         step()
@@ -375,7 +388,7 @@ def run_ours_mg(args, w, rank, local, world):
         if flush is not None:
             flush.fill_(1)
         starts[i].record(stream)
-        kgw.kgw_mgrouped_bf16(kargs, ws, stream=stream)
+        call(kargs, x.sfa, x.sfb)
         ends[i].record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -387,7 +400,7 @@ def run_ours_mg(args, w, rank, local, world):
     if args.no_e2e:
         return ms_per_step, per_launch_ms, None, 0, 0, clk
     # end to end: inputs from pinned host memory, the call, D back to pinned host memory (serial)
-    host_in = [t.cpu().pin_memory() for t in (x.a, x.b, x.groups)]
+    host_in = [t.cpu().pin_memory() for t in (x.a, x.b, x.groups) + ((x.sfa, x.sfb) if w.fp8 else ())]
     host_d0 = None if x.d0 is None else x.d0.cpu().pin_memory()
     d_in = [torch.empty_like(t, device=dev) for t in host_in]
     d_out = torch.empty_like(d)
@@ -401,7 +414,7 @@ def run_ours_mg(args, w, rank, local, world):
             dd.copy_(h, non_blocking=True)
         if host_d0 is not None:
             d_out.copy_(host_d0, non_blocking=True)
-        kgw.kgw_mgrouped_bf16(ea, ws, stream=stream)
+        call(ea, d_in[3] if w.fp8 else None, d_in[4] if w.fp8 else None)
         h_out.copy_(d_out, non_blocking=True)
 
     e2e_step()
@@ -426,8 +439,12 @@ def cpu_oracle_rate_mg(w, budget_s: float):
     import oracle.mgrouped_oracle as MO
 
     x = MW.make_mg_inputs(w, "cpu")
-    A = O.bf16_to_f64(x.a.contiguous().view(torch.int16).numpy().view(np.uint16)).reshape(-1, w.k)
-    B = O.bf16_to_f64(x.b.contiguous().view(torch.int16).numpy().view(np.uint16))
+    if w.fp8:
+        u8 = lambda t: t.contiguous().view(torch.uint8).numpy()
+        A, B = MO.dequantize_fp8(u8(x.a), u8(x.b), x.sfa.numpy(), x.sfb.numpy(), w.b_major, w.sf_format)
+    else:
+        A = O.bf16_to_f64(x.a.contiguous().view(torch.int16).numpy().view(np.uint16)).reshape(-1, w.k)
+        B = O.bf16_to_f64(x.b.contiguous().view(torch.int16).numpy().view(np.uint16))
     groups = x.groups.numpy()
     per_group = [(g, r) for g, r in enumerate(MO.group_rows(w.layout, groups, w.m, w.num_groups)) if len(r)]
     flops, done = 0.0, 0
@@ -480,19 +497,20 @@ def main_mg(args, world, rank, local):
     achieved = flops / (launch_ms * 1e-3) / 1e12
     abytes = mg_algorithmic_bytes(w)
     # below the ridge point (few rows per group: the decode case) the weights' HBM reads bound it
-    hbm_bound = flops / abytes < peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tpeak = peaks["bf16_tflops"] * (2.0 if w.fp8 else 1.0)   # fp8: the nominal dense ratio x the bf16 burst
+    hbm_bound = flops / abytes < tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": abytes / (launch_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "peak_source": f"{peaks['source']} HBM copy"}
     else:
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "peak_source": f"{peaks['source']} bf16 burst"}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                "peak_source": f"{peaks['source']} bf16 burst" + (" x2 (nominal dense ratio)" if w.fp8 else "")}
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": traffic_record(args.workload),
                  "algorithmic_bytes": abytes, "flops": flops,
                  "kernel": "wgrad_kernel M-grouped instantiation (+ plan_mgrouped_kernel)"})
     line = {"metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+            "vs_baseline": None, "dtype": "fp8" if w.fp8 else "bf16", "data": "synthetic", "config": config,
             "roofline": roof,
             "e2e": None if e2e_ms is None else {"value": job_throughput(flops, e2e_ms, world), "unit": "TFLOP/s",
                                                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

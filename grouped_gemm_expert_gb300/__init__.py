@@ -20,6 +20,7 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_wgrad_bf16_unaligned(args, workspace, stream=None)
   kgw_mgrouped_workspace_size(args) -> int
   kgw_mgrouped_bf16(args, workspace, stream=None)
+  kgw_mgrouped_fp8(args, sfa, sfb, sf_format, workspace, stream=None)
 
 ``make_args`` / ``make_mgrouped_args`` build the argument structs from torch tensors.
 """
@@ -60,7 +61,7 @@ EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
             "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc",
             "kgw_debug_check_ragged_maps", "kgw_wgrad_fp8_ue8m0", "kgw_mgrouped_workspace_size",
             "kgw_mgrouped_bf16", "kgw_wgrad_fp4_ue8m0", "kgw_wgrad_bf16_unaligned",
-            "kgw_debug_check_tail_maps")
+            "kgw_debug_check_tail_maps", "kgw_mgrouped_fp8")
 
 
 class KgwArgs(ctypes.Structure):
@@ -140,6 +141,9 @@ def lib() -> ctypes.CDLL:
         L.kgw_mgrouped_bf16.argtypes = [ctypes.POINTER(KgwMgroupedArgs), ctypes.c_void_p, ctypes.c_size_t,
                                         ctypes.c_void_p]
         L.kgw_mgrouped_bf16.restype = ctypes.c_int
+        L.kgw_mgrouped_fp8.argtypes = [ctypes.POINTER(KgwMgroupedArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_mgrouped_fp8.restype = ctypes.c_int
         L.kgw_status_string.argtypes = [ctypes.c_int32]
         L.kgw_status_string.restype = ctypes.c_char_p
         L.kgw_version.argtypes = []
@@ -280,6 +284,17 @@ def kgw_wgrad_fp4_ue8m0(args: KgwArgs, sfa_packed, sfb_packed, workspace, worksp
     return rc
 
 
+def kgw_mgrouped_fp8(args: KgwMgroupedArgs, sfa, sfb, sf_format: int, workspace,
+                     workspace_bytes: Optional[int] = None, stream=None, check: bool = True) -> int:
+    """FP8 M-grouped GEMM: e4m3 operands, sf_format 0 (FP32 per 128 K) or 1 (packed UE8M0 per 32 K)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_mgrouped_fp8(ctypes.byref(args), _ptr(sfa), _ptr(sfb), int(sf_format), _ptr(workspace), nbytes,
+                                _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_mgrouped_fp8")
+    return rc
+
+
 def kgw_wgrad_bf16_noalloc(args: KgwArgs, stream=None, check: bool = True) -> int:
     """kgw_wgrad_bf16 using the library's static 2 MiB scratch instead of a workspace.
 
@@ -350,7 +365,8 @@ def wgrad(a, b, offsets, *, hidden: int, intermediate: int, out=None, out_ptrs=N
 
 
 def mgrouped(a, b, groups, *, layout: str = "offsets", d=None, b_major: str = "k", out_dtype: str = "bf16",
-             accumulate: bool = False, workspace=None, status_dev=None, stream=None):
+             accumulate: bool = False, workspace=None, status_dev=None, stream=None, sfa=None, sfb=None,
+             sf_format: str = "f32_128"):
     """M-grouped GEMM on torch CUDA tensors: D[rows of g] (+)= A[rows of g] @ op(B[g]).
 
     ``a`` bf16 [m, k] (contiguous layouts) or [G, max_m, k] (``layout="masked"``); ``b`` bf16
@@ -374,5 +390,8 @@ def mgrouped(a, b, groups, *, layout: str = "offsets", d=None, b_major: str = "k
                               accumulate=accumulate, status_dev=status_dev)
     if workspace is None:
         workspace = torch.empty(kgw_mgrouped_workspace_size(args), dtype=torch.uint8, device=a.device)
-    kgw_mgrouped_bf16(args, workspace, stream=stream)
+    if a.dtype == torch.float8_e4m3fn:
+        kgw_mgrouped_fp8(args, sfa, sfb, 1 if sf_format == "ue8m0_32" else 0, workspace, stream=stream)
+    else:
+        kgw_mgrouped_bf16(args, workspace, stream=stream)
     return d

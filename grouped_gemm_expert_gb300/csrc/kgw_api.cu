@@ -391,7 +391,7 @@ int64_t mg_max_tiles(const kgw_mgrouped_args* a) {
   return a->layout == KGW_MG_MASKED ? int64_t(a->num_groups) * ((a->m + kgw::BM - 1) / kgw::BM) : a->m / kgw::BM;
 }
 
-kgw_status validate_mg(const kgw_mgrouped_args* a) {
+kgw_status validate_mg(const kgw_mgrouped_args* a, bool fp8 = false) {
   if (!a) return KGW_ERR_INVALID_ARG;
   if (a->num_groups < 1 || a->num_groups > kgw::MAX_EXPERTS) return KGW_ERR_INVALID_ARG;
   if (a->layout != KGW_MG_OFFSETS && a->layout != KGW_MG_INDICES && a->layout != KGW_MG_MASKED)
@@ -399,7 +399,7 @@ kgw_status validate_mg(const kgw_mgrouped_args* a) {
   if (a->m < 0 || a->n <= 0 || a->k <= 0) return KGW_ERR_INVALID_ARG;
   if (a->layout != KGW_MG_MASKED && a->m % kgw::MG_ROW_ALIGN != 0) return KGW_ERR_INVALID_ARG;
   if (a->m >= (int64_t(1) << 31) || mg_rows(a) >= (int64_t(1) << 31)) return KGW_ERR_UNSUPPORTED;
-  if (a->n % kgw::BN != 0 || a->k % kgw::BK_BF16 != 0) return KGW_ERR_UNSUPPORTED;
+  if (a->n % kgw::BN != 0 || a->k % (fp8 ? kgw::BK_FP8 : kgw::BK_BF16) != 0) return KGW_ERR_UNSUPPORTED;
   if (int64_t(a->num_groups) * a->n >= (int64_t(1) << 31) || int64_t(a->num_groups) * a->k >= (int64_t(1) << 31))
     return KGW_ERR_UNSUPPORTED;
   if (mg_max_tiles(a) * (a->n / kgw::BN) >= (int64_t(1) << 31)) return KGW_ERR_UNSUPPORTED;
@@ -417,9 +417,15 @@ kgw_status validate_mg(const kgw_mgrouped_args* a) {
   return KGW_OK;
 }
 
-kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* stream) {
-  kgw_status st = validate_mg(a);
+kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* stream, bool fp8 = false,
+                  const void* sfa = nullptr, const void* sfb = nullptr, int32_t sf_format = 0) {
+  kgw_status st = validate_mg(a, fp8);
   if (st != KGW_OK) return st;
+  if (fp8) {
+    if (sf_format != 0 && sf_format != 1) return KGW_ERR_INVALID_ARG;
+    if (mg_rows(a) > 0 && (!sfa || !sfb)) return KGW_ERR_INVALID_ARG;
+    if ((sfa && !aligned(sfa, 16)) || (sfb && !aligned(sfb, 16))) return KGW_ERR_ALIGNMENT;
+  }
   if (!ws || !aligned(ws, 256)) return KGW_ERR_WORKSPACE;
   const WsLayout L = kgw::ws_layout_mg(mg_max_tiles(a));
   if (ws_bytes < L.total) return KGW_ERR_WORKSPACE;
@@ -433,14 +439,16 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
   std::memset(&tmB, 0, sizeof(tmB));
   const uint64_t M = static_cast<uint64_t>(mg_rows(a)), N = static_cast<uint64_t>(a->n),
                  K = static_cast<uint64_t>(a->k), G = static_cast<uint64_t>(a->num_groups);
-  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t esz = fp8 ? 1 : 2;
+  const uint32_t bk = fp8 ? kgw::BK_FP8 : kgw::BK_BF16;   // one 128-byte swizzle row of K
   if (M > 0) {
-    st = encode_2d(&tmA, dt, a->a, K, M, K * 2, kgw::BK_BF16, kgw::BM);                // A [rows, K]
+    st = encode_2d(&tmA, dt, a->a, K, M, K * esz, bk, kgw::BM);                          // A [rows, K]
     if (st != KGW_OK) return st;
     if (a->b_major == KGW_K_MAJOR)
-      st = encode_2d(&tmB, dt, a->b, K, G * N, K * 2, kgw::BK_BF16, kgw::BN);         // B [G*N, K]
+      st = encode_2d(&tmB, dt, a->b, K, G * N, K * esz, bk, kgw::BN);                   // B [G*N, K]
     else
-      st = encode_2d(&tmB, dt, a->b, N, G * K, N * 2, 64, kgw::BK_BF16);             // B [G*K, N]
+      st = encode_2d(&tmB, dt, a->b, N, G * K, N * esz, static_cast<uint32_t>(128 / esz), bk);  // B [G*K, N]
     if (st != KGW_OK) return st;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -458,8 +466,13 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
   if (kgw::launch_plan_mgrouped(pp, s) != cudaSuccess) return KGW_ERR_CUDA;
   kgw::MainParams mp{};
   mp.E = a->num_groups;
+  mp.H = static_cast<int32_t>(M);   // rows of A: the row stride of A's scales
   mp.I = a->n;
   mp.K = a->k;
+  mp.fp8 = fp8;
+  mp.sfa = static_cast<const float*>(sfa);
+  mp.sfb = static_cast<const float*>(sfb);
+  mp.sf_packed = sf_format == 1;
   mp.tokens_sum = static_cast<int64_t>(M);
   mp.out = a->d;
   mp.out_bf16 = a->out_dtype == KGW_OUT_BF16 || a->out_dtype == KGW_OUT_F16;
@@ -653,6 +666,11 @@ kgw_status kgw_mgrouped_workspace_size(const kgw_mgrouped_args* args, size_t* by
 
 kgw_status kgw_mgrouped_bf16(const kgw_mgrouped_args* args, void* workspace, size_t workspace_bytes, void* stream) {
   return run_mg(args, workspace, workspace_bytes, stream);
+}
+
+kgw_status kgw_mgrouped_fp8(const kgw_mgrouped_args* args, const void* sfa, const void* sfb, int32_t sf_format,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  return run_mg(args, workspace, workspace_bytes, stream, true, sfa, sfb, sf_format);
 }
 
 const char* kgw_status_string(int32_t status) {

@@ -738,9 +738,11 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             // they complete on the stage's scale barrier
             const int64_t kblk = tok / SCALE_BLOCK;
             uint8_t* sS = sB + kStageB;
+            // (M-grouped: A's scales are [K/128, rows], the group's weight scales [G, K/128, N])
+            const int64_t bblk = kMG ? int64_t(it.e) * (p.K / SCALE_BLOCK) + kblk : kblk;
             mbar_arrive_expect_tx(&ctl->sfdata[stage], SF_SMEM_BYTES);
             bulk_load(sS, p.sfa + kblk * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
-            bulk_load(sS + BM * 4, p.sfb + kblk * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
+            bulk_load(sS + BM * 4, p.sfb + bblk * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
           }
           constexpr int kAtom = kFp8 ? 128 : 64;  // elements per 128-byte swizzle row
           // A: K-major -> one box [128 rows x bk tokens]; MN-major -> boxes [bk tokens x 128 B of rows]
@@ -987,7 +989,9 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           __syncwarp();
           char* cbase = obase + size_t(c * 32 + csub * 8) * 2;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(cbase + (8 * j + rsub) * ostride) = unstage4(j);
+          for (int j = 0; j < 4; ++j)
+            if (!kMG || q * 32 + 8 * j + rsub < it.rows)  // M-grouped masked layout: valid rows only
+              *reinterpret_cast<uint4*>(cbase + (8 * j + rsub) * ostride) = unstage4(j);
           __syncwarp();
         }
       } else if (it.nsplit == 1) {
@@ -1005,17 +1009,20 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           }
           __syncwarp();
           char* cbase = obase + size_t(c * 16 + csub * 4) * esz;
+          auto live = [&](int j) { return !kMG || q * 32 + 8 * j + rsub < it.rows; };
           uint4 old[4];
           if (p.accumulate) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) old[j] = load_old4(p, cbase + (8 * j + rsub) * ostride);
+            for (int j = 0; j < 4; ++j)
+              if (live(j)) old[j] = load_old4(p, cbase + (8 * j + rsub) * ostride);
           }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const uint4 u = unstage4(j);
-            emit4(p, cbase + (8 * j + rsub) * ostride,
-                  make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)),
-                  old[j]);
+            if (live(j))
+              emit4(p, cbase + (8 * j + rsub) * ostride,
+                    make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)),
+                    old[j]);
           }
           __syncwarp();
         }
@@ -1403,6 +1410,10 @@ cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const 
 
 cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                  cudaStream_t s) {
+  if (p.fp8) {
+    if (p.b_kmajor) return launch_main<true, false, true, true, true>(p, tmA, tmB, grid, s);
+    return launch_main<true, false, true, false, true>(p, tmA, tmB, grid, s);
+  }
   if (p.b_kmajor) return launch_main<false, false, true, true, true>(p, tmA, tmB, grid, s);
   return launch_main<false, false, true, false, true>(p, tmA, tmB, grid, s);
 }

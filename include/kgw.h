@@ -251,6 +251,20 @@ kgw_status kgw_mgrouped_workspace_size(const kgw_mgrouped_args* args, size_t* by
 /* M-grouped BF16 GEMM (see kgw_mgrouped_args). workspace: 256-byte aligned device buffer. */
 kgw_status kgw_mgrouped_bf16(const kgw_mgrouped_args* args, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * FP8 M-grouped GEMM ("05 · Grouped GEMM 与 Expert 计算", section 2.1 names m_grouped_fp8_gemm_nt_contiguous
+ * and, for the masked layout, m_grouped_fp8_gemm_nt_masked; section 3: FP8 operands with per-block
+ * 1x128 scaling along K). a and b are float8 e4m3 ("fn") in the layouts of kgw_mgrouped_args.
+ * sf_format 0: sfa float32 [k/128, rows of A] (rows of A = m, or G*m for the masked layout),
+ * sfa[kb][r] scales A[r, 128*kb : 128*kb+128]; sfb float32 [G, k/128, n], sfb[g][kb][c] scales
+ * column c of op(B_g) over the same K block; every scale a power of two. sf_format 1: the same
+ * shapes as int32 words of four UE8M0 bytes, byte j scaling K 32j..32j+31 of the block (as in
+ * kgw_wgrad_fp8_ue8m0). Products accumulate in FP32; k must be a multiple of 128. A bad scale is
+ * reported as KGW_ERR_SCALES. Workspace: kgw_mgrouped_workspace_size.
+ */
+kgw_status kgw_mgrouped_fp8(const kgw_mgrouped_args* args, const void* sfa, const void* sfb, int32_t sf_format,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* kgw_status_string(int32_t status);
 

@@ -49,12 +49,23 @@ def run_mg(w, x, out, status=None, workspace=None):
                                   out_dtype=odt, accumulate=w.accumulate, status_dev=status)
     if workspace is None:
         workspace = torch.empty(kgw.kgw_mgrouped_workspace_size(args), dtype=torch.uint8, device=DEV)
-    kgw.kgw_mgrouped_bf16(args, workspace)
+    if w.fp8:
+        kgw.kgw_mgrouped_fp8(args, x.sfa, x.sfb, 1 if w.sf_format == "ue8m0_32" else 0, workspace)
+    else:
+        kgw.kgw_mgrouped_bf16(args, workspace)
     return args
+
+
+def u8(t):
+    return t.contiguous().view(torch.uint8).numpy()
 
 
 def oracle_ref(w, x_cpu):
     d0 = None if x_cpu.d0 is None else to_f64(x_cpu.d0).reshape(w.rows, w.n)
+    if w.fp8:
+        return MO.mgrouped_fp8_from_storage(u8(x_cpu.a), u8(x_cpu.b), x_cpu.sfa.numpy(), x_cpu.sfb.numpy(),
+                                            w.layout, x_cpu.groups.numpy(), w.m, b_major=w.b_major,
+                                            sf_format=w.sf_format, d_init=d0, accumulate=w.accumulate)
     return MO.mgrouped_from_storage(bits16(x_cpu.a), bits16(x_cpu.b), w.layout, x_cpu.groups.numpy(), w.m,
                                     b_major=w.b_major, d_init=d0, accumulate=w.accumulate)
 
@@ -112,6 +123,15 @@ CASES = {
                                      out_dtype="f32", accumulate=True, b_major="mn"),
     "masked_all_empty": C(3, 256, 64, "masked", [0, 0, 0], seed=53, max_m=128),
     "many_groups": C(40, 256, 128, "offsets", [128 * (i % 3) for i in range(40)], seed=54),
+    # FP8 (e4m3 with per-128-K scales per row of A and per column of each weight)
+    "fp8_offsets_forward": C(4, 512, 256, "offsets", [256, 0, 384, 128], seed=70, fp8=True, b_std=1.0),
+    "fp8_dgrad_f32": C(3, 256, 512, "offsets", [128, 256, 128], seed=71, fp8=True, b_std=1.0, b_major="mn",
+                       out_dtype="f32"),
+    "fp8_indices_shuffled_ue8m0": C(4, 256, 256, "indices", [256, 128, 0, 256], seed=72, fp8=True, b_std=1.0,
+                                    shuffle_blocks=True, sf_format="ue8m0_32"),
+    "fp8_masked_partial_tiles": C(4, 512, 384, "masked", [1, 129, 0, 200], seed=73, fp8=True, b_std=1.0, max_m=256),
+    "fp8_masked_accumulate_f16": C(3, 256, 256, "masked", [64, 300, 17], seed=74, fp8=True, b_std=1.0, max_m=320,
+                                   accumulate=True, out_dtype="f16"),
 }
 
 
@@ -263,13 +283,14 @@ def test_graph_capture_replays():
 # Full-size workloads: sampled rows against the oracle, unowned rows bit-exact
 # ------------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["mg_forward", "mg_dgrad", "mg_masked"])
+@pytest.mark.parametrize("name", ["mg_forward", "mg_dgrad", "mg_masked", "mg_fp8_forward", "mg_fp8_masked"])
 def test_mgrouped_full_size_sampled(name):
     kgw = ensure_built()
     w = MW.MG_NAMED[name]()
     x_cpu = MW.make_mg_inputs(w, "cpu")
     x = MW.MGInputs(x_cpu.a.to(DEV), x_cpu.b.to(DEV), x_cpu.groups.to(DEV),
-                    None if x_cpu.d0 is None else x_cpu.d0.to(DEV))
+                    None if x_cpu.d0 is None else x_cpu.d0.to(DEV),
+                    None if x_cpu.sfa is None else x_cpu.sfa.to(DEV), None if x_cpu.sfb is None else x_cpu.sfb.to(DEV))
     out = MGOut(w, x.d0)
     status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
     run_mg(w, x, out, status)
@@ -286,15 +307,39 @@ def test_mgrouped_full_size_sampled(name):
         if len(rs):
             picks.update([int(rs[0]), int(rs[-1])])
     cols = sorted(set([0, 255, 256, w.n - 1] + rng.choice(w.n, size=12, replace=False).tolist()))
-    a_bits, b_bits = bits16(x_cpu.a), bits16(x_cpu.b)
     got_rows = to_f64(out.d[torch.tensor(sorted(picks), device=DEV)])
     ref = np.zeros((len(picks), len(cols)))
     S = np.zeros_like(ref)
+    if w.fp8:
+        a_bits, b_bits = u8(x_cpu.a), u8(x_cpu.b)
+        elem = lambda r, c: MO.element_fp8_from_storage(a_bits, b_bits, x_cpu.sfa.numpy(), x_cpu.sfb.numpy(),
+                                                        w.layout, groups, w.m, r, c, b_major=w.b_major,
+                                                        sf_format=w.sf_format)
+    else:
+        a_bits, b_bits = bits16(x_cpu.a), bits16(x_cpu.b)
+        elem = lambda r, c: MO.element_from_storage(a_bits, b_bits, w.layout, groups, w.m, r, c, b_major=w.b_major)
     for i, r in enumerate(sorted(picks)):
         for j, c in enumerate(cols):
-            ref[i, j], S[i, j] = MO.element_from_storage(a_bits, b_bits, w.layout, groups, w.m, r, c,
-                                                         b_major=w.b_major)
+            ref[i, j], S[i, j] = elem(r, c)
     check_close(w, got_rows[:, cols], ref, S)
     if (~own).any():
         mask = torch.from_numpy(~own).to(DEV)
         assert torch.equal(out.d[mask], x.d0.reshape(w.rows, w.n)[mask]), "rows past masked_m changed"
+
+
+def test_fp8_host_rules():
+    """FP8: k must be a multiple of 128; scales must be given and 16-byte aligned."""
+    kgw = ensure_built()
+    a = torch.zeros(256, 192, dtype=torch.uint8, device=DEV)
+    b = torch.zeros(2, 256, 192, dtype=torch.uint8, device=DEV)
+    g = torch.tensor([128, 256], dtype=torch.int32, device=DEV)
+    d = torch.zeros(256, 256, dtype=torch.bfloat16, device=DEV)
+    sf = torch.ones(8 * 256, dtype=torch.float32, device=DEV)
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device=DEV)
+    args = kgw.make_mgrouped_args(2, 256, 256, 192, a, b, g, d)
+    assert kgw.kgw_mgrouped_fp8(args, sf, sf, 0, ws, check=False) == kgw.KGW_ERR_UNSUPPORTED       # k % 128
+    args = kgw.make_mgrouped_args(2, 256, 256, 128, a, b, g, d)
+    assert kgw.kgw_mgrouped_fp8(args, None, sf, 0, ws, check=False) == kgw.KGW_ERR_INVALID_ARG
+    assert kgw.kgw_mgrouped_fp8(args, sf.data_ptr() + 4, sf, 0, ws, check=False) == kgw.KGW_ERR_ALIGNMENT
+    assert kgw.kgw_mgrouped_fp8(args, sf, sf, 5, ws, check=False) == kgw.KGW_ERR_INVALID_ARG
+    torch.cuda.synchronize()
