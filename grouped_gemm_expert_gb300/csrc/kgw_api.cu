@@ -442,11 +442,15 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint64_t esz = fp8 ? 1 : 2;
   const uint32_t bk = fp8 ? kgw::BK_FP8 : kgw::BK_BF16;   // one 128-byte swizzle row of K
+  // BF16 runs on CTA pairs (two 128-row tiles of one group per work row); FP8 on single CTAs.
+  // In a pair each CTA loads 128 of the tile's 256 columns of B.
+  const bool pair = !fp8 && g_single_cta.load() == 0;
+  const uint32_t b_rows_cta = pair ? kgw::BN / 2 : kgw::BN;
   if (M > 0) {
     st = encode_2d(&tmA, dt, a->a, K, M, K * esz, bk, kgw::BM);                          // A [rows, K]
     if (st != KGW_OK) return st;
     if (a->b_major == KGW_K_MAJOR)
-      st = encode_2d(&tmB, dt, a->b, K, G * N, K * esz, bk, kgw::BN);                   // B [G*N, K]
+      st = encode_2d(&tmB, dt, a->b, K, G * N, K * esz, bk, b_rows_cta);               // B [G*N, K]
     else
       st = encode_2d(&tmB, dt, a->b, N, G * K, N * esz, static_cast<uint32_t>(128 / esz), bk);  // B [G*K, N]
     if (st != KGW_OK) return st;
@@ -463,6 +467,8 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
   pp.tile_m = kgw::BM;
   pp.mg_layout = a->layout;
   pp.mg_m = a->m;
+  pp.mg_pair = pair;
+  const int grid = pair ? (dev.sm_count & ~1) : dev.sm_count;
   if (kgw::launch_plan_mgrouped(pp, s) != cudaSuccess) return KGW_ERR_CUDA;
   kgw::MainParams mp{};
   mp.E = a->num_groups;
@@ -481,13 +487,13 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
   mp.a_kmajor = 1;
   mp.b_kmajor = a->b_major == KGW_K_MAJOR;
   mp.num_n_tiles = a->n / kgw::BN;
-  mp.tile_m = kgw::BM;
+  mp.tile_m = pair ? 2 * kgw::BM : kgw::BM;
   mp.status_dev = a->status_dev;
   mp.ws = static_cast<uint8_t*>(ws);
   mp.L = L;
   mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
   mp.test_drop_stage = -1;
-  return kgw::launch_main_mgrouped(mp, tmA, tmB, dev.sm_count, s) == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
+  return kgw::launch_main_mgrouped(mp, tmA, tmB, grid, s) == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
 }
 
 }  // namespace

@@ -111,13 +111,18 @@ inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1) {
   return L;
 }
 
-// M-grouped GEMM workspace: [PlanHeader][tile table: int2 {first row, group | rows << 16} per
-// 128-row tile, max_tiles entries]. The table lives where the K-grouped layout keeps `order`.
+// M-grouped GEMM workspace: [PlanHeader][work rows: int4 {first row of half 0, first row of half 1,
+// group, valid rows of half 0 | valid rows of half 1 << 16}, max_tiles][tile list: int2 {first row,
+// group | valid rows << 16} per 128-row tile, max_tiles]. A work row is one 128-row tile (one CTA)
+// or two tiles of the same group (a CTA pair); the work rows live where the K-grouped layout keeps
+// `order`, the tile list where it keeps `item_prefix`.
 inline WsLayout ws_layout_mg(int64_t max_tiles) {
   WsLayout L{};
+  const size_t n = size_t(max_tiles > 0 ? max_tiles : 1);
   L.order = sizeof(PlanHeader);
-  L.total = align256(L.order + sizeof(int32_t) * 2 * size_t(max_tiles > 0 ? max_tiles : 1));
-  L.item_prefix = L.splits = L.slot_base = L.counter_base = L.tmaps = L.tmaps_b = L.counters = L.partials = L.total;
+  L.item_prefix = align256(L.order + sizeof(int32_t) * 4 * n);
+  L.total = align256(L.item_prefix + sizeof(int32_t) * 2 * n);
+  L.splits = L.slot_base = L.counter_base = L.tmaps = L.tmaps_b = L.counters = L.partials = L.total;
   L.max_slots = 0;
   return L;
 }
@@ -140,6 +145,7 @@ struct PlanParams {
   const uint8_t* b;             // B base
   int32_t esz;                  // bytes per operand element
   int32_t mg_layout;            // M-grouped: kgw_mg_layout
+  int32_t mg_pair;              // M-grouped: work rows pair two 128-row tiles of one group
   int64_t mg_m;                 // M-grouped: rows (contiguous) or rows per group (masked)
   int32_t count_align;          // every token count must be a multiple of this (256, or 8 / 1 unaligned)
   // token counts not multiples of the stage: per-expert descriptors whose token extent ends at

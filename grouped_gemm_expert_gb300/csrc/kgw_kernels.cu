@@ -285,13 +285,16 @@ __global__ void __launch_bounds__(PLAN_THREADS)
 __global__ void __launch_bounds__(PLAN_THREADS) plan_mgrouped_kernel(const __grid_constant__ PlanParams p) {
   __shared__ int64_t s_warp[32];
   __shared__ int32_t s_err;
+  __shared__ int32_t s_cnt[MAX_EXPERTS];   // CTA pairs: tiles per group
+  __shared__ int32_t s_fill[MAX_EXPERTS];  // CTA pairs: next half-row slot of each group
   pdl_launch_dependents();
   const int G = p.E;
   const int tid = threadIdx.x;
   const int NT = p.I / BN;
   const int32_t* grp = p.offsets;
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
-  int2* tiles = reinterpret_cast<int2*>(p.ws + p.L.order);
+  int2* tiles = reinterpret_cast<int2*>(p.ws + p.L.item_prefix);
+  int32_t* rows_out = reinterpret_cast<int32_t*>(p.ws + p.L.order);   // int4 work rows
   if (tid == 0) s_err = 0;
   __syncthreads();
   int64_t ntiles = 0;
@@ -348,10 +351,59 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_mgrouped_kernel(const __gri
     }
   }
   __syncthreads();
+  // work rows: one tile each, or (CTA pairs) two tiles of the same group each; a group with an odd
+  // tile count gets a last row whose second half repeats the first with no valid rows (its
+  // results are not stored)
+  int64_t nrows = ntiles;
+  if (!s_err) {
+    if (!p.mg_pair) {
+      for (int64_t t = tid; t < ntiles; t += blockDim.x) {
+        const int2 tl = tiles[t];
+        reinterpret_cast<int4*>(rows_out)[t] = make_int4(tl.x, tl.x, tl.y & 0xFFFF, static_cast<int>(tl.y >> 16));
+      }
+    } else {
+      for (int g = tid; g < G; g += blockDim.x) s_cnt[g] = 0;
+      __syncthreads();
+      for (int64_t t = tid; t < ntiles; t += blockDim.x) atomicAdd(&s_cnt[tiles[t].y & 0xFFFF], 1);
+      __syncthreads();
+      const Chunk ch = my_chunk(G);
+      int64_t mine = 0;
+      for (int g = ch.lo; g < ch.hi; ++g) mine += (s_cnt[g] + 1) / 2;
+      int64_t run = block_exclusive_scan(mine, s_warp, &nrows);
+      for (int g = ch.lo; g < ch.hi; ++g) {
+        s_fill[g] = static_cast<int32_t>(2 * run);   // half-row slots of group g start at 2 * its first row
+        run += (s_cnt[g] + 1) / 2;
+      }
+      for (int64_t r = tid; r < nrows; r += blockDim.x) rows_out[4 * r + 3] = 0;
+      __syncthreads();
+      for (int64_t t = tid; t < ntiles; t += blockDim.x) {
+        const int2 tl = tiles[t];
+        const int g = tl.y & 0xFFFF;
+        const int h = atomicAdd(&s_fill[g], 1);
+        const int64_t r = h >> 1;
+        const int vrows = static_cast<int>(static_cast<uint32_t>(tl.y) >> 16);
+        if ((h & 1) == 0) {
+          rows_out[4 * r + 0] = tl.x;
+          rows_out[4 * r + 2] = g;
+          atomicOr(&rows_out[4 * r + 3], vrows);
+        } else {
+          rows_out[4 * r + 1] = tl.x;
+          atomicOr(&rows_out[4 * r + 3], vrows << 16);
+        }
+      }
+      __syncthreads();
+      for (int g = tid; g < G; g += blockDim.x)
+        if (s_fill[g] & 1) {  // odd tile count: the last row's second half repeats the first, no rows valid
+          const int64_t r = (s_fill[g] - 1) >> 1;
+          rows_out[4 * r + 1] = rows_out[4 * r + 0];
+        }
+    }
+  }
+  __syncthreads();
   if (tid == 0) {
     const int32_t err = s_err ? KGW_ERR_OFFSETS : KGW_OK;
     hdr->error = err;
-    hdr->total_items = err ? 0 : static_cast<int32_t>(ntiles * NT);
+    hdr->total_items = err ? 0 : static_cast<int32_t>(nrows * NT);
     hdr->chunk_kiters = 0;
     hdr->slots_used = 0;
     hdr->counters_used = 0;
@@ -370,6 +422,7 @@ struct Item {
   int kbeg, kend;        // k-iterations (relative to the expert's first token)
   int split, nsplit, tile;
   int rows;              // valid rows of the tile (M-grouped masked layout: may be < 128)
+  int m1, rows1;         // M-grouped CTA pair: first row and valid rows of the second CTA's half
   int64_t begin;         // expert's first token
   int64_t n_e;           // expert's token count
 };
@@ -381,10 +434,12 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
     // M-grouped: item = (128-row tile, n-tile); the tile table gives the rows and the group
     const int mt = idx / p.num_n_tiles;
     const int nt = idx - mt * p.num_n_tiles;
-    const int2 ti = __ldg(reinterpret_cast<const int2*>(p.ws + p.L.order) + mt);
-    it.e = ti.y & 0xFFFF;
-    it.rows = ti.y >> 16;
-    it.m0 = ti.x;
+    const int4 wr = __ldg(reinterpret_cast<const int4*>(p.ws + p.L.order) + mt);
+    it.m0 = wr.x;
+    it.m1 = wr.y;
+    it.e = wr.z;
+    it.rows = wr.w & 0xFFFF;
+    it.rows1 = static_cast<int>(static_cast<uint32_t>(wr.w) >> 16);
     it.n0 = nt * BN;
     it.split = 0;
     it.nsplit = 1;
@@ -406,6 +461,8 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
   it.e = __ldg(order + lo);
   const int local = idx - __ldg(prefix + lo);
   it.rows = p.tile_m;
+  it.m1 = 0;
+  it.rows1 = 0;
   it.nsplit = __ldg(splits + it.e);
   const int T = p.num_m_tiles * p.num_n_tiles;
   it.split = local / T;
@@ -538,8 +595,11 @@ __device__ __forceinline__ float4 unstage(const uint4* stg, int j, int lane) {
 template <bool kMG = false>
 __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it, int row) {
   const size_t esz = p.out_bf16 ? 2 : 4;
+  if constexpr (kMG) {  // D [rows, N]; rows at or past BM belong to the second half of a CTA pair
+    const size_t rr = static_cast<size_t>(row >= BM ? it.m1 + (row - BM) : it.m0 + row);
+    return reinterpret_cast<char*>(p.out) + (rr * p.I + it.n0) * esz;
+  }
   const size_t r = static_cast<size_t>(it.m0 + row);
-  if constexpr (kMG) return reinterpret_cast<char*>(p.out) + (r * p.I + it.n0) * esz;  // D [M_total, N]
   if (p.discrete) {
     char* base = reinterpret_cast<char*>(static_cast<uintptr_t>(__ldg(p.out_ptrs + it.e)));
     return base + (r * p.I + it.n0) * esz;
@@ -692,7 +752,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         bmap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps_b + size_t(it.e) * 128);
         if (lane == 0 && it.kend > it.kbeg) fence_tmap_acquire(bmap);
       }
-      const int a_row = it.m0 + static_cast<int>(rank) * BM;            // this CTA's A rows
+      // this CTA's A rows (M-grouped pair: the row's own tile for each CTA)
+      const int a_row = kMG ? (rank ? it.m1 : it.m0) : it.m0 + static_cast<int>(rank) * BM;
       const int b_col = it.n0 + static_cast<int>(rank) * (BN / kHalves);  // this CTA's B columns
       for (int kb = it.kbeg; kb < it.kend; ++kb) {
         bool ok2 = true;
@@ -1150,7 +1211,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           __syncwarp();
           uint4 old[8];
           // M-grouped masked layout: rows at or past the group's valid count are not touched
-          auto live = [&](int j) { return !kMG || q * 32 + 4 * j + (lane >> 3) < it.rows; };
+          auto live = [&](int j) { return !kMG || q * 32 + 4 * j + (lane >> 3) < (rank ? it.rows1 : it.rows); };
           if (p.accumulate) {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -1413,6 +1474,10 @@ cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, co
   if (p.fp8) {
     if (p.b_kmajor) return launch_main<true, false, true, true, true>(p, tmA, tmB, grid, s);
     return launch_main<true, false, true, false, true>(p, tmA, tmB, grid, s);
+  }
+  if (p.tile_m == 2 * BM) {
+    if (p.b_kmajor) return launch_main<false, true, true, true, true>(p, tmA, tmB, grid, s);
+    return launch_main<false, true, true, false, true>(p, tmA, tmB, grid, s);
   }
   if (p.b_kmajor) return launch_main<false, false, true, true, true>(p, tmA, tmB, grid, s);
   return launch_main<false, false, true, false, true>(p, tmA, tmB, grid, s);

@@ -343,3 +343,26 @@ def test_fp8_host_rules():
     assert kgw.kgw_mgrouped_fp8(args, sf.data_ptr() + 4, sf, 0, ws, check=False) == kgw.KGW_ERR_ALIGNMENT
     assert kgw.kgw_mgrouped_fp8(args, sf, sf, 5, ws, check=False) == kgw.KGW_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", ["offsets_forward_bf16", "indices_shuffled", "masked_partial_tiles",
+                                  "masked_odd_max_m", "offsets_accumulate_bf16_dgrad"])
+def test_single_cta_and_pair_rows_agree(name):
+    """BF16 calls run on CTA pairs (two 128-row tiles of one group per work row; a group with an
+    odd tile count ends with a half-empty row). The same call on single-CTA tiles gives the same
+    bits, and rows outside the groups stay untouched either way."""
+    kgw = ensure_built()
+    w = CASES[name]
+    x = MW.make_mg_inputs(w, DEV)
+    o_pair = MGOut(w, x.d0)
+    run_mg(w, x, o_pair)
+    prev = kgw.kgw_debug_set(3, 1)
+    try:
+        o_single = MGOut(w, x.d0)
+        run_mg(w, x, o_single)
+    finally:
+        kgw.kgw_debug_set(3, prev)
+    torch.cuda.synchronize()
+    assert o_pair.guards_intact() and o_single.guards_intact()
+    assert torch.equal(o_pair.buf.view(torch.int16) if o_pair.buf.element_size() == 2 else o_pair.buf,
+                       o_single.buf.view(torch.int16) if o_single.buf.element_size() == 2 else o_single.buf)
