@@ -366,3 +366,24 @@ def test_single_cta_and_pair_rows_agree(name):
     assert o_pair.guards_intact() and o_single.guards_intact()
     assert torch.equal(o_pair.buf.view(torch.int16) if o_pair.buf.element_size() == 2 else o_pair.buf,
                        o_single.buf.view(torch.int16) if o_single.buf.element_size() == 2 else o_single.buf)
+
+
+@pytest.mark.parametrize("layout", ["offsets", "indices", "masked"])
+def test_no_rows_at_all(layout):
+    """A call with no rows (every group empty) enqueues nothing harmful and reports KGW_OK."""
+    kgw = ensure_built()
+    G = 3
+    b = torch.zeros(G, 256, 64, dtype=torch.bfloat16, device=DEV)
+    groups = torch.zeros(G, dtype=torch.int32, device=DEV)
+    m = 128 if layout == "masked" else 0
+    a = torch.zeros(max(1, G * m), 64, dtype=torch.bfloat16, device=DEV)
+    d = torch.full((max(1, G * m), 256), 7.25, dtype=torch.bfloat16, device=DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    lay = {"offsets": kgw.KGW_MG_OFFSETS, "indices": kgw.KGW_MG_INDICES, "masked": kgw.KGW_MG_MASKED}[layout]
+    args = kgw.make_mgrouped_args(G, m, 256, 64, a if m else None, b, groups if layout != "indices" else None,
+                                  d if m else None, layout=lay, status_dev=status)
+    ws = torch.empty(kgw.kgw_mgrouped_workspace_size(args), dtype=torch.uint8, device=DEV)
+    kgw.kgw_mgrouped_bf16(args, ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == kgw.KGW_OK
+    assert torch.all(d == 7.25)
