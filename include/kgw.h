@@ -275,8 +275,8 @@ int32_t kgw_version(void);
  * Testing hooks (process-wide, host side). key 1: device wait limit in nanoseconds
  * (default 2e9); key 2: when >= 0, the TMA producer of CTA 0 skips the arrival of that
  * k-iteration so that the bounded wait path is exercised (default -1); key 3: non-zero runs every
- * K-grouped BF16 call on single-CTA 128-row tiles (default 0). Returns the previous value, or -1
- * for an unknown key.
+ * BF16 call (K- and M-grouped) on single-CTA 128-row tiles (default 0). Returns the previous
+ * value, or -1 for an unknown key.
  */
 int64_t kgw_debug_set(int32_t key, int64_t value);
 
