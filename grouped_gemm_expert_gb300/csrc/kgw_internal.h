@@ -22,11 +22,15 @@ constexpr int MAX_STAGES = 6;
 constexpr int TOKEN_ALIGN = 256;
 constexpr int SCALE_BLOCK = 128;
 
-constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+// warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue, warp 6 scheduler
+constexpr int NUM_THREADS = 224;
 // block-scaled kernels (one accumulator, so the MMA waits while the epilogue drains TMEM): eight
-// epilogue warps, two per TMEM lane quadrant, one per 128-column half; warp 10 converts scales
-constexpr int NUM_THREADS_FP8 = 352;
+// epilogue warps, two per TMEM lane quadrant, one per 128-column half; warp 10 converts scales,
+// warp 11 schedules
+constexpr int NUM_THREADS_FP8 = 384;
 constexpr int SF_WARP = 10;
+constexpr int SCHED_WARP = 6;
+constexpr int SCHED_WARP_FP8 = 11;
 constexpr int EPI_WARP0 = 2;
 constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_EPI_WARPS_FP8 = 8;

@@ -416,7 +416,9 @@ __global__ void __launch_bounds__(PLAN_THREADS) plan_mgrouped_kernel(const __gri
 // Main kernel
 // =============================================================================================
 
-struct Item {
+// A decoded work item. The scheduler warp decodes each item once and publishes it in the shared-
+// memory work ring (and, in a pair, in the peer CTA's ring); e < 0 ends the stream.
+struct alignas(16) Item {
   int e;
   int m0, n0;
   int kbeg, kend;        // k-iterations (relative to the expert's first token)
@@ -426,6 +428,7 @@ struct Item {
   int64_t begin;         // expert's first token
   int64_t n_e;           // expert's token count
 };
+static_assert(sizeof(Item) == 64, "an item is four 16-byte words");
 
 template <bool kMG = false>
 __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk) {
@@ -489,7 +492,8 @@ struct SmemCtl {
   uint64_t mma_done;
   uint64_t sf_full[MAX_STAGES]; // FP8: scale factors of a stage are in TMEM (on the leader in a pair)
   uint64_t sfdata[MAX_STAGES];  // FP8: this CTA's FP32 scales of a stage have landed in shared memory
-  int32_t work_item[WORK_RING];
+  uint64_t sched_go;            // the producer has started an item: the scheduler may claim the next
+  Item work[WORK_RING];         // decoded work items (written by the scheduler of the leader CTA)
   uint32_t tmem_base;
   int32_t abort_flag;
 };
@@ -660,8 +664,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     }
     for (int w = 0; w < WORK_RING; ++w) {
       mbar_init(&ctl->wfull[w], 1);
-      mbar_init(&ctl->wempty[w], kHalves * (1 + kEpiWarps + (kFp8 ? 1 : 0)));
+      // consumers: the producer and the epilogue warps of each CTA, the MMA thread, the converter
+      mbar_init(&ctl->wempty[w], kHalves * (1 + kEpiWarps) + 1 + (kFp8 ? 1 : 0));
     }
+    mbar_init(&ctl->sched_go, 1);
     mbar_init(&ctl->mma_done, 1);
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&ctl->sf_full[st], 1);
@@ -705,42 +711,21 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   };
 
   if (warp == 0) {
-    // ======================= TMA producer (+ scheduler on the leader) =======================
+    // ======================= TMA producer =======================
     int stage = 0;
     uint32_t phase = 0;
     int issued = 0;
-    int cur = 0;
-    if (lane == 0 && leader) cur = atomicAdd(item_counter, 1);
     for (int n = 0;; ++n) {
       const int slot = n % WORK_RING;
-      bool ok = true;
+      const bool okw = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, okw)) break;
+      const Item it = ctl->work[slot];
+      __syncwarp();
       if (lane == 0) {
-        if (leader) {
-          ok = wait_bounded_t<kPair>(&ctl->wempty[slot], ((n / WORK_RING) & 1) ^ 1, abort_flag, p.timeout_ns);
-          if (ok) {
-            const int v = cur < total_items ? cur : -1;
-            ctl->work_item[slot] = v;
-            if constexpr (kPair) {
-              st_cluster_s32(mapa_shared(smem_u32(&ctl->work_item[slot]), 1), v);
-              mbar_arrive_remote(mapa_shared(smem_u32(&ctl->wfull[slot]), 1));
-            }
-            mbar_arrive(&ctl->wfull[slot]);
-          }
-        } else {
-          ok = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
-          if (ok) {
-            cur = ctl->work_item[slot];
-            if (cur < 0) cur = total_items;
-            release_slot(slot);
-          }
-        }
+        release_slot(slot);
+        if (leader && it.e >= 0) mbar_arrive(&ctl->sched_go);  // the scheduler may claim the next item
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      cur = __shfl_sync(0xffffffffu, cur, 0);
-      if (!ok || cur >= total_items) break;
-      int nxt = 0;
-      if (lane == 0 && leader) nxt = atomicAdd(item_counter, 1);
-      const Item it = decode_item<kMG>(p, cur, bk);
+      if (it.e < 0) break;
       // ragged + K-major operand: the expert's own descriptor, coordinates relative to its block
       const CUtensorMap* amap = &tmA;
       const CUtensorMap* bmap = &tmB;
@@ -830,7 +815,6 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         }
       }
       if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-      cur = nxt;
     }
     // Drain: the leader's last kStages stages must land before exit (the peer's copies complete
     // on the leader's barriers, which the cluster barrier at the end waits for).
@@ -876,10 +860,9 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       for (int n = 0;; ++n) {
         const int slot = n % WORK_RING;
         if (!wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns)) break;
-        const int cur = ctl->work_item[slot];
+        const Item it = ctl->work[slot];
         release_slot(slot);
-        if (cur < 0) break;
-        const Item it = decode_item<kMG>(p, cur, bk);
+        if (it.e < 0) break;
         if (it.kend == it.kbeg) continue;
         // BF16: two accumulators alternate; FP8: one accumulator (TMEM also holds scale factors)
         const int acc = kFp8 ? 0 : (tcount & 1);
@@ -986,11 +969,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       const int slot = n % WORK_RING;
       const bool okw = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
       if (!__all_sync(0xffffffffu, okw)) break;
-      const int cur = ctl->work_item[slot];
+      const Item it = ctl->work[slot];
       __syncwarp();
       if (lane == 0) release_slot(slot);
-      if (cur < 0) break;
-      const Item it = decode_item<kMG>(p, cur, bk);
+      if (it.e < 0) break;
       const int esz = p.out_bf16 ? 2 : 4;
       char* obase = out_row_ptr<kMG>(p, it, static_cast<int>(rank) * BM + q * 32) + size_t(col0) * esz;
       const size_t ostride = size_t(p.I) * esz;
@@ -1161,11 +1143,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       const int slot = n % WORK_RING;
       const bool okw = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
       if (!__all_sync(0xffffffffu, okw)) break;
-      const int cur = ctl->work_item[slot];
+      const Item it = ctl->work[slot];
       __syncwarp();
       if (lane == 0) release_slot(slot);
-      if (cur < 0) break;
-      const Item it = decode_item<kMG>(p, cur, bk);
+      if (it.e < 0) break;
       // this warp's 32 output rows start at tile row rank*128 + q*32; row r is `ostride` bytes further
       char* obase = out_row_ptr<kMG>(p, it, static_cast<int>(rank) * BM + q * 32);
       const size_t ostride = size_t(p.I) * (p.out_bf16 ? 2 : 4);
@@ -1301,11 +1282,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         const int slot = n % WORK_RING;
         const bool okw = wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
         if (!__all_sync(0xffffffffu, okw)) break;
-        const int cur = ctl->work_item[slot];
+        const Item it = ctl->work[slot];
         __syncwarp();
         if (lane == 0) release_slot(slot);
-        if (cur < 0) break;
-        const Item it = decode_item<kMG>(p, cur, bk);
+        if (it.e < 0) break;
         bool ok = true;
         for (int kb = it.kbeg; kb < it.kend; ++kb) {
           // the scales have landed; this also means the copies of the previous round are done
@@ -1390,6 +1370,41 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           }
         }
         if (!ok) break;
+      }
+    }
+  }
+
+  if (warp == (kFp8 ? SCHED_WARP_FP8 : SCHED_WARP)) {
+    // ======================= Scheduler (leader CTA) =======================
+    // Claims items from the call's atomic counter one item ahead of the producer (the claim for
+    // item n+1 waits until the producer has started item n, so no CTA hoards work at the end of the
+    // queue), decodes each item once -- a binary search over the plan's prefix sums and a few reads
+    // of the offsets, a chain of dependent global loads -- and publishes the decoded item in the
+    // work ring of this CTA and of its peer, while the current item's k-loop runs.
+    if (lane == 0 && leader) {
+      int cur = atomicAdd(item_counter, 1);
+      for (int n = 0;; ++n) {
+        const int slot = n % WORK_RING;
+        Item it;
+        if (cur < total_items) {
+          it = decode_item<kMG>(p, cur, bk);
+        } else {
+          it = Item{};
+          it.e = -1;
+        }
+        if (!wait_bounded_t<kPair>(&ctl->wempty[slot], ((n / WORK_RING) & 1) ^ 1, abort_flag, p.timeout_ns)) break;
+        ctl->work[slot] = it;
+        if constexpr (kPair) {
+          const uint32_t dst = mapa_shared(smem_u32(&ctl->work[slot]), 1);
+          const uint4* w = reinterpret_cast<const uint4*>(&ctl->work[slot]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) st_cluster_v4(dst + 16 * i, w[i]);
+          mbar_arrive_remote(mapa_shared(smem_u32(&ctl->wfull[slot]), 1));
+        }
+        mbar_arrive(&ctl->wfull[slot]);
+        if (it.e < 0) break;
+        if (!wait_bounded_t<kPair>(&ctl->sched_go, n & 1, abort_flag, p.timeout_ns)) break;
+        cur = atomicAdd(item_counter, 1);
       }
     }
   }
