@@ -4,12 +4,15 @@
 //                             experts longest-first and writes the per-call schedule into the
 //                             workspace ("Grouped GEMM + WGrad (Unified)", sections "BF16 contract"
 //                             and "Scheduling, cache, and errors": dynamic persistent scheduling).
-//   wgrad_kernel (1 CTA / SM) persistent, warp-specialised: warp 0 claims work items from an
-//                             atomic counter and streams K-slices of A and B with TMA into a
-//                             4-stage shared-memory ring; warp 1 issues tcgen05.mma into one of two
-//                             FP32 TMEM accumulators; warps 2..5 drain TMEM and write the output
-//                             (overwrite / accumulate, FP32 / BF16, dense / per-expert pointers),
-//                             reducing split-K partial tiles in a fixed order.
+//   wgrad_kernel (1 CTA / SM, or a CTA pair per 256-row tile) persistent, warp-specialised: a
+//                             scheduler warp claims work items from an atomic counter one item
+//                             ahead and publishes them decoded in a shared-memory ring; warp 0
+//                             streams K-slices of A and B with TMA into a multi-stage shared-memory
+//                             ring; warp 1 issues tcgen05.mma into one of two FP32 TMEM
+//                             accumulators; warps 2..5 drain TMEM and write the output (overwrite /
+//                             accumulate, FP32 / BF16, dense / per-expert pointers), reducing
+//                             split-K partial tiles in a fixed order. The block-scaled variant adds
+//                             a scale-factor converter warp and uses eight epilogue warps.
 //
 // A work item is (expert, m-tile, n-tile, K chunk). For expert e the contraction runs over tokens
 // [begin_e, end_e) ("Grouped GEMM + WGrad (Unified)", section "Operation").
@@ -648,7 +651,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_stage_mem + EPI_STAGE_TOTAL);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: leader (issues MMAs, claims work)
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: leader (issues MMAs, schedules work)
   const bool leader = rank == 0;
   int32_t* item_counter = const_cast<int32_t*>(&hdr->item_counter);
   volatile int* abort_flag = &ctl->abort_flag;
@@ -1272,7 +1275,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
 
   if constexpr (kFp8) {
     if (warp == SF_WARP) {
-      // ======================= FP8 scale-factor converter (warp 6) =======================
+      // ======================= FP8 / FP4 scale-factor converter (warp 10) =======================
       // Per k-iteration: the stage's FP32 scales (128 of A, 256 of B) -> UE8M0 bytes (replicated
       // over the four 32-token blocks) in the TMEM layout read by the block-scaled MMA: 32 rows x
       // 4 words per block, word c of row l holding row/column 32c + l.
