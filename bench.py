@@ -8,11 +8,18 @@ Default workload: BF16 balanced, 8 experts, hidden 4096, intermediate 2048, per-
 round_to_256(4096*U(0.7,1.3)) (seed 1), FP32 dense output, overwrite. Its working set
 (A + B + output, ~0.67 GB) is larger than L2, so no explicit flush is needed between steps.
 
-Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle on the host cores
-instead (a bounded sample of the same workload per step).
+Prints ONE JSON line (rank 0): the device-timed rate, the roofline of the main kernel (achieved
+rate from CUDA events around each call, the measured peak, the DRAM bytes of one launch from the
+committed ncu summary while the kernel source is unchanged), the end-to-end rate through the same
+C entry point with pinned host inputs copied in and the result copied out every step (median of
+five timed blocks), sampled clocks, and the float64 CPU oracle's rate on a bounded sample.
+``--impl reference`` times the CPU oracle on the host cores instead (a bounded sample of the same
+workload per step).
 
-``--workload mg_forward|mg_dgrad|mg_masked`` times the M-grouped GEMM instead (forward / dgrad
-of the same MoE layer, and the masked decode layout): TFLOP/s counting 2*N*K*(valid rows).
+Other K-grouped workloads: ``--workload wide|skewed|fp8|fp4|unaligned|tiny``. The M-grouped GEMM
+(forward / dgrad of the same MoE layer, the masked decode layout, and their FP8 forms):
+``--workload mg_forward|mg_dgrad|mg_masked|mg_fp8_forward|mg_fp8_masked|mg_tiny``, TFLOP/s
+counting 2*N*K*(valid rows).
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (experts are
 independent; there is no data-path exchange), timing is the max over ranks: weak scaling.
