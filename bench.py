@@ -4,9 +4,12 @@ One step = one call of the whole operation (plan kernel + persistent tcgen05 ker
 batch of synthetic input: Wgrad[e] = A[:, begin_e:end_e] @ B[begin_e:end_e, :] for every
 expert. Metric: TFLOP/s counting 2*hidden*intermediate*sum(n_e) FLOPs.
 
-Default workload: BF16 balanced, 8 experts, hidden 4096, intermediate 2048, per-expert tokens
-round_to_256(4096*U(0.7,1.3)) (seed 1), FP32 dense output, overwrite. Its working set
-(A + B + output, ~0.67 GB) is larger than L2, so no explicit flush is needed between steps.
+Default workload: BF16 wide-hidden, 32 experts, hidden 7168, intermediate 2048, per-expert tokens
+round_to_256(2048*U(0.5,1.5)) with two experts set to 0 (seed 2), BF16 dense output pre-filled
+N(0,1), accumulate: the largest of the configurations that fit one GPU. Its working set (A + B +
+output, ~2.9 GB) is larger than L2, so no explicit flush is needed between steps. The default
+2000 timed steps (~2 s) run long enough for the clock sampler (every 50 ms) to see the GPU under
+sustained load; the roofline then uses the measured sustained bf16 peak.
 
 Prints ONE JSON line (rank 0): the device-timed rate, the roofline of the main kernel (achieved
 rate from CUDA events around each call, the measured peak, the DRAM bytes of one launch from the
@@ -21,8 +24,12 @@ Other K-grouped workloads: ``--workload wide|skewed|fp8|fp4|unaligned|tiny``. Th
 ``--workload mg_forward|mg_dgrad|mg_masked|mg_fp8_forward|mg_fp8_masked|mg_tiny``, TFLOP/s
 counting 2*N*K*(valid rows).
 
-Multi-GPU (torchrun): every rank runs its own replica of the workload (experts are
-independent; there is no data-path exchange), timing is the max over ranks: weak scaling.
+Multi-GPU (torchrun, N ranks): the job is the gradients of N MoE layers of the workload's shape
+(layer 0 is the workload itself; layer l permutes its expert counts with seed + 1000*l), and the
+N*E experts are placed on ranks by ``grouped_gemm_expert_gb300.partition.assign_experts``
+(longest first, balanced token sums). Each rank computes its own experts from its own tokens with
+no data-path exchange; timing is the max over ranks and the value counts all N layers: weak
+scaling (the work per rank stays one layer's worth).
 """
 from __future__ import annotations
 
@@ -68,20 +75,24 @@ def dist_env():
 # Clock sampling during the timed region
 # ---------------------------------------------------------------------------------------------
 class ClockSampler:
+    """nvidia-smi sampled every 50 ms in the background; each line is stamped with the host clock
+    so that only the samples taken inside the timed region count as "under load"."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.lines = []
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.INTERVAL_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except (FileNotFoundError, OSError):
@@ -89,33 +100,50 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """The host-clock window of the timed region."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0,
+                    "samples_under_load": 0}
         time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return summarize_clocks(self.lines, self.window)
+
+
+def summarize_clocks(lines, window):
+    """Median SM clock, maximum clock, active throttle reasons and sample counts.
+
+    lines: [(host time, csv line)] in ClockSampler.FIELDS order. Samples stamped inside
+    ``window`` (the timed region) are the ones under load; the median and the reasons come from
+    them (from every sample when none falls inside).
+    """
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    rows = []
+    for t, ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm, smax, pw = float(parts[0]), float(parts[1]), float(parts[2])
+        except ValueError:
+            continue
+        rows.append((t, sm, smax, pw, [nm for nm, v in zip(names, parts[4:8]) if v.lower() == "active"]))
+    load = [r for r in rows if window and window[0] <= r[0] <= window[1]]
+    use = load or rows
+    reasons = sorted({nm for r in use for nm in r[4]})
+    return {"sm_mhz": statistics.median(r[1] for r in use) if use else None,
+            "sm_max_mhz": max(r[2] for r in rows) if rows else None,
+            "power_w_median": statistics.median(r[3] for r in use) if use else None,
+            "reasons": reasons, "samples": len(rows), "samples_under_load": len(load)}
 
 
 def max_over_ranks(value: float, world: int, device=None) -> float:
@@ -175,14 +203,59 @@ def algorithmic_bytes(w) -> int:
     return int(b)
 
 
+NOMINAL_DENSE_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0, "fp4": 13500.0}
+SUSTAINED_AFTER_S = 1.0   # a timed region at least this long is compared with the sustained peak
+
+
+def tensor_roofline(achieved: float, w, peaks, timed_s: float) -> dict:
+    """Roofline of a tensor-bound call: the measured bf16 peak (the sustained loop figure when the
+    timed region lasts a second or more, else the burst), times the nominal dense ratio for FP8 (2)
+    and FP4 (6); the fractions of the burst and of the nominal dense peak are reported beside it."""
+    dt = "fp4" if getattr(w, "fp4", False) else ("fp8" if w.fp8 else "bf16")
+    ratio = NOMINAL_DENSE_TFLOPS[dt] / NOMINAL_DENSE_TFLOPS["bf16"]
+    sustained = timed_s >= SUSTAINED_AFTER_S and peaks.get("bf16_tflops_sustained")
+    base = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    peak = base * ratio
+    kind = "sustained" if sustained else "burst"
+    return {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"{peaks['source']} bf16 {kind}" + (f" x{ratio:g} (nominal dense ratio)" if ratio != 1 else "")
+            + f", timed region {timed_s:.2f} s",
+            "frac_vs_burst": achieved / (peaks["bf16_tflops"] * ratio),
+            "frac_vs_nominal": achieved / NOMINAL_DENSE_TFLOPS[dt]}
+
+
+def layer_counts(w, layer: int) -> np.ndarray:
+    """Expert token counts of MoE layer ``layer`` of a multi-rank job: layer 0 is the workload's own
+    counts, layer l a seeded permutation of them (the same count mix on other experts)."""
+    counts = np.asarray(w.counts, dtype=np.int64)
+    if layer == 0:
+        return counts
+    return counts[np.random.default_rng(w.seed + 1000 * layer).permutation(len(counts))]
+
+
+def rank_workload(w, rank: int, world: int):
+    """This rank's share of an N-layer job: the experts ``assign_experts`` places on it, as a local
+    problem of the same shape and modes (its own tokens, drawn with a per-rank seed)."""
+    import dataclasses
+
+    from grouped_gemm_expert_gb300.partition import assign_experts
+
+    if world == 1:
+        return w
+    all_counts = np.concatenate([layer_counts(w, l) for l in range(world)])
+    mine = assign_experts(all_counts, world)[rank]
+    if not mine:
+        return None
+    return dataclasses.replace(w, num_experts=len(mine), counts=all_counts[mine], seed=w.seed + 1000 * rank,
+                               name=f"{w.name} [rank {rank} of {world}: {len(mine)} experts]")
+
+
 def run_ours(args, w, rank, local, world):
     import grouped_gemm_expert_gb300 as kgw
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    # each rank processes its own batch: same shapes and counts, its own random values
-    import dataclasses
-    x = W.make_inputs_device(dataclasses.replace(w, seed=w.seed + 1000 * rank), dev)
+    x = W.make_inputs_device(w, dev)
     E, H, I = w.num_experts, w.hidden, w.intermediate
     odt = torch.bfloat16 if w.out_dtype == "bf16" else torch.float32
     if w.output_mode == "dense":
@@ -239,6 +312,7 @@ def run_ours(args, w, rank, local, world):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    h0 = time.monotonic()
     t0.record(stream)
     for i in range(args.steps):
         starts[i].record(stream)
@@ -246,16 +320,19 @@ def run_ours(args, w, rank, local, world):
         ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
+    h1 = time.monotonic()
     if world > 1:
         torch.distributed.barrier()
+    clocks.mark(h0, h1)
     clk = clocks.stop() if rank == 0 else None
     total_ms = t0.elapsed_time(t1)
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
+    timed_s = total_ms * 1e-3
 
     if args.no_e2e:
-        return ms_per_step, per_launch_ms, None, 0, 0, clk
+        return ms_per_step, per_launch_ms, None, 0, 0, clk, timed_s
     # ---- end to end through the public API, every step: the step's inputs are copied from
     # pinned host memory to the device, the call runs, and its result is copied back to pinned
     # host memory. Steps are pipelined over two buffer sets and three streams (copy-in, compute,
@@ -328,7 +405,7 @@ def run_ours(args, w, rank, local, world):
     e2e_ms = max_over_ranks(statistics.median(blocks), world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {kgw.kgw_status_string(int(status.item()))}")
-    return ms_per_step, per_launch_ms, e2e_ms, h2d, d2h, clk
+    return ms_per_step, per_launch_ms, e2e_ms, h2d, d2h, clk, timed_s
 
 
 def mg_algorithmic_bytes(w) -> int:
@@ -396,6 +473,7 @@ def run_ours_mg(args, w, rank, local, world):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    h0 = time.monotonic()
     for i in range(args.steps):
         if flush is not None:
             flush.fill_(1)
@@ -403,14 +481,17 @@ def run_ours_mg(args, w, rank, local, world):
         call(kargs, x.sfa, x.sfb)
         ends[i].record(stream)
     torch.cuda.synchronize()
+    h1 = time.monotonic()
     if world > 1:
         torch.distributed.barrier()
+    clocks.mark(h0, h1)
     clk = clocks.stop() if rank == 0 else None
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     # a step is the call; the L2 flush between calls is not part of it
     ms_per_step = max_over_ranks(statistics.mean(per_launch_ms), world, dev)
+    timed_s = h1 - h0
     if args.no_e2e:
-        return ms_per_step, per_launch_ms, None, 0, 0, clk
+        return ms_per_step, per_launch_ms, None, 0, 0, clk, timed_s
     # end to end: inputs from pinned host memory, the call, D back to pinned host memory (serial)
     host_in = [t.cpu().pin_memory() for t in (x.a, x.b, x.groups) + ((x.sfa, x.sfb) if w.fp8 else ())]
     host_d0 = None if x.d0 is None else x.d0.cpu().pin_memory()
@@ -446,35 +527,51 @@ def run_ours_mg(args, w, rank, local, world):
     e2e_ms = max_over_ranks(statistics.median(blocks), world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {kgw.kgw_status_string(int(status.item()))}")
-    return ms_per_step, per_launch_ms, e2e_ms, h2d, d2h, clk
+    return ms_per_step, per_launch_ms, e2e_ms, h2d, d2h, clk, timed_s
 
 
-def cpu_oracle_rate_mg(w, budget_s: float):
-    """Time the float64 M-grouped oracle over whole groups until ``budget_s`` is spent."""
-    import oracle.kgw_oracle as O
-    import oracle.mgrouped_oracle as MO
+class MgOracleSampler:
+    """The float64 M-grouped oracle, as it stands, on the host cores: the operands are decoded once,
+    then ``run`` evaluates the oracle on blocks of up to 512 rows of one group at a time (each a
+    single-group problem through the oracle's own entry point) until a time budget is spent."""
+    ROWS = 512
 
-    x = MW.make_mg_inputs(w, "cpu")
-    if w.fp8:
-        u8 = lambda t: t.contiguous().view(torch.uint8).numpy()
-        A, B = MO.dequantize_fp8(u8(x.a), u8(x.b), x.sfa.numpy(), x.sfb.numpy(), w.b_major, w.sf_format)
-    else:
-        A = O.bf16_to_f64(x.a.contiguous().view(torch.int16).numpy().view(np.uint16)).reshape(-1, w.k)
-        B = O.bf16_to_f64(x.b.contiguous().view(torch.int16).numpy().view(np.uint16))
-    groups = x.groups.numpy()
-    per_group = [(g, r) for g, r in enumerate(MO.group_rows(w.layout, groups, w.m, w.num_groups)) if len(r)]
-    flops, done = 0.0, 0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s:
-        for g, r in per_group:
-            # one group at a time through the oracle's own entry point (a single-group problem)
-            MO.mgrouped(A[r], B[g:g + 1], "offsets", [len(r)], len(r), b_major=w.b_major, with_bound=False)
+    def __init__(self, w):
+        import oracle.kgw_oracle as O
+        import oracle.mgrouped_oracle as MO
+
+        self.w, self.MO = w, MO
+        x = MW.make_mg_inputs(w, "cpu")
+        if w.fp8:
+            u8 = lambda t: t.contiguous().view(torch.uint8).numpy()
+            self.A, self.B = MO.dequantize_fp8(u8(x.a), u8(x.b), x.sfa.numpy(), x.sfb.numpy(), w.b_major, w.sf_format)
+        else:
+            self.A = O.bf16_to_f64(x.a.contiguous().view(torch.int16).numpy().view(np.uint16)).reshape(-1, w.k)
+            self.B = O.bf16_to_f64(x.b.contiguous().view(torch.int16).numpy().view(np.uint16))
+        groups = x.groups.numpy()
+        self.units = [(g, r[i:i + self.ROWS]) for g, r in enumerate(MO.group_rows(w.layout, groups, w.m, w.num_groups))
+                      for i in range(0, len(r), self.ROWS)]
+        self.next = 0
+
+    def run(self, budget_s: float):
+        """(TFLOP/s, seconds, units done): at least one unit, then more until ``budget_s``."""
+        w = self.w
+        flops, done = 0.0, 0
+        t0 = time.perf_counter()
+        while done == 0 or time.perf_counter() - t0 < budget_s:
+            g, r = self.units[self.next % len(self.units)]
+            self.next += 1
+            self.MO.mgrouped(self.A[r], self.B[g:g + 1], "offsets", [len(r)], len(r), b_major=w.b_major,
+                             with_bound=False)
             flops += 2.0 * len(r) * w.n * w.k
             done += 1
-            if time.perf_counter() - t0 > budget_s:
-                break
-    dt = time.perf_counter() - t0
-    return flops / dt / 1e12, dt, done
+        dt = time.perf_counter() - t0
+        return flops / dt / 1e12, dt, done
+
+
+def reference_budget(args) -> float:
+    """Seconds of oracle work per reference step, so that warm-up plus timed steps take ~2 minutes."""
+    return max(0.05, min(15.0, 120.0 / max(1, args.steps + args.warmup)))
 
 
 def main_mg(args, world, rank, local):
@@ -484,14 +581,16 @@ def main_mg(args, world, rank, local):
     config = {"workload": w.name, "groups": w.num_groups, "layout": w.layout, "m": w.m, "n": w.n, "k": w.k,
               "valid_rows": w.valid_rows, "b_major": w.b_major, "output": w.out_dtype, "accumulate": w.accumulate,
               "l2": "L2 flushed (256 MB write) between steps" if w.layout == "masked"
-              else "inputs larger than L2 (no flush needed)", "parallelism": f"replica x{args.gpus}"}
+              else "inputs larger than L2 (no flush needed)",
+              "parallelism": "single GPU" if world == 1 else f"replica x{world} (one batch per rank)"}
     if args.impl == "reference":
         if rank != 0:
             return
-        budget = max(2.0, min(15.0, 120.0 / max(1, args.steps + args.warmup)))
+        sampler = MgOracleSampler(w)
+        budget = reference_budget(args)
         rates = []
         for i in range(args.warmup + args.steps):
-            r, dt, done = cpu_oracle_rate_mg(w, budget)
+            r, dt, done = sampler.run(budget)
             if i >= args.warmup:
                 rates.append((r, dt, done))
         val = statistics.median(r for r, _, _ in rates)
@@ -501,26 +600,26 @@ def main_mg(args, world, rank, local):
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic", "config": config,
                           "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                                           "sample": f"float64 oracle over whole groups, {ms / 1e3:.1f} s per step"},
+                                           "sample": f"float64 oracle over blocks of up to {MgOracleSampler.ROWS} rows of one group, "
+                                                     f"{ms / 1e3:.2f} s per step"},
                           "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
         return
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    ms_per_step, per_launch, e2e_ms, h2d, d2h, clk = run_ours_mg(args, w, rank, local, world)
+    ms_per_step, per_launch, e2e_ms, h2d, d2h, clk, timed_s = run_ours_mg(args, w, rank, local, world)
     value = job_throughput(flops, ms_per_step, world)
     peaks = measured_peaks()
     launch_ms = statistics.mean(per_launch)
     achieved = flops / (launch_ms * 1e-3) / 1e12
     abytes = mg_algorithmic_bytes(w)
     # below the ridge point (few rows per group: the decode case) the weights' HBM reads bound it
-    tpeak = peaks["bf16_tflops"] * (2.0 if w.fp8 else 1.0)   # fp8: the nominal dense ratio x the bf16 burst
-    hbm_bound = flops / abytes < tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    troof = tensor_roofline(achieved, w, peaks, timed_s)
+    hbm_bound = flops / abytes < troof["peak"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if hbm_bound:
         roof = {"bound": "hbm", "achieved": abytes / (launch_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "peak_source": f"{peaks['source']} HBM copy"}
     else:
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
-                "peak_source": f"{peaks['source']} bf16 burst" + (" x2 (nominal dense ratio)" if w.fp8 else "")}
+        roof = troof
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": traffic_record(args.workload),
                  "algorithmic_bytes": abytes, "flops": flops,
                  "kernel": "wgrad_kernel M-grouped instantiation (+ plan_mgrouped_kernel)"})
@@ -532,45 +631,58 @@ def main_mg(args, world, rank, local):
                                                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps, "clocks": clk}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, dt, done = cpu_oracle_rate_mg(w, args.cpu_budget)
+        r, dt, done = MgOracleSampler(w).run(args.cpu_budget)
         line["cpu_baseline"] = {"value": r, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"float64 oracle, {done} whole-group products of the same workload, {dt:.1f} s"}
+                                "sample": f"float64 oracle, {done} blocks of up to {MgOracleSampler.ROWS} rows of one "
+                                          f"group of the same workload, {dt:.1f} s"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def cpu_oracle_rate(w, budget_s: float):
-    """Time the float64 oracle on the host cores over whole experts until ``budget_s`` is spent."""
-    import oracle.kgw_oracle as O
+class OracleSampler:
+    """The float64 oracle, as it stands, on the host cores: the operands are decoded (and scaled)
+    once, then ``run`` evaluates the oracle's ``wgrad`` on blocks of up to 512 rows of A_e for one
+    expert at a time (the same definition on a row block) until a time budget is spent."""
+    ROWS = 512
 
-    x = W.make_inputs(w, "cpu")
-    bits = (lambda t: t.contiguous().view(torch.uint8).numpy()) if (w.fp8 or w.fp4) else \
-        (lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16))
-    a_bits, b_bits = bits(x.a), bits(x.b)
-    dec = O.e2m1_to_f64 if w.fp4 else (O.e4m3_to_f64 if w.fp8 else O.bf16_to_f64)
-    A = O.logical_a(dec(a_bits), w.hidden, w.offsets, w.input_order, w.a_major)
-    B = O.logical_b(dec(b_bits), w.intermediate, w.offsets, w.input_order, w.b_major)
-    if w.fp8 or w.fp4:
-        sa, blk = O.decode_scales(x.sfa.numpy(), w.sf_format)
-        sb, _ = O.decode_scales(x.sfb.numpy(), w.sf_format)
-        A = O.apply_scales_rows(A, sa, blk)
-        B = O.apply_scales_cols(B, sb, blk)
-    ranges = [(e, b, end) for e, (b, end) in enumerate(O.expert_ranges(w.offsets)) if end > b]
-    flops = 0.0
-    n_experts = 0
-    t0 = time.perf_counter()
-    # whole experts, in order, repeating the workload until the time budget is spent
-    while time.perf_counter() - t0 < budget_s:
-        for e, b, end in ranges:
-            O.wgrad(A[:, b:end], B[b:end, :], np.array([end - b], dtype=np.int64), with_bound=False)
-            flops += 2.0 * w.hidden * w.intermediate * (end - b)
-            n_experts += 1
-            if time.perf_counter() - t0 > budget_s:
-                break
-    dt = time.perf_counter() - t0
-    return flops / dt / 1e12, dt, n_experts
+    def __init__(self, w):
+        import oracle.kgw_oracle as O
+
+        self.w, self.O = w, O
+        x = W.make_inputs(w, "cpu")
+        bits = (lambda t: t.contiguous().view(torch.uint8).numpy()) if (w.fp8 or w.fp4) else \
+            (lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16))
+        a_bits, b_bits = bits(x.a), bits(x.b)
+        del x.a, x.b
+        dec = O.e2m1_to_f64 if w.fp4 else (O.e4m3_to_f64 if w.fp8 else O.bf16_to_f64)
+        A = O.logical_a(dec(a_bits), w.hidden, w.offsets, w.input_order, w.a_major)
+        B = O.logical_b(dec(b_bits), w.intermediate, w.offsets, w.input_order, w.b_major)
+        if w.fp8 or w.fp4:
+            sa, blk = O.decode_scales(x.sfa.numpy(), w.sf_format)
+            sb, _ = O.decode_scales(x.sfb.numpy(), w.sf_format)
+            A = O.apply_scales_rows(A, sa, blk)
+            B = O.apply_scales_cols(B, sb, blk)
+        self.A, self.B = A, B
+        self.units = [(b, end, r0) for (b, end) in O.expert_ranges(w.offsets) if end > b
+                      for r0 in range(0, w.hidden, self.ROWS)]
+        self.next = 0
+
+    def run(self, budget_s: float):
+        """(TFLOP/s, seconds, units done): at least one unit, then more until ``budget_s``."""
+        w, O = self.w, self.O
+        flops, done = 0.0, 0
+        t0 = time.perf_counter()
+        while done == 0 or time.perf_counter() - t0 < budget_s:
+            b, end, r0 = self.units[self.next % len(self.units)]
+            self.next += 1
+            r1 = min(w.hidden, r0 + self.ROWS)
+            O.wgrad(self.A[r0:r1, b:end], self.B[b:end, :], np.array([end - b], dtype=np.int64), with_bound=False)
+            flops += 2.0 * (r1 - r0) * w.intermediate * (end - b)
+            done += 1
+        dt = time.perf_counter() - t0
+        return flops / dt / 1e12, dt, done
 
 
 def blas_threads():
@@ -585,10 +697,10 @@ def blas_threads():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="balanced", choices=sorted(W.NAMED) + sorted(MW.MG_NAMED))
+    ap.add_argument("--workload", default="wide", choices=sorted(W.NAMED) + sorted(MW.MG_NAMED))
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (profiling runs)")
@@ -604,17 +716,19 @@ def main():
     config = {"workload": w.name, "experts": w.num_experts, "hidden": w.hidden, "intermediate": w.intermediate,
               "tokens_sum": w.tokens_sum, "input_order": w.input_order, "output": f"{w.output_mode} {w.out_dtype}",
               "accumulate": w.accumulate, "l2": "inputs larger than L2 (no flush needed)",
-              "parallelism": f"replica x{args.gpus}"}
+              "parallelism": "single GPU" if world == 1 else
+              f"expert-parallel x{world}: {world} layers' experts placed longest-first on {world} ranks"}
     if w.tokens_sum * (w.hidden + w.intermediate) * 2 < 129e6:
         config["l2"] = "working set fits L2 (warm)"
 
     if args.impl == "reference":
         if rank != 0:
             return
-        budget = max(2.0, min(15.0, 120.0 / max(1, args.steps + args.warmup)))
+        sampler = OracleSampler(w)
+        budget = reference_budget(args)
         rates = []
         for i in range(args.warmup + args.steps):
-            r, dt, done = cpu_oracle_rate(w, budget)
+            r, dt, done = sampler.run(budget)
             if i >= args.warmup:
                 rates.append((r, dt, done))
         val = statistics.median(r for r, _, _ in rates)
@@ -624,41 +738,40 @@ def main():
                 "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                                 "sample": f"float64 oracle over whole experts of the workload (repeating it), "
-                                           f"{ms / 1e3:.1f} s per step"},
+                                 "sample": f"float64 oracle over blocks of up to {OracleSampler.ROWS} rows of one "
+                                           f"expert's product (cycling through the workload), {ms / 1e3:.2f} s per step"},
                 "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
 
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    ms_per_step, per_launch, e2e_ms, h2d, d2h, clk = run_ours(args, w, rank, local, world)
+    wl = rank_workload(w, rank, world)
+    if wl is None:
+        raise RuntimeError(f"rank {rank} was assigned no experts")
+    ms_per_step, per_launch, e2e_ms, h2d, d2h, clk, timed_s = run_ours(args, wl, rank, local, world)
+    # every layer has the workload's token sum: the job's FLOPs are world x the workload's
     value = job_throughput(flops, ms_per_step, world)
     peaks = measured_peaks()
     launch_ms = statistics.mean(per_launch)
-    achieved = flops / (launch_ms * 1e-3) / 1e12
-    # another dtype's peak: the measured bf16 burst times the nominal dense ratio (fp8 2x, fp4 6x)
-    ratio = 6.0 if w.fp4 else (2.0 if w.fp8 else 1.0)
-    peak = peaks["bf16_tflops"] * ratio
-    traffic = traffic_record(args.workload)
+    achieved = wl.flops / (launch_ms * 1e-3) / 1e12
+    roof = tensor_roofline(achieved, w, peaks, timed_s)
+    traffic = traffic_record(args.workload) if world == 1 else None
     line = {"metric": "K-grouped wgrad TFLOP/s (2*H*I*sum n_e)", "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp4" if w.fp4 else ("fp8" if w.fp8 else "bf16"), "data": "synthetic", "config": config,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes": algorithmic_bytes(w),
-                         "peak_source": f"{peaks['source']} bf16 burst" + (f" x{ratio:g} (nominal dense ratio)" if ratio != 1 else ""),
-                         "kernel": "wgrad_kernel (+ plan_kernel, a few us, inside the same events)"},
+            "roofline": dict(roof, traffic=traffic, algorithmic_bytes=algorithmic_bytes(wl),
+                             kernel="wgrad_kernel (+ plan_kernel, a few us, inside the same events)"),
             "e2e": None if e2e_ms is None else {"value": job_throughput(flops, e2e_ms, world), "unit": "TFLOP/s",
                                                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * args.steps,
             "clocks": clk}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, dt, done = cpu_oracle_rate(w, args.cpu_budget)
+        r, dt, done = OracleSampler(w).run(args.cpu_budget)
         line["cpu_baseline"] = {"value": r, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"float64 oracle, {done} whole-expert products of the same workload "
-                                          f"(repeating it), {dt:.1f} s"}
+                                "sample": f"float64 oracle, {done} blocks of up to {OracleSampler.ROWS} rows of one "
+                                          f"expert's product of the same workload, {dt:.1f} s"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

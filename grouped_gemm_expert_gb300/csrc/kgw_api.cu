@@ -358,10 +358,33 @@ constexpr int32_t kNoAllocMaxExperts = 1024;
 // device array. Its device address comes from cudaGetSymbolAddress (noalloc_scratch below).
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Per device: the context the address was looked up in, and the address. A device reset (or a
+// primary context torn down and created again) gives the device a new context in which the array
+// lives at another address, so the address is looked up again whenever the current context differs.
 void* g_noalloc_ptr[kMaxDevices] = {};
+CUcontext g_noalloc_ctx[kMaxDevices] = {};
 std::mutex g_noalloc_mu;
 
-// Device address of the static scratch on the current device (looked up once per device).
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_current_once;
+
+kgw_status current_context(CUcontext* ctx) {
+  std::call_once(g_ctx_current_once, [] {
+    cudaDriverEntryPointQueryResult q{};
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    else
+      cudaGetLastError();
+  });
+  if (!g_ctx_current) return KGW_ERR_CUDA;
+  *ctx = nullptr;
+  return g_ctx_current(ctx) == CUDA_SUCCESS ? KGW_OK : KGW_ERR_CUDA;
+}
+
+// Device address of the static scratch on the current device: looked up (cudaGetSymbolAddress,
+// with the device current) on the first call on each device and again after its context changed.
 kgw_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -370,16 +393,25 @@ kgw_status noalloc_scratch(void** out) {
   }
   if (dev < 0 || dev >= kMaxDevices) return KGW_ERR_DEVICE;
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
+  void* p = g_noalloc_ptr[dev];
+  if (p) {
+    CUcontext ctx = nullptr;
+    if (current_context(&ctx) != KGW_OK) return KGW_ERR_CUDA;
+    if (ctx != g_noalloc_ctx[dev]) p = nullptr;
+  }
+  if (!p) {
+    // the runtime binds the device's primary context here if no call has yet
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return KGW_ERR_CUDA;
     }
+    CUcontext ctx = nullptr;
+    if (current_context(&ctx) != KGW_OK || ctx == nullptr) return KGW_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = p;
   return KGW_OK;
 }
 

@@ -101,8 +101,11 @@ typedef struct kgw_wgrad_args {
  * Workspace bytes needed by kgw_wgrad_bf16 (is_fp8 = 0) or kgw_wgrad_fp8_blockscaled
  * (is_fp8 = 1) for these shapes. Depends only on num_experts, hidden, intermediate and
  * tokens_sum (not on the offsets' values). Host-only; never touches the GPU.
- * The workspace holds the per-call schedule and the FP32 partial tiles of split-K; a caller
- * may pass less than this (down to the schedule alone) and the kernel then splits less.
+ * The workspace holds the per-call schedule of the dynamic persistent scheduler ("Grouped GEMM +
+ * WGrad (Unified)", section "Scheduling, cache, and errors") and the FP32 partial tiles of
+ * split-K; a caller may pass less than this (down to the schedule alone) and the kernel then
+ * splits less. Errors as for the calls it sizes (KGW_ERR_INVALID_ARG, KGW_ERR_UNSUPPORTED,
+ * KGW_ERR_ALIGNMENT); *bytes is written only on KGW_OK.
  */
 kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t* bytes);
 
@@ -178,14 +181,22 @@ kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
  *
  * Scratch: the per-call schedule and the split-K partial tiles live in one static device array
  * of 2 MiB inside the library, which every GPU that loads the library keeps until the process
- * exits. It holds the schedule for up to 1024 experts plus a few FP32 partial tiles; calls with
- * more than 1024 experts return KGW_ERR_SCRATCH_LIMIT and enqueue nothing. With fewer partial
- * tiles than kgw_wgrad_bf16 may use, long experts are split less; results stay within the same
- * error bound (the summation order can differ from kgw_wgrad_bf16's).
+ * exits. It holds the schedule for up to 1024 experts plus a few FP32 partial tiles (13 to 15
+ * of 128 x 256, or 6 to 7 of the 256 x 256 tiles used when hidden % 256 == 0, fewer the more
+ * experts there are); calls with more than 1024 experts return KGW_ERR_SCRATCH_LIMIT and enqueue
+ * nothing. An expert is split along its tokens only when all of its pieces fit: splitting needs at
+ * least 2 * T partial tiles, with T = (hidden / tile rows) * (intermediate / 256) output tiles
+ * per expert, so split-K is off once T exceeds 3 (256-row tiles) or 6 to 7 (128-row tiles), which
+ * includes every full-size workload of this library's benchmarks; long experts then run unsplit,
+ * which changes the load balance under skewed routing but not the results' error bound (the
+ * summation order can differ from kgw_wgrad_bf16's).
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture. No call allocates (no cudaMalloc/cudaFree, no allocating library routine).
+ * capture. The address belongs to the device's current CUDA context: after a device reset, or
+ * when the primary context is destroyed and created again, the next call sees a different
+ * current context and looks the address up again (that call, too, should come before any stream
+ * capture). No call allocates (no cudaMalloc/cudaFree, no allocating library routine).
  *
  * Sharing: every call on a device uses the same array and it keeps the previous call's
  * contents; the kernels re-initialise every counter they read, so nothing needs clearing by
@@ -265,7 +276,10 @@ kgw_status kgw_mgrouped_bf16(const kgw_mgrouped_args* args, void* workspace, siz
 kgw_status kgw_mgrouped_fp8(const kgw_mgrouped_args* args, const void* sfa, const void* sfb, int32_t sf_format,
                             void* workspace, size_t workspace_bytes, void* stream);
 
-/* Human-readable name of a status code (static storage). */
+/* Human-readable name of a status code (static storage; "KGW_ERR_UNKNOWN" for any other value). The
+ * codes mirror the rejections listed in "Grouped GEMM + WGrad (Unified)", section "Scheduling,
+ * cache, and errors" (unsupported dtypes or layouts, malformed offsets or pointers, devices below
+ * SM100), plus the device-side bounded-wait and scale checks of this library. */
 const char* kgw_status_string(int32_t status);
 
 /* Library ABI version (major*100 + minor). */

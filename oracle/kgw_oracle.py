@@ -53,10 +53,6 @@ def bf16_to_f64(bits) -> np.ndarray:
     return u.view(np.float32).astype(np.float64)
 
 
-def f32_to_f64(x) -> np.ndarray:
-    return np.asarray(x, dtype=np.float32).astype(np.float64)
-
-
 def e4m3_to_f64(bits) -> np.ndarray:
     """Decode raw float8 e4m3 (the 'fn' variant: no infinities) bit patterns to float64.
 
@@ -172,20 +168,6 @@ def logical_b(b_values: np.ndarray, intermediate: int, offsets, input_order: str
         if n:
             out[b:e, :] = flat[b * intermediate:(b + n) * intermediate].reshape(intermediate, n).T
     return out
-
-
-def apply_block_scales_rows(x: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """A-side FP8 scaling: x [rows, tokens], scales [tokens/128, rows] -> x[m,k]*s[k//128, m]."""
-    rows, tokens = x.shape
-    s = np.asarray(scales, dtype=np.float64).reshape(tokens // SCALE_BLOCK, rows)
-    return x * np.repeat(s.T, SCALE_BLOCK, axis=1)
-
-
-def apply_block_scales_cols(x: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """B-side FP8 scaling: x [tokens, cols], scales [tokens/128, cols] -> x[k,n]*s[k//128, n]."""
-    tokens, cols = x.shape
-    s = np.asarray(scales, dtype=np.float64).reshape(tokens // SCALE_BLOCK, cols)
-    return x * np.repeat(s, SCALE_BLOCK, axis=0)
 
 
 def unpack_ue8m0_32(packed) -> np.ndarray:
@@ -316,7 +298,7 @@ def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int
 
     Only row m of A_e and column n of B_e are decoded, so this works at full problem size.
     Addressing follows ``logical_a``/``logical_b``; FP8 scales follow
-    ``apply_block_scales_rows``/``apply_block_scales_cols``.
+    ``apply_scales_rows``/``apply_scales_cols``.
     """
     b, end = expert_ranges(offsets)[e]
     cnt = end - b
@@ -362,3 +344,53 @@ def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int
         arow = arow * sa[ks, m]
         bcol = bcol * sb[ks, n]
     return float(np.dot(arow, bcol)), float(np.dot(np.abs(arow), np.abs(bcol)))
+
+
+def expert_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, e: int, *,
+                        input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
+                        a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128",
+                        fp4: bool = False):
+    """(R_e, S_e) of one expert, decoding only that expert's operands (full-size checks).
+
+    The same definition as ``wgrad_from_storage`` restricted to expert e: A_e [hidden, n_e] and
+    B_e [n_e, intermediate] are read through the addressing of ``logical_a``/``logical_b``, each
+    element multiplied by the scale of its token block (FP8/FP4, as in ``apply_scales_rows``/
+    ``apply_scales_cols``), then R_e = A_e @ B_e and S_e = |A_e| @ |B_e| in float64. Memory is
+    bounded by one expert's operands, so every output element of a full-size problem can be
+    checked expert by expert. An empty expert gives zeros.
+    """
+    b, end = expert_ranges(offsets)[e]
+    n = end - b
+    if n == 0:
+        z = np.zeros((hidden, intermediate), dtype=np.float64)
+        return z, z.copy()
+    tokens_sum = expert_ranges(offsets)[-1][1]
+    fa = np.asarray(a_bits).reshape(-1)
+    fb = np.asarray(b_bits).reshape(-1)
+    if fp4:
+        # packed e2m1, both operands K-major tensor2d: row r holds tokens_sum/2 bytes
+        assert a_major == "k" and b_major == "k" and input_order == "tensor2d" and b % 2 == 0 and n % 2 == 0
+        Ae = e2m1_to_f64(np.ascontiguousarray(fa.reshape(hidden, tokens_sum // 2)[:, b // 2:end // 2])).reshape(hidden, n)
+        Be = e2m1_to_f64(np.ascontiguousarray(fb.reshape(intermediate, tokens_sum // 2)[:, b // 2:end // 2]))
+        Be = Be.reshape(intermediate, n).T
+    else:
+        dec = e4m3_to_f64 if fp8 else bf16_to_f64
+        if a_major == "mn":
+            Ae = dec(fa[b * hidden:end * hidden]).reshape(n, hidden).T
+        elif input_order == "tensor2d":
+            Ae = dec(fa.reshape(hidden, tokens_sum)[:, b:end])
+        else:
+            Ae = dec(fa[b * hidden:end * hidden]).reshape(hidden, n)
+        if b_major == "mn":
+            Be = dec(fb[b * intermediate:end * intermediate]).reshape(n, intermediate)
+        elif input_order == "tensor2d":
+            Be = dec(fb.reshape(intermediate, tokens_sum)[:, b:end]).T
+        else:
+            Be = dec(fb[b * intermediate:end * intermediate]).reshape(intermediate, n).T
+    if fp8 or fp4:
+        sa, blk = decode_scales(sfa, sf_format)
+        sb, _ = decode_scales(sfb, sf_format)
+        ks = np.arange(b, end) // blk
+        Ae = Ae * sa[ks, :].T
+        Be = Be * sb[ks, :]
+    return Ae @ Be, np.abs(Ae) @ np.abs(Be)

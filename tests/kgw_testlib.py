@@ -123,3 +123,50 @@ def assert_close_to_oracle(w, got: np.ndarray, ref: np.ndarray, S: np.ndarray, c
         msg = "; ".join(f"{tuple(i)} got={got[tuple(i)]:.6g} ref={ref[tuple(i)]:.6g} tol={tol[tuple(i)]:.3g}"
                         for i in idx)
         raise AssertionError(f"{int(bad.sum())} of {bad.size} elements out of tolerance: {msg}")
+
+
+def check_full(w, label=None, device="cuda"):
+    """Run workload ``w`` on the GPU and compare every output element with the oracle."""
+    import oracle.kgw_oracle as O
+    import workloads as W
+    kgw = ensure_built()
+    x_cpu = W.make_inputs(w, "cpu")
+    x = W.Inputs(*[None if t is None else t.to(device) for t in
+                   (x_cpu.a, x_cpu.b, x_cpu.offsets, x_cpu.sfa, x_cpu.sfb, x_cpu.c)])
+    status = torch.full((1,), -1, dtype=torch.int32, device=device)
+    outs = run_gpu(w, x, device, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, kgw.kgw_status_string(int(status.item()))
+    assert outs.guards_intact()
+    bits = bits8 if (w.fp8 or w.fp4) else bits16
+    a_bits, b_bits = bits(x_cpu.a), bits(x_cpu.b)
+    offsets = x_cpu.offsets.numpy()
+    sf = dict(sfa=None if x_cpu.sfa is None else x_cpu.sfa.numpy(),
+              sfb=None if x_cpu.sfb is None else x_cpu.sfb.numpy())
+    counts = np.asarray(w.counts)
+    worst, checked, bad = 0.0, 0, []
+    for e in range(w.num_experts):
+        if counts[e] == 0:
+            if w.accumulate:
+                assert torch.equal(outs.views[e], x.c[e]), f"empty expert {e} changed"
+            else:
+                assert not outs.views[e].any(), f"empty expert {e} not zero"
+            continue
+        r, s = O.expert_from_storage(a_bits, b_bits, offsets, w.hidden, w.intermediate, e,
+                                     input_order=w.input_order, fp8=w.fp8, a_major=w.a_major, b_major=w.b_major,
+                                     sf_format=w.sf_format, fp4=w.fp4, **sf)
+        c = to_f64(x_cpu.c[e]) if w.accumulate else None
+        ref = r if c is None else c + r
+        tol = O.tolerance(s, ref, w.out_dtype, c if (w.accumulate and w.out_dtype == "f32") else None)
+        got = to_f64(outs.views[e])
+        err = np.abs(got - ref)
+        ratio = err / tol
+        worst = max(worst, float(np.nanmax(ratio)) if ratio.size else 0.0)
+        checked += ref.size
+        over = ~(err <= tol)
+        if over.any():
+            i = tuple(np.argwhere(over)[0])
+            bad.append((e, int(over.sum()), i, float(got[i]), float(ref[i]), float(tol[i])))
+    print(f"[full parity] {label or w.name}: {checked} elements, worst err/tol = {worst:.3g}")
+    assert not bad, f"experts out of tolerance (expert, count, first index, got, ref, tol): {bad[:5]}"
+    return worst

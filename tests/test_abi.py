@@ -150,3 +150,12 @@ def test_binding_constants_match_the_header():
     assert len(found) >= 15
     for name, value in found:
         assert getattr(kgw, name) == int(value), name
+
+
+def test_noalloc_rejects_more_experts_than_its_scratch_holds():
+    """The entry point without a workspace keeps its scratch in a fixed static array: more than
+    1024 experts is rejected on the host, before any device query or launch."""
+    args = good_args(num_experts=1025, tokens_sum=256)
+    assert kgw.lib().kgw_wgrad_bf16_noalloc(ctypes.byref(args), None) == kgw.KGW_ERR_SCRATCH_LIMIT
+    bad = good_args(num_experts=1024, hidden=100)
+    assert kgw.lib().kgw_wgrad_bf16_noalloc(ctypes.byref(bad), None) == kgw.KGW_ERR_UNSUPPORTED

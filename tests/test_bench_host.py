@@ -83,3 +83,85 @@ def test_measured_peaks_come_from_the_driver_file_when_present():
         assert p["bf16_tflops"] > 1000 and p["hbm_gbs"] > 1000
     else:
         assert p["source"] == "fallback"
+
+
+# ------------------------------------------------------------------------------------------
+# Clock samples inside the timed region; the peak a long timed region is compared with
+# ------------------------------------------------------------------------------------------
+
+def _line(sm, power, cap="Not Active", hw="Not Active"):
+    return f"{sm}, 2070, {power}, 0x0, {hw}, Not Active, Not Active, {cap}"
+
+
+def test_clock_summary_counts_only_samples_inside_the_timed_region():
+    lines = [(0.0, _line(1980, 190)), (1.0, _line(1700, 1300, cap="Active")), (1.5, _line(1600, 1390, cap="Active")),
+             (2.0, _line(1650, 1350)), (3.5, _line(1990, 200)), (3.6, "garbage")]
+    c = bench.summarize_clocks(lines, (0.9, 2.1))
+    assert c["samples"] == 5 and c["samples_under_load"] == 3
+    assert c["sm_mhz"] == 1650 and c["sm_max_mhz"] == 2070
+    assert c["reasons"] == ["sw_power_cap"]
+    # no window: every sample counts, none is "under load"
+    c = bench.summarize_clocks(lines, None)
+    assert c["samples_under_load"] == 0 and c["sm_mhz"] == 1700
+
+
+def test_clock_summary_reports_hardware_slowdown():
+    c = bench.summarize_clocks([(1.0, _line(900, 700, hw="Active"))], (0.0, 2.0))
+    assert c["reasons"] == ["hw_slowdown"]
+
+
+def test_long_timed_regions_use_the_sustained_peak():
+    peaks = {"bf16_tflops": 1933.3, "bf16_tflops_sustained": 1720.6, "hbm_gbs": 6775.3, "source": "measured"}
+    w = W.NAMED["wide"]()
+    short = bench.tensor_roofline(1600.0, w, peaks, 0.02)
+    long = bench.tensor_roofline(1600.0, w, peaks, 2.1)
+    assert short["peak"] == 1933.3 and "burst" in short["peak_source"]
+    assert long["peak"] == 1720.6 and "sustained" in long["peak_source"]
+    assert long["frac"] == pytest.approx(1600.0 / 1720.6)
+    assert long["frac_vs_burst"] == pytest.approx(1600.0 / 1933.3)
+    assert long["frac_vs_nominal"] == pytest.approx(1600.0 / 2250.0)
+    f8 = bench.tensor_roofline(2400.0, W.NAMED["fp8"](), peaks, 2.1)
+    assert f8["peak"] == pytest.approx(2 * 1720.6) and f8["frac_vs_nominal"] == pytest.approx(2400.0 / 4500.0)
+    f4 = bench.tensor_roofline(4000.0, W.NAMED["fp4"](), peaks, 0.5)
+    assert f4["peak"] == pytest.approx(6 * 1933.3)
+
+
+def test_default_run_is_the_wide_hidden_workload_for_about_two_seconds():
+    import argparse
+    import inspect
+    src = inspect.getsource(bench.main)
+    assert 'default="wide"' in src and "default=2000" in src
+    w = W.NAMED["wide"]()
+    assert (w.num_experts, w.hidden, w.intermediate, w.accumulate, w.out_dtype) == (32, 7168, 2048, True, "bf16")
+    # ~1.06 ms per call: 2000 steps keep the clock sampler (50 ms) busy for ~40 samples
+    assert 2000 * 1.0e-3 >= 40 * bench.ClockSampler.INTERVAL_MS * 1e-3
+    del argparse
+
+
+def test_reference_steps_stay_bounded():
+    class A:
+        steps, warmup = 2000, 5
+    assert bench.reference_budget(A) * (A.steps + A.warmup) <= 130
+    A.steps, A.warmup = 2, 3
+    assert bench.reference_budget(A) == 15.0
+
+
+# ------------------------------------------------------------------------------------------
+# Expert placement under torchrun (host side; the GPU path is per rank)
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("world", [1, 2, 4, 8])
+@pytest.mark.parametrize("name", ["wide", "skewed", "balanced"])
+def test_rank_workloads_partition_every_layer_expert_once(name, world):
+    w = W.NAMED[name]()
+    parts = [bench.rank_workload(w, r, world) for r in range(world)]
+    all_counts = np.concatenate([bench.layer_counts(w, l) for l in range(world)])
+    assert sorted(np.concatenate([np.asarray(p.counts) for p in parts]).tolist()) == sorted(all_counts.tolist())
+    sums = [p.tokens_sum for p in parts]
+    assert sum(sums) == world * w.tokens_sum
+    assert max(sums) - min(sums) <= int(np.max(all_counts))
+    assert all(p.hidden == w.hidden and p.intermediate == w.intermediate and p.accumulate == w.accumulate
+               and p.out_dtype == w.out_dtype and p.input_order == w.input_order for p in parts)
+    if world == 1:
+        assert parts[0] is w
+    assert np.array_equal(bench.layer_counts(w, 0), np.asarray(w.counts))

@@ -408,7 +408,7 @@ def test_fp8_quantiser_is_in_range_and_power_of_two():
     assert np.all(mant == 0.5)                                    # powers of two
     dec = O.e4m3_to_f64(e4m3_bits(q))
     assert np.all(np.abs(dec) <= 448)
-    recon = O.apply_block_scales_rows(dec, s)
+    recon = O.apply_scales_rows(dec, s, 128)
     # e4m3 keeps 3 mantissa bits: relative error <= 2**-4 (plus subnormal floor)
     err = np.abs(recon - x.numpy().astype(np.float64))
     assert np.all(err <= 2.0 ** -4 * np.abs(x.numpy()) + np.repeat(s.T, 128, axis=1) * 2.0 ** -10)
@@ -716,3 +716,54 @@ def test_fp4_element_from_storage_matches_full():
         v, s = O.element_from_storage(x.a.numpy(), x.b.numpy(), w.offsets, 128, 256, e, m, n, fp4=True,
                                       sfa=x.sfa.numpy(), sfb=x.sfb.numpy(), b_major="k", sf_format="ue8m0_32")
         assert abs(v - full[e, m, n]) <= 1e-12 * (1 + S[e, m, n]) and abs(s - S[e, m, n]) <= 1e-12 * (1 + S[e, m, n])
+
+
+# ------------------------------------------------------------------------------------------
+# One expert at a time (the full-size parity tests compare every element this way)
+# ------------------------------------------------------------------------------------------
+
+_EXPERT_CASES = [
+    dict(),
+    dict(input_order="ragged"),
+    dict(a_major="mn"),
+    dict(b_major="k"),
+    dict(input_order="ragged", a_major="mn", b_major="k"),
+    dict(input_order="ragged", b_major="k"),
+    dict(fp8=True),
+    dict(fp8=True, sf_format="ue8m0_32", input_order="ragged"),
+    dict(fp8=True, a_major="mn", b_major="k"),
+    dict(fp4=True, b_major="k", sf_format="ue8m0_32"),
+]
+
+
+@pytest.mark.parametrize("kw", _EXPERT_CASES, ids=lambda kw: "-".join(f"{k}={v}" for k, v in kw.items()) or "bf16")
+def test_expert_from_storage_matches_whole_problem(kw):
+    """Each expert's (R_e, S_e) read straight from storage equals the whole-problem oracle's."""
+    counts = [256, 0, 512, 768]
+    w = W.custom(4, 128, 256, counts, seed=81, **kw)
+    x = W.make_inputs(w, "cpu")
+    if w.fp8 or w.fp4:
+        bits = lambda t: t.contiguous().view(torch.uint8).numpy()
+    else:
+        bits = bf16_bits
+    sf = dict(sfa=None if x.sfa is None else x.sfa.numpy(), sfb=None if x.sfb is None else x.sfb.numpy())
+    common = dict(input_order=w.input_order, fp8=w.fp8, a_major=w.a_major, b_major=w.b_major,
+                  sf_format=w.sf_format, fp4=w.fp4, **sf)
+    full, S = O.wgrad_from_storage(bits(x.a), bits(x.b), w.offsets, 128, 256, **common)
+    for e in range(4):
+        r, s = O.expert_from_storage(bits(x.a), bits(x.b), w.offsets, 128, 256, e, **common)
+        assert r.shape == (128, 256) and s.shape == (128, 256)
+        assert np.all(np.abs(r - full[e]) <= 1e-12 * S[e] + 1e-300)
+        assert np.all(np.abs(s - S[e]) <= 1e-12 * S[e] + 1e-300)
+    assert not np.any(O.expert_from_storage(bits(x.a), bits(x.b), w.offsets, 128, 256, 1, **common)[0])
+
+
+def test_expert_from_storage_catches_a_shifted_expert():
+    """Reading expert e's neighbour (an off-by-one expert index in the addressing) must differ."""
+    counts = [256, 512, 768]
+    w = W.custom(3, 128, 256, counts, seed=82, input_order="ragged")
+    x = W.make_inputs(w, "cpu")
+    full, S = O.wgrad_from_storage(bf16_bits(x.a), bf16_bits(x.b), w.offsets, 128, 256, input_order="ragged")
+    r, _ = O.expert_from_storage(bf16_bits(x.a), bf16_bits(x.b), w.offsets, 128, 256, 1, input_order="ragged")
+    assert np.all(np.abs(r - full[1]) <= 1e-12 * S[1] + 1e-300)
+    assert not np.allclose(r, full[2][:, :]) and not np.allclose(r, full[0])

@@ -153,29 +153,8 @@ def test_device_rejects_counts_breaking_the_rule(a_major, b_major, counts):
     assert torch.all(outs.buf == 7.25)
 
 
-def test_full_unaligned_sampled():
-    """The unaligned workload (balanced shape, counts multiples of 8) at full size, sampled."""
+def test_full_unaligned():
+    """The unaligned workload (balanced shape, counts multiples of 8) at full size, every element."""
     _require_maps()
-    import oracle.kgw_oracle as O
-    from kgw_testlib import bits16
-    kgw = ensure_built()
-    w = W.unaligned()
-    x_cpu = W.make_inputs(w, "cpu")
-    x = W.Inputs(x_cpu.a.to(DEV), x_cpu.b.to(DEV), x_cpu.offsets.to(DEV))
-    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
-    outs = run_gpu(w, x, DEV, status=status)
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0, kgw.kgw_status_string(int(status.item()))
-    assert outs.guards_intact()
-    a_bits, b_bits = bits16(x_cpu.a), bits16(x_cpu.b)
-    rng = np.random.default_rng(77)
-    bad = []
-    for e in range(w.num_experts):
-        for (m, n) in [(0, 0), (w.hidden - 1, w.intermediate - 1)] + [
-                (int(rng.integers(w.hidden)), int(rng.integers(w.intermediate))) for _ in range(40)]:
-            r, s = O.element_from_storage(a_bits, b_bits, w.offsets, w.hidden, w.intermediate, e, m, n)
-            got = float(outs.views[e][m, n].item())
-            tol = float(O.tolerance(np.array(s), np.array(r), w.out_dtype))
-            if not abs(got - r) <= tol:
-                bad.append((e, m, n, got, r, tol))
-    assert not bad, bad[:5]
+    from kgw_testlib import check_full
+    check_full(W.unaligned(), "unaligned")

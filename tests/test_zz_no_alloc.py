@@ -74,11 +74,3 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
         assert got_outs.guards_intact()
         _compare(w, got_outs.stacked(), want, x_cpu)
 
-
-def test_noalloc_rejects_more_experts_than_its_scratch_holds():
-    kgw = ensure_built()
-    E = 1025
-    x = torch.zeros(1, dtype=torch.int32, device=DEV)
-    args = kgw.make_args(E, 128, 256, 256, x, x, x, out=x)
-    rc = kgw.lib().kgw_wgrad_bf16_noalloc(ctypes.byref(args), None)
-    assert rc == kgw.KGW_ERR_SCRATCH_LIMIT
