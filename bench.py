@@ -19,7 +19,7 @@ five timed blocks), sampled clocks, and the float64 CPU oracle's rate on a bound
 ``--impl reference`` times the CPU oracle on the host cores instead (a bounded sample of the same
 workload per step).
 
-Other K-grouped workloads: ``--workload wide|skewed|fp8|fp4|unaligned|tiny``. The M-grouped GEMM
+Other K-grouped workloads: ``--workload balanced|skewed|fp8|fp4|unaligned|fp8_unaligned|fp4_unaligned|tiny``. The M-grouped GEMM
 (forward / dgrad of the same MoE layer, the masked decode layout, and their FP8 forms):
 ``--workload mg_forward|mg_dgrad|mg_masked|mg_fp8_forward|mg_fp8_masked|mg_tiny``, TFLOP/s
 counting 2*N*K*(valid rows).
@@ -187,14 +187,15 @@ def traffic_record(workload: str):
 
 def algorithmic_bytes(w) -> int:
     ts = w.tokens_sum
-    if w.fp4:   # e2m1 two per byte, one UE8M0 byte per 32 tokens
-        b = (w.hidden + w.intermediate) * ts // 2 + (w.hidden + w.intermediate) * (ts // 32)
+    counts = np.asarray(w.counts)
+    blocks = int(np.sum(-(-counts // 128)))   # 128-token scale blocks of all experts (ts/128 when aligned)
+    if w.fp4:   # e2m1 two per byte, one UE8M0 byte per 32 tokens (a 4-byte word per 128-token block)
+        b = (w.hidden + w.intermediate) * ts // 2 + (w.hidden + w.intermediate) * blocks * 4
     else:
         b = (w.hidden + w.intermediate) * ts * (1 if w.fp8 else 2)
     if w.fp8:
-        b += (w.hidden + w.intermediate) * (ts // 128) * 4
+        b += (w.hidden + w.intermediate) * blocks * 4
     osz = 2 if w.out_dtype == "bf16" else 4
-    counts = np.asarray(w.counts)
     nonempty = int((counts > 0).sum())
     if w.accumulate:
         b += 2 * nonempty * w.hidden * w.intermediate * osz
@@ -281,7 +282,11 @@ def run_ours(args, w, rank, local, world):
     scaled = w.fp8 or w.fp4
 
     def call(args, sfa, sfb, s):
-        if w.fp4:
+        if w.fp4 and w.unaligned:
+            kgw.kgw_wgrad_fp4_unaligned(args, sfa, sfb, ws, stream=s)
+        elif w.fp8 and w.unaligned:
+            kgw.kgw_wgrad_fp8_unaligned(args, sfa, sfb, 1 if w.sf_format == "ue8m0_32" else 0, ws, stream=s)
+        elif w.fp4:
             kgw.kgw_wgrad_fp4_ue8m0(args, sfa, sfb, ws, stream=s)
         elif w.fp8 and w.sf_format == "ue8m0_32":
             kgw.kgw_wgrad_fp8_ue8m0(args, sfa, sfb, ws, stream=s)
@@ -662,8 +667,9 @@ class OracleSampler:
         if w.fp8 or w.fp4:
             sa, blk = O.decode_scales(x.sfa.numpy(), w.sf_format)
             sb, _ = O.decode_scales(x.sfb.numpy(), w.sf_format)
-            A = O.apply_scales_rows(A, sa, blk)
-            B = O.apply_scales_cols(B, sb, blk)
+            rows = O.token_scale_rows(w.offsets, blk)
+            A = O.apply_scales_rows(A, sa, blk, rows)
+            B = O.apply_scales_cols(B, sb, blk, rows)
         self.A, self.B = A, B
         self.units = [(b, end, r0) for (b, end) in O.expert_ranges(w.offsets) if end > b
                       for r0 in range(0, w.hidden, self.ROWS)]

@@ -21,6 +21,9 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_mgrouped_workspace_size(args) -> int
   kgw_mgrouped_bf16(args, workspace, stream=None)
   kgw_mgrouped_fp8(args, sfa, sfb, sf_format, workspace, stream=None)
+  kgw_wgrad_fp8_unaligned(args, sfa, sfb, sf_format, workspace, stream=None)
+  kgw_wgrad_fp4_unaligned(args, sfa_packed, sfb_packed, workspace, stream=None)
+  kgw_debug_check_tail_maps_kind(args, kind, host_offsets, workspace) -> int
 
 ``make_args`` / ``make_mgrouped_args`` build the argument structs from torch tensors.
 """
@@ -61,7 +64,8 @@ EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
             "kgw_status_string", "kgw_version", "kgw_debug_set", "kgw_wgrad_bf16_noalloc",
             "kgw_debug_check_ragged_maps", "kgw_wgrad_fp8_ue8m0", "kgw_mgrouped_workspace_size",
             "kgw_mgrouped_bf16", "kgw_wgrad_fp4_ue8m0", "kgw_wgrad_bf16_unaligned",
-            "kgw_debug_check_tail_maps", "kgw_mgrouped_fp8")
+            "kgw_debug_check_tail_maps", "kgw_mgrouped_fp8", "kgw_wgrad_fp8_unaligned", "kgw_wgrad_fp4_unaligned",
+            "kgw_debug_check_tail_maps_kind")
 
 
 class KgwArgs(ctypes.Structure):
@@ -156,6 +160,15 @@ def lib() -> ctypes.CDLL:
         L.kgw_debug_check_tail_maps.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
                                                 ctypes.c_size_t, ctypes.c_void_p]
         L.kgw_debug_check_tail_maps.restype = ctypes.c_int32
+        L.kgw_wgrad_fp8_unaligned.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_wgrad_fp8_unaligned.restype = ctypes.c_int
+        L.kgw_wgrad_fp4_unaligned.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_wgrad_fp4_unaligned.restype = ctypes.c_int
+        L.kgw_debug_check_tail_maps_kind.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_int32, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_debug_check_tail_maps_kind.restype = ctypes.c_int32
         L.kgw_debug_set.argtypes = [ctypes.c_int32, ctypes.c_int64]
         L.kgw_debug_set.restype = ctypes.c_int64
         _lib = L
@@ -256,6 +269,30 @@ def kgw_wgrad_fp8_ue8m0(args: KgwArgs, sfa_packed, sfb_packed, workspace, worksp
     return rc
 
 
+def kgw_wgrad_fp8_unaligned(args: KgwArgs, sfa, sfb, sf_format: int, workspace,
+                            workspace_bytes: Optional[int] = None, stream=None, check: bool = True) -> int:
+    """FP8 with token counts that are multiples of 16 (any count if A and B are MN-major); scales
+    per 128-token block of each expert, sf_format 0 (FP32) or 1 (packed UE8M0 per 32 tokens)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_wgrad_fp8_unaligned(ctypes.byref(args), _ptr(sfa), _ptr(sfb), int(sf_format), _ptr(workspace),
+                                       nbytes, _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_fp8_unaligned")
+    return rc
+
+
+def kgw_wgrad_fp4_unaligned(args: KgwArgs, sfa_packed, sfb_packed, workspace, workspace_bytes: Optional[int] = None,
+                            stream=None, check: bool = True) -> int:
+    """FP4 (K-major A and B) with token counts that are multiples of 32; packed UE8M0 scales per
+    32 tokens of each expert's 128-token blocks."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_wgrad_fp4_unaligned(ctypes.byref(args), _ptr(sfa_packed), _ptr(sfb_packed), _ptr(workspace),
+                                       nbytes, _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_fp4_unaligned")
+    return rc
+
+
 def kgw_mgrouped_workspace_size(args: KgwMgroupedArgs) -> int:
     n = ctypes.c_size_t(0)
     rc = lib().kgw_mgrouped_workspace_size(ctypes.byref(args), ctypes.byref(n))
@@ -327,6 +364,17 @@ def kgw_debug_check_tail_maps(args: KgwArgs, host_offsets, workspace, workspace_
     nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
     dump = None if host_dump is None else host_dump.ctypes.data
     return int(lib().kgw_debug_check_tail_maps(ctypes.byref(args), offs.ctypes.data, _ptr(workspace), nbytes, dump))
+
+
+def kgw_debug_check_tail_maps_kind(args: KgwArgs, kind: int, host_offsets, workspace,
+                                   workspace_bytes: Optional[int] = None, host_dump=None) -> int:
+    """Testing hook: kgw_debug_check_tail_maps for BF16 (kind 0), FP8 (1) or FP4 (2) descriptors."""
+    import numpy as np
+    offs = np.ascontiguousarray(np.asarray(host_offsets, dtype=np.int32))
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    dump = None if host_dump is None else host_dump.ctypes.data
+    return int(lib().kgw_debug_check_tail_maps_kind(ctypes.byref(args), int(kind), offs.ctypes.data,
+                                                    _ptr(workspace), nbytes, dump))
 
 
 # ---------------------------------------------------------------------------------------------

@@ -155,15 +155,19 @@ struct Prepared {
   int grid;
 };
 
-// Token-count multiple of the unaligned BF16 entry: 8 when an operand stores tokens innermost
-// (TMA coordinates must start on 16 bytes), else 1.
-int64_t unaligned_count_multiple(const kgw_wgrad_args* a) {
-  return (a->a_major == KGW_K_MAJOR || a->b_major == KGW_K_MAJOR) ? 8 : 1;
+// Token-count multiple of the unaligned entries. A TMA coordinate along an operand's innermost
+// axis must start on 16 bytes, so when an operand stores tokens innermost (K-major) every
+// expert's first token must sit on a 16-byte boundary: 8 BF16 tokens, 16 e4m3 tokens, 32 packed
+// e2m1 tokens (FP4 operands are always K-major). With both operands MN-major any count works.
+int64_t unaligned_count_multiple(const kgw_wgrad_args* a, bool fp8 = false, bool fp4 = false) {
+  if (fp4) return 32;
+  if (a->a_major != KGW_K_MAJOR && a->b_major != KGW_K_MAJOR) return 1;
+  return fp8 ? 16 : 8;
 }
 
 kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws,
                    size_t ws_bytes, Prepared* P, bool fp4 = false, bool tail = false) {
-  const int64_t count_align = tail ? unaligned_count_multiple(a) : kgw::TOKEN_ALIGN;
+  const int64_t count_align = tail ? unaligned_count_multiple(a, fp8, fp4) : kgw::TOKEN_ALIGN;
   kgw_status st = validate(a, fp8, fp4, count_align);
   if (st != KGW_OK) return st;
   if (fp8 && !kgw::fp8_supported()) return KGW_ERR_UNSUPPORTED;
@@ -293,6 +297,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   pp.b = static_cast<const uint8_t*>(a->b);
   pp.esz = static_cast<int32_t>(esz);
   pp.count_align = static_cast<int32_t>(count_align);
+  pp.tok_per_unit = fp4 ? 2 : 1;
   if (tail && a->tokens_sum > 0) {
     pp.tail_a = (ragged && a_k) ? 0 : (a_k ? 1 : 2);   // ragged K-major blocks already end at n_e
     pp.tail_b = (ragged && b_k) ? 0 : (b_k ? 1 : 2);
@@ -567,6 +572,19 @@ kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
              workspace, workspace_bytes, stream, true, true);
 }
 
+kgw_status kgw_wgrad_fp8_unaligned(const kgw_wgrad_args* args, const void* sfa, const void* sfb, int32_t sf_format,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (sf_format != 0 && sf_format != 1) return KGW_ERR_INVALID_ARG;
+  return run(args, true, static_cast<const float*>(sfa), static_cast<const float*>(sfb), workspace, workspace_bytes,
+             stream, sf_format == 1, false, true);
+}
+
+kgw_status kgw_wgrad_fp4_unaligned(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  return run(args, true, reinterpret_cast<const float*>(sfa_packed), reinterpret_cast<const float*>(sfb_packed),
+             workspace, workspace_bytes, stream, true, true, true);
+}
+
 kgw_status kgw_wgrad_bf16_noalloc(const kgw_wgrad_args* args, void* stream) {
   kgw_status st = validate(args, false);
   if (st != KGW_OK) return st;
@@ -634,11 +652,14 @@ int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, 
   return mismatches;
 }
 
-int32_t kgw_debug_check_tail_maps(const kgw_wgrad_args* args, const int32_t* host_offsets, void* workspace,
-                                  size_t workspace_bytes, void* host_dump) {
-  if (!args || !host_offsets || args->tokens_sum <= 0) return -KGW_ERR_INVALID_ARG;
+int32_t kgw_debug_check_tail_maps_kind(const kgw_wgrad_args* args, int32_t kind, const int32_t* host_offsets,
+                                       void* workspace, size_t workspace_bytes, void* host_dump) {
+  if (!args || !host_offsets || args->tokens_sum <= 0 || kind < 0 || kind > 2) return -KGW_ERR_INVALID_ARG;
+  const bool fp8 = kind >= 1, fp4 = kind == 2;
   Prepared P;
-  kgw_status st = prepare(args, false, nullptr, nullptr, workspace, workspace_bytes, &P, false, true);
+  // the scale pointers are only checked for presence here (the plan kernel does not read them)
+  const float* dummy = reinterpret_cast<const float*>(args->a);
+  kgw_status st = prepare(args, fp8, dummy, dummy, workspace, workspace_bytes, &P, fp4, true);
   if (st != KGW_OK) return -static_cast<int32_t>(st);
   if (kgw::launch_plan(P.pp, P.tpl, nullptr) != cudaSuccess) return -KGW_ERR_CUDA;
   if (cudaDeviceSynchronize() != cudaSuccess) return -KGW_ERR_CUDA;
@@ -653,10 +674,14 @@ int32_t kgw_debug_check_tail_maps(const kgw_wgrad_args* args, const int32_t* hos
     std::free(dev_maps);
     return -KGW_ERR_CUDA;
   }
-  const uint64_t esz = 2, Ts = static_cast<uint64_t>(args->tokens_sum);
+  const uint64_t esz = fp8 ? 1 : 2;
+  const uint64_t tpu = fp4 ? 2 : 1;                       // tokens per element of the token axis
+  const uint64_t Ts = static_cast<uint64_t>(args->tokens_sum);
   const uint64_t H = static_cast<uint64_t>(args->hidden), I = static_cast<uint64_t>(args->intermediate);
   const uint32_t b_rows_cta = static_cast<uint32_t>(kgw::BN / (P.pp.tile_m / kgw::BM));
-  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t box_k = fp4 ? 128u : static_cast<uint32_t>(bk_of(fp8));   // token-axis box (elements)
+  const uint32_t atom = static_cast<uint32_t>(128 / esz);
   int32_t mismatches = 0;
   for (int32_t op = 0; op < 2; ++op) {
     const int mode = op == 0 ? P.pp.tail_a : P.pp.tail_b;
@@ -672,11 +697,10 @@ int32_t kgw_debug_check_tail_maps(const kgw_wgrad_args* args, const int32_t* hos
       const uint64_t n = static_cast<uint64_t>(end - begin);
       CUtensorMap ref;
       std::memset(&ref, 0, sizeof(ref));
-      kgw_status r = block       ? encode_2d(&ref, dt, base + begin * rows * esz, n, rows, n * esz, kgw::BK_BF16, box_rows)
-                     : mode == 1 ? encode_2d(&ref, dt, base, static_cast<uint64_t>(end), rows, Ts * esz, kgw::BK_BF16,
-                                             box_rows)
-                                 : encode_2d(&ref, dt, base, rows, static_cast<uint64_t>(end), rows * esz, 64,
-                                             kgw::BK_BF16);
+      kgw_status r = block ? encode_2d(&ref, dt, base + begin * rows * esz, n, rows, n * esz, box_k, box_rows)
+                     : mode == 1 ? encode_2d(&ref, dt, base, static_cast<uint64_t>(end) / tpu, rows, Ts / tpu * esz,
+                                             box_k, box_rows)
+                                 : encode_2d(&ref, dt, base, rows, static_cast<uint64_t>(end), rows * esz, atom, box_k);
       if (r != KGW_OK) {
         std::free(dev_maps);
         return -KGW_ERR_CUDA;
@@ -692,6 +716,11 @@ int32_t kgw_debug_check_tail_maps(const kgw_wgrad_args* args, const int32_t* hos
   }
   std::free(dev_maps);
   return mismatches;
+}
+
+int32_t kgw_debug_check_tail_maps(const kgw_wgrad_args* args, const int32_t* host_offsets, void* workspace,
+                                  size_t workspace_bytes, void* host_dump) {
+  return kgw_debug_check_tail_maps_kind(args, 0, host_offsets, workspace, workspace_bytes, host_dump);
 }
 
 kgw_status kgw_mgrouped_workspace_size(const kgw_mgrouped_args* args, size_t* bytes) {

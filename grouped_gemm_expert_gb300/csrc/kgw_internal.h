@@ -86,12 +86,14 @@ struct PlanHeader {
 static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte block");
 
 // Workspace layout (all offsets 256-byte aligned):
-//   [PlanHeader][order E][item_prefix E+1][splits E][slot_base E][counter_base E]
+//   [PlanHeader][order E][item_prefix E+1][splits E][slot_base E][counter_base E][scale_row E]
 //   [per-expert TMA descriptors of ragged K-major A, then of ragged K-major B: 128 B each, 2E]
 //   [arrival counters 4*max_slots (one per split tile and TMEM lane quadrant)]
 //   [partials max_slots * PARTIAL_TILE_BYTES]
+// scale_row[e]: first scale row of expert e in the block-scaled entries, the sum over f < e of
+// ceil(n_f / 128) (each expert's 128-token scale blocks start at its first token).
 struct WsLayout {
-  size_t order, item_prefix, splits, slot_base, counter_base, tmaps, tmaps_b, counters, partials, total;
+  size_t order, item_prefix, splits, slot_base, counter_base, scale_row, tmaps, tmaps_b, counters, partials, total;
   int32_t max_slots;
 };
 
@@ -106,6 +108,7 @@ inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1) {
   L.splits = off;       off = align256(off + sizeof(int32_t) * E);
   L.slot_base = off;    off = align256(off + sizeof(int32_t) * E);
   L.counter_base = off; off = align256(off + sizeof(int32_t) * E);
+  L.scale_row = off;    off = align256(off + sizeof(int32_t) * E);
   L.tmaps = off;        off = align256(off + size_t(128) * E);
   L.tmaps_b = off;      off = align256(off + size_t(128) * E);
   L.counters = off;     off = align256(off + sizeof(int32_t) * EPI_COUNTERS * halves * (max_slots > 0 ? max_slots : 1));
@@ -126,7 +129,7 @@ inline WsLayout ws_layout_mg(int64_t max_tiles) {
   L.order = sizeof(PlanHeader);
   L.item_prefix = align256(L.order + sizeof(int32_t) * 4 * n);
   L.total = align256(L.item_prefix + sizeof(int32_t) * 2 * n);
-  L.splits = L.slot_base = L.counter_base = L.tmaps = L.tmaps_b = L.counters = L.partials = L.total;
+  L.splits = L.slot_base = L.counter_base = L.scale_row = L.tmaps = L.tmaps_b = L.counters = L.partials = L.total;
   L.max_slots = 0;
   return L;
 }
@@ -158,6 +161,7 @@ struct PlanParams {
   // are the operand's own descriptor (small: for dimension-1 extents x row stride < 128 KiB)
   int32_t tail_a, tail_b;
   uint64_t row_bytes_a, row_bytes_b;   // row strides of MN-major operands (size class of tails)
+  int32_t tok_per_unit;         // tokens per element of a descriptor's token axis (2: packed FP4 bytes)
 };
 
 // Host-encoded templates of the per-expert descriptors (ragged, K-major operands: one per size

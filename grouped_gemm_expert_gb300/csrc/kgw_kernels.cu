@@ -170,8 +170,8 @@ __global__ void __launch_bounds__(PLAN_THREADS)
         const uint4* src = reinterpret_cast<const uint4*>(t);
 #pragma unroll
         for (int j = 0; j < 8; ++j) dst[j] = src[j];
-        if (mode == 1)
-          tmap_set_dim0(dst, static_cast<uint32_t>(end));
+        if (mode == 1)  // (packed FP4: the token axis of the descriptor counts bytes, two tokens each)
+          tmap_set_dim0(dst, static_cast<uint32_t>(p.tok_per_unit > 1 ? end / p.tok_per_unit : end));
         else
           tmap_set_dim1(dst, static_cast<uint32_t>(end));
         fence_tmap_release();
@@ -186,6 +186,24 @@ __global__ void __launch_bounds__(PLAN_THREADS)
   int64_t ksum;
   block_exclusive_scan(mysum, s_warp, &ksum);
   const int64_t W = ksum * T;
+
+  // 2b. first scale row of every expert (block-scaled entries): each expert's tokens form
+  //     ceil(n_e / 128) scale blocks starting at its first token, numbered in expert order
+  {
+    int32_t* scale_row = reinterpret_cast<int32_t*>(p.ws + p.L.scale_row);
+    auto blocks = [&](int e) {
+      const int64_t prev = e ? static_cast<int64_t>(p.offsets[e - 1]) : 0;
+      return (static_cast<int64_t>(p.offsets[e]) - prev + SCALE_BLOCK - 1) / SCALE_BLOCK;
+    };
+    int64_t mine = 0;
+    for (int e = ch.lo; e < ch.hi; ++e) mine += blocks(e);
+    int64_t nblk;
+    int64_t run = block_exclusive_scan(mine, s_warp, &nblk);
+    for (int e = ch.lo; e < ch.hi; ++e) {
+      scale_row[e] = static_cast<int32_t>(run);
+      run += blocks(e);
+    }
+  }
 
   // 3. split-K chunk: items no longer than W/(2*grid) k-iterations (at least MIN_SPLIT_KITERS),
   //    doubled until the partial tiles fit in the workspace.
@@ -428,6 +446,7 @@ struct alignas(16) Item {
   int split, nsplit, tile;
   int rows;              // valid rows of the tile (M-grouped masked layout: may be < 128)
   int m1, rows1;         // M-grouped CTA pair: first row and valid rows of the second CTA's half
+  int srow;              // block-scaled: scale row of the expert's first 128-token block
   int64_t begin;         // expert's first token
   int64_t n_e;           // expert's token count
 };
@@ -452,6 +471,7 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
     it.tile = idx;
     it.kbeg = 0;
     it.kend = p.K / bk;
+    it.srow = 0;
     it.begin = 0;
     it.n_e = 0;
     return it;
@@ -479,6 +499,7 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
   it.n0 = nt * BN;
   it.begin = it.e ? static_cast<int64_t>(__ldg(p.offsets + it.e - 1)) : 0;
   it.n_e = static_cast<int64_t>(__ldg(p.offsets + it.e)) - it.begin;
+  it.srow = __ldg(reinterpret_cast<const int32_t*>(p.ws + p.L.scale_row) + it.e);
   const int64_t kit = (it.n_e + bk - 1) / bk;  // a partial last stage counts (zero-filled tail)
   it.kbeg = static_cast<int>(it.split * kit / it.nsplit);
   it.kend = static_cast<int>((it.split + 1) * kit / it.nsplit);
@@ -774,18 +795,22 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           // work is done by the time the MMA has its operands
           if constexpr (kFp4) {
             // the two 128-token scale words of this 256-token stage: [A word 0][A word 1]
-            // [B word 0][B word 1], on the stage's scale barrier
-            const int64_t kblk = tok / SCALE_BLOCK;
+            // [B word 0][B word 1], on the stage's scale barrier. Scale blocks are the expert's own
+            // (rows from it.srow on); when its last stage holds a single block, word 1 repeats
+            // word 0 (the stage's second half is zero-filled, and no row past the tensor is read).
+            const int64_t kblk = int64_t(it.srow) + 2 * int64_t(kb);
+            const int64_t kblk1 = (2 * int64_t(kb) + 1) * SCALE_BLOCK < it.n_e ? kblk + 1 : kblk;
             uint8_t* sS = sB + kStageB;
             mbar_arrive_expect_tx(&ctl->sfdata[stage], SF_SMEM_BYTES_FP4);
             bulk_load(sS, p.sfa + kblk * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
-            bulk_load(sS + BM * 4, p.sfa + (kblk + 1) * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
+            bulk_load(sS + BM * 4, p.sfa + kblk1 * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
             bulk_load(sS + 2 * BM * 4, p.sfb + kblk * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
-            bulk_load(sS + 2 * BM * 4 + BN * 4, p.sfb + (kblk + 1) * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
+            bulk_load(sS + 2 * BM * 4 + BN * 4, p.sfb + kblk1 * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
           } else if constexpr (kFp8) {
             // this 128-token block's FP32 scales: the tile's 128 rows of A and 256 columns of B;
-            // they complete on the stage's scale barrier
-            const int64_t kblk = tok / SCALE_BLOCK;
+            // they complete on the stage's scale barrier. K-grouped: the expert's block kb
+            // (scale rows from it.srow on); M-grouped: block kb of the fixed K axis.
+            const int64_t kblk = kMG ? tok / SCALE_BLOCK : int64_t(it.srow) + kb;
             uint8_t* sS = sB + kStageB;
             // (M-grouped: A's scales are [K/128, rows], the group's weight scales [G, K/128, N])
             const int64_t bblk = kMG ? int64_t(it.e) * (p.K / SCALE_BLOCK) + kblk : kblk;

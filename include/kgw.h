@@ -171,6 +171,38 @@ kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Block-scaled entries without the 256-token contract on the counts (an extension beyond the
+ * pages' contract, like kgw_wgrad_bf16_unaligned). An expert's last pipeline stage may be partly
+ * beyond its last token: it is read through a per-expert TMA descriptor whose token extent ends at
+ * end_e, so the rest of the stage is zero and the next expert's tokens are not read.
+ *
+ * Scale blocks. "05 · Grouped GEMM 与 Expert 计算", section 4 (quantization padding) pads every
+ * expert segment to the quantisation alignment before the FP8/FP4 cast, so every scale block lies
+ * inside one expert. Here the operands are not padded but the scales keep that layout: expert e's
+ * tokens are cut into 128-token blocks from its first token (the last one possibly partial), and
+ * its blocks are scale rows r_e, r_e + 1, ..., r_e + ceil(n_e/128) - 1, with
+ * r_e = sum over f < e of ceil(n_f / 128). sfa has sum_e ceil(n_e/128) rows of hidden entries,
+ * sfb as many rows of intermediate entries. When every count is a multiple of 128 these are the
+ * rows tokens/128 of the aligned entries (kgw_wgrad_fp8_blockscaled, kgw_wgrad_fp8_ue8m0,
+ * kgw_wgrad_fp4_ue8m0), which follow the same rule.
+ *
+ * kgw_wgrad_fp8_unaligned: e4m3 operands in any storage order and input order of kgw_wgrad_bf16.
+ * sf_format 0: FP32 powers of two, one per 128-token block (as kgw_wgrad_fp8_blockscaled);
+ * sf_format 1: packed UE8M0 words, byte j scaling tokens 32j..32j+31 of the block (as
+ * kgw_wgrad_fp8_ue8m0); any other value is KGW_ERR_INVALID_ARG. Counts (and tokens_sum) must be
+ * multiples of 16 when A or B is K-major (a TMA coordinate along the innermost axis starts on 16
+ * bytes), any count when both are MN-major.
+ * kgw_wgrad_fp4_unaligned: e2m1 operands as in kgw_wgrad_fp4_ue8m0 (K-major A and B, tensor2d);
+ * counts multiples of 32 (16 packed bytes).
+ * A count that breaks the rule is KGW_ERR_OFFSETS on the device (nothing written). Workspace:
+ * kgw_workspace_size with is_fp8 = 1. Everything else as for the aligned entries.
+ */
+kgw_status kgw_wgrad_fp8_unaligned(const kgw_wgrad_args* args, const void* sfa, const void* sfb, int32_t sf_format,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+kgw_status kgw_wgrad_fp4_unaligned(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * kgw_wgrad_bf16 without a workspace argument and without any device allocation.
  *
  * The paper has no counterpart to this entry point. It exists for callers that cannot allocate
@@ -313,6 +345,12 @@ int32_t kgw_debug_check_ragged_maps(const kgw_wgrad_args* args, int32_t is_fp8, 
  * kgw_debug_check_ragged_maps. */
 int32_t kgw_debug_check_tail_maps(const kgw_wgrad_args* args, const int32_t* host_offsets, void* workspace,
                                   size_t workspace_bytes, void* host_dump);
+
+/* Testing hook: kgw_debug_check_tail_maps for the descriptors of kgw_wgrad_bf16_unaligned (kind 0),
+ * kgw_wgrad_fp8_unaligned (kind 1) or kgw_wgrad_fp4_unaligned (kind 2; the token axis of a packed
+ * FP4 descriptor counts bytes). Other kinds: -KGW_ERR_INVALID_ARG. */
+int32_t kgw_debug_check_tail_maps_kind(const kgw_wgrad_args* args, int32_t kind, const int32_t* host_offsets,
+                                       void* workspace, size_t workspace_bytes, void* host_dump);
 
 #ifdef __cplusplus
 }

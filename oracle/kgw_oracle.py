@@ -24,7 +24,9 @@ scale per block of 128 consecutive tokens ("05 · Grouped GEMM 与 Expert 计算
 section 3: per-block 1x128 scaling, scales stored MN-major). The FP4 variant
 does the same with e2m1 elements (two per byte along the token axis, first
 token in the low nibble) and one UE8M0 scale per 32 tokens ("How to Use K-Grouped
-GEMM ...", steps 1-2: FP4 casts with gran_k = 32 for both operands).
+GEMM ...", steps 1-2: FP4 casts with gran_k = 32 for both operands). Token
+blocks start at each expert's first token (``token_scale_rows``); with the
+pages' counts (multiples of 256) they are the global blocks k // 128.
 
 Every product here is exact in float64 only up to rounding of the float64
 sums; the tests pin it against exact rational brute force, so "the oracle"
@@ -186,14 +188,42 @@ def unpack_ue8m0_32(packed) -> np.ndarray:
     return out
 
 
-def apply_scales_rows(x: np.ndarray, scales: np.ndarray, block: int) -> np.ndarray:
-    """x [rows, tokens] * s[k // block, m] for scales [tokens/block, rows]."""
-    return x * np.repeat(np.asarray(scales, dtype=np.float64).T, block, axis=1)
+def token_scale_rows(offsets, block: int) -> np.ndarray:
+    """Scale row of every token: int64 [tokens_sum].
+
+    Each expert's tokens are cut into blocks of 128 from its own first token, the last block
+    possibly partial (the pages pad every expert to the quantisation alignment before FP8/FP4
+    casts, "05 · Grouped GEMM 与 Expert 计算", section 4: quantization padding of each expert
+    segment); expert e's 128-token blocks take scale rows sb_e, sb_e + 1, ... with
+    sb_e = sum over f < e of ceil(n_f / 128). A scale of ``block`` (128, or 32 for UE8M0
+    sub-blocks) tokens is row sb_e * (128 / block) + (k - begin_e) // block. When every count is a
+    multiple of 128 this is k // block: the global blocks of the aligned contract.
+    """
+    per = SCALE_BLOCK // block
+    rows = []
+    sb = 0
+    for (b, end) in expert_ranges(offsets):
+        n = end - b
+        rows.append(sb * per + np.arange(n, dtype=np.int64) // block)
+        sb += (n + SCALE_BLOCK - 1) // SCALE_BLOCK
+    return np.concatenate(rows) if rows else np.zeros(0, dtype=np.int64)
 
 
-def apply_scales_cols(x: np.ndarray, scales: np.ndarray, block: int) -> np.ndarray:
-    """x [tokens, cols] * s[k // block, n] for scales [tokens/block, cols]."""
-    return x * np.repeat(np.asarray(scales, dtype=np.float64), block, axis=0)
+def apply_scales_rows(x: np.ndarray, scales: np.ndarray, block: int, rows=None) -> np.ndarray:
+    """x [rows, tokens] * s[r(k), m] for scales [blocks, rows]; r(k) = k // block, or the given
+    per-token scale rows (``token_scale_rows``)."""
+    s = np.asarray(scales, dtype=np.float64)
+    if rows is None:
+        return x * np.repeat(s.T, block, axis=1)
+    return x * s[np.asarray(rows), :].T
+
+
+def apply_scales_cols(x: np.ndarray, scales: np.ndarray, block: int, rows=None) -> np.ndarray:
+    """x [tokens, cols] * s[r(k), n] for scales [blocks, cols]; r(k) as in ``apply_scales_rows``."""
+    s = np.asarray(scales, dtype=np.float64)
+    if rows is None:
+        return x * np.repeat(s, block, axis=0)
+    return x * s[np.asarray(rows), :]
 
 
 def decode_scales(sf, sf_format: str):
@@ -255,8 +285,9 @@ def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, 
     if fp8:
         sa, blk = decode_scales(sfa, sf_format)
         sb, _ = decode_scales(sfb, sf_format)
-        A = apply_scales_rows(A, sa, blk)
-        B = apply_scales_cols(B, sb, blk)
+        rows = token_scale_rows(offsets, blk)
+        A = apply_scales_rows(A, sa, blk, rows)
+        B = apply_scales_cols(B, sb, blk, rows)
     return wgrad(A, B, offsets, c_init=c_init, accumulate=accumulate, with_bound=with_bound)
 
 
@@ -318,7 +349,7 @@ def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int
         bcol = e2m1_to_f64(fb[sb0 // 2:(sb0 + cnt) // 2])
         sa, blk = decode_scales(sfa, sf_format)
         sb, _ = decode_scales(sfb, sf_format)
-        ks = np.arange(b, end) // blk
+        ks = token_scale_rows(offsets, blk)[b:end]
         arow = arow * sa[ks, m]
         bcol = bcol * sb[ks, n]
         return float(np.dot(arow, bcol)), float(np.dot(np.abs(arow), np.abs(bcol)))
@@ -340,7 +371,7 @@ def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int
     if fp8:
         sa, blk = decode_scales(sfa, sf_format)
         sb, _ = decode_scales(sfb, sf_format)
-        ks = np.arange(b, end) // blk
+        ks = token_scale_rows(offsets, blk)[b:end]
         arow = arow * sa[ks, m]
         bcol = bcol * sb[ks, n]
     return float(np.dot(arow, bcol)), float(np.dot(np.abs(arow), np.abs(bcol)))
@@ -390,7 +421,7 @@ def expert_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int,
     if fp8 or fp4:
         sa, blk = decode_scales(sfa, sf_format)
         sb, _ = decode_scales(sfb, sf_format)
-        ks = np.arange(b, end) // blk
+        ks = token_scale_rows(offsets, blk)[b:end]
         Ae = Ae * sa[ks, :].T
         Be = Be * sb[ks, :]
     return Ae @ Be, np.abs(Ae) @ np.abs(Be)

@@ -88,7 +88,11 @@ def run_gpu(w, x, device="cuda", status=None, workspace=None, outputs=None):
                          status_dev=status)
     if workspace is None:
         workspace = kgw.workspace_for(args, w.fp8 or w.fp4, device=device)
-    if w.fp4:
+    if w.fp4 and w.unaligned:
+        kgw.kgw_wgrad_fp4_unaligned(args, x.sfa, x.sfb, workspace)
+    elif w.fp8 and w.unaligned:
+        kgw.kgw_wgrad_fp8_unaligned(args, x.sfa, x.sfb, 1 if w.sf_format == "ue8m0_32" else 0, workspace)
+    elif w.fp4:
         kgw.kgw_wgrad_fp4_ue8m0(args, x.sfa, x.sfb, workspace)
     elif w.fp8 and w.sf_format == "ue8m0_32":
         kgw.kgw_wgrad_fp8_ue8m0(args, x.sfa, x.sfb, workspace)

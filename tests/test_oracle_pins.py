@@ -767,3 +767,93 @@ def test_expert_from_storage_catches_a_shifted_expert():
     r, _ = O.expert_from_storage(bf16_bits(x.a), bf16_bits(x.b), w.offsets, 128, 256, 1, input_order="ragged")
     assert np.all(np.abs(r - full[1]) <= 1e-12 * S[1] + 1e-300)
     assert not np.allclose(r, full[2][:, :]) and not np.allclose(r, full[0])
+
+
+# ------------------------------------------------------------------------------------------
+# Scale blocks per expert (counts that are not multiples of 128): each expert's 128-token blocks
+# start at its first token ("05 · Grouped GEMM 与 Expert 计算", section 4: every expert segment is
+# padded to the quantisation alignment before the FP8/FP4 cast)
+# ------------------------------------------------------------------------------------------
+
+def test_token_scale_rows_by_hand():
+    rows = O.token_scale_rows([40, 40, 240], 128)            # counts 40, 0, 200
+    assert rows.tolist() == [0] * 40 + [1] * 128 + [2] * 72
+    rows32 = O.token_scale_rows([40, 40, 240], 32)
+    assert rows32.tolist() == [0] * 32 + [1] * 8 + sum(([4 + j] * 32 for j in range(6)), []) + [10] * 8
+    # multiples of 128: the global blocks k // block
+    offs = np.cumsum([256, 0, 384, 128])
+    for blk in (32, 128):
+        assert np.array_equal(O.token_scale_rows(offs, blk), np.arange(768) // blk)
+
+
+def _fp8_brute(codes_a, codes_b, sa, sb, counts):
+    """Exact sum over each expert's tokens of dec(a)*sa[block]*dec(b)*sb[block], with blocks counted
+    from each expert's first token (written out with explicit loops, independently of the oracle)."""
+    table = {c: Fraction(float(v)) for c, v in enumerate(O.e4m3_to_f64(np.arange(256, dtype=np.uint8)))
+             if np.isfinite(v)}
+    H, I = codes_a.shape[0], codes_b.shape[1]
+    out, b, sblk = [], 0, 0
+    for n in counts:
+        res = [[Fraction(0)] * I for _ in range(H)]
+        for j in range(n):
+            k, blk = b + j, sblk + j // 128
+            for m in range(H):
+                fa = table[int(codes_a[m, k])] * Fraction(float(sa[blk, m]))
+                for c in range(I):
+                    res[m][c] += fa * table[int(codes_b[k, c])] * Fraction(float(sb[blk, c]))
+        out.append(res)
+        b += n
+        sblk += -(-n // 128)
+    return out
+
+
+def test_fp8_per_expert_blocks_brute_force():
+    rng = np.random.default_rng(41)
+    counts = [48, 0, 176, 16]                                  # multiples of 16, not of 128
+    T, H, I = sum(counts), 3, 4
+    nblk = sum(-(-n // 128) for n in counts)                   # 1 + 0 + 2 + 1
+    codes_a = rng.integers(0, 126, size=(H, T)).astype(np.uint8)   # finite codes only
+    codes_b = rng.integers(0, 126, size=(T, I)).astype(np.uint8)
+    sa = np.ldexp(1.0, rng.integers(-6, 7, size=(nblk, H))).astype(np.float32)
+    sb = np.ldexp(1.0, rng.integers(-6, 7, size=(nblk, I))).astype(np.float32)
+    offs = np.cumsum(counts).astype(np.int32)
+    got, S = O.wgrad_from_storage(codes_a, codes_b, offs, H, I, fp8=True, sfa=sa, sfb=sb)
+    exact = _fp8_brute(codes_a, codes_b, sa, sb, counts)
+    for e in range(len(counts)):
+        for m in range(H):
+            for n in range(I):
+                assert abs(Fraction(got[e, m, n]) - exact[e][m][n]) <= Fraction(1e-12) * Fraction(S[e, m, n]) + Fraction(1e-300)
+    # the same numbers through the one-expert and one-element readers
+    for e in range(len(counts)):
+        r, _ = O.expert_from_storage(codes_a, codes_b, offs, H, I, e, fp8=True, sfa=sa, sfb=sb)
+        assert np.all(np.abs(r - got[e]) <= 1e-12 * S[e] + 1e-300)
+        v, _ = O.element_from_storage(codes_a, codes_b, offs, H, I, e, H - 1, I - 1, fp8=True, sfa=sa, sfb=sb)
+        assert abs(v - got[e, H - 1, I - 1]) <= 1e-12 * S[e, H - 1, I - 1] + 1e-300
+
+
+@pytest.mark.parametrize("kind", ["fp8", "fp8_ue8m0", "fp4"])
+def test_per_expert_quantisation_roundtrip_needs_per_expert_scale_rows(kind):
+    """Decoding the quantised operands with the oracle's per-expert scale rows gives back the
+    drawn values within the element format's precision; reading the scales at global rows
+    k // 128 instead (a plausible indexing mistake) does not."""
+    counts = [48, 0, 176, 96] if kind != "fp4" else [64, 0, 160, 96]
+    kw = dict(fp8=True) if kind == "fp8" else (dict(fp8=True, sf_format="ue8m0_32") if kind == "fp8_ue8m0" else
+                                                dict(fp4=True, b_major="k", sf_format="ue8m0_32"))
+    w = W.custom(4, 128, 256, counts, seed=42, unaligned=True, **kw)
+    x = W.make_inputs(w, "cpu")
+    g = torch.Generator().manual_seed(42)
+    a32 = torch.randn(128, w.tokens_sum, generator=g).double().numpy()
+    dec = O.e2m1_to_f64 if w.fp4 else O.e4m3_to_f64
+    bits = x.a.contiguous().view(torch.uint8).numpy()
+    a = dec(bits).reshape(128, w.tokens_sum)
+    sa, blk = O.decode_scales(x.sfa.numpy(), w.sf_format)
+    good = O.apply_scales_rows(a, sa, blk, O.token_scale_rows(w.offsets, blk))
+    # half a unit in the last place of the element format, relative, plus half its smallest step
+    # (e2m1: 0.5; e4m3: 2**-9) times the element's scale for values that round towards zero
+    rel, step = (2.0 ** -2, 0.5) if w.fp4 else (2.0 ** -4, 2.0 ** -9)
+    rows = O.token_scale_rows(w.offsets, blk)
+    floor = 0.5 * step * O.apply_scales_rows(np.ones_like(a), sa, blk, rows)
+    assert np.all(np.abs(good - a32) <= rel * np.abs(a32) + floor)
+    rows_global = np.minimum(np.arange(w.tokens_sum) // blk, sa.shape[0] - 1)
+    bad = O.apply_scales_rows(a, sa, blk, rows_global)
+    assert not np.all(np.abs(bad - a32) <= rel * np.abs(a32) + floor)

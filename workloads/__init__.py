@@ -159,8 +159,32 @@ def fp4() -> Workload:
                     out_dtype="bf16", fp4=True, b_major="k", sf_format="ue8m0_32")
 
 
+def round_to(x: np.ndarray, m: int) -> np.ndarray:
+    """Nearest multiple of m: m * floor(x / m + 0.5)."""
+    return (m * np.floor(np.asarray(x, dtype=np.float64) / m + 0.5)).astype(np.int64)
+
+
+def fp8_unaligned() -> Workload:
+    """The FP8 workload's shape with counts rounded to 16 tokens (same seed and spread)."""
+    rng = np.random.default_rng(3)
+    counts = round_to(4096 * rng.uniform(0.7, 1.3, size=16), 16)
+    return Workload("FP8 unaligned counts: E=16 hidden=4096 intermediate=1536, counts multiples of 16, "
+                    "per-expert 128-token scale blocks, BF16 dense overwrite", 16, 4096, 1536, counts, seed=11,
+                    out_dtype="bf16", fp8=True, unaligned=True)
+
+
+def fp4_unaligned() -> Workload:
+    """The FP4 workload's shape with counts rounded to 32 tokens (same seed and spread)."""
+    rng = np.random.default_rng(3)
+    counts = round_to(4096 * rng.uniform(0.7, 1.3, size=16), 32)
+    return Workload("FP4 unaligned counts: E=16 hidden=4096 intermediate=1536, counts multiples of 32, "
+                    "e2m1 with UE8M0 per 32 tokens of each expert's 128-token blocks, BF16 dense overwrite",
+                    16, 4096, 1536, counts, seed=12, out_dtype="bf16", fp4=True, b_major="k",
+                    sf_format="ue8m0_32", unaligned=True)
+
+
 NAMED = {"tiny": tiny, "balanced": balanced, "wide": wide, "fp8": fp8, "skewed": skewed, "fp4": fp4,
-         "unaligned": unaligned}
+         "unaligned": unaligned, "fp8_unaligned": fp8_unaligned, "fp4_unaligned": fp4_unaligned}
 
 
 def custom(num_experts: int, hidden: int, intermediate: int, counts, seed: int, **kw) -> Workload:
@@ -185,7 +209,8 @@ class Inputs:
     With a_major "mn" A is stored [tokens_sum, hidden] (expert blocks [n_e, hidden] back to back
     in both orders); with b_major "k" B is stored [intermediate, tokens_sum] (tensor2d) or as
     per-expert [intermediate, n_e] blocks (ragged).
-    sfa/sfb (FP8 only): float32 [tokens_sum/128, hidden] / [tokens_sum/128, intermediate], or with
+    sfa/sfb (FP8/FP4): float32 [blocks, hidden] / [blocks, intermediate] with one row per 128-token
+       block of each expert (tokens_sum/128 rows when every count is a multiple of 128), or with
        sf_format "ue8m0_32" int32 packed UE8M0 words of the same shapes.
     c: pre-filled output [E, hidden, intermediate] for accumulate mode, else None.
     """
@@ -313,6 +338,43 @@ def quantize_e2m1_ue8m0_32(x: torch.Tensor, token_axis: int):
     return packed, torch.from_numpy(words.view(np.int32).T.copy())
 
 
+def expert_padded_columns(counts):
+    """(cols, width): the column of every token in the layout where each expert's block starts on a
+    multiple of 128 (each expert padded to whole 128-token blocks, as the pages' quantization
+    padding does before FP8/FP4 casts), and that layout's width (sum of ceil(n_e/128)*128)."""
+    cols, start = [], 0
+    for n in np.asarray(counts, dtype=np.int64).tolist():
+        cols.append(start + np.arange(n, dtype=np.int64))
+        start += -(-n // FP8_BLOCK) * FP8_BLOCK
+    return (np.concatenate(cols) if cols else np.zeros(0, dtype=np.int64)), start
+
+
+def quantize_per_expert(quantize, x: torch.Tensor, token_axis: int, counts, packed_fp4: bool = False):
+    """Apply a block quantiser with each expert's tokens padded to whole 128-token blocks.
+
+    The scales come out one row per 128-token block of each expert ([sum ceil(n_e/128), other]);
+    the quantised operand keeps the unpadded token layout (padding zeros never change a block's
+    amax). With counts that are multiples of 128 this is ``quantize`` itself. ``packed_fp4``:
+    ``quantize`` returns e2m1 bytes [other, tokens/2] (counts must then be even).
+    """
+    counts = np.asarray(counts, dtype=np.int64)
+    if np.all(counts % FP8_BLOCK == 0):
+        return quantize(x, token_axis)
+    cols, width = expert_padded_columns(counts)
+    idx = torch.from_numpy(cols)
+    if token_axis == 1:
+        xp = x.new_zeros((x.shape[0], width))
+        xp[:, idx] = x
+    else:
+        xp = x.new_zeros((width, x.shape[1]))
+        xp[idx, :] = x
+    q, sf = quantize(xp, token_axis)
+    if packed_fp4:
+        assert np.all(counts % 2 == 0)
+        return q[:, torch.from_numpy(cols[0::2] // 2)].contiguous(), sf
+    return (q[:, idx] if token_axis == 1 else q[idx, :]).contiguous(), sf
+
+
 def pack_ragged_a(a2d: torch.Tensor, counts) -> torch.Tensor:
     """Re-store a logical [hidden, tokens_sum] A as per-expert K-contiguous blocks.
 
@@ -358,19 +420,19 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
     sfa = sfb = None
     if w.fp4:
         assert w.a_major == "k" and w.b_major == "k" and w.input_order == "tensor2d"
-        a_store, sfa = quantize_e2m1_ue8m0_32(a32, token_axis=1)     # [H, T/2]
-        b_store, sfb = quantize_e2m1_ue8m0_32(b32, token_axis=0)     # [I, T/2] (K-major)
+        a_store, sfa = quantize_per_expert(quantize_e2m1_ue8m0_32, a32, 1, w.counts, packed_fp4=True)  # [H, T/2]
+        b_store, sfb = quantize_per_expert(quantize_e2m1_ue8m0_32, b32, 0, w.counts, packed_fp4=True)  # [I, T/2]
         del a32, b32
         c = _normal(gen, (E, H, I), w.c_std).to(out_torch_dtype(w.out_dtype)) if w.accumulate else None
         offsets = torch.from_numpy(w.offsets.astype(np.int32))
         to = lambda t: None if t is None else t.to(device)
         return Inputs(to(a_store), to(b_store), to(offsets), to(sfa), to(sfb), to(c))
     if w.fp8 and w.sf_format == "ue8m0_32":
-        a_store, sfa = quantize_e4m3_ue8m0_32(a32, token_axis=1)
-        b_store, sfb = quantize_e4m3_ue8m0_32(b32, token_axis=0)
+        a_store, sfa = quantize_per_expert(quantize_e4m3_ue8m0_32, a32, 1, w.counts)
+        b_store, sfb = quantize_per_expert(quantize_e4m3_ue8m0_32, b32, 0, w.counts)
     elif w.fp8:
-        a_store, sfa = quantize_e4m3_blocks(a32, token_axis=1)
-        b_store, sfb = quantize_e4m3_blocks(b32, token_axis=0)
+        a_store, sfa = quantize_per_expert(quantize_e4m3_blocks, a32, 1, w.counts)
+        b_store, sfb = quantize_per_expert(quantize_e4m3_blocks, b32, 0, w.counts)
     else:
         a_store = a32.to(torch.bfloat16)
         b_store = b32.to(torch.bfloat16)
