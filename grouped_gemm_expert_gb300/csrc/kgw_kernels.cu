@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "kgw_internal.h"
 #include "kgw_ptx.cuh"
@@ -1190,9 +1191,6 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       }
       const int acc = kFp8 ? 0 : (tcount & 1);
       const uint32_t use = kFp8 ? static_cast<uint32_t>(tcount) : static_cast<uint32_t>(tcount >> 1);
-      const bool okt = wait_bounded_t<kPair>(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
-      if (!__all_sync(0xffffffffu, okt)) break;
-      tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       // This warp has read its 32 TMEM lanes: hand the accumulator back to the MMA issuer.
       auto release_acc = [&]() {
@@ -1206,6 +1204,82 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         }
       };
       uint4* stg = reinterpret_cast<uint4*>(epi_stage_mem + (warp - EPI_WARP0) * EPI_STAGE_BYTES);
+      // M-grouped masked layout: rows at or past the group's valid count are not touched
+      auto live = [&](int j) { return !kMG || q * 32 + 4 * j + (lane >> 3) < (rank ? it.rows1 : it.rows); };
+      if (it.nsplit == 1 && p.accumulate) {
+        // Accumulate: the previous output is read ahead of its use. The loads of the first D
+        // 32-column chunks are issued before the accumulator is ready, so they overlap the tile's
+        // MMAs; the loads of chunk c + D are issued as soon as chunk c is written. W 32-bit words
+        // hold 4 previous outputs (2: BF16/FP16, 4: FP32). Same arithmetic as the other paths:
+        // one FP32 add, one rounding.
+        auto run = [&](auto w_tag, auto d_tag) -> bool {
+          constexpr int W = decltype(w_tag)::value;
+          constexpr int D = decltype(d_tag)::value;
+          static_assert((BN / 32) % D == 0, "the chunks divide into groups of D");
+          uint32_t old[D][8][W];
+          auto issue = [&](int c, uint32_t (&o)[8][W]) {
+            const char* cb = obase + size_t(c * 32 + (lane & 7) * 4) * esz;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (!live(j)) continue;
+              const char* src = cb + (4 * j + (lane >> 3)) * ostride;
+              if constexpr (W == 2) {
+                const uint2 h = *reinterpret_cast<const uint2*>(src);
+                o[j][0] = h.x;
+                o[j][1] = h.y;
+              } else {
+                const uint4 h = *reinterpret_cast<const uint4*>(src);
+                o[j][0] = h.x;
+                o[j][1] = h.y;
+                o[j][2] = h.z;
+                o[j][3] = h.w;
+              }
+            }
+          };
+#pragma unroll
+          for (int d = 0; d < D; ++d) issue(d, old[d]);
+          const bool okt = wait_bounded_t<kPair>(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
+          if (!__all_sync(0xffffffffu, okt)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < BN / 32; c0 += D) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) {
+              const int c = c0 + d;
+              {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + c * 32, r);
+                tmem_ld_wait();
+                if (c == BN / 32 - 1) release_acc();
+                stage_row(stg, lane, r);
+              }
+              __syncwarp();
+              char* cbase = obase + size_t(c * 32 + (lane & 7) * 4) * esz;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint4 o = W == 2 ? make_uint4(old[d][j][0], old[d][j][1], 0u, 0u)
+                                       : make_uint4(old[d][j][0], old[d][j][1], old[d][j][W > 2 ? 2 : 0],
+                                                    old[d][j][W > 2 ? 3 : 0]);
+                if (live(j)) emit4(p, cbase + (4 * j + (lane >> 3)) * ostride, unstage(stg, j, lane), o);
+              }
+              __syncwarp();
+              if (c + D < BN / 32) issue(c + D, old[d]);
+            }
+          }
+          return true;
+        };
+        // two chunks in flight for 16-bit outputs, one for FP32 (and in the M-grouped kernels, whose
+        // row predicates leave fewer registers), within the 255-register budget without spills
+        constexpr int kDepth16 = kMG ? 1 : 2;
+        const bool ok = p.out_bf16 ? run(std::integral_constant<int, 2>{}, std::integral_constant<int, kDepth16>{})
+                                   : run(std::integral_constant<int, 4>{}, std::integral_constant<int, 1>{});
+        if (!ok) break;
+        ++tcount;
+        continue;
+      }
+      const bool okt = wait_bounded_t<kPair>(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, okt)) break;
+      tc_fence_after();
       if (it.nsplit == 1) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -1218,17 +1292,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             stage_row(stg, lane, r);
           }
           __syncwarp();
-          uint4 old[8];
-          // M-grouped masked layout: rows at or past the group's valid count are not touched
-          auto live = [&](int j) { return !kMG || q * 32 + 4 * j + (lane >> 3) < (rank ? it.rows1 : it.rows); };
-          if (p.accumulate) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (live(j)) old[j] = load_old4(p, cbase + (4 * j + (lane >> 3)) * ostride);
-          }
+          const uint4 none = make_uint4(0u, 0u, 0u, 0u);   // overwrite: no previous values
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            if (live(j)) emit4(p, cbase + (4 * j + (lane >> 3)) * ostride, unstage(stg, j, lane), old[j]);
+            if (live(j)) emit4(p, cbase + (4 * j + (lane >> 3)) * ostride, unstage(stg, j, lane), none);
           __syncwarp();
         }
       } else {

@@ -372,7 +372,8 @@ def quantize_per_expert(quantize, x: torch.Tensor, token_axis: int, counts, pack
     if packed_fp4:
         assert np.all(counts % 2 == 0)
         return q[:, torch.from_numpy(cols[0::2] // 2)].contiguous(), sf
-    return (q[:, idx] if token_axis == 1 else q[idx, :]).contiguous(), sf
+    u = q.view(torch.uint8)            # gather the bytes (float8 tensors cannot be indexed on every torch)
+    return (u[:, idx] if token_axis == 1 else u[idx, :]).contiguous().view(q.dtype), sf
 
 
 def pack_ragged_a(a2d: torch.Tensor, counts) -> torch.Tensor:
