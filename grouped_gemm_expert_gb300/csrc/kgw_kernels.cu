@@ -233,7 +233,10 @@ __global__ void __launch_bounds__(PLAN_THREADS)
   }
   __syncthreads();
 
-  // 5. longest items first (ties by expert index): rank = #experts ordered before e
+  // 5. order: rank the experts longest item first (ties by expert index), then interleave the two
+  //    ends of that list -- longest, shortest, second longest, second shortest, ... A short
+  //    expert's tiles finish their MMAs faster than the epilogue drains an accumulator; taken in
+  //    turn with long tiles, their epilogues run under the long tiles' MMAs instead of back to back.
   for (int e = tid; e < E; e += blockDim.x) {
     const int key = s_key[e];
     int rank = 0;
@@ -1205,7 +1208,46 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       };
       uint4* stg = reinterpret_cast<uint4*>(epi_stage_mem + (warp - EPI_WARP0) * EPI_STAGE_BYTES);
       // M-grouped masked layout: rows at or past the group's valid count are not touched
-      auto live = [&](int j) { return !kMG || q * 32 + 4 * j + (lane >> 3) < (rank ? it.rows1 : it.rows); };
+      auto live_row = [&](int r) { return !kMG || q * 32 + r < (rank ? it.rows1 : it.rows); };
+      auto live = [&](int j) { return live_row(4 * j + (lane >> 3)); };
+      if (it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
+        // 16-bit outputs (BF16 / FP16), overwrite: each thread rounds row `lane` of a 32-column
+        // chunk in registers, so the per-warp staging carries packed 16-bit rows (64 bytes) -- half
+        // the shared-memory traffic of staging FP32, which competes with the tensor pipe's operand
+        // reads. Stores: 4 lanes per 64-byte row segment, 8 rows per instruction.
+        const bool okt = wait_bounded_t<kPair>(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, okt)) break;
+        tc_fence_after();
+        const int sw = (lane >> 1) & 3;        // 16-byte chunk swizzle of staging row `lane`
+        const int rsub = lane >> 2, csub = lane & 3;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t pk[16];
+          {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + c * 32, r);
+            tmem_ld_wait();
+            if (c == BN / 32 - 1) release_acc();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = p.out_f16 ? pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]))
+                                : pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            stg[lane * 4 + (i ^ sw)] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          __syncwarp();
+          char* cbase = obase + size_t(c * 32 + csub * 8) * 2;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 8 * j + rsub;
+            if (live_row(r)) *reinterpret_cast<uint4*>(cbase + r * ostride) = stg[r * 4 + (csub ^ ((r >> 1) & 3))];
+          }
+          __syncwarp();
+        }
+        ++tcount;
+        continue;
+      }
       if (it.nsplit == 1 && p.accumulate) {
         // Accumulate: the previous output is read ahead of its use. The loads of the first D
         // 32-column chunks are issued before the accumulator is ready, so they overlap the tile's
