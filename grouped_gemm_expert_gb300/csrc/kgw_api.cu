@@ -109,9 +109,9 @@ kgw_status validate(const kgw_wgrad_args* a, bool fp8, bool fp4 = false, int64_t
   if (a->out_dtype != KGW_OUT_F32 && a->out_dtype != KGW_OUT_BF16 && a->out_dtype != KGW_OUT_F16)
     return KGW_ERR_INVALID_ARG;
   if (a->accumulate != 0 && a->accumulate != 1) return KGW_ERR_INVALID_ARG;
-  // FP4: both operands K-major (the token axis packed two elements per byte), tensor2d order
-  if (fp4 && (a->a_major != KGW_K_MAJOR || a->b_major != KGW_K_MAJOR || a->input_order != KGW_TENSOR2D))
-    return KGW_ERR_UNSUPPORTED;
+  // FP4: both operands K-major (the token axis packed two elements per byte; the packed-FP4 MMA
+  // reads K-major operands only), in either input order
+  if (fp4 && (a->a_major != KGW_K_MAJOR || a->b_major != KGW_K_MAJOR)) return KGW_ERR_UNSUPPORTED;
   if (!a->offsets) return KGW_ERR_INVALID_ARG;
   if ((a->out == nullptr) == (a->out_ptrs == nullptr)) return KGW_ERR_INVALID_ARG;
   if (!aligned(a->offsets, 4)) return KGW_ERR_ALIGNMENT;
@@ -197,6 +197,9 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
 
   const int bk = fp4 ? kgw::BK_FP4 : bk_of(fp8);
   const uint64_t esz = fp8 ? 1 : 2;
+  // token-axis box of a K-major operand in descriptor elements: one 128-byte swizzle row (packed
+  // FP4 descriptors count bytes, so its 256 tokens are 128 elements)
+  const uint32_t box_k = fp4 ? 128u : static_cast<uint32_t>(bk);
   std::memset(&P->tmA, 0, sizeof(P->tmA));
   std::memset(&P->tmB, 0, sizeof(P->tmB));
   std::memset(&P->tpl, 0, sizeof(P->tpl));
@@ -218,18 +221,18 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
       uint64_t n_large = (kgw::TMAP_SIZE_CLASS_BYTES + rows * esz - 1) / (rows * esz);
       n_large = (n_large + kgw::TOKEN_ALIGN - 1) / kgw::TOKEN_ALIGN * kgw::TOKEN_ALIGN;
       if (n_large < n_small) n_large = n_small;
-      kgw_status r = encode_2d(small, dt, base, n_small, rows, n_small * esz, bk, box_rows);
-      if (r == KGW_OK) r = encode_2d(large, dt, base, n_large, rows, n_large * esz, bk, box_rows);
+      kgw_status r = encode_2d(small, dt, base, n_small, rows, n_small * esz, box_k, box_rows);
+      if (r == KGW_OK) r = encode_2d(large, dt, base, n_large, rows, n_large * esz, box_k, box_rows);
       return r;
     };
-    if (fp4) {
+    if (fp4 && !ragged) {
       // packed e2m1: the tensors count bytes along the token axis (two tokens per byte)
       st = encode_2d(&P->tmA, dt, a->a, Ts / 2, H, Ts / 2, 128, kgw::BM);             // [H, tokens/2]
       if (st == KGW_OK) st = encode_2d(&P->tmB, dt, a->b, Ts / 2, I, Ts / 2, 128, kgw::BN);  // [I, tokens/2]
       if (st != KGW_OK) return st;
     }
-    // A
-    if (fp4) {
+    // A (ragged packed FP4: per-expert [hidden, n_e/2]-byte blocks, through the templates below)
+    if (fp4 && !ragged) {
     } else if (a_k && !ragged) {
       st = encode_2d(&P->tmA, dt, a->a, Ts, H, Ts * esz, bk, kgw::BM);             // [H, tokens]
     } else if (a_k) {
@@ -240,7 +243,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     }
     if (st != KGW_OK) return st;
     // B
-    if (fp4) {
+    if (fp4 && !ragged) {
     } else if (b_k && !ragged) {
       st = encode_2d(&P->tmB, dt, a->b, Ts, I, Ts * esz, bk, b_rows_cta);         // [I, tokens]
     } else if (b_k) {
@@ -697,7 +700,8 @@ int32_t kgw_debug_check_tail_maps_kind(const kgw_wgrad_args* args, int32_t kind,
       const uint64_t n = static_cast<uint64_t>(end - begin);
       CUtensorMap ref;
       std::memset(&ref, 0, sizeof(ref));
-      kgw_status r = block ? encode_2d(&ref, dt, base + begin * rows * esz, n, rows, n * esz, box_k, box_rows)
+      kgw_status r = block ? encode_2d(&ref, dt, base + begin * rows * esz / tpu, n / tpu, rows, n * esz / tpu, box_k,
+                                       box_rows)
                      : mode == 1 ? encode_2d(&ref, dt, base, static_cast<uint64_t>(end) / tpu, rows, Ts / tpu * esz,
                                              box_k, box_rows)
                                  : encode_2d(&ref, dt, base, rows, static_cast<uint64_t>(end), rows * esz, atom, box_k);

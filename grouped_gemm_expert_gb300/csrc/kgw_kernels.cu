@@ -136,16 +136,19 @@ __global__ void __launch_bounds__(PLAN_THREADS)
       for (int op = 0; op < 2; ++op) {
         if (op == 0 ? !p.build_a : !p.build_b) continue;
         const int64_t rows = op == 0 ? p.H : p.I;
+        // block extent along the token axis in descriptor elements (packed FP4: bytes, two tokens each)
+        const int64_t tpu = p.tok_per_unit > 1 ? p.tok_per_unit : 1;
+        const int64_t nu = n / tpu;
         uint4* dst = reinterpret_cast<uint4*>(p.ws + (op == 0 ? p.L.tmaps : p.L.tmaps_b) + size_t(e) * 128);
-        const bool large = uint64_t(n) * uint64_t(rows) * uint64_t(p.esz) >= TMAP_SIZE_CLASS_BYTES;
+        const bool large = uint64_t(nu) * uint64_t(rows) * uint64_t(p.esz) >= TMAP_SIZE_CLASS_BYTES;
         const CUtensorMap* t = op == 0 ? (large ? &tm.a_large : &tm.a_small) : (large ? &tm.b_large : &tm.b_small);
         const uint4* src = reinterpret_cast<const uint4*>(t);
 #pragma unroll
         for (int j = 0; j < 8; ++j) dst[j] = src[j];
         const uint8_t* base = op == 0 ? p.a : p.b;
-        tmap_set_address(dst, reinterpret_cast<uint64_t>(base + prev * rows * p.esz));
-        tmap_set_dim0(dst, static_cast<uint32_t>(n));
-        tmap_set_stride1(dst, static_cast<uint64_t>(n * p.esz));
+        tmap_set_address(dst, reinterpret_cast<uint64_t>(base + prev * rows * p.esz / tpu));
+        tmap_set_dim0(dst, static_cast<uint32_t>(nu));
+        tmap_set_stride1(dst, static_cast<uint64_t>(nu * p.esz));
         fence_tmap_release();
       }
     }

@@ -163,7 +163,9 @@ kgw_status kgw_wgrad_fp8_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
  * 2 exponent bits with bias 1, 1 mantissa bit; values 0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte
  * along the token axis with the earlier token in the low nibble. Both operands K-major: A stored
  * [hidden, tokens_sum/2] bytes, B stored [intermediate, tokens_sum/2] bytes (a_major = b_major =
- * KGW_K_MAJOR), tensor2d input order; anything else is KGW_ERR_UNSUPPORTED. Scales as in
+ * KGW_K_MAJOR; MN-major is KGW_ERR_UNSUPPORTED: the packed-FP4 MMA reads K-major operands only);
+ * ragged input order: expert e's blocks are [hidden, n_e/2] and [intermediate, n_e/2] bytes at
+ * byte offsets begin_e*hidden/2 and begin_e*intermediate/2. Scales as in
  * kgw_wgrad_fp8_ue8m0 (packed UE8M0 words, one byte per 32 tokens). Workspace as for FP8
  * (kgw_workspace_size with is_fp8 = 1).
  */
@@ -192,8 +194,8 @@ kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
  * kgw_wgrad_fp8_ue8m0); any other value is KGW_ERR_INVALID_ARG. Counts (and tokens_sum) must be
  * multiples of 16 when A or B is K-major (a TMA coordinate along the innermost axis starts on 16
  * bytes), any count when both are MN-major.
- * kgw_wgrad_fp4_unaligned: e2m1 operands as in kgw_wgrad_fp4_ue8m0 (K-major A and B, tensor2d);
- * counts multiples of 32 (16 packed bytes).
+ * kgw_wgrad_fp4_unaligned: e2m1 operands as in kgw_wgrad_fp4_ue8m0 (K-major A and B, either
+ * input order); counts multiples of 32 (16 packed bytes).
  * A count that breaks the rule is KGW_ERR_OFFSETS on the device (nothing written). Workspace:
  * kgw_workspace_size with is_fp8 = 1. Everything else as for the aligned entries.
  */

@@ -209,6 +209,35 @@ def token_scale_rows(offsets, block: int) -> np.ndarray:
     return np.concatenate(rows) if rows else np.zeros(0, dtype=np.int64)
 
 
+def ue4m3_to_f64(bits) -> np.ndarray:
+    """Decode unsigned E4M3 scale bytes (UE4M3: the e4m3 'fn' encoding without a sign bit) exactly.
+
+    4 exponent bits (bias 7) and 3 mantissa bits: exponent field 0 is subnormal m/8 * 2**-6,
+    otherwise (1 + m/8) * 2**(e-7); 0x7F (all ones) is NaN. A byte with bit 7 set is not a UE4M3
+    value and decodes to NaN as well.
+    """
+    b = np.asarray(bits).view(np.uint8).astype(np.int64)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    v = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.ldexp(1.0, (e - 7).astype(np.int64)))
+    return np.where(((b & 0x7F) == 0x7F) | (b >= 0x80), np.nan, v)
+
+
+def unpack_ue4m3_16(packed) -> np.ndarray:
+    """Packed UE4M3 words [tokens/64, other] -> float64 scales [tokens/16, other].
+
+    Byte j (least significant first) of word [w][r] scales tokens 64*w + 16*j .. +16 of row or
+    column r: one scale per 16 tokens, the block size the cuDNN page's block-scaled contract
+    defaults to (sf_vec_size = 16), in the unsigned E4M3 format of NVFP4 block scales.
+    """
+    w = np.asarray(packed).view(np.uint32)
+    nw, other = w.shape
+    out = np.empty((nw * 4, other), dtype=np.float64)
+    for j in range(4):
+        out[j::4, :] = ue4m3_to_f64(((w >> (8 * j)) & 0xFF).astype(np.uint8))
+    return out
+
+
 def apply_scales_rows(x: np.ndarray, scales: np.ndarray, block: int, rows=None) -> np.ndarray:
     """x [rows, tokens] * s[r(k), m] for scales [blocks, rows]; r(k) = k // block, or the given
     per-token scale rows (``token_scale_rows``)."""
@@ -227,10 +256,20 @@ def apply_scales_cols(x: np.ndarray, scales: np.ndarray, block: int, rows=None) 
 
 
 def decode_scales(sf, sf_format: str):
-    """(scales as float64 [tokens/block, other], block) for either scale format."""
+    """(scales as float64 [tokens/block, other], block) for each scale format: FP32 per 128 tokens,
+    packed UE8M0 per 32 tokens, packed UE4M3 per 16 tokens."""
     if sf_format == "ue8m0_32":
         return unpack_ue8m0_32(sf), 32
+    if sf_format == "ue4m3_16":
+        return unpack_ue4m3_16(sf), 16
     return np.asarray(sf, dtype=np.float64), SCALE_BLOCK
+
+
+def global_factor(global_scale_a=None, global_scale_b=None) -> float:
+    """The product of the per-tensor global scales (1 where one is not given), exactly as float64."""
+    ga = 1.0 if global_scale_a is None else float(np.float32(global_scale_a))
+    gb = 1.0 if global_scale_b is None else float(np.float32(global_scale_b))
+    return ga * gb
 
 
 # ---------------------------------------------------------------------------------------------
@@ -268,7 +307,7 @@ def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, 
                        input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
                        c_init=None, accumulate: bool = False, with_bound: bool = True,
                        a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128",
-                       fp4: bool = False):
+                       fp4: bool = False, global_scale_a=None, global_scale_b=None):
     """Decode stored operands (raw bits) and evaluate the operation in float64.
 
     a_bits/b_bits: uint16 (bf16), uint8 (e4m3) or uint8 packed e2m1 (fp4, K-major only) numpy
@@ -277,7 +316,7 @@ def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, 
     decoded by the caller) or None.
     """
     if fp4:
-        assert a_major == "k" and b_major == "k" and sf_format == "ue8m0_32"
+        assert a_major == "k" and b_major == "k" and sf_format in ("ue8m0_32", "ue4m3_16")
         fp8 = True   # from here on the same steps: decoded elements times their scales
     dec = e2m1_to_f64 if fp4 else (e4m3_to_f64 if fp8 else bf16_to_f64)
     A = logical_a(dec(a_bits), hidden, offsets, input_order, a_major)
@@ -288,6 +327,11 @@ def wgrad_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, 
         rows = token_scale_rows(offsets, blk)
         A = apply_scales_rows(A, sa, blk, rows)
         B = apply_scales_cols(B, sb, blk, rows)
+    g = global_factor(global_scale_a, global_scale_b)
+    if g != 1.0:
+        # per-tensor global scales multiply the whole product (cuDNN page, "Block-scaled contract":
+        # global_scale_a / global_scale_b where the low-precision format requires them)
+        A = A * g
     return wgrad(A, B, offsets, c_init=c_init, accumulate=accumulate, with_bound=with_bound)
 
 
@@ -380,7 +424,7 @@ def element_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int
 def expert_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int, e: int, *,
                         input_order: str = "tensor2d", fp8: bool = False, sfa=None, sfb=None,
                         a_major: str = "k", b_major: str = "mn", sf_format: str = "f32_128",
-                        fp4: bool = False):
+                        fp4: bool = False, global_scale_a=None, global_scale_b=None):
     """(R_e, S_e) of one expert, decoding only that expert's operands (full-size checks).
 
     The same definition as ``wgrad_from_storage`` restricted to expert e: A_e [hidden, n_e] and
@@ -399,11 +443,17 @@ def expert_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int,
     fa = np.asarray(a_bits).reshape(-1)
     fb = np.asarray(b_bits).reshape(-1)
     if fp4:
-        # packed e2m1, both operands K-major tensor2d: row r holds tokens_sum/2 bytes
-        assert a_major == "k" and b_major == "k" and input_order == "tensor2d" and b % 2 == 0 and n % 2 == 0
-        Ae = e2m1_to_f64(np.ascontiguousarray(fa.reshape(hidden, tokens_sum // 2)[:, b // 2:end // 2])).reshape(hidden, n)
-        Be = e2m1_to_f64(np.ascontiguousarray(fb.reshape(intermediate, tokens_sum // 2)[:, b // 2:end // 2]))
-        Be = Be.reshape(intermediate, n).T
+        # packed e2m1, both operands K-major: tensor2d rows hold tokens_sum/2 bytes; ragged blocks
+        # are [rows, n_e/2] bytes starting at byte begin_e*rows/2
+        assert a_major == "k" and b_major == "k" and b % 2 == 0 and n % 2 == 0
+        if input_order == "tensor2d":
+            pa = fa.reshape(hidden, tokens_sum // 2)[:, b // 2:end // 2]
+            pb = fb.reshape(intermediate, tokens_sum // 2)[:, b // 2:end // 2]
+        else:
+            pa = fa[b * hidden // 2:end * hidden // 2]
+            pb = fb[b * intermediate // 2:end * intermediate // 2]
+        Ae = e2m1_to_f64(np.ascontiguousarray(pa)).reshape(hidden, n)
+        Be = e2m1_to_f64(np.ascontiguousarray(pb)).reshape(intermediate, n).T
     else:
         dec = e4m3_to_f64 if fp8 else bf16_to_f64
         if a_major == "mn":
@@ -424,4 +474,7 @@ def expert_from_storage(a_bits, b_bits, offsets, hidden: int, intermediate: int,
         ks = token_scale_rows(offsets, blk)[b:end]
         Ae = Ae * sa[ks, :].T
         Be = Be * sb[ks, :]
+    g = global_factor(global_scale_a, global_scale_b)
+    if g != 1.0:
+        Ae = Ae * g
     return Ae @ Be, np.abs(Ae) @ np.abs(Be)

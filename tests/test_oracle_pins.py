@@ -733,7 +733,23 @@ _EXPERT_CASES = [
     dict(fp8=True, sf_format="ue8m0_32", input_order="ragged"),
     dict(fp8=True, a_major="mn", b_major="k"),
     dict(fp4=True, b_major="k", sf_format="ue8m0_32"),
+    dict(fp4=True, b_major="k", sf_format="ue8m0_32", input_order="ragged"),
 ]
+
+
+def test_fp4_ragged_order_is_the_same_problem_as_tensor2d():
+    """Ragged FP4 stores each expert's [rows, n_e/2]-byte block back to back; the oracle reads the same
+    logical values as from the tensor2d layout, and the stored bytes really moved."""
+    kw = dict(fp4=True, b_major="k", sf_format="ue8m0_32")
+    counts = [256, 0, 512, 768]
+    w2 = W.custom(4, 128, 256, counts, seed=83, **kw)
+    wr = W.custom(4, 128, 256, counts, seed=83, input_order="ragged", **kw)
+    x2, xr = W.make_inputs(w2, "cpu"), W.make_inputs(wr, "cpu")
+    assert not np.array_equal(x2.a.numpy().ravel(), xr.a.numpy().ravel())
+    common = dict(fp4=True, b_major="k", sf_format="ue8m0_32", sfa=x2.sfa.numpy(), sfb=x2.sfb.numpy())
+    r2, _ = O.wgrad_from_storage(x2.a.numpy(), x2.b.numpy(), w2.offsets, 128, 256, **common)
+    rr, _ = O.wgrad_from_storage(xr.a.numpy(), xr.b.numpy(), wr.offsets, 128, 256, input_order="ragged", **common)
+    assert np.array_equal(r2, rr)
 
 
 @pytest.mark.parametrize("kw", _EXPERT_CASES, ids=lambda kw: "-".join(f"{k}={v}" for k, v in kw.items()) or "bf16")
@@ -857,3 +873,75 @@ def test_per_expert_quantisation_roundtrip_needs_per_expert_scale_rows(kind):
     rows_global = np.minimum(np.arange(w.tokens_sum) // blk, sa.shape[0] - 1)
     bad = O.apply_scales_rows(a, sa, blk, rows_global)
     assert not np.all(np.abs(bad - a32) <= rel * np.abs(a32) + floor)
+
+
+# ------------------------------------------------------------------------------------------
+# NVFP4: e2m1 elements, unsigned-E4M3 scales per 16 tokens, FP32 global scales (the cuDNN page's
+# block-scaled contract: sf_vec_size 16 and global_scale_a / global_scale_b)
+# ------------------------------------------------------------------------------------------
+
+def test_ue4m3_decoder_matches_torch_e4m3_on_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    got = O.ue4m3_to_f64(codes)
+    ref = torch.from_numpy(codes[:128].copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(got[:127], ref[:127])                 # 0x00..0x7E: the e4m3 values
+    assert np.isnan(got[127]) and np.all(np.isnan(got[128:]))   # 0x7F NaN; a sign bit is invalid
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0 and got[1] == 2.0 ** -9
+
+
+def test_ue4m3_words_unpack_to_16_token_rows():
+    w = np.array([[0x38403038, 0x7E000001]], dtype=np.uint32).view(np.int32)     # [1 word-row, 2 columns]
+    s = O.unpack_ue4m3_16(w)
+    assert s.shape == (4, 2)
+    assert s[:, 0].tolist() == [1.0, 0.5, 2.0, 1.0]       # bytes 0x38, 0x30, 0x40, 0x38
+    assert s[:, 1].tolist() == [2.0 ** -9, 0.0, 0.0, 448.0]
+
+
+def test_nvfp4_quantiser_round_trip():
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(64, 512, generator=g) * 5
+    gs = W.nvfp4_global_scale(x)
+    q, words = W.quantize_e2m1_ue4m3_16(x, 1, gs)
+    s, blk = O.decode_scales(words.numpy(), "ue4m3_16")
+    assert blk == 16 and not np.isnan(s).any() and s.max() <= 448
+    dec = O.apply_scales_rows(O.e2m1_to_f64(q.numpy()).reshape(64, 512), s, 16) * gs
+    per = O.apply_scales_rows(np.ones((64, 512)), s, 16) * gs
+    err = np.abs(dec - x.double().numpy())
+    assert np.all(err <= 2.0 ** -2 * np.abs(x.double().numpy()) + 0.25 * per + 1e-12)
+    # scales are the smallest E4M3 values that cover each block's amax / 6
+    amax = np.abs(x.double().numpy()).reshape(64, 32, 16).max(axis=2).T           # [blocks, rows]
+    assert np.all(s * gs * 6 >= amax * (1 - 2.0 ** -23))
+
+
+def test_nvfp4_brute_force_with_global_scales():
+    rng = np.random.default_rng(44)
+    counts = [128, 0, 128]
+    T, H, I = 256, 2, 3
+    offs = np.cumsum(counts).astype(np.int32)
+    codes_a = rng.integers(0, 16, size=(H, T)).astype(np.uint8)
+    codes_b = rng.integers(0, 16, size=(I, T)).astype(np.uint8)
+    pa = codes_a[:, 0::2] | (codes_a[:, 1::2] << 4)
+    pb = codes_b[:, 0::2] | (codes_b[:, 1::2] << 4)
+    sa_codes = rng.integers(0x20, 0x50, size=(T // 16, H)).astype(np.uint32)
+    sb_codes = rng.integers(0x20, 0x50, size=(T // 16, I)).astype(np.uint32)
+
+    def pack(c):
+        c = c.reshape(T // 64, 4, -1)
+        return (c[:, 0] | (c[:, 1] << 8) | (c[:, 2] << 16) | (c[:, 3] << 24)).view(np.int32)
+
+    ga, gb = np.float32(0.375), np.float32(-1.25)
+    got, S = O.wgrad_from_storage(pa, pb, offs, H, I, fp4=True, b_major="k", sf_format="ue4m3_16",
+                                  sfa=pack(sa_codes), sfb=pack(sb_codes), global_scale_a=ga, global_scale_b=gb)
+    e2m1 = {c: Fraction(v) for c, v in _fp4_golden().items()}
+    e4m3 = lambda c: Fraction(float(torch.tensor([int(c)], dtype=torch.uint8).view(torch.float8_e4m3fn).double()))
+    g = Fraction(float(ga)) * Fraction(float(gb))
+    for e, (b, end) in enumerate([(0, 128), (128, 128), (128, 256)]):
+        for m in range(H):
+            for n in range(I):
+                exact = g * sum(e2m1[int(codes_a[m, k])] * e4m3(sa_codes[k // 16, m]) *
+                                e2m1[int(codes_b[n, k])] * e4m3(sb_codes[k // 16, n]) for k in range(b, end))
+                assert abs(Fraction(got[e, m, n]) - exact) <= Fraction(1e-12) * Fraction(S[e, m, n]) + Fraction(1e-300)
+    # the global scales multiply exactly: doubling one doubles every result
+    got2, _ = O.wgrad_from_storage(pa, pb, offs, H, I, fp4=True, b_major="k", sf_format="ue4m3_16",
+                                   sfa=pack(sa_codes), sfb=pack(sb_codes), global_scale_a=2 * ga, global_scale_b=gb)
+    assert np.array_equal(got2, 2 * got)

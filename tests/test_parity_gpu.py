@@ -97,6 +97,10 @@ CASES = {
                                    sf_format="ue8m0_32"),
     "fp4_split_k_accumulate": W.custom(3, 128, 256, [32768, 0, 256], seed=112, fp4=True, b_major="k",
                                        sf_format="ue8m0_32", accumulate=True),
+    "fp4_ragged": W.custom(4, 256, 512, [768, 0, 256, 1280], seed=115, fp4=True, b_major="k",
+                           sf_format="ue8m0_32", input_order="ragged", out_dtype="bf16"),
+    "fp4_ragged_split_k_f32": W.custom(2, 128, 256, [24576, 512], seed=116, fp4=True, b_major="k",
+                                       sf_format="ue8m0_32", input_order="ragged"),
     "fp4_discrete_f16": W.custom(3, 256, 256, [1024, 512, 256], seed=113, fp4=True, b_major="k",
                                  sf_format="ue8m0_32", out_dtype="f16", output_mode="discrete"),
 }
@@ -240,13 +244,14 @@ def test_small_workspace_still_correct():
 
 
 def test_fp4_rejects_unsupported_layouts():
-    """FP4 needs K-major A and B in tensor2d order: anything else is KGW_ERR_UNSUPPORTED, host-side."""
+    """FP4 needs K-major A and B (the packed-FP4 MMA reads K-major operands): an MN-major operand is
+    KGW_ERR_UNSUPPORTED, host-side."""
     kgw = ensure_built()
     w = W.custom(2, 128, 256, [256, 256], seed=114, fp4=True, b_major="k", sf_format="ue8m0_32")
     x = W.make_inputs(w, DEV)
     out = torch.empty((2, 128, 256), dtype=torch.float32, device=DEV)
     ws = torch.empty(1 << 20, dtype=torch.uint8, device=DEV)
-    for kw in ({"b_major": kgw.KGW_MN_MAJOR}, {"a_major": kgw.KGW_MN_MAJOR}, {"input_order": kgw.KGW_RAGGED}):
+    for kw in ({"b_major": kgw.KGW_MN_MAJOR}, {"a_major": kgw.KGW_MN_MAJOR}):
         args = kgw.make_args(2, 128, 256, 512, x.a, x.b, x.offsets, out=out,
                              **{"b_major": kgw.KGW_K_MAJOR, **kw})
         assert kgw.kgw_wgrad_fp4_ue8m0(args, x.sfa, x.sfb, ws, check=False) == kgw.KGW_ERR_UNSUPPORTED

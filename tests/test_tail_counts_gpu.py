@@ -198,10 +198,11 @@ def test_fp8_tail_descriptors_match_host_encoding(a_major, b_major, order):
     _map_check_kind(1, [4112, 5200, 3216, 5200], 4096, 1536, a_major, b_major, order)
 
 
-def test_fp4_tail_descriptors_match_host_encoding():
+@pytest.mark.parametrize("order", ["tensor2d", "ragged"])
+def test_fp4_tail_descriptors_match_host_encoding(order):
     _MAPS_BS["checked"] = True
-    _map_check_kind(2, [32, 0, 160, 1024, 4064], 256, 512, "k", "k", "tensor2d")
-    _map_check_kind(2, [4128, 5216, 3200, 5184], 4096, 1536, "k", "k", "tensor2d")
+    _map_check_kind(2, [32, 0, 160, 1024, 4064], 256, 512, "k", "k", order)
+    _map_check_kind(2, [4128, 5216, 3200, 5184], 4096, 1536, "k", "k", order)
 
 
 def _require_bs_maps():
@@ -231,6 +232,7 @@ BS_CASES = {
     "fp4": F4(4, 256, 512, [32, 0, 160, 1056], seed=150),
     "fp4_single_block_last_stage": F4(3, 128, 256, [96, 352, 128], seed=151, out_dtype="bf16"),
     "fp4_split_k": F4(2, 128, 256, [20000, 32], seed=152),
+    "fp4_ragged": F4(4, 256, 512, [96, 0, 1184, 32], seed=155, input_order="ragged", out_dtype="bf16"),
 }
 
 

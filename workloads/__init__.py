@@ -159,6 +159,13 @@ def fp4() -> Workload:
                     out_dtype="bf16", fp4=True, b_major="k", sf_format="ue8m0_32")
 
 
+def nvfp4() -> Workload:
+    return Workload("NVFP4 block-scaled: E=16 hidden=4096 intermediate=1536, e2m1 with UE4M3 scales per 16 "
+                    "tokens and FP32 global scales, K-major A and B, BF16 dense overwrite",
+                    16, 4096, 1536, counts_uniform_spread(3, 16, 4096, 0.7, 1.3), seed=13,
+                    out_dtype="bf16", fp4=True, b_major="k", sf_format="ue4m3_16")
+
+
 def round_to(x: np.ndarray, m: int) -> np.ndarray:
     """Nearest multiple of m: m * floor(x / m + 0.5)."""
     return (m * np.floor(np.asarray(x, dtype=np.float64) / m + 0.5)).astype(np.int64)
@@ -184,7 +191,7 @@ def fp4_unaligned() -> Workload:
 
 
 NAMED = {"tiny": tiny, "balanced": balanced, "wide": wide, "fp8": fp8, "skewed": skewed, "fp4": fp4,
-         "unaligned": unaligned, "fp8_unaligned": fp8_unaligned, "fp4_unaligned": fp4_unaligned}
+         "unaligned": unaligned, "fp8_unaligned": fp8_unaligned, "fp4_unaligned": fp4_unaligned, "nvfp4": nvfp4}
 
 
 def custom(num_experts: int, hidden: int, intermediate: int, counts, seed: int, **kw) -> Workload:
@@ -213,6 +220,7 @@ class Inputs:
        block of each expert (tokens_sum/128 rows when every count is a multiple of 128), or with
        sf_format "ue8m0_32" int32 packed UE8M0 words of the same shapes.
     c: pre-filled output [E, hidden, intermediate] for accumulate mode, else None.
+    gsa/gsb (NVFP4, sf_format "ue4m3_16"): float32 [1] per-tensor global scales.
     """
     a: torch.Tensor
     b: torch.Tensor
@@ -220,6 +228,8 @@ class Inputs:
     sfa: Optional[torch.Tensor] = None
     sfb: Optional[torch.Tensor] = None
     c: Optional[torch.Tensor] = None
+    gsa: Optional[torch.Tensor] = None      # NVFP4: float32 [1] global scale of A (decode multiplier)
+    gsb: Optional[torch.Tensor] = None      # NVFP4: float32 [1] global scale of B
 
 
 def out_torch_dtype(name: str) -> torch.dtype:
@@ -376,6 +386,64 @@ def quantize_per_expert(quantize, x: torch.Tensor, token_axis: int, counts, pack
     return (u[:, idx] if token_axis == 1 else u[idx, :]).contiguous().view(q.dtype), sf
 
 
+_E4M3_POS = None
+
+
+def e4m3_positive_values() -> np.ndarray:
+    """The finite positive values of the e4m3 'fn' encoding (codes 1..126), ascending."""
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        codes = torch.arange(1, 127, dtype=torch.uint8)
+        _E4M3_POS = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return _E4M3_POS
+
+
+def quantize_e2m1_ue4m3_16(x: torch.Tensor, token_axis: int, gs: float):
+    """Quantise ``x`` (float32 2-D) to NVFP4: e2m1 elements, one unsigned-E4M3 scale per 16 tokens,
+    and the per-tensor global scale ``gs`` (a decode multiplier: value = e2m1 * block scale * gs).
+
+    The block scale is the smallest E4M3 value >= amax / (6 * gs) (1 for an all-zero block), so
+    |x / (scale * gs)| <= 6 up to the float32 rounding of the division and nothing saturates;
+    elements round to the nearest e2m1 value, ties to the even code. Returns (packed uint8
+    [other, tokens/2], the token axis contiguous, first token in the low nibble; int32 words
+    [tokens/64, other], byte j of word [w][r] = the scale code of tokens 64w + 16j .. +16).
+    """
+    assert x.dim() == 2 and x.dtype == torch.float32
+    xt = (x if token_axis == 1 else x.t()).contiguous()
+    other, tokens = xt.shape
+    assert tokens % 64 == 0
+    blocks = xt.view(other, tokens // 16, 16)
+    amax = blocks.abs().amax(dim=2).double().numpy()
+    need = amax / (E2M1_MAX * gs)
+    vals = e4m3_positive_values()
+    idx = np.minimum(np.searchsorted(vals, need, side="left"), len(vals) - 1)
+    scale = np.where(amax == 0.0, 1.0, vals[idx])                          # exact E4M3 values
+    codes = torch.from_numpy(scale.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    div = torch.from_numpy((scale * gs).astype(np.float32))
+    mids = torch.tensor(_E2M1_MIDS, dtype=torch.float32)
+    packed = torch.empty((other, tokens // 2), dtype=torch.uint8)
+    step = max(1, (1 << 22) // tokens)
+    for r0 in range(0, other, step):
+        y = blocks[r0:r0 + step] / div[r0:r0 + step, :, None]
+        a = y.abs().reshape(-1)
+        code = torch.bucketize(a, mids)
+        tie_up = (code < 7) & (a == mids[code.clamp(max=6)]) & ((code & 1) == 1)
+        code = code + tie_up.to(code.dtype)
+        neg = torch.signbit(y.reshape(-1)) & (code != 0)
+        code = (code | (neg.to(code.dtype) << 3)).to(torch.uint8).view(-1, tokens)
+        packed[r0:r0 + step] = code[:, 0::2] | (code[:, 1::2] << 4)
+    byte = codes.astype(np.uint32).reshape(other, tokens // 64, 4)
+    words = (byte[..., 0] | (byte[..., 1] << 8) | (byte[..., 2] << 16) | (byte[..., 3] << 24)).astype(np.uint32)
+    return packed, torch.from_numpy(words.view(np.int32).T.copy())
+
+
+def nvfp4_global_scale(x: torch.Tensor) -> float:
+    """Per-tensor global scale (decode multiplier) that keeps every 16-token block scale within E4M3:
+    amax / (6 * 448) as float32 (1 for an all-zero tensor)."""
+    amax = float(x.abs().max())
+    return float(np.float32(amax / (E2M1_MAX * E4M3_MAX))) if amax > 0 else 1.0
+
+
 def pack_ragged_a(a2d: torch.Tensor, counts) -> torch.Tensor:
     """Re-store a logical [hidden, tokens_sum] A as per-expert K-contiguous blocks.
 
@@ -420,14 +488,26 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
     b32 = _normal(gen, (T, I), w.b_std)
     sfa = sfb = None
     if w.fp4:
-        assert w.a_major == "k" and w.b_major == "k" and w.input_order == "tensor2d"
-        a_store, sfa = quantize_per_expert(quantize_e2m1_ue8m0_32, a32, 1, w.counts, packed_fp4=True)  # [H, T/2]
-        b_store, sfb = quantize_per_expert(quantize_e2m1_ue8m0_32, b32, 0, w.counts, packed_fp4=True)  # [I, T/2]
+        assert w.a_major == "k" and w.b_major == "k"
+        gsa = gsb = None
+        if w.sf_format == "ue4m3_16":
+            # NVFP4: 16-token blocks on the pages' 256-token counts (blocks never cross experts)
+            assert np.all(np.asarray(w.counts) % 64 == 0)
+            ga, gb = nvfp4_global_scale(a32), nvfp4_global_scale(b32)
+            a_store, sfa = quantize_e2m1_ue4m3_16(a32, 1, ga)
+            b_store, sfb = quantize_e2m1_ue4m3_16(b32, 0, gb)
+            gsa, gsb = torch.tensor([ga], dtype=torch.float32), torch.tensor([gb], dtype=torch.float32)
+        else:
+            a_store, sfa = quantize_per_expert(quantize_e2m1_ue8m0_32, a32, 1, w.counts, packed_fp4=True)  # [H, T/2]
+            b_store, sfb = quantize_per_expert(quantize_e2m1_ue8m0_32, b32, 0, w.counts, packed_fp4=True)  # [I, T/2]
+        if w.input_order == "ragged":   # per-expert [rows, n_e/2]-byte blocks back to back
+            half = np.asarray(w.counts) // 2
+            a_store, b_store = pack_ragged_a(a_store, half), pack_ragged_a(b_store, half)
         del a32, b32
         c = _normal(gen, (E, H, I), w.c_std).to(out_torch_dtype(w.out_dtype)) if w.accumulate else None
         offsets = torch.from_numpy(w.offsets.astype(np.int32))
         to = lambda t: None if t is None else t.to(device)
-        return Inputs(to(a_store), to(b_store), to(offsets), to(sfa), to(sfb), to(c))
+        return Inputs(to(a_store), to(b_store), to(offsets), to(sfa), to(sfb), to(c), to(gsa), to(gsb))
     if w.fp8 and w.sf_format == "ue8m0_32":
         a_store, sfa = quantize_per_expert(quantize_e4m3_ue8m0_32, a32, 1, w.counts)
         b_store, sfb = quantize_per_expert(quantize_e4m3_ue8m0_32, b32, 0, w.counts)
@@ -463,8 +543,9 @@ def make_inputs_device(w: Workload, device) -> Inputs:
 
     if w.fp8 or w.fp4:
         cpu = make_inputs(w, "cpu")   # quantisation recipe lives on the CPU side
-        return Inputs(cpu.a.to(device), cpu.b.to(device), cpu.offsets.to(device),
-                      cpu.sfa.to(device), cpu.sfb.to(device), None if cpu.c is None else cpu.c.to(device))
+        to = lambda t: None if t is None else t.to(device)
+        return Inputs(to(cpu.a), to(cpu.b), to(cpu.offsets), to(cpu.sfa), to(cpu.sfb), to(cpu.c), to(cpu.gsa),
+                      to(cpu.gsb))
     a = normal((H, T), w.a_std, torch.bfloat16)
     b = normal((T, I), w.b_std, torch.bfloat16)
     a, b = store_operands(w, a, b)
