@@ -21,6 +21,7 @@ The functions keep the C names of ``include/kgw.h``:
   kgw_mgrouped_workspace_size(args) -> int
   kgw_mgrouped_bf16(args, workspace, stream=None)
   kgw_mgrouped_fp8(args, sfa, sfb, sf_format, workspace, stream=None)
+  kgw_wgrad_nvfp4(args, sfa_packed, sfb_packed, global_scale_a, global_scale_b, workspace, stream=None)
   kgw_wgrad_fp8_unaligned(args, sfa, sfb, sf_format, workspace, stream=None)
   kgw_wgrad_fp4_unaligned(args, sfa_packed, sfb_packed, workspace, stream=None)
   kgw_debug_check_tail_maps_kind(args, kind, host_offsets, workspace) -> int
@@ -65,7 +66,7 @@ EXPORTED = ("kgw_workspace_size", "kgw_wgrad_bf16", "kgw_wgrad_fp8_blockscaled",
             "kgw_debug_check_ragged_maps", "kgw_wgrad_fp8_ue8m0", "kgw_mgrouped_workspace_size",
             "kgw_mgrouped_bf16", "kgw_wgrad_fp4_ue8m0", "kgw_wgrad_bf16_unaligned",
             "kgw_debug_check_tail_maps", "kgw_mgrouped_fp8", "kgw_wgrad_fp8_unaligned", "kgw_wgrad_fp4_unaligned",
-            "kgw_debug_check_tail_maps_kind")
+            "kgw_debug_check_tail_maps_kind", "kgw_wgrad_nvfp4")
 
 
 class KgwArgs(ctypes.Structure):
@@ -160,6 +161,9 @@ def lib() -> ctypes.CDLL:
         L.kgw_debug_check_tail_maps.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
                                                 ctypes.c_size_t, ctypes.c_void_p]
         L.kgw_debug_check_tail_maps.restype = ctypes.c_int32
+        L.kgw_wgrad_nvfp4.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        L.kgw_wgrad_nvfp4.restype = ctypes.c_int
         L.kgw_wgrad_fp8_unaligned.argtypes = [ctypes.POINTER(KgwArgs), ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.kgw_wgrad_fp8_unaligned.restype = ctypes.c_int
@@ -266,6 +270,18 @@ def kgw_wgrad_fp8_ue8m0(args: KgwArgs, sfa_packed, sfb_packed, workspace, worksp
                                    _stream_handle(stream))
     if check and rc != KGW_OK:
         raise KgwError(rc, "kgw_wgrad_fp8_ue8m0")
+    return rc
+
+
+def kgw_wgrad_nvfp4(args: KgwArgs, sfa_packed, sfb_packed, global_scale_a, global_scale_b, workspace,
+                    workspace_bytes: Optional[int] = None, stream=None, check: bool = True) -> int:
+    """NVFP4: e2m1 operands (K-major), UE4M3 scales per 16 tokens packed four to an int32 word, and
+    per-tensor FP32 global scales given as device tensors of one float (or None for 1)."""
+    nbytes = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    rc = lib().kgw_wgrad_nvfp4(ctypes.byref(args), _ptr(sfa_packed), _ptr(sfb_packed), _ptr(global_scale_a),
+                               _ptr(global_scale_b), _ptr(workspace), nbytes, _stream_handle(stream))
+    if check and rc != KGW_OK:
+        raise KgwError(rc, "kgw_wgrad_nvfp4")
     return rc
 
 

@@ -342,11 +342,16 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
 }
 
 kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws, size_t ws_bytes,
-               void* stream, bool sf_packed = false, bool fp4 = false, bool tail = false) {
+               void* stream, bool sf_packed = false, bool fp4 = false, bool tail = false, bool nvfp4 = false,
+               const float* gscale_a = nullptr, const float* gscale_b = nullptr) {
+  if ((gscale_a && !aligned(gscale_a, 4)) || (gscale_b && !aligned(gscale_b, 4))) return KGW_ERR_ALIGNMENT;
   Prepared P;
   kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P, fp4, tail);
   if (st != KGW_OK) return st;
   P.mp.sf_packed = sf_packed;
+  P.mp.nvfp4 = nvfp4;
+  P.mp.gscale_a = gscale_a;
+  P.mp.gscale_b = gscale_b;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kgw::launch_plan(P.pp, P.tpl, s) != cudaSuccess) return KGW_ERR_CUDA;
   cudaError_t e = fp4 ? kgw::launch_main_fp4(P.mp, P.tmA, P.tmB, P.grid, s)
@@ -573,6 +578,13 @@ kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
                                void* workspace, size_t workspace_bytes, void* stream) {
   return run(args, true, reinterpret_cast<const float*>(sfa_packed), reinterpret_cast<const float*>(sfb_packed),
              workspace, workspace_bytes, stream, true, true);
+}
+
+kgw_status kgw_wgrad_nvfp4(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
+                           const float* global_scale_a, const float* global_scale_b, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  return run(args, true, reinterpret_cast<const float*>(sfa_packed), reinterpret_cast<const float*>(sfb_packed),
+             workspace, workspace_bytes, stream, true, true, false, true, global_scale_a, global_scale_b);
 }
 
 kgw_status kgw_wgrad_fp8_unaligned(const kgw_wgrad_args* args, const void* sfa, const void* sfb, int32_t sf_format,

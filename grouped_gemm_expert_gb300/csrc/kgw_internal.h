@@ -69,6 +69,13 @@ constexpr uint32_t SF_STAGE_COLS = 12;
 // B word 1 likewise) that land in 24 TMEM columns per stage.
 constexpr uint32_t SF_SMEM_BYTES_FP4 = 2 * (BM + BN) * 4;
 constexpr uint32_t SF_STAGE_COLS_FP4 = 24;
+// NVFP4 stages (UE4M3 scales per 16 tokens): four 64-token scale words per row/column (A 4 x 128,
+// B 4 x 256 words, 6 KiB), rearranged in place into 12 blocks (for each MMA k: A word k, B word k
+// columns 0..127, 128..255) that land in 48 TMEM columns per stage; 3 stages of 54 KiB.
+constexpr uint32_t SF_SMEM_BYTES_NV = 4 * (BM + BN) * 4;
+constexpr uint32_t SF_SMEM_PAD_NV = 6144;
+constexpr uint32_t SF_STAGE_COLS_NV = 48;
+constexpr int STAGES_NV = 3;
 // Block-scaled epilogue: TMEM columns 384..511 (past the accumulator and the scale-factor ring)
 // hold each epilogue warp's 32 x 128 results packed to 16 bits (64 columns per column half), so
 // the accumulator can be handed back before the stores.
@@ -187,6 +194,9 @@ struct MainParams {
   const float* sfa;             // FP8: [tokens_sum/128, H] FP32 (or packed UE8M0 words)
   const float* sfb;             // FP8: [tokens_sum/128, I]
   int32_t sf_packed;            // FP8 scales given as packed UE8M0 words (4 x 32-token blocks)
+  int32_t nvfp4;                // FP4 with UE4M3 scales per 16 tokens (kind::mxf4nvf4, scale_vec::4X)
+  const float* gscale_a;        // NVFP4: per-tensor global scales (device, one float each; null = 1)
+  const float* gscale_b;
   int32_t* status_dev;
   uint8_t* ws;
   WsLayout L;
@@ -207,7 +217,7 @@ cudaError_t launch_plan_mgrouped(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                  cudaStream_t s);
 constexpr int MG_ROW_ALIGN = 128;   // every group's row count is a multiple of the 128-row tile
-size_t main_smem_bytes(bool pair, bool fp8);
+size_t main_smem_bytes(bool pair, bool fp8, bool nv = false);
 bool fp8_supported();
 
 }  // namespace kgw

@@ -534,8 +534,9 @@ struct SmemCtl {
 constexpr uint32_t EPI_STAGE_TOTAL = 16384;
 constexpr uint32_t EPI_STAGE_BYTES = EPI_STAGE_TOTAL / NUM_EPI_WARPS;
 
-size_t main_smem_bytes(bool pair, bool fp8) {
+size_t main_smem_bytes(bool pair, bool fp8, bool nv) {
   const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + (fp8 ? SF_SMEM_PAD : 0u))
+                      : nv ? size_t(STAGES_NV) * (STAGE_BYTES + SF_SMEM_PAD_NV)
                            : size_t(STAGES) * (STAGE_BYTES + (fp8 ? SF_SMEM_PAD : 0u));
   return ring + EPI_STAGE_TOTAL + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
 }
@@ -649,8 +650,10 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
 //    both CTAs' shared memory and writes each CTA's 128 rows into its own TMEM. Per SM this moves
 //    32 KiB per k-iteration into shared memory instead of 48 KiB.
 // kFp8 selects the block-scaled path (scale-factor converter, one accumulator); kFp4 narrows it
-// to e2m1 operands (kind::mxf4, 256 tokens per stage, K-major A and B, UE8M0 words only).
-template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false>
+// to e2m1 operands (kind::mxf4, 256 tokens per stage, K-major A and B, UE8M0 words only); kNv
+// makes that NVFP4 (kind::mxf4nvf4 scale_vec::4X: UE4M3 scales per 16 tokens, 48 TMEM scale
+// columns per stage, 3 stages, per-tensor global scales applied in the epilogue).
+template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false, bool kNv = false>
 __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
@@ -658,9 +661,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   // all 256 B columns in each CTA's TMEM) was correct but 1.85x slower on the FP8 workload.
   static_assert(!(kFp8 && kPair), "the FP8 path runs on single CTAs");
   static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
-  constexpr int kStages = kPair ? STAGES_PAIR : STAGES;
+  static_assert(!kNv || kFp4, "NVFP4 is the FP4 kernel with UE4M3 scales");
+  constexpr int kStages = kPair ? STAGES_PAIR : (kNv ? STAGES_NV : STAGES);
   constexpr uint32_t kStageB = kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
-  constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB + (kFp8 ? SF_SMEM_PAD : 0u);
+  constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB + (kNv ? SF_SMEM_PAD_NV : (kFp8 ? SF_SMEM_PAD : 0u));
   constexpr uint32_t kStageTx = STAGE_A_BYTES + kStageB;
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
   constexpr int kHalves = kPair ? 2 : 1;
@@ -800,7 +804,18 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           const int32_t b_tok = kMG ? it.e * p.K + kb * bk : static_cast<int32_t>(tok);
           // scales first: they are small and land before the operand tiles, so the converter's
           // work is done by the time the MMA has its operands
-          if constexpr (kFp4) {
+          if constexpr (kNv) {
+            // NVFP4: the four 64-token scale words of this 256-token stage (UE4M3 bytes per 16
+            // tokens): [A word 0..3][B word 0..3]; word rows are the expert's 64-token groups
+            const int64_t w0 = 2 * int64_t(it.srow) + 4 * int64_t(kb);
+            uint8_t* sS = sB + kStageB;
+            mbar_arrive_expect_tx(&ctl->sfdata[stage], SF_SMEM_BYTES_NV);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) bulk_load(sS + j * BM * 4, p.sfa + (w0 + j) * p.H + it.m0, BM * 4, &ctl->sfdata[stage]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              bulk_load(sS + 4 * BM * 4 + j * BN * 4, p.sfb + (w0 + j) * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
+          } else if constexpr (kFp4) {
             // the two 128-token scale words of this 256-token stage: [A word 0][A word 1]
             // [B word 0][B word 1], on the stage's scale barrier. Scale blocks are the expert's own
             // (rows from it.srow on); when its last stage holds a single block, word 1 repeats
@@ -872,7 +887,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       uint32_t phase = 0;
       int tcount = 0;
       constexpr uint32_t a_mn = kAK ? 0u : 1u, b_mn = kBK ? 0u : 1u;
-      const uint32_t idesc = kFp4 ? idesc_mxf4(BM, BN)
+      const uint32_t idesc = kNv ? idesc_nvf4(BM, BN) : kFp4 ? idesc_mxf4(BM, BN)
                              : kFp8 ? idesc_mxf8(BM * kHalves, BN, a_mn, b_mn, 0)
                                     : idesc_bf16_f32(BM * kHalves, BN, a_mn, b_mn);
       // Shared-memory operand descriptors (128-byte swizzle). K-major: 128-byte rows, 8-row groups
@@ -920,7 +935,20 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * kStageBytes);
           const uint32_t b_addr = a_addr + STAGE_A_BYTES;
-          if constexpr (kFp4) {
+          if constexpr (kNv) {
+            // 12 scale blocks of this stage -> TMEM columns 4i of the stage's 48; MMA k (64 tokens)
+            // reads A block 3k (columns 12k..12k+3) and B blocks 3k+1, 3k+2 (12k+4..12k+11), all
+            // four UE4M3 bytes of each column
+            const uint32_t sf = tmem_base + SF_COL0 + stage * SF_STAGE_COLS_NV;
+            const uint32_t ue8 = b_addr + kStageB;
+#pragma unroll
+            for (int blk = 0; blk < 12; ++blk)
+              tmem_cp_32x128b_warpx4(sf + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_nvf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc, sf + 12 * k,
+                       sf + 12 * k + 4, (kb > it.kbeg || k > 0) ? 1u : 0u);
+          } else if constexpr (kFp4) {
             // 6 scale blocks of this stage -> TMEM columns 4i of the stage's 24; MMA k (64 tokens)
             // reads word k/2 of A (columns 0/4) and B (8/16), byte pair (k%2)*2 of it
             const uint32_t sf = tmem_base + SF_COL0 + stage * SF_STAGE_COLS_FP4;
@@ -999,6 +1027,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     uint4* stg = reinterpret_cast<uint4*>(epi_stage_mem + ew * (EPI_STAGE_TOTAL / NUM_EPI_WARPS_FP8));
     const int rsub = lane >> 2;       // row within an 8-row group of the read-back
     const int csub = lane & 3;        // 16-byte chunk within a 64-byte row segment
+    // NVFP4: the product of the per-tensor global scales (1 where one is not given)
+    const float gscale = kNv ? (p.gscale_a ? __ldg(p.gscale_a) : 1.0f) * (p.gscale_b ? __ldg(p.gscale_b) : 1.0f) : 1.0f;
     int tcount = 0;
     for (int n = 0;; ++n) {
       const int slot = n % WORK_RING;
@@ -1040,7 +1070,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         const int r = 8 * j + rsub;
         return stg[r * 4 + (csub ^ ((r >> 1) & 3))];
       };
-      if (it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
+      if (!kNv && it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
         // TMEM accumulator -> packed 16-bit values in this warp's holding columns -> hand back
         const uint32_t hold = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + EPI_HOLD_COL0 + (ew >> 2) * 64;
 #pragma unroll 1
@@ -1082,6 +1112,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             tmem_ld_32x32b_x16(taddr + c * 16, r);
             tmem_ld_wait();
             if (c == 7) release_acc();
+            if constexpr (kNv) {   // per-tensor global scales multiply the whole product
+#pragma unroll
+              for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * gscale);
+            }
             stage4(make_uint4(r[0], r[1], r[2], r[3]), make_uint4(r[4], r[5], r[6], r[7]),
                    make_uint4(r[8], r[9], r[10], r[11]), make_uint4(r[12], r[13], r[14], r[15]));
           }
@@ -1157,6 +1191,15 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                 v[j].y += x.y;
                 v[j].z += x.z;
                 v[j].w += x.w;
+              }
+            }
+            if constexpr (kNv) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                v[j].x *= gscale;
+                v[j].y *= gscale;
+                v[j].z *= gscale;
+                v[j].w *= gscale;
               }
             }
 #pragma unroll
@@ -1435,6 +1478,45 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             break;
           }
           uint8_t* sS = stage_mem + size_t(stage) * kStageBytes + STAGE_A_BYTES + kStageB;
+          if constexpr (kNv) {
+            // four 64-token UE4M3 words per row/column, rearranged in place into 12 blocks: for each
+            // MMA k, A word k, then B word k for columns 0..127 and 128..255
+            uint32_t* sw = reinterpret_cast<uint32_t*>(sS);
+            uint32_t a[4][4], b[4][8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) a[k][j] = sw[k * BM + 32 * j + lane];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) b[k][j] = sw[4 * BM + k * BN + 32 * j + lane];
+            }
+            __syncwarp();  // every lane has read its words before any is overwritten
+            uint4* ue = reinterpret_cast<uint4*>(sS);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              ue[(3 * k) * 32 + lane] = make_uint4(a[k][0], a[k][1], a[k][2], a[k][3]);
+              ue[(3 * k + 1) * 32 + lane] = make_uint4(b[k][0], b[k][1], b[k][2], b[k][3]);
+              ue[(3 * k + 2) * 32 + lane] = make_uint4(b[k][4], b[k][5], b[k][6], b[k][7]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->sf_full[stage]);
+            // after the hand-off: a UE4M3 byte must not have its top bit set, and 0x7F is NaN
+            uint32_t bad = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) bad |= (a[k][j] & 0x80808080u) | (((a[k][j] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) bad |= (b[k][j] & 0x80808080u) | (((b[k][j] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u);
+            }
+            if (bad && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           if constexpr (kFp4) {
             // packed UE8M0 words, two per row/column; rearranged in place into the 6 TMEM blocks
             uint32_t* sw = reinterpret_cast<uint32_t*>(sS);
@@ -1582,11 +1664,11 @@ cudaError_t launch_plan(const PlanParams& p, const MapTemplates& t, cudaStream_t
   return cudaGetLastError();
 }
 
-template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false>
+template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false, bool kNv = false>
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
-  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG, kFp4>;
-  const size_t smem = main_smem_bytes(kPair, kFp8);
+  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG, kFp4, kNv>;
+  const size_t smem = main_smem_bytes(kPair, kFp8, kNv);
   // set on every launch: the attribute is per device and the call is cheap
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -1645,6 +1727,7 @@ cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const C
 
 cudaError_t launch_main_fp4(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s) {
+  if (p.nvfp4) return launch_main<true, false, true, true, false, true, true>(p, tmA, tmB, grid, s);
   return launch_main<true, false, true, true, false, true>(p, tmA, tmB, grid, s);
 }
 

@@ -287,6 +287,19 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// NVFP4 MMA (kind::mxf4nvf4, e2m1 x e2m1, K = 64 per instruction) with four UE4M3 scale factors per
+// row / column (one per 16 elements of K), all four bytes of a 32-bit TMEM scale column.
+__device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+          "r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -392,6 +405,13 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32
 // the scale factor ids (0 or 2) pick the byte pair of the 32-bit TMEM scale column.
 __host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N) {
   return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf4nvf4 with UE4M3 scales (scale format bit 23 = 0): A=B=E2M1
+// (bits 7-9, 10-12), both K-major, N>>3 at 17-22, M>>4 at 24-28; with scale_vec::4X each MMA uses
+// the whole 32-bit TMEM scale column (scale factor ids 0).
+__host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Scale-factor byte selector of the block-scaled instruction descriptor (A: bits 29-30, B: 4-5).

@@ -173,6 +173,27 @@ kgw_status kgw_wgrad_fp4_ue8m0(const kgw_wgrad_args* args, const int32_t* sfa_pa
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * NVFP4 variant: the block-scaled contract with scale blocks of 16 tokens and per-tensor global
+ * scales ("Grouped GEMM + WGrad (Unified)", sections "BF16 contract" -- sf_vec_size 16 -- and
+ * "Block-scaled contract": sfa/sfb plus global_scale_a / global_scale_b where the low-precision
+ * format requires them). a, b: e2m1 packed as in kgw_wgrad_fp4_ue8m0 (K-major A and B, tensor2d or
+ * ragged). sfa_packed: int32 [tokens_sum/64, hidden], sfb_packed: int32 [tokens_sum/64,
+ * intermediate]; byte j (least significant first) of word [w][r] is the unsigned E4M3 scale
+ * (UE4M3: 4 exponent bits with bias 7, 3 mantissa bits, no sign) of tokens 64w + 16j .. 64w + 16j + 15
+ * of row / column r. A byte with its top bit set, or 0x7F (NaN), is KGW_ERR_SCALES on the device.
+ * global_scale_a, global_scale_b: device pointers to one float each (NULL = 1), 4-byte aligned.
+ *
+ *     Wgrad[e][m][n] = global_scale_a * global_scale_b
+ *                      * sum over tokens k of expert e of (sa[k/16][m] * a[m][k]) * (sb[k/16][n] * b[k][n])
+ *
+ * accumulated in FP32 (the global product multiplies the FP32 sum before the output rounding).
+ * Counts: multiples of 256 (the pages' contract). Workspace: kgw_workspace_size with is_fp8 = 1.
+ */
+kgw_status kgw_wgrad_nvfp4(const kgw_wgrad_args* args, const int32_t* sfa_packed, const int32_t* sfb_packed,
+                           const float* global_scale_a, const float* global_scale_b, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
  * Block-scaled entries without the 256-token contract on the counts (an extension beyond the
  * pages' contract, like kgw_wgrad_bf16_unaligned). An expert's last pipeline stage may be partly
  * beyond its last token: it is read through a per-expert TMA descriptor whose token extent ends at

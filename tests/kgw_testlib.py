@@ -88,7 +88,9 @@ def run_gpu(w, x, device="cuda", status=None, workspace=None, outputs=None):
                          status_dev=status)
     if workspace is None:
         workspace = kgw.workspace_for(args, w.fp8 or w.fp4, device=device)
-    if w.fp4 and w.unaligned:
+    if w.fp4 and w.sf_format == "ue4m3_16":
+        kgw.kgw_wgrad_nvfp4(args, x.sfa, x.sfb, x.gsa, x.gsb, workspace)
+    elif w.fp4 and w.unaligned:
         kgw.kgw_wgrad_fp4_unaligned(args, x.sfa, x.sfb, workspace)
     elif w.fp8 and w.unaligned:
         kgw.kgw_wgrad_fp8_unaligned(args, x.sfa, x.sfb, 1 if w.sf_format == "ue8m0_32" else 0, workspace)
@@ -114,7 +116,9 @@ def oracle_full(w, x_cpu):
                                 sfa=None if x_cpu.sfa is None else x_cpu.sfa.numpy(),
                                 sfb=None if x_cpu.sfb is None else x_cpu.sfb.numpy(),
                                 c_init=c, accumulate=w.accumulate, a_major=w.a_major, b_major=w.b_major,
-                                sf_format=w.sf_format, fp4=w.fp4)
+                                sf_format=w.sf_format, fp4=w.fp4,
+                                global_scale_a=None if x_cpu.gsa is None else float(x_cpu.gsa[0]),
+                                global_scale_b=None if x_cpu.gsb is None else float(x_cpu.gsb[0]))
 
 
 def assert_close_to_oracle(w, got: np.ndarray, ref: np.ndarray, S: np.ndarray, c_init=None):
@@ -136,7 +140,7 @@ def check_full(w, label=None, device="cuda"):
     kgw = ensure_built()
     x_cpu = W.make_inputs(w, "cpu")
     x = W.Inputs(*[None if t is None else t.to(device) for t in
-                   (x_cpu.a, x_cpu.b, x_cpu.offsets, x_cpu.sfa, x_cpu.sfb, x_cpu.c)])
+                   (x_cpu.a, x_cpu.b, x_cpu.offsets, x_cpu.sfa, x_cpu.sfb, x_cpu.c, x_cpu.gsa, x_cpu.gsb)])
     status = torch.full((1,), -1, dtype=torch.int32, device=device)
     outs = run_gpu(w, x, device, status=status)
     torch.cuda.synchronize()
@@ -146,7 +150,9 @@ def check_full(w, label=None, device="cuda"):
     a_bits, b_bits = bits(x_cpu.a), bits(x_cpu.b)
     offsets = x_cpu.offsets.numpy()
     sf = dict(sfa=None if x_cpu.sfa is None else x_cpu.sfa.numpy(),
-              sfb=None if x_cpu.sfb is None else x_cpu.sfb.numpy())
+              sfb=None if x_cpu.sfb is None else x_cpu.sfb.numpy(),
+              global_scale_a=None if x_cpu.gsa is None else float(x_cpu.gsa[0]),
+              global_scale_b=None if x_cpu.gsb is None else float(x_cpu.gsb[0]))
     counts = np.asarray(w.counts)
     worst, checked, bad = 0.0, 0, []
     for e in range(w.num_experts):

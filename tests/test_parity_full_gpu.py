@@ -47,3 +47,7 @@ def test_full_fp4_blockscaled():
     """FP4 e2m1 operands with UE8M0 scales per 32 tokens, at the FP8 workload's shape."""
     check_full(W.fp4(), "fp4")
 
+
+def test_full_nvfp4():
+    """NVFP4 (UE4M3 scales per 16 tokens, FP32 global scales) at the FP8 workload's shape."""
+    check_full(W.nvfp4(), "nvfp4")

@@ -101,6 +101,13 @@ CASES = {
                            sf_format="ue8m0_32", input_order="ragged", out_dtype="bf16"),
     "fp4_ragged_split_k_f32": W.custom(2, 128, 256, [24576, 512], seed=116, fp4=True, b_major="k",
                                        sf_format="ue8m0_32", input_order="ragged"),
+    "nvfp4_bf16_out": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=117, fp4=True, b_major="k",
+                               sf_format="ue4m3_16", out_dtype="bf16"),
+    "nvfp4_split_k_f32_accumulate": W.custom(3, 128, 256, [32768, 0, 256], seed=118, fp4=True, b_major="k",
+                                             sf_format="ue4m3_16", accumulate=True),
+    "nvfp4_ragged_discrete_f16": W.custom(3, 256, 256, [1024, 512, 256], seed=119, fp4=True, b_major="k",
+                                          sf_format="ue4m3_16", input_order="ragged", output_mode="discrete",
+                                          out_dtype="f16"),
     "fp4_discrete_f16": W.custom(3, 256, 256, [1024, 512, 256], seed=113, fp4=True, b_major="k",
                                  sf_format="ue8m0_32", out_dtype="f16", output_mode="discrete"),
 }
@@ -257,7 +264,7 @@ def test_fp4_rejects_unsupported_layouts():
         assert kgw.kgw_wgrad_fp4_ue8m0(args, x.sfa, x.sfb, ws, check=False) == kgw.KGW_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("kind", ["fp8_f32_not_pow2", "fp8_ue8m0_nan", "fp4_ue8m0_nan"])
+@pytest.mark.parametrize("kind", ["fp8_f32_not_pow2", "fp8_ue8m0_nan", "fp4_ue8m0_nan", "nvfp4_sign_bit"])
 def test_bad_scales_are_reported(kind):
     """A scale that is not a power of two (FP32 scales) or a UE8M0 byte 0xFF (NaN) anywhere in
     the scale tensors is reported as KGW_ERR_SCALES; clean scales report KGW_OK."""
@@ -266,8 +273,11 @@ def test_bad_scales_are_reported(kind):
         w = W.custom(3, 256, 512, [512, 256, 768], seed=140, fp8=True, out_dtype="bf16")
     elif kind == "fp8_ue8m0_nan":
         w = W.custom(3, 256, 512, [512, 256, 768], seed=141, fp8=True, sf_format="ue8m0_32", out_dtype="bf16")
-    else:
+    elif kind == "fp4_ue8m0_nan":
         w = W.custom(3, 256, 512, [512, 256, 768], seed=142, fp4=True, b_major="k", sf_format="ue8m0_32",
+                     out_dtype="bf16")
+    else:
+        w = W.custom(3, 256, 512, [512, 256, 768], seed=143, fp4=True, b_major="k", sf_format="ue4m3_16",
                      out_dtype="bf16")
     x = W.make_inputs(w, DEV)
     status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
@@ -282,7 +292,9 @@ def test_bad_scales_are_reported(kind):
     else:
         words = sfb.view(torch.int32)
         words[-1, 300] = int(np.array([0x7FFF7F7F], dtype=np.uint32).view(np.int32)[0])
-    x2 = W.Inputs(x.a, x.b, x.offsets, x.sfa, sfb, x.c)
+    if kind == "nvfp4_sign_bit":
+        words[-1, 300] = int(np.array([0x38B83838], dtype=np.uint32).view(np.int32)[0])   # 0xB8: sign bit set
+    x2 = W.Inputs(x.a, x.b, x.offsets, x.sfa, sfb, x.c, x.gsa, x.gsb)
     status.fill_(-1)
     run_gpu(w, x2, DEV, status=status)
     torch.cuda.synchronize()
