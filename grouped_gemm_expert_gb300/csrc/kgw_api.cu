@@ -352,8 +352,13 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
   P.mp.nvfp4 = nvfp4;
   P.mp.gscale_a = gscale_a;
   P.mp.gscale_b = gscale_b;
+  // FP8 with FP32 scales: a device check of every scale decides whether the FP8 kernel uses the
+  // block-scaled MMA (all powers of two) or its per-block promotion path
+  const bool general = fp8 && !fp4 && !sf_packed;
+  P.mp.general_dispatch = general;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kgw::launch_plan(P.pp, P.tpl, s) != cudaSuccess) return KGW_ERR_CUDA;
+  if (general && a->tokens_sum > 0 && kgw::launch_scale_check(P.mp, 4 * P.grid, s) != cudaSuccess) return KGW_ERR_CUDA;
   cudaError_t e = fp4 ? kgw::launch_main_fp4(P.mp, P.tmA, P.tmB, P.grid, s)
                  : fp8 ? kgw::launch_main_fp8(P.mp, P.tmA, P.tmB, P.grid, s)
                        : kgw::launch_main_bf16(P.mp, P.tmA, P.tmB, P.grid, s);

@@ -88,7 +88,9 @@ struct PlanHeader {
   int32_t slots_used;     // FP32 partial tiles in use
   int32_t counters_used;  // split tiles (one arrival counter each)
   int32_t item_counter;   // dynamic scheduler: next item to hand out
-  int32_t pad[58];
+  int32_t general_scales; // FP8 with FP32 scales: some scale is not a power of two (promotion path)
+  int32_t scale_rows;     // block-scaled entries: scale rows of the call (sum over experts of ceil(n_e/128))
+  int32_t pad[56];
 };
 static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte block");
 
@@ -195,6 +197,8 @@ struct MainParams {
   const float* sfb;             // FP8: [tokens_sum/128, I]
   int32_t sf_packed;            // FP8 scales given as packed UE8M0 words (4 x 32-token blocks)
   int32_t nvfp4;                // FP4 with UE4M3 scales per 16 tokens (kind::mxf4nvf4, scale_vec::4X)
+  int32_t general_dispatch;     // FP8 with FP32 scales: the FP8 kernel takes its promotion path when
+                                // the scale check found a scale that is not a power of two
   const float* gscale_a;        // NVFP4: per-tensor global scales (device, one float each; null = 1)
   const float* gscale_b;
   int32_t* status_dev;
@@ -212,6 +216,9 @@ cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const C
                             cudaStream_t s);
 cudaError_t launch_main_fp4(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s);
+// FP8 with FP32 scales: a check of every scale of the call, between the plan and the FP8 kernel
+// (sets general_scales: the FP8 kernel then takes its per-block promotion path).
+cudaError_t launch_scale_check(const MainParams& p, int grid, cudaStream_t s);
 // M-grouped GEMM (rows of A grouped by expert, each group with its own B): schedule + main kernel.
 cudaError_t launch_plan_mgrouped(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,

@@ -119,6 +119,8 @@ __global__ void __launch_bounds__(PLAN_THREADS)
       hdr->item_counter = 0;
       hdr->slots_used = 0;
       hdr->counters_used = 0;
+      hdr->general_scales = 0;
+      hdr->scale_rows = 0;
       if (p.status_dev) *p.status_dev = code;
     }
     return;
@@ -207,6 +209,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
       scale_row[e] = static_cast<int32_t>(run);
       run += blocks(e);
     }
+    if (tid == 0) hdr->scale_rows = static_cast<int32_t>(nblk);
   }
 
   // 3. split-K chunk: items no longer than W/(2*grid) k-iterations (at least MIN_SPLIT_KITERS),
@@ -299,6 +302,7 @@ __global__ void __launch_bounds__(PLAN_THREADS)
     hdr->slots_used = static_cast<int32_t>(slots_total);
     hdr->counters_used = static_cast<int32_t>(cnt_total);
     hdr->item_counter = 0;
+    hdr->general_scales = 0;
     if (p.status_dev) *p.status_dev = KGW_OK;
   }
 }
@@ -643,6 +647,405 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
   return reinterpret_cast<char*>(p.out) + ((static_cast<size_t>(it.e) * p.H + r) * p.I + it.n0) * esz;
 }
 
+// =============================================================================================
+// FP8 with general FP32 scales
+// =============================================================================================
+
+// Checks every FP32 scale of the call once the plan is complete: a scale that is not a positive
+// power of two UE8M0 can hold sets general_scales (the promotion kernel then runs the call); a NaN
+// or infinite scale is KGW_ERR_SCALES.
+__global__ void __launch_bounds__(256) scale_check_kernel(const __grid_constant__ MainParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
+  if (hdr->error != 0) return;
+  // 16-byte loads (rows of hidden and of intermediate are multiples of 4 floats), four in flight
+  // per thread, so the check costs a couple of memory round trips rather than one per element
+  const int64_t na = int64_t(hdr->scale_rows) * p.H / 4, nb = int64_t(hdr->scale_rows) * p.I / 4;
+  const uint4* va = reinterpret_cast<const uint4*>(p.sfa);
+  const uint4* vb = reinterpret_cast<const uint4*>(p.sfb);
+  uint32_t general = 0, bad = 0;
+  auto check = [&](uint32_t b) {
+    const uint32_t e = (b >> 23) & 0xFFu, m = b & 0x7FFFFFu;
+    bad |= e == 255u;
+    general |= (e != 255u) & (((b >> 31) != 0u) | (e == 0u ? m != 0x400000u : m != 0u));
+  };
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i0 < na + nb; i0 += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      v[u] = i < na ? __ldg(va + i) : (i < na + nb ? __ldg(vb + (i - na)) : make_uint4(0x3F800000u, 0x3F800000u, 0x3F800000u, 0x3F800000u));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      check(v[u].x);
+      check(v[u].y);
+      check(v[u].z);
+      check(v[u].w);
+    }
+  }
+  if (__any_sync(0xffffffffu, general) && (threadIdx.x & 31) == 0) atomicOr(&hdr->general_scales, 1);
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
+}
+
+// Promotion path: FP8 (e4m3) K-grouped wgrad with arbitrary FP32 scales per 128-token block
+// ("05 · Grouped GEMM 与 Expert 计算", section 3: x_scales float, per-block 1x128 scaling). A scale
+// that is not a power of two cannot be folded into the block-scaled MMA exactly, so each block's
+// unscaled partial sum P = sum over its 128 tokens of a*b runs on the tensor cores
+// (tcgen05.mma kind::f8f6f4, FP32 in TMEM) and eight warps add sa[m]*sb[n]*P to FP32 running sums
+// held in registers: the per-block promotion of the pages' FP8 GEMMs. Tiles are 128 x 128 (two
+// per 128 x 256 plan item, so the running sums fit the registers) with P double-buffered in TMEM;
+// the stage ring is the block-scaled kernel's (A 128 rows, B the 256-column box of K-major B or
+// the tile's 128 columns of N-major B, and the block's 128 + 128 scales). Split-K items of the plan
+// are merged: split 0 covers the expert's whole token range, the others are skipped.
+// Roles: warp 0 TMA producer, warp 1 MMA + TMEM owner, warps 2..9 promotion and output, warp 11
+// scheduler (warp 10 idle).
+constexpr int PR_TN = 128;
+constexpr int PR_STAGES = 4;
+constexpr uint32_t PR_SF_BYTES = 1024;                        // 128 FP32 of A + 128 FP32 of B
+constexpr uint32_t PR_STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES + PR_SF_BYTES;   // 49 KiB
+constexpr int PR_WARPS = 8;
+
+struct PromoteCtl {
+  uint64_t full[PR_STAGES];
+  uint64_t empty[PR_STAGES];
+  uint64_t pfull[2];
+  uint64_t pempty[2];
+  uint64_t wfull[WORK_RING];
+  uint64_t wempty[WORK_RING];
+  uint64_t sched_go;
+  uint64_t mma_done;
+  Item work[WORK_RING];
+  uint32_t tmem_base;
+  int32_t abort_flag;
+};
+
+size_t promote_smem_bytes() { return size_t(PR_STAGES) * PR_STAGE_BYTES + EPI_STAGE_TOTAL + 1024 + sizeof(PromoteCtl) + 64; }
+
+// Runs inside the FP8 kernel (same launch, same dynamic shared memory, which is at least
+// promote_smem_bytes()) once the scale check has found a scale that is not a power of two.
+template <bool kAK, bool kBK>
+__device__ __forceinline__ void promote_body(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                             uint8_t* smem_raw) {
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
+  const int total_items = 2 * hdr->total_items;   // two 128-column halves per plan item
+  if (total_items == 0) return;
+  constexpr int bk = BK_FP8;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_mem = base;
+  uint8_t* epi_stage_mem = base + size_t(PR_STAGES) * PR_STAGE_BYTES;
+  PromoteCtl* ctl = reinterpret_cast<PromoteCtl*>(epi_stage_mem + EPI_STAGE_TOTAL);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t* item_counter = const_cast<int32_t*>(&hdr->item_counter);
+  volatile int* abort_flag = &ctl->abort_flag;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PR_STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1 + PR_WARPS);   // the MMA commit and every promotion warp
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&ctl->pfull[b], 1);
+      mbar_init(&ctl->pempty[b], PR_WARPS);
+    }
+    for (int w = 0; w < WORK_RING; ++w) {
+      mbar_init(&ctl->wfull[w], 1);
+      mbar_init(&ctl->wempty[w], 2 + PR_WARPS);    // producer, MMA thread, promotion warps
+    }
+    mbar_init(&ctl->sched_go, 1);
+    mbar_init(&ctl->mma_done, 1);
+    ctl->abort_flag = 0;
+    fence_mbarrier_init();
+    if (p.tokens_sum > 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+  // expert k-iterations of a split-0 item (the whole expert), 0 for the other splits
+  auto kiters = [&](const Item& it) { return it.split > 0 ? 0 : static_cast<int>((it.n_e + bk - 1) / bk); };
+  auto read_item = [&](int n, Item& it) {
+    const int slot = n % WORK_RING;
+    const bool ok = wait_bounded(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
+    it = ctl->work[slot];
+    return ok;
+  };
+
+  if (warp == 0) {
+    // ======================= TMA producer =======================
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    for (int n = 0;; ++n) {
+      Item it;
+      const bool okw = read_item(n, it);
+      if (!__all_sync(0xffffffffu, okw)) break;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl->wempty[n % WORK_RING]);
+        if (it.e >= 0) mbar_arrive(&ctl->sched_go);
+      }
+      if (it.e < 0) break;
+      const int kit = kiters(it);
+      const CUtensorMap* amap = &tmA;
+      const CUtensorMap* bmap = &tmB;
+      if ((kAK && p.ragged) || p.tail_a) {
+        amap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps + size_t(it.e) * 128);
+        if (lane == 0 && kit > 0) fence_tmap_acquire(amap);
+      }
+      if ((kBK && p.ragged) || p.tail_b) {
+        bmap = reinterpret_cast<const CUtensorMap*>(p.ws + p.L.tmaps_b + size_t(it.e) * 128);
+        if (lane == 0 && kit > 0) fence_tmap_acquire(bmap);
+      }
+      const int n0_tile = it.n0 - it.m1 * PR_TN;   // the plan item's 256-column tile
+      for (int kb = 0; kb < kit; ++kb) {
+        bool ok2 = true;
+        if (lane == 0) {
+          ok2 = wait_bounded(&ctl->empty[stage], phase ^ 1, abort_flag, p.timeout_ns);
+          if (ok2) mbar_arrive_expect_tx(&ctl->full[stage], STAGE_A_BYTES + (kBK ? STAGE_B_BYTES : STAGE_B_BYTES / 2) + PR_SF_BYTES);
+        }
+        ok2 = __shfl_sync(0xffffffffu, ok2, 0);
+        if (!ok2) break;
+        uint8_t* sA = stage_mem + size_t(stage) * PR_STAGE_BYTES;
+        uint8_t* sB = sA + STAGE_A_BYTES;
+        uint8_t* sS = sB + STAGE_B_BYTES;
+        const int64_t tok = it.begin + int64_t(kb) * bk;
+        if (lane == 0) {
+          const int64_t kblk = int64_t(it.srow) + kb;   // the expert's block kb
+          bulk_load(sS, p.sfa + kblk * p.H + it.m0, BM * 4, &ctl->full[stage]);
+          bulk_load(sS + BM * 4, p.sfb + kblk * p.I + it.n0, PR_TN * 4, &ctl->full[stage]);
+          const int32_t kx = p.ragged ? kb * bk : static_cast<int32_t>(tok);
+          if constexpr (kAK) tma_load_2d(sA, amap, &ctl->full[stage], kx, it.m0);
+          else tma_load_2d(sA, amap, &ctl->full[stage], it.m0, static_cast<int32_t>(tok));
+          // K-major B: the plan tile's 256-row box (the MMA reads this half's 128 rows);
+          // N-major B: this half's 128 columns (one 128-byte atom)
+          if constexpr (kBK) tma_load_2d(sB, bmap, &ctl->full[stage], kx, n0_tile);
+          else tma_load_2d(sB, bmap, &ctl->full[stage], it.n0, static_cast<int32_t>(tok));
+        }
+        ++issued;
+        if (++stage == PR_STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+    }
+    if (lane == 0) {  // the last stages land before exit
+      int s = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < PR_STAGES && i < issued; ++i) {
+        if (--s < 0) {
+          s = PR_STAGES - 1;
+          ph ^= 1;
+        }
+        int dummy = 0;
+        wait_bounded(&ctl->full[s], ph, &dummy, p.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =======================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t blk = 0;
+      constexpr uint32_t a_mn = kAK ? 0u : 1u, b_mn = kBK ? 0u : 1u;
+      const uint32_t idesc = idesc_f8f6f4(BM, PR_TN, a_mn, b_mn);
+      const uint64_t a_tmpl = kAK ? sdesc_sw128(0, 16, 1024) : sdesc_sw128(0, uint32_t(bk) * 128u, 1024);
+      const uint64_t b_tmpl = kBK ? sdesc_sw128(0, 16, 1024) : sdesc_sw128(0, uint32_t(bk) * 128u, 1024);
+      constexpr uint32_t a_step = (kAK ? 32u : 4096u) >> 4;
+      constexpr uint32_t b_step = (kBK ? 32u : 4096u) >> 4;
+      auto desc = [](uint64_t tmpl, uint32_t addr, uint32_t step, int k) {
+        return tmpl + static_cast<uint64_t>(((addr & 0x3FFFFu) >> 4) + k * step);
+      };
+      for (int n = 0;; ++n) {
+        Item it;
+        if (!read_item(n, it)) break;
+        mbar_arrive(&ctl->wempty[n % WORK_RING]);
+        if (it.e < 0) break;
+        const int kit = kiters(it);
+        bool ok = true;
+        for (int kb = 0; kb < kit; ++kb, ++blk) {
+          const uint32_t pb = blk & 1;
+          if (!wait_bounded(&ctl->pempty[pb], ((blk >> 1) & 1) ^ 1, abort_flag, p.timeout_ns) ||
+              !wait_bounded(&ctl->full[stage], phase, abort_flag, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * PR_STAGE_BYTES);
+          const uint32_t b_addr = a_addr + STAGE_A_BYTES + (kBK ? static_cast<uint32_t>(it.m1) * (STAGE_B_BYTES / 2) : 0u);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f8f6f4(tmem_base + pb * PR_TN, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc,
+                       k > 0 ? 1u : 0u);
+          mma_commit(&ctl->empty[stage]);
+          mma_commit(&ctl->pfull[pb]);
+          if (++stage == PR_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      mma_commit(&ctl->mma_done);
+      int dummy = 0;
+      wait_bounded(&ctl->mma_done, 0, &dummy, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + PR_WARPS) {
+    // ======================= promotion and output (warps 2..9) =======================
+    const int q = warp & 3;                    // TMEM lane quadrant: rows 32q .. 32q+31
+    const int h = (warp - EPI_WARP0) >> 2;     // columns 64h .. 64h+63 of the 128-column tile
+    const int row = q * 32 + lane;
+    uint4* stg = reinterpret_cast<uint4*>(epi_stage_mem + (warp - EPI_WARP0) * (EPI_STAGE_TOTAL / PR_WARPS));
+    const int rsub = lane >> 2, csub = lane & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t blk = 0;
+    for (int n = 0;; ++n) {
+      Item it;
+      const bool okw = read_item(n, it);
+      if (!__all_sync(0xffffffffu, okw)) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->wempty[n % WORK_RING]);
+      if (it.e < 0) break;
+      if (it.split > 0) continue;
+      const int esz = p.out_bf16 ? 2 : 4;
+      char* obase = out_row_ptr<false>(p, it, q * 32) + size_t(64 * h) * esz;
+      const size_t ostride = size_t(p.I) * esz;
+      const int kit = kiters(it);
+      if (kit == 0) {  // empty expert, overwrite mode: zeros
+#pragma unroll 1
+        for (int r = 0; r < 32; ++r)
+          for (int off = lane * 16; off < 64 * esz; off += 32 * 16)
+            *reinterpret_cast<uint4*>(obase + r * ostride + off) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      float R[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) R[j] = 0.f;
+      bool ok = true;
+      for (int kb = 0; kb < kit; ++kb, ++blk) {
+        const uint32_t pb = blk & 1;
+        const bool okp = wait_bounded(&ctl->pfull[pb], (blk >> 1) & 1, abort_flag, p.timeout_ns) &&
+                         wait_bounded(&ctl->full[stage], phase, abort_flag, p.timeout_ns);  // scales visible
+        if (!__all_sync(0xffffffffu, okp)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float* sS = reinterpret_cast<const float*>(stage_mem + size_t(stage) * PR_STAGE_BYTES + STAGE_A_BYTES + STAGE_B_BYTES);
+        const float sa = sS[row];
+        const float4* sb = reinterpret_cast<const float4*>(sS + BM + 64 * h);
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * PR_TN + 64 * h;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t P[32];
+          tmem_ld_32x32b_x32(taddr + 32 * c, P);
+          tmem_ld_wait();
+          if (c == 1) {  // both halves of this warp's partial are in registers: hand P back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->pempty[pb]);
+          }
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 b4 = sb[8 * c + j4];
+            const int j = 32 * c + 4 * j4;
+            R[j] = fmaf(__uint_as_float(P[4 * j4]), sa * b4.x, R[j]);
+            R[j + 1] = fmaf(__uint_as_float(P[4 * j4 + 1]), sa * b4.y, R[j + 1]);
+            R[j + 2] = fmaf(__uint_as_float(P[4 * j4 + 2]), sa * b4.z, R[j + 2]);
+            R[j + 3] = fmaf(__uint_as_float(P[4 * j4 + 3]), sa * b4.w, R[j + 3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->empty[stage]);   // this warp is done with the stage's scales
+        if (++stage == PR_STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      // output: 4 rounds of 16 columns through the per-warp staging, 4 lanes per 64-byte row segment
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          stg[lane * 4 + (i ^ sw)] = make_uint4(__float_as_uint(R[16 * c + 4 * i]), __float_as_uint(R[16 * c + 4 * i + 1]),
+                                                __float_as_uint(R[16 * c + 4 * i + 2]), __float_as_uint(R[16 * c + 4 * i + 3]));
+        __syncwarp();
+        char* cbase = obase + size_t(c * 16 + csub * 4) * esz;
+        uint4 old[4];
+        if (p.accumulate) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) old[j] = load_old4(p, cbase + (8 * j + rsub) * ostride);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 8 * j + rsub;
+          const uint4 u = stg[r * 4 + (csub ^ ((r >> 1) & 3))];
+          emit4(p, cbase + r * ostride,
+                make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)), old[j]);
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp == SCHED_WARP_FP8) {
+    // ======================= scheduler =======================
+    // Claims the next half-tile one ahead of the producer (item 2i + h is half h of plan item i).
+    if (lane == 0) {
+      int cur = atomicAdd(item_counter, 1);
+      for (int n = 0;; ++n) {
+        const int slot = n % WORK_RING;
+        Item it;
+        if (cur < total_items) {
+          it = decode_item<false>(p, cur >> 1, bk);
+          it.m1 = cur & 1;              // the 128-column half
+          it.n0 += (cur & 1) * PR_TN;
+        } else {
+          it = Item{};
+          it.e = -1;
+        }
+        if (!wait_bounded(&ctl->wempty[slot], ((n / WORK_RING) & 1) ^ 1, abort_flag, p.timeout_ns)) break;
+        ctl->work[slot] = it;
+        mbar_arrive(&ctl->wfull[slot]);
+        if (it.e < 0) break;
+        if (!wait_bounded(&ctl->sched_go, n & 1, abort_flag, p.timeout_ns)) break;
+        cur = atomicAdd(item_counter, 1);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 256);
+  }
+  if (threadIdx.x == 0 && ctl->abort_flag && p.status_dev) atomicExch(p.status_dev, KGW_ERR_TIMEOUT);
+}
+
+cudaError_t launch_scale_check(const MainParams& p, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, scale_check_kernel, p);
+}
+
 // One persistent kernel, two shapes:
 //  - kPair = false: one CTA owns a 128 x 256 output tile (BF16 or FP8).
 //  - kPair = true : a cluster of two CTAs owns a 256 x 256 tile (BF16). Each CTA loads its own
@@ -671,9 +1074,16 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
   const int bk = kFp4 ? BK_FP4 : (kFp8 ? BK_FP8 : BK_BF16);
-  pdl_wait();  // the plan of this call is complete and visible
+  pdl_wait();  // the plan of this call (and any scale check before it) is complete and visible
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
   if (hdr->error != 0) return;  // offsets/pointers rejected by the plan: write nothing
+  if constexpr (kFp8 && !kFp4 && !kMG && !kPair) {
+    // FP32 scales of which some is not a power of two: the per-block promotion path runs the call
+    if (p.general_dispatch && hdr->general_scales) {
+      promote_body<kAK, kBK>(p, tmA, tmB, smem_raw);
+      return;
+    }
+  }
   const int total_items = hdr->total_items;
   if (total_items == 0) return;
 
@@ -1648,6 +2058,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   if (threadIdx.x == 0 && ctl->abort_flag && p.status_dev) atomicExch(p.status_dev, KGW_ERR_TIMEOUT);
 }
 
+
+
 // =============================================================================================
 // Launchers
 // =============================================================================================
@@ -1668,7 +2080,9 @@ template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
   auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG, kFp4, kNv>;
-  const size_t smem = main_smem_bytes(kPair, kFp8, kNv);
+  size_t smem = main_smem_bytes(kPair, kFp8, kNv);
+  // the K-grouped FP8 kernel also hosts the promotion path, which lays out the same memory its own way
+  if (kFp8 && !kFp4 && !kMG && !kPair && promote_smem_bytes() > smem) smem = promote_smem_bytes();
   // set on every launch: the attribute is per device and the call is cheap
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;

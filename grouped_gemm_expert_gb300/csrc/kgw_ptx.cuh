@@ -300,6 +300,17 @@ __device__ __forceinline__ void mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// FP8 MMA without block scaling (kind::f8f6f4): D[tmem] (+)= A * B, FP32 accumulation.
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -412,6 +423,12 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N) {
 // the whole 32-bit TMEM scale column (scale factor ids 0).
 __host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t M, uint32_t N) {
   return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4: D=F32 (bits 4-5 = 1), A=B=E4M3 (format 0 at bits 7-9 and
+// 10-12), A / B MN-major (bits 15 / 16), N>>3 at 17-22, M>>4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t M, uint32_t N, uint32_t a_mn_major, uint32_t b_mn_major) {
+  return (1u << 4) | (a_mn_major << 15) | (b_mn_major << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Scale-factor byte selector of the block-scaled instruction descriptor (A: bits 29-30, B: 4-5).

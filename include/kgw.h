@@ -49,9 +49,10 @@ typedef enum kgw_status {
   KGW_ERR_WORKSPACE = 8,     /* workspace null, misaligned or smaller than the minimum */
   KGW_ERR_OUT_PTRS = 9,      /* device-detected: an out_ptrs[e] is null or not 16-byte aligned */
   KGW_ERR_SCRATCH_LIMIT = 10, /* kgw_wgrad_bf16_noalloc: the call exceeds its static scratch limits */
-  KGW_ERR_SCALES = 11        /* device-detected: an FP8 scale is not a positive power of two in
-                                [2^-127, 2^127], or a packed UE8M0 byte is 0xFF (the output of that
-                                call is meaningless) */
+  KGW_ERR_SCALES = 11        /* device-detected: an FP32 scale is NaN or infinite, a packed UE8M0
+                                byte is 0xFF, a UE4M3 byte has its top bit set or is 0x7F, or (the
+                                M-grouped FP8 entry) an FP32 scale is not a power of two; the output
+                                of that call is meaningless */
 } kgw_status;
 
 /* Storage order of an operand ("Grouped GEMM + WGrad (Unified)", section "BF16 contract"). */
@@ -137,8 +138,13 @@ kgw_status kgw_wgrad_bf16_unaligned(const kgw_wgrad_args* args, void* workspace,
  * contract"). a, b: float8 e4m3 (the "fn" encoding) in the same logical layouts as the BF16
  * entry. sfa: float32 [tokens_sum/128, hidden], sfb: float32 [tokens_sum/128, intermediate]:
  * sfa[kb][m] scales A[m, 128*kb : 128*kb+128] and sfb[kb][n] scales B[128*kb : 128*kb+128, n]
- * (token blocks are global, also in ragged order). Every scale must be a power of two in
- * [2^-127, 2^127]; the product is accumulated in FP32 with the scales applied per block.
+ * (token blocks are global, also in ragged order). Any finite FP32 scale is accepted ("05 · ...",
+ * section 3: x_scales float): when every scale of the call is a power of two in [2^-127, 2^127]
+ * the scales are exact UE8M0 factors of the block-scaled MMA; otherwise each 128-token block's
+ * unscaled partial product is formed on the tensor cores and sa*sb*partial is added to FP32 running
+ * sums on the CUDA cores (the per-block promotion of the pages' FP8 GEMMs). A device-side check of
+ * the scales chooses between the two, so the call stays asynchronous and capturable. A NaN or
+ * infinite scale is KGW_ERR_SCALES. The product is accumulated in FP32 either way.
  */
 kgw_status kgw_wgrad_fp8_blockscaled(const kgw_wgrad_args* args, const float* sfa, const float* sfb,
                                      void* workspace, size_t workspace_bytes, void* stream);

@@ -262,6 +262,7 @@ def decode_scales(sf, sf_format: str):
         return unpack_ue8m0_32(sf), 32
     if sf_format == "ue4m3_16":
         return unpack_ue4m3_16(sf), 16
+    # FP32 scales per 128 tokens ("f32_128": powers of two; "f32_any": any finite value)
     return np.asarray(sf, dtype=np.float64), SCALE_BLOCK
 
 

@@ -945,3 +945,38 @@ def test_nvfp4_brute_force_with_global_scales():
     got2, _ = O.wgrad_from_storage(pa, pb, offs, H, I, fp4=True, b_major="k", sf_format="ue4m3_16",
                                    sfa=pack(sa_codes), sfb=pack(sb_codes), global_scale_a=2 * ga, global_scale_b=gb)
     assert np.array_equal(got2, 2 * got)
+
+
+# ------------------------------------------------------------------------------------------
+# General FP32 scales ("05 · Grouped GEMM 与 Expert 计算", section 3: x_scales float)
+# ------------------------------------------------------------------------------------------
+
+def test_general_fp32_scale_quantiser_round_trip():
+    g = torch.Generator().manual_seed(9)
+    x = torch.randn(16, 512, generator=g) * 7
+    q, s = W.quantize_e4m3_fp32_blocks(x, token_axis=1)
+    s = s.numpy()
+    mant, _ = np.frexp(s)
+    assert np.mean(mant != 0.5) > 0.9                       # not powers of two
+    dec = O.e4m3_to_f64(e4m3_bits(q))
+    assert np.all(np.abs(dec) <= 448) and np.all(np.isfinite(dec))
+    recon = O.apply_scales_rows(dec, s, 128)
+    err = np.abs(recon - x.numpy().astype(np.float64))
+    assert np.all(err <= 2.0 ** -4 * np.abs(x.numpy()) + np.repeat(s.T, 128, axis=1) * 2.0 ** -10)
+
+
+def test_fp8_brute_force_with_general_fp32_scales():
+    rng = np.random.default_rng(45)
+    counts = [128, 256]
+    T, H, I = 384, 2, 3
+    codes_a = rng.integers(0, 126, size=(H, T)).astype(np.uint8)
+    codes_b = rng.integers(0, 126, size=(T, I)).astype(np.uint8)
+    sa = rng.uniform(0.01, 3.0, size=(T // 128, H)).astype(np.float32)
+    sb = (rng.uniform(-2.0, 2.0, size=(T // 128, I))).astype(np.float32)   # negative and fractional scales
+    offs = np.cumsum(counts).astype(np.int32)
+    got, S = O.wgrad_from_storage(codes_a, codes_b, offs, H, I, fp8=True, sfa=sa, sfb=sb, sf_format="f32_any")
+    exact = _fp8_brute(codes_a, codes_b, sa, sb, counts)
+    for e in range(2):
+        for m in range(H):
+            for n in range(I):
+                assert abs(Fraction(got[e, m, n]) - exact[e][m][n]) <= Fraction(1e-12) * Fraction(S[e, m, n]) + Fraction(1e-300)

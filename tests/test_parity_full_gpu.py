@@ -51,3 +51,8 @@ def test_full_fp4_blockscaled():
 def test_full_nvfp4():
     """NVFP4 (UE4M3 scales per 16 tokens, FP32 global scales) at the FP8 workload's shape."""
     check_full(W.nvfp4(), "nvfp4")
+
+
+def test_full_fp8_general_fp32_scales():
+    """FP8 with FP32 scales amax/448 (not powers of two): the promotion path at full size."""
+    check_full(W.fp8_fp32(), "fp8 general FP32 scales")

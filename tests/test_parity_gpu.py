@@ -101,6 +101,14 @@ CASES = {
                            sf_format="ue8m0_32", input_order="ragged", out_dtype="bf16"),
     "fp4_ragged_split_k_f32": W.custom(2, 128, 256, [24576, 512], seed=116, fp4=True, b_major="k",
                                        sf_format="ue8m0_32", input_order="ragged"),
+    "fp8_general_scales_bf16": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=120, fp8=True, sf_format="f32_any",
+                                        out_dtype="bf16"),
+    "fp8_general_mn_a_k_b_accumulate_f32": W.custom(3, 256, 768, [256, 1280, 512], seed=121, fp8=True,
+                                                    sf_format="f32_any", a_major="mn", b_major="k", accumulate=True),
+    "fp8_general_ragged_discrete_f16": W.custom(3, 384, 512, [768, 256, 0], seed=122, fp8=True, sf_format="f32_any",
+                                                input_order="ragged", output_mode="discrete", out_dtype="f16"),
+    "fp8_general_long_expert_split_by_plan": W.custom(2, 128, 256, [32768, 256], seed=123, fp8=True,
+                                                      sf_format="f32_any", accumulate=True, out_dtype="bf16"),
     "nvfp4_bf16_out": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=117, fp4=True, b_major="k",
                                sf_format="ue4m3_16", out_dtype="bf16"),
     "nvfp4_split_k_f32_accumulate": W.custom(3, 128, 256, [32768, 0, 256], seed=118, fp4=True, b_major="k",
@@ -264,12 +272,12 @@ def test_fp4_rejects_unsupported_layouts():
         assert kgw.kgw_wgrad_fp4_ue8m0(args, x.sfa, x.sfb, ws, check=False) == kgw.KGW_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("kind", ["fp8_f32_not_pow2", "fp8_ue8m0_nan", "fp4_ue8m0_nan", "nvfp4_sign_bit"])
+@pytest.mark.parametrize("kind", ["fp8_f32_nan", "fp8_ue8m0_nan", "fp4_ue8m0_nan", "nvfp4_sign_bit"])
 def test_bad_scales_are_reported(kind):
-    """A scale that is not a power of two (FP32 scales) or a UE8M0 byte 0xFF (NaN) anywhere in
-    the scale tensors is reported as KGW_ERR_SCALES; clean scales report KGW_OK."""
+    """A NaN FP32 scale, a UE8M0 byte 0xFF (NaN) or an invalid UE4M3 byte anywhere in the scale
+    tensors is reported as KGW_ERR_SCALES; clean scales report KGW_OK."""
     kgw = ensure_built()
-    if kind == "fp8_f32_not_pow2":
+    if kind == "fp8_f32_nan":
         w = W.custom(3, 256, 512, [512, 256, 768], seed=140, fp8=True, out_dtype="bf16")
     elif kind == "fp8_ue8m0_nan":
         w = W.custom(3, 256, 512, [512, 256, 768], seed=141, fp8=True, sf_format="ue8m0_32", out_dtype="bf16")
@@ -287,8 +295,8 @@ def test_bad_scales_are_reported(kind):
     # one bad entry, in B's scales of the last expert's last 128-token block, a column in the
     # second 128-column half of its n-tile, one byte that is not byte 0
     sfb = x.sfb.clone()
-    if kind == "fp8_f32_not_pow2":
-        sfb[-1, 300] = 3.0
+    if kind == "fp8_f32_nan":
+        sfb[-1, 300] = float("nan")
     else:
         words = sfb.view(torch.int32)
         words[-1, 300] = int(np.array([0x7FFF7F7F], dtype=np.uint32).view(np.int32)[0])
@@ -299,3 +307,31 @@ def test_bad_scales_are_reported(kind):
     run_gpu(w, x2, DEV, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == kgw.KGW_ERR_SCALES
+
+
+def test_fp8_scales_that_are_not_powers_of_two_take_the_promotion_path():
+    """The same e4m3 operands with one scale changed from a power of two to 3x it: no error, the
+    result follows the oracle, and it is exactly 3x the original for the block that scale covers."""
+    kgw = ensure_built()
+    w = W.custom(2, 128, 256, [256, 256], seed=124, fp8=True)
+    x = W.make_inputs(w, DEV)
+    x_cpu = W.make_inputs(w, "cpu")
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    base = run_gpu(w, x, DEV, status=status).stacked().clone()
+    torch.cuda.synchronize()
+    assert int(status.item()) == kgw.KGW_OK
+    sfa = x.sfa.clone()
+    sfa[:, 5] *= 3.0                       # every block of A's row 5: not a power of two any more
+    x2 = W.Inputs(x.a, x.b, x.offsets, sfa, x.sfb, x.c)
+    status.fill_(-1)
+    got = run_gpu(w, x2, DEV, status=status).stacked().clone()
+    torch.cuda.synchronize()
+    assert int(status.item()) == kgw.KGW_OK
+    x2c = W.Inputs(x_cpu.a, x_cpu.b, x_cpu.offsets, sfa.cpu(), x_cpu.sfb, x_cpu.c)
+    ref, S = oracle_full(w, x2c)
+    assert_close_to_oracle(w, to_f64(got), ref, S)
+    others = torch.ones(128, dtype=torch.bool)
+    others[5] = False
+    # (different kernels sum in different orders: equal up to FP32 accumulation, not bit for bit)
+    assert torch.allclose(got[:, 5, :], 3.0 * base[:, 5, :], rtol=1e-5, atol=1e-3)
+    assert torch.allclose(got[:, others, :], base[:, others, :], rtol=1e-5, atol=1e-3)

@@ -229,6 +229,7 @@ BS_CASES = {
     "fp8_split_k": F8(2, 128, 256, [12304, 16], seed=146),
     "fp8_split_k_accumulate": F8(3, 256, 256, [10000, 0, 528], seed=147, accumulate=True, out_dtype="bf16"),
     "fp8_discrete_f16": F8(3, 128, 512, [144, 16, 2000], seed=148, output_mode="discrete", out_dtype="f16"),
+    "fp8_general_scales": F8(4, 256, 512, [48, 0, 1040, 16], seed=149, sf_format="f32_any", out_dtype="bf16"),
     "fp4": F4(4, 256, 512, [32, 0, 160, 1056], seed=150),
     "fp4_single_block_last_stage": F4(3, 128, 256, [96, 352, 128], seed=151, out_dtype="bf16"),
     "fp4_split_k": F4(2, 128, 256, [20000, 32], seed=152),

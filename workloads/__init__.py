@@ -90,7 +90,8 @@ class Workload:
     output_mode: str = "dense"      # "dense" | "discrete"
     fp8: bool = False
     a_major: str = "k"              # "k": A stored [hidden, tokens]; "mn": stored [tokens, hidden]
-    sf_format: str = "f32_128"      # FP8 scales: "f32_128" (FP32 per 128 tokens) | "ue8m0_32" (packed)
+    sf_format: str = "f32_128"      # FP8 scales: "f32_128" (FP32 powers of two per 128 tokens) | "f32_any"
+                                    # (general FP32 per 128 tokens) | "ue8m0_32" (packed) | "ue4m3_16" (NVFP4)
     b_major: str = "mn"             # "mn": B stored [tokens, intermediate]; "k": stored [intermediate, tokens]
     fp4: bool = False               # e2m1 operands (K-major A and B), UE8M0 scales per 32 tokens
     unaligned: bool = False         # counts multiples of 8, not 256 (the unaligned BF16 entry point)
@@ -159,6 +160,13 @@ def fp4() -> Workload:
                     out_dtype="bf16", fp4=True, b_major="k", sf_format="ue8m0_32")
 
 
+def fp8_fp32() -> Workload:
+    """The FP8 workload with general FP32 scales (amax/448, not rounded to powers of two)."""
+    return Workload("FP8 general FP32 scales: E=16 hidden=4096 intermediate=1536, scale amax/448 per 128 tokens, "
+                    "BF16 dense overwrite", 16, 4096, 1536, counts_uniform_spread(3, 16, 4096, 0.7, 1.3), seed=14,
+                    out_dtype="bf16", fp8=True, sf_format="f32_any")
+
+
 def nvfp4() -> Workload:
     return Workload("NVFP4 block-scaled: E=16 hidden=4096 intermediate=1536, e2m1 with UE4M3 scales per 16 "
                     "tokens and FP32 global scales, K-major A and B, BF16 dense overwrite",
@@ -191,7 +199,8 @@ def fp4_unaligned() -> Workload:
 
 
 NAMED = {"tiny": tiny, "balanced": balanced, "wide": wide, "fp8": fp8, "skewed": skewed, "fp4": fp4,
-         "unaligned": unaligned, "fp8_unaligned": fp8_unaligned, "fp4_unaligned": fp4_unaligned, "nvfp4": nvfp4}
+         "unaligned": unaligned, "fp8_unaligned": fp8_unaligned, "fp4_unaligned": fp4_unaligned, "nvfp4": nvfp4,
+         "fp8_fp32": fp8_fp32}
 
 
 def custom(num_experts: int, hidden: int, intermediate: int, counts, seed: int, **kw) -> Workload:
@@ -269,6 +278,28 @@ def quantize_e4m3_blocks(x: torch.Tensor, token_axis: int):
     if token_axis == 0:
         q = q.t().contiguous()
     return q.contiguous(), scale.t().contiguous()   # scales as [nblk, other]
+
+
+def quantize_e4m3_fp32_blocks(x: torch.Tensor, token_axis: int):
+    """Quantise ``x`` (float32 2-D) to e4m3 with one general FP32 scale per 128 tokens: the scale is
+    amax/448 in float32, raised by one ulp when the division would otherwise exceed 448 (1 for an
+    all-zero block), so the scales are in general not powers of two. Same return layout as
+    ``quantize_e4m3_blocks``."""
+    assert x.dim() == 2 and x.dtype == torch.float32
+    xt = x if token_axis == 1 else x.t()
+    other, tokens = xt.shape
+    assert tokens % FP8_BLOCK == 0
+    blocks = xt.reshape(other, tokens // FP8_BLOCK, FP8_BLOCK)
+    amax = blocks.abs().amax(dim=2).numpy().astype(np.float32)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    over = (amax / np.maximum(scale, np.float32(1e-30))) > np.float32(E4M3_MAX)
+    scale = np.where(over, np.nextafter(scale, np.float32(np.inf)), scale).astype(np.float32)
+    scale = np.where(amax == 0, np.float32(1.0), scale).astype(np.float32)
+    st = torch.from_numpy(scale)
+    q = (blocks / st.unsqueeze(2)).to(torch.float8_e4m3fn).reshape(other, tokens)
+    if token_axis == 0:
+        q = q.t().contiguous()
+    return q.contiguous(), st.t().contiguous()
 
 
 def quantize_e4m3_ue8m0_32(x: torch.Tensor, token_axis: int):
@@ -511,6 +542,9 @@ def make_inputs(w: Workload, device="cpu") -> Inputs:
     if w.fp8 and w.sf_format == "ue8m0_32":
         a_store, sfa = quantize_per_expert(quantize_e4m3_ue8m0_32, a32, 1, w.counts)
         b_store, sfb = quantize_per_expert(quantize_e4m3_ue8m0_32, b32, 0, w.counts)
+    elif w.fp8 and w.sf_format == "f32_any":
+        a_store, sfa = quantize_per_expert(quantize_e4m3_fp32_blocks, a32, 1, w.counts)
+        b_store, sfb = quantize_per_expert(quantize_e4m3_fp32_blocks, b32, 0, w.counts)
     elif w.fp8:
         a_store, sfa = quantize_per_expert(quantize_e4m3_blocks, a32, 1, w.counts)
         b_store, sfb = quantize_per_expert(quantize_e4m3_blocks, b32, 0, w.counts)
