@@ -1667,37 +1667,36 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       auto live_row = [&](int r) { return !kMG || q * 32 + r < (rank ? it.rows1 : it.rows); };
       auto live = [&](int j) { return live_row(4 * j + (lane >> 3)); };
       if (it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
-        // 16-bit outputs (BF16 / FP16), overwrite: each thread rounds row `lane` of a 32-column
-        // chunk in registers, so the per-warp staging carries packed 16-bit rows (64 bytes) -- half
-        // the shared-memory traffic of staging FP32, which competes with the tensor pipe's operand
-        // reads. Stores: 4 lanes per 64-byte row segment, 8 rows per instruction.
+        // 16-bit outputs (BF16 / FP16), overwrite: each thread reads row `lane` of a 64-column chunk
+        // (one TMEM load), rounds it in registers and stages the packed 128-byte row, so a tile
+        // takes four load / stage / store rounds and the staging carries half the bytes of FP32.
+        // Stores: 8 lanes per 128-byte row segment, 4 rows per instruction.
         const bool okt = wait_bounded_t<kPair>(&ctl->tfull[acc], use & 1, abort_flag, p.timeout_ns);
         if (!__all_sync(0xffffffffu, okt)) break;
         tc_fence_after();
-        const int sw = (lane >> 1) & 3;        // 16-byte chunk swizzle of staging row `lane`
-        const int rsub = lane >> 2, csub = lane & 3;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t pk[16];
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t pk[32];
           {
-            uint32_t r[32];
-            tmem_ld_32x32b_x32(taddr + c * 32, r);
+            uint32_t r[64];
+            tmem_ld_32x32b_x64(taddr + c * 64, r);
             tmem_ld_wait();
-            if (c == BN / 32 - 1) release_acc();
+            if (c == BN / 64 - 1) release_acc();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 32; ++i)
               pk[i] = p.out_f16 ? pack_f16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]))
                                 : pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
           }
+          // row `lane` = 8 16-byte chunks, chunk i at slot i ^ (lane & 7) (the FP32 staging's swizzle)
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            stg[lane * 4 + (i ^ sw)] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 8; ++i)
+            stg[lane * 8 + (i ^ (lane & 7))] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           __syncwarp();
-          char* cbase = obase + size_t(c * 32 + csub * 8) * 2;
+          char* cbase = obase + size_t(c * 64 + (lane & 7) * 8) * 2;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = 8 * j + rsub;
-            if (live_row(r)) *reinterpret_cast<uint4*>(cbase + r * ostride) = stg[r * 4 + (csub ^ ((r >> 1) & 3))];
+          for (int j = 0; j < 8; ++j) {
+            const int r = 4 * j + (lane >> 3);
+            if (live_row(r)) *reinterpret_cast<uint4*>(cbase + r * ostride) = stg[r * 8 + ((lane & 7) ^ (r & 7))];
           }
           __syncwarp();
         }
