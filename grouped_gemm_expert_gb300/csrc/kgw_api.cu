@@ -79,15 +79,21 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int bk_of(bool fp8) { return fp8 ? kgw::BK_FP8 : kgw::BK_BF16; }
 
-// Rows of a work tile: BF16 problems whose hidden size is a multiple of 256 run on CTA pairs.
-int32_t tile_rows(const kgw_wgrad_args* a, bool fp8) {
-  if (!fp8 && a->hidden % (2 * kgw::BM) == 0 && g_single_cta.load() == 0) return 2 * kgw::BM;
+// Rows of a work tile: BF16 and FP8 problems whose hidden size is a multiple of 256 run on CTA
+// pairs (FP4 and NVFP4 on single CTAs).
+int32_t tile_rows(const kgw_wgrad_args* a, bool fp8, bool fp4 = false) {
+  if (!fp4 && a->hidden % (2 * kgw::BM) == 0 && g_single_cta.load() == 0) return 2 * kgw::BM;
+  (void)fp8;
   return kgw::BM;
 }
 
+// Scale rows reserved for the prepared scale words of FP8 on CTA pairs: at least the sum over
+// experts of ceil(n_e / 128), which tokens_sum / 128 + E bounds.
+int64_t prep_rows(const kgw_wgrad_args* a) { return a->tokens_sum / kgw::SCALE_BLOCK + a->num_experts; }
+
 // Upper bound of the FP32 partial tiles split-K can use for these shapes.
-int32_t slot_cap(const kgw_wgrad_args* a, bool fp8) {
-  const int64_t T = int64_t(a->hidden / tile_rows(a, fp8)) * (a->intermediate / kgw::BN);
+int32_t slot_cap(const kgw_wgrad_args* a, bool fp8, bool fp4 = false) {
+  const int64_t T = int64_t(a->hidden / tile_rows(a, fp8, fp4)) * (a->intermediate / kgw::BN);
   const int64_t kit = a->tokens_sum / bk_of(fp8);
   // an expert is split only when its k-iterations exceed the chunk (>= MIN_SPLIT_KITERS), and
   // then into fewer than 2*kiters/chunk pieces
@@ -133,6 +139,18 @@ kgw_status validate(const kgw_wgrad_args* a, bool fp8, bool fp4 = false, int64_t
   return KGW_OK;
 }
 
+// Plain (unswizzled) 2-D map of 32-bit words: the prepared scale words of FP8 on CTA pairs.
+kgw_status encode_2d_words(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {box_inner, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? KGW_OK : KGW_ERR_CUDA;
+}
+
 kgw_status encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
   const cuuint64_t dims[2] = {inner, outer};
@@ -176,18 +194,23 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return KGW_ERR_ALIGNMENT;
   }
   if (!ws || !aligned(ws, 256)) return KGW_ERR_WORKSPACE;
-  const int32_t tile_m = tile_rows(a, fp8);
+  const int32_t tile_m = tile_rows(a, fp8, fp4);
   const int32_t halves = tile_m / kgw::BM;
-  const WsLayout L0 = kgw::ws_layout(a->num_experts, 0, halves);
+  // FP8 on CTA pairs: prepared scale words of every scale row in the workspace
+  const bool fp8_pair = fp8 && !fp4 && halves == 2;
+  const int64_t sf_rows = fp8_pair ? prep_rows(a) : 0;
+  const WsLayout L0 = kgw::ws_layout(a->num_experts, 0, halves, sf_rows, a->hidden, a->intermediate);
   if (ws_bytes < L0.total) return KGW_ERR_WORKSPACE;
-  int32_t max_slots = slot_cap(a, fp8);
+  int32_t max_slots = slot_cap(a, fp8, fp4);
   {
     const size_t room = ws_bytes - L0.total;
     const size_t fit = room / (halves * (kgw::PARTIAL_TILE_BYTES + 4 * kgw::EPI_COUNTERS));
     if (size_t(max_slots) > fit) max_slots = static_cast<int32_t>(fit);
-    while (max_slots > 0 && kgw::ws_layout(a->num_experts, max_slots, halves).total > ws_bytes) --max_slots;
+    while (max_slots > 0 &&
+           kgw::ws_layout(a->num_experts, max_slots, halves, sf_rows, a->hidden, a->intermediate).total > ws_bytes)
+      --max_slots;
   }
-  const WsLayout L = kgw::ws_layout(a->num_experts, max_slots, halves);
+  const WsLayout L = kgw::ws_layout(a->num_experts, max_slots, halves, sf_rows, a->hidden, a->intermediate);
 
   DevInfo dev;
   st = device_info(&dev);
@@ -337,6 +360,16 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   mp.test_drop_stage = static_cast<int32_t>(g_drop_stage.load());
   mp.tail_a = pp.tail_a;
   mp.tail_b = pp.tail_b;
+  mp.sf_prep = fp8_pair;
+  if (fp8_pair && a->tokens_sum > 0) {
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    st = encode_2d_words(&mp.tm_sfa, w + L.sf_prep_a, static_cast<uint64_t>(a->hidden), static_cast<uint64_t>(sf_rows),
+                         kgw::BM);
+    if (st == KGW_OK)
+      st = encode_2d_words(&mp.tm_sfb, w + L.sf_prep_b, static_cast<uint64_t>(a->intermediate),
+                           static_cast<uint64_t>(sf_rows), kgw::BN);
+    if (st != KGW_OK) return st;
+  }
   P->grid = grid;
   return KGW_OK;
 }
@@ -358,7 +391,11 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
   P.mp.general_dispatch = general;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kgw::launch_plan(P.pp, P.tpl, s) != cudaSuccess) return KGW_ERR_CUDA;
-  if (general && a->tokens_sum > 0 && kgw::launch_scale_check(P.mp, 4 * P.grid, s) != cudaSuccess) return KGW_ERR_CUDA;
+  // the scale kernel: the FP32 power-of-two check, and the prepared scale words of FP8 pairs
+  if ((general || P.mp.sf_prep) && a->tokens_sum > 0 && kgw::launch_scale_check(P.mp, 4 * P.grid, s) != cudaSuccess)
+    return KGW_ERR_CUDA;
+  if (general && P.mp.sf_prep && a->tokens_sum > 0 && kgw::launch_promote_kernel(P.mp, P.tmA, P.tmB, P.grid, s) != cudaSuccess)
+    return KGW_ERR_CUDA;
   cudaError_t e = fp4 ? kgw::launch_main_fp4(P.mp, P.tmA, P.tmB, P.grid, s)
                  : fp8 ? kgw::launch_main_fp8(P.mp, P.tmA, P.tmB, P.grid, s)
                        : kgw::launch_main_bf16(P.mp, P.tmA, P.tmB, P.grid, s);
@@ -554,8 +591,12 @@ kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t
   if (!bytes) return KGW_ERR_INVALID_ARG;
   kgw_status st = validate(args, is_fp8 != 0, false, 1);  // sizing only: the call checks its own count rule
   if (st != KGW_OK) return st;
+  // is_fp8 sizes the FP8 and the FP4 entries alike: the larger need (FP8 on CTA pairs, with its
+  // prepared scale words) covers both
   const int32_t halves = tile_rows(args, is_fp8 != 0) / kgw::BM;
-  *bytes = kgw::ws_layout(args->num_experts, slot_cap(args, is_fp8 != 0), halves).total;
+  const int64_t sf_rows = (is_fp8 != 0 && halves == 2) ? prep_rows(args) : 0;
+  *bytes = kgw::ws_layout(args->num_experts, slot_cap(args, is_fp8 != 0), halves, sf_rows, args->hidden,
+                          args->intermediate).total;
   return KGW_OK;
 }
 

@@ -72,6 +72,11 @@ constexpr uint32_t SF_STAGE_COLS_FP4 = 24;
 // NVFP4 stages (UE4M3 scales per 16 tokens): four 64-token scale words per row/column (A 4 x 128,
 // B 4 x 256 words, 6 KiB), rearranged in place into 12 blocks (for each MMA k: A word k, B word k
 // columns 0..127, 128..255) that land in 48 TMEM columns per stage; 3 stages of 54 KiB.
+// FP8 on CTA pairs: each stage carries this CTA's A scale-factor block and both B blocks (its own
+// and its peer's columns: the pair MMA reads all 256), in TMEM order, 1.5 KiB padded to 2 KiB;
+// they arrive by TMA from the prepared words in the workspace, on the operands' barrier.
+constexpr uint32_t SF_SMEM_PAD_PAIR = 2048;
+constexpr uint32_t SF_PAIR_BYTES = 3 * SF_UE8_BLOCK;
 constexpr uint32_t SF_SMEM_BYTES_NV = 4 * (BM + BN) * 4;
 constexpr uint32_t SF_SMEM_PAD_NV = 6144;
 constexpr uint32_t SF_STAGE_COLS_NV = 48;
@@ -101,15 +106,22 @@ static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte block");
 //   [partials max_slots * PARTIAL_TILE_BYTES]
 // scale_row[e]: first scale row of expert e in the block-scaled entries, the sum over f < e of
 // ceil(n_f / 128) (each expert's 128-token scale blocks start at its first token).
+// [prepared scale words of A, then of B] (FP8 on CTA pairs): UE8M0 scale factors in TMEM order,
+// [scale rows][hidden] and [scale rows][intermediate] int32 words, within each 128-row / 128-column
+// group word 4l + c holding row / column 32c + l.
 struct WsLayout {
-  size_t order, item_prefix, splits, slot_base, counter_base, scale_row, tmaps, tmaps_b, counters, partials, total;
+  size_t order, item_prefix, splits, slot_base, counter_base, scale_row, tmaps, tmaps_b, counters, partials,
+      sf_prep_a, sf_prep_b, total;
   int32_t max_slots;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // halves = 2 when a work tile spans a CTA pair (256 rows): partial tiles and counters double.
-inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1) {
+// sf_rows: scale rows reserved for prepared scale words (FP8 on CTA pairs), with rows_a / rows_b
+// words each (hidden, intermediate); 0 for every other call.
+inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1, int64_t sf_rows = 0, int64_t rows_a = 0,
+                          int64_t rows_b = 0) {
   WsLayout L{};
   size_t off = sizeof(PlanHeader);
   L.order = off;        off = align256(off + sizeof(int32_t) * E);
@@ -122,6 +134,8 @@ inline WsLayout ws_layout(int32_t E, int32_t max_slots, int32_t halves = 1) {
   L.tmaps_b = off;      off = align256(off + size_t(128) * E);
   L.counters = off;     off = align256(off + sizeof(int32_t) * EPI_COUNTERS * halves * (max_slots > 0 ? max_slots : 1));
   L.partials = off;     off = align256(off + PARTIAL_TILE_BYTES * halves * size_t(max_slots));
+  L.sf_prep_a = off;    off = align256(off + sizeof(int32_t) * size_t(sf_rows) * size_t(rows_a));
+  L.sf_prep_b = off;    off = align256(off + sizeof(int32_t) * size_t(sf_rows) * size_t(rows_b));
   L.total = off;
   L.max_slots = max_slots;
   return L;
@@ -139,6 +153,7 @@ inline WsLayout ws_layout_mg(int64_t max_tiles) {
   L.item_prefix = align256(L.order + sizeof(int32_t) * 4 * n);
   L.total = align256(L.item_prefix + sizeof(int32_t) * 2 * n);
   L.splits = L.slot_base = L.counter_base = L.scale_row = L.tmaps = L.tmaps_b = L.counters = L.partials = L.total;
+  L.sf_prep_a = L.sf_prep_b = L.total;
   L.max_slots = 0;
   return L;
 }
@@ -199,6 +214,9 @@ struct MainParams {
   int32_t nvfp4;                // FP4 with UE4M3 scales per 16 tokens (kind::mxf4nvf4, scale_vec::4X)
   int32_t general_dispatch;     // FP8 with FP32 scales: the FP8 kernel takes its promotion path when
                                 // the scale check found a scale that is not a power of two
+  int32_t sf_prep;              // FP8 on CTA pairs: the scale kernel writes the prepared scale words
+  CUtensorMap tm_sfa;           // FP8 on CTA pairs: the prepared words of A ([rows][hidden] int32,
+  CUtensorMap tm_sfb;           // 128-word boxes) and of B ([rows][intermediate], 256-word boxes)
   const float* gscale_a;        // NVFP4: per-tensor global scales (device, one float each; null = 1)
   const float* gscale_b;
   int32_t* status_dev;
@@ -216,9 +234,14 @@ cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const C
                             cudaStream_t s);
 cudaError_t launch_main_fp4(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s);
-// FP8 with FP32 scales: a check of every scale of the call, between the plan and the FP8 kernel
-// (sets general_scales: the FP8 kernel then takes its per-block promotion path).
+// FP8 scales, between the plan and the FP8 kernel: checks every scale of the call (FP32 scales:
+// sets general_scales, and the FP8 kernel then takes its per-block promotion path) and, for FP8 on
+// CTA pairs, writes the prepared UE8M0 scale words the pair kernel loads by TMA.
 cudaError_t launch_scale_check(const MainParams& p, int grid, cudaStream_t s);
+// FP8 on CTA pairs with FP32 scales: the promotion path as its own kernel (a kernel may not mix
+// single-CTA and CTA-pair tcgen05 instructions), launched between the scale kernel and the pair kernel.
+cudaError_t launch_promote_kernel(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                                  cudaStream_t s);
 // M-grouped GEMM (rows of A grouped by expert, each group with its own B): schedule + main kernel.
 cudaError_t launch_plan_mgrouped(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,

@@ -539,7 +539,7 @@ constexpr uint32_t EPI_STAGE_TOTAL = 16384;
 constexpr uint32_t EPI_STAGE_BYTES = EPI_STAGE_TOTAL / NUM_EPI_WARPS;
 
 size_t main_smem_bytes(bool pair, bool fp8, bool nv) {
-  const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + (fp8 ? SF_SMEM_PAD : 0u))
+  const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + (fp8 ? SF_SMEM_PAD_PAIR : 0u))
                       : nv ? size_t(STAGES_NV) * (STAGE_BYTES + SF_SMEM_PAD_NV)
                            : size_t(STAGES) * (STAGE_BYTES + (fp8 ? SF_SMEM_PAD : 0u));
   return ring + EPI_STAGE_TOTAL + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
@@ -651,40 +651,52 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
 // FP8 with general FP32 scales
 // =============================================================================================
 
-// Checks every FP32 scale of the call once the plan is complete: a scale that is not a positive
-// power of two UE8M0 can hold sets general_scales (the promotion kernel then runs the call); a NaN
-// or infinite scale is KGW_ERR_SCALES.
+// Scale kernel of the K-grouped FP8 entries, between the plan and the FP8 kernel. It reads every
+// scale of the call once (the plan's scale rows x hidden / intermediate):
+//  - FP32 scales: a scale that is not a positive power of two UE8M0 can hold sets general_scales
+//    (the FP8 kernel then takes its promotion path); a NaN or infinite scale is KGW_ERR_SCALES;
+//  - packed UE8M0 words: a byte 0xFF (NaN) is KGW_ERR_SCALES;
+//  - FP8 on CTA pairs (p.sf_prep): writes the UE8M0 scale factors in TMEM order into the workspace,
+//    so that a pair stage loads them by TMA: within each group of 128 rows (columns), word 4l + c
+//    holds row 32c + l, the FP32 scale's exponent byte repeated four times or the packed word.
+// One work unit is such a 4-word group entry: four coalesced loads (32 rows apart), one 16-byte store.
 __global__ void __launch_bounds__(256) scale_check_kernel(const __grid_constant__ MainParams p) {
   pdl_launch_dependents();
   pdl_wait();
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
   if (hdr->error != 0) return;
-  // 16-byte loads (rows of hidden and of intermediate are multiples of 4 floats), four in flight
-  // per thread, so the check costs a couple of memory round trips rather than one per element
-  const int64_t na = int64_t(hdr->scale_rows) * p.H / 4, nb = int64_t(hdr->scale_rows) * p.I / 4;
-  const uint4* va = reinterpret_cast<const uint4*>(p.sfa);
-  const uint4* vb = reinterpret_cast<const uint4*>(p.sfb);
+  const int64_t rows = hdr->scale_rows;
+  const int64_t ua = rows * (p.H / 4), ub = rows * (p.I / 4);
+  const uint32_t* sa = reinterpret_cast<const uint32_t*>(p.sfa);
+  const uint32_t* sb = reinterpret_cast<const uint32_t*>(p.sfb);
+  uint32_t* pa = reinterpret_cast<uint32_t*>(p.ws + p.L.sf_prep_a);
+  uint32_t* pb = reinterpret_cast<uint32_t*>(p.ws + p.L.sf_prep_b);
   uint32_t general = 0, bad = 0;
-  auto check = [&](uint32_t b) {
-    const uint32_t e = (b >> 23) & 0xFFu, m = b & 0x7FFFFFu;
-    bad |= e == 255u;
-    general |= (e != 255u) & (((b >> 31) != 0u) | (e == 0u ? m != 0x400000u : m != 0u));
-  };
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i0 < na + nb; i0 += 4 * stride) {
-    uint4 v[4];
+  for (int64_t u = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; u < ua + ub; u += stride) {
+    const bool is_a = u < ua;
+    const int64_t v = is_a ? u : u - ua;
+    const int64_t cols = is_a ? p.H : p.I;
+    const int64_t kb = v / (cols / 4);
+    const int64_t rem = v - kb * (cols / 4);
+    const int64_t g = rem >> 5, l = rem & 31;
+    const uint32_t* src = (is_a ? sa : sb) + kb * cols + g * 128 + l;
+    uint32_t w[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int64_t i = i0 + u * stride;
-      v[u] = i < na ? __ldg(va + i) : (i < na + nb ? __ldg(vb + (i - na)) : make_uint4(0x3F800000u, 0x3F800000u, 0x3F800000u, 0x3F800000u));
-    }
+    for (int c = 0; c < 4; ++c) w[c] = __ldg(src + 32 * c);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      check(v[u].x);
-      check(v[u].y);
-      check(v[u].z);
-      check(v[u].w);
+    for (int c = 0; c < 4; ++c) {
+      if (p.sf_packed) {
+        bad |= ff_bytes(w[c]);
+      } else {
+        const uint32_t e = (w[c] >> 23) & 0xFFu, m = w[c] & 0x7FFFFFu;
+        bad |= e == 255u;
+        general |= (e != 255u) & (((w[c] >> 31) != 0u) | (e == 0u ? m != 0x400000u : m != 0u));
+        w[c] = e * 0x01010101u;     // the UE8M0 byte of a power of two, one per 32-token block
+      }
     }
+    if (p.sf_prep)
+      *reinterpret_cast<uint4*>((is_a ? pa : pb) + kb * cols + g * 128 + 4 * l) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   if (__any_sync(0xffffffffu, general) && (threadIdx.x & 31) == 0) atomicOr(&hdr->general_scales, 1);
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && p.status_dev) atomicExch(p.status_dev, KGW_ERR_SCALES);
@@ -730,7 +742,13 @@ template <bool kAK, bool kBK>
 __device__ __forceinline__ void promote_body(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB,
                                              uint8_t* smem_raw) {
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
-  const int total_items = 2 * hdr->total_items;   // two 128-column halves per plan item
+  // 128 x 128 sub-tiles of the plan's items: two column halves, and two row halves when the plan
+  // laid out 256-row CTA-pair tiles
+  const int subs = 2 * (p.tile_m / BM);
+  const int total_items = subs * hdr->total_items;
+  // K-major B descriptors of CTA-pair plans have 128-row boxes (this sub-tile's columns), those of
+  // single-CTA plans 256-row boxes (both halves; the MMA reads this half's)
+  const bool half_box = p.tile_m == 2 * BM;
   if (total_items == 0) return;
   constexpr int bk = BK_FP8;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -810,7 +828,9 @@ __device__ __forceinline__ void promote_body(const MainParams& p, const CUtensor
         bool ok2 = true;
         if (lane == 0) {
           ok2 = wait_bounded(&ctl->empty[stage], phase ^ 1, abort_flag, p.timeout_ns);
-          if (ok2) mbar_arrive_expect_tx(&ctl->full[stage], STAGE_A_BYTES + (kBK ? STAGE_B_BYTES : STAGE_B_BYTES / 2) + PR_SF_BYTES);
+          if (ok2)
+            mbar_arrive_expect_tx(&ctl->full[stage],
+                                  STAGE_A_BYTES + (kBK && !half_box ? STAGE_B_BYTES : STAGE_B_BYTES / 2) + PR_SF_BYTES);
         }
         ok2 = __shfl_sync(0xffffffffu, ok2, 0);
         if (!ok2) break;
@@ -827,7 +847,7 @@ __device__ __forceinline__ void promote_body(const MainParams& p, const CUtensor
           else tma_load_2d(sA, amap, &ctl->full[stage], it.m0, static_cast<int32_t>(tok));
           // K-major B: the plan tile's 256-row box (the MMA reads this half's 128 rows);
           // N-major B: this half's 128 columns (one 128-byte atom)
-          if constexpr (kBK) tma_load_2d(sB, bmap, &ctl->full[stage], kx, n0_tile);
+          if constexpr (kBK) tma_load_2d(sB, bmap, &ctl->full[stage], kx, half_box ? it.n0 : n0_tile);
           else tma_load_2d(sB, bmap, &ctl->full[stage], it.n0, static_cast<int32_t>(tok));
         }
         ++issued;
@@ -881,7 +901,8 @@ __device__ __forceinline__ void promote_body(const MainParams& p, const CUtensor
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * PR_STAGE_BYTES);
-          const uint32_t b_addr = a_addr + STAGE_A_BYTES + (kBK ? static_cast<uint32_t>(it.m1) * (STAGE_B_BYTES / 2) : 0u);
+          const uint32_t b_addr =
+              a_addr + STAGE_A_BYTES + (kBK && !half_box ? static_cast<uint32_t>(it.m1) * (STAGE_B_BYTES / 2) : 0u);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_f8f6f4(tmem_base + pb * PR_TN, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc,
@@ -1001,16 +1022,18 @@ __device__ __forceinline__ void promote_body(const MainParams& p, const CUtensor
     }
   } else if (warp == SCHED_WARP_FP8) {
     // ======================= scheduler =======================
-    // Claims the next half-tile one ahead of the producer (item 2i + h is half h of plan item i).
+    // Claims the next sub-tile one ahead of the producer (item subs * i + s is sub-tile s of plan item i).
     if (lane == 0) {
       int cur = atomicAdd(item_counter, 1);
       for (int n = 0;; ++n) {
         const int slot = n % WORK_RING;
         Item it;
         if (cur < total_items) {
-          it = decode_item<false>(p, cur >> 1, bk);
-          it.m1 = cur & 1;              // the 128-column half
-          it.n0 += (cur & 1) * PR_TN;
+          const int sub = cur % subs;
+          it = decode_item<false>(p, cur / subs, bk);
+          it.m0 += (sub >> 1) * BM;     // the 128-row half of a CTA-pair item
+          it.m1 = sub & 1;              // the 128-column half
+          it.n0 += (sub & 1) * PR_TN;
         } else {
           it = Item{};
           it.e = -1;
@@ -1031,6 +1054,49 @@ __device__ __forceinline__ void promote_body(const MainParams& p, const CUtensor
     tmem_dealloc(tmem_base, 256);
   }
   if (threadIdx.x == 0 && ctl->abort_flag && p.status_dev) atomicExch(p.status_dev, KGW_ERR_TIMEOUT);
+}
+
+// The promotion path as a kernel of its own, launched before the FP8 CTA-pair kernel of calls with
+// FP32 scales: it runs the call when the scale kernel found a scale that is not a power of two and
+// otherwise leaves at once (the pair kernel then runs it).
+template <bool kAK, bool kBK>
+__global__ void __launch_bounds__(NUM_THREADS_FP8, 1)
+    promote_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB) {
+  extern __shared__ uint8_t smem_raw[];
+  pdl_launch_dependents();
+  pdl_wait();
+  const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
+  if (hdr->error != 0 || !hdr->general_scales || hdr->total_items == 0) return;
+  promote_body<kAK, kBK>(p, tmA, tmB, smem_raw);
+}
+
+template <bool kAK, bool kBK>
+static cudaError_t launch_promote(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                                  cudaStream_t s) {
+  auto kernel = promote_kernel<kAK, kBK>;
+  const size_t smem = promote_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS_FP8, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p, tmA, tmB);
+}
+
+cudaError_t launch_promote_kernel(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
+                                  cudaStream_t s) {
+  if (p.a_kmajor && !p.b_kmajor) return launch_promote<true, false>(p, tmA, tmB, grid, s);
+  if (!p.a_kmajor && !p.b_kmajor) return launch_promote<false, false>(p, tmA, tmB, grid, s);
+  if (p.a_kmajor && p.b_kmajor) return launch_promote<true, true>(p, tmA, tmB, grid, s);
+  return launch_promote<false, true>(p, tmA, tmB, grid, s);
 }
 
 cudaError_t launch_scale_check(const MainParams& p, int grid, cudaStream_t s) {
@@ -1060,15 +1126,16 @@ template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4
 __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
-  // FP8 runs on single CTAs: a CTA-pair version (block-scaled cta_group::2 MMA, scale factors of
-  // all 256 B columns in each CTA's TMEM) was correct but 1.85x slower on the FP8 workload.
-  static_assert(!(kFp8 && kPair), "the FP8 path runs on single CTAs");
+  // FP8 on CTA pairs: K-grouped e4m3 with scale factors prepared in TMEM order by the scale kernel
+  // and loaded by TMA with the operands (FP4, NVFP4 and the M-grouped FP8 GEMM run on single CTAs).
+  static_assert(!(kFp8 && kPair) || (!kFp4 && !kMG), "block-scaled CTA pairs: K-grouped FP8 only");
   static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
   static_assert(!kNv || kFp4, "NVFP4 is the FP4 kernel with UE4M3 scales");
   constexpr int kStages = kPair ? STAGES_PAIR : (kNv ? STAGES_NV : STAGES);
   constexpr uint32_t kStageB = kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
-  constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB + (kNv ? SF_SMEM_PAD_NV : (kFp8 ? SF_SMEM_PAD : 0u));
-  constexpr uint32_t kStageTx = STAGE_A_BYTES + kStageB;
+  constexpr uint32_t kStageBytes =
+      STAGE_A_BYTES + kStageB + (kNv ? SF_SMEM_PAD_NV : (kFp8 ? (kPair ? SF_SMEM_PAD_PAIR : SF_SMEM_PAD) : 0u));
+  constexpr uint32_t kStageTx = STAGE_A_BYTES + kStageB + (kFp8 && kPair ? SF_PAIR_BYTES : 0u);
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
   constexpr int kHalves = kPair ? 2 : 1;
   constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
@@ -1077,10 +1144,13 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   pdl_wait();  // the plan of this call (and any scale check before it) is complete and visible
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
   if (hdr->error != 0) return;  // offsets/pointers rejected by the plan: write nothing
-  if constexpr (kFp8 && !kFp4 && !kMG && !kPair) {
+  if constexpr (kFp8 && !kFp4 && !kMG) {
     // FP32 scales of which some is not a power of two: the per-block promotion path runs the call
+
     if (p.general_dispatch && hdr->general_scales) {
-      promote_body<kAK, kBK>(p, tmA, tmB, smem_raw);
+      // (a kernel may not mix single-CTA and CTA-pair tcgen05 instructions: for pairs the
+      // promotion kernel launched before this one has run the call)
+      if constexpr (!kPair) promote_body<kAK, kBK>(p, tmA, tmB, smem_raw);
       return;
     }
   }
@@ -1110,7 +1180,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     for (int w = 0; w < WORK_RING; ++w) {
       mbar_init(&ctl->wfull[w], 1);
       // consumers: the producer and the epilogue warps of each CTA, the MMA thread, the converter
-      mbar_init(&ctl->wempty[w], kHalves * (1 + kEpiWarps) + 1 + (kFp8 ? 1 : 0));
+      mbar_init(&ctl->wempty[w], kHalves * (1 + kEpiWarps) + 1 + (kFp8 && !kPair ? 1 : 0));
     }
     mbar_init(&ctl->sched_go, 1);
     mbar_init(&ctl->mma_done, 1);
@@ -1123,6 +1193,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     if (p.tokens_sum > 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      if constexpr (kFp8 && kPair) {
+        tma_prefetch_desc(&p.tm_sfa);
+        tma_prefetch_desc(&p.tm_sfb);
+      }
     }
   }
   if (warp == 1) {
@@ -1214,7 +1288,14 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           const int32_t b_tok = kMG ? it.e * p.K + kb * bk : static_cast<int32_t>(tok);
           // scales first: they are small and land before the operand tiles, so the converter's
           // work is done by the time the MMA has its operands
-          if constexpr (kNv) {
+          if constexpr (kFp8 && kPair) {
+            // prepared scale factors of this 128-token block, in TMEM order: this CTA's A rows and
+            // all 256 B columns, by TMA onto the leader's barrier with the operands
+            const int32_t kblk = it.srow + kb;
+            uint8_t* sS = sB + kStageB;
+            load(sS, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk);
+            load(sS + SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk);
+          } else if constexpr (kNv) {
             // NVFP4: the four 64-token scale words of this 256-token stage (UE4M3 bytes per 16
             // tokens): [A word 0..3][B word 0..3]; word rows are the expert's 64-token groups
             const int64_t w0 = 2 * int64_t(it.srow) + 4 * int64_t(kb);
@@ -1336,7 +1417,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             ok = false;
             break;
           }
-          if constexpr (kFp8) {
+          if constexpr (kFp8 && !kPair) {
             if (!wait_bounded_t<kPair>(&ctl->sf_full[stage], phase, abort_flag, p.timeout_ns)) {
               ok = false;
               break;
@@ -1345,7 +1426,21 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * kStageBytes);
           const uint32_t b_addr = a_addr + STAGE_A_BYTES;
-          if constexpr (kNv) {
+          if constexpr (kFp8 && kPair) {
+            // the stage's 3 scale-factor blocks -> TMEM columns 4i of the stage's 12 in both CTAs
+            // (each CTA's own shared memory to its own TMEM); MMA k uses byte k of every word (the
+            // FP32 scales' byte is repeated, packed UE8M0 words hold one per 32-token block)
+            const uint32_t sfa = tmem_base + SF_COL0 + stage * SF_STAGE_COLS;
+            const uint32_t ue8 = b_addr + kStageB;
+#pragma unroll
+            for (int blk = 0; blk < 3; ++blk)
+              tmem_cp_pair_32x128b_warpx4(sfa + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_mxf8_pair(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k),
+                            idesc | idesc_sf_id(static_cast<uint32_t>(k)), sfa, sfa + SF_A_COLS,
+                            (kb > it.kbeg || k > 0) ? 1u : 0u);
+          } else if constexpr (kNv) {
             // 12 scale blocks of this stage -> TMEM columns 4i of the stage's 48; MMA k (64 tokens)
             // reads A block 3k (columns 12k..12k+3) and B blocks 3k+1, 3k+2 (12k+4..12k+11), all
             // four UE4M3 bytes of each column
@@ -1466,7 +1561,12 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       auto release_acc = [&]() {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->tempty[0]);
+        if (lane == 0) {
+          if (kPair && !leader)
+            mbar_arrive_remote(leader_tempty0);
+          else
+            mbar_arrive(&ctl->tempty[0]);
+        }
       };
       // row `lane` of the staging buffer: four 16-byte chunks, chunk c at slot c ^ ((lane >> 1) & 3)
       auto stage4 = [&](uint4 v0, uint4 v1, uint4 v2, uint4 v3) {
@@ -1862,7 +1962,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     }
   }
 
-  if constexpr (kFp8) {
+  if constexpr (kFp8 && !kPair) {
     if (warp == SF_WARP) {
       // ======================= FP8 / FP4 scale-factor converter (warp 10) =======================
       // Per k-iteration: the stage's FP32 scales (128 of A, 256 of B) -> UE8M0 bytes (replicated
@@ -2081,7 +2181,7 @@ static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, cons
   auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG, kFp4, kNv>;
   size_t smem = main_smem_bytes(kPair, kFp8, kNv);
   // the K-grouped FP8 kernel also hosts the promotion path, which lays out the same memory its own way
-  if (kFp8 && !kFp4 && !kMG && !kPair && promote_smem_bytes() > smem) smem = promote_smem_bytes();
+  if (kFp8 && !kFp4 && !kMG && promote_smem_bytes() > smem) smem = promote_smem_bytes();
   // set on every launch: the attribute is per device and the call is cheap
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -2135,6 +2235,7 @@ cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, co
 
 cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s) {
+  if (p.tile_m == 2 * BM) return launch_orders<true, true>(p, tmA, tmB, grid, s);
   return launch_orders<true, false>(p, tmA, tmB, grid, s);
 }
 

@@ -335,3 +335,26 @@ def test_fp8_scales_that_are_not_powers_of_two_take_the_promotion_path():
     # (different kernels sum in different orders: equal up to FP32 accumulation, not bit for bit)
     assert torch.allclose(got[:, 5, :], 3.0 * base[:, 5, :], rtol=1e-5, atol=1e-3)
     assert torch.allclose(got[:, others, :], base[:, others, :], rtol=1e-5, atol=1e-3)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(sf_format="ue8m0_32", a_major="mn", b_major="k"),
+                                dict(input_order="ragged", out_dtype="bf16"), dict(sf_format="f32_any")],
+                         ids=["f32_scales", "ue8m0_mn_a_k_b", "ragged_bf16", "general_scales"])
+def test_fp8_pair_tiles_agree_with_single_cta_tiles(kw):
+    """FP8 problems whose hidden size is a multiple of 256 run on CTA pairs (256 x 256 tiles, scale
+    factors prepared by the scale kernel); the same call forced onto single-CTA 128 x 256 tiles
+    gives the same result within the FP32 accumulation bound, and both match the oracle."""
+    kgw = ensure_built()
+    w = W.custom(3, 512, 512, [768, 0, 1280], seed=125, fp8=True, **kw)
+    x = W.make_inputs(w, DEV)
+    x_cpu = W.make_inputs(w, "cpu")
+    pair = run_gpu(w, x, DEV).stacked().clone()
+    prev = kgw.kgw_debug_set(3, 1)
+    try:
+        single = run_gpu(w, x, DEV).stacked().clone()
+    finally:
+        kgw.kgw_debug_set(3, prev)
+    torch.cuda.synchronize()
+    ref, S = oracle_full(w, x_cpu)
+    assert_close_to_oracle(w, to_f64(pair), ref, S)
+    assert_close_to_oracle(w, to_f64(single), ref, S)
