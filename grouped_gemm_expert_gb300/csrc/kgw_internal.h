@@ -26,7 +26,9 @@ constexpr int SCALE_BLOCK = 128;
 constexpr int NUM_THREADS = 224;
 // block-scaled kernels (one accumulator, so the MMA waits while the epilogue drains TMEM): eight
 // epilogue warps, two per TMEM lane quadrant, one per 128-column half; warp 10 converts scales,
-// warp 11 schedules
+// warp 11 schedules. In a CTA pair (no converter) warp 10 of the even CTA copies the prepared scale
+// factors into TMEM. (A thirteenth warp would cap every warp at 128 registers: the warps share four
+// register files of 16384.)
 constexpr int NUM_THREADS_FP8 = 384;
 constexpr int SF_WARP = 10;
 constexpr int SCHED_WARP = 6;

@@ -525,8 +525,11 @@ struct SmemCtl {
   uint64_t wfull[WORK_RING];
   uint64_t wempty[WORK_RING];
   uint64_t mma_done;
-  uint64_t sf_full[MAX_STAGES]; // FP8: scale factors of a stage are in TMEM (on the leader in a pair)
-  uint64_t sfdata[MAX_STAGES];  // FP8: this CTA's FP32 scales of a stage have landed in shared memory
+  uint64_t sf_full[MAX_STAGES]; // block-scaled: single CTA, the converter has written a stage's scale
+                                // factors in TMEM order; pair, warp 10 has copied them to TMEM after
+                                // the stage's operands landed (on the even CTA)
+  uint64_t sfdata[MAX_STAGES];  // block-scaled: this CTA's raw scales of a stage have landed in shared memory
+  uint64_t cp_done;             // CTA pair: warp 10's last scale-factor copies have completed
   uint64_t sched_go;            // the producer has started an item: the scheduler may claim the next
   Item work[WORK_RING];         // decoded work items (written by the scheduler of the leader CTA)
   uint32_t tmem_base;
@@ -1179,11 +1182,13 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     }
     for (int w = 0; w < WORK_RING; ++w) {
       mbar_init(&ctl->wfull[w], 1);
-      // consumers: the producer and the epilogue warps of each CTA, the MMA thread, the converter
-      mbar_init(&ctl->wempty[w], kHalves * (1 + kEpiWarps) + 1 + (kFp8 && !kPair ? 1 : 0));
+      // consumers: the producer and the epilogue warps of each CTA, the MMA thread, and in the
+      // block-scaled kernels warp 10 (of the even CTA in a pair)
+      mbar_init(&ctl->wempty[w], kHalves * (1 + kEpiWarps) + 1 + (kFp8 ? 1 : 0));
     }
     mbar_init(&ctl->sched_go, 1);
     mbar_init(&ctl->mma_done, 1);
+    mbar_init(&ctl->cp_done, 1);
     for (int st = 0; st < kStages; ++st) {
       mbar_init(&ctl->sf_full[st], 1);
       mbar_init(&ctl->sfdata[st], 1);
@@ -1227,6 +1232,54 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       mbar_arrive_remote(leader_wempty0 + slot * 8);
     else
       mbar_arrive(&ctl->wempty[slot]);
+  };
+
+  // Block-scaled kernels: a stage's scale-factor blocks (32 rows x 16 bytes each, in TMEM order in
+  // shared memory) -> the stage's TMEM columns, repeated in the four lane quadrants; a pair's copies
+  // take each CTA's own shared memory to its own TMEM.
+  constexpr int kSfBlocks = kNv ? 12 : (kFp4 ? 6 : 3);
+  constexpr uint32_t kSfCols = kNv ? SF_STAGE_COLS_NV : (kFp4 ? SF_STAGE_COLS_FP4 : SF_STAGE_COLS);
+  // (single-CTA FP8 stages keep the raw FP32 scales ahead of the converted blocks)
+  constexpr uint32_t kSfSrc = STAGE_A_BYTES + kStageB + ((kFp4 || kPair) ? 0u : SF_UE8_OFFSET);
+  auto copy_scale_factors = [&](int stage) {
+    const uint32_t sf = tmem_base + SF_COL0 + stage * kSfCols;
+    const uint32_t src = smem_u32(stage_mem + size_t(stage) * kStageBytes) + kSfSrc;
+#pragma unroll
+    for (int blk = 0; blk < kSfBlocks; ++blk) {
+      const uint64_t d = sdesc_noswizzle(src + blk * SF_UE8_BLOCK, 16, 128);
+      if constexpr (kPair)
+        tmem_cp_pair_32x128b_warpx4(sf + 4 * blk, d);
+      else
+        tmem_cp_32x128b_warpx4(sf + 4 * blk, d);
+    }
+  };
+  // CTA pairs, warp 10 of the even CTA, per stage: wait for the stage's operands and prepared scale
+  // factors, copy the scale factors and commit them to sf_full, the one barrier the MMA thread
+  // waits on. (Every tcgen05 instruction holds its issuing thread for tens of cycles: next to its
+  // four MMAs, its wait and its commit, the MMA thread has no room for the copies within the 512
+  // cycles those MMAs run.) The stage's columns are free again by then: the producers reload a
+  // stage only after the MMAs that read it have completed. Returns false (in every lane) on timeout
+  // or abort.
+  auto hand_off_scale_factors = [&](int stage, uint32_t phase) -> bool {
+    int good = 1;
+    if (lane == 0) {
+      good = wait_bounded_t<kPair>(&ctl->full[stage], phase, abort_flag, p.timeout_ns) ? 1 : 0;
+      if (good) {
+        tc_fence_after();
+        copy_scale_factors(stage);
+        mma_commit_pair(&ctl->sf_full[stage], 0x1);
+      }
+    }
+    return __shfl_sync(0xffffffffu, good, 0) != 0;
+  };
+  // warp 10's copies complete before TMEM is released
+  auto drain_scale_copies = [&]() {
+    if (lane == 0) {
+      mma_commit_pair(&ctl->cp_done, 0x1);
+      int dummy = 0;
+      wait_bounded_t<kPair>(&ctl->cp_done, 0, &dummy, p.timeout_ns);
+    }
+    __syncwarp();
   };
 
   if (warp == 0) {
@@ -1413,54 +1466,47 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = it.kbeg; kb < it.kend; ++kb) {
-          if (!wait_bounded_t<kPair>(&ctl->full[stage], phase, abort_flag, p.timeout_ns)) {
+          // FP8 pairs: warp 10's barrier, which it completes only after the operands landed
+          if (!wait_bounded_t<kPair>((kFp8 && kPair) ? &ctl->sf_full[stage] : &ctl->full[stage], phase, abort_flag,
+                                     p.timeout_ns)) {
             ok = false;
             break;
           }
           if constexpr (kFp8 && !kPair) {
-            if (!wait_bounded_t<kPair>(&ctl->sf_full[stage], phase, abort_flag, p.timeout_ns)) {
+            // single CTA: the converter has written the stage's scale factors in TMEM order
+            if (!wait_bounded(&ctl->sf_full[stage], phase, abort_flag, p.timeout_ns)) {
               ok = false;
               break;
             }
           }
           tc_fence_after();
+          // single CTA: the copies come first in this thread's order, so its MMAs see them
+          if constexpr (kFp8 && !kPair) copy_scale_factors(stage);
           const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * kStageBytes);
           const uint32_t b_addr = a_addr + STAGE_A_BYTES;
           if constexpr (kFp8 && kPair) {
-            // the stage's 3 scale-factor blocks -> TMEM columns 4i of the stage's 12 in both CTAs
-            // (each CTA's own shared memory to its own TMEM); MMA k uses byte k of every word (the
-            // FP32 scales' byte is repeated, packed UE8M0 words hold one per 32-token block)
+            // the stage's scale factors are in TMEM columns 4i of the stage's 12 in both CTAs; MMA k
+            // uses byte k of every word (the FP32 scales' byte is repeated, packed UE8M0 words hold
+            // one per 32-token block)
             const uint32_t sfa = tmem_base + SF_COL0 + stage * SF_STAGE_COLS;
-            const uint32_t ue8 = b_addr + kStageB;
-#pragma unroll
-            for (int blk = 0; blk < 3; ++blk)
-              tmem_cp_pair_32x128b_warpx4(sfa + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_mxf8_pair(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k),
                             idesc | idesc_sf_id(static_cast<uint32_t>(k)), sfa, sfa + SF_A_COLS,
                             (kb > it.kbeg || k > 0) ? 1u : 0u);
           } else if constexpr (kNv) {
-            // 12 scale blocks of this stage -> TMEM columns 4i of the stage's 48; MMA k (64 tokens)
-            // reads A block 3k (columns 12k..12k+3) and B blocks 3k+1, 3k+2 (12k+4..12k+11), all
-            // four UE4M3 bytes of each column
+            // the stage's 12 scale blocks are in TMEM columns 4i of its 48; MMA k (64 tokens) reads
+            // A block 3k (columns 12k..12k+3) and B blocks 3k+1, 3k+2 (12k+4..12k+11), all four
+            // UE4M3 bytes of each column
             const uint32_t sf = tmem_base + SF_COL0 + stage * SF_STAGE_COLS_NV;
-            const uint32_t ue8 = b_addr + kStageB;
-#pragma unroll
-            for (int blk = 0; blk < 12; ++blk)
-              tmem_cp_32x128b_warpx4(sf + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_nvf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc, sf + 12 * k,
                        sf + 12 * k + 4, (kb > it.kbeg || k > 0) ? 1u : 0u);
           } else if constexpr (kFp4) {
-            // 6 scale blocks of this stage -> TMEM columns 4i of the stage's 24; MMA k (64 tokens)
-            // reads word k/2 of A (columns 0/4) and B (8/16), byte pair (k%2)*2 of it
+            // the stage's 6 scale blocks are in TMEM columns 4i of its 24; MMA k (64 tokens) reads
+            // word k/2 of A (columns 0/4) and B (8/16), byte pair (k%2)*2 of it
             const uint32_t sf = tmem_base + SF_COL0 + stage * SF_STAGE_COLS_FP4;
-            const uint32_t ue8 = b_addr + kStageB;
-#pragma unroll
-            for (int blk = 0; blk < 6; ++blk)
-              tmem_cp_32x128b_warpx4(sf + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               mma_mxf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k),
@@ -1469,11 +1515,6 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           } else if constexpr (kFp8) {
             const uint32_t sfa = tmem_base + SF_COL0 + stage * SF_STAGE_COLS;
             const uint32_t sfb = sfa + SF_A_COLS;
-            // scale factors of this stage: shared memory (TMEM layout) -> TMEM, in order before the MMAs
-            const uint32_t ue8 = b_addr + kStageB + SF_UE8_OFFSET;
-#pragma unroll
-            for (int blk = 0; blk < 3; ++blk)
-              tmem_cp_32x128b_warpx4(sfa + 4 * blk, sdesc_noswizzle(ue8 + blk * SF_UE8_BLOCK, 16, 128));
 #pragma unroll
             for (int k = 0; k < 4; ++k)  // packed scales: MMA k uses byte k (its 32-token block)
               mma_mxf8(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k),
@@ -1558,12 +1599,14 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       if (!__all_sync(0xffffffffu, okt)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + col0;
+      // (the peer's arrive is relaxed: the accumulator's TMEM loads have completed, and the
+      // hand-back publishes nothing)
       auto release_acc = [&]() {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           if (kPair && !leader)
-            mbar_arrive_remote(leader_tempty0);
+            mbar_arrive_remote_relaxed(leader_tempty0);
           else
             mbar_arrive(&ctl->tempty[0]);
         }
@@ -1751,13 +1794,14 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       const int acc = kFp8 ? 0 : (tcount & 1);
       const uint32_t use = kFp8 ? static_cast<uint32_t>(tcount) : static_cast<uint32_t>(tcount >> 1);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
-      // This warp has read its 32 TMEM lanes: hand the accumulator back to the MMA issuer.
+      // This warp has read its 32 TMEM lanes: hand the accumulator back to the MMA issuer (the
+      // peer's arrive is relaxed: the loads have completed, and the hand-back publishes nothing).
       auto release_acc = [&]() {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           if (kPair && !leader)
-            mbar_arrive_remote(leader_tempty0 + acc * 8);
+            mbar_arrive_remote_relaxed(leader_tempty0 + acc * 8);
           else
             mbar_arrive(&ctl->tempty[acc]);
         }
@@ -2102,6 +2146,37 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         }
         if (!ok) break;
       }
+    }
+  }
+
+  if constexpr (kFp8 && kPair) {
+    if (warp == SF_WARP && leader) {
+      // ======================= scale-factor copier of a CTA pair (warp 10, even CTA) ==============
+      // the prepared scale factors arrive by TMA with the operands; warp 10 only copies them to TMEM
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int n = 0;; ++n) {
+        const int slot = n % WORK_RING;
+        const bool okw = wait_bounded_t<kPair>(&ctl->wfull[slot], (n / WORK_RING) & 1, abort_flag, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, okw)) break;
+        const Item it = ctl->work[slot];
+        __syncwarp();
+        if (lane == 0) release_slot(slot);
+        if (it.e < 0) break;
+        bool ok = true;
+        for (int kb = it.kbeg; kb < it.kend; ++kb) {
+          if (!hand_off_scale_factors(stage, phase)) {
+            ok = false;
+            break;
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      drain_scale_copies();
     }
   }
 

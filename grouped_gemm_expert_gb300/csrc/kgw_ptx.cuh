@@ -117,6 +117,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local_addr, uint32_t ra
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Remote arrive without release semantics: it orders none of this thread's earlier memory
+// operations. For a hand-back that publishes no data and whose earlier reads have completed
+// (TMEM loads waited with tcgen05.wait::ld). A cluster-scope release here costs the arriving thread
+// about a microsecond (measured on GB300), the relaxed arrive a few hundred nanoseconds.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 __device__ __forceinline__ void st_cluster_s32(uint32_t cluster_addr, int32_t v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
