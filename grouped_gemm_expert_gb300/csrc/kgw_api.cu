@@ -79,21 +79,22 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int bk_of(bool fp8) { return fp8 ? kgw::BK_FP8 : kgw::BK_BF16; }
 
-// Rows of a work tile: BF16 and FP8 problems whose hidden size is a multiple of 256 run on CTA
-// pairs (FP4 and NVFP4 on single CTAs).
-int32_t tile_rows(const kgw_wgrad_args* a, bool fp8, bool fp4 = false) {
-  if (!fp4 && a->hidden % (2 * kgw::BM) == 0 && g_single_cta.load() == 0) return 2 * kgw::BM;
+// Rows of a work tile: BF16, FP8 and FP4 problems whose hidden size is a multiple of 256 run on
+// CTA pairs (NVFP4 on single CTAs).
+int32_t tile_rows(const kgw_wgrad_args* a, bool fp8, bool fp4 = false, bool nv = false) {
+  if (!nv && a->hidden % (2 * kgw::BM) == 0 && g_single_cta.load() == 0) return 2 * kgw::BM;
   (void)fp8;
+  (void)fp4;
   return kgw::BM;
 }
 
-// Scale rows reserved for the prepared scale words of FP8 on CTA pairs: at least the sum over
-// experts of ceil(n_e / 128), which tokens_sum / 128 + E bounds.
+// Scale rows reserved for the prepared scale words of FP8 and FP4 on CTA pairs: at least the sum
+// over experts of ceil(n_e / 128), which tokens_sum / 128 + E bounds.
 int64_t prep_rows(const kgw_wgrad_args* a) { return a->tokens_sum / kgw::SCALE_BLOCK + a->num_experts; }
 
 // Upper bound of the FP32 partial tiles split-K can use for these shapes.
-int32_t slot_cap(const kgw_wgrad_args* a, bool fp8, bool fp4 = false) {
-  const int64_t T = int64_t(a->hidden / tile_rows(a, fp8, fp4)) * (a->intermediate / kgw::BN);
+int32_t slot_cap(const kgw_wgrad_args* a, bool fp8, bool fp4 = false, bool nv = false) {
+  const int64_t T = int64_t(a->hidden / tile_rows(a, fp8, fp4, nv)) * (a->intermediate / kgw::BN);
   const int64_t kit = a->tokens_sum / bk_of(fp8);
   // an expert is split only when its k-iterations exceed the chunk (>= MIN_SPLIT_KITERS), and
   // then into fewer than 2*kiters/chunk pieces
@@ -184,7 +185,7 @@ int64_t unaligned_count_multiple(const kgw_wgrad_args* a, bool fp8 = false, bool
 }
 
 kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float* sfb, void* ws,
-                   size_t ws_bytes, Prepared* P, bool fp4 = false, bool tail = false) {
+                   size_t ws_bytes, Prepared* P, bool fp4 = false, bool tail = false, bool nv = false) {
   const int64_t count_align = tail ? unaligned_count_multiple(a, fp8, fp4) : kgw::TOKEN_ALIGN;
   kgw_status st = validate(a, fp8, fp4, count_align);
   if (st != KGW_OK) return st;
@@ -194,14 +195,14 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return KGW_ERR_ALIGNMENT;
   }
   if (!ws || !aligned(ws, 256)) return KGW_ERR_WORKSPACE;
-  const int32_t tile_m = tile_rows(a, fp8, fp4);
+  const int32_t tile_m = tile_rows(a, fp8, fp4, nv);
   const int32_t halves = tile_m / kgw::BM;
-  // FP8 on CTA pairs: prepared scale words of every scale row in the workspace
-  const bool fp8_pair = fp8 && !fp4 && halves == 2;
+  // FP8 and FP4 on CTA pairs: prepared scale words of every scale row in the workspace
+  const bool fp8_pair = fp8 && halves == 2;
   const int64_t sf_rows = fp8_pair ? prep_rows(a) : 0;
   const WsLayout L0 = kgw::ws_layout(a->num_experts, 0, halves, sf_rows, a->hidden, a->intermediate);
   if (ws_bytes < L0.total) return KGW_ERR_WORKSPACE;
-  int32_t max_slots = slot_cap(a, fp8, fp4);
+  int32_t max_slots = slot_cap(a, fp8, fp4, nv);
   {
     const size_t room = ws_bytes - L0.total;
     const size_t fit = room / (halves * (kgw::PARTIAL_TILE_BYTES + 4 * kgw::EPI_COUNTERS));
@@ -251,7 +252,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     if (fp4 && !ragged) {
       // packed e2m1: the tensors count bytes along the token axis (two tokens per byte)
       st = encode_2d(&P->tmA, dt, a->a, Ts / 2, H, Ts / 2, 128, kgw::BM);             // [H, tokens/2]
-      if (st == KGW_OK) st = encode_2d(&P->tmB, dt, a->b, Ts / 2, I, Ts / 2, 128, kgw::BN);  // [I, tokens/2]
+      if (st == KGW_OK) st = encode_2d(&P->tmB, dt, a->b, Ts / 2, I, Ts / 2, 128, b_rows_cta);  // [I, tokens/2]
       if (st != KGW_OK) return st;
     }
     // A (ragged packed FP4: per-expert [hidden, n_e/2]-byte blocks, through the templates below)
@@ -379,7 +380,7 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
                const float* gscale_a = nullptr, const float* gscale_b = nullptr) {
   if ((gscale_a && !aligned(gscale_a, 4)) || (gscale_b && !aligned(gscale_b, 4))) return KGW_ERR_ALIGNMENT;
   Prepared P;
-  kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P, fp4, tail);
+  kgw_status st = prepare(a, fp8, sfa, sfb, ws, ws_bytes, &P, fp4, tail, nvfp4);
   if (st != KGW_OK) return st;
   P.mp.sf_packed = sf_packed;
   P.mp.nvfp4 = nvfp4;
@@ -391,7 +392,8 @@ kgw_status run(const kgw_wgrad_args* a, bool fp8, const float* sfa, const float*
   P.mp.general_dispatch = general;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kgw::launch_plan(P.pp, P.tpl, s) != cudaSuccess) return KGW_ERR_CUDA;
-  // the scale kernel: the FP32 power-of-two check, and the prepared scale words of FP8 pairs
+  // the scale kernel: the FP32 power-of-two check, and the prepared scale words of FP8 and FP4
+  // pairs (with the NaN-byte check of packed words)
   if ((general || P.mp.sf_prep) && a->tokens_sum > 0 && kgw::launch_scale_check(P.mp, 4 * P.grid, s) != cudaSuccess)
     return KGW_ERR_CUDA;
   if (general && P.mp.sf_prep && a->tokens_sum > 0 && kgw::launch_promote_kernel(P.mp, P.tmA, P.tmB, P.grid, s) != cudaSuccess)

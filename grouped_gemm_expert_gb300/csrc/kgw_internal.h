@@ -79,6 +79,12 @@ constexpr uint32_t SF_STAGE_COLS_FP4 = 24;
 // they arrive by TMA from the prepared words in the workspace, on the operands' barrier.
 constexpr uint32_t SF_SMEM_PAD_PAIR = 2048;
 constexpr uint32_t SF_PAIR_BYTES = 3 * SF_UE8_BLOCK;
+// FP4 on CTA pairs: the stage's two 128-token blocks, laid out as on single CTAs ([A word 0]
+// [A word 1][B word 0: columns 0..127, 128..255][B word 1: likewise], 3 KiB); five stages of 35 KiB
+// fit beside the epilogue staging.
+constexpr uint32_t SF_SMEM_PAD_PAIR_FP4 = 3072;
+constexpr uint32_t SF_PAIR_BYTES_FP4 = 6 * SF_UE8_BLOCK;
+constexpr int STAGES_PAIR_FP4 = 5;
 constexpr uint32_t SF_SMEM_BYTES_NV = 4 * (BM + BN) * 4;
 constexpr uint32_t SF_SMEM_PAD_NV = 6144;
 constexpr uint32_t SF_STAGE_COLS_NV = 48;
@@ -249,7 +255,7 @@ cudaError_t launch_plan_mgrouped(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                  cudaStream_t s);
 constexpr int MG_ROW_ALIGN = 128;   // every group's row count is a multiple of the 128-row tile
-size_t main_smem_bytes(bool pair, bool fp8, bool nv = false);
+size_t main_smem_bytes(bool pair, bool fp8, bool nv = false, bool fp4 = false);
 bool fp8_supported();
 
 }  // namespace kgw

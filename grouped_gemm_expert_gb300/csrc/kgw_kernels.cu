@@ -541,8 +541,9 @@ struct SmemCtl {
 constexpr uint32_t EPI_STAGE_TOTAL = 16384;
 constexpr uint32_t EPI_STAGE_BYTES = EPI_STAGE_TOTAL / NUM_EPI_WARPS;
 
-size_t main_smem_bytes(bool pair, bool fp8, bool nv) {
-  const size_t ring = pair ? size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + (fp8 ? SF_SMEM_PAD_PAIR : 0u))
+size_t main_smem_bytes(bool pair, bool fp8, bool nv, bool fp4) {
+  const size_t ring = pair ? (fp4 ? size_t(STAGES_PAIR_FP4) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_FP4)
+                                  : size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + (fp8 ? SF_SMEM_PAD_PAIR : 0u)))
                       : nv ? size_t(STAGES_NV) * (STAGE_BYTES + SF_SMEM_PAD_NV)
                            : size_t(STAGES) * (STAGE_BYTES + (fp8 ? SF_SMEM_PAD : 0u));
   return ring + EPI_STAGE_TOTAL + 1024 /* alignment slack */ + sizeof(SmemCtl) + 64;
@@ -1129,16 +1130,20 @@ template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4
 __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
-  // FP8 on CTA pairs: K-grouped e4m3 with scale factors prepared in TMEM order by the scale kernel
-  // and loaded by TMA with the operands (FP4, NVFP4 and the M-grouped FP8 GEMM run on single CTAs).
-  static_assert(!(kFp8 && kPair) || (!kFp4 && !kMG), "block-scaled CTA pairs: K-grouped FP8 only");
+  // FP8 and FP4 on CTA pairs: K-grouped, with the scale factors prepared in TMEM order by the scale
+  // kernel and loaded by TMA with the operands (NVFP4 and the M-grouped FP8 GEMM run on single CTAs).
+  static_assert(!(kFp8 && kPair) || (!kNv && !kMG), "block-scaled CTA pairs: K-grouped FP8 and FP4 only");
   static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
   static_assert(!kNv || kFp4, "NVFP4 is the FP4 kernel with UE4M3 scales");
-  constexpr int kStages = kPair ? STAGES_PAIR : (kNv ? STAGES_NV : STAGES);
+  constexpr int kStages = kPair ? (kFp4 ? STAGES_PAIR_FP4 : STAGES_PAIR) : (kNv ? STAGES_NV : STAGES);
   constexpr uint32_t kStageB = kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
-  constexpr uint32_t kStageBytes =
-      STAGE_A_BYTES + kStageB + (kNv ? SF_SMEM_PAD_NV : (kFp8 ? (kPair ? SF_SMEM_PAD_PAIR : SF_SMEM_PAD) : 0u));
-  constexpr uint32_t kStageTx = STAGE_A_BYTES + kStageB + (kFp8 && kPair ? SF_PAIR_BYTES : 0u);
+  constexpr uint32_t kSfPad = kNv ? SF_SMEM_PAD_NV
+                              : !kFp8 ? 0u
+                              : kPair ? (kFp4 ? SF_SMEM_PAD_PAIR_FP4 : SF_SMEM_PAD_PAIR)
+                                      : SF_SMEM_PAD;
+  constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB + kSfPad;
+  constexpr uint32_t kStageTx =
+      STAGE_A_BYTES + kStageB + (kFp8 && kPair ? (kFp4 ? SF_PAIR_BYTES_FP4 : SF_PAIR_BYTES) : 0u);
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
   constexpr int kHalves = kPair ? 2 : 1;
   constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
@@ -1341,7 +1346,18 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           const int32_t b_tok = kMG ? it.e * p.K + kb * bk : static_cast<int32_t>(tok);
           // scales first: they are small and land before the operand tiles, so the converter's
           // work is done by the time the MMA has its operands
-          if constexpr (kFp8 && kPair) {
+          if constexpr (kFp8 && kPair && kFp4) {
+            // prepared scale factors of this 256-token stage's two 128-token blocks, in TMEM order:
+            // [A block 0][A block 1][B block 0 (all 256 columns)][B block 1]; when the expert's last
+            // stage holds a single block, block 1 repeats block 0 (its second half is zero-filled)
+            const int32_t kblk = it.srow + 2 * kb;
+            const int32_t kblk1 = (2 * int64_t(kb) + 1) * SCALE_BLOCK < it.n_e ? kblk + 1 : kblk;
+            uint8_t* sS = sB + kStageB;
+            load(sS, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk);
+            load(sS + SF_UE8_BLOCK, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk1);
+            load(sS + 2 * SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk);
+            load(sS + 4 * SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk1);
+          } else if constexpr (kFp8 && kPair) {
             // prepared scale factors of this 128-token block, in TMEM order: this CTA's A rows and
             // all 256 B columns, by TMA onto the leader's barrier with the operands
             const int32_t kblk = it.srow + kb;
@@ -1431,7 +1447,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       uint32_t phase = 0;
       int tcount = 0;
       constexpr uint32_t a_mn = kAK ? 0u : 1u, b_mn = kBK ? 0u : 1u;
-      const uint32_t idesc = kNv ? idesc_nvf4(BM, BN) : kFp4 ? idesc_mxf4(BM, BN)
+      const uint32_t idesc = kNv ? idesc_nvf4(BM, BN) : kFp4 ? idesc_mxf4(BM * kHalves, BN)
                              : kFp8 ? idesc_mxf8(BM * kHalves, BN, a_mn, b_mn, 0)
                                     : idesc_bf16_f32(BM * kHalves, BN, a_mn, b_mn);
       // Shared-memory operand descriptors (128-byte swizzle). K-major: 128-byte rows, 8-row groups
@@ -1484,7 +1500,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           if constexpr (kFp8 && !kPair) copy_scale_factors(stage);
           const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * kStageBytes);
           const uint32_t b_addr = a_addr + STAGE_A_BYTES;
-          if constexpr (kFp8 && kPair) {
+          if constexpr (kFp8 && kPair && !kFp4) {
             // the stage's scale factors are in TMEM columns 4i of the stage's 12 in both CTAs; MMA k
             // uses byte k of every word (the FP32 scales' byte is repeated, packed UE8M0 words hold
             // one per 32-token block)
@@ -1508,10 +1524,16 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             // word k/2 of A (columns 0/4) and B (8/16), byte pair (k%2)*2 of it
             const uint32_t sf = tmem_base + SF_COL0 + stage * SF_STAGE_COLS_FP4;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_mxf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k),
-                       idesc | idesc_sf_id(static_cast<uint32_t>(k & 1) * 2u), sf + 4 * (k >> 1), sf + 8 + 8 * (k >> 1),
-                       (kb > it.kbeg || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t id = idesc | idesc_sf_id(static_cast<uint32_t>(k & 1) * 2u);
+              const uint32_t acc_in = (kb > it.kbeg || k > 0) ? 1u : 0u;
+              if constexpr (kPair)
+                mma_mxf4_pair(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), id,
+                              sf + 4 * (k >> 1), sf + 8 + 8 * (k >> 1), acc_in);
+              else
+                mma_mxf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), id,
+                         sf + 4 * (k >> 1), sf + 8 + 8 * (k >> 1), acc_in);
+            }
           } else if constexpr (kFp8) {
             const uint32_t sfa = tmem_base + SF_COL0 + stage * SF_STAGE_COLS;
             const uint32_t sfb = sfa + SF_A_COLS;
@@ -2254,7 +2276,7 @@ template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
   auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG, kFp4, kNv>;
-  size_t smem = main_smem_bytes(kPair, kFp8, kNv);
+  size_t smem = main_smem_bytes(kPair, kFp8, kNv, kFp4);
   // the K-grouped FP8 kernel also hosts the promotion path, which lays out the same memory its own way
   if (kFp8 && !kFp4 && !kMG && promote_smem_bytes() > smem) smem = promote_smem_bytes();
   // set on every launch: the attribute is per device and the call is cheap
@@ -2317,6 +2339,7 @@ cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const C
 cudaError_t launch_main_fp4(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s) {
   if (p.nvfp4) return launch_main<true, false, true, true, false, true, true>(p, tmA, tmB, grid, s);
+  if (p.tile_m == 2 * BM) return launch_main<true, true, true, true, false, true>(p, tmA, tmB, grid, s);
   return launch_main<true, false, true, true, false, true>(p, tmA, tmB, grid, s);
 }
 

@@ -358,3 +358,28 @@ def test_fp8_pair_tiles_agree_with_single_cta_tiles(kw):
     ref, S = oracle_full(w, x_cpu)
     assert_close_to_oracle(w, to_f64(pair), ref, S)
     assert_close_to_oracle(w, to_f64(single), ref, S)
+
+
+@pytest.mark.parametrize("kw", [dict(out_dtype="bf16"), dict(input_order="ragged", accumulate=True),
+                                dict(unaligned=True, out_dtype="bf16")],
+                         ids=["tensor2d_bf16", "ragged_accumulate_f32", "unaligned_counts"])
+def test_fp4_pair_tiles_agree_with_single_cta_tiles(kw):
+    """FP4 problems whose hidden size is a multiple of 256 run on CTA pairs (scale factors prepared
+    by the scale kernel, two 128-token blocks per stage); forced onto single-CTA tiles they give
+    the same result within the FP32 accumulation bound, and both match the oracle. The unaligned
+    case ends experts on a stage that holds a single scale block (384 and 96 tokens)."""
+    kgw = ensure_built()
+    counts = [384, 0, 1280, 96] if kw.get("unaligned") else [768, 0, 1280, 512]
+    w = W.custom(4, 512, 512, counts, seed=127, fp4=True, b_major="k", sf_format="ue8m0_32", **kw)
+    x = W.make_inputs(w, DEV)
+    x_cpu = W.make_inputs(w, "cpu")
+    pair = run_gpu(w, x, DEV).stacked().clone()
+    prev = kgw.kgw_debug_set(3, 1)
+    try:
+        single = run_gpu(w, x, DEV).stacked().clone()
+    finally:
+        kgw.kgw_debug_set(3, prev)
+    torch.cuda.synchronize()
+    ref, S = oracle_full(w, x_cpu)
+    assert_close_to_oracle(w, to_f64(pair), ref, S)
+    assert_close_to_oracle(w, to_f64(single), ref, S)
