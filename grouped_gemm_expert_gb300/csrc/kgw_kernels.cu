@@ -239,10 +239,8 @@ __global__ void __launch_bounds__(PLAN_THREADS)
   }
   __syncthreads();
 
-  // 5. order: rank the experts longest item first (ties by expert index), then interleave the two
-  //    ends of that list -- longest, shortest, second longest, second shortest, ... A short
-  //    expert's tiles finish their MMAs faster than the epilogue drains an accumulator; taken in
-  //    turn with long tiles, their epilogues run under the long tiles' MMAs instead of back to back.
+  // 5. order: rank the experts longest item first (ties by expert index), so that the longest
+  //    items start in the first wave and the short ones fill the tail of the schedule.
   for (int e = tid; e < E; e += blockDim.x) {
     const int key = s_key[e];
     int rank = 0;
