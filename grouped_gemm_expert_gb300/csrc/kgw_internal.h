@@ -38,6 +38,10 @@ constexpr int NUM_EPI_WARPS = 4;
 constexpr int NUM_EPI_WARPS_FP8 = 8;
 constexpr int EPI_COUNTERS = 8;    // split-K arrival counters per (tile, CTA half): one per epilogue warp
 constexpr int WORK_RING = 8;       // depth of the shared-memory work-item queue
+// Items the scheduler may claim and decode ahead of the item the producer is on: decoding an item
+// is a chain of dependent global loads (microseconds), longer than the loads of a short expert's
+// tile take to issue.
+constexpr int SCHED_LOOKAHEAD = 2;
 
 constexpr int MAX_EXPERTS = 4096;
 constexpr int PLAN_THREADS = 1024;

@@ -19,6 +19,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 #include <type_traits>
 
@@ -515,6 +516,60 @@ __device__ __forceinline__ Item decode_item(const MainParams& p, int idx, int bk
   return it;
 }
 
+// K-grouped item idx, decoded by a whole warp (every lane returns the item decode_item gives).
+// The item lies in the largest ordered expert position q with prefix[q] <= idx. A warp's claims only
+// grow, so q is at or after the position of its previous item (lo_hint, updated here): one 32-wide
+// window of the prefix sums and a ballot find it (the window slides only past 31 experts;
+// prefix[E], the item total, exceeds every idx). Then the expert's index, and its split count,
+// token range and first scale row in parallel: three rounds of global loads instead of a dozen
+// dependent ones.
+__device__ __forceinline__ Item decode_item_warp(const MainParams& p, int idx, int bk, int& lo_hint, int lane) {
+  const int32_t* order = reinterpret_cast<const int32_t*>(p.ws + p.L.order);
+  const int32_t* prefix = reinterpret_cast<const int32_t*>(p.ws + p.L.item_prefix);
+  const int32_t* splits = reinterpret_cast<const int32_t*>(p.ws + p.L.splits);
+  const int32_t* scale_row = reinterpret_cast<const int32_t*>(p.ws + p.L.scale_row);
+  int lo = lo_hint;
+  int base = 0;
+  for (;;) {
+    const int q = lo + lane;
+    const int v = q <= p.E ? __ldg(prefix + q) : INT_MAX;
+    const int cnt = __popc(__ballot_sync(0xffffffffu, v <= idx));  // lanes 0..cnt-1 (prefix is non-decreasing)
+    if (cnt < 32) {
+      base = __shfl_sync(0xffffffffu, v, cnt - 1);
+      lo += cnt - 1;
+      break;
+    }
+    lo += 31;
+  }
+  lo_hint = lo;
+  Item it;
+  it.e = __ldg(order + lo);
+  int32_t w = 0;
+  if (lane == 0) w = __ldg(splits + it.e);
+  if (lane == 1) w = it.e ? __ldg(p.offsets + it.e - 1) : 0;
+  if (lane == 2) w = __ldg(p.offsets + it.e);
+  if (lane == 3) w = __ldg(scale_row + it.e);
+  it.nsplit = __shfl_sync(0xffffffffu, w, 0);
+  it.begin = static_cast<int64_t>(__shfl_sync(0xffffffffu, w, 1));
+  it.n_e = static_cast<int64_t>(__shfl_sync(0xffffffffu, w, 2)) - it.begin;
+  it.srow = __shfl_sync(0xffffffffu, w, 3);
+  const int local = idx - base;
+  it.rows = p.tile_m;
+  it.m1 = 0;
+  it.rows1 = 0;
+  const int T = p.num_m_tiles * p.num_n_tiles;
+  it.split = local / T;
+  it.tile = local - it.split * T;
+  const int mt = it.tile / p.num_n_tiles;
+  const int nt = it.tile - mt * p.num_n_tiles;
+  it.m0 = mt * p.tile_m;
+  it.n0 = nt * BN;
+  const int64_t kit = (it.n_e + bk - 1) / bk;  // a partial last stage counts (zero-filled tail)
+  it.kbeg = static_cast<int>(it.split * kit / it.nsplit);
+  it.kend = static_cast<int>((it.split + 1) * kit / it.nsplit);
+  return it;
+}
+
 struct SmemCtl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
@@ -528,10 +583,10 @@ struct SmemCtl {
                                 // the stage's operands landed (on the even CTA)
   uint64_t sfdata[MAX_STAGES];  // block-scaled: this CTA's raw scales of a stage have landed in shared memory
   uint64_t cp_done;             // CTA pair: warp 10's last scale-factor copies have completed
-  uint64_t sched_go;            // the producer has started an item: the scheduler may claim the next
   Item work[WORK_RING];         // decoded work items (written by the scheduler of the leader CTA)
   uint32_t tmem_base;
   int32_t abort_flag;
+  int32_t items_started;        // items the producer (of the leader CTA) has started
 };
 
 // Epilogue staging: 16 KiB per CTA, split over its epilogue warps (4 x 32 rows x 32 FP32, or in the
@@ -1189,7 +1244,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       // block-scaled kernels warp 10 (of the even CTA in a pair)
       mbar_init(&ctl->wempty[w], kHalves * (1 + kEpiWarps) + 1 + (kFp8 ? 1 : 0));
     }
-    mbar_init(&ctl->sched_go, 1);
+    ctl->items_started = 0;
     mbar_init(&ctl->mma_done, 1);
     mbar_init(&ctl->cp_done, 1);
     for (int st = 0; st < kStages; ++st) {
@@ -1298,7 +1353,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         release_slot(slot);
-        if (leader && it.e >= 0) mbar_arrive(&ctl->sched_go);  // the scheduler may claim the next item
+        // the scheduler may claim further items
+        if (leader && it.e >= 0) *reinterpret_cast<volatile int32_t*>(&ctl->items_started) = n + 1;
       }
       if (it.e < 0) break;
       // ragged + K-major operand: the expert's own descriptor, coordinates relative to its block
@@ -2202,35 +2258,64 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
 
   if (warp == (kFp8 ? SCHED_WARP_FP8 : SCHED_WARP)) {
     // ======================= Scheduler (leader CTA) =======================
-    // Claims items from the call's atomic counter one item ahead of the producer (the claim for
-    // item n+1 waits until the producer has started item n, so no CTA hoards work at the end of the
-    // queue), decodes each item once -- a binary search over the plan's prefix sums and a few reads
-    // of the offsets, a chain of dependent global loads -- and publishes the decoded item in the
-    // work ring of this CTA and of its peer, while the current item's k-loop runs.
-    if (lane == 0 && leader) {
-      int cur = atomicAdd(item_counter, 1);
+    // Claims items from the call's atomic counter up to SCHED_LOOKAHEAD items ahead of the producer
+    // (the claim for item n+1 waits until the producer has started item n+1-SCHED_LOOKAHEAD, so no
+    // CTA hoards more than that at the end of the queue, where the items are the shortest), decodes
+    // each item once with the whole warp (decode_item_warp) and publishes it in the work ring of
+    // this CTA and of its peer, while the current items' k-loops run.
+    if (leader) {
+      int lo_hint = 0;
+      int cur = 0;
+      if (lane == 0) cur = atomicAdd(item_counter, 1);
+      cur = __shfl_sync(0xffffffffu, cur, 0);
       for (int n = 0;; ++n) {
         const int slot = n % WORK_RING;
         Item it;
         if (cur < total_items) {
-          it = decode_item<kMG>(p, cur, bk);
+          if constexpr (kMG)
+            it = decode_item<kMG>(p, cur, bk);
+          else
+            it = decode_item_warp(p, cur, bk, lo_hint, lane);
         } else {
           it = Item{};
           it.e = -1;
         }
-        if (!wait_bounded_t<kPair>(&ctl->wempty[slot], ((n / WORK_RING) & 1) ^ 1, abort_flag, p.timeout_ns)) break;
-        ctl->work[slot] = it;
-        if constexpr (kPair) {
-          const uint32_t dst = mapa_shared(smem_u32(&ctl->work[slot]), 1);
-          const uint4* w = reinterpret_cast<const uint4*>(&ctl->work[slot]);
+        int ok = 1;
+        if (lane == 0) {
+          ok = wait_bounded_t<kPair>(&ctl->wempty[slot], ((n / WORK_RING) & 1) ^ 1, abort_flag, p.timeout_ns) ? 1 : 0;
+          if (ok) {
+            ctl->work[slot] = it;
+            if constexpr (kPair) {
+              const uint32_t dst = mapa_shared(smem_u32(&ctl->work[slot]), 1);
+              const uint4* w = reinterpret_cast<const uint4*>(&ctl->work[slot]);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) st_cluster_v4(dst + 16 * i, w[i]);
-          mbar_arrive_remote(mapa_shared(smem_u32(&ctl->wfull[slot]), 1));
+              for (int i = 0; i < 4; ++i) st_cluster_v4(dst + 16 * i, w[i]);
+              mbar_arrive_remote(mapa_shared(smem_u32(&ctl->wfull[slot]), 1));
+            }
+            mbar_arrive(&ctl->wfull[slot]);
+          }
         }
-        mbar_arrive(&ctl->wfull[slot]);
-        if (it.e < 0) break;
-        if (!wait_bounded_t<kPair>(&ctl->sched_go, n & 1, abort_flag, p.timeout_ns)) break;
-        cur = atomicAdd(item_counter, 1);
+        if (!__shfl_sync(0xffffffffu, ok, 0) || it.e < 0) break;
+        // claim item n+1 once the producer has started item n+1-SCHED_LOOKAHEAD (bounded wait)
+        int go = 1;
+        if (lane == 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (*reinterpret_cast<volatile int32_t*>(&ctl->items_started) < n + 2 - SCHED_LOOKAHEAD) {
+            if (*abort_flag) {
+              go = 0;
+              break;
+            }
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+              *abort_flag = 1;
+              go = 0;
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (go) cur = atomicAdd(item_counter, 1);
+        }
+        if (!__shfl_sync(0xffffffffu, go, 0)) break;
+        cur = __shfl_sync(0xffffffffu, cur, 0);
       }
     }
   }
