@@ -189,7 +189,9 @@ def algorithmic_bytes(w) -> int:
     ts = w.tokens_sum
     counts = np.asarray(w.counts)
     blocks = int(np.sum(-(-counts // 128)))   # 128-token scale blocks of all experts (ts/128 when aligned)
-    if w.fp4:   # e2m1 two per byte, one UE8M0 byte per 32 tokens (a 4-byte word per 128-token block)
+    if w.fp4 and w.sf_format == "ue4m3_16":   # NVFP4: one UE4M3 byte per 16 tokens (a word per 64)
+        b = (w.hidden + w.intermediate) * ts // 2 + (w.hidden + w.intermediate) * int(np.sum(-(-counts // 64))) * 4
+    elif w.fp4:   # e2m1 two per byte, one UE8M0 byte per 32 tokens (a 4-byte word per 128-token block)
         b = (w.hidden + w.intermediate) * ts // 2 + (w.hidden + w.intermediate) * blocks * 4
     else:
         b = (w.hidden + w.intermediate) * ts * (1 if w.fp8 else 2)
@@ -286,6 +288,8 @@ def run_ours(args, w, rank, local, world):
             kgw.kgw_wgrad_fp4_unaligned(args, sfa, sfb, ws, stream=s)
         elif w.fp8 and w.unaligned:
             kgw.kgw_wgrad_fp8_unaligned(args, sfa, sfb, 1 if w.sf_format == "ue8m0_32" else 0, ws, stream=s)
+        elif w.fp4 and w.sf_format == "ue4m3_16":
+            kgw.kgw_wgrad_nvfp4(args, sfa, sfb, x.gsa, x.gsb, ws, stream=s)
         elif w.fp4:
             kgw.kgw_wgrad_fp4_ue8m0(args, sfa, sfb, ws, stream=s)
         elif w.fp8 and w.sf_format == "ue8m0_32":

@@ -30,10 +30,12 @@ def _closed_form(name):
         return (H + I) * T + (H + I) * (T // 128) * 4 + E * H * I * 2
     if name == "fp4":           # e2m1 (two per byte) + one UE8M0 byte per 32 tokens per row/column, BF16 out
         return (H + I) * T // 2 + (H + I) * (T // 32) + E * H * I * 2
+    if name == "nvfp4":         # e2m1 (two per byte) + one UE4M3 byte per 16 tokens per row/column, BF16 out
+        return (H + I) * T // 2 + (H + I) * (T // 16) + E * H * I * 2
     raise KeyError(name)
 
 
-@pytest.mark.parametrize("name", ["balanced", "wide", "skewed", "fp8", "fp4"])
+@pytest.mark.parametrize("name", ["balanced", "wide", "skewed", "fp8", "fp4", "nvfp4"])
 def test_algorithmic_bytes_match_closed_forms(name):
     assert bench.algorithmic_bytes(W.NAMED[name]()) == _closed_form(name)
 
