@@ -79,22 +79,22 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int bk_of(bool fp8) { return fp8 ? kgw::BK_FP8 : kgw::BK_BF16; }
 
-// Rows of a work tile: BF16, FP8 and FP4 problems whose hidden size is a multiple of 256 run on
-// CTA pairs (NVFP4 on single CTAs).
-int32_t tile_rows(const kgw_wgrad_args* a, bool fp8, bool fp4 = false, bool nv = false) {
-  if (!nv && a->hidden % (2 * kgw::BM) == 0 && g_single_cta.load() == 0) return 2 * kgw::BM;
-  (void)fp8;
-  (void)fp4;
+// Rows of a work tile: problems whose hidden size is a multiple of 256 run on CTA pairs.
+int32_t tile_rows(const kgw_wgrad_args* a) {
+  if (a->hidden % (2 * kgw::BM) == 0 && g_single_cta.load() == 0) return 2 * kgw::BM;
   return kgw::BM;
 }
 
-// Scale rows reserved for the prepared scale words of FP8 and FP4 on CTA pairs: at least the sum
-// over experts of ceil(n_e / 128), which tokens_sum / 128 + E bounds.
-int64_t prep_rows(const kgw_wgrad_args* a) { return a->tokens_sum / kgw::SCALE_BLOCK + a->num_experts; }
+// Scale rows reserved for the prepared scale words of block-scaled calls on CTA pairs: at least the
+// sum over experts of ceil(n_e / 128), which tokens_sum / 128 + E bounds; NVFP4 has two 64-token
+// word rows per 128-token block.
+int64_t prep_rows(const kgw_wgrad_args* a, bool nv = false) {
+  return (a->tokens_sum / kgw::SCALE_BLOCK + a->num_experts) * (nv ? 2 : 1);
+}
 
 // Upper bound of the FP32 partial tiles split-K can use for these shapes.
-int32_t slot_cap(const kgw_wgrad_args* a, bool fp8, bool fp4 = false, bool nv = false) {
-  const int64_t T = int64_t(a->hidden / tile_rows(a, fp8, fp4, nv)) * (a->intermediate / kgw::BN);
+int32_t slot_cap(const kgw_wgrad_args* a, bool fp8) {
+  const int64_t T = int64_t(a->hidden / tile_rows(a)) * (a->intermediate / kgw::BN);
   const int64_t kit = a->tokens_sum / bk_of(fp8);
   // an expert is split only when its k-iterations exceed the chunk (>= MIN_SPLIT_KITERS), and
   // then into fewer than 2*kiters/chunk pieces
@@ -195,14 +195,14 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     if (!aligned(sfa, 16) || !aligned(sfb, 16)) return KGW_ERR_ALIGNMENT;
   }
   if (!ws || !aligned(ws, 256)) return KGW_ERR_WORKSPACE;
-  const int32_t tile_m = tile_rows(a, fp8, fp4, nv);
+  const int32_t tile_m = tile_rows(a);
   const int32_t halves = tile_m / kgw::BM;
-  // FP8 and FP4 on CTA pairs: prepared scale words of every scale row in the workspace
+  // block-scaled calls on CTA pairs: prepared scale words of every scale row in the workspace
   const bool fp8_pair = fp8 && halves == 2;
-  const int64_t sf_rows = fp8_pair ? prep_rows(a) : 0;
+  const int64_t sf_rows = fp8_pair ? prep_rows(a, nv) : 0;
   const WsLayout L0 = kgw::ws_layout(a->num_experts, 0, halves, sf_rows, a->hidden, a->intermediate);
   if (ws_bytes < L0.total) return KGW_ERR_WORKSPACE;
-  int32_t max_slots = slot_cap(a, fp8, fp4, nv);
+  int32_t max_slots = slot_cap(a, fp8);
   {
     const size_t room = ws_bytes - L0.total;
     const size_t fit = room / (halves * (kgw::PARTIAL_TILE_BYTES + 4 * kgw::EPI_COUNTERS));
@@ -593,10 +593,10 @@ kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t
   if (!bytes) return KGW_ERR_INVALID_ARG;
   kgw_status st = validate(args, is_fp8 != 0, false, 1);  // sizing only: the call checks its own count rule
   if (st != KGW_OK) return st;
-  // is_fp8 sizes the FP8 and the FP4 entries alike: the larger need (FP8 on CTA pairs, with its
-  // prepared scale words) covers both
-  const int32_t halves = tile_rows(args, is_fp8 != 0) / kgw::BM;
-  const int64_t sf_rows = (is_fp8 != 0 && halves == 2) ? prep_rows(args) : 0;
+  // is_fp8 sizes the FP8, FP4 and NVFP4 entries alike: the largest need (NVFP4 on CTA pairs, with
+  // two prepared word rows per 128-token block) covers all three
+  const int32_t halves = tile_rows(args) / kgw::BM;
+  const int64_t sf_rows = (is_fp8 != 0 && halves == 2) ? prep_rows(args, true) : 0;
   *bytes = kgw::ws_layout(args->num_experts, slot_cap(args, is_fp8 != 0), halves, sf_rows, args->hidden,
                           args->intermediate).total;
   return KGW_OK;

@@ -89,6 +89,13 @@ constexpr uint32_t SF_PAIR_BYTES = 3 * SF_UE8_BLOCK;
 constexpr uint32_t SF_SMEM_PAD_PAIR_FP4 = 3072;
 constexpr uint32_t SF_PAIR_BYTES_FP4 = 6 * SF_UE8_BLOCK;
 constexpr int STAGES_PAIR_FP4 = 5;
+// NVFP4 on CTA pairs: the stage's four 64-token scale words as the single-CTA converter lays them
+// out (for each MMA k: [A word k][B word k: columns 0..127, 128..255]), 6 KiB; five stages of
+// 38 KiB; 48 TMEM scale columns per stage (NVFP4 keeps no 16-bit holding area, so they may reach
+// column 511).
+constexpr uint32_t SF_SMEM_PAD_PAIR_NV = 6144;
+constexpr uint32_t SF_PAIR_BYTES_NV = 12 * SF_UE8_BLOCK;
+constexpr int STAGES_PAIR_NV = 5;
 constexpr uint32_t SF_SMEM_BYTES_NV = 4 * (BM + BN) * 4;
 constexpr uint32_t SF_SMEM_PAD_NV = 6144;
 constexpr uint32_t SF_STAGE_COLS_NV = 48;

@@ -595,7 +595,8 @@ constexpr uint32_t EPI_STAGE_TOTAL = 16384;
 constexpr uint32_t EPI_STAGE_BYTES = EPI_STAGE_TOTAL / NUM_EPI_WARPS;
 
 size_t main_smem_bytes(bool pair, bool fp8, bool nv, bool fp4) {
-  const size_t ring = pair ? (fp4 ? size_t(STAGES_PAIR_FP4) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_FP4)
+  const size_t ring = pair && nv ? size_t(STAGES_PAIR_NV) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_NV)
+                      : pair ? (fp4 ? size_t(STAGES_PAIR_FP4) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_FP4)
                                   : size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + (fp8 ? SF_SMEM_PAD_PAIR : 0u)))
                       : nv ? size_t(STAGES_NV) * (STAGE_BYTES + SF_SMEM_PAD_NV)
                            : size_t(STAGES) * (STAGE_BYTES + (fp8 ? SF_SMEM_PAD : 0u));
@@ -713,16 +714,19 @@ __device__ __forceinline__ char* out_row_ptr(const MainParams& p, const Item& it
 //  - FP32 scales: a scale that is not a positive power of two UE8M0 can hold sets general_scales
 //    (the FP8 kernel then takes its promotion path); a NaN or infinite scale is KGW_ERR_SCALES;
 //  - packed UE8M0 words: a byte 0xFF (NaN) is KGW_ERR_SCALES;
-//  - FP8 on CTA pairs (p.sf_prep): writes the UE8M0 scale factors in TMEM order into the workspace,
-//    so that a pair stage loads them by TMA: within each group of 128 rows (columns), word 4l + c
-//    holds row 32c + l, the FP32 scale's exponent byte repeated four times or the packed word.
+//  - block-scaled calls on CTA pairs (p.sf_prep): writes the scale factors in TMEM order into the
+//    workspace, so that a pair stage loads them by TMA: within each group of 128 rows (columns),
+//    word 4l + c holds row 32c + l, the FP32 scale's exponent byte repeated four times or the
+//    packed word (UE8M0; NVFP4: UE4M3, two 64-token word rows per 128-token block, each byte
+//    checked for a set top bit or the NaN code 0x7F).
 // One work unit is such a 4-word group entry: four coalesced loads (32 rows apart), one 16-byte store.
 __global__ void __launch_bounds__(256) scale_check_kernel(const __grid_constant__ MainParams p) {
   pdl_launch_dependents();
   pdl_wait();
   PlanHeader* hdr = reinterpret_cast<PlanHeader*>(p.ws);
   if (hdr->error != 0) return;
-  const int64_t rows = hdr->scale_rows;
+  // (NVFP4: two 64-token word rows per 128-token scale block)
+  const int64_t rows = int64_t(hdr->scale_rows) * (p.nvfp4 ? 2 : 1);
   const int64_t ua = rows * (p.H / 4), ub = rows * (p.I / 4);
   const uint32_t* sa = reinterpret_cast<const uint32_t*>(p.sfa);
   const uint32_t* sb = reinterpret_cast<const uint32_t*>(p.sfb);
@@ -743,7 +747,9 @@ __global__ void __launch_bounds__(256) scale_check_kernel(const __grid_constant_
     for (int c = 0; c < 4; ++c) w[c] = __ldg(src + 32 * c);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      if (p.sf_packed) {
+      if (p.nvfp4) {   // UE4M3: no byte with its top bit set, none equal to 0x7F (NaN)
+        bad |= (w[c] & 0x80808080u) | (((w[c] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u);
+      } else if (p.sf_packed) {
         bad |= ff_bytes(w[c]);
       } else {
         const uint32_t e = (w[c] >> 23) & 0xFFu, m = w[c] & 0x7FFFFFu;
@@ -1183,20 +1189,22 @@ template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4
 __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
-  // FP8 and FP4 on CTA pairs: K-grouped, with the scale factors prepared in TMEM order by the scale
-  // kernel and loaded by TMA with the operands (NVFP4 and the M-grouped FP8 GEMM run on single CTAs).
-  static_assert(!(kFp8 && kPair) || (!kNv && !kMG), "block-scaled CTA pairs: K-grouped FP8 and FP4 only");
+  // FP8, FP4 and NVFP4 on CTA pairs: K-grouped, with the scale factors prepared in TMEM order by
+  // the scale kernel and loaded by TMA with the operands (the M-grouped FP8 GEMM runs on single CTAs).
+  static_assert(!(kFp8 && kPair) || !kMG, "block-scaled CTA pairs: K-grouped only");
   static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
   static_assert(!kNv || kFp4, "NVFP4 is the FP4 kernel with UE4M3 scales");
-  constexpr int kStages = kPair ? (kFp4 ? STAGES_PAIR_FP4 : STAGES_PAIR) : (kNv ? STAGES_NV : STAGES);
+  constexpr int kStages =
+      kPair ? (kNv ? STAGES_PAIR_NV : kFp4 ? STAGES_PAIR_FP4 : STAGES_PAIR) : (kNv ? STAGES_NV : STAGES);
   constexpr uint32_t kStageB = kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
-  constexpr uint32_t kSfPad = kNv ? SF_SMEM_PAD_NV
+  constexpr uint32_t kSfPad = kNv ? (kPair ? SF_SMEM_PAD_PAIR_NV : SF_SMEM_PAD_NV)
                               : !kFp8 ? 0u
                               : kPair ? (kFp4 ? SF_SMEM_PAD_PAIR_FP4 : SF_SMEM_PAD_PAIR)
                                       : SF_SMEM_PAD;
   constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB + kSfPad;
   constexpr uint32_t kStageTx =
-      STAGE_A_BYTES + kStageB + (kFp8 && kPair ? (kFp4 ? SF_PAIR_BYTES_FP4 : SF_PAIR_BYTES) : 0u);
+      STAGE_A_BYTES + kStageB +
+      (kFp8 && kPair ? (kNv ? SF_PAIR_BYTES_NV : kFp4 ? SF_PAIR_BYTES_FP4 : SF_PAIR_BYTES) : 0u);
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
   constexpr int kHalves = kPair ? 2 : 1;
   constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
@@ -1400,7 +1408,18 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           const int32_t b_tok = kMG ? it.e * p.K + kb * bk : static_cast<int32_t>(tok);
           // scales first: they are small and land before the operand tiles, so the converter's
           // work is done by the time the MMA has its operands
-          if constexpr (kFp8 && kPair && kFp4) {
+          if constexpr (kFp8 && kPair && kNv) {
+            // prepared UE4M3 scale factors of this 256-token stage's four 64-token words, in TMEM
+            // order: for each MMA k, [A word k][B word k (all 256 columns)]; word rows are the
+            // expert's 64-token groups
+            const int32_t w0 = 2 * it.srow + 4 * kb;
+            uint8_t* sS = sB + kStageB;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              load(sS + 3 * j * SF_UE8_BLOCK, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, w0 + j);
+              load(sS + (3 * j + 1) * SF_UE8_BLOCK, &p.tm_sfb, it.n0, w0 + j);
+            }
+          } else if constexpr (kFp8 && kPair && kFp4) {
             // prepared scale factors of this 256-token stage's two 128-token blocks, in TMEM order:
             // [A block 0][A block 1][B block 0 (all 256 columns)][B block 1]; when the expert's last
             // stage holds a single block, block 1 repeats block 0 (its second half is zero-filled)
@@ -1501,7 +1520,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
       uint32_t phase = 0;
       int tcount = 0;
       constexpr uint32_t a_mn = kAK ? 0u : 1u, b_mn = kBK ? 0u : 1u;
-      const uint32_t idesc = kNv ? idesc_nvf4(BM, BN) : kFp4 ? idesc_mxf4(BM * kHalves, BN)
+      const uint32_t idesc = kNv ? idesc_nvf4(BM * kHalves, BN) : kFp4 ? idesc_mxf4(BM * kHalves, BN)
                              : kFp8 ? idesc_mxf8(BM * kHalves, BN, a_mn, b_mn, 0)
                                     : idesc_bf16_f32(BM * kHalves, BN, a_mn, b_mn);
       // Shared-memory operand descriptors (128-byte swizzle). K-major: 128-byte rows, 8-row groups
@@ -1570,9 +1589,15 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             // UE4M3 bytes of each column
             const uint32_t sf = tmem_base + SF_COL0 + stage * SF_STAGE_COLS_NV;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_nvf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc, sf + 12 * k,
-                       sf + 12 * k + 4, (kb > it.kbeg || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t acc_in = (kb > it.kbeg || k > 0) ? 1u : 0u;
+              if constexpr (kPair)
+                mma_nvf4_pair(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc,
+                              sf + 12 * k, sf + 12 * k + 4, acc_in);
+              else
+                mma_nvf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc, sf + 12 * k,
+                         sf + 12 * k + 4, acc_in);
+            }
           } else if constexpr (kFp4) {
             // the stage's 6 scale blocks are in TMEM columns 4i of its 24; MMA k (64 tokens) reads
             // word k/2 of A (columns 0/4) and B (8/16), byte pair (k%2)*2 of it
@@ -2421,6 +2446,7 @@ cudaError_t launch_main_fp8(const MainParams& p, const CUtensorMap& tmA, const C
 
 cudaError_t launch_main_fp4(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                             cudaStream_t s) {
+  if (p.nvfp4 && p.tile_m == 2 * BM) return launch_main<true, true, true, true, false, true, true>(p, tmA, tmB, grid, s);
   if (p.nvfp4) return launch_main<true, false, true, true, false, true, true>(p, tmA, tmB, grid, s);
   if (p.tile_m == 2 * BM) return launch_main<true, true, true, true, false, true>(p, tmA, tmB, grid, s);
   return launch_main<true, false, true, true, false, true>(p, tmA, tmB, grid, s);

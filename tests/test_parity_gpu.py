@@ -101,6 +101,11 @@ CASES = {
                            sf_format="ue8m0_32", input_order="ragged", out_dtype="bf16"),
     "fp4_ragged_split_k_f32": W.custom(2, 128, 256, [24576, 512], seed=116, fp4=True, b_major="k",
                                        sf_format="ue8m0_32", input_order="ragged"),
+    # CTA-pair tiles (hidden 256) with the long expert split along K
+    "fp4_pair_split_k_f32": W.custom(2, 256, 256, [32768, 512], seed=128, fp4=True, b_major="k",
+                                     sf_format="ue8m0_32"),
+    "nvfp4_pair_split_k_accumulate": W.custom(2, 256, 256, [32768, 512], seed=129, fp4=True, b_major="k",
+                                              sf_format="ue4m3_16", accumulate=True),
     "fp8_general_scales_bf16": W.custom(4, 256, 512, [512, 0, 768, 1024], seed=120, fp8=True, sf_format="f32_any",
                                         out_dtype="bf16"),
     "fp8_general_mn_a_k_b_accumulate_f32": W.custom(3, 256, 768, [256, 1280, 512], seed=121, fp8=True,
@@ -272,20 +277,24 @@ def test_fp4_rejects_unsupported_layouts():
         assert kgw.kgw_wgrad_fp4_ue8m0(args, x.sfa, x.sfb, ws, check=False) == kgw.KGW_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("kind", ["fp8_f32_nan", "fp8_ue8m0_nan", "fp4_ue8m0_nan", "nvfp4_sign_bit"])
-def test_bad_scales_are_reported(kind):
-    """A NaN FP32 scale, a UE8M0 byte 0xFF (NaN) or an invalid UE4M3 byte anywhere in the scale
-    tensors is reported as KGW_ERR_SCALES; clean scales report KGW_OK."""
+@pytest.mark.parametrize("hidden", [256, 384], ids=["pair", "single_cta"])
+@pytest.mark.parametrize("kind", ["fp8_f32_nan", "fp8_ue8m0_nan", "fp4_ue8m0_nan", "nvfp4_sign_bit", "nvfp4_nan_byte"])
+def test_bad_scales_are_reported(kind, hidden):
+    """A NaN FP32 scale, a UE8M0 byte 0xFF (NaN) or an invalid UE4M3 byte (top bit set, or the NaN
+    code 0x7F) anywhere in the scale tensors is reported as KGW_ERR_SCALES; clean scales report
+    KGW_OK. Hidden 256 runs CTA pairs (the scale kernel checks the scales it prepares), hidden 384
+    single CTAs (the converter warp checks them)."""
     kgw = ensure_built()
+    H = hidden
     if kind == "fp8_f32_nan":
-        w = W.custom(3, 256, 512, [512, 256, 768], seed=140, fp8=True, out_dtype="bf16")
+        w = W.custom(3, H, 512, [512, 256, 768], seed=140, fp8=True, out_dtype="bf16")
     elif kind == "fp8_ue8m0_nan":
-        w = W.custom(3, 256, 512, [512, 256, 768], seed=141, fp8=True, sf_format="ue8m0_32", out_dtype="bf16")
+        w = W.custom(3, H, 512, [512, 256, 768], seed=141, fp8=True, sf_format="ue8m0_32", out_dtype="bf16")
     elif kind == "fp4_ue8m0_nan":
-        w = W.custom(3, 256, 512, [512, 256, 768], seed=142, fp4=True, b_major="k", sf_format="ue8m0_32",
+        w = W.custom(3, H, 512, [512, 256, 768], seed=142, fp4=True, b_major="k", sf_format="ue8m0_32",
                      out_dtype="bf16")
     else:
-        w = W.custom(3, 256, 512, [512, 256, 768], seed=143, fp4=True, b_major="k", sf_format="ue4m3_16",
+        w = W.custom(3, H, 512, [512, 256, 768], seed=143, fp4=True, b_major="k", sf_format="ue4m3_16",
                      out_dtype="bf16")
     x = W.make_inputs(w, DEV)
     status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
@@ -302,6 +311,8 @@ def test_bad_scales_are_reported(kind):
         words[-1, 300] = int(np.array([0x7FFF7F7F], dtype=np.uint32).view(np.int32)[0])
     if kind == "nvfp4_sign_bit":
         words[-1, 300] = int(np.array([0x38B83838], dtype=np.uint32).view(np.int32)[0])   # 0xB8: sign bit set
+    if kind == "nvfp4_nan_byte":
+        words[-1, 300] = int(np.array([0x387F3838], dtype=np.uint32).view(np.int32)[0])   # 0x7F: UE4M3 NaN
     x2 = W.Inputs(x.a, x.b, x.offsets, x.sfa, sfb, x.c, x.gsa, x.gsb)
     status.fill_(-1)
     run_gpu(w, x2, DEV, status=status)
@@ -361,16 +372,22 @@ def test_fp8_pair_tiles_agree_with_single_cta_tiles(kw):
 
 
 @pytest.mark.parametrize("kw", [dict(out_dtype="bf16"), dict(input_order="ragged", accumulate=True),
-                                dict(unaligned=True, out_dtype="bf16")],
-                         ids=["tensor2d_bf16", "ragged_accumulate_f32", "unaligned_counts"])
+                                dict(unaligned=True, out_dtype="bf16"),
+                                dict(sf_format="ue4m3_16", out_dtype="bf16"),
+                                dict(sf_format="ue4m3_16", input_order="ragged")],
+                         ids=["tensor2d_bf16", "ragged_accumulate_f32", "unaligned_counts", "nvfp4_tensor2d_bf16",
+                              "nvfp4_ragged_f32"])
 def test_fp4_pair_tiles_agree_with_single_cta_tiles(kw):
-    """FP4 problems whose hidden size is a multiple of 256 run on CTA pairs (scale factors prepared
-    by the scale kernel, two 128-token blocks per stage); forced onto single-CTA tiles they give
-    the same result within the FP32 accumulation bound, and both match the oracle. The unaligned
-    case ends experts on a stage that holds a single scale block (384 and 96 tokens)."""
+    """FP4 and NVFP4 problems whose hidden size is a multiple of 256 run on CTA pairs (scale
+    factors prepared by the scale kernel: two 128-token blocks per stage, NVFP4 four 64-token
+    words); forced onto single-CTA tiles they give the same result within the FP32 accumulation
+    bound, and both match the oracle. The unaligned case ends experts on a stage that holds a
+    single scale block (384 and 96 tokens)."""
     kgw = ensure_built()
     counts = [384, 0, 1280, 96] if kw.get("unaligned") else [768, 0, 1280, 512]
-    w = W.custom(4, 512, 512, counts, seed=127, fp4=True, b_major="k", sf_format="ue8m0_32", **kw)
+    kw = dict(kw)
+    sf_format = kw.pop("sf_format", "ue8m0_32")
+    w = W.custom(4, 512, 512, counts, seed=127, fp4=True, b_major="k", sf_format=sf_format, **kw)
     x = W.make_inputs(w, DEV)
     x_cpu = W.make_inputs(w, "cpu")
     pair = run_gpu(w, x, DEV).stacked().clone()
