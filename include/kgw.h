@@ -99,14 +99,15 @@ typedef struct kgw_wgrad_args {
 } kgw_wgrad_args;
 
 /*
- * Workspace bytes needed by kgw_wgrad_bf16 (is_fp8 = 0) or kgw_wgrad_fp8_blockscaled
- * (is_fp8 = 1) for these shapes. Depends only on num_experts, hidden, intermediate and
- * tokens_sum (not on the offsets' values). Host-only; never touches the GPU.
+ * Workspace bytes needed by kgw_wgrad_bf16 (is_fp8 = 0) or by the block-scaled entries
+ * (is_fp8 = 1: FP8, FP4 and NVFP4) for these shapes. Depends only on num_experts, hidden,
+ * intermediate and tokens_sum (not on the offsets' values). Host-only; never touches the GPU.
  * The workspace holds the per-call schedule of the dynamic persistent scheduler ("Grouped GEMM +
- * WGrad (Unified)", section "Scheduling, cache, and errors") and the FP32 partial tiles of
- * split-K; a caller may pass less than this (down to the schedule alone) and the kernel then
- * splits less. Errors as for the calls it sizes (KGW_ERR_INVALID_ARG, KGW_ERR_UNSUPPORTED,
- * KGW_ERR_ALIGNMENT); *bytes is written only on KGW_OK.
+ * WGrad (Unified)", section "Scheduling, cache, and errors"), for block-scaled calls on CTA pairs
+ * (hidden % 256 == 0) the scale factors prepared in TMEM order, and the FP32 partial tiles of
+ * split-K; a caller may pass less than this (down to the schedule and the prepared scale
+ * factors) and the kernel then splits less. Errors as for the calls it sizes (KGW_ERR_INVALID_ARG,
+ * KGW_ERR_UNSUPPORTED, KGW_ERR_ALIGNMENT); *bytes is written only on KGW_OK.
  */
 kgw_status kgw_workspace_size(const kgw_wgrad_args* args, int32_t is_fp8, size_t* bytes);
 
@@ -350,8 +351,8 @@ int32_t kgw_version(void);
  * Testing hooks (process-wide, host side). key 1: device wait limit in nanoseconds
  * (default 2e9); key 2: when >= 0, the TMA producer of CTA 0 skips the arrival of that
  * k-iteration so that the bounded wait path is exercised (default -1); key 3: non-zero runs every
- * BF16 call (K- and M-grouped) on single-CTA 128-row tiles (default 0). Returns the previous
- * value, or -1 for an unknown key.
+ * call that would use 256-row CTA-pair tiles (K-grouped BF16, FP8, FP4 and NVFP4; M-grouped BF16)
+ * on single-CTA 128-row tiles (default 0). Returns the previous value, or -1 for an unknown key.
  */
 int64_t kgw_debug_set(int32_t key, int64_t value);
 

@@ -44,6 +44,38 @@ def test_max_experts_k_grouped():
     assert not bad, f"experts out of tolerance: {bad[:8]}"
 
 
+def test_max_experts_k_grouped_accumulate():
+    """4096 experts accumulating into BF16, one in sixteen with 256 tokens: the empty experts have
+    no work items (their prefix sums repeat, so the scheduler's expert search crosses runs of
+    fifteen equal entries), their outputs must stay bit-identical, and every element of the
+    others must match C + the oracle's product."""
+    kgw = ensure_built()
+    E = 4096
+    counts = np.where(np.arange(E) % 16 == 5, 256, 0)
+    w = W.custom(E, 128, 256, counts, seed=161, out_dtype="bf16", accumulate=True)
+    x_cpu = W.make_inputs(w, "cpu")
+    x = W.Inputs(x_cpu.a.to(DEV), x_cpu.b.to(DEV), x_cpu.offsets.to(DEV), c=x_cpu.c.to(DEV))
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    outs = run_gpu(w, x, DEV, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, kgw.kgw_status_string(int(status.item()))
+    assert outs.guards_intact()
+    empty = torch.from_numpy(counts == 0).to(DEV)
+    assert torch.equal(outs.dense[empty].view(torch.int16), x.c[empty].view(torch.int16)), \
+        "an empty expert's accumulated output changed"
+    a_bits, b_bits = bits16(x_cpu.a), bits16(x_cpu.b)
+    c64 = x_cpu.c.to(torch.float64).numpy()
+    bad = []
+    for e in np.nonzero(counts)[0]:
+        r, s = O.expert_from_storage(a_bits, b_bits, w.offsets, 128, 256, int(e))
+        ref = c64[e] + r
+        got = to_f64(outs.dense[e])
+        tol = O.tolerance(s, ref, "bf16")
+        if not np.all(np.abs(got - ref) <= tol):
+            bad.append(int(e))
+    assert not bad, f"experts out of tolerance: {bad[:8]}"
+
+
 def test_max_groups_m_grouped():
     kgw = ensure_built()
     G = 4096
