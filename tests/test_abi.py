@@ -159,3 +159,26 @@ def test_noalloc_rejects_more_experts_than_its_scratch_holds():
     assert kgw.lib().kgw_wgrad_bf16_noalloc(ctypes.byref(args), None) == kgw.KGW_ERR_SCRATCH_LIMIT
     bad = good_args(num_experts=1024, hidden=100)
     assert kgw.lib().kgw_wgrad_bf16_noalloc(ctypes.byref(bad), None) == kgw.KGW_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("entry", ["fp8", "fp4", "nvfp4"])
+def test_block_scaled_pairs_need_room_for_the_prepared_scale_factors(entry):
+    """Block-scaled calls on CTA pairs (hidden % 256 == 0) keep their scale factors, prepared in
+    TMEM order, in the workspace: a workspace that holds only the schedule is KGW_ERR_WORKSPACE on
+    the host, before any device query, while a BF16 call of the same shape passes with it; the size
+    kgw_workspace_size gives (is_fp8 = 1) passes the host checks, and the call then stops at the
+    device check here, without a GPU."""
+    args = good_args(hidden=256, tokens_sum=65536, b_major=kgw.KGW_K_MAJOR)
+    L = kgw.lib()
+    small = 64 * 1024   # the schedule of 4 experts fits; 516 prepared scale rows of 512 words do not
+
+    def call(nbytes):
+        if entry == "fp8":
+            return L.kgw_wgrad_fp8_blockscaled(ctypes.byref(args), FAKE, FAKE, FAKE, nbytes, None)
+        if entry == "fp4":
+            return L.kgw_wgrad_fp4_ue8m0(ctypes.byref(args), FAKE, FAKE, FAKE, nbytes, None)
+        return L.kgw_wgrad_nvfp4(ctypes.byref(args), FAKE, FAKE, None, None, FAKE, nbytes, None)
+
+    assert call(small) == kgw.KGW_ERR_WORKSPACE
+    assert rc_bf16(args, nbytes=small) in (kgw.KGW_ERR_DEVICE, kgw.KGW_ERR_CUDA)
+    assert call(kgw.kgw_workspace_size(args, True)) in (kgw.KGW_ERR_DEVICE, kgw.KGW_ERR_CUDA)
