@@ -219,11 +219,14 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   if (dev.major != 10 || dev.minor != 3) return KGW_ERR_DEVICE;
   if (get_encoder() != KGW_OK) return KGW_ERR_CUDA;
 
-  const int bk = fp4 ? kgw::BK_FP4 : bk_of(fp8);
+  // k-iteration length in tokens (K-grouped BF16 on CTA pairs, aligned entries: 128 tokens per stage)
+  const bool wide_k = !fp8 && halves == 2 && !tail;
+  const int bk = fp4 ? kgw::BK_FP4 : fp8 ? kgw::BK_FP8 : (wide_k ? kgw::BK_BF16_PAIR : kgw::BK_BF16);
   const uint64_t esz = fp8 ? 1 : 2;
   // token-axis box of a K-major operand in descriptor elements: one 128-byte swizzle row (packed
-  // FP4 descriptors count bytes, so its 256 tokens are 128 elements)
-  const uint32_t box_k = fp4 ? 128u : static_cast<uint32_t>(bk);
+  // FP4 descriptors count bytes, so its 256 tokens are 128 elements; a 128-token BF16 stage loads
+  // two such boxes)
+  const uint32_t box_k = fp4 ? 128u : fp8 ? static_cast<uint32_t>(bk) : static_cast<uint32_t>(kgw::BK_BF16);
   std::memset(&P->tmA, 0, sizeof(P->tmA));
   std::memset(&P->tmB, 0, sizeof(P->tmB));
   std::memset(&P->tpl, 0, sizeof(P->tpl));
@@ -258,7 +261,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     // A (ragged packed FP4: per-expert [hidden, n_e/2]-byte blocks, through the templates below)
     if (fp4 && !ragged) {
     } else if (a_k && !ragged) {
-      st = encode_2d(&P->tmA, dt, a->a, Ts, H, Ts * esz, bk, kgw::BM);             // [H, tokens]
+      st = encode_2d(&P->tmA, dt, a->a, Ts, H, Ts * esz, box_k, kgw::BM);          // [H, tokens]
     } else if (a_k) {
       st = templates(a->a, H, kgw::BM, &P->tpl.a_small, &P->tpl.a_large);
       P->tmA = P->tpl.a_small;
@@ -269,7 +272,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
     // B
     if (fp4 && !ragged) {
     } else if (b_k && !ragged) {
-      st = encode_2d(&P->tmB, dt, a->b, Ts, I, Ts * esz, bk, b_rows_cta);         // [I, tokens]
+      st = encode_2d(&P->tmB, dt, a->b, Ts, I, Ts * esz, box_k, b_rows_cta);      // [I, tokens]
     } else if (b_k) {
       st = templates(a->b, I, b_rows_cta, &P->tpl.b_small, &P->tpl.b_large);
       P->tmB = P->tpl.b_small;
@@ -359,6 +362,7 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   mp.L = L;
   mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
   mp.test_drop_stage = static_cast<int32_t>(g_drop_stage.load());
+  mp.wide_k = wide_k ? 1 : 0;
   mp.tail_a = pp.tail_a;
   mp.tail_b = pp.tail_b;
   mp.sf_prep = fp8_pair;
@@ -582,6 +586,7 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
   mp.L = L;
   mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
   mp.test_drop_stage = -1;
+  mp.wide_k = 0;
   return kgw::launch_main_mgrouped(mp, tmA, tmB, grid, s) == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
 }
 
@@ -764,7 +769,8 @@ int32_t kgw_debug_check_tail_maps_kind(const kgw_wgrad_args* args, int32_t kind,
                                        box_rows)
                      : mode == 1 ? encode_2d(&ref, dt, base, static_cast<uint64_t>(end) / tpu, rows, Ts / tpu * esz,
                                              box_k, box_rows)
-                                 : encode_2d(&ref, dt, base, rows, static_cast<uint64_t>(end), rows * esz, atom, box_k);
+                                 : encode_2d(&ref, dt, base, rows, static_cast<uint64_t>(end), rows * esz, atom,
+                                             static_cast<uint32_t>(P.pp.bk));   // MN-major: k-iteration rows
       if (r != KGW_OK) {
         std::free(dev_maps);
         return -KGW_ERR_CUDA;

@@ -14,6 +14,13 @@ namespace kgw {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK_BF16 = 64;    // 64 bf16 = 128 bytes
+// K-grouped BF16 on CTA pairs, aligned entries: 128-token stages (two 128-byte rows of K per
+// operand row, eight MMAs), three of 64 KiB per CTA. The MMA thread pays its barrier wait and its
+// commit once per eight MMAs instead of four, and those instructions hold it for about as long as
+// MMAs do. The unaligned entry keeps 64-token stages: an expert's last stage is partly zero-filled,
+// and a longer stage wastes more MMA work.
+constexpr int BK_BF16_PAIR = 128;
+constexpr int STAGES_PAIR_BF16 = 3;
 constexpr int BK_FP8 = 128;    // 128 e4m3 = 128 bytes = one scale block
 constexpr int BK_FP4 = 256;    // 256 e2m1 = 128 bytes = two 128-token scale words
 constexpr int STAGES = 4;          // single-CTA ring: 4 x 48 KiB
@@ -243,6 +250,7 @@ struct MainParams {
   WsLayout L;
   uint64_t timeout_ns;
   int32_t test_drop_stage;      // test hook: >=0 makes the producer skip one arrival (timeout path)
+  int32_t wide_k;               // K-grouped BF16 on CTA pairs with 128-token stages (aligned entries)
 };
 
 // Launchers (kgw_kernels.cu).
@@ -266,7 +274,7 @@ cudaError_t launch_plan_mgrouped(const PlanParams& p, cudaStream_t s);
 cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                  cudaStream_t s);
 constexpr int MG_ROW_ALIGN = 128;   // every group's row count is a multiple of the 128-row tile
-size_t main_smem_bytes(bool pair, bool fp8, bool nv = false, bool fp4 = false);
+size_t main_smem_bytes(bool pair, bool fp8, bool nv = false, bool fp4 = false, bool wide_k = false);
 bool fp8_supported();
 
 }  // namespace kgw

@@ -594,8 +594,9 @@ struct SmemCtl {
 constexpr uint32_t EPI_STAGE_TOTAL = 16384;
 constexpr uint32_t EPI_STAGE_BYTES = EPI_STAGE_TOTAL / NUM_EPI_WARPS;
 
-size_t main_smem_bytes(bool pair, bool fp8, bool nv, bool fp4) {
-  const size_t ring = pair && nv ? size_t(STAGES_PAIR_NV) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_NV)
+size_t main_smem_bytes(bool pair, bool fp8, bool nv, bool fp4, bool wide_k) {
+  const size_t ring = pair && wide_k ? size_t(STAGES_PAIR_BF16) * (2 * STAGE_A_BYTES + STAGE_B_BYTES)
+                      : pair && nv ? size_t(STAGES_PAIR_NV) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_NV)
                       : pair ? (fp4 ? size_t(STAGES_PAIR_FP4) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_FP4)
                                   : size_t(STAGES_PAIR) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + (fp8 ? SF_SMEM_PAD_PAIR : 0u)))
                       : nv ? size_t(STAGES_NV) * (STAGE_BYTES + SF_SMEM_PAD_NV)
@@ -1185,7 +1186,8 @@ cudaError_t launch_scale_check(const MainParams& p, int grid, cudaStream_t s) {
 // to e2m1 operands (kind::mxf4, 256 tokens per stage, K-major A and B, UE8M0 words only); kNv
 // makes that NVFP4 (kind::mxf4nvf4 scale_vec::4X: UE4M3 scales per 16 tokens, 48 TMEM scale
 // columns per stage, 3 stages, per-tensor global scales applied in the epilogue).
-template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false, bool kNv = false>
+template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false, bool kNv = false,
+          bool kWideK = false>
 __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
@@ -1194,22 +1196,25 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   static_assert(!(kFp8 && kPair) || !kMG, "block-scaled CTA pairs: K-grouped only");
   static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
   static_assert(!kNv || kFp4, "NVFP4 is the FP4 kernel with UE4M3 scales");
-  constexpr int kStages =
-      kPair ? (kNv ? STAGES_PAIR_NV : kFp4 ? STAGES_PAIR_FP4 : STAGES_PAIR) : (kNv ? STAGES_NV : STAGES);
-  constexpr uint32_t kStageB = kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
+  // kWideK: K-grouped BF16 on CTA pairs with 128-token stages (K-major operands in two 64-token boxes)
+  static_assert(!kWideK || (!kFp8 && kPair && !kMG), "128-token stages: K-grouped BF16 CTA pairs");
+  constexpr int kStages = kPair ? (kNv ? STAGES_PAIR_NV : kFp4 ? STAGES_PAIR_FP4 : kWideK ? STAGES_PAIR_BF16 : STAGES_PAIR)
+                                : (kNv ? STAGES_NV : STAGES);
+  constexpr uint32_t kStageA = STAGE_A_BYTES * (kWideK ? 2 : 1);
+  constexpr uint32_t kStageB = (kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES) * (kWideK ? 2 : 1);
   constexpr uint32_t kSfPad = kNv ? (kPair ? SF_SMEM_PAD_PAIR_NV : SF_SMEM_PAD_NV)
                               : !kFp8 ? 0u
                               : kPair ? (kFp4 ? SF_SMEM_PAD_PAIR_FP4 : SF_SMEM_PAD_PAIR)
                                       : SF_SMEM_PAD;
-  constexpr uint32_t kStageBytes = STAGE_A_BYTES + kStageB + kSfPad;
+  constexpr uint32_t kStageBytes = kStageA + kStageB + kSfPad;
   constexpr uint32_t kStageTx =
-      STAGE_A_BYTES + kStageB +
+      kStageA + kStageB +
       (kFp8 && kPair ? (kNv ? SF_PAIR_BYTES_NV : kFp4 ? SF_PAIR_BYTES_FP4 : SF_PAIR_BYTES) : 0u);
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
   constexpr int kHalves = kPair ? 2 : 1;
   constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
-  const int bk = kFp4 ? BK_FP4 : (kFp8 ? BK_FP8 : BK_BF16);
+  const int bk = kFp4 ? BK_FP4 : (kFp8 ? BK_FP8 : (kWideK ? BK_BF16_PAIR : BK_BF16));
   pdl_wait();  // the plan of this call (and any scale check before it) is complete and visible
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
   if (hdr->error != 0) return;  // offsets/pointers rejected by the plan: write nothing
@@ -1306,7 +1311,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   constexpr int kSfBlocks = kNv ? 12 : (kFp4 ? 6 : 3);
   constexpr uint32_t kSfCols = kNv ? SF_STAGE_COLS_NV : (kFp4 ? SF_STAGE_COLS_FP4 : SF_STAGE_COLS);
   // (single-CTA FP8 stages keep the raw FP32 scales ahead of the converted blocks)
-  constexpr uint32_t kSfSrc = STAGE_A_BYTES + kStageB + ((kFp4 || kPair) ? 0u : SF_UE8_OFFSET);
+  constexpr uint32_t kSfSrc = kStageA + kStageB + ((kFp4 || kPair) ? 0u : SF_UE8_OFFSET);
   auto copy_scale_factors = [&](int stage) {
     const uint32_t sf = tmem_base + SF_COL0 + stage * kSfCols;
     const uint32_t src = smem_u32(stage_mem + size_t(stage) * kStageBytes) + kSfSrc;
@@ -1389,7 +1394,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         ok2 = __shfl_sync(0xffffffffu, ok2, 0);
         if (!ok2) break;
         uint8_t* sA = stage_mem + size_t(stage) * kStageBytes;
-        uint8_t* sB = sA + STAGE_A_BYTES;
+        uint8_t* sB = sA + kStageA;
         const int64_t tok = it.begin + int64_t(kb) * bk;
         if (!drop && lane == 0) {
           const uint32_t fb = kPair ? leader_full0 + stage * 8 : 0u;
@@ -1477,6 +1482,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           // A: K-major -> one box [128 rows x bk tokens]; MN-major -> boxes [bk tokens x 128 B of rows]
           if constexpr (kAK) {
             load(sA, amap, kx, a_row);
+            if constexpr (kWideK) load(sA + BM * 128, amap, kx + BK_BF16, a_row);  // second 64 tokens
           } else {
 #pragma unroll
             for (int j = 0; j < BM / kAtom; ++j)
@@ -1485,6 +1491,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           // B: K-major -> one box [this CTA's columns x bk tokens]; MN-major -> boxes of 128 B of columns
           if constexpr (kBK) {
             load(sB, bmap, kx, b_row);
+            if constexpr (kWideK) load(sB + (BN / kHalves) * 128, bmap, kx + BK_BF16, b_row);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / kHalves / kAtom; ++j)
@@ -1572,7 +1579,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           // single CTA: the copies come first in this thread's order, so its MMAs see them
           if constexpr (kFp8 && !kPair) copy_scale_factors(stage);
           const uint32_t a_addr = smem_u32(stage_mem + size_t(stage) * kStageBytes);
-          const uint32_t b_addr = a_addr + STAGE_A_BYTES;
+          const uint32_t b_addr = a_addr + kStageA;
           if constexpr (kFp8 && kPair && !kFp4) {
             // the stage's scale factors are in TMEM columns 4i of the stage's 12 in both CTAs; MMA k
             // uses byte k of every word (the FP32 scales' byte is repeated, packed UE8M0 words hold
@@ -1622,11 +1629,17 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                        idesc | (idesc_sf_id(static_cast<uint32_t>(k)) & sf_sel), sfa, sfb,
                        (kb > it.kbeg || k > 0) ? 1u : 0u);
           } else {
+            // 128-token stages: a K-major operand's second 64 tokens are a box of their own
+            // (A 128 rows x 128 B, B this CTA's columns x 128 B further on); MN-major atoms hold all
+            // of the stage's tokens
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < (kWideK ? 8 : 4); ++k) {
               // in a pair each CTA holds 128 rows of A and 128 columns of B
-              const uint64_t adesc = desc(a_tmpl, a_addr, a_step, k);
-              const uint64_t bdesc = desc(b_tmpl, b_addr, b_step, k);
+              const uint64_t adesc = kAK && kWideK ? desc(a_tmpl, a_addr + (k >> 2) * (BM * 128u), a_step, k & 3)
+                                                   : desc(a_tmpl, a_addr, a_step, k);
+              const uint64_t bdesc = kBK && kWideK
+                                         ? desc(b_tmpl, b_addr + (k >> 2) * ((BN / kHalves) * 128u), b_step, k & 3)
+                                         : desc(b_tmpl, b_addr, b_step, k);
               if constexpr (kPair)
                 mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > it.kbeg || k > 0) ? 1u : 0u);
               else
@@ -2131,7 +2144,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             ok = false;
             break;
           }
-          uint8_t* sS = stage_mem + size_t(stage) * kStageBytes + STAGE_A_BYTES + kStageB;
+          uint8_t* sS = stage_mem + size_t(stage) * kStageBytes + kStageA + kStageB;
           if constexpr (kNv) {
             // four 64-token UE4M3 words per row/column, rearranged in place into 12 blocks: for each
             // MMA k, A word k, then B word k for columns 0..127 and 128..255
@@ -2380,11 +2393,12 @@ cudaError_t launch_plan(const PlanParams& p, const MapTemplates& t, cudaStream_t
   return cudaGetLastError();
 }
 
-template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false, bool kNv = false>
+template <bool kFp8, bool kPair, bool kAK, bool kBK, bool kMG = false, bool kFp4 = false, bool kNv = false,
+          bool kWideK = false>
 static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                cudaStream_t s) {
-  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG, kFp4, kNv>;
-  size_t smem = main_smem_bytes(kPair, kFp8, kNv, kFp4);
+  auto kernel = wgrad_kernel<kFp8, kPair, kAK, kBK, kMG, kFp4, kNv, kWideK>;
+  size_t smem = main_smem_bytes(kPair, kFp8, kNv, kFp4, kWideK);
   // the K-grouped FP8 kernel also hosts the promotion path, which lays out the same memory its own way
   if (kFp8 && !kFp4 && !kMG && promote_smem_bytes() > smem) smem = promote_smem_bytes();
   // set on every launch: the attribute is per device and the call is cheap
@@ -2409,17 +2423,18 @@ static cudaError_t launch_main(const MainParams& p, const CUtensorMap& tmA, cons
 }
 
 // One instantiation per operand storage order (K-major A / K-major B), chosen at run time.
-template <bool kFp8, bool kPair>
+template <bool kFp8, bool kPair, bool kWideK = false>
 static cudaError_t launch_orders(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                                  cudaStream_t s) {
-  if (p.a_kmajor && !p.b_kmajor) return launch_main<kFp8, kPair, true, false>(p, tmA, tmB, grid, s);
-  if (!p.a_kmajor && !p.b_kmajor) return launch_main<kFp8, kPair, false, false>(p, tmA, tmB, grid, s);
-  if (p.a_kmajor && p.b_kmajor) return launch_main<kFp8, kPair, true, true>(p, tmA, tmB, grid, s);
-  return launch_main<kFp8, kPair, false, true>(p, tmA, tmB, grid, s);
+  if (p.a_kmajor && !p.b_kmajor) return launch_main<kFp8, kPair, true, false, false, false, false, kWideK>(p, tmA, tmB, grid, s);
+  if (!p.a_kmajor && !p.b_kmajor) return launch_main<kFp8, kPair, false, false, false, false, false, kWideK>(p, tmA, tmB, grid, s);
+  if (p.a_kmajor && p.b_kmajor) return launch_main<kFp8, kPair, true, true, false, false, false, kWideK>(p, tmA, tmB, grid, s);
+  return launch_main<kFp8, kPair, false, true, false, false, false, kWideK>(p, tmA, tmB, grid, s);
 }
 
 cudaError_t launch_main_bf16(const MainParams& p, const CUtensorMap& tmA, const CUtensorMap& tmB, int grid,
                              cudaStream_t s) {
+  if (p.tile_m == 2 * BM && p.wide_k) return launch_orders<false, true, true>(p, tmA, tmB, grid, s);
   if (p.tile_m == 2 * BM) return launch_orders<false, true>(p, tmA, tmB, grid, s);
   return launch_orders<false, false>(p, tmA, tmB, grid, s);
 }
