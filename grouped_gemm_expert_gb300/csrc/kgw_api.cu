@@ -536,8 +536,11 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
   const uint64_t esz = fp8 ? 1 : 2;
   const uint32_t bk = fp8 ? kgw::BK_FP8 : kgw::BK_BF16;   // one 128-byte swizzle row of K
   // BF16 runs on CTA pairs (two 128-row tiles of one group per work row); FP8 on single CTAs.
-  // In a pair each CTA loads 128 of the tile's 256 columns of B.
+  // In a pair each CTA loads 128 of the tile's 256 columns of B. BF16 pairs take 128-token stages
+  // (two rows of K) when K is a multiple of 128, except in the masked layout: its decode batches
+  // are HBM-bound, and the shorter stages keep more loads in flight (128-token stages: +3.7 %).
   const bool pair = !fp8 && g_single_cta.load() == 0;
+  const bool wide_k = pair && a->k % (2 * kgw::BK_BF16) == 0 && a->layout != KGW_MG_MASKED;
   const uint32_t b_rows_cta = pair ? kgw::BN / 2 : kgw::BN;
   if (M > 0) {
     st = encode_2d(&tmA, dt, a->a, K, M, K * esz, bk, kgw::BM);                          // A [rows, K]
@@ -545,7 +548,7 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
     if (a->b_major == KGW_K_MAJOR)
       st = encode_2d(&tmB, dt, a->b, K, G * N, K * esz, bk, b_rows_cta);               // B [G*N, K]
     else
-      st = encode_2d(&tmB, dt, a->b, N, G * K, N * esz, static_cast<uint32_t>(128 / esz), bk);  // B [G*K, N]
+      st = encode_2d(&tmB, dt, a->b, N, G * K, N * esz, static_cast<uint32_t>(128 / esz), bk * (wide_k ? 2 : 1));  // B [G*K, N]
     if (st != KGW_OK) return st;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -586,7 +589,7 @@ kgw_status run_mg(const kgw_mgrouped_args* a, void* ws, size_t ws_bytes, void* s
   mp.L = L;
   mp.timeout_ns = static_cast<uint64_t>(g_timeout_ns.load());
   mp.test_drop_stage = -1;
-  mp.wide_k = 0;
+  mp.wide_k = wide_k ? 1 : 0;
   return kgw::launch_main_mgrouped(mp, tmA, tmB, grid, s) == cudaSuccess ? KGW_OK : KGW_ERR_CUDA;
 }
 

@@ -1196,8 +1196,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   static_assert(!(kFp8 && kPair) || !kMG, "block-scaled CTA pairs: K-grouped only");
   static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
   static_assert(!kNv || kFp4, "NVFP4 is the FP4 kernel with UE4M3 scales");
-  // kWideK: K-grouped BF16 on CTA pairs with 128-token stages (K-major operands in two 64-token boxes)
-  static_assert(!kWideK || (!kFp8 && kPair && !kMG), "128-token stages: K-grouped BF16 CTA pairs");
+  // kWideK: BF16 on CTA pairs with 128-token stages (K-major operands in two 64-token boxes)
+  static_assert(!kWideK || (!kFp8 && kPair), "128-token stages: BF16 CTA pairs");
   constexpr int kStages = kPair ? (kNv ? STAGES_PAIR_NV : kFp4 ? STAGES_PAIR_FP4 : kWideK ? STAGES_PAIR_BF16 : STAGES_PAIR)
                                 : (kNv ? STAGES_NV : STAGES);
   constexpr uint32_t kStageA = STAGE_A_BYTES * (kWideK ? 2 : 1);
@@ -2444,6 +2444,10 @@ cudaError_t launch_main_mgrouped(const MainParams& p, const CUtensorMap& tmA, co
   if (p.fp8) {
     if (p.b_kmajor) return launch_main<true, false, true, true, true>(p, tmA, tmB, grid, s);
     return launch_main<true, false, true, false, true>(p, tmA, tmB, grid, s);
+  }
+  if (p.tile_m == 2 * BM && p.wide_k) {
+    if (p.b_kmajor) return launch_main<false, true, true, true, true, false, false, true>(p, tmA, tmB, grid, s);
+    return launch_main<false, true, true, false, true, false, false, true>(p, tmA, tmB, grid, s);
   }
   if (p.tile_m == 2 * BM) {
     if (p.b_kmajor) return launch_main<false, true, true, true, true>(p, tmA, tmB, grid, s);
