@@ -1769,6 +1769,37 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
               *reinterpret_cast<uint4*>(cbase + (8 * j + rsub) * ostride) = unstage4(j);
           __syncwarp();
         }
+      } else if (kNv && it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
+        // NVFP4 (its scale-factor ring leaves TMEM no holding columns): the warp's 32 x 128 block,
+        // times the global scales and packed to 16 bits, waits in registers (64 per thread) while
+        // the accumulator goes back to the MMA
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float x0 = __uint_as_float(r[2 * i]) * gscale, x1 = __uint_as_float(r[2 * i + 1]) * gscale;
+            pk[c * 16 + i] = p.out_f16 ? pack_f16x2(x0, x1) : pack_bf16x2(x0, x1);
+          }
+        }
+        release_acc();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          stage4(make_uint4(pk[c * 16 + 0], pk[c * 16 + 1], pk[c * 16 + 2], pk[c * 16 + 3]),
+                 make_uint4(pk[c * 16 + 4], pk[c * 16 + 5], pk[c * 16 + 6], pk[c * 16 + 7]),
+                 make_uint4(pk[c * 16 + 8], pk[c * 16 + 9], pk[c * 16 + 10], pk[c * 16 + 11]),
+                 make_uint4(pk[c * 16 + 12], pk[c * 16 + 13], pk[c * 16 + 14], pk[c * 16 + 15]));
+          __syncwarp();
+          char* cbase = obase + size_t(c * 32 + csub * 8) * 2;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (!kMG || q * 32 + 8 * j + rsub < it.rows)
+              *reinterpret_cast<uint4*>(cbase + (8 * j + rsub) * ostride) = unstage4(j);
+          __syncwarp();
+        }
       } else if (it.nsplit == 1) {
         // FP32 output or accumulation: 16 columns per TMEM load, the accumulator is handed back
         // after the last load
