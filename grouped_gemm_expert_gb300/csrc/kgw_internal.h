@@ -87,7 +87,7 @@ constexpr uint32_t SF_STAGE_COLS_FP4 = 24;
 // columns 0..127, 128..255) that land in 48 TMEM columns per stage; 3 stages of 54 KiB.
 // FP8 on CTA pairs: each stage carries this CTA's A scale-factor block and both B blocks (its own
 // and its peer's columns: the pair MMA reads all 256), in TMEM order, 1.5 KiB padded to 2 KiB;
-// they arrive by TMA from the prepared words in the workspace, on the operands' barrier.
+// they arrive by TMA from the prepared words in the workspace, on a barrier of their own.
 constexpr uint32_t SF_SMEM_PAD_PAIR = 2048;
 constexpr uint32_t SF_PAIR_BYTES = 3 * SF_UE8_BLOCK;
 // FP4 on CTA pairs: the stage's two 128-token blocks, laid out as on single CTAs ([A word 0]

@@ -579,9 +579,10 @@ struct SmemCtl {
   uint64_t wempty[WORK_RING];
   uint64_t mma_done;
   uint64_t sf_full[MAX_STAGES]; // block-scaled: single CTA, the converter has written a stage's scale
-                                // factors in TMEM order; pair, warp 10 has copied them to TMEM after
-                                // the stage's operands landed (on the even CTA)
-  uint64_t sfdata[MAX_STAGES];  // block-scaled: this CTA's raw scales of a stage have landed in shared memory
+                                // factors in TMEM order; pair, warp 10 has copied them to TMEM once
+                                // they landed (on the even CTA)
+  uint64_t sfdata[MAX_STAGES];  // block-scaled: this CTA's raw scales of a stage have landed in shared memory;
+                                // CTA pair: both CTAs' prepared scale factors of a stage (even CTA)
   uint64_t cp_done;             // CTA pair: warp 10's last scale-factor copies have completed
   Item work[WORK_RING];         // decoded work items (written by the scheduler of the leader CTA)
   uint32_t tmem_base;
@@ -1192,7 +1193,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     wgrad_kernel(const __grid_constant__ MainParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
   // FP8, FP4 and NVFP4 on CTA pairs: K-grouped, with the scale factors prepared in TMEM order by
-  // the scale kernel and loaded by TMA with the operands (the M-grouped FP8 GEMM runs on single CTAs).
+  // the scale kernel and loaded by TMA with each stage (the M-grouped FP8 GEMM runs on single CTAs).
   static_assert(!(kFp8 && kPair) || !kMG, "block-scaled CTA pairs: K-grouped only");
   static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
   static_assert(!kNv || kFp4, "NVFP4 is the FP4 kernel with UE4M3 scales");
@@ -1207,10 +1208,12 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                               : kPair ? (kFp4 ? SF_SMEM_PAD_PAIR_FP4 : SF_SMEM_PAD_PAIR)
                                       : SF_SMEM_PAD;
   constexpr uint32_t kStageBytes = kStageA + kStageB + kSfPad;
-  constexpr uint32_t kStageTx =
-      kStageA + kStageB +
-      (kFp8 && kPair ? (kNv ? SF_PAIR_BYTES_NV : kFp4 ? SF_PAIR_BYTES_FP4 : SF_PAIR_BYTES) : 0u);
+  // Block-scaled CTA pairs: the prepared scale factors of a stage land on their own barrier (sfdata
+  // of the even CTA), ahead of the operands, so warp 10 copies them to TMEM while the operand tiles
+  // are still arriving; `full` counts the operand bytes only.
+  constexpr uint32_t kStageTx = kStageA + kStageB;
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
+  constexpr uint32_t kSfTx = kFp8 && kPair ? (kNv ? SF_PAIR_BYTES_NV : kFp4 ? SF_PAIR_BYTES_FP4 : SF_PAIR_BYTES) : 0u;
   constexpr int kHalves = kPair ? 2 : 1;
   constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
@@ -1296,6 +1299,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   const uint32_t leader_full0 = kPair ? mapa_shared(smem_u32(&ctl->full[0]), 0) : 0u;
   const uint32_t leader_wempty0 = kPair ? mapa_shared(smem_u32(&ctl->wempty[0]), 0) : 0u;
   const uint32_t leader_tempty0 = kPair ? mapa_shared(smem_u32(&ctl->tempty[0]), 0) : 0u;
+  const uint32_t leader_sfdata0 = kPair ? mapa_shared(smem_u32(&ctl->sfdata[0]), 0) : 0u;
 
   // A consumer is done with work-ring slot `slot`.
   auto release_slot = [&](int slot) {
@@ -1324,17 +1328,18 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         tmem_cp_32x128b_warpx4(sf + 4 * blk, d);
     }
   };
-  // CTA pairs, warp 10 of the even CTA, per stage: wait for the stage's operands and prepared scale
-  // factors, copy the scale factors and commit them to sf_full, the one barrier the MMA thread
-  // waits on. (Every tcgen05 instruction holds its issuing thread for tens of cycles: next to its
-  // four MMAs, its wait and its commit, the MMA thread has no room for the copies within the 512
-  // cycles those MMAs run.) The stage's columns are free again by then: the producers reload a
-  // stage only after the MMAs that read it have completed. Returns false (in every lane) on timeout
-  // or abort.
+  // CTA pairs, warp 10 of the even CTA, per stage: wait for the stage's prepared scale factors (their
+  // own barrier: they land before the operand tiles), copy them and commit them to sf_full, which
+  // the MMA thread waits on after the operands' barrier. The copies thus run while the operand
+  // tiles arrive, off the stage's critical path. (Every tcgen05 instruction holds its issuing thread
+  // for tens of cycles: next to its four MMAs, its waits and its commit, the MMA thread has no room
+  // for the copies within the 512 cycles those MMAs run.) The stage's columns are free again by
+  // then: the producers reload a stage only after the MMAs that read it have completed. Returns
+  // false (in every lane) on timeout or abort.
   auto hand_off_scale_factors = [&](int stage, uint32_t phase) -> bool {
     int good = 1;
     if (lane == 0) {
-      good = wait_bounded_t<kPair>(&ctl->full[stage], phase, abort_flag, p.timeout_ns) ? 1 : 0;
+      good = wait_bounded_t<kPair>(&ctl->sfdata[stage], phase, abort_flag, p.timeout_ns) ? 1 : 0;
       if (good) {
         tc_fence_after();
         copy_scale_factors(stage);
@@ -1389,7 +1394,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         const bool drop = (p.test_drop_stage >= 0 && blockIdx.x == 0 && issued == p.test_drop_stage);
         if (lane == 0) {
           ok2 = wait_bounded_t<kPair>(&ctl->empty[stage], phase ^ 1, abort_flag, p.timeout_ns);
-          if (ok2 && !drop && leader) mbar_arrive_expect_tx(&ctl->full[stage], kExpectTx);
+          if (ok2 && !drop && leader) {
+            if constexpr (kSfTx > 0) mbar_arrive_expect_tx(&ctl->sfdata[stage], 2 * kSfTx);
+            mbar_arrive_expect_tx(&ctl->full[stage], kExpectTx);
+          }
         }
         ok2 = __shfl_sync(0xffffffffu, ok2, 0);
         if (!ok2) break;
@@ -1403,6 +1411,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
               tma_load_2d_pair(dst, map, fb, x, y);
             else
               tma_load_2d(dst, map, &ctl->full[stage], x, y);
+          };
+          // block-scaled pairs: the scale factors complete on the even CTA's sfdata barrier
+          auto load_sf = [&](void* dst, const CUtensorMap* map, int32_t x, int32_t y) {
+            tma_load_2d_pair(dst, map, leader_sfdata0 + stage * 8, x, y);
           };
           // token coordinate: relative to the expert's block for per-expert descriptors (and for
           // the M-grouped GEMM, whose K axis is the fixed contraction axis)
@@ -1421,8 +1433,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             uint8_t* sS = sB + kStageB;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              load(sS + 3 * j * SF_UE8_BLOCK, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, w0 + j);
-              load(sS + (3 * j + 1) * SF_UE8_BLOCK, &p.tm_sfb, it.n0, w0 + j);
+              load_sf(sS + 3 * j * SF_UE8_BLOCK, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, w0 + j);
+              load_sf(sS + (3 * j + 1) * SF_UE8_BLOCK, &p.tm_sfb, it.n0, w0 + j);
             }
           } else if constexpr (kFp8 && kPair && kFp4) {
             // prepared scale factors of this 256-token stage's two 128-token blocks, in TMEM order:
@@ -1431,17 +1443,17 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             const int32_t kblk = it.srow + 2 * kb;
             const int32_t kblk1 = (2 * int64_t(kb) + 1) * SCALE_BLOCK < it.n_e ? kblk + 1 : kblk;
             uint8_t* sS = sB + kStageB;
-            load(sS, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk);
-            load(sS + SF_UE8_BLOCK, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk1);
-            load(sS + 2 * SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk);
-            load(sS + 4 * SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk1);
+            load_sf(sS, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk);
+            load_sf(sS + SF_UE8_BLOCK, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk1);
+            load_sf(sS + 2 * SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk);
+            load_sf(sS + 4 * SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk1);
           } else if constexpr (kFp8 && kPair) {
             // prepared scale factors of this 128-token block, in TMEM order: this CTA's A rows and
-            // all 256 B columns, by TMA onto the leader's barrier with the operands
+            // all 256 B columns, by TMA onto the leader's scale-factor barrier
             const int32_t kblk = it.srow + kb;
             uint8_t* sS = sB + kStageB;
-            load(sS, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk);
-            load(sS + SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk);
+            load_sf(sS, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, kblk);
+            load_sf(sS + SF_UE8_BLOCK, &p.tm_sfb, it.n0, kblk);
           } else if constexpr (kNv) {
             // NVFP4: the four 64-token scale words of this 256-token stage (UE4M3 bytes per 16
             // tokens): [A word 0..3][B word 0..3]; word rows are the expert's 64-token groups
@@ -1518,6 +1530,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         }
         int dummy = 0;
         wait_bounded_t<kPair>(&ctl->full[s], ph, &dummy, p.timeout_ns);
+        if constexpr (kSfTx > 0) wait_bounded_t<kPair>(&ctl->sfdata[s], ph, &dummy, p.timeout_ns);
       }
     }
   } else if (warp == 1) {
@@ -1562,11 +1575,16 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = it.kbeg; kb < it.kend; ++kb) {
-          // FP8 pairs: warp 10's barrier, which it completes only after the operands landed
-          if (!wait_bounded_t<kPair>((kFp8 && kPair) ? &ctl->sf_full[stage] : &ctl->full[stage], phase, abort_flag,
-                                     p.timeout_ns)) {
+          if (!wait_bounded_t<kPair>(&ctl->full[stage], phase, abort_flag, p.timeout_ns)) {
             ok = false;
             break;
+          }
+          if constexpr (kFp8 && kPair) {
+            // block-scaled pairs: warp 10 has copied the stage's scale factors to TMEM
+            if (!wait_bounded_t<kPair>(&ctl->sf_full[stage], phase, abort_flag, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
           }
           if constexpr (kFp8 && !kPair) {
             // single CTA: the converter has written the stage's scale factors in TMEM order
@@ -1675,8 +1693,8 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
     // ======================= Epilogue of the block-scaled kernels (warps 2..9) =======================
     // Eight warps: warp w reads TMEM lane quadrant w % 4 and accumulator columns 128 * ((w - 2) / 4)
     // onward. With 16-bit output and no accumulation the warp first moves its whole 32 x 128 block
-    // into its holding columns of TMEM (packed to 16 bits) and hands the accumulator back, so the
-    // MMA of the next tile does not wait for the stores.
+    // into its holding columns of TMEM (NVFP4: into registers), packed to 16 bits, and hands the
+    // accumulator back, so the MMA of the next tile does not wait for the stores.
     const int q = warp & 3;
     const int ew = warp - EPI_WARP0;
     const int col0 = (ew >> 2) * (BN / 2);
@@ -2297,7 +2315,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   if constexpr (kFp8 && kPair) {
     if (warp == SF_WARP && leader) {
       // ======================= scale-factor copier of a CTA pair (warp 10, even CTA) ==============
-      // the prepared scale factors arrive by TMA with the operands; warp 10 only copies them to TMEM
+      // the prepared scale factors arrive by TMA ahead of the operands; warp 10 only copies them to TMEM
       int stage = 0;
       uint32_t phase = 0;
       for (int n = 0;; ++n) {
