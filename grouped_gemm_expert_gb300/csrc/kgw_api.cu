@@ -219,9 +219,11 @@ kgw_status prepare(const kgw_wgrad_args* a, bool fp8, const float* sfa, const fl
   if (dev.major != 10 || dev.minor != 3) return KGW_ERR_DEVICE;
   if (get_encoder() != KGW_OK) return KGW_ERR_CUDA;
 
-  // k-iteration length in tokens (K-grouped BF16 on CTA pairs, aligned entries: 128 tokens per stage)
-  const bool wide_k = !fp8 && halves == 2 && !tail;
-  const int bk = fp4 ? kgw::BK_FP4 : fp8 ? kgw::BK_FP8 : (wide_k ? kgw::BK_BF16_PAIR : kgw::BK_BF16);
+  // k-iteration length in tokens (K-grouped CTA pairs, aligned entries: BF16 128 tokens per stage,
+  // FP4 with UE8M0 scales 512)
+  const bool wide_k = (!fp8 || (fp4 && !nv)) && halves == 2 && !tail;
+  const int bk = fp4 ? (wide_k ? kgw::BK_FP4_PAIR : kgw::BK_FP4)
+                     : fp8 ? kgw::BK_FP8 : (wide_k ? kgw::BK_BF16_PAIR : kgw::BK_BF16);
   const uint64_t esz = fp8 ? 1 : 2;
   // token-axis box of a K-major operand in descriptor elements: one 128-byte swizzle row (packed
   // FP4 descriptors count bytes, so its 256 tokens are 128 elements; a 128-token BF16 stage loads

@@ -96,6 +96,16 @@ constexpr uint32_t SF_PAIR_BYTES = 3 * SF_UE8_BLOCK;
 constexpr uint32_t SF_SMEM_PAD_PAIR_FP4 = 3072;
 constexpr uint32_t SF_PAIR_BYTES_FP4 = 6 * SF_UE8_BLOCK;
 constexpr int STAGES_PAIR_FP4 = 5;
+// FP4 on CTA pairs, aligned entry: 512-token stages (two 128-byte boxes per operand row, eight MMAs)
+// carrying four 128-token blocks ([A word 0..3][B word 0..3, each columns 0..127, 128..255], 6 KiB,
+// 48 TMEM columns); three stages of 70 KiB. The MMA thread and warp 10 pay their waits and commits
+// once per eight MMAs. Three such stages and the epilogue staging fill shared memory exactly: the
+// kernel relies on the dynamic shared memory starting 1024-byte aligned, and checks it.
+constexpr int BK_FP4_PAIR = 512;
+constexpr int STAGES_PAIR_FP4_WIDE = 3;
+constexpr uint32_t SF_SMEM_PAD_PAIR_FP4_WIDE = 6144;
+constexpr uint32_t SF_PAIR_BYTES_FP4_WIDE = 12 * SF_UE8_BLOCK;
+constexpr uint32_t SF_STAGE_COLS_FP4_WIDE = 48;
 // NVFP4 on CTA pairs: the stage's four 64-token scale words as the single-CTA converter lays them
 // out (for each MMA k: [A word k][B word k: columns 0..127, 128..255]), 6 KiB; five stages of
 // 38 KiB; 48 TMEM scale columns per stage (NVFP4 keeps no 16-bit holding area, so they may reach

@@ -596,6 +596,9 @@ constexpr uint32_t EPI_STAGE_TOTAL = 16384;
 constexpr uint32_t EPI_STAGE_BYTES = EPI_STAGE_TOTAL / NUM_EPI_WARPS;
 
 size_t main_smem_bytes(bool pair, bool fp8, bool nv, bool fp4, bool wide_k) {
+  if (pair && fp4 && wide_k)  // fills shared memory: no alignment slack (the kernel checks the base)
+    return size_t(STAGES_PAIR_FP4_WIDE) * (2 * STAGE_A_BYTES + STAGE_B_BYTES + SF_SMEM_PAD_PAIR_FP4_WIDE) +
+           EPI_STAGE_TOTAL + sizeof(SmemCtl) + 64;
   const size_t ring = pair && wide_k ? size_t(STAGES_PAIR_BF16) * (2 * STAGE_A_BYTES + STAGE_B_BYTES)
                       : pair && nv ? size_t(STAGES_PAIR_NV) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_NV)
                       : pair ? (fp4 ? size_t(STAGES_PAIR_FP4) * (STAGE_A_BYTES + STAGE_B_BYTES / 2 + SF_SMEM_PAD_PAIR_FP4)
@@ -1197,15 +1200,18 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   static_assert(!(kFp8 && kPair) || !kMG, "block-scaled CTA pairs: K-grouped only");
   static_assert(!kFp4 || (kFp8 && kAK && kBK && !kMG), "FP4 operands are K-major, block-scaled");
   static_assert(!kNv || kFp4, "NVFP4 is the FP4 kernel with UE4M3 scales");
-  // kWideK: BF16 on CTA pairs with 128-token stages (K-major operands in two 64-token boxes)
-  static_assert(!kWideK || (!kFp8 && kPair), "128-token stages: BF16 CTA pairs");
-  constexpr int kStages = kPair ? (kNv ? STAGES_PAIR_NV : kFp4 ? STAGES_PAIR_FP4 : kWideK ? STAGES_PAIR_BF16 : STAGES_PAIR)
+  // kWideK: stages of two 128-byte rows of K per operand row on CTA pairs: BF16 128-token stages
+  // (K-major operands in two 64-token boxes), FP4 512-token stages (two 256-token boxes)
+  static_assert(!kWideK || (kPair && (!kFp8 || (kFp4 && !kNv))), "two-row stages: BF16 or FP4 CTA pairs");
+  constexpr int kStages = kPair ? (kNv ? STAGES_PAIR_NV
+                                   : kFp4 ? (kWideK ? STAGES_PAIR_FP4_WIDE : STAGES_PAIR_FP4)
+                                   : kWideK ? STAGES_PAIR_BF16 : STAGES_PAIR)
                                 : (kNv ? STAGES_NV : STAGES);
   constexpr uint32_t kStageA = STAGE_A_BYTES * (kWideK ? 2 : 1);
   constexpr uint32_t kStageB = (kPair ? STAGE_B_BYTES / 2 : STAGE_B_BYTES) * (kWideK ? 2 : 1);
   constexpr uint32_t kSfPad = kNv ? (kPair ? SF_SMEM_PAD_PAIR_NV : SF_SMEM_PAD_NV)
                               : !kFp8 ? 0u
-                              : kPair ? (kFp4 ? SF_SMEM_PAD_PAIR_FP4 : SF_SMEM_PAD_PAIR)
+                              : kPair ? (kFp4 ? (kWideK ? SF_SMEM_PAD_PAIR_FP4_WIDE : SF_SMEM_PAD_PAIR_FP4) : SF_SMEM_PAD_PAIR)
                                       : SF_SMEM_PAD;
   constexpr uint32_t kStageBytes = kStageA + kStageB + kSfPad;
   // Block-scaled CTA pairs: the prepared scale factors of a stage land on their own barrier (sfdata
@@ -1213,11 +1219,13 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   // are still arriving; `full` counts the operand bytes only.
   constexpr uint32_t kStageTx = kStageA + kStageB;
   constexpr uint32_t kExpectTx = kPair ? 2 * kStageTx : kStageTx;
-  constexpr uint32_t kSfTx = kFp8 && kPair ? (kNv ? SF_PAIR_BYTES_NV : kFp4 ? SF_PAIR_BYTES_FP4 : SF_PAIR_BYTES) : 0u;
+  constexpr uint32_t kSfTx =
+      kFp8 && kPair ? (kNv ? SF_PAIR_BYTES_NV : kFp4 ? (kWideK ? SF_PAIR_BYTES_FP4_WIDE : SF_PAIR_BYTES_FP4) : SF_PAIR_BYTES)
+                    : 0u;
   constexpr int kHalves = kPair ? 2 : 1;
   constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
   extern __shared__ uint8_t smem_raw[];
-  const int bk = kFp4 ? BK_FP4 : (kFp8 ? BK_FP8 : (kWideK ? BK_BF16_PAIR : BK_BF16));
+  const int bk = kFp4 ? (kWideK ? BK_FP4_PAIR : BK_FP4) : (kFp8 ? BK_FP8 : (kWideK ? BK_BF16_PAIR : BK_BF16));
   pdl_wait();  // the plan of this call (and any scale check before it) is complete and visible
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
   if (hdr->error != 0) return;  // offsets/pointers rejected by the plan: write nothing
@@ -1235,6 +1243,13 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   if (total_items == 0) return;
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if constexpr (kFp4 && kWideK) {
+    // sized without alignment slack (the ring fills shared memory): the base must be aligned already
+    if (base != smem_raw) {
+      if (threadIdx.x == 0 && p.status_dev) atomicExch(p.status_dev, KGW_ERR_CUDA);
+      return;
+    }
+  }
   uint8_t* stage_mem = base;
   uint8_t* epi_stage_mem = base + size_t(kStages) * kStageBytes;
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(epi_stage_mem + EPI_STAGE_TOTAL);
@@ -1312,8 +1327,9 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
   // Block-scaled kernels: a stage's scale-factor blocks (32 rows x 16 bytes each, in TMEM order in
   // shared memory) -> the stage's TMEM columns, repeated in the four lane quadrants; a pair's copies
   // take each CTA's own shared memory to its own TMEM.
-  constexpr int kSfBlocks = kNv ? 12 : (kFp4 ? 6 : 3);
-  constexpr uint32_t kSfCols = kNv ? SF_STAGE_COLS_NV : (kFp4 ? SF_STAGE_COLS_FP4 : SF_STAGE_COLS);
+  constexpr int kSfBlocks = kNv ? 12 : (kFp4 ? (kWideK ? 12 : 6) : 3);
+  constexpr uint32_t kSfCols =
+      kNv ? SF_STAGE_COLS_NV : (kFp4 ? (kWideK ? SF_STAGE_COLS_FP4_WIDE : SF_STAGE_COLS_FP4) : SF_STAGE_COLS);
   // (single-CTA FP8 stages keep the raw FP32 scales ahead of the converted blocks)
   constexpr uint32_t kSfSrc = kStageA + kStageB + ((kFp4 || kPair) ? 0u : SF_UE8_OFFSET);
   auto copy_scale_factors = [&](int stage) {
@@ -1436,6 +1452,20 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
               load_sf(sS + 3 * j * SF_UE8_BLOCK, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, w0 + j);
               load_sf(sS + (3 * j + 1) * SF_UE8_BLOCK, &p.tm_sfb, it.n0, w0 + j);
             }
+          } else if constexpr (kFp8 && kPair && kFp4 && kWideK) {
+            // prepared scale factors of this 512-token stage's four 128-token blocks, in TMEM order:
+            // [A block 0..3][B block 0..3 (all 256 columns each)]; blocks past the expert's last one
+            // repeat it (the MMAs of those tokens are not issued)
+            const int32_t kblk = it.srow + 4 * kb;
+            const int64_t left = it.n_e - int64_t(kb) * bk;
+            const int32_t nb = left >= 4 * SCALE_BLOCK ? 4 : static_cast<int32_t>((left + SCALE_BLOCK - 1) / SCALE_BLOCK);
+            uint8_t* sS = sB + kStageB;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int32_t bj = kblk + (j < nb ? j : nb - 1);
+              load_sf(sS + j * SF_UE8_BLOCK, &p.tm_sfa, it.m0 + static_cast<int32_t>(rank) * BM, bj);
+              load_sf(sS + (4 + 2 * j) * SF_UE8_BLOCK, &p.tm_sfb, it.n0, bj);
+            }
           } else if constexpr (kFp8 && kPair && kFp4) {
             // prepared scale factors of this 256-token stage's two 128-token blocks, in TMEM order:
             // [A block 0][A block 1][B block 0 (all 256 columns)][B block 1]; when the expert's last
@@ -1491,10 +1521,11 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
             bulk_load(sS + BM * 4, p.sfb + bblk * p.I + it.n0, BN * 4, &ctl->sfdata[stage]);
           }
           constexpr int kAtom = kFp8 ? 128 : 64;  // elements per 128-byte swizzle row
+          constexpr int32_t kBoxX = kFp4 ? 128 : BK_BF16;  // a K-major box's token extent in descriptor units
           // A: K-major -> one box [128 rows x bk tokens]; MN-major -> boxes [bk tokens x 128 B of rows]
           if constexpr (kAK) {
             load(sA, amap, kx, a_row);
-            if constexpr (kWideK) load(sA + BM * 128, amap, kx + BK_BF16, a_row);  // second 64 tokens
+            if constexpr (kWideK) load(sA + BM * 128, amap, kx + kBoxX, a_row);  // second box of the stage
           } else {
 #pragma unroll
             for (int j = 0; j < BM / kAtom; ++j)
@@ -1503,7 +1534,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
           // B: K-major -> one box [this CTA's columns x bk tokens]; MN-major -> boxes of 128 B of columns
           if constexpr (kBK) {
             load(sB, bmap, kx, b_row);
-            if constexpr (kWideK) load(sB + (BN / kHalves) * 128, bmap, kx + BK_BF16, b_row);
+            if constexpr (kWideK) load(sB + (BN / kHalves) * 128, bmap, kx + kBoxX, b_row);
           } else {
 #pragma unroll
             for (int j = 0; j < BN / kHalves / kAtom; ++j)
@@ -1622,6 +1653,23 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
               else
                 mma_nvf4(d_tmem, desc(a_tmpl, a_addr, a_step, k), desc(b_tmpl, b_addr, b_step, k), idesc, sf + 12 * k,
                          sf + 12 * k + 4, acc_in);
+            }
+          } else if constexpr (kFp4 && kWideK) {
+            // 512-token stage: 12 scale blocks in TMEM columns 4i of its 48 (A words 0..3, then B words
+            // 0..3 of 8 columns each); MMA k (64 tokens, box k/4) reads word k/2 of A (columns 4(k/2))
+            // and B (16 + 8(k/2)), byte pair (k%2)*2 of it. An expert's last stage may hold 256 tokens
+            // only: the MMAs of the other half are not issued (the same MMAs as with 256-token stages).
+            const uint32_t sf = tmem_base + SF_COL0 + stage * SF_STAGE_COLS_FP4_WIDE;
+            const int nk = int64_t(kb) * bk + bk / 2 >= it.n_e ? 4 : 8;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (k < nk) {
+                const uint32_t id = idesc | idesc_sf_id(static_cast<uint32_t>(k & 1) * 2u);
+                const uint32_t acc_in = (kb > it.kbeg || k > 0) ? 1u : 0u;
+                mma_mxf4_pair(d_tmem, desc(a_tmpl, a_addr + (k >> 2) * (BM * 128u), a_step, k & 3),
+                              desc(b_tmpl, b_addr + (k >> 2) * ((BN / kHalves) * 128u), b_step, k & 3), id,
+                              sf + 4 * (k >> 1), sf + 16 + 8 * (k >> 1), acc_in);
+              }
             }
           } else if constexpr (kFp4) {
             // the stage's 6 scale blocks are in TMEM columns 4i of its 24; MMA k (64 tokens) reads
@@ -1755,7 +1803,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
         const int r = 8 * j + rsub;
         return stg[r * 4 + (csub ^ ((r >> 1) & 3))];
       };
-      if (!kNv && it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
+      if (!kNv && !(kFp4 && kWideK) && it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
         // TMEM accumulator -> packed 16-bit values in this warp's holding columns -> hand back
         const uint32_t hold = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + EPI_HOLD_COL0 + (ew >> 2) * 64;
 #pragma unroll 1
@@ -1787,10 +1835,10 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
               *reinterpret_cast<uint4*>(cbase + (8 * j + rsub) * ostride) = unstage4(j);
           __syncwarp();
         }
-      } else if (kNv && it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
-        // NVFP4 (its scale-factor ring leaves TMEM no holding columns): the warp's 32 x 128 block,
-        // times the global scales and packed to 16 bits, waits in registers (64 per thread) while
-        // the accumulator goes back to the MMA
+      } else if ((kNv || (kFp4 && kWideK)) && it.nsplit == 1 && p.out_bf16 && !p.accumulate) {
+        // NVFP4 and 512-token FP4 stages (their scale-factor rings leave TMEM no holding columns):
+        // the warp's 32 x 128 block, times the global scales (NVFP4; else 1) and packed to 16 bits,
+        // waits in registers (64 per thread) while the accumulator goes back to the MMA
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -2516,6 +2564,8 @@ cudaError_t launch_main_fp4(const MainParams& p, const CUtensorMap& tmA, const C
                             cudaStream_t s) {
   if (p.nvfp4 && p.tile_m == 2 * BM) return launch_main<true, true, true, true, false, true, true>(p, tmA, tmB, grid, s);
   if (p.nvfp4) return launch_main<true, false, true, true, false, true, true>(p, tmA, tmB, grid, s);
+  if (p.tile_m == 2 * BM && p.wide_k)
+    return launch_main<true, true, true, true, false, true, false, true>(p, tmA, tmB, grid, s);
   if (p.tile_m == 2 * BM) return launch_main<true, true, true, true, false, true>(p, tmA, tmB, grid, s);
   return launch_main<true, false, true, true, false, true>(p, tmA, tmB, grid, s);
 }
