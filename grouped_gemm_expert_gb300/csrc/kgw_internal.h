@@ -100,7 +100,7 @@ constexpr int STAGES_PAIR_FP4 = 5;
 // carrying four 128-token blocks ([A word 0..3][B word 0..3, each columns 0..127, 128..255], 6 KiB,
 // 48 TMEM columns); three stages of 70 KiB. The MMA thread and warp 10 pay their waits and commits
 // once per eight MMAs. Three such stages and the epilogue staging fill shared memory exactly: the
-// kernel relies on the dynamic shared memory starting 1024-byte aligned, and checks it.
+// kernel declares its dynamic shared memory 1024-byte aligned (no alignment slack), and checks it.
 constexpr int BK_FP4_PAIR = 512;
 constexpr int STAGES_PAIR_FP4_WIDE = 3;
 constexpr uint32_t SF_SMEM_PAD_PAIR_FP4_WIDE = 6144;

@@ -1224,7 +1224,7 @@ __global__ void __launch_bounds__(kFp8 ? NUM_THREADS_FP8 : NUM_THREADS, 1)
                     : 0u;
   constexpr int kHalves = kPair ? 2 : 1;
   constexpr int kEpiWarps = kFp8 ? NUM_EPI_WARPS_FP8 : NUM_EPI_WARPS;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];  // (the 512-token FP4 ring relies on it)
   const int bk = kFp4 ? (kWideK ? BK_FP4_PAIR : BK_FP4) : (kFp8 ? BK_FP8 : (kWideK ? BK_BF16_PAIR : BK_BF16));
   pdl_wait();  // the plan of this call (and any scale check before it) is complete and visible
   const PlanHeader* hdr = reinterpret_cast<const PlanHeader*>(p.ws);
